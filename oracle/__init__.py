@@ -1,0 +1,194 @@
+"""CPU oracle for GGUF Q4_K / Q6_K x Q8 integer matmul (ctypes over plain C).
+
+TEST INFRASTRUCTURE. Only ``tests/``, ``__graft_entry__.smoke()`` and the
+``cpu_baseline`` / reference leg of ``bench.py`` may import this package. The
+CUDA library and its Python binding never import it, and it imports nothing
+from them.
+
+The arithmetic lives in ``oracle.c`` (scalar loops, exact int64 sub-block
+sums, fp64 combine; the Q8 quantizer in fp32 exactly as written). This module
+only compiles that file with gcc and marshals numpy arrays.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB = os.path.join(_HERE, "_build", "liboracle.so")
+
+Q4K_BYTES = 144
+Q6K_BYTES = 210
+
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into a shared library (gcc, -O2, no FP contraction)."""
+    os.makedirs(os.path.dirname(_LIB), exist_ok=True)
+    deps = [_SRC, os.path.join(_HERE, "oracle.h")]
+    if (not force and os.path.exists(_LIB)
+            and os.path.getmtime(_LIB) >= max(os.path.getmtime(d) for d in deps)):
+        return _LIB
+    tmp = _LIB + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared",
+           "-std=c99", "-Wall", "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    if _lib is not None:
+        return _lib
+    lib = ctypes.CDLL(build())
+    P = ctypes.c_void_p
+    I = ctypes.c_int
+    lib.oracle_half_to_double.argtypes = [ctypes.c_uint16]
+    lib.oracle_half_to_double.restype = ctypes.c_double
+    lib.oracle_quantize_q8.argtypes = [P, I, I, P, P, P]
+    lib.oracle_q4k_fields.argtypes = [P, P, P, P, P, P]
+    lib.oracle_q4k_fields.restype = None
+    lib.oracle_q6k_fields.argtypes = [P, P, P, P]
+    lib.oracle_q6k_fields.restype = None
+    lib.oracle_dequant_q4k.argtypes = [P, I, I, P]
+    lib.oracle_dequant_q6k.argtypes = [P, I, I, P]
+    lib.oracle_dequant_q8.argtypes = [P, P, I, I, P]
+    lib.oracle_matmul_q4k_q8.argtypes = [P, P, P, I, I, I, P, P, P]
+    lib.oracle_matmul_q6k_q8.argtypes = [P, P, P, I, I, I, P, P, P]
+    lib.oracle_gemv_f64.argtypes = [P, P, I, I, I, P]
+    for name in ("oracle_quantize_q8", "oracle_dequant_q4k", "oracle_dequant_q6k",
+                 "oracle_dequant_q8", "oracle_matmul_q4k_q8", "oracle_matmul_q6k_q8",
+                 "oracle_gemv_f64"):
+        getattr(lib, name).restype = ctypes.c_int
+    _lib = lib
+    return lib
+
+
+def _p(a: np.ndarray):
+    assert a.flags["C_CONTIGUOUS"], "oracle arrays must be C-contiguous"
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _check(rc: int, what: str):
+    if rc != 0:
+        raise ValueError(f"oracle: bad shape for {what}")
+
+
+def half_to_double(h: int) -> float:
+    return _load().oracle_half_to_double(int(h) & 0xFFFF)
+
+
+def quantize_q8(x: np.ndarray):
+    """Q8 activation quantization of fp32 x [M][K] -> (qs int8, d8 f32, s8 f32)."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    M, K = x.shape
+    qs = np.zeros((M, K), np.int8)
+    d8 = np.zeros((M, K // 32), np.float32)
+    s8 = np.zeros((M, K // 32), np.float32)
+    _check(_load().oracle_quantize_q8(_p(x), M, K, _p(qs), _p(d8), _p(s8)), "quantize_q8")
+    return qs, d8, s8
+
+
+def q4k_fields(blk: np.ndarray):
+    """Decoded fields of one 144-byte Q4_K super-block: (d, dmin, sc[8], m[8], q[256])."""
+    blk = np.ascontiguousarray(blk, dtype=np.uint8)
+    assert blk.size == Q4K_BYTES
+    d = ctypes.c_double()
+    dmin = ctypes.c_double()
+    sc = np.zeros(8, np.int32)
+    mn = np.zeros(8, np.int32)
+    q = np.zeros(256, np.int32)
+    _load().oracle_q4k_fields(_p(blk), ctypes.byref(d), ctypes.byref(dmin), _p(sc), _p(mn), _p(q))
+    return d.value, dmin.value, sc, mn, q
+
+
+def q6k_fields(blk: np.ndarray):
+    """Decoded fields of one 210-byte Q6_K super-block: (d, s[16], q[256])."""
+    blk = np.ascontiguousarray(blk, dtype=np.uint8)
+    assert blk.size == Q6K_BYTES
+    d = ctypes.c_double()
+    s = np.zeros(16, np.int32)
+    q = np.zeros(256, np.int32)
+    _load().oracle_q6k_fields(_p(blk), ctypes.byref(d), _p(s), _p(q))
+    return d.value, s, q
+
+
+def _weight_shape(W: np.ndarray, K: int, nbytes: int):
+    W = np.ascontiguousarray(W, dtype=np.uint8)
+    nsb = K // 256
+    assert K % 256 == 0 and W.size % (nsb * nbytes) == 0
+    return W, W.size // (nsb * nbytes)
+
+
+def dequant_q4k(W: np.ndarray, K: int) -> np.ndarray:
+    W, N = _weight_shape(W, K, Q4K_BYTES)
+    w = np.zeros((N, K), np.float64)
+    _check(_load().oracle_dequant_q4k(_p(W), N, K, _p(w)), "dequant_q4k")
+    return w
+
+
+def dequant_q6k(W: np.ndarray, K: int) -> np.ndarray:
+    W, N = _weight_shape(W, K, Q6K_BYTES)
+    w = np.zeros((N, K), np.float64)
+    _check(_load().oracle_dequant_q6k(_p(W), N, K, _p(w)), "dequant_q6k")
+    return w
+
+
+def dequant_q8(qs: np.ndarray, d8: np.ndarray) -> np.ndarray:
+    qs = np.ascontiguousarray(qs, dtype=np.int8)
+    d8 = np.ascontiguousarray(d8, dtype=np.float32)
+    M, K = qs.shape
+    xhat = np.zeros((M, K), np.float64)
+    _check(_load().oracle_dequant_q8(_p(qs), _p(d8), M, K, _p(xhat)), "dequant_q8")
+    return xhat
+
+
+def _matmul(fn, W, qs, d8, K, nbytes, want_isum, isum_per_row):
+    W, N = _weight_shape(W, K, nbytes)
+    qs = np.ascontiguousarray(qs, dtype=np.int8)
+    d8 = np.ascontiguousarray(d8, dtype=np.float32)
+    M = qs.shape[0]
+    assert qs.shape == (M, K) and d8.shape == (M, K // 32)
+    y = np.zeros((M, N), np.float64)
+    ab = np.zeros((M, N), np.float64)
+    isum = np.zeros((M, N, isum_per_row), np.int32) if want_isum else None
+    rc = fn(_p(W), _p(qs), _p(d8), M, N, K, _p(y), _p(ab),
+            _p(isum) if want_isum else None)
+    _check(rc, "matmul")
+    return y, ab, isum
+
+
+def matmul_q4k_q8(W, qs, d8, K, want_isum=False):
+    """Integer route: y [M][N] (double), sum|terms| [M][N], isums [M][N][K/32] or None."""
+    return _matmul(_load().oracle_matmul_q4k_q8, W, qs, d8, K, Q4K_BYTES, want_isum, K // 32)
+
+
+def matmul_q6k_q8(W, qs, d8, K, want_isum=False):
+    """Integer route: y [M][N] (double), sum|terms| [M][N], isums [M][N][K/16] or None."""
+    return _matmul(_load().oracle_matmul_q6k_q8, W, qs, d8, K, Q6K_BYTES, want_isum, K // 16)
+
+
+def gemv_f64(w: np.ndarray, x: np.ndarray) -> np.ndarray:
+    """Plain definition y[m][n] = sum_k w[n][k] * x[m][k] in double."""
+    w = np.ascontiguousarray(w, dtype=np.float64)
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    N, K = w.shape
+    M = x.shape[0]
+    y = np.zeros((M, N), np.float64)
+    _check(_load().oracle_gemv_f64(_p(w), _p(x), M, N, K, _p(y)), "gemv_f64")
+    return y
+
+
+def matmul(qtype: int, W, qs, d8, K, want_isum=False):
+    """Dispatch on the GGUF type id (12 = Q4_K, 14 = Q6_K)."""
+    if qtype == 12:
+        return matmul_q4k_q8(W, qs, d8, K, want_isum)
+    if qtype == 14:
+        return matmul_q6k_q8(W, qs, d8, K, want_isum)
+    raise ValueError(f"unsupported type {qtype}")

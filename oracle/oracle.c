@@ -1,0 +1,326 @@
+/*
+ * CPU oracle for GGUF Q4_K / Q6_K x Q8 integer matmul.
+ *
+ * TEST INFRASTRUCTURE. Only the tests, the smoke check and the bench's CPU
+ * baseline leg may link, load or call this file. The CUDA library never does,
+ * and this file shares no code, header, table or helper with it.
+ *
+ * Plain, slow, obviously correct: scalar loops, integer sub-block sums in
+ * int64, every scale combine in double. Built with -O2 -ffp-contract=off so
+ * that the one fp32 routine (the Q8 quantizer) runs exactly the IEEE
+ * operations written here, one rounding each.
+ *
+ * What it computes (the sources):
+ *  - xLLM v0.7 long-context article (Tencent Cloud), section 一 "背景":
+ *    Q4_K / Q6_K weights are not dequantized to fp32; the kernel takes
+ *    integer dot products against Q8-quantized activations and emits fp32.
+ *  - same article, section B1.3: the Q8 activation quantization adds about
+ *    0.5% RMS noise against the unquantized product and keeps the arg-max.
+ *  - same article, section A2: a mixed model keeps attn_v and ffn_down in
+ *    Q6_K, the other projections in Q4_K.
+ *  - Agent Telemetry log, entry "批次化 MMVQ": the activation format is the
+ *    q8_1 kind (int8 per 32 with a scale and a sum).
+ *  - The pages name the Q4_K / Q6_K formats but never print their bit
+ *    layout; the layout below is the public GGUF k-quant block layout,
+ *    restated in words beside each decoder.
+ *
+ * Readings where the pages are silent (each applies in one place below):
+ *  - Q8: d8 = amax/127 (IEEE fp32 divide), id = 1/d8 (0 if d8 == 0),
+ *    q = clamp(roundf(x*id), -127, 127) with C roundf (ties away from zero),
+ *    s8 = d8 * (float)sum(q), one fp32 multiply. amax == 0 gives all zeros.
+ *  - Q6_K "sub-block" for integer sums is the 16-weight scale group.
+ *  - fp16 fields are IEEE binary16, little endian.
+ */
+#include "oracle.h"
+
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+/* IEEE 754 binary16 -> double, from the definition of the format:
+ * 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits; exponent 0 is
+ * subnormal (fraction * 2^-24), exponent 31 is inf/nan. */
+double oracle_half_to_double(uint16_t h)
+{
+    int sign = (h >> 15) & 1;
+    int expo = (h >> 10) & 31;
+    int frac = h & 1023;
+    double v;
+    if (expo == 0) {
+        v = ldexp((double)frac, -24);
+    } else if (expo == 31) {
+        v = frac ? NAN : INFINITY;
+    } else {
+        v = ldexp((double)(1024 + frac), expo - 25);
+    }
+    return sign ? -v : v;
+}
+
+static uint16_t read_u16le(const uint8_t *p)
+{
+    return (uint16_t)(p[0] | (p[1] << 8));
+}
+
+/* ---------------------------------------------------------------- Q8 */
+
+/* Q8 activation quantization, one 32-block at a time, fp32 throughout.
+ * x is [M][K] row-major; qs is [M][K]; d8 and s8 are [M][K/32]. */
+int oracle_quantize_q8(const float *x, int M, int K,
+                       int8_t *qs, float *d8, float *s8)
+{
+    if (M < 0 || K <= 0 || K % 32 != 0) return 1;
+    int nblk = K / 32;
+    for (int m = 0; m < M; m++) {
+        for (int b = 0; b < nblk; b++) {
+            const float *xb = x + (size_t)m * K + (size_t)b * 32;
+            int8_t *qb = qs + (size_t)m * K + (size_t)b * 32;
+            float amax = 0.0f;
+            for (int i = 0; i < 32; i++) {
+                float a = fabsf(xb[i]);
+                if (a > amax) amax = a;
+            }
+            float d = amax / 127.0f;
+            float id = (d != 0.0f) ? 1.0f / d : 0.0f;
+            int isum = 0;
+            for (int i = 0; i < 32; i++) {
+                float t = xb[i] * id;
+                float r = roundf(t);
+                int q = (int)r;
+                if (q > 127) q = 127;
+                if (q < -127) q = -127;
+                qb[i] = (int8_t)q;
+                isum += q;
+            }
+            d8[(size_t)m * nblk + b] = d;
+            s8[(size_t)m * nblk + b] = d * (float)isum;
+        }
+    }
+    return 0;
+}
+
+/* -------------------------------------------------------------- Q4_K */
+
+/* Decode one Q4_K super-block (144 bytes, 256 weights) into its fields.
+ * Layout (GGUF): d fp16 at byte 0, dmin fp16 at 2, 12 packed scale bytes at
+ * 4..15, 128 quant bytes at 16..143.
+ * The 12 scale bytes hold eight 6-bit scales sc[j] and eight 6-bit mins m[j]:
+ *   j < 4 : sc = s[j] & 63,                         m = s[j+4] & 63
+ *   j >= 4: sc = (s[j+4] & 15) | ((s[j-4] >> 6) << 4),
+ *           m  = (s[j+4] >> 4) | ((s[j]   >> 6) << 4)
+ * Quant byte 32*g + l (g = 0..3, l = 0..31) holds weight 64*g + l in its low
+ * nibble and weight 64*g + 32 + l in its high nibble, so sub-block 2g is the
+ * low nibbles of bytes 32g..32g+31 and sub-block 2g+1 their high nibbles. */
+void oracle_q4k_fields(const uint8_t *blk, double *d, double *dmin,
+                       int sc[8], int mn[8], int q[256])
+{
+    const uint8_t *s = blk + 4;
+    const uint8_t *qb = blk + 16;
+    *d = oracle_half_to_double(read_u16le(blk));
+    *dmin = oracle_half_to_double(read_u16le(blk + 2));
+    for (int j = 0; j < 8; j++) {
+        if (j < 4) {
+            sc[j] = s[j] & 63;
+            mn[j] = s[j + 4] & 63;
+        } else {
+            sc[j] = (s[j + 4] & 15) | ((s[j - 4] >> 6) << 4);
+            mn[j] = (s[j + 4] >> 4) | ((s[j] >> 6) << 4);
+        }
+    }
+    for (int g = 0; g < 4; g++) {
+        for (int l = 0; l < 32; l++) {
+            uint8_t byte = qb[32 * g + l];
+            q[64 * g + l] = byte & 15;
+            q[64 * g + 32 + l] = byte >> 4;
+        }
+    }
+}
+
+/* Dequantize Q4_K rows to double: w = d*sc[j]*q - dmin*m[j] for the weight's
+ * sub-block j. W is [N][K/256] super-blocks; w is [N][K]. */
+int oracle_dequant_q4k(const uint8_t *W, int N, int K, double *w)
+{
+    if (N < 0 || K <= 0 || K % 256 != 0) return 1;
+    int nsb = K / 256;
+    for (int n = 0; n < N; n++) {
+        for (int b = 0; b < nsb; b++) {
+            const uint8_t *blk = W + ((size_t)n * nsb + b) * ORACLE_Q4K_BYTES;
+            double d, dmin;
+            int sc[8], mn[8], q[256];
+            oracle_q4k_fields(blk, &d, &dmin, sc, mn, q);
+            for (int i = 0; i < 256; i++) {
+                int j = i / 32;
+                w[(size_t)n * K + (size_t)b * 256 + i] =
+                    d * sc[j] * q[i] - dmin * mn[j];
+            }
+        }
+    }
+    return 0;
+}
+
+/* -------------------------------------------------------------- Q6_K */
+
+/* Decode one Q6_K super-block (210 bytes, 256 weights) into its fields.
+ * Layout (GGUF): ql[128] at byte 0, qh[64] at 128, scales int8[16] at 192,
+ * d fp16 at 208. For half h in {0,1} and l in 0..31, with L = ql + 64h and
+ * H = qh + 32h, the 6-bit quants are
+ *   weight 128h +      l = (L[l]    & 15) | (((H[l] >> 0) & 3) << 4)
+ *   weight 128h + 32 + l = (L[l+32] & 15) | (((H[l] >> 2) & 3) << 4)
+ *   weight 128h + 64 + l = (L[l]    >> 4) | (((H[l] >> 4) & 3) << 4)
+ *   weight 128h + 96 + l = (L[l+32] >> 4) | (((H[l] >> 6) & 3) << 4)
+ * Scale s[g] covers the 16 contiguous weights 16g..16g+15. */
+void oracle_q6k_fields(const uint8_t *blk, double *d, int s[16], int q[256])
+{
+    const uint8_t *ql = blk;
+    const uint8_t *qh = blk + 128;
+    const int8_t *sc = (const int8_t *)(blk + 192);
+    *d = oracle_half_to_double(read_u16le(blk + 208));
+    for (int g = 0; g < 16; g++) s[g] = sc[g];
+    for (int h = 0; h < 2; h++) {
+        const uint8_t *L = ql + 64 * h;
+        const uint8_t *H = qh + 32 * h;
+        for (int l = 0; l < 32; l++) {
+            q[128 * h + l]      = (L[l] & 15)      | (((H[l] >> 0) & 3) << 4);
+            q[128 * h + 32 + l] = (L[l + 32] & 15) | (((H[l] >> 2) & 3) << 4);
+            q[128 * h + 64 + l] = (L[l] >> 4)      | (((H[l] >> 4) & 3) << 4);
+            q[128 * h + 96 + l] = (L[l + 32] >> 4) | (((H[l] >> 6) & 3) << 4);
+        }
+    }
+}
+
+/* Dequantize Q6_K rows to double: w = d*s[g]*(q - 32). */
+int oracle_dequant_q6k(const uint8_t *W, int N, int K, double *w)
+{
+    if (N < 0 || K <= 0 || K % 256 != 0) return 1;
+    int nsb = K / 256;
+    for (int n = 0; n < N; n++) {
+        for (int b = 0; b < nsb; b++) {
+            const uint8_t *blk = W + ((size_t)n * nsb + b) * ORACLE_Q6K_BYTES;
+            double d;
+            int s[16], q[256];
+            oracle_q6k_fields(blk, &d, s, q);
+            for (int i = 0; i < 256; i++) {
+                w[(size_t)n * K + (size_t)b * 256 + i] = d * s[i / 16] * (q[i] - 32);
+            }
+        }
+    }
+    return 0;
+}
+
+/* ----------------------------------------------------- integer route */
+
+/* Q4_K x Q8 by integer sub-block sums (the route the kernels take).
+ * For row n, token m, super-block b and sub-block j (32 weights):
+ *   isum  = sum_i q[32j+i] * q8[m][256b+32j+i]            (exact, int64)
+ *   isum8 = sum_i q8[m][256b+32j+i]                        (exact, int64)
+ *   y[m][n] += d*sc_j*d8[m][8b+j]*isum - dmin*m_j*d8[m][8b+j]*isum8
+ * All in double. isum_out (optional, [M][N][K/32]) receives isum.
+ * absterm_out (optional, [M][N]) receives the sum of the absolute values of
+ * every scaled term above, both the d-term and the dmin-term. */
+int oracle_matmul_q4k_q8(const uint8_t *W, const int8_t *qs, const float *d8,
+                         int M, int N, int K,
+                         double *y, double *absterm_out, int32_t *isum_out)
+{
+    if (M < 0 || N < 0 || K <= 0 || K % 256 != 0) return 1;
+    int nsb = K / 256;
+    int nsub = K / 32;
+    double d, dmin;
+    int sc[8], mn[8], q[256];
+    for (int m = 0; m < M; m++)
+        for (int n = 0; n < N; n++) {
+            y[(size_t)m * N + n] = 0.0;
+            if (absterm_out) absterm_out[(size_t)m * N + n] = 0.0;
+        }
+    for (int n = 0; n < N; n++) {
+        for (int b = 0; b < nsb; b++) {
+            oracle_q4k_fields(W + ((size_t)n * nsb + b) * ORACLE_Q4K_BYTES,
+                              &d, &dmin, sc, mn, q);
+            for (int m = 0; m < M; m++) {
+                const int8_t *a = qs + (size_t)m * K + (size_t)b * 256;
+                for (int j = 0; j < 8; j++) {
+                    int64_t isum = 0, isum8 = 0;
+                    for (int i = 0; i < 32; i++) {
+                        isum += (int64_t)q[32 * j + i] * a[32 * j + i];
+                        isum8 += a[32 * j + i];
+                    }
+                    double da = (double)d8[(size_t)m * nsub + 8 * b + j];
+                    double t1 = d * sc[j] * da * (double)isum;
+                    double t2 = dmin * mn[j] * da * (double)isum8;
+                    y[(size_t)m * N + n] += t1 - t2;
+                    if (absterm_out) absterm_out[(size_t)m * N + n] += fabs(t1) + fabs(t2);
+                    if (isum_out)
+                        isum_out[((size_t)m * N + n) * nsub + 8 * b + j] = (int32_t)isum;
+                }
+            }
+        }
+    }
+    return 0;
+}
+
+/* Q6_K x Q8 by integer sums over each 16-weight scale group g:
+ *   isum_g = sum_i (q[16g+i] - 32) * q8[m][256b+16g+i]     (exact, int64)
+ *   y[m][n] += d * s_g * d8[m][(256b+16g)/32] * isum_g     (double)
+ * isum_out (optional) is [M][N][K/16]; absterm_out as for Q4_K. */
+int oracle_matmul_q6k_q8(const uint8_t *W, const int8_t *qs, const float *d8,
+                         int M, int N, int K,
+                         double *y, double *absterm_out, int32_t *isum_out)
+{
+    if (M < 0 || N < 0 || K <= 0 || K % 256 != 0) return 1;
+    int nsb = K / 256;
+    int nsub = K / 32;
+    int ngrp = K / 16;
+    double d;
+    int s[16], q[256];
+    for (int m = 0; m < M; m++)
+        for (int n = 0; n < N; n++) {
+            y[(size_t)m * N + n] = 0.0;
+            if (absterm_out) absterm_out[(size_t)m * N + n] = 0.0;
+        }
+    for (int n = 0; n < N; n++) {
+        for (int b = 0; b < nsb; b++) {
+            oracle_q6k_fields(W + ((size_t)n * nsb + b) * ORACLE_Q6K_BYTES, &d, s, q);
+            for (int m = 0; m < M; m++) {
+                const int8_t *a = qs + (size_t)m * K + (size_t)b * 256;
+                for (int g = 0; g < 16; g++) {
+                    int64_t isum = 0;
+                    for (int i = 0; i < 16; i++)
+                        isum += (int64_t)(q[16 * g + i] - 32) * a[16 * g + i];
+                    double da = (double)d8[(size_t)m * nsub + 8 * b + g / 2];
+                    double t = d * s[g] * da * (double)isum;
+                    y[(size_t)m * N + n] += t;
+                    if (absterm_out) absterm_out[(size_t)m * N + n] += fabs(t);
+                    if (isum_out)
+                        isum_out[((size_t)m * N + n) * ngrp + 16 * b + g] = (int32_t)isum;
+                }
+            }
+        }
+    }
+    return 0;
+}
+
+/* ----------------------------------------------- straight dot products */
+
+/* The plain definition: y[m][n] = sum_k w[n][k] * x[m][k], all double.
+ * Used with x = d8*q8 (the dequantize-then-GEMV route the integer path
+ * rearranges) and with x = the unquantized fp32 activation. */
+int oracle_gemv_f64(const double *w, const double *x, int M, int N, int K, double *y)
+{
+    if (M < 0 || N < 0 || K < 0) return 1;
+    for (int m = 0; m < M; m++) {
+        for (int n = 0; n < N; n++) {
+            double acc = 0.0;
+            for (int k = 0; k < K; k++) acc += w[(size_t)n * K + k] * x[(size_t)m * K + k];
+            y[(size_t)m * N + n] = acc;
+        }
+    }
+    return 0;
+}
+
+/* Dequantized Q8 activation: xhat[m][k] = d8[m][k/32] * q8[m][k] (double). */
+int oracle_dequant_q8(const int8_t *qs, const float *d8, int M, int K, double *xhat)
+{
+    if (M < 0 || K <= 0 || K % 32 != 0) return 1;
+    for (int m = 0; m < M; m++)
+        for (int k = 0; k < K; k++)
+            xhat[(size_t)m * K + k] = (double)d8[(size_t)m * (K / 32) + k / 32] * qs[(size_t)m * K + k];
+    return 0;
+}

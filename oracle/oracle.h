@@ -1,0 +1,54 @@
+/*
+ * CPU oracle for GGUF Q4_K / Q6_K x Q8 integer matmul.
+ *
+ * TEST INFRASTRUCTURE. Only the tests, the smoke check and the bench's CPU
+ * baseline leg may use it. It shares nothing with the CUDA library.
+ *
+ * Layouts (all row-major, host memory, caller-owned):
+ *   x   fp32 [M][K]            unquantized activations
+ *   qs  int8 [M][K]            Q8 quants
+ *   d8  fp32 [M][K/32]         Q8 block scales
+ *   s8  fp32 [M][K/32]         Q8 block scale * block sum of quants
+ *   W   bytes [N][K/256][144]  Q4_K super-blocks, or [N][K/256][210] Q6_K
+ *   y   double [M][N]
+ * Every function returns 0 on success, 1 on a bad shape.
+ */
+#ifndef XQ_ORACLE_H
+#define XQ_ORACLE_H
+
+#include <stdint.h>
+
+#define ORACLE_Q4K_BYTES 144
+#define ORACLE_Q6K_BYTES 210
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+double oracle_half_to_double(uint16_t h);
+
+int oracle_quantize_q8(const float *x, int M, int K,
+                       int8_t *qs, float *d8, float *s8);
+
+void oracle_q4k_fields(const uint8_t *blk, double *d, double *dmin,
+                       int sc[8], int mn[8], int q[256]);
+void oracle_q6k_fields(const uint8_t *blk, double *d, int s[16], int q[256]);
+
+int oracle_dequant_q4k(const uint8_t *W, int N, int K, double *w);
+int oracle_dequant_q6k(const uint8_t *W, int N, int K, double *w);
+int oracle_dequant_q8(const int8_t *qs, const float *d8, int M, int K, double *xhat);
+
+int oracle_matmul_q4k_q8(const uint8_t *W, const int8_t *qs, const float *d8,
+                         int M, int N, int K,
+                         double *y, double *absterm_out, int32_t *isum_out);
+int oracle_matmul_q6k_q8(const uint8_t *W, const int8_t *qs, const float *d8,
+                         int M, int N, int K,
+                         double *y, double *absterm_out, int32_t *isum_out);
+
+int oracle_gemv_f64(const double *w, const double *x, int M, int N, int K, double *y);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif
