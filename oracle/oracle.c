@@ -27,7 +27,9 @@
  * Readings where the pages are silent (each applies in one place below):
  *  - Q8: d8 = amax/127 (IEEE fp32 divide), id = 1/d8 (0 if d8 == 0),
  *    q = clamp(roundf(x*id), -127, 127) with C roundf (ties away from zero),
- *    s8 = d8 * (float)sum(q), one fp32 multiply. amax == 0 gives all zeros.
+ *    the clamp done in float (NaN -> 0, +-inf -> +-127) before the int
+ *    conversion, s8 = d8 * (float)sum(q), one fp32 multiply. amax == 0 gives
+ *    all zeros.
  *  - Q6_K "sub-block" for integer sums is the 16-weight scale group.
  *  - fp16 fields are IEEE binary16, little endian.
  */
@@ -85,9 +87,13 @@ int oracle_quantize_q8(const float *x, int M, int K,
             for (int i = 0; i < 32; i++) {
                 float t = xb[i] * id;
                 float r = roundf(t);
+                /* Saturate in float before converting: when amax is so small
+                 * that 1/d8 overflows, x*id is +-inf (-> +-127) or 0*inf = NaN
+                 * (-> 0); converting those to int directly is undefined. */
+                if (r != r) r = 0.0f;
+                if (r > 127.0f) r = 127.0f;
+                if (r < -127.0f) r = -127.0f;
                 int q = (int)r;
-                if (q > 127) q = 127;
-                if (q < -127) q = -127;
                 qb[i] = (int8_t)q;
                 isum += q;
             }

@@ -381,3 +381,16 @@ def test_q8_output_noise_and_argmax():
             assert np.argmax(y[m]) == np.argmax(yf[m])
             checked += 1
     assert checked >= 1
+
+
+def test_q8_overflowing_reciprocal_saturates():
+    # amax so small that 1/d8 overflows to inf: x*id is +-inf for x != 0
+    # (saturates to +-127) and NaN for x == 0 (maps to 0).
+    x = np.zeros((1, 32), np.float32)
+    x[0, 0] = np.float32(3e-41)
+    x[0, 1] = np.float32(-1e-41)
+    qs, d8, s8 = oracle.quantize_q8(x)
+    assert np.isinf(np.float32(1.0) / d8[0, 0])
+    expect = np.zeros(32, np.int8)
+    expect[0], expect[1] = 127, -127
+    assert np.array_equal(qs[0], expect) and s8[0, 0] == 0.0
