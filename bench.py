@@ -1,0 +1,527 @@
+#!/usr/bin/env python
+"""Benchmark of the GGUF Q4_K/Q6_K x Q8 integer matmul path on GB300.
+
+One step = one decode pass of the Llama-3-8B-shaped 32-layer sweep at M=8:
+per layer, xq_layer_mixed quantizes the layer's four fp32 inputs to Q8 and
+runs the seven Q4_K projections (Q, K, V, O, gate, up, down). All 3.93 GB of
+weights stay resident in HBM (far larger than the 129 MB L2, so every step
+streams them from HBM; no flush needed). The metric is weight GB/s: the
+algorithmic weight bytes (144/256 B per Q4_K weight, 210/256 B per Q6_K
+weight) per step over the step time.
+
+Prints ONE JSON line (rank 0). Extra objects on it:
+  by_m        the same sweep at M = 1, 2, 4, 8;
+  roofline    the dominant kernel (the Q4_K matmul), bytes per launch over
+              its CUDA-event launch time, against the measured HBM peak;
+  secondary   the other workloads: Qwen2.5-1.5B and Qwen3-8B mixed layers
+              (weights rotated over >= 3x L2 of copies) and the M=512
+              Qwen3-8B FFN prefill tile;
+  cpu_baseline the CPU oracle on a bounded sample of the same sweep;
+  e2e         the same metric through the public API with pinned host
+              inputs/outputs copied inside the timed region.
+
+`--impl reference` times the CPU oracle instead (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from gguf_quant_integer_gb300 import synth  # noqa: E402
+
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_HBM_GBS = 6800.0
+HEADLINE = "llama3-8b-32layer"
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=10)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["xq", "reference"], default="xq")
+    p.add_argument("--m", type=int, default=8, help="tokens per step (headline sweep)")
+    p.add_argument("--no-secondary", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--cpu-sample-layers", type=int, default=8)
+    return p.parse_args(argv)
+
+
+# ------------------------------------------------------------ multi-rank
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def dist_init(backend: str):
+    rank, world, _ = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        if not dist.is_initialized():
+            os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+            os.environ.setdefault("MASTER_PORT", "29511")
+            dist.init_process_group(backend, rank=rank, world_size=world)
+    return rank, world
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v: float, world: int, device=None) -> float:
+    """The slowest rank's value (timing is taken as the max over ranks)."""
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_value(bytes_per_step_per_rank: float, world: int, max_seconds: float) -> float:
+    """Whole-job weight GB/s: every rank streams its own replica each step."""
+    return bytes_per_step_per_rank * world / max_seconds / 1e9
+
+
+# ------------------------------------------------------------ peaks, clocks
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            with open(path) as f:
+                d = json.load(f)
+            v = d.get("hbm_gbs") or d.get("hbm_GBps") or d.get("hbm")
+            if isinstance(v, dict):
+                v = v.get("value")
+            if v:
+                return float(v), "measured"
+        except Exception:
+            pass
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during a region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"xq_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        try:
+            os.remove(self.path)
+        except OSError:
+            pass
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------ CPU oracle
+
+def oracle_sweep_seconds(wl, M, layers, host_weights, host_inputs):
+    """Time the CPU oracle over `layers` layers of the sweep (quantize the
+    layer inputs, then every projection). Returns (seconds, weight bytes)."""
+    import oracle
+    oracle.build()
+    nbytes = 0
+    t0 = time.perf_counter()
+    for l in layers:
+        q8 = [oracle.quantize_q8(x) for x in host_inputs[l]]
+        for t, p in enumerate(wl.projs):
+            qs, d8, _ = q8[p.input]
+            oracle.matmul(p.qtype, host_weights[l][t], qs, d8, p.K)
+            nbytes += synth.weight_bytes(p.qtype, p.N, p.K)
+    return time.perf_counter() - t0, nbytes
+
+
+def reference_arm(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    wl = synth.WORKLOADS[HEADLINE]
+    M = args.m
+    layers_per_step = 1
+    sample = list(range(layers_per_step))
+    host_w = {l: synth.gen_layer_weights(wl, l) for l in sample}
+    host_x = {l: synth.gen_layer_inputs(wl, M, l) for l in sample}
+    for _ in range(args.warmup):
+        oracle_sweep_seconds(wl, M, sample, host_w, host_x)
+    secs, nbytes = [], 0
+    for _ in range(args.steps):
+        s, nbytes = oracle_sweep_seconds(wl, M, sample, host_w, host_x)
+        secs.append(s)
+    tot = sum(secs)
+    value = nbytes * args.steps / tot / 1e9
+    sample_desc = (f"layer 0 of the 32-layer sweep per step (Q8 quantize of its 4 inputs + 7 Q4_K "
+                   f"projections, {nbytes / 1e6:.1f} MB of weights) at M={M}")
+    line = {
+        "impl": "reference", "metric": "Q4_K/Q6_K x Q8 matmul weight GB/s (M=%d)" % M,
+        "value": round(value, 6), "unit": "GB/s", "n_gpus": args.gpus, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(1e3 * tot / args.steps, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded GGUF Q4_K blocks, fp32 N(0,1) activations)",
+        "config": {"workload": HEADLINE, "M": M, "layers": wl.layers, "sample": sample_desc},
+        "cpu_baseline": {"value": round(value, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": sample_desc},
+        "e2e": {"value": round(value, 6), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------ GPU arm
+
+class Sweep:
+    """All layers of a workload resident on the device, with per-M outputs."""
+
+    def __init__(self, wl, layers_weights, device):
+        import torch
+        self.wl = wl
+        self.device = device
+        self.W = [[torch.from_numpy(w.reshape(-1)).to(device) for w in lw] for lw in layers_weights]
+        self.n_inputs = 1 + max(p.input for p in wl.projs)
+        self.state = {}
+
+    def prepare(self, M, inputs_host):
+        """Device inputs, outputs and workspace for batch M."""
+        import torch
+        from gguf_quant_integer_gb300 import xq
+        ins = [[torch.from_numpy(x).to(self.device) for x in li] for li in inputs_host]
+        ys = [[torch.empty((M, p.N), dtype=torch.float32, device=self.device) for p in self.wl.projs]
+              for _ in self.W]
+        descs = [[(p.qtype, p.N, p.K, self.W[l][t], ys[l][t], p.input) for t, p in enumerate(self.wl.projs)]
+                 for l in range(len(self.W))]
+        wsb = xq.layer_workspace_bytes(descs[0], self.n_inputs, M)
+        ws = torch.empty(max(wsb, 256), dtype=torch.uint8, device=self.device)
+        self.state[M] = (ins, ys, descs, ws)
+
+    def step(self, M):
+        from gguf_quant_integer_gb300 import xq
+        ins, ys, descs, ws = self.state[M]
+        for l in range(len(self.W)):
+            xq.layer_mixed(descs[l], ins[l], M, ws)
+
+    def launches_per_step(self, M):
+        chunks = (M + 7) // 8
+        used = len({p.input for p in self.wl.projs})
+        return len(self.W) * (used + chunks * len(self.wl.projs))
+
+    def bytes_per_step(self):
+        return len(self.W) * self.wl.layer_weight_bytes()
+
+
+def time_region(fn, steps, warmup, world, device):
+    import torch
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    s = torch.cuda.current_stream()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(s)
+    for _ in range(steps):
+        fn()
+    e1.record(s)
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / 1e3
+
+
+def per_launch_matmul_times(sweep, M, reps=3):
+    """CUDA-event duration of every projection launch of one sweep (the
+    dominant kernel), on the stream the kernels run on. Returns a list of
+    (qtype, bytes, seconds) per launch (average over reps sweeps)."""
+    import torch
+    from gguf_quant_integer_gb300 import xq
+    ins, ys, descs, ws = sweep.state[M]
+    s = torch.cuda.current_stream()
+    wl = sweep.wl
+    recs = []
+    for _ in range(reps):
+        evs = []
+        for l in range(len(sweep.W)):
+            bufs = {}
+            for i in sorted({p.input for p in wl.projs}):
+                bufs[i] = xq.quantize_q8(ins[l][i])
+            for t, p in enumerate(wl.projs):
+                a = torch.cuda.Event(enable_timing=True)
+                b = torch.cuda.Event(enable_timing=True)
+                a.record(s)
+                xq.matmul(p.qtype, sweep.W[l][t], bufs[p.input], M, p.N, p.K, y=ys[l][t])
+                b.record(s)
+                evs.append((p, a, b))
+        torch.cuda.synchronize()
+        recs.append([(p.qtype, synth.weight_bytes(p.qtype, p.N, p.K), a.elapsed_time(b) / 1e3)
+                     for p, a, b in evs])
+    out = []
+    for i in range(len(recs[0])):
+        out.append((recs[0][i][0], recs[0][i][1], sum(r[i][2] for r in recs) / reps))
+    return out
+
+
+def read_ncu_traffic(kernel_key: str):
+    """Per-launch DRAM bytes of `kernel_key` from the committed ncu summary,
+    valid only if the kernel source hash recorded there matches the current one."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "traffic.md")
+    if not os.path.exists(path):
+        return None
+    src = os.path.join(ROOT, "gguf_quant_integer_gb300", "csrc")
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(src)):
+        if name.endswith((".cu", ".cuh")):
+            with open(os.path.join(src, name), "rb") as f:
+                h.update(f.read())
+    digest = h.hexdigest()[:16]
+    with open(path) as f:
+        for line in f:
+            parts = line.strip().strip("|").split("|")
+            parts = [p.strip() for p in parts]
+            if len(parts) >= 4 and parts[0] == kernel_key and parts[3] == digest:
+                try:
+                    return float(parts[1]), parts[2]
+                except ValueError:
+                    return None
+    return None
+
+
+def gpu_arm(args):
+    import torch
+    rank, world = dist_init("nccl" if torch.cuda.is_available() else "gloo")
+    _, _, local = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py: no CUDA device (the xq path has no CPU fallback)")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    from gguf_quant_integer_gb300 import build, xq
+    if rank == 0 or not os.path.exists(xq.LIB_PATH):
+        build.build()
+    barrier(world)
+    xq.lib()
+
+    wl = synth.WORKLOADS[HEADLINE]
+    M = args.m
+    host_w = [synth.gen_layer_weights(wl, l) for l in range(wl.layers)]
+    sweep = Sweep(wl, host_w, device)
+    ms_list = sorted({1, 2, 4, 8, M})
+    host_inputs = {m: [synth.gen_layer_inputs(wl, m, l) for l in range(wl.layers)] for m in ms_list}
+    for m in ms_list:
+        sweep.prepare(m, host_inputs[m])
+    nbytes = sweep.bytes_per_step()
+
+    # ---- headline: timed region with clocks sampled during it
+    clk = ClockSampler(local)
+    clk.start()
+    secs = time_region(lambda: sweep.step(M), args.steps, args.warmup, world, device)
+    clocks = clk.stop()
+    secs = max_over_ranks(secs, world, device)
+    ms_per_step = 1e3 * secs / args.steps
+    value = aggregate_value(nbytes, world, secs / args.steps)
+
+    # ---- the same sweep at other M
+    by_m = {}
+    for m in ms_list:
+        s = time_region(lambda: sweep.step(m), max(3, args.steps // 2), 3, world, device)
+        s = max_over_ranks(s, world, device) / max(3, args.steps // 2)
+        by_m[str(m)] = {"GBps": round(nbytes / s / 1e9, 1), "ms_per_step": round(1e3 * s, 4),
+                        "tokens_per_s": round(m / s, 1)}
+
+    # ---- dominant kernel: per-launch CUDA events around every matmul launch
+    peak, peak_kind = measured_peaks()
+    lt = per_launch_matmul_times(sweep, M)
+    kb = sum(b for _, b, _ in lt)
+    kt = sum(t for _, _, t in lt)
+    achieved = kb / kt / 1e9
+    n_launch = len(lt)
+    tr = read_ncu_traffic(f"gemv_q4k_M{M}")
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "peak_source": peak_kind,
+                "kernel": "Q4_K x Q8 matmul (all %d projection launches of one sweep)" % n_launch,
+                "bytes_per_launch": round(kb / n_launch), "avg_launch_us": round(1e6 * kt / n_launch, 3),
+                "traffic": (round(tr[0]) if tr else None),
+                "traffic_note": (tr[1] if tr else "no ncu capture of the current kernel source")}
+    per_proj = {}
+    for t, p in enumerate(wl.projs):
+        xs = lt[t::len(wl.projs)]
+        bb = sum(b for _, b, _ in xs)
+        tt = sum(s for _, _, s in xs)
+        per_proj[p.name] = {"GBps": round(bb / tt / 1e9, 1), "us": round(1e6 * tt / len(xs), 2)}
+    roofline["per_projection"] = per_proj
+
+    # ---- e2e through the public API: pinned host in/out copied in the timed region
+    e2e = None
+    if not args.no_e2e:
+        ins, ys, descs, ws = sweep.state[M]
+        h_in = [[x.cpu().pin_memory() for x in li] for li in ins]
+        h_out = [[torch.empty(y.shape, dtype=y.dtype).pin_memory() for y in ly] for ly in ys]
+        h2d = sum(x.numel() * 4 for li in h_in for x in li)
+        d2h = sum(y.numel() * 4 for ly in h_out for y in ly)
+
+        def e2e_step():
+            for l in range(len(sweep.W)):
+                for d, h in zip(ins[l], h_in[l]):
+                    d.copy_(h, non_blocking=True)
+                xq.layer_mixed(descs[l], ins[l], M, ws)
+                for h, d in zip(h_out[l], ys[l]):
+                    h.copy_(d, non_blocking=True)
+
+        s = time_region(e2e_step, args.steps, max(3, args.warmup), world, device)
+        s = max_over_ranks(s, world, device) / args.steps
+        e2e = {"value": round(aggregate_value(nbytes, world, s), 1), "unit": "GB/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(1e3 * s, 4)}
+
+    # ---- secondary workloads
+    secondary = None
+    if not args.no_secondary:
+        secondary = secondary_workloads(device, world)
+
+    # ---- CPU oracle on a bounded sample (rank 0, N=1 only)
+    cpu = None
+    if not args.no_cpu_baseline and rank == 0 and world == 1:
+        S = max(1, min(args.cpu_sample_layers, wl.layers))
+        cs, cb = oracle_sweep_seconds(wl, M, list(range(S)), host_w, host_inputs[M])
+        cpu = {"value": round(cb / cs / 1e9, 5), "unit": "GB/s", "cores": 1, "kind": "oracle",
+               "seconds": round(cs, 2),
+               "sample": f"layers 0..{S - 1} of the 32-layer sweep at M={M} "
+                         f"({cb / 1e9:.3f} GB of weights), single-threaded C oracle"}
+
+    if rank == 0:
+        line = {
+            "metric": "Q4_K/Q6_K x Q8 matmul weight GB/s (M=%d) and %% of GB300 HBM roofline" % M,
+            "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "int8",
+            "data": "synthetic (seeded GGUF Q4_K blocks, fp32 N(0,1) activations)",
+            "config": {"workload": HEADLINE, "M": M, "layers": wl.layers,
+                       "weight_bytes_per_step": nbytes, "hidden": 4096, "ffn": 14336,
+                       "l2": "weights 3.93 GB >> 129 MB L2, streamed from HBM every step; no flush",
+                       "parallelism": f"replicas x{world}"},
+            "hbm_frac": round(value / world / peak, 4),
+            "tokens_per_s": round(M * world / (secs / args.steps), 1),
+            "gpu_launches": sweep.launches_per_step(M) * args.steps,
+            "clocks": clocks, "roofline": roofline, "by_m": by_m,
+            "e2e": e2e, "secondary": secondary, "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def secondary_workloads(device, world):
+    """Single-layer workloads that fit in L2: weights rotated over enough
+    device copies (>= 3x L2) that every launch reads from HBM."""
+    import torch
+    from gguf_quant_integer_gb300 import xq
+    out = {}
+    for name in ("qwen2.5-1.5b-layer", "qwen3-8b-mixed-layer"):
+        wl = synth.WORKLOADS[name]
+        lw = synth.gen_layer_weights(wl, 0)
+        copies = max(3, -(-3 * L2_BYTES // wl.layer_weight_bytes()))
+        base = [torch.from_numpy(w.reshape(-1)).to(device) for w in lw]
+        reps = [base] + [[w.clone() for w in base] for _ in range(copies - 1)]
+        res = {}
+        for M in wl.ms:
+            ins = [torch.from_numpy(x).to(device) for x in synth.gen_layer_inputs(wl, M, 0)]
+            ys = [torch.empty((M, p.N), dtype=torch.float32, device=device) for p in wl.projs]
+            descs = [[(p.qtype, p.N, p.K, reps[c][t], ys[t], p.input) for t, p in enumerate(wl.projs)]
+                     for c in range(copies)]
+            ws = torch.empty(max(256, xq.layer_workspace_bytes(descs[0], 4, M)), dtype=torch.uint8, device=device)
+
+            def step():
+                for c in range(copies):
+                    xq.layer_mixed(descs[c], ins, M, ws)
+
+            s = time_region(step, 5, 3, world, device)
+            s = max_over_ranks(s, world, device) / (5 * copies)
+            res[str(M)] = {"GBps": round(wl.layer_weight_bytes() / s / 1e9, 1), "us_per_layer": round(1e6 * s, 2),
+                           "tokens_per_s": round(M / s, 1)}
+        out[name] = {"rotated_copies": copies, "layer_bytes": wl.layer_weight_bytes(), "by_m": res}
+    # prefill tile M=512: up (Q4_K) then down (Q6_K)
+    wl = synth.WORKLOADS["qwen3-8b-ffn-prefill512"]
+    M = 512
+    lw = synth.gen_layer_weights(wl, 0)
+    Wd = [torch.from_numpy(w.reshape(-1)).to(device) for w in lw]
+    xs = [torch.from_numpy(x).to(device) for x in synth.gen_layer_inputs(wl, M, 0)]
+    ys = [torch.empty((M, p.N), dtype=torch.float32, device=device) for p in wl.projs]
+    bufs = [xq.quantize_q8(x) for x in xs]
+
+    def pstep():
+        for t, p in enumerate(wl.projs):
+            xq.quantize_q8(xs[p.input], out=bufs[p.input])
+            xq.matmul(p.qtype, Wd[t], bufs[p.input], M, p.N, p.K, y=ys[t])
+
+    s = time_region(pstep, 5, 3, world, device) / 5
+    s = max_over_ranks(s, world, device)
+    flops = sum(2.0 * M * p.N * p.K for p in wl.projs)
+    out[wl.key] = {"M": M, "ms": round(1e3 * s, 3), "TOPS_int": round(flops / s / 1e12, 2),
+                   "GBps_weights": round(wl.layer_weight_bytes() / s / 1e9, 1),
+                   "path": "8-token GEMV launches (no tensor-core tile yet)"}
+    return out
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        return reference_arm(args)
+    return gpu_arm(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,211 @@
+// The C ABI of include/xq.h: argument checks, buffer layout and dispatch.
+// Every check runs before anything is enqueued; nothing here allocates.
+#include <cstdint>
+
+#include "xq.h"
+#include "xq_common.cuh"
+
+namespace {
+
+using xq::GemvArgs;
+
+constexpr int kMaxGemvM = 8;  // tokens per GEMV launch (the kernels' M template)
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int block_bytes(int type) {
+  return type == XQ_TYPE_Q4_K ? xq::kQ4kBytes : (type == XQ_TYPE_Q6_K ? xq::kQ6kBytes : 0);
+}
+
+xq_status check_shape(int M, int N, int K) {
+  if (M < 0 || N < 0 || K <= 0 || (K % 256) != 0) return XQ_ERR_SHAPE;
+  return XQ_OK;
+}
+
+struct Q8View {
+  const int8_t* qs;
+  const float* d8;
+  const float* s8;
+};
+
+Q8View q8_view(const void* xq, int M, int K) {
+  const uint8_t* base = static_cast<const uint8_t*>(xq);
+  const size_t mk = static_cast<size_t>(M) * K;
+  Q8View v;
+  v.qs = reinterpret_cast<const int8_t*>(base);
+  v.d8 = reinterpret_cast<const float*>(base + mk);
+  v.s8 = reinterpret_cast<const float*>(base + mk + 4 * (mk / 32));
+  return v;
+}
+
+// Enqueue y = x W^T for any M, in launches of at most 8 tokens.
+xq_status run_matmul(int type, const void* W, const void* xq, int M, int N, int K, float* y,
+                     int32_t* isum, cudaStream_t s) {
+  const Q8View v = q8_view(xq, M, K);
+  for (int m0 = 0; m0 < M; m0 += kMaxGemvM) {
+    const int mc = (M - m0) < kMaxGemvM ? (M - m0) : kMaxGemvM;
+    GemvArgs a;
+    a.W = static_cast<const uint8_t*>(W);
+    a.qs = v.qs + static_cast<size_t>(m0) * K;
+    a.d8 = v.d8 + static_cast<size_t>(m0) * (K / 32);
+    a.s8 = v.s8 + static_cast<size_t>(m0) * (K / 32);
+    a.M = mc;
+    a.N = N;
+    a.K = K;
+    a.y = y + static_cast<size_t>(m0) * N;
+    a.ldy = N;
+    a.isum = isum;
+    const cudaError_t e = (type == XQ_TYPE_Q4_K) ? xq::launch_gemv_q4k(a, s) : xq::launch_gemv_q6k(a, s);
+    if (e != cudaSuccess) return XQ_ERR_CUDA;
+  }
+  return XQ_OK;
+}
+
+xq_status matmul_entry(int type, const void* W, const void* xq, int M, int N, int K, float* y,
+                       int32_t* isum, xq_stream stream) {
+  xq_status st = check_shape(M, N, K);
+  if (st != XQ_OK) return st;
+  if (M == 0 || N == 0) return XQ_OK;
+  if (!W || !xq || !y) return XQ_ERR_ARG;
+  if (!aligned16(W) || !aligned16(xq) || !aligned16(y)) return XQ_ERR_ALIGN;
+  if (isum) {
+    if (M > kMaxGemvM) return XQ_ERR_UNSUPPORTED;
+    if (!aligned16(isum)) return XQ_ERR_ALIGN;
+  }
+  return run_matmul(type, W, xq, M, N, K, y, isum, reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t round256(size_t b) { return (b + 255) & ~static_cast<size_t>(255); }
+
+// Validate a layer description and find each input's K (0 = unused).
+xq_status layer_inputs(const xq_proj* proj, int n_proj, int n_inputs, int M, int* in_k) {
+  if (!proj || n_proj < 0 || n_inputs < 0 || n_inputs > 64) return XQ_ERR_ARG;
+  if (M < 0) return XQ_ERR_SHAPE;
+  for (int i = 0; i < n_inputs; ++i) in_k[i] = 0;
+  for (int p = 0; p < n_proj; ++p) {
+    const xq_proj& q = proj[p];
+    if (block_bytes(q.type) == 0) return XQ_ERR_ARG;
+    if (q.input < 0 || q.input >= n_inputs) return XQ_ERR_ARG;
+    const xq_status st = check_shape(M, q.N, q.K);
+    if (st != XQ_OK) return st;
+    if (in_k[q.input] == 0) in_k[q.input] = q.K;
+    if (in_k[q.input] != q.K) return XQ_ERR_SHAPE;
+  }
+  return XQ_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* xq_status_str(xq_status s) {
+  switch (s) {
+    case XQ_OK: return "ok";
+    case XQ_ERR_ARG: return "invalid argument";
+    case XQ_ERR_SHAPE: return "invalid shape";
+    case XQ_ERR_ALIGN: return "pointer not 16-byte aligned";
+    case XQ_ERR_WORKSPACE: return "workspace too small";
+    case XQ_ERR_CUDA: return "CUDA launch failed";
+    case XQ_ERR_UNSUPPORTED: return "unsupported";
+  }
+  return "unknown status";
+}
+
+size_t xq_q8_bytes(int M, int K) {
+  if (M < 0 || K <= 0 || (K % 32) != 0) return 0;
+  const size_t mk = static_cast<size_t>(M) * K;
+  return mk + 8 * (mk / 32);
+}
+
+size_t xq_weight_bytes(int type, int N, int K) {
+  const int bb = block_bytes(type);
+  if (bb == 0 || N < 0 || K <= 0 || (K % 256) != 0) return 0;
+  return static_cast<size_t>(N) * (K / 256) * bb;
+}
+
+xq_status xq_quantize_q8(const float* x, int M, int K, void* xq, xq_stream stream) {
+  if (M < 0 || K <= 0 || (K % 256) != 0) return XQ_ERR_SHAPE;
+  if (M == 0) return XQ_OK;
+  if (!x || !xq) return XQ_ERR_ARG;
+  if (!aligned16(x) || !aligned16(xq)) return XQ_ERR_ALIGN;
+  const size_t mk = static_cast<size_t>(M) * K;
+  uint8_t* base = static_cast<uint8_t*>(xq);
+  const cudaError_t e = xq::launch_quantize_q8(
+      x, M, K, reinterpret_cast<int8_t*>(base), reinterpret_cast<float*>(base + mk),
+      reinterpret_cast<float*>(base + mk + 4 * (mk / 32)), reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? XQ_OK : XQ_ERR_CUDA;
+}
+
+xq_status xq_matmul_q4k_q8(const void* W, const void* xq, int M, int N, int K, float* y,
+                           xq_stream stream) {
+  return matmul_entry(XQ_TYPE_Q4_K, W, xq, M, N, K, y, nullptr, stream);
+}
+
+xq_status xq_matmul_q6k_q8(const void* W, const void* xq, int M, int N, int K, float* y,
+                           xq_stream stream) {
+  return matmul_entry(XQ_TYPE_Q6_K, W, xq, M, N, K, y, nullptr, stream);
+}
+
+xq_status xq_debug_isums_q4k(const void* W, const void* xq, int M, int N, int K, float* y,
+                             int32_t* isum, xq_stream stream) {
+  if (!isum) return XQ_ERR_ARG;
+  return matmul_entry(XQ_TYPE_Q4_K, W, xq, M, N, K, y, isum, stream);
+}
+
+xq_status xq_debug_isums_q6k(const void* W, const void* xq, int M, int N, int K, float* y,
+                             int32_t* isum, xq_stream stream) {
+  if (!isum) return XQ_ERR_ARG;
+  return matmul_entry(XQ_TYPE_Q6_K, W, xq, M, N, K, y, isum, stream);
+}
+
+size_t xq_layer_workspace_bytes(const xq_proj* proj, int n_proj, int n_inputs, int M) {
+  int in_k[64];
+  if (layer_inputs(proj, n_proj, n_inputs, M, in_k) != XQ_OK) return 0;
+  size_t total = 0;
+  for (int i = 0; i < n_inputs; ++i)
+    if (in_k[i]) total += round256(xq_q8_bytes(M, in_k[i]));
+  return total;
+}
+
+xq_status xq_layer_mixed(const xq_proj* proj, int n_proj, const float* const* inputs, int n_inputs,
+                         int M, void* workspace, size_t ws_bytes, xq_stream stream) {
+  int in_k[64];
+  xq_status st = layer_inputs(proj, n_proj, n_inputs, M, in_k);
+  if (st != XQ_OK) return st;
+  if (M == 0) return XQ_OK;
+  if (n_inputs > 0 && !inputs) return XQ_ERR_ARG;
+  size_t need = 0;
+  size_t off[64];
+  for (int i = 0; i < n_inputs; ++i) {
+    off[i] = need;
+    if (in_k[i]) {
+      if (!inputs[i]) return XQ_ERR_ARG;
+      if (!aligned16(inputs[i])) return XQ_ERR_ALIGN;
+      need += round256(xq_q8_bytes(M, in_k[i]));
+    }
+  }
+  if (need > 0 && !workspace) return XQ_ERR_ARG;
+  if (ws_bytes < need) return XQ_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return XQ_ERR_ALIGN;
+  for (int p = 0; p < n_proj; ++p) {
+    if (proj[p].N == 0) continue;
+    if (!proj[p].W || !proj[p].y) return XQ_ERR_ARG;
+    if (!aligned16(proj[p].W) || !aligned16(proj[p].y)) return XQ_ERR_ALIGN;
+  }
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  for (int i = 0; i < n_inputs; ++i) {
+    if (!in_k[i]) continue;
+    st = xq_quantize_q8(inputs[i], M, in_k[i], ws + off[i], stream);
+    if (st != XQ_OK) return st;
+  }
+  for (int p = 0; p < n_proj; ++p) {
+    const xq_proj& q = proj[p];
+    if (q.N == 0) continue;
+    st = run_matmul(q.type, q.W, ws + off[q.input], M, q.N, q.K, q.y, nullptr, s);
+    if (st != XQ_OK) return st;
+  }
+  return XQ_OK;
+}
+
+}  // extern "C"

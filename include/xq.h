@@ -1,0 +1,157 @@
+/*
+ * xq — GGUF Q4_K / Q6_K x Q8 integer matmul on GB300 (sm_103a).
+ *
+ * The operation (xLLM v0.7 long-context article, Tencent Cloud, section 一
+ * "背景"): weights stay in their GGUF k-quant super-blocks; activations are
+ * quantized to 8-bit; each 32-weight (Q4_K) or 16-weight (Q6_K) sub-block is
+ * reduced with an exact integer dot product; scales and mins are applied in
+ * fp32 afterwards; the output is fp32. Weights are never dequantized.
+ *
+ *   y[m][n] = sum_k w[n][k] * (d8[m][k/32] * q8[m][k])
+ *
+ * with w from the super-block formulas (Q4_K: w = d*sc*q - dmin*m;
+ * Q6_K: w = d*s*(q-32)), rearranged as sums of integer sub-block dot products.
+ *
+ * Conventions for every entry point:
+ *  - Every pointer argument is a DEVICE pointer, owned by the caller. The
+ *    library allocates nothing and keeps no state between calls.
+ *  - Calls only enqueue work on `stream` (a cudaStream_t; NULL is the legacy
+ *    default stream) and return without synchronizing.
+ *  - Argument, shape and alignment errors return before anything is enqueued.
+ *    XQ_ERR_CUDA means a launch failed (the CUDA error is left for the caller
+ *    to inspect with cudaGetLastError / cudaPeekAtLastError).
+ *  - There is no fallback: nothing here dequantizes to a float matrix,
+ *    calls cuBLAS, or computes on the CPU.
+ *  - Shapes: K (input features) is a positive multiple of 256; N (output
+ *    features) >= 0; M (tokens) >= 0. M == 0 or N == 0 is an empty product
+ *    and returns XQ_OK without enqueuing anything.
+ *  - Alignment: every pointer must be 16-byte aligned.
+ *
+ * Data layouts (all row-major):
+ *  - x   : fp32 [M][K].
+ *  - W   : GGUF super-blocks, row n is K/256 consecutive blocks;
+ *          Q4_K 144 B per block, Q6_K 210 B per block (public GGUF layout).
+ *  - xq  : one buffer of xq_q8_bytes(M, K) bytes holding three regions,
+ *            qs int8  [M][K]      at byte 0
+ *            d8 fp32  [M][K/32]   at byte M*K
+ *            s8 fp32  [M][K/32]   at byte M*K + 4*M*(K/32)
+ *          d8 = amax/127 of the 32-block, q = round-half-away(x * (1/d8))
+ *          clamped to +-127, s8 = d8 * sum(q) (q8_1 kind: scale and sum).
+ *  - y   : fp32 [M][N].
+ */
+#ifndef XQ_H
+#define XQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define XQ_API __attribute__((visibility("default")))
+#else
+#define XQ_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t; the same type, spelled without the CUDA headers. */
+typedef struct CUstream_st *xq_stream;
+
+typedef enum {
+    XQ_OK = 0,
+    XQ_ERR_ARG = 1,         /* null pointer or unknown type / input index */
+    XQ_ERR_SHAPE = 2,       /* K not a positive multiple of 256, negative M or N,
+                               mismatched K between projections sharing an input */
+    XQ_ERR_ALIGN = 3,       /* a pointer is not 16-byte aligned */
+    XQ_ERR_WORKSPACE = 4,   /* workspace smaller than xq_layer_workspace_bytes() */
+    XQ_ERR_CUDA = 5,        /* a kernel launch failed */
+    XQ_ERR_UNSUPPORTED = 6  /* a shape or type this build does not handle */
+} xq_status;
+
+/* GGUF tensor type ids. */
+#define XQ_TYPE_Q4_K 12
+#define XQ_TYPE_Q6_K 14
+
+/* Human-readable name of a status code (static string, never NULL). */
+XQ_API const char *xq_status_str(xq_status s);
+
+/* Bytes of the Q8 activation buffer for M tokens of K features: 1.25*M*K.
+ * Returns 0 when K is not a positive multiple of 32 or M < 0. */
+XQ_API size_t xq_q8_bytes(int M, int K);
+
+/* Bytes of an N x K weight of GGUF type `type` (N*(K/256)*144 for Q4_K,
+ * N*(K/256)*210 for Q6_K). Returns 0 for an unknown type or a bad shape. */
+XQ_API size_t xq_weight_bytes(int type, int N, int K);
+
+/* Q8 activation quantization (xLLM v0.7 article, sections B1.3 and C.1:
+ * the activation is quantized once to 8-bit and shared by every projection
+ * that reads it; Agent Telemetry log, "批次化 MMVQ": q8_1 blocks of 32 with
+ * a scale and a sum).
+ *   x  : fp32 [M][K], device, read-only.
+ *   xq : device buffer of xq_q8_bytes(M, K) bytes, written (layout above).
+ * K must be a positive multiple of 256 (the super-block width) so that the
+ * result feeds the matmuls directly. Deterministic and bit-exact: fp32 IEEE
+ * divide and reciprocal, round-half-away-from-zero, no contraction. */
+XQ_API xq_status xq_quantize_q8(const float *x, int M, int K, void *xq, xq_stream stream);
+
+/* y = x * W^T for a Q4_K weight (xLLM v0.7 article, section 一 and the M
+ * template of section B2; batch M read once per weight byte, Agent Telemetry
+ * log "批次化 MMVQ").
+ *   W  : Q4_K bytes [N][K/256][144], device, read-only.
+ *   xq : Q8 activations from xq_quantize_q8(.., M, K, ..), device, read-only.
+ *   y  : fp32 [M][N], device, overwritten.
+ * Any M >= 0. */
+XQ_API xq_status xq_matmul_q4k_q8(const void *W, const void *xq, int M, int N, int K,
+                           float *y, xq_stream stream);
+
+/* Same for a Q6_K weight (xLLM v0.7 article, section A2: attn_v and ffn_down
+ * of the mixed model are Q6_K).
+ *   W  : Q6_K bytes [N][K/256][210], device, read-only. Individual blocks are
+ *        2-byte aligned (210 is not a multiple of 4); only the base pointer
+ *        must be 16-byte aligned. */
+XQ_API xq_status xq_matmul_q6k_q8(const void *W, const void *xq, int M, int N, int K,
+                           float *y, xq_stream stream);
+
+/* One projection of a transformer layer for xq_layer_mixed. */
+typedef struct {
+    int type;        /* XQ_TYPE_Q4_K or XQ_TYPE_Q6_K */
+    int N, K;        /* output and input features */
+    const void *W;   /* weight bytes, device */
+    float *y;        /* fp32 [M][N] output, device */
+    int input;       /* index into the layer's inputs[] */
+} xq_proj;
+
+/* Workspace bytes xq_layer_mixed needs: the Q8 buffers of every input that
+ * some projection reads, each rounded up to 256 bytes. 0 on bad arguments. */
+XQ_API size_t xq_layer_workspace_bytes(const xq_proj *proj, int n_proj, int n_inputs, int M);
+
+/* One layer's projections with a quant type per tensor (xLLM v0.7 article,
+ * section A1: Q/K/V/attn_o/gate/up/down dispatch points; section A2: mixed
+ * Q4_K/Q6_K; section C.1: one Q8 quantization shared by every reader).
+ *   proj     : host array of n_proj descriptors (read during the call only).
+ *   inputs   : host array of n_inputs device pointers, fp32 [M][K_i].
+ *              All projections that read input i must agree on K.
+ *   workspace: device buffer of at least xq_layer_workspace_bytes() bytes;
+ *              receives the Q8 activations, one region per input.
+ * Enqueues one quantization per used input and the projections, in order,
+ * on `stream`. */
+XQ_API xq_status xq_layer_mixed(const xq_proj *proj, int n_proj,
+                         const float *const *inputs, int n_inputs, int M,
+                         void *workspace, size_t ws_bytes, xq_stream stream);
+
+/* Test hooks: the same matmul kernels with their exact int32 sub-block sums
+ * written out instead of only consumed.
+ *   Q4_K: isum int32 [M][N][K/32], sub-block j of super-block b at 8b+j.
+ *   Q6_K: isum int32 [M][N][K/16], 16-weight scale group g at 16b+g.
+ * Also writes y like the matmul. M must be in 1..8. */
+XQ_API xq_status xq_debug_isums_q4k(const void *W, const void *xq, int M, int N, int K,
+                             float *y, int32_t *isum, xq_stream stream);
+XQ_API xq_status xq_debug_isums_q6k(const void *W, const void *xq, int M, int N, int K,
+                             float *y, int32_t *isum, xq_stream stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* XQ_H */

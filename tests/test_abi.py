@@ -1,0 +1,107 @@
+"""Host-side checks of the C ABI (no GPU needed, no compute calls).
+
+libxq.so must load and export every entry point include/xq.h declares; the
+size helpers and the argument checks that return before any CUDA call are
+exercised directly.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+from gguf_quant_integer_gb300 import build as xqbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    xqbuild.build()
+    from gguf_quant_integer_gb300 import xq
+    return xq.lib()
+
+
+def declared_symbols():
+    src = open(os.path.join(ROOT, "include", "xq.h")).read()
+    return sorted(set(re.findall(r"XQ_API\s+[\w\s\*]*?\b(xq_\w+)\s*\(", src)))
+
+
+def test_exports_every_declared_symbol(L):
+    from gguf_quant_integer_gb300 import xq
+    decl = declared_symbols()
+    assert len(decl) >= 10
+    assert sorted(xq.SYMBOLS) == decl
+    for name in decl:
+        assert hasattr(L, name), name
+
+
+def test_sizes(L):
+    from gguf_quant_integer_gb300 import xq
+    assert xq.q8_bytes(1, 2048) == 2048 + 8 * 64
+    assert xq.q8_bytes(8, 4096) == int(1.25 * 8 * 4096)
+    assert xq.q8_bytes(0, 256) == 0
+    assert L.xq_q8_bytes(1, 100) == 0
+    assert xq.weight_bytes(12, 256, 2048) == 256 * 8 * 144
+    assert xq.weight_bytes(14, 1024, 4096) == 1024 * 16 * 210
+    assert xq.weight_bytes(99, 1, 256) == 0
+    assert xq.weight_bytes(12, 1, 300) == 0
+
+
+def test_status_strings(L):
+    for code in range(7):
+        assert L.xq_status_str(code)
+    assert L.xq_status_str(99) == b"unknown status"
+
+
+FAKE = 1 << 20  # a 16-byte aligned address that is never dereferenced
+
+
+def test_shape_and_argument_errors_return_before_launch(L):
+    P = ctypes.c_void_p
+    # K not a multiple of 256, negative sizes
+    assert L.xq_matmul_q4k_q8(P(FAKE), P(FAKE), 1, 4, 300, P(FAKE), None) == 2
+    assert L.xq_matmul_q6k_q8(P(FAKE), P(FAKE), -1, 4, 256, P(FAKE), None) == 2
+    assert L.xq_matmul_q4k_q8(P(FAKE), P(FAKE), 1, -4, 256, P(FAKE), None) == 2
+    assert L.xq_quantize_q8(P(FAKE), 1, 0, P(FAKE), None) == 2
+    # empty products are no-ops
+    assert L.xq_matmul_q4k_q8(None, None, 0, 4, 256, None, None) == 0
+    assert L.xq_matmul_q6k_q8(None, None, 2, 0, 256, None, None) == 0
+    assert L.xq_quantize_q8(None, 0, 256, None, None) == 0
+    # null pointers
+    assert L.xq_matmul_q4k_q8(None, P(FAKE), 1, 4, 256, P(FAKE), None) == 1
+    assert L.xq_quantize_q8(P(FAKE), 1, 256, None, None) == 1
+    assert L.xq_debug_isums_q4k(P(FAKE), P(FAKE), 1, 4, 256, P(FAKE), None, None) == 1
+    # misaligned pointers
+    assert L.xq_matmul_q4k_q8(P(FAKE + 8), P(FAKE), 1, 4, 256, P(FAKE), None) == 3
+    assert L.xq_matmul_q6k_q8(P(FAKE), P(FAKE + 4), 1, 4, 256, P(FAKE), None) == 3
+    assert L.xq_quantize_q8(P(FAKE + 2), 1, 256, P(FAKE), None) == 3
+    # the isum hook is limited to one launch of at most 8 tokens
+    assert L.xq_debug_isums_q6k(P(FAKE), P(FAKE), 9, 4, 256, P(FAKE), P(FAKE), None) == 6
+
+
+def test_layer_argument_errors(L):
+    from gguf_quant_integer_gb300 import xq
+    P = ctypes.c_void_p
+
+    def projs(*specs):
+        return xq._proj_array([(t, n, k, None, None, i) for (t, n, k, i) in specs]), len(specs)
+
+    arr, n = projs((12, 16, 512, 0), (14, 8, 512, 0), (12, 16, 1024, 1))
+    need = L.xq_layer_workspace_bytes(arr, n, 2, 4)
+    expect = sum(((xq.q8_bytes(4, k) + 255) // 256) * 256 for k in (512, 1024))
+    assert need == expect
+    # mismatched K on one input
+    bad, nb = projs((12, 16, 512, 0), (12, 16, 768, 0))
+    assert L.xq_layer_workspace_bytes(bad, nb, 1, 4) == 0
+    ins = (ctypes.c_void_p * 2)(FAKE, FAKE)
+    assert L.xq_layer_mixed(bad, nb, ins, 1, 4, P(FAKE), 1 << 20, None) == 2
+    # unknown type, input index out of range
+    bad, nb = projs((13, 16, 512, 0))
+    assert L.xq_layer_mixed(bad, nb, ins, 1, 4, P(FAKE), 1 << 20, None) == 1
+    bad, nb = projs((12, 16, 512, 3))
+    assert L.xq_layer_mixed(bad, nb, ins, 2, 4, P(FAKE), 1 << 20, None) == 1
+    # workspace too small (checked before the projections' pointers)
+    assert L.xq_layer_mixed(arr, n, ins, 2, 4, P(FAKE), need - 1, None) == 4
+    # missing weight pointer
+    assert L.xq_layer_mixed(arr, n, ins, 2, 4, P(FAKE), need, None) == 1
