@@ -55,6 +55,8 @@ def parse_args(argv=None):
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--cpu-sample-layers", type=int, default=8)
+    p.add_argument("--layers", type=int, default=0,
+                   help="run only the first L layers of the sweep (0 = all; small cases for ncu)")
     return p.parse_args(argv)
 
 
@@ -130,13 +132,22 @@ class ClockSampler:
         self.path = os.path.join("/tmp", f"xq_clocks_{os.getpid()}.csv")
 
     def start(self):
+        """Start sampling and wait until the first sample is written, so the
+        sampler is already running when the timed region begins."""
         try:
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.f, stderr=subprocess.DEVNULL)
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu=timestamp,{self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"], stdout=self.f, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
+            return
+        t0 = time.time()
+        while time.time() - t0 < 5.0 and os.path.getsize(self.path) == 0:
+            time.sleep(0.02)
+
+    def mark(self, name):
+        setattr(self, name, time.time())
 
     def stop(self):
         if self.proc is None:
@@ -152,14 +163,14 @@ class ClockSampler:
         with open(self.path) as f:
             for line in f:
                 parts = [p.strip() for p in line.split(",")]
-                if len(parts) < 9:
+                if len(parts) < 10:
                     continue
                 try:
-                    sm.append(float(parts[1]))
-                    smax.append(float(parts[2]))
+                    sm.append(float(parts[2]))
+                    smax.append(float(parts[3]))
                 except ValueError:
                     continue
-                for n, v in zip(names, parts[5:9]):
+                for n, v in zip(names, parts[6:10]):
                     if v.lower() == "active":
                         reasons.add(n)
         try:
@@ -359,10 +370,11 @@ def gpu_arm(args):
 
     wl = synth.WORKLOADS[HEADLINE]
     M = args.m
-    host_w = [synth.gen_layer_weights(wl, l) for l in range(wl.layers)]
+    n_layers = wl.layers if args.layers <= 0 else min(args.layers, wl.layers)
+    host_w = [synth.gen_layer_weights(wl, l) for l in range(n_layers)]
     sweep = Sweep(wl, host_w, device)
     ms_list = sorted({1, 2, 4, 8, M})
-    host_inputs = {m: [synth.gen_layer_inputs(wl, m, l) for l in range(wl.layers)] for m in ms_list}
+    host_inputs = {m: [synth.gen_layer_inputs(wl, m, l) for l in range(n_layers)] for m in ms_list}
     for m in ms_list:
         sweep.prepare(m, host_inputs[m])
     nbytes = sweep.bytes_per_step()
@@ -436,7 +448,7 @@ def gpu_arm(args):
     # ---- CPU oracle on a bounded sample (rank 0, N=1 only)
     cpu = None
     if not args.no_cpu_baseline and rank == 0 and world == 1:
-        S = max(1, min(args.cpu_sample_layers, wl.layers))
+        S = max(1, min(args.cpu_sample_layers, n_layers))
         cs, cb = oracle_sweep_seconds(wl, M, list(range(S)), host_w, host_inputs[M])
         cpu = {"value": round(cb / cs / 1e9, 5), "unit": "GB/s", "cores": 1, "kind": "oracle",
                "seconds": round(cs, 2),
@@ -450,7 +462,8 @@ def gpu_arm(args):
             "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "int8",
             "data": "synthetic (seeded GGUF Q4_K blocks, fp32 N(0,1) activations)",
-            "config": {"workload": HEADLINE, "M": M, "layers": wl.layers,
+            "config": {"workload": HEADLINE if n_layers == wl.layers else f"{HEADLINE} (first {n_layers} layers)",
+                       "M": M, "layers": n_layers,
                        "weight_bytes_per_step": nbytes, "hidden": 4096, "ffn": 14336,
                        "l2": "weights 3.93 GB >> 129 MB L2, streamed from HBM every step; no flush",
                        "parallelism": f"replicas x{world}"},
