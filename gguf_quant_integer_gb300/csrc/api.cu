@@ -22,41 +22,46 @@ xq_status check_shape(int M, int N, int K) {
   return XQ_OK;
 }
 
-struct Q8View {
-  const int8_t* qs;
-  const float* d8;
-  const float* s8;
-};
-
-Q8View q8_view(const void* xq, int M, int K) {
-  const uint8_t* base = static_cast<const uint8_t*>(xq);
-  const size_t mk = static_cast<size_t>(M) * K;
-  Q8View v;
-  v.qs = reinterpret_cast<const int8_t*>(base);
-  v.d8 = reinterpret_cast<const float*>(base + mk);
-  v.s8 = reinterpret_cast<const float*>(base + mk + 4 * (mk / 32));
-  return v;
-}
-
-// Enqueue y = x W^T for any M, in launches of at most 8 tokens.
+// Enqueue y = x W^T for any M: Q4_K on the tensor-core kernel (8-token
+// chunks, up to kMaxProj chunks per launch), Q6_K on the dp4a kernel.
 xq_status run_matmul(int type, const void* W, const void* xq, int M, int N, int K, float* y,
                      int32_t* isum, cudaStream_t s) {
-  const Q8View v = q8_view(xq, M, K);
+  const xq::Q8Layout L = xq::q8_layout(M, K);
+  const uint8_t* base = static_cast<const uint8_t*>(xq);
+  if (type == XQ_TYPE_Q4_K) {
+    xq::MmaProj items[xq::kMaxProj];
+    int n = 0;
+    for (int c = 0; c < L.chunks; ++c) {
+      xq::MmaProj& q = items[n++];
+      q.W = static_cast<const uint8_t*>(W);
+      q.xq = base;
+      q.y = y;
+      q.isum = isum;
+      q.N = N;
+      q.K = K;
+      q.M_total = M;
+      q.chunk = c;
+      if (n == xq::kMaxProj || c + 1 == L.chunks) {
+        if (xq::launch_gemv_q4k_mma(items, n, s, true) != cudaSuccess) return XQ_ERR_CUDA;
+        n = 0;
+      }
+    }
+    return XQ_OK;
+  }
   for (int m0 = 0; m0 < M; m0 += kMaxGemvM) {
     const int mc = (M - m0) < kMaxGemvM ? (M - m0) : kMaxGemvM;
     GemvArgs a;
     a.W = static_cast<const uint8_t*>(W);
-    a.qs = v.qs + static_cast<size_t>(m0) * K;
-    a.d8 = v.d8 + static_cast<size_t>(m0) * (K / 32);
-    a.s8 = v.s8 + static_cast<size_t>(m0) * (K / 32);
+    a.qs = reinterpret_cast<const int8_t*>(base + L.qs) + static_cast<size_t>(m0) * K;
+    a.d8 = reinterpret_cast<const float*>(base + L.d8) + static_cast<size_t>(m0) * (K / 32);
+    a.s8 = reinterpret_cast<const float*>(base + L.s8) + static_cast<size_t>(m0) * (K / 32);
     a.M = mc;
     a.N = N;
     a.K = K;
     a.y = y + static_cast<size_t>(m0) * N;
     a.ldy = N;
     a.isum = isum;
-    const cudaError_t e = (type == XQ_TYPE_Q4_K) ? xq::launch_gemv_q4k(a, s) : xq::launch_gemv_q6k(a, s);
-    if (e != cudaSuccess) return XQ_ERR_CUDA;
+    if (xq::launch_gemv_q6k(a, s) != cudaSuccess) return XQ_ERR_CUDA;
   }
   return XQ_OK;
 }
@@ -113,8 +118,7 @@ const char* xq_status_str(xq_status s) {
 
 size_t xq_q8_bytes(int M, int K) {
   if (M < 0 || K <= 0 || (K % 32) != 0) return 0;
-  const size_t mk = static_cast<size_t>(M) * K;
-  return mk + 8 * (mk / 32);
+  return xq::q8_layout(M, K).total;
 }
 
 size_t xq_weight_bytes(int type, int N, int K) {
@@ -128,11 +132,12 @@ xq_status xq_quantize_q8(const float* x, int M, int K, void* xq, xq_stream strea
   if (M == 0) return XQ_OK;
   if (!x || !xq) return XQ_ERR_ARG;
   if (!aligned16(x) || !aligned16(xq)) return XQ_ERR_ALIGN;
-  const size_t mk = static_cast<size_t>(M) * K;
-  uint8_t* base = static_cast<uint8_t*>(xq);
-  const cudaError_t e = xq::launch_quantize_q8(
-      x, M, K, reinterpret_cast<int8_t*>(base), reinterpret_cast<float*>(base + mk),
-      reinterpret_cast<float*>(base + mk + 4 * (mk / 32)), reinterpret_cast<cudaStream_t>(stream));
+  xq::QuantJob job;
+  job.x = x;
+  job.xq = static_cast<uint8_t*>(xq);
+  job.M = M;
+  job.K = K;
+  const cudaError_t e = xq::launch_quantize_q8(&job, 1, reinterpret_cast<cudaStream_t>(stream), true);
   return e == cudaSuccess ? XQ_OK : XQ_ERR_CUDA;
 }
 
@@ -194,14 +199,53 @@ xq_status xq_layer_mixed(const xq_proj* proj, int n_proj, const float* const* in
   }
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  for (int i = 0; i < n_inputs; ++i) {
-    if (!in_k[i]) continue;
-    st = xq_quantize_q8(inputs[i], M, in_k[i], ws + off[i], stream);
-    if (st != XQ_OK) return st;
+  // One launch quantizes every input that is read (up to kMaxProj per launch).
+  {
+    xq::QuantJob jobs[xq::kMaxProj];
+    int n = 0;
+    for (int i = 0; i < n_inputs; ++i) {
+      if (!in_k[i]) continue;
+      xq::QuantJob& j = jobs[n++];
+      j.x = inputs[i];
+      j.xq = ws + off[i];
+      j.M = M;
+      j.K = in_k[i];
+      if (n == xq::kMaxProj) {
+        if (xq::launch_quantize_q8(jobs, n, s, true) != cudaSuccess) return XQ_ERR_CUDA;
+        n = 0;
+      }
+    }
+    if (n && xq::launch_quantize_q8(jobs, n, s, true) != cudaSuccess) return XQ_ERR_CUDA;
+  }
+  // One launch for the Q4_K projections (8-token chunks, kMaxProj items per launch).
+  {
+    xq::MmaProj items[xq::kMaxProj];
+    int n = 0;
+    const int chunks = (M + 7) / 8;
+    for (int p = 0; p < n_proj; ++p) {
+      const xq_proj& q = proj[p];
+      if (q.N == 0 || q.type != XQ_TYPE_Q4_K) continue;
+      for (int c = 0; c < chunks; ++c) {
+        xq::MmaProj& it = items[n++];
+        it.W = static_cast<const uint8_t*>(q.W);
+        it.xq = ws + off[q.input];
+        it.y = q.y;
+        it.isum = nullptr;
+        it.N = q.N;
+        it.K = q.K;
+        it.M_total = M;
+        it.chunk = c;
+        if (n == xq::kMaxProj) {
+          if (xq::launch_gemv_q4k_mma(items, n, s, true) != cudaSuccess) return XQ_ERR_CUDA;
+          n = 0;
+        }
+      }
+    }
+    if (n && xq::launch_gemv_q4k_mma(items, n, s, true) != cudaSuccess) return XQ_ERR_CUDA;
   }
   for (int p = 0; p < n_proj; ++p) {
     const xq_proj& q = proj[p];
-    if (q.N == 0) continue;
+    if (q.N == 0 || q.type != XQ_TYPE_Q6_K) continue;
     st = run_matmul(q.type, q.W, ws + off[q.input], M, q.N, q.K, q.y, nullptr, s);
     if (st != XQ_OK) return st;
   }

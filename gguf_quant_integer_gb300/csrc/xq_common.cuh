@@ -24,6 +24,12 @@ __device__ __forceinline__ uint4 ld_stream16(const void* p) {
   return v;
 }
 
+__device__ __forceinline__ uint2 ld_stream8(const void* p) {
+  uint2 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
+  return v;
+}
+
 __device__ __forceinline__ unsigned ld_stream4(const void* p) {
   unsigned v;
   asm volatile("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(v) : "l"(p));
@@ -57,6 +63,40 @@ __device__ __forceinline__ float half_bits_to_float(unsigned bits16) {
   return __half2float(__ushort_as_half(static_cast<unsigned short>(bits16 & 0xFFFFu)));
 }
 
+// ------------------------------------------------------- Q8 buffer layout
+//
+// The Q8 activation buffer of M tokens x K features holds, in order:
+//   qs   int8 [M][K]                      at 0
+//   d8   fp32 [M][K/32]                   at M*K
+//   s8   fp32 [M][K/32]                   at M*K + 4*M*K/32
+//   frag fp16 [C][K/32][32][8]            at F = round_up(1.25*M*K, 256)
+//   fsc  fp32 [C][K/32][4][4]             at F + C*16*K
+// with C = ceil(M/8) chunks of 8 tokens. frag and fsc hold the same numbers
+// as qs/d8/s8, laid out as the tensor-core operand of an m16n8k16 MMA with
+// 8 token columns: for chunk c, 32-block j, lane = 4n + t (token n, quad t),
+// slot s: frag = (half) qs[8c+n][32j + 8t + perm[s]], perm = 0,2,1,3,4,6,5,7;
+// fsc[c][j][t] = (d8[8c+2t][j], d8[8c+2t+1][j], s8[8c+2t][j], s8[8c+2t+1][j]).
+// Tokens past M in the last chunk are zero.
+struct Q8Layout {
+  size_t qs, d8, s8, frag, fsc, total;
+  int chunks;
+};
+
+__host__ __device__ inline Q8Layout q8_layout(int M, int K) {
+  Q8Layout L;
+  const size_t mk = static_cast<size_t>(M) * K;
+  L.qs = 0;
+  L.d8 = mk;
+  L.s8 = mk + 4 * (mk / 32);
+  L.chunks = (M + 7) / 8;
+  L.frag = (mk + 8 * (mk / 32) + 255) & ~static_cast<size_t>(255);
+  L.fsc = L.frag + static_cast<size_t>(L.chunks) * 16 * K;
+  L.total = L.fsc + static_cast<size_t>(L.chunks) * 2 * K;
+  return L;
+}
+
+constexpr int kMaxProj = 8;  // projections per grouped launch
+
 // --------------------------------------------------------- launchers
 
 struct GemvArgs {
@@ -70,8 +110,25 @@ struct GemvArgs {
   int32_t* isum;        // optional sub-block sums (test hook)
 };
 
-cudaError_t launch_quantize_q8(const float* x, int M, int K, int8_t* qs, float* d8, float* s8,
-                               cudaStream_t s);
+struct QuantJob {
+  const float* x;   // fp32 [M][K]
+  uint8_t* xq;      // Q8 buffer (layout above)
+  int M, K;
+};
+
+// One launch quantizing up to kMaxProj activations.
+cudaError_t launch_quantize_q8(const QuantJob* jobs, int n, cudaStream_t s, bool pdl);
+
+struct MmaProj {
+  const uint8_t* W;    // Q4_K super-blocks [N][K/256]
+  const uint8_t* xq;   // Q8 buffer of this projection's input (M_total tokens)
+  float* y;            // [M_total][N]; this launch writes tokens 8*chunk .. 8*chunk+7
+  int32_t* isum;       // optional [M_total][N][K/32], only with M_total <= 8
+  int N, K, M_total, chunk;
+};
+
+// One launch for up to kMaxProj Q4_K projections, M <= 8 tokens each.
+cudaError_t launch_gemv_q4k_mma(const MmaProj* projs, int n, cudaStream_t s, bool pdl);
 cudaError_t launch_gemv_q4k(const GemvArgs& a, cudaStream_t s);
 cudaError_t launch_gemv_q6k(const GemvArgs& a, cudaStream_t s);
 

@@ -31,12 +31,19 @@
  *  - x   : fp32 [M][K].
  *  - W   : GGUF super-blocks, row n is K/256 consecutive blocks;
  *          Q4_K 144 B per block, Q6_K 210 B per block (public GGUF layout).
- *  - xq  : one buffer of xq_q8_bytes(M, K) bytes holding three regions,
- *            qs int8  [M][K]      at byte 0
- *            d8 fp32  [M][K/32]   at byte M*K
- *            s8 fp32  [M][K/32]   at byte M*K + 4*M*(K/32)
- *          d8 = amax/127 of the 32-block, q = round-half-away(x * (1/d8))
- *          clamped to +-127, s8 = d8 * sum(q) (q8_1 kind: scale and sum).
+ *  - xq  : one buffer of xq_q8_bytes(M, K) bytes holding five regions,
+ *            qs   int8 [M][K]          at byte 0
+ *            d8   fp32 [M][K/32]       at byte M*K
+ *            s8   fp32 [M][K/32]       at byte M*K + 4*M*(K/32)
+ *            frag fp16 [C][K/32][32][8] at F = round_up(1.25*M*K, 256)
+ *            fsc  fp32 [C][K/32][4][4]  at F + 16*C*K
+ *          with C = ceil(M/8). d8 = amax/127 of the 32-block,
+ *          q = round-half-away(x * (1/d8)) clamped to +-127, s8 = d8*sum(q)
+ *          (q8_1 kind: scale and sum). frag and fsc repeat the same numbers
+ *          in the operand order of the tensor-core matmul (8-token chunks:
+ *          frag[c][j][4n+t][s] = qs[8c+n][32j+8t+p(s)], p = 0,2,1,3,4,6,5,7;
+ *          fsc[c][j][t] = d8,d8,s8,s8 of tokens 8c+2t, 8c+2t+1); tokens
+ *          past M are zero. xq_quantize_q8 writes all five.
  *  - y   : fp32 [M][N].
  */
 #ifndef XQ_H
@@ -76,8 +83,9 @@ typedef enum {
 /* Human-readable name of a status code (static string, never NULL). */
 XQ_API const char *xq_status_str(xq_status s);
 
-/* Bytes of the Q8 activation buffer for M tokens of K features: 1.25*M*K.
- * Returns 0 when K is not a positive multiple of 32 or M < 0. */
+/* Bytes of the Q8 activation buffer for M tokens of K features:
+ * round_up(1.25*M*K, 256) + 18*K*ceil(M/8). Returns 0 when K is not a
+ * positive multiple of 32 or M < 0. */
 XQ_API size_t xq_q8_bytes(int M, int K);
 
 /* Bytes of an N x K weight of GGUF type `type` (N*(K/256)*144 for Q4_K,

@@ -38,9 +38,11 @@ def test_exports_every_declared_symbol(L):
 
 def test_sizes(L):
     from gguf_quant_integer_gb300 import xq
-    assert xq.q8_bytes(1, 2048) == 2048 + 8 * 64
-    assert xq.q8_bytes(8, 4096) == int(1.25 * 8 * 4096)
-    assert xq.q8_bytes(0, 256) == 0
+    def layout(M, K):
+        base = -(-int(1.25 * M * K) // 256) * 256
+        return base + 18 * K * (-(-M // 8))
+    for M, K in ((1, 2048), (8, 4096), (9, 256), (512, 12288), (0, 256)):
+        assert xq.q8_bytes(M, K) == layout(M, K)
     assert L.xq_q8_bytes(1, 100) == 0
     assert xq.weight_bytes(12, 256, 2048) == 256 * 8 * 144
     assert xq.weight_bytes(14, 1024, 4096) == 1024 * 16 * 210

@@ -77,6 +77,49 @@ def test_quantize_bitexact_workload_inputs(xq):
         assert_q8_exact(xq, x)
 
 
+PERM = [0, 2, 1, 3, 4, 6, 5, 7]
+
+
+def expected_operand_image(qs, d8, s8):
+    """The frag / fsc regions restated from their definition in include/xq.h."""
+    M, K = qs.shape
+    C = -(-M // 8)
+    nsub = K // 32
+    qp = np.zeros((8 * C, K), np.int8)
+    qp[:M] = qs
+    dp = np.zeros((8 * C, nsub), np.float32)
+    sp = np.zeros((8 * C, nsub), np.float32)
+    dp[:M], sp[:M] = d8, s8
+    frag = np.zeros((C, nsub, 32, 8), np.float16)
+    fsc = np.zeros((C, nsub, 4, 4), np.float32)
+    for c in range(C):
+        for n in range(8):
+            for t in range(4):
+                pos = 8 * t + np.array(PERM)
+                frag[c, :, 4 * n + t, :] = qp[8 * c + n].reshape(nsub, 32)[:, pos].astype(np.float16)
+        for t in range(4):
+            fsc[c, :, t, 0] = dp[8 * c + 2 * t]
+            fsc[c, :, t, 1] = dp[8 * c + 2 * t + 1]
+            fsc[c, :, t, 2] = sp[8 * c + 2 * t]
+            fsc[c, :, t, 3] = sp[8 * c + 2 * t + 1]
+    return frag, fsc
+
+
+@pytest.mark.parametrize("M,K", [(1, 256), (3, 2048), (8, 4096), (13, 1536)])
+def test_quantize_operand_image(xq, M, K):
+    x = synth.gen_x(300 + M, M, K)
+    buf, rq, rd = assert_q8_exact(xq, x)
+    rs = oracle.quantize_q8(x)[2]
+    frag, fsc = expected_operand_image(rq, rd, rs)
+    raw = buf.cpu().numpy()
+    F = -(-int(1.25 * M * K) // 256) * 256
+    C = -(-M // 8)
+    got_f = raw[F:F + 16 * C * K].view(np.float16).reshape(frag.shape)
+    got_s = raw[F + 16 * C * K:F + 18 * C * K].view(np.float32).reshape(fsc.shape)
+    assert np.array_equal(got_f.view(np.uint16), frag.view(np.uint16))
+    assert np.array_equal(got_s.view(np.uint32), fsc.view(np.uint32))
+
+
 def test_quantize_edge_blocks(xq):
     K = 512
     rng = np.random.default_rng(1)
