@@ -82,6 +82,9 @@ xq_status matmul_entry(int type, const void* W, const void* xq, int M, int N, in
 
 size_t round256(size_t b) { return (b + 255) & ~static_cast<size_t>(255); }
 
+// The layer workspace ends with the grouped matmul's task counter.
+constexpr size_t kCounterBytes = 256;
+
 // Validate a layer description and find each input's K (0 = unused).
 xq_status layer_inputs(const xq_proj* proj, int n_proj, int n_inputs, int M, int* in_k) {
   if (!proj || n_proj < 0 || n_inputs < 0 || n_inputs > 64) return XQ_ERR_ARG;
@@ -169,7 +172,7 @@ size_t xq_layer_workspace_bytes(const xq_proj* proj, int n_proj, int n_inputs, i
   size_t total = 0;
   for (int i = 0; i < n_inputs; ++i)
     if (in_k[i]) total += round256(xq_q8_bytes(M, in_k[i]));
-  return total;
+  return total + kCounterBytes;
 }
 
 xq_status xq_layer_mixed(const xq_proj* proj, int n_proj, const float* const* inputs, int n_inputs,
@@ -189,7 +192,9 @@ xq_status xq_layer_mixed(const xq_proj* proj, int n_proj, const float* const* in
       need += round256(xq_q8_bytes(M, in_k[i]));
     }
   }
-  if (need > 0 && !workspace) return XQ_ERR_ARG;
+  const size_t counter_off = need;
+  need += kCounterBytes;
+  if (!workspace) return XQ_ERR_ARG;
   if (ws_bytes < need) return XQ_ERR_WORKSPACE;
   if (!aligned16(workspace)) return XQ_ERR_ALIGN;
   for (int p = 0; p < n_proj; ++p) {
@@ -199,10 +204,19 @@ xq_status xq_layer_mixed(const xq_proj* proj, int n_proj, const float* const* in
   }
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
+  unsigned int* counter = reinterpret_cast<unsigned int*>(ws + counter_off);
+  const int chunks = (M + 7) / 8;
+  int q4_items = 0;
+  for (int p = 0; p < n_proj; ++p)
+    if (proj[p].N > 0 && proj[p].type == XQ_TYPE_Q4_K) q4_items += chunks;
+  // Dynamic task fetch when every Q4_K chunk fits one launch: the quantize
+  // launch just before it zeroes the counter.
+  const bool dynamic = q4_items > 0 && q4_items <= xq::kMaxProj;
   // One launch quantizes every input that is read (up to kMaxProj per launch).
   {
     xq::QuantJob jobs[xq::kMaxProj];
-    int n = 0;
+    int n = 0, left = 0;
+    for (int i = 0; i < n_inputs; ++i) left += in_k[i] ? 1 : 0;
     for (int i = 0; i < n_inputs; ++i) {
       if (!in_k[i]) continue;
       xq::QuantJob& j = jobs[n++];
@@ -210,18 +224,18 @@ xq_status xq_layer_mixed(const xq_proj* proj, int n_proj, const float* const* in
       j.xq = ws + off[i];
       j.M = M;
       j.K = in_k[i];
-      if (n == xq::kMaxProj) {
-        if (xq::launch_quantize_q8(jobs, n, s, true) != cudaSuccess) return XQ_ERR_CUDA;
+      --left;
+      if (n == xq::kMaxProj || left == 0) {
+        if (xq::launch_quantize_q8(jobs, n, s, true, (left == 0 && dynamic) ? counter : nullptr) != cudaSuccess)
+          return XQ_ERR_CUDA;
         n = 0;
       }
     }
-    if (n && xq::launch_quantize_q8(jobs, n, s, true) != cudaSuccess) return XQ_ERR_CUDA;
   }
   // One launch for the Q4_K projections (8-token chunks, kMaxProj items per launch).
   {
     xq::MmaProj items[xq::kMaxProj];
     int n = 0;
-    const int chunks = (M + 7) / 8;
     for (int p = 0; p < n_proj; ++p) {
       const xq_proj& q = proj[p];
       if (q.N == 0 || q.type != XQ_TYPE_Q4_K) continue;
@@ -236,12 +250,14 @@ xq_status xq_layer_mixed(const xq_proj* proj, int n_proj, const float* const* in
         it.M_total = M;
         it.chunk = c;
         if (n == xq::kMaxProj) {
-          if (xq::launch_gemv_q4k_mma(items, n, s, true) != cudaSuccess) return XQ_ERR_CUDA;
+          if (xq::launch_gemv_q4k_mma(items, n, s, true, dynamic ? counter : nullptr) != cudaSuccess)
+            return XQ_ERR_CUDA;
           n = 0;
         }
       }
     }
-    if (n && xq::launch_gemv_q4k_mma(items, n, s, true) != cudaSuccess) return XQ_ERR_CUDA;
+    if (n && xq::launch_gemv_q4k_mma(items, n, s, true, dynamic ? counter : nullptr) != cudaSuccess)
+      return XQ_ERR_CUDA;
   }
   for (int p = 0; p < n_proj; ++p) {
     const xq_proj& q = proj[p];

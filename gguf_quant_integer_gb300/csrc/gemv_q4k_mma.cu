@@ -1,5 +1,6 @@
 // Q4_K x Q8 -> fp32 for M <= 8 tokens on the tensor cores (mma.sync
-// m16n8k16, fp16 operands holding exact integers, fp32 accumulation).
+// m16n8k16, fp16 operands holding exact integers, fp32 accumulation), with
+// the weights streamed by TMA through a shared-memory ring.
 //
 // What it computes (xLLM v0.7 long-context article, section 一; M template
 // of section B2): for output row n and token m,
@@ -21,64 +22,101 @@
 // accumulation is exact and isum = D * 2^24 (low nibbles) or D * 2^20 (high
 // nibbles), bit for bit. The 2^24 / 2^20 factors are folded into d.
 //
-// Fragment mapping. Lane (n8 = lane/4, t = lane%4) loads 8 quant bytes
-// 32g + 8t .. 32g + 8t + 7 of rows n8 and n8+8 for each g = 0..3: its low
-// nibbles are positions 8t..8t+7 of sub-block 2g, its high nibbles the same
+// Fragment mapping. Lane (n8 = lane/4, t = lane%4) takes 8 quant bytes
+// 32g + 8t .. 32g + 8t + 7 of two rows for each g = 0..3: its low nibbles
+// are positions 8t..8t+7 of sub-block 2g, its high nibbles the same
 // positions of sub-block 2g+1. Even bytes (mask) and odd bytes (shift 8,
 // mask) give the k-slot pairs (2t, 2t+1) and (2t+8, 2t+9) of two MMAs; the
 // activation image written by the quantizer uses the same position order.
+// MMA row i holds weight row pi(i) = 8*(i/8) + 2*(i%4) + (i%8)/4 of the
+// 16-row group, which makes the 8-byte shared-memory loads bank-conflict
+// free on 144-byte rows.
 //
-// Schedule. Persistent CTAs of 4 warps walk a task list covering every
-// projection of the launch. A task is 16 rows whose K is split in quarters
-// over the 4 warps (halves or whole for K < 1024); the partials meet in
-// shared memory in a fixed order. Each warp keeps the next super-block's
-// weight loads in flight while it computes the current one, across task
-// boundaries.
+// Pipeline. Each CTA has one producer lane and 4 consumer warps. A task is
+// 16 rows x all of K; its super-blocks go 4 per ring stage, one per
+// consumer warp (split-K by interleaving), so a warp's partials meet in
+// shared memory in a fixed order at the end of the task. The producer
+// issues one 2D TMA copy (16 rows x 144 bytes, rows past N zero-filled by
+// the tensor map) per super-block into a 4-stage ring guarded by mbarriers,
+// and writes each stage's task id, so it runs ahead across tasks without
+// any CTA-wide barrier. Tasks come from a static stride, or, when a work
+// counter is given, from an atomic counter over a list ordered by cost.
+// Activation operands are read through L1: the image of one input is a few
+// tens of KB shared by every CTA of the projection.
+//
+// Every mbarrier wait is bounded (about 2^32 clocks); on expiry the kernel
+// records an error code and returns.
+#include <cuda.h>
+
 #include "xq_common.cuh"
 
 namespace xq {
 
+__device__ unsigned int g_gemv_error;  // set by a timed-out wait (never expected)
+
 namespace {
 
 struct Proj {
-  const uint8_t* W;
-  const uint4* frag;   // [K/32][32] 16-byte lane operands (chunk 0)
+  CUtensorMap map;     // 2D: {row_bytes/8 u64, N}, box {18, 16}
+  const uint4* frag;   // [K/32][32] 16-byte lane operands of the 8-token chunk
   const float4* fsc;   // [K/32][4]
   float* y;
   int32_t* isum;
-  int N, K, M, kw, task0;
+  int N, K, M, task0;
 };
 
 struct Group {
   Proj p[kMaxProj];
+  unsigned int* counter;  // dynamic task counter (zeroed before launch) or null
   int n, total;
 };
 
-struct Pos {
-  int p, rg, b0, b1;
-  bool valid;
-};
+constexpr int kStages = 4;
+constexpr int kBlockBytes = 16 * kQ4kBytes;                 // 16 rows x one super-block
+constexpr int kStageBytes = 4 * kBlockBytes;                // one super-block per consumer warp
+constexpr int kDecBytes = 8 * 16 * 16;                      // (a, a, b, b) per sub-block and row
+constexpr int kRedBytes = 2 * 4 * 32 * 16;
+constexpr int kSmemBytes = kStages * kStageBytes + 4 * kDecBytes + kRedBytes + kStages * 16 + 2 * kStages * 8;
+constexpr long long kWaitClocks = 1LL << 32;
 
-__device__ __forceinline__ Pos locate(const Group& G, int task, int warp) {
-  Pos s;
-  s.valid = task < G.total;
-  if (!s.valid) {
-    s.p = 0; s.rg = 0; s.b0 = 0; s.b1 = 0;
-    return s;
+__device__ __forceinline__ int mma_row(int i) { return 8 * (i >> 3) + 2 * (i & 3) + ((i >> 2) & 1); }
+
+// ---------------------------------------------------------------- PTX
+__device__ __forceinline__ void mbar_init(uint32_t a, unsigned n) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(a), "r"(n));
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t a, unsigned bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(a), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t a) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(a) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t a, unsigned parity) {
+  unsigned ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(a), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait: false (and an error code recorded) if the phase never completes.
+__device__ __forceinline__ bool mbar_wait(uint32_t a, unsigned parity, unsigned code) {
+  if (mbar_try_wait(a, parity)) return true;
+  const long long t0 = clock64();
+  while (!mbar_try_wait(a, parity)) {
+    if (clock64() - t0 > kWaitClocks) {
+      atomicExch(&g_gemv_error, code);
+      return false;
+    }
   }
-  int p = 0;
-#pragma unroll 1
-  while (p + 1 < G.n && task >= G.p[p + 1].task0) ++p;
-  const Proj& P = G.p[p];
-  const int kw = P.kw;
-  const int tl = task - P.task0;
-  const int nsb = P.K >> 8;
-  const int kp = warp % kw;
-  s.p = p;
-  s.rg = tl * (4 / kw) + warp / kw;
-  s.b0 = nsb * kp / kw;
-  s.b1 = nsb * (kp + 1) / kw;
-  return s;
+  return true;
+}
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t mbar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(map), "r"(x), "r"(y), "r"(mbar)
+      : "memory");
 }
 
 __device__ __forceinline__ void mma16816(float (&d)[4], unsigned a0, unsigned a1, unsigned a2,
@@ -90,114 +128,108 @@ __device__ __forceinline__ void mma16816(float (&d)[4], unsigned a0, unsigned a1
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-constexpr int kRing = 4;            // weight steps in flight per warp
-constexpr int kStepBytes = 16 * kQ4kBytes;  // 16 rows x one super-block
-
-// Shared-memory slot of weight row i (0..15) of a step. Lane (n8, t) reads
-// rows n8 and n8+8; with 144-byte rows, slot 2*(n8%4) + n8/4 puts the four
-// rows a half-warp reads 8 banks apart, so the 8-byte quant loads and the
-// 16-byte header loads are conflict-free.
-__device__ __forceinline__ int row_slot(int i) {
-  return 8 * (i >> 3) + 2 * (i & 3) + ((i >> 2) & 1);
-}
-
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes));
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N)); }
-
-// Packed fp32 pairs.
-__device__ __forceinline__ unsigned long long pk(float lo, float hi) {
-  unsigned long long r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-  return r;
-}
-__device__ __forceinline__ unsigned long long fma2(unsigned long long a, unsigned long long b,
-                                                   unsigned long long c) {
-  unsigned long long d;
+// Packed fp32 pairs (.x in the low half).
+typedef unsigned long long f2;
+__device__ __forceinline__ f2 fma2(f2 a, f2 b, f2 c) {
+  f2 d;
   asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
   return d;
 }
-__device__ __forceinline__ unsigned long long mul2(unsigned long long a, unsigned long long b) {
-  unsigned long long d;
+__device__ __forceinline__ f2 mul2(f2 a, f2 b) {
+  f2 d;
   asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
   return d;
 }
-__device__ __forceinline__ float lo32(unsigned long long v) { return __uint_as_float(static_cast<unsigned>(v)); }
-__device__ __forceinline__ float hi32(unsigned long long v) { return __uint_as_float(static_cast<unsigned>(v >> 32)); }
+__device__ __forceinline__ f2 pk(float lo, float hi) {
+  f2 r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ float lo32(f2 v) { return __uint_as_float(static_cast<unsigned>(v)); }
+__device__ __forceinline__ float hi32(f2 v) { return __uint_as_float(static_cast<unsigned>(v >> 32)); }
 
 // Byte k of a packed word as 2^23 + byte, an exact fp32 (0x4B0000xx).
 __device__ __forceinline__ float byte_plus_2p23(unsigned w, int k) {
   return __uint_as_float(prmt(w, 0x4B000000u, 0x7540u | static_cast<unsigned>(k)));
 }
 
-// Issue the copies of one step (16 rows x super-block b) into a ring slot.
-// Chunk c (0..143) of the step is 16 bytes: row c/9, piece c%9.
-__device__ __forceinline__ void issue_step(const Proj& P, int rg, int b, uint32_t slot_base, int lane) {
-  const int nsb = P.K >> 8;
+// ---------------------------------------------------------------- tasks
+struct TaskPos {
+  int p, rg, nsb;
+};
+
+__device__ __forceinline__ TaskPos task_pos(const Group& G, int task) {
+  int p = 0;
+#pragma unroll 1
+  while (p + 1 < G.n && task >= G.p[p + 1].task0) ++p;
+  TaskPos s;
+  s.p = p;
+  s.rg = task - G.p[p].task0;
+  s.nsb = G.p[p].K >> 8;
+  return s;
+}
+
+// Decode the 16 rows' scales of one super-block into the warp's table:
+// lane l takes weight row l/2 and sub-blocks 4*(l&1) .. +3, writing
+// (alpha, alpha, beta, beta) with alpha = d*sc*2^24 (low nibbles) or
+// d*sc*2^20 (high), beta = -dmin*m, each as (2^23 + byte)*x - 2^23*x: one
+// rounding of an exact product. Packed bytes (public Q4_K layout):
+//   j < 4 : sc = s[j] & 63, m = s[j+4] & 63
+//   j >= 4: sc = (s[j+4] & 15) | (s[j-4] >> 6) << 4, m = (s[j+4] >> 4) | (s[j] >> 6) << 4
+__device__ __forceinline__ void decode_scales(const uint8_t* blk, float4* dec, int lane) {
+  const int r = lane >> 1, half = lane & 1;
+  const uint4 hd = *reinterpret_cast<const uint4*>(blk + r * kQ4kBytes);
+  const unsigned scw = half ? ((hd.w & 0x0F0F0F0Fu) | ((hd.y >> 2) & 0x30303030u)) : (hd.y & 0x3F3F3F3Fu);
+  const unsigned mnw = half ? (((hd.w >> 4) & 0x0F0F0F0Fu) | ((hd.z >> 2) & 0x30303030u)) : (hd.z & 0x3F3F3F3Fu);
+  const float d = half_bits_to_float(hd.x);
+  const float dl = d * 16777216.0f, dh = d * 1048576.0f;
+  const float dm = -half_bits_to_float(hd.x >> 16);
+  const float cl = -8388608.0f * dl, ch = -8388608.0f * dh, cm = -8388608.0f * dm;
 #pragma unroll
-  for (int k = 0; k < 5; ++k) {
-    const int c = lane + 32 * k;
-    if (c < 144) {
-      const int i = c / 9, piece = c - 9 * (c / 9);
-      const int row = rg * 16 + i;
-      const bool ok = row < P.N;
-      const uint8_t* src = ok ? P.W + (static_cast<size_t>(row) * nsb + b) * kQ4kBytes + 16 * piece : P.W;
-      cp_async16(slot_base + row_slot(i) * kQ4kBytes + 16 * piece, src, ok ? 16u : 0u);
-    }
+  for (int k = 0; k < 4; ++k) {
+    const int j = 4 * half + k;
+    const float a = (k & 1) ? fmaf(byte_plus_2p23(scw, k), dh, ch) : fmaf(byte_plus_2p23(scw, k), dl, cl);
+    const float bm = fmaf(byte_plus_2p23(mnw, k), dm, cm);
+    dec[j * 16 + r] = make_float4(a, a, bm, bm);
   }
 }
 
 template <bool ISUM>
-__device__ __forceinline__ void compute_step(const uint8_t* st, const Proj& P, int rg, int b, int n8,
-                                             int t, int lane, unsigned long long (&acc)[2]) {
-  // Weight operands of rows n8 and n8 + 8 from the ring slot.
-  const int s0 = row_slot(n8), s1 = row_slot(n8 + 8);
-  const uint4 h0 = *reinterpret_cast<const uint4*>(st + s0 * kQ4kBytes);
-  const uint4 h1 = *reinterpret_cast<const uint4*>(st + s1 * kQ4kBytes);
+__device__ __forceinline__ void compute_block(const uint8_t* blk, const float4* dec, const Proj& P, int rg, int b,
+                                              int n8, int t, int lane, f2 (&acc)[2]) {
+  const int r0 = mma_row(n8), r1 = r0 + 8;
   uint2 q0[4], q1[4];
 #pragma unroll
   for (int g = 0; g < 4; ++g) {
-    q0[g] = *reinterpret_cast<const uint2*>(st + s0 * kQ4kBytes + 16 + 32 * g + 8 * t);
-    q1[g] = *reinterpret_cast<const uint2*>(st + s1 * kQ4kBytes + 16 + 32 * g + 8 * t);
+    q0[g] = *reinterpret_cast<const uint2*>(blk + r0 * kQ4kBytes + 16 + 32 * g + 8 * t);
+    q1[g] = *reinterpret_cast<const uint2*>(blk + r1 * kQ4kBytes + 16 + 32 * g + 8 * t);
   }
-  // sc and m of the 8 sub-blocks as packed bytes:
-  //   j < 4 : sc = s[j] & 63, m = s[j+4] & 63
-  //   j >= 4: sc = (s[j+4] & 15) | (s[j-4] >> 6) << 4, m = (s[j+4] >> 4) | (s[j] >> 6) << 4
-  unsigned scw[2][2], mnw[2][2];
-  float dl[2], dh[2], dm[2];
-  const uint4 hh[2] = {h0, h1};
-#pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    const uint4 hd = hh[h];
-    scw[h][0] = hd.y & 0x3F3F3F3Fu;
-    mnw[h][0] = hd.z & 0x3F3F3F3Fu;
-    scw[h][1] = (hd.w & 0x0F0F0F0Fu) | ((hd.y >> 2) & 0x30303030u);
-    mnw[h][1] = ((hd.w >> 4) & 0x0F0F0F0Fu) | ((hd.z >> 2) & 0x30303030u);
-    const float d = half_bits_to_float(hd.x);
-    dl[h] = d * 16777216.0f;  // 2^24: low-nibble sums arrive as isum * 2^-24
-    dh[h] = d * 1048576.0f;   // 2^20: high-nibble sums arrive as 16 * isum * 2^-24
-    dm[h] = -half_bits_to_float(hd.x >> 16);
-  }
-  const int nsub = P.K >> 5;
-  // Activation operands of the 8 sub-blocks, loaded one sub-block ahead.
   const uint4* fp = P.frag + static_cast<size_t>(8 * b) * 32 + lane;
-  const float4* sp = P.fsc + static_cast<size_t>(8 * b) * 4 + t;
+  const ulonglong2* sp = reinterpret_cast<const ulonglong2*>(P.fsc + static_cast<size_t>(8 * b) * 4) + t;
+  const ulonglong2* dp = reinterpret_cast<const ulonglong2*>(dec);
   uint4 Bn = __ldg(fp);
-  float4 fn = __ldg(sp);
+  ulonglong2 fn = __ldg(sp);
+  // Pull this warp's next super-block of activation operands (36 lines of
+  // 128 bytes: 32 of operands, 4 of scale quads) into L1 while this one runs.
+  if (b + 4 < (P.K >> 8)) {
+    const char* nf = reinterpret_cast<const char*>(P.frag + static_cast<size_t>(8 * (b + 4)) * 32);
+    asm volatile("prefetch.global.L1 [%0];" ::"l"(nf + 128 * lane));
+    if (lane < 4) {
+      const char* ns = reinterpret_cast<const char*>(P.fsc + static_cast<size_t>(8 * (b + 4)) * 4);
+      asm volatile("prefetch.global.L1 [%0];" ::"l"(ns + 128 * lane));
+    }
+  }
 #pragma unroll
   for (int g = 0; g < 4; ++g) {
-    const unsigned w0a = q0[g].x, w1a = q0[g].y;  // row n8
-    const unsigned w0b = q1[g].x, w1b = q1[g].y;  // row n8 + 8
+    const unsigned w0a = q0[g].x, w1a = q0[g].y;  // row r0
+    const unsigned w0b = q1[g].x, w1b = q1[g].y;  // row r1
     const unsigned s0a = w0a >> 8, s1a = w1a >> 8, s0b = w0b >> 8, s1b = w1b >> 8;
 #pragma unroll
     for (int hi = 0; hi < 2; ++hi) {
       const unsigned mk = hi ? 0x00F000F0u : 0x000F000Fu;
       const int j = 2 * g + hi;
       const uint4 B = Bn;
-      const float4 f = fn;
+      const ulonglong2 f = fn;  // (d8 c0, d8 c1), (s8 c0, s8 c1)
       if (j < 7) {
         Bn = __ldg(fp + (j + 1) * 32);
         fn = __ldg(sp + (j + 1) * 4);
@@ -205,22 +237,17 @@ __device__ __forceinline__ void compute_step(const uint8_t* st, const Proj& P, i
       float D[4] = {0.0f, 0.0f, 0.0f, 0.0f};
       mma16816(D, w0a & mk, w0b & mk, s0a & mk, s0b & mk, B.x, B.y);
       mma16816(D, w1a & mk, w1b & mk, s1a & mk, s1b & mk, B.z, B.w);
-      // alpha = d*sc*2^24 (or 2^20), beta = -dmin*m, each from the byte via
-      // (2^23 + byte)*x - 2^23*x: one rounding of an exact product.
-      const int k = j & 3, wsel = j >> 2;
-      const float a0 = fmaf(byte_plus_2p23(scw[0][wsel], k), hi ? dh[0] : dl[0], -8388608.0f * (hi ? dh[0] : dl[0]));
-      const float a1 = fmaf(byte_plus_2p23(scw[1][wsel], k), hi ? dh[1] : dl[1], -8388608.0f * (hi ? dh[1] : dl[1]));
-      const float b0 = fmaf(byte_plus_2p23(mnw[0][wsel], k), dm[0], -8388608.0f * dm[0]);
-      const float b1 = fmaf(byte_plus_2p23(mnw[1][wsel], k), dm[1], -8388608.0f * dm[1]);
-      const unsigned long long d8p = pk(f.x, f.y), s8p = pk(f.z, f.w);
-      acc[0] = fma2(mul2(pk(a0, a0), d8p), pk(D[0], D[1]), fma2(pk(b0, b0), s8p, acc[0]));
-      acc[1] = fma2(mul2(pk(a1, a1), d8p), pk(D[2], D[3]), fma2(pk(b1, b1), s8p, acc[1]));
+      const ulonglong2 e0 = dp[j * 16 + r0];  // (a, a), (b, b) of row r0
+      const ulonglong2 e1 = dp[j * 16 + r1];
+      acc[0] = fma2(mul2(e0.x, f.x), pk(D[0], D[1]), fma2(e0.y, f.y, acc[0]));
+      acc[1] = fma2(mul2(e1.x, f.x), pk(D[2], D[3]), fma2(e1.y, f.y, acc[1]));
       if (ISUM) {
         const float scale = hi ? 1048576.0f : 16777216.0f;
+        const int nsub = P.K >> 5;
         const int sb = 8 * b + j;
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const int row = rg * 16 + n8 + 8 * (e >> 1);
+          const int row = rg * 16 + ((e >> 1) ? r1 : r0);
           const int col = 2 * t + (e & 1);
           if (row < P.N && col < P.M)
             P.isum[(static_cast<size_t>(col) * P.N + row) * nsub + sb] = static_cast<int32_t>(D[e] * scale);
@@ -230,9 +257,9 @@ __device__ __forceinline__ void compute_step(const uint8_t* st, const Proj& P, i
   }
 }
 
-__device__ __forceinline__ void store_y(const Proj& P, int rg, int n8, int t, float v00, float v01,
-                                        float v10, float v11) {
-  const int r0 = rg * 16 + n8, r1 = r0 + 8, c0 = 2 * t, c1 = c0 + 1;
+__device__ __forceinline__ void store_y(const Proj& P, int rg, int n8, int t, float v00, float v01, float v10,
+                                        float v11) {
+  const int r0 = rg * 16 + mma_row(n8), r1 = r0 + 8, c0 = 2 * t, c1 = c0 + 1;
   if (r0 < P.N) {
     if (c0 < P.M) P.y[static_cast<size_t>(c0) * P.N + r0] = v00;
     if (c1 < P.M) P.y[static_cast<size_t>(c1) * P.N + r0] = v01;
@@ -243,96 +270,120 @@ __device__ __forceinline__ void store_y(const Proj& P, int rg, int n8, int t, fl
   }
 }
 
-// A cursor over this warp's steps: (task, super-block) pairs.
-struct Cursor {
-  int task;
-  Pos pos;
-  int b;
-};
-
-__device__ __forceinline__ void cursor_init(Cursor& c, const Group& G, int task, int warp) {
-  c.task = task;
-  c.pos = locate(G, task, warp);
-  c.b = c.pos.b0;
-}
-
-__device__ __forceinline__ void cursor_next(Cursor& c, const Group& G, int warp) {
-  if (++c.b >= c.pos.b1) cursor_init(c, G, c.task + gridDim.x, warp);
+__device__ __forceinline__ int next_task(const Group& G, int cur) {
+  if (G.counter) return static_cast<int>(atomicAdd(G.counter, 1u));
+  return cur + static_cast<int>(gridDim.x);
 }
 
 template <bool ISUM>
-__global__ void __launch_bounds__(128, 4)
+__global__ void __launch_bounds__(160, 3)
 gemv_q4k_mma_kernel(const __grid_constant__ Group G) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint8_t* ring = smem;
+  float4* dec_all = reinterpret_cast<float4*>(smem + kStages * kStageBytes);
+  float4* red = reinterpret_cast<float4*>(smem + kStages * kStageBytes + 4 * kDecBytes);
+  int4* meta = reinterpret_cast<int4*>(smem + kStages * kStageBytes + 4 * kDecBytes + kRedBytes);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes + 4 * kDecBytes + kRedBytes + kStages * 16);
+  const uint32_t ring_s = static_cast<uint32_t>(__cvta_generic_to_shared(ring));
+  const uint32_t full_s = static_cast<uint32_t>(__cvta_generic_to_shared(bars));
+  const uint32_t empty_s = full_s + kStages * 8;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(full_s + 8 * s, 1);
+      mbar_init(empty_s + 8 * s, 4);
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  // The activation image and the task counter may be written by the
+  // previous grid on the stream: wait for it before reading either.
   cudaGridDependencySynchronize();
   cudaTriggerProgrammaticLaunchCompletion();
-  const int lane = threadIdx.x & 31;
-  const int warp = threadIdx.x >> 5;
-  const int n8 = lane >> 2, t = lane & 3;
-  __shared__ __align__(16) uint8_t ring[4][kRing][kStepBytes];
-  __shared__ float4 red[2][4][32];
-  int nbar = 0;
-  const uint32_t ring_base = static_cast<uint32_t>(__cvta_generic_to_shared(&ring[warp][0][0]));
 
-  // Producer cursor runs kRing - 1 steps ahead of the consumer cursor.
-  Cursor pc, cc;
-  cursor_init(pc, G, blockIdx.x, warp);
-  cc = pc;
-  int issued = 0;
-#pragma unroll
-  for (int k = 0; k < kRing - 1; ++k) {
-    if (pc.pos.valid) {
-      issue_step(G.p[pc.pos.p], pc.pos.rg, pc.b, ring_base + (issued % kRing) * kStepBytes, lane);
-      cursor_next(pc, G, warp);
-    }
-    cp_async_commit();
-    ++issued;
-  }
-  int consumed = 0;
-  while (cc.pos.valid) {
-    const Proj& P = G.p[cc.pos.p];
-    unsigned long long acc[2] = {0ull, 0ull};
-    const int rg = cc.pos.rg;
-    const int b1 = cc.pos.b1;
-    for (int b = cc.pos.b0; b < b1; ++b) {
-      if (pc.pos.valid) {
-        issue_step(G.p[pc.pos.p], pc.pos.rg, pc.b, ring_base + (issued % kRing) * kStepBytes, lane);
-        cursor_next(pc, G, warp);
+  if (warp == 4) {
+    // ------------------------------------------------------- producer
+    if (lane != 0) return;
+    int task = G.counter ? static_cast<int>(atomicAdd(G.counter, 1u)) : static_cast<int>(blockIdx.x);
+    int slot = 0;
+    unsigned fills = 0;  // completed passes over the ring
+    for (;;) {
+      const bool valid = task < G.total;
+      TaskPos tp = {0, 0, 0};
+      int nst = 1;
+      if (valid) {
+        tp = task_pos(G, task);
+        nst = (tp.nsb + 3) >> 2;
       }
-      cp_async_commit();
-      ++issued;
-      cp_async_wait<kRing - 1>();
-      __syncwarp();
-      compute_step<ISUM>(&ring[warp][consumed % kRing][0], P, rg, b, n8, t, lane, acc);
-      __syncwarp();
-      ++consumed;
+      const int nxt = valid ? next_task(G, task) : task;
+      for (int k = 0; k < nst; ++k) {
+        if (fills > 0 && !mbar_wait(empty_s + 8 * slot, (fills - 1) & 1, 1)) return;
+        meta[slot] = make_int4(valid ? task : -1, k, (k == nst - 1) ? 1 : 0, 0);
+        if (!valid) {
+          mbar_arrive(full_s + 8 * slot);
+          return;
+        }
+        const int b0 = 4 * k;
+        const int nb = (tp.nsb - b0) < 4 ? (tp.nsb - b0) : 4;
+        mbar_expect_tx(full_s + 8 * slot, static_cast<unsigned>(nb * kBlockBytes));
+        const CUtensorMap* map = &G.p[tp.p].map;
+        for (int w = 0; w < nb; ++w)
+          tma_load_2d(ring_s + slot * kStageBytes + w * kBlockBytes, map, (b0 + w) * (kQ4kBytes / 8), tp.rg * 16,
+                      full_s + 8 * slot);
+        if (++slot == kStages) {
+          slot = 0;
+          ++fills;
+        }
+      }
+      task = nxt;
     }
-    if (P.kw == 1) {
-      store_y(P, rg, n8, t, lo32(acc[0]), hi32(acc[0]), lo32(acc[1]), hi32(acc[1]));
-    } else {
-      const int buf = nbar & 1;
-      ++nbar;
-      red[buf][warp][lane] = make_float4(lo32(acc[0]), hi32(acc[0]), lo32(acc[1]), hi32(acc[1]));
-      __syncthreads();
-      if (warp % P.kw == 0) {
-        float4 v = red[buf][warp][lane];
-        for (int w = 1; w < P.kw; ++w) {
-          const float4 u = red[buf][warp + w][lane];
+  }
+
+  // --------------------------------------------------------- consumers
+  const int n8 = lane >> 2, t = lane & 3;
+  float4* dec = dec_all + warp * (kDecBytes / 16);
+  f2 acc[2] = {0ull, 0ull};
+  int slot = 0, nred = 0;
+  unsigned fills = 0;
+  for (;;) {
+    if (!mbar_wait(full_s + 8 * slot, fills & 1, 2)) return;
+    const int4 m = meta[slot];
+    if (m.x < 0) return;
+    const TaskPos tp = task_pos(G, m.x);
+    const Proj& P = G.p[tp.p];
+    const int b = 4 * m.y + warp;
+    const uint8_t* blk = ring + slot * kStageBytes + warp * kBlockBytes;
+    if (b < tp.nsb) {
+      decode_scales(blk, dec, lane);
+      __syncwarp();
+      compute_block<ISUM>(blk, dec, P, tp.rg, b, n8, t, lane, acc);
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty_s + 8 * slot);
+    if (m.z) {
+      // End of the task: the 4 warps' split-K partials, summed in warp order.
+      float4* rb = red + (nred & 1) * 4 * 32;
+      rb[warp * 32 + lane] = make_float4(lo32(acc[0]), hi32(acc[0]), lo32(acc[1]), hi32(acc[1]));
+      asm volatile("bar.sync 1, 128;" ::: "memory");
+      if (warp == 0) {
+        float4 v = rb[lane];
+#pragma unroll
+        for (int w = 1; w < 4; ++w) {
+          const float4 u = rb[w * 32 + lane];
           v.x += u.x; v.y += u.y; v.z += u.z; v.w += u.w;
         }
-        store_y(P, rg, n8, t, v.x, v.y, v.z, v.w);
+        store_y(P, tp.rg, n8, t, v.x, v.y, v.z, v.w);
       }
+      ++nred;
+      acc[0] = 0ull;
+      acc[1] = 0ull;
     }
-    cursor_init(cc, G, cc.task + gridDim.x, warp);
+    if (++slot == kStages) {
+      slot = 0;
+      ++fills;
+    }
   }
-  cp_async_wait<0>();
-}
-
-// Split-K factor: 4 warps share each 16-row group whenever K allows, so a
-// layer has thousands of short tasks and the persistent grid ends evenly.
-int choose_kw(int nsb) {
-  if (nsb >= 4) return 4;
-  if (nsb >= 2) return 2;
-  return 1;
 }
 
 template <bool ISUM>
@@ -340,30 +391,71 @@ int max_ctas() {
   static int per_sm = -1;
   if (per_sm < 0) {
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, gemv_q4k_mma_kernel<ISUM>, 128, 0) != cudaSuccess || n < 1)
+    cudaFuncSetAttribute(gemv_q4k_mma_kernel<ISUM>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, gemv_q4k_mma_kernel<ISUM>, 160, kSmemBytes) != cudaSuccess ||
+        n < 1)
       n = 1;
     per_sm = n;
   }
   return per_sm * kNumSMs;
 }
 
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+// Q4_K rows as a 2D tensor of 8-byte elements: {row_bytes/8, N}.
+bool encode_weight_map(CUtensorMap* map, const uint8_t* W, int N, int K) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t row_bytes = static_cast<cuuint64_t>(K / 256) * kQ4kBytes;
+  const cuuint64_t dims[2] = {row_bytes / 8, static_cast<cuuint64_t>(N)};
+  const cuuint64_t strides[1] = {row_bytes};
+  const cuuint32_t box[2] = {kQ4kBytes / 8, 16};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT64, 2, const_cast<uint8_t*>(W), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace
 
-cudaError_t launch_gemv_q4k_mma(const MmaProj* projs, int n, cudaStream_t s, bool pdl) {
+cudaError_t launch_gemv_q4k_mma(const MmaProj* projs, int n, cudaStream_t s, bool pdl, unsigned int* counter) {
   if (n <= 0 || n > kMaxProj) return cudaErrorInvalidValue;
+  // Most expensive tasks first (dynamic scheduling takes them in order).
+  int order[kMaxProj];
+  for (int k = 0; k < n; ++k) order[k] = k;
+  for (int a = 1; a < n; ++a)
+    for (int b = a; b > 0 && projs[order[b]].K > projs[order[b - 1]].K; --b) {
+      const int tmp = order[b];
+      order[b] = order[b - 1];
+      order[b - 1] = tmp;
+    }
   Group G;
   G.n = n;
+  G.counter = counter;
   int total = 0;
   bool isum = false;
   for (int k = 0; k < n; ++k) {
-    const MmaProj& q = projs[k];
-    const int nsb = q.K >> 8;
-    int kw = choose_kw(nsb);
-    if (kw > nsb) kw = 1;
+    const MmaProj& q = projs[order[k]];
     const Q8Layout L = q8_layout(q.M_total, q.K);
     const int m0 = 8 * q.chunk;
     Proj& P = G.p[k];
-    P.W = q.W;
+    if (!encode_weight_map(&P.map, q.W, q.N, q.K)) return cudaErrorInvalidValue;
     P.frag = reinterpret_cast<const uint4*>(q.xq + L.frag + static_cast<size_t>(q.chunk) * 16 * q.K);
     P.fsc = reinterpret_cast<const float4*>(q.xq + L.fsc + static_cast<size_t>(q.chunk) * 2 * q.K);
     P.y = q.y + static_cast<size_t>(m0) * q.N;
@@ -371,10 +463,8 @@ cudaError_t launch_gemv_q4k_mma(const MmaProj* projs, int n, cudaStream_t s, boo
     P.N = q.N;
     P.K = q.K;
     P.M = (q.M_total - m0) < 8 ? (q.M_total - m0) : 8;
-    P.kw = kw;
     P.task0 = total;
-    const int rows_per_task = 16 * (4 / kw);
-    total += (q.N + rows_per_task - 1) / rows_per_task;
+    total += (q.N + 15) / 16;
     isum = isum || (q.isum != nullptr);
   }
   G.total = total;
@@ -382,7 +472,8 @@ cudaError_t launch_gemv_q4k_mma(const MmaProj* projs, int n, cudaStream_t s, boo
   const int cap = isum ? max_ctas<true>() : max_ctas<false>();
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(total < cap ? total : cap));
-  cfg.blockDim = dim3(128);
+  cfg.blockDim = dim3(160);
+  cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

@@ -25,6 +25,7 @@ namespace xq {
 struct QuantGroup {
   QuantJob job[kMaxProj];
   long long blk0[kMaxProj + 1];  // prefix of padded 32-blocks per job
+  unsigned int* zero_word;       // optional: set to 0 (the next matmul's task counter)
   int n;
 };
 
@@ -32,6 +33,7 @@ __global__ void __launch_bounds__(256)
 quantize_q8_kernel(const __grid_constant__ QuantGroup G) {
   // Inputs may be written by the previous kernel on the stream.
   cudaGridDependencySynchronize();
+  if (G.zero_word && blockIdx.x == 0 && threadIdx.x == 0) *G.zero_word = 0u;
   const int lane = threadIdx.x & 31;
   const long long warp = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const long long nwarps = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
@@ -89,10 +91,11 @@ quantize_q8_kernel(const __grid_constant__ QuantGroup G) {
   cudaTriggerProgrammaticLaunchCompletion();
 }
 
-cudaError_t launch_quantize_q8(const QuantJob* jobs, int n, cudaStream_t s, bool pdl) {
+cudaError_t launch_quantize_q8(const QuantJob* jobs, int n, cudaStream_t s, bool pdl, unsigned int* zero_word) {
   if (n <= 0 || n > kMaxProj) return cudaErrorInvalidValue;
   QuantGroup G;
   G.n = n;
+  G.zero_word = zero_word;
   G.blk0[0] = 0;
   for (int k = 0; k < n; ++k) {
     G.job[k] = jobs[k];

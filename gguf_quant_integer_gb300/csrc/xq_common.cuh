@@ -116,8 +116,10 @@ struct QuantJob {
   int M, K;
 };
 
-// One launch quantizing up to kMaxProj activations.
-cudaError_t launch_quantize_q8(const QuantJob* jobs, int n, cudaStream_t s, bool pdl);
+// One launch quantizing up to kMaxProj activations; also stores 0 to
+// *zero_word when it is given (the next grouped matmul's task counter).
+cudaError_t launch_quantize_q8(const QuantJob* jobs, int n, cudaStream_t s, bool pdl,
+                               unsigned int* zero_word = nullptr);
 
 struct MmaProj {
   const uint8_t* W;    // Q4_K super-blocks [N][K/256]
@@ -127,8 +129,11 @@ struct MmaProj {
   int N, K, M_total, chunk;
 };
 
-// One launch for up to kMaxProj Q4_K projections, M <= 8 tokens each.
-cudaError_t launch_gemv_q4k_mma(const MmaProj* projs, int n, cudaStream_t s, bool pdl);
+// One launch for up to kMaxProj Q4_K projection chunks of <= 8 tokens. With
+// a counter (zeroed by the previous kernel on the stream) tasks are fetched
+// dynamically, most expensive first; without one they are strided.
+cudaError_t launch_gemv_q4k_mma(const MmaProj* projs, int n, cudaStream_t s, bool pdl,
+                                unsigned int* counter = nullptr);
 cudaError_t launch_gemv_q4k(const GemvArgs& a, cudaStream_t s);
 cudaError_t launch_gemv_q6k(const GemvArgs& a, cudaStream_t s);
 

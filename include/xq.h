@@ -131,7 +131,8 @@ typedef struct {
 } xq_proj;
 
 /* Workspace bytes xq_layer_mixed needs: the Q8 buffers of every input that
- * some projection reads, each rounded up to 256 bytes. 0 on bad arguments. */
+ * some projection reads, each rounded up to 256 bytes, plus 256 bytes of
+ * scheduling state. 0 on bad arguments. */
 XQ_API size_t xq_layer_workspace_bytes(const xq_proj *proj, int n_proj, int n_inputs, int M);
 
 /* One layer's projections with a quant type per tensor (xLLM v0.7 article,
