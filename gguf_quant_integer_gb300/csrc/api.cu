@@ -82,8 +82,27 @@ xq_status matmul_entry(int type, const void* W, const void* xq, int M, int N, in
 
 size_t round256(size_t b) { return (b + 255) & ~static_cast<size_t>(255); }
 
-// The layer workspace ends with the grouped matmul's task counter.
+// The layer workspace ends with the grouped matmul's scheduling state: a
+// 256-byte task counter, the arrival counts of split projections, and their
+// partial sums (sizes from the same helpers the launcher uses).
 constexpr size_t kCounterBytes = 256;
+
+struct SchedBytes {
+  size_t arrive, partial;
+};
+
+SchedBytes sched_bytes(const xq_proj* proj, int n_proj, int M) {
+  SchedBytes b = {0, 0};
+  for (int p = 0; p < n_proj; ++p) {
+    if (proj[p].type != XQ_TYPE_Q4_K || proj[p].N == 0) continue;
+    const int nch = xq::q4k_split_chunks(proj[p].K, M);
+    if (nch > 1) {
+      b.arrive += xq::q4k_split_arrive_bytes(proj[p].N);
+      b.partial += xq::q4k_split_partial_bytes(proj[p].N, nch);
+    }
+  }
+  return b;
+}
 
 // Validate a layer description and find each input's K (0 = unused).
 xq_status layer_inputs(const xq_proj* proj, int n_proj, int n_inputs, int M, int* in_k) {
@@ -172,7 +191,8 @@ size_t xq_layer_workspace_bytes(const xq_proj* proj, int n_proj, int n_inputs, i
   size_t total = 0;
   for (int i = 0; i < n_inputs; ++i)
     if (in_k[i]) total += round256(xq_q8_bytes(M, in_k[i]));
-  return total + kCounterBytes;
+  const SchedBytes sb = sched_bytes(proj, n_proj, M);
+  return total + kCounterBytes + sb.arrive + sb.partial;
 }
 
 xq_status xq_layer_mixed(const xq_proj* proj, int n_proj, const float* const* inputs, int n_inputs,
@@ -193,7 +213,8 @@ xq_status xq_layer_mixed(const xq_proj* proj, int n_proj, const float* const* in
     }
   }
   const size_t counter_off = need;
-  need += kCounterBytes;
+  const SchedBytes sb = sched_bytes(proj, n_proj, M);
+  need += kCounterBytes + sb.arrive + sb.partial;
   if (!workspace) return XQ_ERR_ARG;
   if (ws_bytes < need) return XQ_ERR_WORKSPACE;
   if (!aligned16(workspace)) return XQ_ERR_ALIGN;
@@ -209,9 +230,12 @@ xq_status xq_layer_mixed(const xq_proj* proj, int n_proj, const float* const* in
   int q4_items = 0;
   for (int p = 0; p < n_proj; ++p)
     if (proj[p].N > 0 && proj[p].type == XQ_TYPE_Q4_K) q4_items += chunks;
-  // Dynamic task fetch when every Q4_K chunk fits one launch: the quantize
-  // launch just before it zeroes the counter.
+  // Dynamic task fetch and K-split when every Q4_K chunk fits one launch:
+  // the quantize launch just before it zeroes the counter and the arrival
+  // counts (which the matmul also leaves at zero).
   const bool dynamic = q4_items > 0 && q4_items <= xq::kMaxProj;
+  uint8_t* split_ws = dynamic ? ws + counter_off + kCounterBytes : nullptr;
+  const int zero_words = static_cast<int>((kCounterBytes + sb.arrive) / 4);
   // One launch quantizes every input that is read (up to kMaxProj per launch).
   {
     xq::QuantJob jobs[xq::kMaxProj];
@@ -226,7 +250,8 @@ xq_status xq_layer_mixed(const xq_proj* proj, int n_proj, const float* const* in
       j.K = in_k[i];
       --left;
       if (n == xq::kMaxProj || left == 0) {
-        if (xq::launch_quantize_q8(jobs, n, s, true, (left == 0 && dynamic) ? counter : nullptr) != cudaSuccess)
+        if (xq::launch_quantize_q8(jobs, n, s, true, (left == 0 && dynamic) ? counter : nullptr, zero_words) !=
+            cudaSuccess)
           return XQ_ERR_CUDA;
         n = 0;
       }
@@ -250,13 +275,13 @@ xq_status xq_layer_mixed(const xq_proj* proj, int n_proj, const float* const* in
         it.M_total = M;
         it.chunk = c;
         if (n == xq::kMaxProj) {
-          if (xq::launch_gemv_q4k_mma(items, n, s, true, dynamic ? counter : nullptr) != cudaSuccess)
+          if (xq::launch_gemv_q4k_mma(items, n, s, true, dynamic ? counter : nullptr, split_ws) != cudaSuccess)
             return XQ_ERR_CUDA;
           n = 0;
         }
       }
     }
-    if (n && xq::launch_gemv_q4k_mma(items, n, s, true, dynamic ? counter : nullptr) != cudaSuccess)
+    if (n && xq::launch_gemv_q4k_mma(items, n, s, true, dynamic ? counter : nullptr, split_ws) != cudaSuccess)
       return XQ_ERR_CUDA;
   }
   for (int p = 0; p < n_proj; ++p) {

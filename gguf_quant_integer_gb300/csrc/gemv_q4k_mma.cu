@@ -33,16 +33,19 @@
 // free on 144-byte rows.
 //
 // Pipeline. Each CTA has one producer lane and 4 consumer warps. A task is
-// 16 rows x all of K; its super-blocks go 4 per ring stage, one per
-// consumer warp (split-K by interleaving), so a warp's partials meet in
-// shared memory in a fixed order at the end of the task. The producer
-// issues one 2D TMA copy (16 rows x 144 bytes, rows past N zero-filled by
-// the tensor map) per super-block into a 4-stage ring guarded by mbarriers,
-// and writes each stage's task id, so it runs ahead across tasks without
-// any CTA-wide barrier. Tasks come from a static stride, or, when a work
-// counter is given, from an atomic counter over a list ordered by cost.
-// Activation operands are read through L1: the image of one input is a few
-// tens of KB shared by every CTA of the projection.
+// 64 rows (16 per consumer warp) x a range of super-blocks; every ring stage
+// holds one super-block of those 64 rows (four 2D TMA boxes of 16 rows x
+// 144 bytes, rows past N zero-filled by the tensor map) and the activation
+// operands of that super-block (two 1D bulk copies, 4.6 KB), which all four
+// warps share. The producer writes each stage's task id and runs ahead
+// across tasks through a 4-stage ring guarded by mbarriers, with no
+// CTA-wide barrier. Tasks come from a static stride, or, when a work counter
+// is given, from an atomic counter over a list ordered by cost. Long rows
+// (more than 24 super-blocks) can be split into K-chunks of about 16
+// super-blocks handled by different CTAs: each writes its partial sums to a
+// workspace, and the last CTA to finish a 64-row block (an atomic arrival
+// count) adds the chunks in chunk order and writes y, so the result does
+// not depend on which CTA finishes last.
 //
 // Every mbarrier wait is bounded (about 2^32 clocks); on expiry the kernel
 // records an error code and returns.
@@ -58,11 +61,13 @@ namespace {
 
 struct Proj {
   CUtensorMap map;     // 2D: {row_bytes/8 u64, N}, box {18, 16}
-  const uint4* frag;   // [K/32][32] 16-byte lane operands of the 8-token chunk
-  const float4* fsc;   // [K/32][4]
+  const uint8_t* frag; // [K/32][32][16 B] lane operands of the 8-token chunk
+  const uint8_t* fsc;  // [K/32][4][16 B]
   float* y;
   int32_t* isum;
-  int N, K, M, task0;
+  float* partial;      // split: [nch][8][64 * row blocks]
+  unsigned int* arrive;  // split: one arrival count per 64-row block
+  int N, K, M, task0, nch;
 };
 
 struct Group {
@@ -73,10 +78,11 @@ struct Group {
 
 constexpr int kStages = 4;
 constexpr int kBlockBytes = 16 * kQ4kBytes;                 // 16 rows x one super-block
-constexpr int kStageBytes = 4 * kBlockBytes;                // one super-block per consumer warp
+constexpr int kFragOff = 4 * kBlockBytes;                   // 9216
+constexpr int kFscOff = kFragOff + 8 * 512;                 // 13312
+constexpr int kStageBytes = kFscOff + 8 * 64;               // 13824
 constexpr int kDecBytes = 8 * 16 * 16;                      // (a, a, b, b) per sub-block and row
-constexpr int kRedBytes = 2 * 4 * 32 * 16;
-constexpr int kSmemBytes = kStages * kStageBytes + 4 * kDecBytes + kRedBytes + kStages * 16 + 2 * kStages * 8;
+constexpr int kSmemBytes = kStages * kStageBytes + 4 * kDecBytes + kStages * 16 + 2 * kStages * 8 + 16;
 constexpr long long kWaitClocks = 1LL << 32;
 
 __device__ __forceinline__ int mma_row(int i) { return 8 * (i >> 3) + 2 * (i & 3) + ((i >> 2) & 1); }
@@ -119,9 +125,15 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, unsigned bytes, uint32_t mbar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(mbar)
+               : "memory");
+}
+
 __device__ __forceinline__ void mma16816(float (&d)[4], unsigned a0, unsigned a1, unsigned a2,
                                          unsigned a3, unsigned b0, unsigned b1) {
-  asm volatile(
+  asm(
       "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
       "{%0,%1,%2,%3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
@@ -155,17 +167,22 @@ __device__ __forceinline__ float byte_plus_2p23(unsigned w, int k) {
 
 // ---------------------------------------------------------------- tasks
 struct TaskPos {
-  int p, rg, nsb;
+  int p, rb, b0, b1, c;
 };
 
 __device__ __forceinline__ TaskPos task_pos(const Group& G, int task) {
   int p = 0;
 #pragma unroll 1
   while (p + 1 < G.n && task >= G.p[p + 1].task0) ++p;
+  const Proj& P = G.p[p];
+  const int local = task - P.task0;
+  const int nsb = P.K >> 8;
   TaskPos s;
   s.p = p;
-  s.rg = task - G.p[p].task0;
-  s.nsb = G.p[p].K >> 8;
+  s.rb = local / P.nch;
+  s.c = local - s.rb * P.nch;
+  s.b0 = nsb * s.c / P.nch;
+  s.b1 = nsb * (s.c + 1) / P.nch;
   return s;
 }
 
@@ -195,8 +212,8 @@ __device__ __forceinline__ void decode_scales(const uint8_t* blk, float4* dec, i
 }
 
 template <bool ISUM>
-__device__ __forceinline__ void compute_block(const uint8_t* blk, const float4* dec, const Proj& P, int rg, int b,
-                                              int n8, int t, int lane, f2 (&acc)[2]) {
+__device__ __forceinline__ void compute_block(const uint8_t* blk, const uint8_t* act, const float4* dec,
+                                              const Proj& P, int rg, int b, int n8, int t, int lane, f2 (&acc)[2]) {
   const int r0 = mma_row(n8), r1 = r0 + 8;
   uint2 q0[4], q1[4];
 #pragma unroll
@@ -204,21 +221,14 @@ __device__ __forceinline__ void compute_block(const uint8_t* blk, const float4* 
     q0[g] = *reinterpret_cast<const uint2*>(blk + r0 * kQ4kBytes + 16 + 32 * g + 8 * t);
     q1[g] = *reinterpret_cast<const uint2*>(blk + r1 * kQ4kBytes + 16 + 32 * g + 8 * t);
   }
-  const uint4* fp = P.frag + static_cast<size_t>(8 * b) * 32 + lane;
-  const ulonglong2* sp = reinterpret_cast<const ulonglong2*>(P.fsc + static_cast<size_t>(8 * b) * 4) + t;
+  // Activation operands and scale quads of the super-block, from the stage.
+  const uint4* fp = reinterpret_cast<const uint4*>(act) + lane;
+  const ulonglong2* sp = reinterpret_cast<const ulonglong2*>(act + (kFscOff - kFragOff)) + t;
   const ulonglong2* dp = reinterpret_cast<const ulonglong2*>(dec);
-  uint4 Bn = __ldg(fp);
-  ulonglong2 fn = __ldg(sp);
-  // Pull this warp's next super-block of activation operands (36 lines of
-  // 128 bytes: 32 of operands, 4 of scale quads) into L1 while this one runs.
-  if (b + 4 < (P.K >> 8)) {
-    const char* nf = reinterpret_cast<const char*>(P.frag + static_cast<size_t>(8 * (b + 4)) * 32);
-    asm volatile("prefetch.global.L1 [%0];" ::"l"(nf + 128 * lane));
-    if (lane < 4) {
-      const char* ns = reinterpret_cast<const char*>(P.fsc + static_cast<size_t>(8 * (b + 4)) * 4);
-      asm volatile("prefetch.global.L1 [%0];" ::"l"(ns + 128 * lane));
-    }
-  }
+  // The four shared-memory operands of a sub-block are loaded one sub-block
+  // ahead of their use.
+  uint4 Bn = fp[0];
+  ulonglong2 fn = sp[0], e0n = dp[r0], e1n = dp[r1];
 #pragma unroll
   for (int g = 0; g < 4; ++g) {
     const unsigned w0a = q0[g].x, w1a = q0[g].y;  // row r0
@@ -230,15 +240,16 @@ __device__ __forceinline__ void compute_block(const uint8_t* blk, const float4* 
       const int j = 2 * g + hi;
       const uint4 B = Bn;
       const ulonglong2 f = fn;  // (d8 c0, d8 c1), (s8 c0, s8 c1)
+      const ulonglong2 e0 = e0n, e1 = e1n;  // (a, a), (b, b) of rows r0, r1
       if (j < 7) {
-        Bn = __ldg(fp + (j + 1) * 32);
-        fn = __ldg(sp + (j + 1) * 4);
+        Bn = fp[(j + 1) * 32];
+        fn = sp[(j + 1) * 4];
+        e0n = dp[(j + 1) * 16 + r0];
+        e1n = dp[(j + 1) * 16 + r1];
       }
       float D[4] = {0.0f, 0.0f, 0.0f, 0.0f};
       mma16816(D, w0a & mk, w0b & mk, s0a & mk, s0b & mk, B.x, B.y);
       mma16816(D, w1a & mk, w1b & mk, s1a & mk, s1b & mk, B.z, B.w);
-      const ulonglong2 e0 = dp[j * 16 + r0];  // (a, a), (b, b) of row r0
-      const ulonglong2 e1 = dp[j * 16 + r1];
       acc[0] = fma2(mul2(e0.x, f.x), pk(D[0], D[1]), fma2(e0.y, f.y, acc[0]));
       acc[1] = fma2(mul2(e1.x, f.x), pk(D[2], D[3]), fma2(e1.y, f.y, acc[1]));
       if (ISUM) {
@@ -281,9 +292,9 @@ gemv_q4k_mma_kernel(const __grid_constant__ Group G) {
   extern __shared__ __align__(128) uint8_t smem[];
   uint8_t* ring = smem;
   float4* dec_all = reinterpret_cast<float4*>(smem + kStages * kStageBytes);
-  float4* red = reinterpret_cast<float4*>(smem + kStages * kStageBytes + 4 * kDecBytes);
-  int4* meta = reinterpret_cast<int4*>(smem + kStages * kStageBytes + 4 * kDecBytes + kRedBytes);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes + 4 * kDecBytes + kRedBytes + kStages * 16);
+  int4* meta = reinterpret_cast<int4*>(smem + kStages * kStageBytes + 4 * kDecBytes);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes + 4 * kDecBytes + kStages * 16);
+  int* last_flag = reinterpret_cast<int*>(smem + kStages * kStageBytes + 4 * kDecBytes + kStages * 16 + 2 * kStages * 8);
   const uint32_t ring_s = static_cast<uint32_t>(__cvta_generic_to_shared(ring));
   const uint32_t full_s = static_cast<uint32_t>(__cvta_generic_to_shared(bars));
   const uint32_t empty_s = full_s + kStages * 8;
@@ -297,8 +308,8 @@ gemv_q4k_mma_kernel(const __grid_constant__ Group G) {
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
-  // The activation image and the task counter may be written by the
-  // previous grid on the stream: wait for it before reading either.
+  // The activation image, the task counter and the arrival counts may be
+  // written by the previous grid on the stream: wait for it first.
   cudaGridDependencySynchronize();
   cudaTriggerProgrammaticLaunchCompletion();
 
@@ -310,27 +321,25 @@ gemv_q4k_mma_kernel(const __grid_constant__ Group G) {
     unsigned fills = 0;  // completed passes over the ring
     for (;;) {
       const bool valid = task < G.total;
-      TaskPos tp = {0, 0, 0};
-      int nst = 1;
-      if (valid) {
-        tp = task_pos(G, task);
-        nst = (tp.nsb + 3) >> 2;
-      }
+      TaskPos tp = {0, 0, 0, 1, 0};
+      if (valid) tp = task_pos(G, task);
       const int nxt = valid ? next_task(G, task) : task;
-      for (int k = 0; k < nst; ++k) {
+      for (int b = tp.b0; b < tp.b1; ++b) {
         if (fills > 0 && !mbar_wait(empty_s + 8 * slot, (fills - 1) & 1, 1)) return;
-        meta[slot] = make_int4(valid ? task : -1, k, (k == nst - 1) ? 1 : 0, 0);
+        meta[slot] = make_int4(valid ? task : -1, b, (b == tp.b1 - 1) ? 1 : 0, 0);
         if (!valid) {
           mbar_arrive(full_s + 8 * slot);
           return;
         }
-        const int b0 = 4 * k;
-        const int nb = (tp.nsb - b0) < 4 ? (tp.nsb - b0) : 4;
-        mbar_expect_tx(full_s + 8 * slot, static_cast<unsigned>(nb * kBlockBytes));
-        const CUtensorMap* map = &G.p[tp.p].map;
-        for (int w = 0; w < nb; ++w)
-          tma_load_2d(ring_s + slot * kStageBytes + w * kBlockBytes, map, (b0 + w) * (kQ4kBytes / 8), tp.rg * 16,
-                      full_s + 8 * slot);
+        const Proj& P = G.p[tp.p];
+        const int rows = P.N - tp.rb * 64;  // > 0
+        const int nblk = rows >= 64 ? 4 : (rows + 15) / 16;
+        mbar_expect_tx(full_s + 8 * slot, static_cast<unsigned>(nblk * kBlockBytes + 8 * 512 + 8 * 64));
+        const uint32_t st = ring_s + slot * kStageBytes;
+        for (int w = 0; w < nblk; ++w)
+          tma_load_2d(st + w * kBlockBytes, &P.map, b * (kQ4kBytes / 8), tp.rb * 64 + 16 * w, full_s + 8 * slot);
+        bulk_load(st + kFragOff, P.frag + static_cast<size_t>(b) * 8 * 512, 8 * 512, full_s + 8 * slot);
+        bulk_load(st + kFscOff, P.fsc + static_cast<size_t>(b) * 8 * 64, 8 * 64, full_s + 8 * slot);
         if (++slot == kStages) {
           slot = 0;
           ++fills;
@@ -344,38 +353,67 @@ gemv_q4k_mma_kernel(const __grid_constant__ Group G) {
   const int n8 = lane >> 2, t = lane & 3;
   float4* dec = dec_all + warp * (kDecBytes / 16);
   f2 acc[2] = {0ull, 0ull};
-  int slot = 0, nred = 0;
+  int slot = 0;
   unsigned fills = 0;
+  int cur_task = -1;
+  TaskPos tp = {0, 0, 0, 0, 0};
   for (;;) {
     if (!mbar_wait(full_s + 8 * slot, fills & 1, 2)) return;
     const int4 m = meta[slot];
     if (m.x < 0) return;
-    const TaskPos tp = task_pos(G, m.x);
+    if (m.x != cur_task) {  // task geometry, once per task
+      cur_task = m.x;
+      tp = task_pos(G, m.x);
+    }
     const Proj& P = G.p[tp.p];
-    const int b = 4 * m.y + warp;
-    const uint8_t* blk = ring + slot * kStageBytes + warp * kBlockBytes;
-    if (b < tp.nsb) {
-      decode_scales(blk, dec, lane);
+    const int rg = tp.rb * 4 + warp;  // this warp's 16-row group
+    const uint8_t* st = ring + slot * kStageBytes;
+    const bool rows_ok = rg * 16 < P.N;
+    if (rows_ok) {
+      decode_scales(st + warp * kBlockBytes, dec, lane);
       __syncwarp();
-      compute_block<ISUM>(blk, dec, P, tp.rg, b, n8, t, lane, acc);
+      compute_block<ISUM>(st + warp * kBlockBytes, st + kFragOff, dec, P, rg, m.y, n8, t, lane, acc);
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(empty_s + 8 * slot);
     if (m.z) {
-      // End of the task: the 4 warps' split-K partials, summed in warp order.
-      float4* rb = red + (nred & 1) * 4 * 32;
-      rb[warp * 32 + lane] = make_float4(lo32(acc[0]), hi32(acc[0]), lo32(acc[1]), hi32(acc[1]));
-      asm volatile("bar.sync 1, 128;" ::: "memory");
-      if (warp == 0) {
-        float4 v = rb[lane];
-#pragma unroll
-        for (int w = 1; w < 4; ++w) {
-          const float4 u = rb[w * 32 + lane];
-          v.x += u.x; v.y += u.y; v.z += u.z; v.w += u.w;
+      if (P.nch == 1) {
+        if (rows_ok) store_y(P, rg, n8, t, lo32(acc[0]), hi32(acc[0]), lo32(acc[1]), hi32(acc[1]));
+      } else {
+        // K-chunk partial of a split task; the last CTA of the row block adds
+        // the chunks in chunk order.
+        const int rows_pad = ((P.N + 63) / 64) * 64;
+        float* part = P.partial + static_cast<size_t>(tp.c) * 8 * rows_pad;
+        const int r0 = rg * 16 + mma_row(n8), r1 = r0 + 8, c0 = 2 * t, c1 = c0 + 1;
+        part[static_cast<size_t>(c0) * rows_pad + r0] = lo32(acc[0]);
+        part[static_cast<size_t>(c1) * rows_pad + r0] = hi32(acc[0]);
+        part[static_cast<size_t>(c0) * rows_pad + r1] = lo32(acc[1]);
+        part[static_cast<size_t>(c1) * rows_pad + r1] = hi32(acc[1]);
+        __threadfence();
+        asm volatile("bar.sync 1, 128;" ::: "memory");
+        if (threadIdx.x == 0) {
+          const unsigned old = atomicAdd(P.arrive + tp.rb, 1u);
+          const int last = old == static_cast<unsigned>(P.nch - 1);
+          if (last) {
+            __threadfence();
+            P.arrive[tp.rb] = 0u;  // ready for the next launch
+          }
+          *last_flag = last;
         }
-        store_y(P, tp.rg, n8, t, v.x, v.y, v.z, v.w);
+        asm volatile("bar.sync 1, 128;" ::: "memory");
+        if (*last_flag && rows_ok) {
+          float v[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+          for (int c = 0; c < P.nch; ++c) {
+            const float* pc = P.partial + static_cast<size_t>(c) * 8 * rows_pad;
+            v[0] += __ldcg(pc + static_cast<size_t>(c0) * rows_pad + r0);
+            v[1] += __ldcg(pc + static_cast<size_t>(c1) * rows_pad + r0);
+            v[2] += __ldcg(pc + static_cast<size_t>(c0) * rows_pad + r1);
+            v[3] += __ldcg(pc + static_cast<size_t>(c1) * rows_pad + r1);
+          }
+          store_y(P, rg, n8, t, v[0], v[1], v[2], v[3]);
+        }
+        asm volatile("bar.sync 1, 128;" ::: "memory");
       }
-      ++nred;
       acc[0] = 0ull;
       acc[1] = 0ull;
     }
@@ -434,37 +472,69 @@ bool encode_weight_map(CUtensorMap* map, const uint8_t* W, int N, int K) {
 
 }  // namespace
 
-cudaError_t launch_gemv_q4k_mma(const MmaProj* projs, int n, cudaStream_t s, bool pdl, unsigned int* counter) {
+cudaError_t launch_gemv_q4k_mma(const MmaProj* projs, int n, cudaStream_t s, bool pdl, unsigned int* counter,
+                                uint8_t* split_ws) {
   if (n <= 0 || n > kMaxProj) return cudaErrorInvalidValue;
+  // Per-projection K-chunking (only with a split workspace) and task cost.
+  int nch[kMaxProj], cost[kMaxProj];
+  for (int k = 0; k < n; ++k) {
+    nch[k] = split_ws ? q4k_split_chunks(projs[k].K, projs[k].M_total) : 1;
+    cost[k] = ((projs[k].K >> 8) + nch[k] - 1) / nch[k];
+  }
   // Most expensive tasks first (dynamic scheduling takes them in order).
   int order[kMaxProj];
   for (int k = 0; k < n; ++k) order[k] = k;
   for (int a = 1; a < n; ++a)
-    for (int b = a; b > 0 && projs[order[b]].K > projs[order[b - 1]].K; --b) {
+    for (int b = a; b > 0 && cost[order[b]] > cost[order[b - 1]]; --b) {
       const int tmp = order[b];
       order[b] = order[b - 1];
       order[b - 1] = tmp;
     }
+  // Split workspace: every item's arrival counts first (one zeroed range),
+  // then the partial buffers, both in item order.
+  size_t arrive_off[kMaxProj], partial_off[kMaxProj];
+  {
+    size_t a = 0, p = 0;
+    for (int k = 0; k < n; ++k)
+      if (nch[k] > 1) {
+        arrive_off[k] = a;
+        a += q4k_split_arrive_bytes(projs[k].N);
+      }
+    for (int k = 0; k < n; ++k)
+      if (nch[k] > 1) {
+        partial_off[k] = a + p;
+        p += q4k_split_partial_bytes(projs[k].N, nch[k]);
+      }
+  }
   Group G;
   G.n = n;
   G.counter = counter;
   int total = 0;
   bool isum = false;
   for (int k = 0; k < n; ++k) {
-    const MmaProj& q = projs[order[k]];
+    const int src = order[k];
+    const MmaProj& q = projs[src];
     const Q8Layout L = q8_layout(q.M_total, q.K);
     const int m0 = 8 * q.chunk;
     Proj& P = G.p[k];
     if (!encode_weight_map(&P.map, q.W, q.N, q.K)) return cudaErrorInvalidValue;
-    P.frag = reinterpret_cast<const uint4*>(q.xq + L.frag + static_cast<size_t>(q.chunk) * 16 * q.K);
-    P.fsc = reinterpret_cast<const float4*>(q.xq + L.fsc + static_cast<size_t>(q.chunk) * 2 * q.K);
+    P.frag = q.xq + L.frag + static_cast<size_t>(q.chunk) * 16 * q.K;
+    P.fsc = q.xq + L.fsc + static_cast<size_t>(q.chunk) * 2 * q.K;
     P.y = q.y + static_cast<size_t>(m0) * q.N;
     P.isum = q.isum;
     P.N = q.N;
     P.K = q.K;
     P.M = (q.M_total - m0) < 8 ? (q.M_total - m0) : 8;
+    P.nch = nch[src];
+    P.partial = nullptr;
+    P.arrive = nullptr;
+    const int rbs = (q.N + 63) / 64;
+    if (P.nch > 1) {
+      P.partial = reinterpret_cast<float*>(split_ws + partial_off[src]);
+      P.arrive = reinterpret_cast<unsigned int*>(split_ws + arrive_off[src]);
+    }
     P.task0 = total;
-    total += (q.N + 15) / 16;
+    total += rbs * P.nch;
     isum = isum || (q.isum != nullptr);
   }
   G.total = total;

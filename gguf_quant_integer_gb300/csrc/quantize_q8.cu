@@ -25,7 +25,8 @@ namespace xq {
 struct QuantGroup {
   QuantJob job[kMaxProj];
   long long blk0[kMaxProj + 1];  // prefix of padded 32-blocks per job
-  unsigned int* zero_word;       // optional: set to 0 (the next matmul's task counter)
+  unsigned int* zero_words;      // optional: words set to 0 (the next matmul's scheduling state)
+  int zero_count;
   int n;
 };
 
@@ -33,7 +34,8 @@ __global__ void __launch_bounds__(256)
 quantize_q8_kernel(const __grid_constant__ QuantGroup G) {
   // Inputs may be written by the previous kernel on the stream.
   cudaGridDependencySynchronize();
-  if (G.zero_word && blockIdx.x == 0 && threadIdx.x == 0) *G.zero_word = 0u;
+  if (blockIdx.x == 0)
+    for (int i = threadIdx.x; i < G.zero_count; i += blockDim.x) G.zero_words[i] = 0u;
   const int lane = threadIdx.x & 31;
   const long long warp = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const long long nwarps = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
@@ -91,11 +93,13 @@ quantize_q8_kernel(const __grid_constant__ QuantGroup G) {
   cudaTriggerProgrammaticLaunchCompletion();
 }
 
-cudaError_t launch_quantize_q8(const QuantJob* jobs, int n, cudaStream_t s, bool pdl, unsigned int* zero_word) {
+cudaError_t launch_quantize_q8(const QuantJob* jobs, int n, cudaStream_t s, bool pdl, unsigned int* zero_words,
+                               int zero_count) {
   if (n <= 0 || n > kMaxProj) return cudaErrorInvalidValue;
   QuantGroup G;
   G.n = n;
-  G.zero_word = zero_word;
+  G.zero_words = zero_words;
+  G.zero_count = zero_words ? zero_count : 0;
   G.blk0[0] = 0;
   for (int k = 0; k < n; ++k) {
     G.job[k] = jobs[k];

@@ -116,10 +116,11 @@ struct QuantJob {
   int M, K;
 };
 
-// One launch quantizing up to kMaxProj activations; also stores 0 to
-// *zero_word when it is given (the next grouped matmul's task counter).
+// One launch quantizing up to kMaxProj activations; also zeroes the
+// zero_count words at zero_words when given (the next grouped matmul's task
+// counter and arrival counts).
 cudaError_t launch_quantize_q8(const QuantJob* jobs, int n, cudaStream_t s, bool pdl,
-                               unsigned int* zero_word = nullptr);
+                               unsigned int* zero_words = nullptr, int zero_count = 0);
 
 struct MmaProj {
   const uint8_t* W;    // Q4_K super-blocks [N][K/256]
@@ -129,11 +130,28 @@ struct MmaProj {
   int N, K, M_total, chunk;
 };
 
+// K-chunks a Q4_K projection's rows are split into when a split workspace
+// is available: rows of more than 24 super-blocks go in chunks of ~16.
+__host__ __device__ inline int q4k_split_chunks(int K, int M_total) {
+  const int nsb = K >> 8;
+  return (M_total <= 8 && nsb > 24) ? (nsb + 15) / 16 : 1;
+}
+// Workspace of a split projection: partial sums [nch][8][64 * row blocks]
+// and one arrival count per 64-row block (both rounded to 256 bytes).
+__host__ __device__ inline size_t q4k_split_partial_bytes(int N, int nch) {
+  return ((static_cast<size_t>(nch) * 8 * (((N + 63) / 64) * 64) * 4) + 255) & ~static_cast<size_t>(255);
+}
+__host__ __device__ inline size_t q4k_split_arrive_bytes(int N) {
+  return ((static_cast<size_t>((N + 63) / 64) * 4) + 255) & ~static_cast<size_t>(255);
+}
+
 // One launch for up to kMaxProj Q4_K projection chunks of <= 8 tokens. With
 // a counter (zeroed by the previous kernel on the stream) tasks are fetched
-// dynamically, most expensive first; without one they are strided.
+// dynamically, most expensive first; without one they are strided. With a
+// split workspace (arrival counts zeroed before the first use) long rows are
+// split into K-chunks across CTAs.
 cudaError_t launch_gemv_q4k_mma(const MmaProj* projs, int n, cudaStream_t s, bool pdl,
-                                unsigned int* counter = nullptr);
+                                unsigned int* counter = nullptr, uint8_t* split_ws = nullptr);
 cudaError_t launch_gemv_q4k(const GemvArgs& a, cudaStream_t s);
 cudaError_t launch_gemv_q6k(const GemvArgs& a, cudaStream_t s);
 

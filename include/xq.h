@@ -131,8 +131,10 @@ typedef struct {
 } xq_proj;
 
 /* Workspace bytes xq_layer_mixed needs: the Q8 buffers of every input that
- * some projection reads, each rounded up to 256 bytes, plus 256 bytes of
- * scheduling state. 0 on bad arguments. */
+ * some projection reads, each rounded up to 256 bytes, then scheduling
+ * state: 256 bytes, plus, for each Q4_K projection with more than 24
+ * super-blocks per row (split over K across CTAs when M <= 8), its arrival
+ * counts and partial sums. 0 on bad arguments. */
 XQ_API size_t xq_layer_workspace_bytes(const xq_proj *proj, int n_proj, int n_inputs, int M);
 
 /* One layer's projections with a quant type per tensor (xLLM v0.7 article,
