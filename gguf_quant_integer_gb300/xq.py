@@ -24,7 +24,7 @@ STATUS = {0: "XQ_OK", 1: "XQ_ERR_ARG", 2: "XQ_ERR_SHAPE", 3: "XQ_ERR_ALIGN",
 # Every symbol include/xq.h declares.
 SYMBOLS = ("xq_status_str", "xq_q8_bytes", "xq_weight_bytes", "xq_quantize_q8",
            "xq_matmul_q4k_q8", "xq_matmul_q6k_q8", "xq_layer_workspace_bytes",
-           "xq_layer_mixed", "xq_debug_isums_q4k", "xq_debug_isums_q6k")
+           "xq_layer_mixed", "xq_debug_isums_q4k", "xq_debug_isums_q6k", "xq_layer_mixed_static")
 
 
 class XQError(RuntimeError):
@@ -66,8 +66,9 @@ def lib(path: str | None = None):
     L.xq_layer_workspace_bytes.argtypes = [ctypes.POINTER(xq_proj), I, I, I]
     L.xq_layer_workspace_bytes.restype = S
     L.xq_layer_mixed.argtypes = [ctypes.POINTER(xq_proj), I, ctypes.POINTER(ctypes.c_void_p), I, I, P, S, P]
+    L.xq_layer_mixed_static.argtypes = [ctypes.POINTER(xq_proj), I, ctypes.POINTER(ctypes.c_void_p), I, I, P]
     for fn in ("xq_quantize_q8", "xq_matmul_q4k_q8", "xq_matmul_q6k_q8", "xq_debug_isums_q4k",
-               "xq_debug_isums_q6k", "xq_layer_mixed"):
+               "xq_debug_isums_q6k", "xq_layer_mixed", "xq_layer_mixed_static"):
         getattr(L, fn).restype = I
     if path is None:
         _lib = L
@@ -174,6 +175,14 @@ def layer_mixed(projs, inputs, M: int, workspace, stream=None):
     rc = lib().xq_layer_mixed(arr, len(projs), ins, len(inputs), M, _ptr(workspace),
                               workspace.numel() if workspace is not None else 0, _stream(stream))
     _check("xq_layer_mixed", rc)
+
+
+def layer_mixed_static(projs, inputs, M: int, stream=None):
+    """layer_mixed without a workspace: the library's fixed per-device array
+    (XQ_LAYER_STATIC_SCRATCH_BYTES) stands in for it; nothing is allocated."""
+    arr = _proj_array(projs)
+    ins = (ctypes.c_void_p * max(1, len(inputs)))(*[t.data_ptr() for t in inputs])
+    _check("xq_layer_mixed_static", lib().xq_layer_mixed_static(arr, len(projs), ins, len(inputs), M, _stream(stream)))
 
 
 class Layer:

@@ -151,6 +151,34 @@ XQ_API xq_status xq_layer_mixed(const xq_proj *proj, int n_proj,
                          const float *const *inputs, int n_inputs, int M,
                          void *workspace, size_t ws_bytes, xq_stream stream);
 
+/* Fixed workspace size of xq_layer_mixed_static: 4 MiB per device. */
+#define XQ_LAYER_STATIC_SCRATCH_BYTES (4u << 20)
+
+/* xq_layer_mixed for callers that cannot allocate device memory. (The pages
+ * have no counterpart: this is an interface convenience, not a step of the
+ * method.) Engines that give all device memory to their own pool at
+ * start-up, plugins whose host owns the allocator, and latency-critical
+ * decode loops that must not call cudaMalloc (it can synchronize the device
+ * and fail under memory pressure mid-request) have no way to provide the
+ * workspace xq_layer_mixed asks for. This entry point takes the same
+ * arguments minus the workspace and uses a fixed device array of
+ * XQ_LAYER_STATIC_SCRATCH_BYTES that the library holds on every GPU that
+ * loads it, until the process exits. It allocates nothing.
+ *  - Requests whose xq_layer_workspace_bytes() exceeds the fixed size return
+ *    XQ_ERR_WORKSPACE before anything is enqueued (one decode layer of an
+ *    8B-class model at M <= 8 needs about 1.3 MB).
+ *  - The first call on a device, with that device current, looks up the
+ *    array's device address (cudaGetSymbolAddress); make it before any
+ *    stream capture. A failed lookup returns XQ_ERR_CUDA.
+ *  - All calls on a device share the array; the state that must start at
+ *    zero is cleared by every call. Calls whose work overlaps on the GPU
+ *    (other streams, or unordered host threads) race on it: order them on
+ *    one stream or synchronize between them.
+ * Results equal xq_layer_mixed's with a caller-provided workspace. */
+XQ_API xq_status xq_layer_mixed_static(const xq_proj *proj, int n_proj,
+                                const float *const *inputs, int n_inputs, int M,
+                                xq_stream stream);
+
 /* Test hooks: the same matmul kernels with their exact int32 sub-block sums
  * written out instead of only consumed.
  *   Q4_K: isum int32 [M][N][K/32], sub-block j of super-block b at 8b+j.
