@@ -22,12 +22,16 @@ xq_status check_shape(int M, int N, int K) {
   return XQ_OK;
 }
 
-// Enqueue y = x W^T for any M: Q4_K on the tensor-core kernel (8-token
-// chunks, up to kMaxProj chunks per launch), Q6_K on the dp4a kernel.
+// Enqueue y = x W^T. M > 8: the tensor-memory tile kernel (both types).
+// M <= 8: Q4_K on the warp-level MMA GEMV, Q6_K on the dp4a GEMV.
 xq_status run_matmul(int type, const void* W, const void* xq, int M, int N, int K, float* y,
                      int32_t* isum, cudaStream_t s) {
   const xq::Q8Layout L = xq::q8_layout(M, K);
   const uint8_t* base = static_cast<const uint8_t*>(xq);
+  if (M > kMaxGemvM) {
+    const cudaError_t e = xq::launch_tile_mma(type, static_cast<const uint8_t*>(W), base, M, N, K, y, s, true);
+    return e == cudaSuccess ? XQ_OK : XQ_ERR_CUDA;
+  }
   if (type == XQ_TYPE_Q4_K) {
     xq::MmaProj items[xq::kMaxProj];
     int n = 0;
@@ -140,6 +144,7 @@ const char* xq_status_str(xq_status s) {
 
 size_t xq_q8_bytes(int M, int K) {
   if (M < 0 || K <= 0 || (K % 32) != 0) return 0;
+  if (M > kMaxGemvM && (K % 256) != 0) return 0;  // the tile image is per super-block
   return xq::q8_layout(M, K).total;
 }
 
@@ -256,6 +261,16 @@ xq_status xq_layer_mixed(const xq_proj* proj, int n_proj, const float* const* in
         n = 0;
       }
     }
+  }
+  if (M > kMaxGemvM) {
+    // every projection on the tile kernel, in the order given
+    for (int p = 0; p < n_proj; ++p) {
+      const xq_proj& q = proj[p];
+      if (q.N == 0) continue;
+      st = run_matmul(q.type, q.W, ws + off[q.input], M, q.N, q.K, q.y, nullptr, s);
+      if (st != XQ_OK) return st;
+    }
+    return XQ_OK;
   }
   // One launch for the Q4_K projections (8-token chunks, kMaxProj items per launch).
   {

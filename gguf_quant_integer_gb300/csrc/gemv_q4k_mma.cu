@@ -52,6 +52,7 @@
 #include <cuda.h>
 
 #include "xq_common.cuh"
+#include "xq_ptx.cuh"
 
 namespace xq {
 
@@ -88,47 +89,11 @@ constexpr long long kWaitClocks = 1LL << 32;
 __device__ __forceinline__ int mma_row(int i) { return 8 * (i >> 3) + 2 * (i & 3) + ((i >> 2) & 1); }
 
 // ---------------------------------------------------------------- PTX
-__device__ __forceinline__ void mbar_init(uint32_t a, unsigned n) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(a), "r"(n));
-}
-__device__ __forceinline__ void mbar_expect_tx(uint32_t a, unsigned bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(a), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint32_t a) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(a) : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint32_t a, unsigned parity) {
-  unsigned ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
-      : "=r"(ok)
-      : "r"(a), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
+using namespace ptx;
+
 // Bounded wait: false (and an error code recorded) if the phase never completes.
 __device__ __forceinline__ bool mbar_wait(uint32_t a, unsigned parity, unsigned code) {
-  if (mbar_try_wait(a, parity)) return true;
-  const long long t0 = clock64();
-  while (!mbar_try_wait(a, parity)) {
-    if (clock64() - t0 > kWaitClocks) {
-      atomicExch(&g_gemv_error, code);
-      return false;
-    }
-  }
-  return true;
-}
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t mbar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-      "l"(map), "r"(x), "r"(y), "r"(mbar)
-      : "memory");
-}
-
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, unsigned bytes, uint32_t mbar) {
-  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-               "l"(src), "r"(bytes), "r"(mbar)
-               : "memory");
+  return ptx::mbar_wait(a, parity, &g_gemv_error, code, kWaitClocks);
 }
 
 __device__ __forceinline__ void mma16816(float (&d)[4], unsigned a0, unsigned a1, unsigned a2,
@@ -139,26 +104,6 @@ __device__ __forceinline__ void mma16816(float (&d)[4], unsigned a0, unsigned a1
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
-
-// Packed fp32 pairs (.x in the low half).
-typedef unsigned long long f2;
-__device__ __forceinline__ f2 fma2(f2 a, f2 b, f2 c) {
-  f2 d;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-  return d;
-}
-__device__ __forceinline__ f2 mul2(f2 a, f2 b) {
-  f2 d;
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-  return d;
-}
-__device__ __forceinline__ f2 pk(float lo, float hi) {
-  f2 r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-  return r;
-}
-__device__ __forceinline__ float lo32(f2 v) { return __uint_as_float(static_cast<unsigned>(v)); }
-__device__ __forceinline__ float hi32(f2 v) { return __uint_as_float(static_cast<unsigned>(v >> 32)); }
 
 // Byte k of a packed word as 2^23 + byte, an exact fp32 (0x4B0000xx).
 __device__ __forceinline__ float byte_plus_2p23(unsigned w, int k) {
@@ -305,7 +250,7 @@ gemv_q4k_mma_kernel(const __grid_constant__ Group G) {
       mbar_init(full_s + 8 * s, 1);
       mbar_init(empty_s + 8 * s, 4);
     }
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    mbar_init_fence();
   }
   __syncthreads();
   // The activation image, the task counter and the arrival counts may be
@@ -438,11 +383,21 @@ int max_ctas() {
   return per_sm * kNumSMs;
 }
 
+// Q4_K rows as a 2D tensor of 8-byte elements: {row_bytes/8, N}, boxes of
+// one super-block x 16 rows.
+bool encode_weight_map(CUtensorMap* map, const uint8_t* W, int N, int K) {
+  const unsigned long long row_bytes = static_cast<unsigned long long>(K / 256) * kQ4kBytes;
+  return encode_tma_2d(map, CU_TENSOR_MAP_DATA_TYPE_UINT64, W, row_bytes / 8, static_cast<unsigned long long>(N),
+                       row_bytes, kQ4kBytes / 8, 16);
+}
+
+}  // namespace
+
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
-EncodeTiledFn encode_fn() {
+static EncodeTiledFn encode_fn() {
   static EncodeTiledFn fn = nullptr;
   static bool tried = false;
   if (!tried) {
@@ -456,21 +411,18 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// Q4_K rows as a 2D tensor of 8-byte elements: {row_bytes/8, N}.
-bool encode_weight_map(CUtensorMap* map, const uint8_t* W, int N, int K) {
+bool encode_tma_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, unsigned long long dim0,
+                   unsigned long long dim1, unsigned long long stride1, unsigned box0, unsigned box1) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
-  const cuuint64_t row_bytes = static_cast<cuuint64_t>(K / 256) * kQ4kBytes;
-  const cuuint64_t dims[2] = {row_bytes / 8, static_cast<cuuint64_t>(N)};
-  const cuuint64_t strides[1] = {row_bytes};
-  const cuuint32_t box[2] = {kQ4kBytes / 8, 16};
+  const cuuint64_t dims[2] = {dim0, dim1};
+  const cuuint64_t strides[1] = {stride1};
+  const cuuint32_t box[2] = {box0, box1};
   const cuuint32_t estr[2] = {1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT64, 2, const_cast<uint8_t*>(W), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return fn(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+         CUDA_SUCCESS;
 }
-
-}  // namespace
 
 cudaError_t launch_gemv_q4k_mma(const MmaProj* projs, int n, cudaStream_t s, bool pdl, unsigned int* counter,
                                 uint8_t* split_ws) {

@@ -14,13 +14,22 @@
 // a bit. The result is therefore the same on any IEEE implementation that
 // performs the same steps.
 //
-// The same pass writes the tensor-core operand image of the quants (fp16
-// copies in m16n8k16 B-fragment order, 8 token columns per chunk) and the
-// per-32-block scale quads the MMA epilogue reads, so that the matmuls never
-// convert activations themselves. One launch serves all inputs of a layer.
+// The same pass writes the tensor-core operand image of the quants, so that
+// the matmuls never convert activations themselves: for M <= 8 fp16 copies
+// in m16n8k16 B-fragment order plus per-32-block scale quads; for M > 8 the
+// 128-token tiles of the tcgen05 B operand, their d8 rows and the three-piece
+// bf16 split of s8 (layouts in xq_common.cuh). One launch serves all inputs
+// of a layer.
 #include "xq_common.cuh"
 
 namespace xq {
+
+// Byte offset of token r, k-slot ks in a 128-token x 32-slot operand in the
+// K-major no-swizzle layout (8x8 core matrices of 128 bytes: slot groups of
+// 8 strided by 128 bytes, token groups of 8 strided by 512 bytes).
+__device__ __forceinline__ int tile_offset(int r, int ks) {
+  return (r >> 3) * 512 + (ks >> 3) * 128 + (r & 7) * 16 + (ks & 7) * 2;
+}
 
 struct QuantGroup {
   QuantJob job[kMaxProj];
@@ -55,7 +64,6 @@ quantize_q8_kernel(const __grid_constant__ QuantGroup G) {
     const int m = static_cast<int>(local / nsub);
     const int j = static_cast<int>(local - static_cast<long long>(m) * nsub);
     const Q8Layout L = q8_layout(J.M, J.K);
-    const int c = m >> 3, n = m & 7;
 
     float d = 0.0f, s = 0.0f;
     int q = 0;
@@ -80,14 +88,38 @@ quantize_q8_kernel(const __grid_constant__ QuantGroup G) {
         reinterpret_cast<float*>(J.xq + L.s8)[static_cast<size_t>(m) * nsub + j] = s;
       }
     }
-    // operand image (zeros for padding tokens)
-    __half* frag = reinterpret_cast<__half*>(J.xq + L.frag);
-    frag[((static_cast<size_t>(c) * nsub + j) * 32 + 4 * n + t) * 8 + slot] = __int2half_rn(q);
-    if (lane == 0) {
-      float* fsc = reinterpret_cast<float*>(J.xq + L.fsc);
-      const size_t base = ((static_cast<size_t>(c) * nsub + j) * 4 + (n >> 1)) * 4;
-      fsc[base + (n & 1)] = d;
-      fsc[base + 2 + (n & 1)] = s;
+    if (L.ttiles == 0) {
+      // GEMV operand image (zeros for padding tokens)
+      const int c = m >> 3, n = m & 7;
+      __half* frag = reinterpret_cast<__half*>(J.xq + L.frag);
+      frag[((static_cast<size_t>(c) * nsub + j) * 32 + 4 * n + t) * 8 + slot] = __int2half_rn(q);
+      if (lane == 0) {
+        float* fsc = reinterpret_cast<float*>(J.xq + L.fsc);
+        const size_t base = ((static_cast<size_t>(c) * nsub + j) * 4 + (n >> 1)) * 4;
+        fsc[base + (n & 1)] = d;
+        fsc[base + 2 + (n & 1)] = s;
+      }
+    } else {
+      // tile image: token r of tile tt, 32-block j = 8b + ib
+      const int tt = m >> 7, r = m & 127, b = j >> 3, ib = j & 7;
+      uint8_t* rec = J.xq + L.tile + (static_cast<size_t>(tt) * (J.K >> 8) + b) * kTileRecord;
+      uint8_t* item = rec + ib * kTileItem;
+      const int ks = (lane & ~7) | slot;  // k-slot of this lane's feature
+      *reinterpret_cast<__half*>(item + tile_offset(r, ks)) = __int2half_rn(q);
+      if (lane == 0) reinterpret_cast<float*>(item + kTileItemOp)[r] = d;
+      uint8_t* beta = rec + 8 * kTileItem;
+      if (lane < 3) {
+        // s8 = p0 + p1 + p2, each piece a bf16 (upper 16 bits of an fp32)
+        const float p0 = __uint_as_float(__float_as_uint(s) & 0xFFFF0000u);
+        const float r1 = __fsub_rn(s, p0);
+        const float p1 = __uint_as_float(__float_as_uint(r1) & 0xFFFF0000u);
+        const float p2 = __fsub_rn(r1, p1);
+        const float pc = lane == 0 ? p0 : (lane == 1 ? p1 : p2);
+        *reinterpret_cast<uint16_t*>(beta + tile_offset(r, 3 * ib + lane)) =
+            static_cast<uint16_t>(__float_as_uint(pc) >> 16);
+      } else if (ib == 7 && lane < 11) {
+        *reinterpret_cast<uint16_t*>(beta + tile_offset(r, 21 + lane)) = 0;
+      }
     }
   }
   cudaTriggerProgrammaticLaunchCompletion();
@@ -103,7 +135,8 @@ cudaError_t launch_quantize_q8(const QuantJob* jobs, int n, cudaStream_t s, bool
   G.blk0[0] = 0;
   for (int k = 0; k < n; ++k) {
     G.job[k] = jobs[k];
-    const long long mp = 8LL * ((jobs[k].M + 7) / 8);
+    // padded token count: the operand image's chunk (8) or tile (128)
+    const long long mp = jobs[k].M > 8 ? 128LL * ((jobs[k].M + 127) / 128) : 8LL * ((jobs[k].M + 7) / 8);
     G.blk0[k + 1] = G.blk0[k] + mp * (jobs[k].K / 32);
   }
   const long long nblocks = G.blk0[n];

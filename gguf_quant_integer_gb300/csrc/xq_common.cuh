@@ -3,6 +3,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -69,17 +70,41 @@ __device__ __forceinline__ float half_bits_to_float(unsigned bits16) {
 //   qs   int8 [M][K]                      at 0
 //   d8   fp32 [M][K/32]                   at M*K
 //   s8   fp32 [M][K/32]                   at M*K + 4*M*K/32
-//   frag fp16 [C][K/32][32][8]            at F = round_up(1.25*M*K, 256)
+// followed, at F = round_up(1.25*M*K, 256), by the tensor-core operand image
+// of the matmul path that serves this M.
+//
+// M <= 8 (warp-level MMA GEMV):
+//   frag fp16 [C][K/32][32][8]            at F
 //   fsc  fp32 [C][K/32][4][4]             at F + C*16*K
-// with C = ceil(M/8) chunks of 8 tokens. frag and fsc hold the same numbers
-// as qs/d8/s8, laid out as the tensor-core operand of an m16n8k16 MMA with
-// 8 token columns: for chunk c, 32-block j, lane = 4n + t (token n, quad t),
-// slot s: frag = (half) qs[8c+n][32j + 8t + perm[s]], perm = 0,2,1,3,4,6,5,7;
-// fsc[c][j][t] = (d8[8c+2t][j], d8[8c+2t+1][j], s8[8c+2t][j], s8[8c+2t+1][j]).
-// Tokens past M in the last chunk are zero.
+// with C = ceil(M/8) chunks of 8 tokens, laid out as the B operand of an
+// m16n8k16 MMA with 8 token columns: for chunk c, 32-block j, lane = 4n + t
+// (token n, quad t), slot s: frag = (half) qs[8c+n][32j + 8t + perm[s]],
+// perm = 0,2,1,3,4,6,5,7; fsc[c][j][t] = (d8[8c+2t][j], d8[8c+2t+1][j],
+// s8[8c+2t][j], s8[8c+2t+1][j]). Tokens past M in the last chunk are zero.
+//
+// M > 8 (tensor-memory tile kernel), T = ceil(M/128) token tiles:
+//   tile [T][K/256] records of kTileRecord bytes at F. Record (t, b) holds,
+//   for the 128 tokens 128t .. 128t+127 and super-block b:
+//     8 items, one per 32-block j = 8b + i (kTileItem bytes each):
+//       op  fp16 [128 tokens][32 k-slots] in the K-major no-swizzle layout of
+//           the MMA B operand: token r, slot s at byte
+//           (r/8)*512 + (s/8)*128 + (r%8)*16 + (s%8)*2, holding
+//           qs[128t+r][32j + 4(s/4) + pr[s%4]], pr = 0,2,1,3;
+//       d8  fp32 [128] at byte kTileItemOp: d8[128t+r][j];
+//     then one bf16 operand (kTileItemOp bytes, same layout) whose slot
+//     3i + p (i < 8, p < 3) holds piece p of s8[128t+r][8b+i] split into
+//     three bf16 numbers by truncation (their sum is s8 exactly); slots
+//     24..31 are zero.
+//   Tokens past M are zero.
+constexpr int kTileTokens = 128;
+constexpr int kTileItemOp = 8192;                         // 128 tokens x 32 slots x 2 B
+constexpr int kTileItem = kTileItemOp + 4 * kTileTokens;  // 8704
+constexpr int kTileRecord = 8 * kTileItem + kTileItemOp;  // 77824
+
 struct Q8Layout {
-  size_t qs, d8, s8, frag, fsc, total;
-  int chunks;
+  size_t qs, d8, s8, frag, fsc, tile, total;
+  int chunks;  // 8-token chunks of the GEMV image (M <= 8), else 0
+  int ttiles;  // 128-token tiles of the tile image (M > 8), else 0
 };
 
 __host__ __device__ inline Q8Layout q8_layout(int M, int K) {
@@ -88,10 +113,19 @@ __host__ __device__ inline Q8Layout q8_layout(int M, int K) {
   L.qs = 0;
   L.d8 = mk;
   L.s8 = mk + 4 * (mk / 32);
-  L.chunks = (M + 7) / 8;
-  L.frag = (mk + 8 * (mk / 32) + 255) & ~static_cast<size_t>(255);
-  L.fsc = L.frag + static_cast<size_t>(L.chunks) * 16 * K;
-  L.total = L.fsc + static_cast<size_t>(L.chunks) * 2 * K;
+  const size_t F = (mk + 8 * (mk / 32) + 255) & ~static_cast<size_t>(255);
+  if (M <= 8) {
+    L.chunks = (M + 7) / 8;
+    L.ttiles = 0;
+    L.frag = F;
+    L.fsc = L.frag + static_cast<size_t>(L.chunks) * 16 * K;
+    L.tile = L.total = L.fsc + static_cast<size_t>(L.chunks) * 2 * K;
+  } else {
+    L.chunks = 0;
+    L.ttiles = (M + kTileTokens - 1) / kTileTokens;
+    L.frag = L.fsc = L.tile = F;
+    L.total = F + static_cast<size_t>(L.ttiles) * (K / 256) * kTileRecord;
+  }
   return L;
 }
 
@@ -153,6 +187,17 @@ __host__ __device__ inline size_t q4k_split_arrive_bytes(int N) {
 cudaError_t launch_gemv_q4k_mma(const MmaProj* projs, int n, cudaStream_t s, bool pdl,
                                 unsigned int* counter = nullptr, uint8_t* split_ws = nullptr);
 cudaError_t launch_gemv_q4k(const GemvArgs& a, cudaStream_t s);
+
+// 2D tensor map (no interleave, no swizzle, zero fill): dims {dim0, dim1}
+// elements of type dt, rows stride1 bytes apart, boxes box0 x box1. False
+// if the driver entry point is missing or rejects the arguments.
+bool encode_tma_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, unsigned long long dim0,
+                   unsigned long long dim1, unsigned long long stride1, unsigned box0, unsigned box1);
+
+// y = x W^T for M > 8 tokens on the tensor-memory tile kernel; type is 12
+// (Q4_K) or 14 (Q6_K), xq the Q8 buffer of M tokens (tile image present).
+cudaError_t launch_tile_mma(int type, const uint8_t* W, const uint8_t* xq, int M, int N, int K, float* y,
+                            cudaStream_t s, bool pdl);
 cudaError_t launch_gemv_q6k(const GemvArgs& a, cudaStream_t s);
 
 }  // namespace xq

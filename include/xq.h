@@ -31,19 +31,26 @@
  *  - x   : fp32 [M][K].
  *  - W   : GGUF super-blocks, row n is K/256 consecutive blocks;
  *          Q4_K 144 B per block, Q6_K 210 B per block (public GGUF layout).
- *  - xq  : one buffer of xq_q8_bytes(M, K) bytes holding five regions,
+ *  - xq  : one buffer of xq_q8_bytes(M, K) bytes holding
  *            qs   int8 [M][K]          at byte 0
  *            d8   fp32 [M][K/32]       at byte M*K
  *            s8   fp32 [M][K/32]       at byte M*K + 4*M*(K/32)
- *            frag fp16 [C][K/32][32][8] at F = round_up(1.25*M*K, 256)
- *            fsc  fp32 [C][K/32][4][4]  at F + 16*C*K
- *          with C = ceil(M/8). d8 = amax/127 of the 32-block,
+ *          and, at F = round_up(1.25*M*K, 256), the operand image of the
+ *          matmul that serves this M. d8 = amax/127 of the 32-block,
  *          q = round-half-away(x * (1/d8)) clamped to +-127, s8 = d8*sum(q)
- *          (q8_1 kind: scale and sum). frag and fsc repeat the same numbers
- *          in the operand order of the tensor-core matmul (8-token chunks:
+ *          (q8_1 kind: scale and sum).
+ *          M <= 8: frag fp16 [C][K/32][32][8] at F and fsc fp32 [C][K/32][4][4]
+ *          at F + 16*C*K, C = ceil(M/8): the same numbers in the operand
+ *          order of the warp-level tensor-core GEMV (8-token chunks:
  *          frag[c][j][4n+t][s] = qs[8c+n][32j+8t+p(s)], p = 0,2,1,3,4,6,5,7;
- *          fsc[c][j][t] = d8,d8,s8,s8 of tokens 8c+2t, 8c+2t+1); tokens
- *          past M are zero. xq_quantize_q8 writes all five.
+ *          fsc[c][j][t] = d8,d8,s8,s8 of tokens 8c+2t, 8c+2t+1).
+ *          M > 8: T = ceil(M/128) tiles of 128 tokens; for tile t and
+ *          super-block b a record of 77,824 bytes at F + (t*K/256 + b)*77824:
+ *          for each 32-block 8b+i an 8,704-byte item (fp16 q of the 128
+ *          tokens as a K-major tensor-core operand, 8x8 core matrices, then
+ *          their 128 d8 values), then an 8,192-byte bf16 operand holding s8
+ *          split into three bf16 pieces per 32-block.
+ *          Tokens past M are zero. xq_quantize_q8 writes every region.
  *  - y   : fp32 [M][N].
  */
 #ifndef XQ_H
@@ -84,8 +91,10 @@ typedef enum {
 XQ_API const char *xq_status_str(xq_status s);
 
 /* Bytes of the Q8 activation buffer for M tokens of K features:
- * round_up(1.25*M*K, 256) + 18*K*ceil(M/8). Returns 0 when K is not a
- * positive multiple of 32 or M < 0. */
+ * round_up(1.25*M*K, 256) + 18*K*ceil(M/8) for M <= 8,
+ * round_up(1.25*M*K, 256) + 77824*(K/256)*ceil(M/128) for M > 8.
+ * Returns 0 when M < 0, when K is not a positive multiple of 32, or when
+ * M > 8 and K is not a multiple of 256. */
 XQ_API size_t xq_q8_bytes(int M, int K);
 
 /* Bytes of an N x K weight of GGUF type `type` (N*(K/256)*144 for Q4_K,
@@ -109,7 +118,10 @@ XQ_API xq_status xq_quantize_q8(const float *x, int M, int K, void *xq, xq_strea
  *   W  : Q4_K bytes [N][K/256][144], device, read-only.
  *   xq : Q8 activations from xq_quantize_q8(.., M, K, ..), device, read-only.
  *   y  : fp32 [M][N], device, overwritten.
- * Any M >= 0. */
+ * Any M >= 0. Dispatch: M <= 8 runs a GEMV that streams every weight byte
+ * once for all M tokens; M > 8 runs the tile kernel (128 weight rows x 128
+ * tokens per CTA on the tcgen05 tensor cores, tile MMQ of section B2), whose
+ * operand image xq_quantize_q8 writes for that M. */
 XQ_API xq_status xq_matmul_q4k_q8(const void *W, const void *xq, int M, int N, int K,
                            float *y, xq_stream stream);
 

@@ -40,10 +40,15 @@ def test_sizes(L):
     from gguf_quant_integer_gb300 import xq
     def layout(M, K):
         base = -(-int(1.25 * M * K) // 256) * 256
-        return base + 18 * K * (-(-M // 8))
-    for M, K in ((1, 2048), (8, 4096), (9, 256), (512, 12288), (0, 256)):
+        if M <= 8:   # GEMV operand image: 18 bytes per feature per 8-token chunk
+            return base + 18 * K * (-(-M // 8))
+        # tile image: one 77,824-byte record per 128-token tile and super-block
+        return base + 77824 * (K // 256) * (-(-M // 128))
+    for M, K in ((1, 2048), (8, 4096), (9, 256), (129, 1536), (512, 12288), (0, 256)):
         assert xq.q8_bytes(M, K) == layout(M, K)
     assert L.xq_q8_bytes(1, 100) == 0
+    assert L.xq_q8_bytes(8, 288) > 0      # M <= 8 needs K % 32 only
+    assert L.xq_q8_bytes(9, 288) == 0     # the tile image is per 256-feature super-block
     assert xq.weight_bytes(12, 256, 2048) == 256 * 8 * 144
     assert xq.weight_bytes(14, 1024, 4096) == 1024 * 16 * 210
     assert xq.weight_bytes(99, 1, 256) == 0

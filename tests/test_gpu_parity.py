@@ -15,6 +15,7 @@ import torch
 
 import oracle
 from gguf_quant_integer_gb300 import synth
+from tile_image import expected_tile_image
 
 pytestmark = pytest.mark.gpu
 
@@ -105,7 +106,7 @@ def expected_operand_image(qs, d8, s8):
     return frag, fsc
 
 
-@pytest.mark.parametrize("M,K", [(1, 256), (3, 2048), (8, 4096), (13, 1536)])
+@pytest.mark.parametrize("M,K", [(1, 256), (3, 2048), (8, 4096)])
 def test_quantize_operand_image(xq, M, K):
     x = synth.gen_x(300 + M, M, K)
     buf, rq, rd = assert_q8_exact(xq, x)
@@ -118,6 +119,19 @@ def test_quantize_operand_image(xq, M, K):
     got_s = raw[F + 16 * C * K:F + 18 * C * K].view(np.float32).reshape(fsc.shape)
     assert np.array_equal(got_f.view(np.uint16), frag.view(np.uint16))
     assert np.array_equal(got_s.view(np.uint32), fsc.view(np.uint32))
+
+
+@pytest.mark.parametrize("M,K", [(9, 256), (13, 1536), (130, 512)])
+def test_quantize_tile_image(xq, M, K):
+    x = synth.gen_x(310 + M, M, K)
+    buf, rq, rd = assert_q8_exact(xq, x)
+    rs = oracle.quantize_q8(x)[2]
+    want = expected_tile_image(rq, rd, rs)
+    raw = buf.cpu().numpy()
+    F = -(-int(1.25 * M * K) // 256) * 256
+    got = raw[F:F + want.size].reshape(want.shape)
+    assert raw.size == F + want.size
+    assert np.array_equal(got, want)
 
 
 def test_quantize_edge_blocks(xq):
@@ -142,6 +156,13 @@ def test_quantize_edge_blocks(xq):
 def run_and_check(xq, qtype, N, K, M, wseed, xseed, want_isum=True):
     W = synth.gen_weight(qtype, wseed, N, K)
     x = synth.gen_x(xseed, M, K)
+    return check_matmul(xq, qtype, W, x, want_isum)
+
+
+def check_matmul(xq, qtype, W, x, want_isum=True):
+    """One xq_matmul (and, for M <= 8, the isum hook) against the oracle."""
+    M, K = x.shape
+    N = W.shape[0]
     buf, rq, rd = assert_q8_exact(xq, x)
     y_ref, ab, isum_ref = oracle.matmul(qtype, W, rq, rd, K, want_isum=want_isum and M <= 8)
     Wd = dev(W.reshape(-1))
@@ -185,6 +206,35 @@ def test_shapes_all_m(xq, qtype, N, K):
 @pytest.mark.parametrize("M", [9, 13, 64])
 def test_more_than_eight_tokens(xq, qtype, M):
     run_and_check(xq, qtype, 48, 1024, M, 900 + M, 901 + M, want_isum=False)
+
+
+# M > 8: the tcgen05 tile kernel. Ragged N and M, one-super-block rows, and
+# Q6_K rows whose byte length is not a multiple of 16 (row windows start at
+# varying offsets; for (37, 256) and (130, 1536) the last window is cut at
+# the end of the weight buffer).
+TILE_SHAPES = [(37, 256, 20), (130, 1536, 200), (300, 4096, 129), (128, 2304, 64), (48, 1024, 9)]
+
+
+@pytest.mark.parametrize("qtype", [synth.Q4_K, synth.Q6_K])
+@pytest.mark.parametrize("N,K,M", TILE_SHAPES)
+def test_tile_shapes(xq, qtype, N, K, M):
+    assert run_and_check(xq, qtype, N, K, M, 41 * N + K + qtype, 3 * M + K, want_isum=False) > 0.0
+
+
+@pytest.mark.parametrize("M", [4, 70])
+def test_q6k_full_range_scales(xq, M):
+    # GGUF Q6_K scales span int8; |s| > 64 takes the two-operand form in the
+    # tile kernel. Rows 0..63 keep |s| <= 64 so that a tile mixes both forms.
+    N, K = 160, 1024
+    W = synth.gen_q6k(77, N, K)
+    blocks = W.reshape(N, K // 256, 210)
+    rng = np.random.default_rng(78)
+    sc = rng.integers(-128, 128, size=(N, K // 256, 16)).astype(np.int8)
+    sc[:64] = np.clip(sc[:64], -64, 64)
+    sc[64, 0, :6] = (-128, 127, -127, 65, -65, 64)
+    blocks[:, :, 192:208] = sc.view(np.uint8)
+    x = synth.gen_x(79, M, K)
+    assert check_matmul(xq, synth.Q6_K, W, x) > 0.0
 
 
 def test_empty_products_leave_outputs_untouched(xq):
@@ -251,6 +301,11 @@ def test_qwen25_layer_full(xq, M):
 def test_qwen3_mixed_layer(xq, M):
     rows = None if M in (1, 8) else 512
     assert layer_check(xq, synth.WORKLOADS["qwen3-8b-mixed-layer"], M, rows=rows) > 0
+
+
+def test_qwen3_mixed_layer_tiles(xq):
+    # M > 8: every projection of the mixed layer (Q4_K and Q6_K) on the tile kernel
+    assert layer_check(xq, synth.WORKLOADS["qwen3-8b-mixed-layer"], 40, rows=96) > 0
 
 
 def test_llama3_32layer_sweep_sampled(xq):
