@@ -8,9 +8,13 @@
 //   Q4_K: y[m][n] = sum_b d[n,b] * sum_j d8[m][8b+j] * sc_j isum_j
 //                 - sum_b dmin[n,b] * sum_j mn_j * s8[m][8b+j]
 //   Q6_K: y[m][n] = sum_b d[n,b] * sum_p d8[m][8b+p] * sum_{k<32} s_g(k) (q_k - 32) q8_k
-// The tile is 128 weight rows (MMA M, the TMEM lanes) x 128 tokens (MMA N).
+// The tile is 128 tokens (MMA M, the TMEM lanes) x 128 weight rows (MMA N);
+// both operands are read from shared memory.
 //
-// A operand (weights), written into TMEM by the unpack warps (tcgen05.st):
+// A operand (tokens): the q8 values as fp16 integers, from the tile image
+// the quantizer writes (one bulk copy of 128 tokens x 32 features per item).
+// B operand (weights), unpacked by four warps (thread = weight row) into the
+// same K-major layout:
 //   Q4_K: sc_j * q * 2^-14 in fp16 (sc*q <= 945, exact): the nibble masked in
 //         place is the fp16 subnormal q * 2^-24 (16q * 2^-24 for a high
 //         nibble), and one fp16 multiply by sc * 2^10 (sc * 2^6) is exact.
@@ -19,29 +23,27 @@
 //         <= 4096, exact) and (s&1)*(q - 32), multiplied by the same token
 //         operand into the same accumulator; the second pair of MMAs is issued
 //         only when some row of the tile needs it.
-// B operand (tokens) in shared memory: the q8 values as fp16 integers, read
-// from the tile image the quantizer writes (one bulk copy per 32-block).
 // Exactness: every product is an integer (times 2^-14 for Q4_K) and every
 // partial sum of a 32-block accumulator stays below 2^24 in magnitude
 // (Q4_K: 945*127*32; Q6_K, worst split: 129*32*127*32 = 16,776,192), so
 // each accumulator is exact whatever the order of accumulation.
-// Q4_K min term: one bf16 MMA per super-block, A = mn_j (exact) against the
-// three-piece bf16 split of s8 (exact), i.e. exact products summed in fp32.
+// Q4_K min term: one bf16 MMA per super-block, the three-piece bf16 split of
+// s8 (exact) against mn_j (exact): exact products summed in fp32.
 //
-// Epilogue: per 32-block acc[m] += d8[m][j] * D[m] (one fp32 FMA per output);
-// per super-block run[m] += d' * acc[m] (- dmin * Dmin[m]), d' = d*2^14 for
-// Q4_K and d for Q6_K, with run kept
-// in TMEM and written to y after the last super-block.
+// Epilogue (thread = token, 64 weight rows): per 32-block acc[n] += d8 * D[n]
+// (one fp32 FMA per output, d8 a per-thread scalar); per super-block
+// run[n] += d'[n] * acc[n] (- dmin[n] * Dmin[n]), d' = d*2^14 for Q4_K and d
+// for Q6_K, with run kept in TMEM and written to y after the last
+// super-block. d' and -dmin reach the epilogue through a shared-memory ring.
 //
-// Warp roles (448 threads): warps 0-3 unpack (thread = weight row = TMEM
-// lane), warps 4-11 epilogue (warp w reads lane quarter w%4, token half
-// (w-4)/4), warp 12 producer (raw weights by TMA or row copies, token items
-// by bulk copy), warp 13 MMA issuer and TMEM owner. TMEM columns: [0,128)
-// running sums, [128,384) two accumulators, [384,512) four A buffers of 32
-// columns (16 for a 32-block of fp16 pairs, 16 more for the Q6_K second
-// operand). Every mbarrier wait is bounded (about 2^32 clocks); on expiry
-// the kernel records an error code, leaves its loops, waits for its own
-// tensor-core work and frees TMEM.
+// Warp roles (512 threads): warps 0-3 unpack, warps 4-11 epilogue (warp w
+// reads TMEM lane quarter w%4, weight-row half (w-4)/4), warp 12 producer
+// (raw weights by TMA or row copies, token items by bulk copy), warps 13-15
+// MMA issuers, one per accumulator (warp 13 also owns TMEM). TMEM columns: [0,128) running sums, then three
+// 128-column accumulators, so the tensor core runs up to three 32-blocks
+// ahead of the epilogue. Every mbarrier wait is bounded (about 2^32 clocks);
+// on expiry the kernel records an error code, leaves its loops, waits for
+// its own tensor-core work and frees TMEM.
 #include <cuda.h>
 
 #include "xq_common.cuh"
@@ -55,46 +57,57 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kRows = 128;        // weight rows per tile
-constexpr int kNumA = 4;          // A buffers in TMEM
-constexpr int kTokStages = 8;     // token item ring
-constexpr int kRawStages = 3;     // raw weight ring (one super-block of 128 rows per stage)
-constexpr uint32_t kColRun = 0, kColD = 128, kColA = 384;
-constexpr int kThreads = 448;
-constexpr int kWarpEpi0 = 4, kWarpProd = 12, kWarpMma = 13;
+constexpr int kRows = 128;      // weight rows per tile (MMA N)
+constexpr int kTokStages = 8;   // token item ring
+constexpr int kWStages = 4;     // unpacked weight operand ring
+constexpr int kNumD = 3;        // accumulators in TMEM
+constexpr int kCoefStages = 4;  // per-super-block row coefficients
+constexpr uint32_t kColRun = 0, kColD = 128;
+constexpr int kThreads = 512;
+constexpr int kWarpEpi0 = 4, kWarpProd = 12, kWarpMma = 13;  // MMA warps 13..15
 constexpr long long kWaitClocks = 1LL << 32;
-constexpr int kQ6Window = 224;    // bytes copied per Q6_K row and super-block
-constexpr int kQ6Pitch = 240;     // their pitch in shared memory (conflict-free 16-byte reads)
+constexpr int kQ6Window = 224;  // bytes copied per Q6_K row and super-block
+constexpr int kQ6Pitch = 240;   // their pitch in shared memory (conflict-free 16-byte reads)
+constexpr int kOpBytes = kRows * 32 * 2;  // one 128-row x 32-slot fp16 operand
 
 template <int TYPE>
 struct Fmt;
 template <>
 struct Fmt<12> {
-  static constexpr int kRawRow = kQ4kBytes, kItems = 9;  // 8 sub-blocks + the min-term item
+  static constexpr int kRawRow = kQ4kBytes, kRawStages = 3;
+  static constexpr int kItems = 9;             // 8 sub-blocks + the min-term item
+  static constexpr int kWBytes = kOpBytes;     // one operand per item
 };
 template <>
 struct Fmt<14> {
-  static constexpr int kRawRow = kQ6Pitch, kItems = 8;
+  static constexpr int kRawRow = kQ6Pitch, kRawStages = 2;
+  static constexpr int kItems = 8;
+  static constexpr int kWBytes = 2 * kOpBytes;  // high and low operands
 };
 
-constexpr int kBarRawFull = 0;
-constexpr int kBarRawEmpty = kBarRawFull + kRawStages;
-constexpr int kBarTokFull = kBarRawEmpty + kRawStages;
-constexpr int kBarTokEmpty = kBarTokFull + kTokStages;
-constexpr int kBarAFull = kBarTokEmpty + kTokStages;
-constexpr int kBarAEmpty = kBarAFull + kNumA;
-constexpr int kBarDFull = kBarAEmpty + kNumA;
-constexpr int kBarDEmpty = kBarDFull + 2;
-constexpr int kBarDone = kBarDEmpty + 2;
-constexpr int kNumBars = kBarDone + 1;
+template <int TYPE>
+struct Smem {
+  static constexpr int kRaw = Fmt<TYPE>::kRawStages * kRows * Fmt<TYPE>::kRawRow;
+  static constexpr int kTok = kTokStages * kTileItem;
+  static constexpr int kW = kWStages * Fmt<TYPE>::kWBytes;
+  static constexpr int kCoef = kCoefStages * kRows * 8;
+  static constexpr int kRawOff = 0, kTokOff = kRaw, kWOff = kTokOff + kTok, kCoefOff = kWOff + kW;
+  static constexpr int kBarOff = kCoefOff + kCoef;
+};
+
+// barrier indices (raw ring first; its size depends on the type)
+template <int TYPE>
+struct Bars {
+  static constexpr int RS = Fmt<TYPE>::kRawStages;
+  static constexpr int kRawFull = 0, kRawEmpty = RS, kTokFull = 2 * RS, kTokEmpty = kTokFull + kTokStages,
+                       kWFull = kTokEmpty + kTokStages, kWEmpty = kWFull + kWStages, kDFull = kWEmpty + kWStages,
+                       kDEmpty = kDFull + kNumD, kCoefFull = kDEmpty + kNumD, kCoefEmpty = kCoefFull + kCoefStages,
+                       kVote = kCoefEmpty + kCoefStages, kDone = kVote + 2, kCount = kDone + kNumD;
+};
 
 template <int TYPE>
-constexpr int raw_stage_bytes() {
-  return kRows * Fmt<TYPE>::kRawRow;
-}
-template <int TYPE>
 constexpr int smem_bytes() {
-  return kRawStages * raw_stage_bytes<TYPE>() + kTokStages * kTileItem + kNumBars * 8 + 16 + kNumA * 4 * 4;
+  return Smem<TYPE>::kBarOff + Bars<TYPE>::kCount * 8 + 16 + (kWStages + 8) * 4;
 }
 
 struct TileArgs {
@@ -106,7 +119,12 @@ struct TileArgs {
   int N, K, M, nsb, row_bytes, ttiles;
 };
 
+// Waits of the producer, unpack and epilogue warps suspend between polls;
+// the MMA issuer, on the critical path, polls without suspending.
 __device__ __forceinline__ bool wait_bar(uint32_t bar, unsigned parity, unsigned code) {
+  return mbar_wait_sleep(bar, parity, &g_tile_error, code, kWaitClocks);
+}
+__device__ __forceinline__ bool wait_bar_spin(uint32_t bar, unsigned parity, unsigned code) {
   return mbar_wait(bar, parity, &g_tile_error, code, kWaitClocks);
 }
 // Every lane waits; the warp goes on only if all of them saw the phase.
@@ -124,7 +142,7 @@ __device__ __forceinline__ unsigned q6_window(const TileArgs& A, int n, int b) {
   return src + kQ6Window <= A.w_bytes ? kQ6Window : static_cast<unsigned>((A.w_bytes - src) & ~15ull);
 }
 
-// nw 32-bit words starting at a 2-byte aligned shared-memory address.
+// NW 32-bit words starting at a 2-byte aligned shared-memory address.
 template <int NW>
 __device__ __forceinline__ void load_words(const uint8_t* p, uint32_t (&out)[NW]) {
   const uintptr_t a = reinterpret_cast<uintptr_t>(p);
@@ -144,24 +162,33 @@ __device__ __forceinline__ uint32_t half2_of(float v) {
   return h | (h << 16);
 }
 
-template <int TYPE>
-__device__ __forceinline__ unsigned load_coef(const TileArgs& A, int n, int b) {
-  const uint8_t* p = A.W + static_cast<size_t>(n) * A.row_bytes;
-  if (TYPE == 12) return __ldg(reinterpret_cast<const unsigned*>(p + static_cast<size_t>(b) * kQ4kBytes));
-  return __ldg(reinterpret_cast<const unsigned short*>(p + static_cast<size_t>(b) * kQ6kBytes + 208));
+// Store one row's 32 k-slots (16 words: word c holds slots 2c, 2c+1) into a
+// 128-row K-major operand: slot group q (8 slots, 16 bytes) of row r at
+// (r/8)*512 + q*128 + (r%8)*16.
+__device__ __forceinline__ void store_row(uint8_t* op, int r, const uint32_t (&v)[16]) {
+  uint8_t* p = op + (r >> 3) * 512 + (r & 7) * 16;
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+    *reinterpret_cast<uint4*>(p + q * 128) = make_uint4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
 }
 
 template <int TYPE>
 __global__ void __launch_bounds__(kThreads, 1) tile_mma_kernel(const __grid_constant__ TileArgs A) {
   using F = Fmt<TYPE>;
-  constexpr int kRawBytes = raw_stage_bytes<TYPE>();
+  using S = Smem<TYPE>;
+  using B = Bars<TYPE>;
+  constexpr int kRawBytes = kRows * F::kRawRow;
   constexpr int kItems = F::kItems;
+  constexpr int RS = F::kRawStages;
   extern __shared__ __align__(1024) uint8_t smem[];
-  uint8_t* raw_ring = smem;
-  uint8_t* tok_ring = smem + kRawStages * kRawBytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(tok_ring + kTokStages * kTileItem);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kNumBars);
-  int* split_flag = reinterpret_cast<int*>(tmem_slot + 4);  // [kNumA][4 unpack warps]
+  uint8_t* raw_ring = smem + S::kRawOff;
+  uint8_t* tok_ring = smem + S::kTokOff;
+  uint8_t* w_ring = smem + S::kWOff;
+  float2* coef_ring = reinterpret_cast<float2*>(smem + S::kCoefOff);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::kBarOff);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + B::kCount);
+  int* split_flag = reinterpret_cast<int*>(tmem_slot + 4);  // [kWStages]: tile uses the two-operand form
+  int* split_vote = split_flag + kWStages;                  // [2][4 unpack warps]
   const uint32_t bar0 = smem_addr(bars);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tt = blockIdx.x % A.ttiles, wt = blockIdx.x / A.ttiles;
@@ -169,23 +196,28 @@ __global__ void __launch_bounds__(kThreads, 1) tile_mma_kernel(const __grid_cons
 #define BAR(i) (bar0 + 8u * static_cast<uint32_t>(i))
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kRawStages; ++s) {
-      mbar_init(BAR(kBarRawFull + s), 1);
-      mbar_init(BAR(kBarRawEmpty + s), 4);
+    for (int s = 0; s < RS; ++s) {
+      mbar_init(BAR(B::kRawFull + s), 1);
+      mbar_init(BAR(B::kRawEmpty + s), 4);
     }
     for (int s = 0; s < kTokStages; ++s) {
-      mbar_init(BAR(kBarTokFull + s), 1);
-      mbar_init(BAR(kBarTokEmpty + s), 8);
+      mbar_init(BAR(B::kTokFull + s), 1);
+      mbar_init(BAR(B::kTokEmpty + s), 8);
     }
-    for (int s = 0; s < kNumA; ++s) {
-      mbar_init(BAR(kBarAFull + s), 4);
-      mbar_init(BAR(kBarAEmpty + s), 1);
+    for (int s = 0; s < kWStages; ++s) {
+      mbar_init(BAR(B::kWFull + s), 4);
+      mbar_init(BAR(B::kWEmpty + s), 1);
     }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(BAR(kBarDFull + s), 1);
-      mbar_init(BAR(kBarDEmpty + s), 8);
+    for (int s = 0; s < kNumD; ++s) {
+      mbar_init(BAR(B::kDFull + s), 1);
+      mbar_init(BAR(B::kDEmpty + s), 8);
     }
-    mbar_init(BAR(kBarDone), 1);
+    for (int s = 0; s < kCoefStages; ++s) {
+      mbar_init(BAR(B::kCoefFull + s), 4);
+      mbar_init(BAR(B::kCoefEmpty + s), 8);
+    }
+    for (int s = 0; s < 2; ++s) mbar_init(BAR(B::kVote + s), 4);
+    for (int s = 0; s < kNumD; ++s) mbar_init(BAR(B::kDone + s), 1);
     mbar_init_fence();
   }
   if (warp == kWarpMma) tmem_alloc(smem_addr(tmem_slot), 512);
@@ -205,36 +237,36 @@ __global__ void __launch_bounds__(kThreads, 1) tile_mma_kernel(const __grid_cons
     unsigned tf = 0;  // token items issued
     bool ok = true;
     for (int b = 0; b < A.nsb && ok; ++b) {
-      const int rs = b % kRawStages;
-      if (b >= kRawStages && !warp_wait(BAR(kBarRawEmpty + rs), ((b / kRawStages) - 1) & 1, 1)) break;
+      const int rs = b % RS;
+      if (b >= RS && !warp_wait(BAR(B::kRawEmpty + rs), ((b / RS) - 1) & 1, 1)) break;
       const uint32_t dst = smem_addr(raw_ring + rs * kRawBytes);
       if (TYPE == 12) {
         if (lane == 0) {
-          mbar_expect_tx(BAR(kBarRawFull + rs), kRawBytes);  // rows past N arrive zero-filled
-          tma_load_2d(dst, &A.map, b * (kQ4kBytes / 8), row0, BAR(kBarRawFull + rs));
+          mbar_expect_tx(BAR(B::kRawFull + rs), kRawBytes);  // rows past N arrive zero-filled
+          tma_load_2d(dst, &A.map, b * (kQ4kBytes / 8), row0, BAR(B::kRawFull + rs));
         }
       } else {
         unsigned mine = 0;
         for (int r = lane; r < rows; r += 32) mine += q6_window(A, row0 + r, b);
         const unsigned total = __reduce_add_sync(0xffffffffu, mine);
-        if (lane == 0) mbar_expect_tx(BAR(kBarRawFull + rs), total);
+        if (lane == 0) mbar_expect_tx(BAR(B::kRawFull + rs), total);
         __syncwarp();
         for (int r = lane; r < rows; r += 32) {
           const unsigned long long start = static_cast<unsigned long long>(row0 + r) * A.row_bytes + 210ull * b;
-          bulk_load(dst + r * kQ6Pitch, A.W + (start & ~15ull), q6_window(A, row0 + r, b), BAR(kBarRawFull + rs));
+          bulk_load(dst + r * kQ6Pitch, A.W + (start & ~15ull), q6_window(A, row0 + r, b), BAR(B::kRawFull + rs));
         }
       }
       for (int it = 0; it < kItems; ++it, ++tf) {
         const int ts = tf % kTokStages;
-        if (tf >= kTokStages && !warp_wait(BAR(kBarTokEmpty + ts), ((tf / kTokStages) - 1) & 1, 2)) {
+        if (tf >= kTokStages && !warp_wait(BAR(B::kTokEmpty + ts), ((tf / kTokStages) - 1) & 1, 2)) {
           ok = false;
           break;
         }
         if (lane == 0) {
           const unsigned bytes = it < 8 ? kTileItem : kTileItemOp;
-          mbar_expect_tx(BAR(kBarTokFull + ts), bytes);
+          mbar_expect_tx(BAR(B::kTokFull + ts), bytes);
           bulk_load(smem_addr(tok_ring + ts * kTileItem), rec + static_cast<size_t>(b) * kTileRecord + it * kTileItem,
-                    bytes, BAR(kBarTokFull + ts));
+                    bytes, BAR(B::kTokFull + ts));
         }
       }
     }
@@ -242,23 +274,22 @@ __global__ void __launch_bounds__(kThreads, 1) tile_mma_kernel(const __grid_cons
     // fill of every stage (already complete on the normal path).
     if (lane == 0) {
       const int nb = A.nsb;
-      for (int b = nb > kRawStages ? nb - kRawStages : 0; b < nb; ++b)
-        wait_bar(BAR(kBarRawFull + b % kRawStages), (b / kRawStages) & 1, 11);
+      for (int b = nb > RS ? nb - RS : 0; b < nb; ++b) wait_bar(BAR(B::kRawFull + b % RS), (b / RS) & 1, 11);
       for (unsigned f = tf > kTokStages ? tf - kTokStages : 0; f < tf; ++f)
-        wait_bar(BAR(kBarTokFull + f % kTokStages), (f / kTokStages) & 1, 12);
+        wait_bar(BAR(B::kTokFull + f % kTokStages), (f / kTokStages) & 1, 12);
     }
     __syncwarp();
   } else if (warp < 4) {
     // ---------------------------------------------------------- unpack
-    const int r = threadIdx.x;  // tile row = TMEM lane
+    const int r = threadIdx.x;  // tile row
     const int n = wt * kRows + r;
     const bool row_ok = n < A.N;
-    const uint32_t tl = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-    unsigned af = 0;  // A buffers filled
+    unsigned wf = 0;  // weight operands filled
     bool ok = true;
     for (int b = 0; b < A.nsb && ok; ++b) {
-      const int rs = b % kRawStages;
-      if (!warp_wait(BAR(kBarRawFull + rs), (b / kRawStages) & 1, 3)) break;
+      const int rs = b % RS, cs = b % kCoefStages;
+      if (!warp_wait(BAR(B::kRawFull + rs), (b / RS) & 1, 3)) break;
+      if (b >= kCoefStages && !warp_wait(BAR(B::kCoefEmpty + cs), ((b / kCoefStages) - 1) & 1, 4)) break;
       const uint8_t* raw = raw_ring + rs * kRawBytes + r * F::kRawRow;
       if (TYPE == 12) {
         // Scales and mins (public Q4_K packing): j < 4: sc = s[j] & 63,
@@ -268,29 +299,32 @@ __global__ void __launch_bounds__(kThreads, 1) tile_mma_kernel(const __grid_cons
         const uint32_t sc_lo = h.y & 0x3F3F3F3Fu, mn_lo = h.z & 0x3F3F3F3Fu;
         const uint32_t sc_hi = (h.w & 0x0F0F0F0Fu) | ((h.y >> 2) & 0x30303030u);
         const uint32_t mn_hi = ((h.w >> 4) & 0x0F0F0F0Fu) | ((h.z >> 2) & 0x30303030u);
+        coef_ring[cs * kRows + r] =
+            make_float2(half_bits_to_float(h.x) * 16384.0f, -half_bits_to_float(h.x >> 16));
+        __syncwarp();
+        if (lane == 0) mbar_arrive(BAR(B::kCoefFull + cs));
 #pragma unroll
-        for (int it = 0; it < 9; ++it, ++af) {
-          const int a = af % kNumA;
-          if (af >= kNumA && !warp_wait(BAR(kBarAEmpty + a), ((af / kNumA) - 1) & 1, 4)) {
+        for (int it = 0; it < 9; ++it, ++wf) {
+          const int ws = wf % kWStages;
+          if (wf >= kWStages && !warp_wait(BAR(B::kWEmpty + ws), ((wf / kWStages) - 1) & 1, 5)) {
             ok = false;
             break;
           }
-          tc_fence_after();
           uint32_t v[16];
           if (it < 8) {
             const int g = it >> 1;
             const bool hi = (it & 1) != 0;
             const uint32_t sc = ((it < 4 ? sc_lo : sc_hi) >> (8 * (it & 3))) & 0xFFu;
-            const uint32_t S = half2_of(static_cast<float>(sc) * (hi ? 64.0f : 1024.0f));
+            const uint32_t S2 = half2_of(static_cast<float>(sc) * (hi ? 64.0f : 1024.0f));
             const uint4* qp = reinterpret_cast<const uint4*>(raw + 16 + 32 * g);
             const uint4 q0 = qp[0], q1 = qp[1];
             const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
             const uint32_t mk = hi ? 0x00F000F0u : 0x000F000Fu;
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-              // columns 2i, 2i+1 = k-slots 4i..4i+3 = weights 4i, 4i+2, 4i+1, 4i+3
-              v[2 * i] = hmul2(w[i] & mk, S);
-              v[2 * i + 1] = hmul2((w[i] >> 8) & mk, S);
+              // words 2i, 2i+1 = k-slots 4i..4i+3 = weights 4i, 4i+2, 4i+1, 4i+3
+              v[2 * i] = hmul2(w[i] & mk, S2);
+              v[2 * i + 1] = hmul2((w[i] >> 8) & mk, S2);
             }
           } else {
             // min-term operand: slot k < 24 holds mn_{k/3} as bf16, the rest 0
@@ -309,11 +343,10 @@ __global__ void __launch_bounds__(kThreads, 1) tile_mma_kernel(const __grid_cons
               v[c] = pair;
             }
           }
-          tmem_st16(tl + kColA + 32 * a, v);
-          tmem_wait_st();
-          tc_fence_before();
+          store_row(w_ring + ws * F::kWBytes, r, v);
+          fence_proxy_async_smem();
           __syncwarp();
-          if (lane == 0) mbar_arrive(BAR(kBarAFull + a));
+          if (lane == 0) mbar_arrive(BAR(B::kWFull + ws));
         }
       } else {
         // Q6_K: ql[128] at 0, qh[64] at 128, scales int8[16] at 192, d at
@@ -321,37 +354,53 @@ __global__ void __launch_bounds__(kThreads, 1) tile_mma_kernel(const __grid_cons
         // super-block.
         const unsigned long long start = static_cast<unsigned long long>(n) * A.row_bytes + 210ull * b;
         const uint8_t* sb = raw + (start & 15);
+        const bool cut = (start & ~15ull) + kQ6Window > A.w_bytes;  // scales and d not all in the window
         uint32_t sw[4] = {0u, 0u, 0u, 0u};
+        float d = 0.0f;
         if (row_ok) {
-          if ((start & ~15ull) + kQ6Window <= A.w_bytes) {
+          if (!cut) {
             load_words<4>(sb + 192, sw);
+            d = half_bits_to_float(*reinterpret_cast<const unsigned short*>(sb + 208));
           } else {
-            // the window was cut at the end of the buffer: scales from memory
             const unsigned short* gs = reinterpret_cast<const unsigned short*>(A.W + start + 192);
 #pragma unroll
             for (int k = 0; k < 4; ++k)
               sw[k] = static_cast<uint32_t>(__ldg(gs + 2 * k)) | (static_cast<uint32_t>(__ldg(gs + 2 * k + 1)) << 16);
+            d = half_bits_to_float(__ldg(gs + 8));
           }
         }
-        // |s| > 64 anywhere in the row needs the two-operand form
+        coef_ring[cs * kRows + r] = make_float2(d, 0.0f);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(BAR(B::kCoefFull + cs));
+        // |s| > 64 in any row of the tile needs the two-operand form for the
+        // whole tile (the low operand is read for all 128 rows): the four
+        // unpack warps vote, double-buffered by super-block parity, through
+        // an mbarrier per buffer (a warp reuses a buffer only after every
+        // warp has passed the next super-block's vote, hence read this one).
         bool big = false;
 #pragma unroll
         for (int k = 0; k < 4; ++k) big = big || (__vcmpgtu4(__vabsss4(sw[k]), 0x40404040u) != 0u);
-        const bool split = __any_sync(0xffffffffu, big);
+        const bool any = __any_sync(0xffffffffu, big);
+        int* vote = split_vote + 4 * (b & 1);
+        if (lane == 0) {
+          vote[warp] = any ? 1 : 0;
+          mbar_arrive(BAR(B::kVote + (b & 1)));
+        }
+        if (!warp_wait(BAR(B::kVote + (b & 1)), (b >> 1) & 1, 15)) break;
+        const bool split = (vote[0] | vote[1] | vote[2] | vote[3]) != 0;
         uint32_t ql[16], qh[8];
 #pragma unroll
-        for (int it = 0; it < 8; ++it, ++af) {
+        for (int it = 0; it < 8; ++it, ++wf) {
           const int hh = it >> 2, rr = it & 3;
           if (rr == 0 && row_ok) {
             load_words<16>(sb + 64 * hh, ql);
             load_words<8>(sb + 128 + 32 * hh, qh);
           }
-          const int a = af % kNumA;
-          if (af >= kNumA && !warp_wait(BAR(kBarAEmpty + a), ((af / kNumA) - 1) & 1, 4)) {
+          const int ws = wf % kWStages;
+          if (wf >= kWStages && !warp_wait(BAR(B::kWEmpty + ws), ((wf / kWStages) - 1) & 1, 5)) {
             ok = false;
             break;
           }
-          tc_fence_after();
           // scales of the two 16-groups of this 32-block
           uint32_t Shi[2], Slo[2];
 #pragma unroll
@@ -377,101 +426,118 @@ __global__ void __launch_bounds__(kThreads, 1) tile_mma_kernel(const __grid_cons
             u[2 * i] = row_ok ? hmul2(x0, Slo[e]) : 0u;
             u[2 * i + 1] = row_ok ? hmul2(x1, Slo[e]) : 0u;
           }
-          tmem_st16(tl + kColA + 32 * a, v);
-          if (split) tmem_st16(tl + kColA + 32 * a + 16, u);
-          tmem_wait_st();
-          tc_fence_before();
+          uint8_t* op = w_ring + ws * F::kWBytes;
+          store_row(op, r, v);
+          if (split) store_row(op + kOpBytes, r, u);
+          fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
-            split_flag[4 * a + warp] = split ? 1 : 0;
-            mbar_arrive(BAR(kBarAFull + a));
+            if (warp == 0) split_flag[ws] = split ? 1 : 0;
+            mbar_arrive(BAR(B::kWFull + ws));
           }
         }
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(BAR(kBarRawEmpty + rs));
+      if (lane == 0) mbar_arrive(BAR(B::kRawEmpty + rs));
     }
-  } else if (warp == kWarpMma) {
+  } else if (warp >= kWarpMma) {
     // ------------------------------------------------------------- MMA
-    if (lane == 0) {
-      constexpr uint32_t kIdH = idesc_f16(kRows, kTileTokens, false);
-      constexpr uint32_t kIdB = idesc_f16(kRows, kTileTokens, true);
-      for (int f = 0; f < nitems; ++f) {
-        const int it = f % kItems, ts = f % kTokStages, a = f % kNumA, d = f & 1;
-        if (!wait_bar(BAR(kBarTokFull + ts), (f / kTokStages) & 1, 5)) break;
-        if (!wait_bar(BAR(kBarAFull + a), (f / kNumA) & 1, 6)) break;
-        if (f >= 2 && !wait_bar(BAR(kBarDEmpty + d), ((f >> 1) - 1) & 1, 7)) break;
+    // Three issuing threads, one per accumulator: thread k issues the items
+    // f = k, k+3, k+6, ... into accumulator k. Each thread's chain of waits,
+    // MMAs and commits is serial; three of them keep the tensor core fed.
+    const int k = warp - kWarpMma;
+    if (lane == 0 && k < nitems) {
+      constexpr uint32_t kIdH = idesc_f16(kTileTokens, kRows, false);
+      constexpr uint32_t kIdB = idesc_f16(kTileTokens, kRows, true);
+      const uint32_t dt = tmem + kColD + 128u * k;
+      const uint32_t tok0 = smem_addr(tok_ring), w0 = smem_addr(w_ring);
+      // ring positions of item f, advanced by kNumD per step
+      int it = k, ts = k, ws = k;
+      unsigned tpar = 0, wpar = 0;
+      for (int f = k, step = 0; f < nitems; f += kNumD, ++step) {
+        if (!wait_bar_spin(BAR(B::kTokFull + ts), tpar, 6)) break;
+        if (!wait_bar_spin(BAR(B::kWFull + ws), wpar, 7)) break;
+        if (step > 0 && !wait_bar_spin(BAR(B::kDEmpty + k), (step - 1) & 1, 8)) break;
         tc_fence_after();
-        const uint32_t dt = tmem + kColD + 128u * d, at = tmem + kColA + 32u * a;
-        const uint32_t bs = smem_addr(tok_ring + ts * kTileItem);
-        const uint64_t b0 = smem_desc(bs, 128, 512), b1 = smem_desc(bs + 256, 128, 512);
+        const uint32_t as = tok0 + ts * kTileItem, bs = w0 + ws * F::kWBytes;
+        const uint64_t a0 = smem_desc(as, 128, 512), a1 = smem_desc(as + 256, 128, 512);
         const uint32_t id = (TYPE == 12 && it == 8) ? kIdB : kIdH;
-        mma_f16_ts(dt, at, b0, id, false);
-        mma_f16_ts(dt, at + 8, b1, id, true);
-        if (TYPE == 14) {
-          const int* fl = split_flag + 4 * a;
-          if (fl[0] | fl[1] | fl[2] | fl[3]) {
-            mma_f16_ts(dt, at + 16, b0, id, true);
-            mma_f16_ts(dt, at + 24, b1, id, true);
-          }
+        mma_f16_ss(dt, a0, smem_desc(bs, 128, 512), id, false);
+        mma_f16_ss(dt, a1, smem_desc(bs + 256, 128, 512), id, true);
+        if (TYPE == 14 && split_flag[ws]) {
+          mma_f16_ss(dt, a0, smem_desc(bs + kOpBytes, 128, 512), id, true);
+          mma_f16_ss(dt, a1, smem_desc(bs + kOpBytes + 256, 128, 512), id, true);
         }
-        tc_commit(BAR(kBarAEmpty + a));
-        tc_commit(BAR(kBarDFull + d));
+        tc_commit(BAR(B::kWEmpty + ws));
+        tc_commit(BAR(B::kDFull + k));
+        it += kNumD;
+        if (it >= kItems) it -= kItems;
+        ts += kNumD;
+        if (ts >= kTokStages) {
+          ts -= kTokStages;
+          tpar ^= 1u;
+        }
+        ws += kNumD;
+        if (ws >= kWStages) {
+          ws -= kWStages;
+          wpar ^= 1u;
+        }
       }
-      // all issued MMAs complete before TMEM is freed
-      tc_commit(BAR(kBarDone));
-      wait_bar(BAR(kBarDone), 0, 8);
+    }
+    // all issued MMAs complete before TMEM is freed
+    if (lane == 0) {
+      tc_commit(BAR(B::kDone + k));
+      wait_bar_spin(BAR(B::kDone + k), 0, 9);
     }
     __syncwarp();
   } else {
     // -------------------------------------------------------- epilogue
     const int quarter = warp & 3, half = (warp - kWarpEpi0) >> 2;
-    const int r = quarter * 32 + lane, n = wt * kRows + r;
-    const bool row_ok = n < A.N;
+    const int r = quarter * 32 + lane;        // token of the tile = TMEM lane
+    const int m = tt * kTileTokens + r;
+    const int n0 = wt * kRows + 64 * half;    // first weight row of this thread's columns
     const uint32_t tl = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-    const int m0 = tt * kTileTokens + 64 * half;  // token of column 0 of this thread
-    f2 acc[32];                                   // token pairs (2i, 2i+1) of the current super-block
+    f2 acc[32];                               // weight-row pairs (2i, 2i+1) of the current super-block
 #pragma unroll
     for (int i = 0; i < 32; ++i) acc[i] = 0ull;
-    unsigned coef = row_ok ? load_coef<TYPE>(A, n, 0) : 0u;
     bool ok = true;
     int f = 0;
     for (int b = 0; b < A.nsb && ok; ++b) {
-      const unsigned cur = coef;
-      if (row_ok && b + 1 < A.nsb) coef = load_coef<TYPE>(A, n, b + 1);
-      // d, times 2^14 for Q4_K (its operand carries sc*q*2^-14)
-      const float da = half_bits_to_float(cur) * (TYPE == 12 ? 16384.0f : 1.0f);
-      const float dm = TYPE == 12 ? -half_bits_to_float(cur >> 16) : 0.0f;
-      const f2 da2 = pk(da, da), dm2 = pk(dm, dm);
       for (int it = 0; it < kItems; ++it, ++f) {
-        const int d = f & 1, ts = f % kTokStages;
-        if (!warp_wait(BAR(kBarDFull + d), (f >> 1) & 1, 9) ||
-            !warp_wait(BAR(kBarTokFull + ts), (f / kTokStages) & 1, 10)) {
+        const int d = f % kNumD, ts = f % kTokStages;
+        if (!warp_wait(BAR(B::kDFull + d), (f / kNumD) & 1, 10) ||
+            !warp_wait(BAR(B::kTokFull + ts), (f / kTokStages) & 1, 13)) {
           ok = false;
           break;
         }
         tc_fence_after();
         const uint32_t dcol = tl + kColD + 128u * d + 64u * half;
         if (it < 8) {
-          const float4* d8 = reinterpret_cast<const float4*>(tok_ring + ts * kTileItem + kTileItemOp) + 16 * half;
+          const float d8 = reinterpret_cast<const float*>(tok_ring + ts * kTileItem + kTileItemOp)[r];
+          const f2 d82 = pk(d8, d8);
+          // two 16-column loads in flight per wait
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            uint32_t v[16];
+          for (int c = 0; c < 4; c += 2) {
+            uint32_t v[16], w[16];
             tmem_ld16(dcol + 16 * c, v);
+            tmem_ld16(dcol + 16 * c + 16, w);
             tmem_wait_ld();
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const float4 s = d8[4 * c + k];
-              acc[8 * c + 2 * k] = fma2(pk(s.x, s.y), pk(__uint_as_float(v[4 * k]), __uint_as_float(v[4 * k + 1])),
-                                        acc[8 * c + 2 * k]);
-              acc[8 * c + 2 * k + 1] =
-                  fma2(pk(s.z, s.w), pk(__uint_as_float(v[4 * k + 2]), __uint_as_float(v[4 * k + 3])),
-                       acc[8 * c + 2 * k + 1]);
+            for (int k = 0; k < 8; ++k) {
+              acc[8 * c + k] = fma2(d82, pk(__uint_as_float(v[2 * k]), __uint_as_float(v[2 * k + 1])), acc[8 * c + k]);
+              acc[8 * c + 8 + k] =
+                  fma2(d82, pk(__uint_as_float(w[2 * k]), __uint_as_float(w[2 * k + 1])), acc[8 * c + 8 + k]);
             }
           }
         }
         if (it == kItems - 1) {
           // super-block end: run += d' * acc (- dmin * Dmin)
+          const int cs = b % kCoefStages;
+          if (!warp_wait(BAR(B::kCoefFull + cs), (b / kCoefStages) & 1, 14)) {
+            ok = false;
+            break;
+          }
+          const float4* cf = reinterpret_cast<const float4*>(coef_ring + cs * kRows + 64 * half);
           const bool last = b == A.nsb - 1;
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
@@ -482,19 +548,28 @@ __global__ void __launch_bounds__(kThreads, 1) tile_mma_kernel(const __grid_cons
             uint32_t out[16];
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
+              const float4 q = cf[8 * c + k];  // (d', -dmin) of rows 2k, 2k+1 of this chunk
               f2 rv = b > 0 ? pk(__uint_as_float(run[2 * k]), __uint_as_float(run[2 * k + 1])) : 0ull;
-              rv = fma2(da2, acc[8 * c + k], rv);
-              if (TYPE == 12) rv = fma2(dm2, pk(__uint_as_float(dmin[2 * k]), __uint_as_float(dmin[2 * k + 1])), rv);
+              rv = fma2(pk(q.x, q.z), acc[8 * c + k], rv);
+              if (TYPE == 12)
+                rv = fma2(pk(q.y, q.w), pk(__uint_as_float(dmin[2 * k]), __uint_as_float(dmin[2 * k + 1])), rv);
               out[2 * k] = static_cast<uint32_t>(rv);
               out[2 * k + 1] = static_cast<uint32_t>(rv >> 32);
               acc[8 * c + k] = 0ull;
             }
             if (last) {
-              if (row_ok) {
+              if (m < A.M) {
+                const int nc = n0 + 16 * c;
+                float* yr = A.y + static_cast<size_t>(m) * A.N;
+                if ((A.N & 3) == 0 && nc + 16 <= A.N) {
 #pragma unroll
-                for (int k = 0; k < 16; ++k) {
-                  const int m = m0 + 16 * c + k;
-                  if (m < A.M) A.y[static_cast<size_t>(m) * A.N + n] = __uint_as_float(out[k]);
+                  for (int k = 0; k < 4; ++k)
+                    *reinterpret_cast<uint4*>(yr + nc + 4 * k) =
+                        make_uint4(out[4 * k], out[4 * k + 1], out[4 * k + 2], out[4 * k + 3]);
+                } else {
+#pragma unroll
+                  for (int k = 0; k < 16; ++k)
+                    if (nc + k < A.N) yr[nc + k] = __uint_as_float(out[k]);
                 }
               }
             } else {
@@ -502,12 +577,14 @@ __global__ void __launch_bounds__(kThreads, 1) tile_mma_kernel(const __grid_cons
             }
           }
           if (!last) tmem_wait_st();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(BAR(B::kCoefEmpty + cs));
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) {
-          mbar_arrive(BAR(kBarDEmpty + d));
-          mbar_arrive(BAR(kBarTokEmpty + ts));
+          mbar_arrive(BAR(B::kDEmpty + d));
+          mbar_arrive(BAR(B::kTokEmpty + ts));
         }
       }
     }

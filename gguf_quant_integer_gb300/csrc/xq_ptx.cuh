@@ -49,6 +49,32 @@ __device__ __forceinline__ bool mbar_wait(uint32_t a, unsigned parity, unsigned 
   return true;
 }
 
+// try_wait that may suspend the thread for up to `ns` nanoseconds while the
+// phase is incomplete (it resumes when the phase completes): waiting warps
+// then leave the issue slots to the warps doing work.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t a, unsigned parity, unsigned ns) {
+  unsigned ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(a), "r"(parity), "r"(ns)
+      : "memory");
+  return ok != 0;
+}
+// mbar_wait with suspending polls.
+__device__ __forceinline__ bool mbar_wait_sleep(uint32_t a, unsigned parity, unsigned int* err, unsigned code,
+                                                long long limit) {
+  if (mbar_try_wait(a, parity)) return true;
+  const long long t0 = clock64();
+  while (!mbar_try_wait_sleep(a, parity, 20000u)) {
+    if (clock64() - t0 > limit) {
+      atomicExch(err, code);
+      return false;
+    }
+  }
+  return true;
+}
+
 // ------------------------------------------------ TMA and bulk copies
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t mbar) {
   asm volatile(
@@ -98,6 +124,20 @@ __device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uin
           d_tmem),
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(static_cast<uint32_t>(accumulate))
       : "memory");
+}
+// D[tmem] (+)= A[smem] x B[smem]^T, one K = 16 step; accumulate unless first.
+__device__ __forceinline__ void mma_f16_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                           bool accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.u32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(
+          d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(static_cast<uint32_t>(accumulate))
+      : "memory");
+}
+// Make this thread's generic-proxy shared-memory writes visible to the async
+// proxy (tensor-core operand reads, bulk copies).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 // Arrive on the mbarrier once every tcgen05 operation issued so far by this
 // thread has completed.
