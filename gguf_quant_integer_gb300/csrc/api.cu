@@ -23,7 +23,9 @@ xq_status check_shape(int M, int N, int K) {
 }
 
 // Enqueue y = x W^T. M > 8: the tensor-memory tile kernel (both types).
-// M <= 8: Q4_K on the warp-level MMA GEMV, Q6_K on the dp4a GEMV.
+// M <= 8: the warp-level MMA GEMV (8-token chunks, up to kMaxProj chunks per
+// launch) for Q4_K and for Q6_K rows that are 16-byte multiples; the dp4a
+// GEMV for the other Q6_K shapes.
 xq_status run_matmul(int type, const void* W, const void* xq, int M, int N, int K, float* y,
                      int32_t* isum, cudaStream_t s) {
   const xq::Q8Layout L = xq::q8_layout(M, K);
@@ -32,7 +34,7 @@ xq_status run_matmul(int type, const void* W, const void* xq, int M, int N, int 
     const cudaError_t e = xq::launch_tile_mma(type, static_cast<const uint8_t*>(W), base, M, N, K, y, s, true);
     return e == cudaSuccess ? XQ_OK : XQ_ERR_CUDA;
   }
-  if (type == XQ_TYPE_Q4_K) {
+  if (xq::gemv_mma_supports(type, K)) {
     xq::MmaProj items[xq::kMaxProj];
     int n = 0;
     for (int c = 0; c < L.chunks; ++c) {
@@ -46,7 +48,7 @@ xq_status run_matmul(int type, const void* W, const void* xq, int M, int N, int 
       q.M_total = M;
       q.chunk = c;
       if (n == xq::kMaxProj || c + 1 == L.chunks) {
-        if (xq::launch_gemv_q4k_mma(items, n, s, true) != cudaSuccess) return XQ_ERR_CUDA;
+        if (xq::launch_gemv_mma(type, items, n, s, true) != cudaSuccess) return XQ_ERR_CUDA;
         n = 0;
       }
     }
@@ -86,26 +88,44 @@ xq_status matmul_entry(int type, const void* W, const void* xq, int M, int N, in
 
 size_t round256(size_t b) { return (b + 255) & ~static_cast<size_t>(255); }
 
-// The layer workspace ends with the grouped matmul's scheduling state: a
-// 256-byte task counter, the arrival counts of split projections, and their
-// partial sums (sizes from the same helpers the launcher uses).
+// The layer workspace ends with the grouped matmuls' scheduling state (for
+// M <= 8): one 256-byte task counter per weight type, then the arrival
+// counts of split projections of both types, then their partial sums (sizes
+// from the same helpers the launcher uses). The counters and arrival counts
+// form one range that the quantize launch zeroes.
 constexpr size_t kCounterBytes = 256;
+constexpr int kTypes = 2;  // 0: Q4_K, 1: Q6_K
 
-struct SchedBytes {
-  size_t arrive, partial;
+int type_index(int type) { return type == XQ_TYPE_Q4_K ? 0 : 1; }
+
+struct Sched {
+  bool dynamic[kTypes];  // the type's grouped GEMV fits one launch: counter and K-split
+  size_t arrive[kTypes], partial[kTypes];
 };
 
-SchedBytes sched_bytes(const xq_proj* proj, int n_proj, int M) {
-  SchedBytes b = {0, 0};
+// Projections that go to the grouped tensor-core GEMV at M <= 8.
+bool in_group(const xq_proj& q, int M) { return q.N > 0 && M <= kMaxGemvM && xq::gemv_mma_supports(q.type, q.K); }
+
+Sched sched_layout(const xq_proj* proj, int n_proj, int M) {
+  Sched sc = {};
+  int items[kTypes] = {0, 0};
+  for (int p = 0; p < n_proj; ++p)
+    if (in_group(proj[p], M)) ++items[type_index(proj[p].type)];
+  for (int g = 0; g < kTypes; ++g) sc.dynamic[g] = items[g] > 0 && items[g] <= xq::kMaxProj;
   for (int p = 0; p < n_proj; ++p) {
-    if (proj[p].type != XQ_TYPE_Q4_K || proj[p].N == 0) continue;
-    const int nch = xq::q4k_split_chunks(proj[p].K, M);
+    if (!in_group(proj[p], M) || !sc.dynamic[type_index(proj[p].type)]) continue;
+    const int g = type_index(proj[p].type);
+    const int nch = xq::gemv_split_chunks(proj[p].K, M);
     if (nch > 1) {
-      b.arrive += xq::q4k_split_arrive_bytes(proj[p].N);
-      b.partial += xq::q4k_split_partial_bytes(proj[p].N, nch);
+      sc.arrive[g] += xq::gemv_split_arrive_bytes(proj[p].N);
+      sc.partial[g] += xq::gemv_split_partial_bytes(proj[p].N, nch);
     }
   }
-  return b;
+  return sc;
+}
+
+size_t sched_bytes(const Sched& sc) {
+  return kTypes * kCounterBytes + sc.arrive[0] + sc.arrive[1] + sc.partial[0] + sc.partial[1];
 }
 
 // Validate a layer description and find each input's K (0 = unused).
@@ -196,8 +216,7 @@ size_t xq_layer_workspace_bytes(const xq_proj* proj, int n_proj, int n_inputs, i
   size_t total = 0;
   for (int i = 0; i < n_inputs; ++i)
     if (in_k[i]) total += round256(xq_q8_bytes(M, in_k[i]));
-  const SchedBytes sb = sched_bytes(proj, n_proj, M);
-  return total + kCounterBytes + sb.arrive + sb.partial;
+  return total + sched_bytes(sched_layout(proj, n_proj, M));
 }
 
 xq_status xq_layer_mixed(const xq_proj* proj, int n_proj, const float* const* inputs, int n_inputs,
@@ -217,9 +236,9 @@ xq_status xq_layer_mixed(const xq_proj* proj, int n_proj, const float* const* in
       need += round256(xq_q8_bytes(M, in_k[i]));
     }
   }
-  const size_t counter_off = need;
-  const SchedBytes sb = sched_bytes(proj, n_proj, M);
-  need += kCounterBytes + sb.arrive + sb.partial;
+  const size_t sched_off = need;
+  const Sched sc = sched_layout(proj, n_proj, M);
+  need += sched_bytes(sc);
   if (!workspace) return XQ_ERR_ARG;
   if (ws_bytes < need) return XQ_ERR_WORKSPACE;
   if (!aligned16(workspace)) return XQ_ERR_ALIGN;
@@ -230,17 +249,25 @@ xq_status xq_layer_mixed(const xq_proj* proj, int n_proj, const float* const* in
   }
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  unsigned int* counter = reinterpret_cast<unsigned int*>(ws + counter_off);
-  const int chunks = (M + 7) / 8;
-  int q4_items = 0;
-  for (int p = 0; p < n_proj; ++p)
-    if (proj[p].N > 0 && proj[p].type == XQ_TYPE_Q4_K) q4_items += chunks;
-  // Dynamic task fetch and K-split when every Q4_K chunk fits one launch:
-  // the quantize launch just before it zeroes the counter and the arrival
-  // counts (which the matmul also leaves at zero).
-  const bool dynamic = q4_items > 0 && q4_items <= xq::kMaxProj;
-  uint8_t* split_ws = dynamic ? ws + counter_off + kCounterBytes : nullptr;
-  const int zero_words = static_cast<int>((kCounterBytes + sb.arrive) / 4);
+  // scheduling state: counters, arrival counts (zeroed by the quantize
+  // launch; the matmuls leave them at zero), partial sums
+  unsigned int* counter[kTypes];
+  uint8_t* arrive[kTypes];
+  uint8_t* partial[kTypes];
+  {
+    uint8_t* c = ws + sched_off;
+    uint8_t* a = c + kTypes * kCounterBytes;
+    uint8_t* pt = a + sc.arrive[0] + sc.arrive[1];
+    for (int g = 0; g < kTypes; ++g) {
+      counter[g] = sc.dynamic[g] ? reinterpret_cast<unsigned int*>(c + g * kCounterBytes) : nullptr;
+      arrive[g] = sc.dynamic[g] ? a : nullptr;
+      partial[g] = sc.dynamic[g] ? pt : nullptr;
+      a += sc.arrive[g];
+      pt += sc.partial[g];
+    }
+  }
+  const bool any_dynamic = sc.dynamic[0] || sc.dynamic[1];
+  const int zero_words = static_cast<int>((kTypes * kCounterBytes + sc.arrive[0] + sc.arrive[1]) / 4);
   // One launch quantizes every input that is read (up to kMaxProj per launch).
   {
     xq::QuantJob jobs[xq::kMaxProj];
@@ -255,9 +282,8 @@ xq_status xq_layer_mixed(const xq_proj* proj, int n_proj, const float* const* in
       j.K = in_k[i];
       --left;
       if (n == xq::kMaxProj || left == 0) {
-        if (xq::launch_quantize_q8(jobs, n, s, true, (left == 0 && dynamic) ? counter : nullptr, zero_words) !=
-            cudaSuccess)
-          return XQ_ERR_CUDA;
+        unsigned int* zero = (left == 0 && any_dynamic) ? reinterpret_cast<unsigned int*>(ws + sched_off) : nullptr;
+        if (xq::launch_quantize_q8(jobs, n, s, true, zero, zero_words) != cudaSuccess) return XQ_ERR_CUDA;
         n = 0;
       }
     }
@@ -272,14 +298,16 @@ xq_status xq_layer_mixed(const xq_proj* proj, int n_proj, const float* const* in
     }
     return XQ_OK;
   }
-  // One launch for the Q4_K projections (8-token chunks, kMaxProj items per launch).
-  {
+  // One grouped tensor-core GEMV launch per weight type (kMaxProj items per
+  // launch; M <= 8 is one chunk per projection), Q4_K first.
+  for (int g = 0; g < kTypes; ++g) {
+    const int type = g == 0 ? XQ_TYPE_Q4_K : XQ_TYPE_Q6_K;
     xq::MmaProj items[xq::kMaxProj];
     int n = 0;
-    for (int p = 0; p < n_proj; ++p) {
-      const xq_proj& q = proj[p];
-      if (q.N == 0 || q.type != XQ_TYPE_Q4_K) continue;
-      for (int c = 0; c < chunks; ++c) {
+    for (int p = 0; p <= n_proj; ++p) {
+      if (p < n_proj) {
+        const xq_proj& q = proj[p];
+        if (!in_group(q, M) || q.type != type) continue;
         xq::MmaProj& it = items[n++];
         it.W = static_cast<const uint8_t*>(q.W);
         it.xq = ws + off[q.input];
@@ -288,20 +316,19 @@ xq_status xq_layer_mixed(const xq_proj* proj, int n_proj, const float* const* in
         it.N = q.N;
         it.K = q.K;
         it.M_total = M;
-        it.chunk = c;
-        if (n == xq::kMaxProj) {
-          if (xq::launch_gemv_q4k_mma(items, n, s, true, dynamic ? counter : nullptr, split_ws) != cudaSuccess)
-            return XQ_ERR_CUDA;
-          n = 0;
-        }
+        it.chunk = 0;
+      }
+      if (n > 0 && (n == xq::kMaxProj || p == n_proj)) {
+        if (xq::launch_gemv_mma(type, items, n, s, true, counter[g], arrive[g], partial[g]) != cudaSuccess)
+          return XQ_ERR_CUDA;
+        n = 0;
       }
     }
-    if (n && xq::launch_gemv_q4k_mma(items, n, s, true, dynamic ? counter : nullptr, split_ws) != cudaSuccess)
-      return XQ_ERR_CUDA;
   }
+  // the rest (Q6_K rows that are not 16-byte multiples) on the dp4a GEMV
   for (int p = 0; p < n_proj; ++p) {
     const xq_proj& q = proj[p];
-    if (q.N == 0 || q.type != XQ_TYPE_Q6_K) continue;
+    if (q.N == 0 || in_group(q, M)) continue;
     st = run_matmul(q.type, q.W, ws + off[q.input], M, q.N, q.K, q.y, nullptr, s);
     if (st != XQ_OK) return st;
   }

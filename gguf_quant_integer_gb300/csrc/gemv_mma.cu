@@ -1,6 +1,8 @@
-// Q4_K x Q8 -> fp32 for M <= 8 tokens on the tensor cores (mma.sync
+// Q4_K / Q6_K x Q8 -> fp32 for M <= 8 tokens on the tensor cores (mma.sync
 // m16n8k16, fp16 operands holding exact integers, fp32 accumulation), with
-// the weights streamed by TMA through a shared-memory ring.
+// the weights streamed by TMA through a shared-memory ring. The Q4_K
+// description follows; Q6_K differences are described at decode_scales_q6
+// and compute_block_q6.
 //
 // What it computes (xLLM v0.7 long-context article, section 一; M template
 // of section B2): for output row n and token m,
@@ -61,7 +63,7 @@ __device__ unsigned int g_gemv_error;  // set by a timed-out wait (never expecte
 namespace {
 
 struct Proj {
-  CUtensorMap map;     // 2D: {row_bytes/8 u64, N}, box {18, 16}
+  CUtensorMap map;     // Q4_K: {row_bytes/8 u64, N}, box {18, 16}; Q6_K: {row_bytes u8, N}, box {240, 16}
   const uint8_t* frag; // [K/32][32][16 B] lane operands of the 8-token chunk
   const uint8_t* fsc;  // [K/32][4][16 B]
   float* y;
@@ -77,13 +79,23 @@ struct Group {
   int n, total;
 };
 
-constexpr int kStages = 4;
-constexpr int kBlockBytes = 16 * kQ4kBytes;                 // 16 rows x one super-block
-constexpr int kFragOff = 4 * kBlockBytes;                   // 9216
-constexpr int kFscOff = kFragOff + 8 * 512;                 // 13312
-constexpr int kStageBytes = kFscOff + 8 * 64;               // 13824
-constexpr int kDecBytes = 8 * 16 * 16;                      // (a, a, b, b) per sub-block and row
-constexpr int kSmemBytes = kStages * kStageBytes + 4 * kDecBytes + kStages * 16 + 2 * kStages * 8 + 16;
+constexpr int kDecBytes = 8 * 16 * 16;  // per warp: one float4 per (32-block, row)
+
+// Stage layout per weight type: four 16-row TMA boxes of one super-block,
+// then the activation operands (8 x 512 B) and scale quads (8 x 64 B).
+// Q4_K boxes are the 144-byte super-blocks; Q6_K boxes are 240-byte windows
+// starting at the 16-byte boundary at or below the 210-byte super-block.
+template <int TYPE>
+struct GLay {
+  static constexpr int kBoxRow = TYPE == 12 ? kQ4kBytes : 240;
+  static constexpr int kStages = TYPE == 12 ? 4 : 3;
+  static constexpr int kBlockBytes = 16 * kBoxRow;  // 16 rows x one super-block
+  static constexpr int kFragOff = 4 * kBlockBytes;
+  static constexpr int kFscOff = kFragOff + 8 * 512;
+  static constexpr int kStageBytes = kFscOff + 8 * 64;
+  static constexpr int kSmemBytes = kStages * kStageBytes + 4 * kDecBytes + kStages * 16 + 2 * kStages * 8 + 16;
+};
+static_assert(GLay<12>::kStageBytes == 13824, "Q4_K stage layout");
 constexpr long long kWaitClocks = 1LL << 32;
 
 __device__ __forceinline__ int mma_row(int i) { return 8 * (i >> 3) + 2 * (i & 3) + ((i >> 2) & 1); }
@@ -138,7 +150,7 @@ __device__ __forceinline__ TaskPos task_pos(const Group& G, int task) {
 // rounding of an exact product. Packed bytes (public Q4_K layout):
 //   j < 4 : sc = s[j] & 63, m = s[j+4] & 63
 //   j >= 4: sc = (s[j+4] & 15) | (s[j-4] >> 6) << 4, m = (s[j+4] >> 4) | (s[j] >> 6) << 4
-__device__ __forceinline__ void decode_scales(const uint8_t* blk, float4* dec, int lane) {
+__device__ __forceinline__ void decode_scales_q4(const uint8_t* blk, float4* dec, int lane) {
   const int r = lane >> 1, half = lane & 1;
   const uint4 hd = *reinterpret_cast<const uint4*>(blk + r * kQ4kBytes);
   const unsigned scw = half ? ((hd.w & 0x0F0F0F0Fu) | ((hd.y >> 2) & 0x30303030u)) : (hd.y & 0x3F3F3F3Fu);
@@ -156,8 +168,46 @@ __device__ __forceinline__ void decode_scales(const uint8_t* blk, float4* dec, i
   }
 }
 
+
+// NW 32-bit words starting at a 2-byte aligned shared-memory address.
+template <int NW>
+__device__ __forceinline__ void load_words(const uint8_t* p, uint32_t (&out)[NW]) {
+  const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+  const uint32_t* w = reinterpret_cast<const uint32_t*>(a & ~static_cast<uintptr_t>(3));
+  const unsigned sh = static_cast<unsigned>(a & 3) * 8;
+  uint32_t prev = w[0];
+#pragma unroll
+  for (int k = 0; k < NW; ++k) {
+    const uint32_t next = w[k + 1];
+    out[k] = __funnelshift_r(prev, next, sh);
+    prev = next;
+  }
+}
+
+// Q6_K (public layout: ql[128] @0, qh[64] @128, int8 scales[16] @192, d @208;
+// the super-block starts `off` bytes into the row's window). Lane l takes
+// weight row l/2 and 32-blocks 4*(l&1) .. +3, writing for each 32-block p
+// (alpha_2p, alpha_2p, alpha_2p+1, alpha_2p+1), alpha_g = d * s_g (one
+// rounding of an exact product): the coefficients of the two 16-weight
+// groups of p.
+__device__ __forceinline__ void decode_scales_q6(const uint8_t* blk, int off, float4* dec, int lane) {
+  const int r = lane >> 1, half = lane & 1;
+  const uint8_t* sb = blk + r * GLay<14>::kBoxRow + off;
+  uint32_t sw[2];
+  load_words<2>(sb + 192 + 8 * half, sw);
+  const float d = half_bits_to_float(*reinterpret_cast<const unsigned short*>(sb + 208));
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const uint32_t w = sw[k >> 1];
+    const int b0 = 2 * (k & 1);
+    const float a0 = d * static_cast<float>(static_cast<int8_t>((w >> (8 * b0)) & 0xFFu));
+    const float a1 = d * static_cast<float>(static_cast<int8_t>((w >> (8 * b0 + 8)) & 0xFFu));
+    dec[(4 * half + k) * 16 + r] = make_float4(a0, a0, a1, a1);
+  }
+}
+
 template <bool ISUM>
-__device__ __forceinline__ void compute_block(const uint8_t* blk, const uint8_t* act, const float4* dec,
+__device__ __forceinline__ void compute_block_q4(const uint8_t* blk, const uint8_t* act, const float4* dec,
                                               const Proj& P, int rg, int b, int n8, int t, int lane, f2 (&acc)[2]) {
   const int r0 = mma_row(n8), r1 = r0 + 8;
   uint2 q0[4], q1[4];
@@ -168,7 +218,7 @@ __device__ __forceinline__ void compute_block(const uint8_t* blk, const uint8_t*
   }
   // Activation operands and scale quads of the super-block, from the stage.
   const uint4* fp = reinterpret_cast<const uint4*>(act) + lane;
-  const ulonglong2* sp = reinterpret_cast<const ulonglong2*>(act + (kFscOff - kFragOff)) + t;
+  const ulonglong2* sp = reinterpret_cast<const ulonglong2*>(act + (GLay<12>::kFscOff - GLay<12>::kFragOff)) + t;
   const ulonglong2* dp = reinterpret_cast<const ulonglong2*>(dec);
   // The four shared-memory operands of a sub-block are loaded one sub-block
   // ahead of their use.
@@ -213,6 +263,82 @@ __device__ __forceinline__ void compute_block(const uint8_t* blk, const uint8_t*
   }
 }
 
+
+// Q6_K 32-block p of rows r0, r1: lane (n8, t) holds the quants of weights
+// 8t..8t+7 of p, i.e. of group 2p for t < 2 and group 2p+1 for t >= 2
+// (the activation image's slot order, as for Q4_K). Each quant is
+// q = (ql nibble) | (qh 2 bits) << 4; the operand is q - 32 in fp16
+// (1024 + q from a byte permute, then an exact subtraction). Four MMAs per
+// 32-block: each group's accumulator gets the two k-halves with the other
+// group's lanes zeroed, so D_g = sum_{16} (q-32)*q8 = isum_g exactly
+// (|isum_g| <= 32*127*16). Combine: acc += (alpha_g * d8) * D_g per group.
+template <bool ISUM>
+__device__ __forceinline__ void compute_block_q6(const uint8_t* blk, int off, const uint8_t* act, const float4* dec,
+                                                 const Proj& P, int rg, int b, int n8, int t, int lane,
+                                                 f2 (&acc)[2]) {
+  const int r0 = mma_row(n8), r1 = r0 + 8;
+  const uint8_t* s0 = blk + r0 * GLay<14>::kBoxRow + off;
+  const uint8_t* s1 = blk + r1 * GLay<14>::kBoxRow + off;
+  const uint4* fp = reinterpret_cast<const uint4*>(act) + lane;
+  const ulonglong2* sp = reinterpret_cast<const ulonglong2*>(act + (GLay<14>::kFscOff - GLay<14>::kFragOff)) + t;
+  const ulonglong2* dp = reinterpret_cast<const ulonglong2*>(dec);
+  const bool first = t < 2;  // this lane's weights belong to group 2p
+#pragma unroll
+  for (int hh = 0; hh < 2; ++hh) {
+    // ql bytes 64hh + 8t (32-blocks 0, 2 of the half) and 64hh + 32 + 8t (1, 3);
+    // qh bytes 128 + 32hh + 8t (all four)
+    uint32_t la0[2], lb0[2], hq0[2], la1[2], lb1[2], hq1[2];
+    load_words<2>(s0 + 64 * hh + 8 * t, la0);
+    load_words<2>(s0 + 64 * hh + 32 + 8 * t, lb0);
+    load_words<2>(s0 + 128 + 32 * hh + 8 * t, hq0);
+    load_words<2>(s1 + 64 * hh + 8 * t, la1);
+    load_words<2>(s1 + 64 * hh + 32 + 8 * t, lb1);
+    load_words<2>(s1 + 128 + 32 * hh + 8 * t, hq1);
+#pragma unroll
+    for (int rr = 0; rr < 4; ++rr) {
+      const int p = 4 * hh + rr;
+      uint32_t a[2][4];  // [k-half][a0..a3]
+#pragma unroll
+      for (int w = 0; w < 2; ++w) {
+        const uint32_t L0 = (rr & 1) ? lb0[w] : la0[w], L1 = (rr & 1) ? lb1[w] : la1[w];
+        const uint32_t H0 = rr == 0 ? (hq0[w] << 4) : (rr == 1 ? (hq0[w] << 2) : (rr == 2 ? hq0[w] : (hq0[w] >> 2)));
+        const uint32_t H1 = rr == 0 ? (hq1[w] << 4) : (rr == 1 ? (hq1[w] << 2) : (rr == 2 ? hq1[w] : (hq1[w] >> 2)));
+        const uint32_t q0 = (((rr >> 1) ? (L0 >> 4) : L0) & 0x0F0F0F0Fu) | (H0 & 0x30303030u);
+        const uint32_t q1 = (((rr >> 1) ? (L1 >> 4) : L1) & 0x0F0F0F0Fu) | (H1 & 0x30303030u);
+        // (1024 + q) pairs, minus 1056: weights (4w, 4w+2) -> a0/a1, (4w+1, 4w+3) -> a2/a3
+        a[w][0] = hsub2(prmt(q0, 0x64646464u, 0x4240u), 0x64206420u);
+        a[w][1] = hsub2(prmt(q1, 0x64646464u, 0x4240u), 0x64206420u);
+        a[w][2] = hsub2(prmt(q0, 0x64646464u, 0x4341u), 0x64206420u);
+        a[w][3] = hsub2(prmt(q1, 0x64646464u, 0x4341u), 0x64206420u);
+      }
+      const uint4 B = fp[p * 32];
+      float D0[4] = {0.0f, 0.0f, 0.0f, 0.0f}, D1[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+      const uint32_t g0 = first ? 0xFFFFFFFFu : 0u, g1 = ~g0;
+      mma16816(D0, a[0][0] & g0, a[0][1] & g0, a[0][2] & g0, a[0][3] & g0, B.x, B.y);
+      mma16816(D0, a[1][0] & g0, a[1][1] & g0, a[1][2] & g0, a[1][3] & g0, B.z, B.w);
+      mma16816(D1, a[0][0] & g1, a[0][1] & g1, a[0][2] & g1, a[0][3] & g1, B.x, B.y);
+      mma16816(D1, a[1][0] & g1, a[1][1] & g1, a[1][2] & g1, a[1][3] & g1, B.z, B.w);
+      const ulonglong2 f = sp[p * 4];  // (d8 c0, d8 c1), (s8 c0, s8 c1)
+      const ulonglong2 e0 = dp[p * 16 + r0], e1 = dp[p * 16 + r1];
+      acc[0] = fma2(mul2(e0.x, f.x), pk(D0[0], D0[1]), fma2(mul2(e0.y, f.x), pk(D1[0], D1[1]), acc[0]));
+      acc[1] = fma2(mul2(e1.x, f.x), pk(D0[2], D0[3]), fma2(mul2(e1.y, f.x), pk(D1[2], D1[3]), acc[1]));
+      if (ISUM) {
+        const int ngrp = P.K >> 4;
+#pragma unroll
+        for (int g = 0; g < 2; ++g)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int row = rg * 16 + ((e >> 1) ? r1 : r0);
+            const int col = 2 * t + (e & 1);
+            if (row < P.N && col < P.M)
+              P.isum[(static_cast<size_t>(col) * P.N + row) * ngrp + 16 * b + 2 * p + g] =
+                  static_cast<int32_t>(g ? D1[e] : D0[e]);
+          }
+      }
+    }
+  }
+}
+
 __device__ __forceinline__ void store_y(const Proj& P, int rg, int n8, int t, float v00, float v01, float v10,
                                         float v11) {
   const int r0 = rg * 16 + mma_row(n8), r1 = r0 + 8, c0 = 2 * t, c1 = c0 + 1;
@@ -231,9 +357,12 @@ __device__ __forceinline__ int next_task(const Group& G, int cur) {
   return cur + static_cast<int>(gridDim.x);
 }
 
-template <bool ISUM>
+template <int TYPE, bool ISUM>
 __global__ void __launch_bounds__(160, 3)
-gemv_q4k_mma_kernel(const __grid_constant__ Group G) {
+gemv_mma_kernel(const __grid_constant__ Group G) {
+  using Lay = GLay<TYPE>;
+  constexpr int kStages = Lay::kStages, kStageBytes = Lay::kStageBytes, kBlockBytes = Lay::kBlockBytes;
+  constexpr int kFragOff = Lay::kFragOff, kFscOff = Lay::kFscOff;
   extern __shared__ __align__(128) uint8_t smem[];
   uint8_t* ring = smem;
   float4* dec_all = reinterpret_cast<float4*>(smem + kStages * kStageBytes);
@@ -282,7 +411,8 @@ gemv_q4k_mma_kernel(const __grid_constant__ Group G) {
         mbar_expect_tx(full_s + 8 * slot, static_cast<unsigned>(nblk * kBlockBytes + 8 * 512 + 8 * 64));
         const uint32_t st = ring_s + slot * kStageBytes;
         for (int w = 0; w < nblk; ++w)
-          tma_load_2d(st + w * kBlockBytes, &P.map, b * (kQ4kBytes / 8), tp.rb * 64 + 16 * w, full_s + 8 * slot);
+          tma_load_2d(st + w * kBlockBytes, &P.map, TYPE == 12 ? b * (kQ4kBytes / 8) : ((kQ6kBytes * b) & ~15),
+                      tp.rb * 64 + 16 * w, full_s + 8 * slot);
         bulk_load(st + kFragOff, P.frag + static_cast<size_t>(b) * 8 * 512, 8 * 512, full_s + 8 * slot);
         bulk_load(st + kFscOff, P.fsc + static_cast<size_t>(b) * 8 * 64, 8 * 64, full_s + 8 * slot);
         if (++slot == kStages) {
@@ -315,9 +445,16 @@ gemv_q4k_mma_kernel(const __grid_constant__ Group G) {
     const uint8_t* st = ring + slot * kStageBytes;
     const bool rows_ok = rg * 16 < P.N;
     if (rows_ok) {
-      decode_scales(st + warp * kBlockBytes, dec, lane);
-      __syncwarp();
-      compute_block<ISUM>(st + warp * kBlockBytes, st + kFragOff, dec, P, rg, m.y, n8, t, lane, acc);
+      if (TYPE == 12) {
+        decode_scales_q4(st + warp * kBlockBytes, dec, lane);
+        __syncwarp();
+        compute_block_q4<ISUM>(st + warp * kBlockBytes, st + kFragOff, dec, P, rg, m.y, n8, t, lane, acc);
+      } else {
+        const int off = (kQ6kBytes * m.y) & 15;  // the same for every row: rows are 16-byte multiples
+        decode_scales_q6(st + warp * kBlockBytes, off, dec, lane);
+        __syncwarp();
+        compute_block_q6<ISUM>(st + warp * kBlockBytes, off, st + kFragOff, dec, P, rg, m.y, n8, t, lane, acc);
+      }
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(empty_s + 8 * slot);
@@ -369,13 +506,14 @@ gemv_q4k_mma_kernel(const __grid_constant__ Group G) {
   }
 }
 
-template <bool ISUM>
+template <int TYPE, bool ISUM>
 int max_ctas() {
   static int per_sm = -1;
   if (per_sm < 0) {
     int n = 0;
-    cudaFuncSetAttribute(gemv_q4k_mma_kernel<ISUM>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, gemv_q4k_mma_kernel<ISUM>, 160, kSmemBytes) != cudaSuccess ||
+    constexpr int kSmemBytes = GLay<TYPE>::kSmemBytes;
+    cudaFuncSetAttribute(gemv_mma_kernel<TYPE, ISUM>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, gemv_mma_kernel<TYPE, ISUM>, 160, kSmemBytes) != cudaSuccess ||
         n < 1)
       n = 1;
     per_sm = n;
@@ -383,12 +521,16 @@ int max_ctas() {
   return per_sm * kNumSMs;
 }
 
-// Q4_K rows as a 2D tensor of 8-byte elements: {row_bytes/8, N}, boxes of
-// one super-block x 16 rows.
-bool encode_weight_map(CUtensorMap* map, const uint8_t* W, int N, int K) {
-  const unsigned long long row_bytes = static_cast<unsigned long long>(K / 256) * kQ4kBytes;
-  return encode_tma_2d(map, CU_TENSOR_MAP_DATA_TYPE_UINT64, W, row_bytes / 8, static_cast<unsigned long long>(N),
-                       row_bytes, kQ4kBytes / 8, 16);
+// Weight rows as a 2D tensor, boxes of 16 rows: Q4_K as 8-byte elements
+// {row_bytes/8, N} with one super-block per box row; Q6_K as bytes
+// {row_bytes, N} with 240-byte box rows (rows must be 16-byte multiples).
+bool encode_weight_map(int type, CUtensorMap* map, const uint8_t* W, int N, int K) {
+  const unsigned long long nsb = static_cast<unsigned long long>(K / 256);
+  if (type == 12)
+    return encode_tma_2d(map, CU_TENSOR_MAP_DATA_TYPE_UINT64, W, nsb * kQ4kBytes / 8, static_cast<unsigned long long>(N),
+                         nsb * kQ4kBytes, kQ4kBytes / 8, 16);
+  return encode_tma_2d(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, W, nsb * kQ6kBytes, static_cast<unsigned long long>(N),
+                       nsb * kQ6kBytes, GLay<14>::kBoxRow, 16);
 }
 
 }  // namespace
@@ -424,13 +566,18 @@ bool encode_tma_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, u
          CUDA_SUCCESS;
 }
 
-cudaError_t launch_gemv_q4k_mma(const MmaProj* projs, int n, cudaStream_t s, bool pdl, unsigned int* counter,
-                                uint8_t* split_ws) {
-  if (n <= 0 || n > kMaxProj) return cudaErrorInvalidValue;
-  // Per-projection K-chunking (only with a split workspace) and task cost.
+bool gemv_mma_supports(int type, int K) {
+  return type == 12 || (type == 14 && ((K / 256) % 8) == 0);
+}
+
+cudaError_t launch_gemv_mma(int type, const MmaProj* projs, int n, cudaStream_t s, bool pdl, unsigned int* counter,
+                            uint8_t* arrive_ws, uint8_t* partial_ws) {
+  if (n <= 0 || n > kMaxProj || (type != 12 && type != 14)) return cudaErrorInvalidValue;
+  // Per-projection K-chunking (only with split workspaces) and task cost.
+  const bool split = arrive_ws != nullptr && partial_ws != nullptr;
   int nch[kMaxProj], cost[kMaxProj];
   for (int k = 0; k < n; ++k) {
-    nch[k] = split_ws ? q4k_split_chunks(projs[k].K, projs[k].M_total) : 1;
+    nch[k] = split ? gemv_split_chunks(projs[k].K, projs[k].M_total) : 1;
     cost[k] = ((projs[k].K >> 8) + nch[k] - 1) / nch[k];
   }
   // Most expensive tasks first (dynamic scheduling takes them in order).
@@ -442,20 +589,16 @@ cudaError_t launch_gemv_q4k_mma(const MmaProj* projs, int n, cudaStream_t s, boo
       order[b] = order[b - 1];
       order[b - 1] = tmp;
     }
-  // Split workspace: every item's arrival counts first (one zeroed range),
-  // then the partial buffers, both in item order.
+  // Split workspaces: arrival counts and partial buffers, in item order.
   size_t arrive_off[kMaxProj], partial_off[kMaxProj];
   {
     size_t a = 0, p = 0;
     for (int k = 0; k < n; ++k)
       if (nch[k] > 1) {
         arrive_off[k] = a;
-        a += q4k_split_arrive_bytes(projs[k].N);
-      }
-    for (int k = 0; k < n; ++k)
-      if (nch[k] > 1) {
-        partial_off[k] = a + p;
-        p += q4k_split_partial_bytes(projs[k].N, nch[k]);
+        a += gemv_split_arrive_bytes(projs[k].N);
+        partial_off[k] = p;
+        p += gemv_split_partial_bytes(projs[k].N, nch[k]);
       }
   }
   Group G;
@@ -469,7 +612,7 @@ cudaError_t launch_gemv_q4k_mma(const MmaProj* projs, int n, cudaStream_t s, boo
     const Q8Layout L = q8_layout(q.M_total, q.K);
     const int m0 = 8 * q.chunk;
     Proj& P = G.p[k];
-    if (!encode_weight_map(&P.map, q.W, q.N, q.K)) return cudaErrorInvalidValue;
+    if (!gemv_mma_supports(type, q.K) || !encode_weight_map(type, &P.map, q.W, q.N, q.K)) return cudaErrorInvalidValue;
     P.frag = q.xq + L.frag + static_cast<size_t>(q.chunk) * 16 * q.K;
     P.fsc = q.xq + L.fsc + static_cast<size_t>(q.chunk) * 2 * q.K;
     P.y = q.y + static_cast<size_t>(m0) * q.N;
@@ -482,8 +625,8 @@ cudaError_t launch_gemv_q4k_mma(const MmaProj* projs, int n, cudaStream_t s, boo
     P.arrive = nullptr;
     const int rbs = (q.N + 63) / 64;
     if (P.nch > 1) {
-      P.partial = reinterpret_cast<float*>(split_ws + partial_off[src]);
-      P.arrive = reinterpret_cast<unsigned int*>(split_ws + arrive_off[src]);
+      P.partial = reinterpret_cast<float*>(partial_ws + partial_off[src]);
+      P.arrive = reinterpret_cast<unsigned int*>(arrive_ws + arrive_off[src]);
     }
     P.task0 = total;
     total += rbs * P.nch;
@@ -491,19 +634,23 @@ cudaError_t launch_gemv_q4k_mma(const MmaProj* projs, int n, cudaStream_t s, boo
   }
   G.total = total;
   if (total == 0) return cudaSuccess;
-  const int cap = isum ? max_ctas<true>() : max_ctas<false>();
+  const int cap = type == 12 ? (isum ? max_ctas<12, true>() : max_ctas<12, false>())
+                             : (isum ? max_ctas<14, true>() : max_ctas<14, false>());
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(total < cap ? total : cap));
   cfg.blockDim = dim3(160);
-  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.dynamicSmemBytes = type == 12 ? GLay<12>::kSmemBytes : GLay<14>::kSmemBytes;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return isum ? cudaLaunchKernelEx(&cfg, gemv_q4k_mma_kernel<true>, G)
-              : cudaLaunchKernelEx(&cfg, gemv_q4k_mma_kernel<false>, G);
+  if (type == 12)
+    return isum ? cudaLaunchKernelEx(&cfg, gemv_mma_kernel<12, true>, G)
+                : cudaLaunchKernelEx(&cfg, gemv_mma_kernel<12, false>, G);
+  return isum ? cudaLaunchKernelEx(&cfg, gemv_mma_kernel<14, true>, G)
+              : cudaLaunchKernelEx(&cfg, gemv_mma_kernel<14, false>, G);
 }
 
 }  // namespace xq

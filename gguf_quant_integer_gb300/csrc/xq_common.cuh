@@ -157,35 +157,43 @@ cudaError_t launch_quantize_q8(const QuantJob* jobs, int n, cudaStream_t s, bool
                                unsigned int* zero_words = nullptr, int zero_count = 0);
 
 struct MmaProj {
-  const uint8_t* W;    // Q4_K super-blocks [N][K/256]
+  const uint8_t* W;    // super-blocks [N][K/256]
   const uint8_t* xq;   // Q8 buffer of this projection's input (M_total tokens)
   float* y;            // [M_total][N]; this launch writes tokens 8*chunk .. 8*chunk+7
   int32_t* isum;       // optional [M_total][N][K/32], only with M_total <= 8
   int N, K, M_total, chunk;
 };
 
-// K-chunks a Q4_K projection's rows are split into when a split workspace
-// is available: rows of more than 24 super-blocks go in chunks of ~16.
-__host__ __device__ inline int q4k_split_chunks(int K, int M_total) {
+// K-chunks a projection's rows are split into when a split workspace is
+// available: rows of more than 24 super-blocks go in chunks of ~16.
+__host__ __device__ inline int gemv_split_chunks(int K, int M_total) {
   const int nsb = K >> 8;
   return (M_total <= 8 && nsb > 24) ? (nsb + 15) / 16 : 1;
 }
 // Workspace of a split projection: partial sums [nch][8][64 * row blocks]
 // and one arrival count per 64-row block (both rounded to 256 bytes).
-__host__ __device__ inline size_t q4k_split_partial_bytes(int N, int nch) {
+__host__ __device__ inline size_t gemv_split_partial_bytes(int N, int nch) {
   return ((static_cast<size_t>(nch) * 8 * (((N + 63) / 64) * 64) * 4) + 255) & ~static_cast<size_t>(255);
 }
-__host__ __device__ inline size_t q4k_split_arrive_bytes(int N) {
+__host__ __device__ inline size_t gemv_split_arrive_bytes(int N) {
   return ((static_cast<size_t>((N + 63) / 64) * 4) + 255) & ~static_cast<size_t>(255);
 }
 
-// One launch for up to kMaxProj Q4_K projection chunks of <= 8 tokens. With
+// Whether the tensor-core GEMV takes this weight: every Q4_K shape; Q6_K
+// when its rows are 16-byte multiples (K/256 a multiple of 8), which the
+// tensor map needs.
+bool gemv_mma_supports(int type, int K);
+
+// One launch for up to kMaxProj projection chunks of <= 8 tokens, all of one
+// type (12 = Q4_K, 14 = Q6_K, the latter only where gemv_mma_supports). With
 // a counter (zeroed by the previous kernel on the stream) tasks are fetched
 // dynamically, most expensive first; without one they are strided. With a
-// split workspace (arrival counts zeroed before the first use) long rows are
-// split into K-chunks across CTAs.
-cudaError_t launch_gemv_q4k_mma(const MmaProj* projs, int n, cudaStream_t s, bool pdl,
-                                unsigned int* counter = nullptr, uint8_t* split_ws = nullptr);
+// split workspace (arrival counts, zeroed before the first use, at arrive_ws;
+// partial sums at partial_ws; sizes from the gemv_split_* helpers in item
+// order) long rows are split into K-chunks across CTAs.
+cudaError_t launch_gemv_mma(int type, const MmaProj* projs, int n, cudaStream_t s, bool pdl,
+                            unsigned int* counter = nullptr, uint8_t* arrive_ws = nullptr,
+                            uint8_t* partial_ws = nullptr);
 cudaError_t launch_gemv_q4k(const GemvArgs& a, cudaStream_t s);
 
 // 2D tensor map (no interleave, no swizzle, zero fill): dims {dim0, dim1}

@@ -129,7 +129,9 @@ XQ_API xq_status xq_matmul_q4k_q8(const void *W, const void *xq, int M, int N, i
  * of the mixed model are Q6_K).
  *   W  : Q6_K bytes [N][K/256][210], device, read-only. Individual blocks are
  *        2-byte aligned (210 is not a multiple of 4); only the base pointer
- *        must be 16-byte aligned. */
+ *        must be 16-byte aligned.
+ * Dispatch at M <= 8: the tensor-core GEMV when rows are 16-byte multiples
+ * (K a multiple of 2048), else a dp4a GEMV; M > 8: the tile kernel. */
 XQ_API xq_status xq_matmul_q6k_q8(const void *W, const void *xq, int M, int N, int K,
                            float *y, xq_stream stream);
 
@@ -144,9 +146,10 @@ typedef struct {
 
 /* Workspace bytes xq_layer_mixed needs: the Q8 buffers of every input that
  * some projection reads, each rounded up to 256 bytes, then scheduling
- * state: 256 bytes, plus, for each Q4_K projection with more than 24
- * super-blocks per row (split over K across CTAs when M <= 8), its arrival
- * counts and partial sums. 0 on bad arguments. */
+ * state: one 256-byte task counter per weight type (Q4_K, Q6_K) and, for
+ * each projection with more than 24 super-blocks per row that the grouped
+ * tensor-core GEMV splits over K across CTAs (M <= 8), its arrival counts
+ * and partial sums. 0 on bad arguments. */
 XQ_API size_t xq_layer_workspace_bytes(const xq_proj *proj, int n_proj, int n_inputs, int M);
 
 /* One layer's projections with a quant type per tensor (xLLM v0.7 article,

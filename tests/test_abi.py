@@ -96,7 +96,8 @@ def test_layer_argument_errors(L):
 
     arr, n = projs((12, 16, 512, 0), (14, 8, 512, 0), (12, 16, 1024, 1))
     need = L.xq_layer_workspace_bytes(arr, n, 2, 4)
-    expect = sum(((xq.q8_bytes(4, k) + 255) // 256) * 256 for k in (512, 1024)) + 256
+    # Q8 buffers, then one 256-byte task counter per weight type (no split at these K)
+    expect = sum(((xq.q8_bytes(4, k) + 255) // 256) * 256 for k in (512, 1024)) + 2 * 256
     assert need == expect
     # mismatched K on one input
     bad, nb = projs((12, 16, 512, 0), (12, 16, 768, 0))

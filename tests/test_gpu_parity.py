@@ -221,11 +221,12 @@ def test_tile_shapes(xq, qtype, N, K, M):
     assert run_and_check(xq, qtype, N, K, M, 41 * N + K + qtype, 3 * M + K, want_isum=False) > 0.0
 
 
-@pytest.mark.parametrize("M", [4, 70])
-def test_q6k_full_range_scales(xq, M):
+@pytest.mark.parametrize("M,K", [(4, 1024), (4, 2048), (70, 1024)])
+def test_q6k_full_range_scales(xq, M, K):
     # GGUF Q6_K scales span int8; |s| > 64 takes the two-operand form in the
     # tile kernel. Rows 0..63 keep |s| <= 64 so that a tile mixes both forms.
-    N, K = 160, 1024
+    # At M = 4, K = 1024 runs the dp4a GEMV and K = 2048 the tensor-core GEMV.
+    N = 160
     W = synth.gen_q6k(77, N, K)
     blocks = W.reshape(N, K // 256, 210)
     rng = np.random.default_rng(78)
