@@ -47,6 +47,7 @@ xq_status run_matmul(int type, const void* W, const void* xq, int M, int N, int 
       q.K = K;
       q.M_total = M;
       q.chunk = c;
+      q.nch = 1;
       if (n == xq::kMaxProj || c + 1 == L.chunks) {
         if (xq::launch_gemv_mma(type, items, n, s, true) != cudaSuccess) return XQ_ERR_CUDA;
         n = 0;
@@ -101,25 +102,43 @@ int type_index(int type) { return type == XQ_TYPE_Q4_K ? 0 : 1; }
 struct Sched {
   bool dynamic[kTypes];  // the type's grouped GEMV fits one launch: counter and K-split
   size_t arrive[kTypes], partial[kTypes];
+  int nch[64];           // K-chunks per projection (1: not split)
 };
 
 // Projections that go to the grouped tensor-core GEMV at M <= 8.
 bool in_group(const xq_proj& q, int M) { return q.N > 0 && M <= kMaxGemvM && xq::gemv_mma_supports(q.type, q.K); }
 
+// K-chunking of a grouped launch: chunks of ~16 super-blocks for long rows;
+// while the group has fewer 64-row tasks than resident CTAs, halve the chunk
+// length (down to 4) so that every CTA gets work.
+void choose_chunks(const xq_proj* proj, int n_proj, int M, int type, int* nch) {
+  for (int chunk = 16;; chunk /= 2) {
+    long long tasks = 0;
+    for (int p = 0; p < n_proj; ++p) {
+      if (!in_group(proj[p], M) || proj[p].type != type) continue;
+      nch[p] = xq::gemv_split_chunks(proj[p].K, M, chunk);
+      tasks += static_cast<long long>((proj[p].N + 63) / 64) * nch[p];
+    }
+    if (tasks >= xq::kGemvSlots || chunk <= 4) return;
+  }
+}
+
 Sched sched_layout(const xq_proj* proj, int n_proj, int M) {
   Sched sc = {};
   int items[kTypes] = {0, 0};
-  for (int p = 0; p < n_proj; ++p)
+  for (int p = 0; p < n_proj && p < 64; ++p) {
+    sc.nch[p] = 1;
     if (in_group(proj[p], M)) ++items[type_index(proj[p].type)];
-  for (int g = 0; g < kTypes; ++g) sc.dynamic[g] = items[g] > 0 && items[g] <= xq::kMaxProj;
+  }
+  for (int g = 0; g < kTypes; ++g) {
+    sc.dynamic[g] = items[g] > 0 && items[g] <= xq::kMaxProj;
+    if (sc.dynamic[g]) choose_chunks(proj, n_proj, M, g == 0 ? XQ_TYPE_Q4_K : XQ_TYPE_Q6_K, sc.nch);
+  }
   for (int p = 0; p < n_proj; ++p) {
-    if (!in_group(proj[p], M) || !sc.dynamic[type_index(proj[p].type)]) continue;
+    if (!in_group(proj[p], M) || !sc.dynamic[type_index(proj[p].type)] || sc.nch[p] <= 1) continue;
     const int g = type_index(proj[p].type);
-    const int nch = xq::gemv_split_chunks(proj[p].K, M);
-    if (nch > 1) {
-      sc.arrive[g] += xq::gemv_split_arrive_bytes(proj[p].N);
-      sc.partial[g] += xq::gemv_split_partial_bytes(proj[p].N, nch);
-    }
+    sc.arrive[g] += xq::gemv_split_arrive_bytes(proj[p].N);
+    sc.partial[g] += xq::gemv_split_partial_bytes(proj[p].N, sc.nch[p]);
   }
   return sc;
 }
@@ -130,7 +149,7 @@ size_t sched_bytes(const Sched& sc) {
 
 // Validate a layer description and find each input's K (0 = unused).
 xq_status layer_inputs(const xq_proj* proj, int n_proj, int n_inputs, int M, int* in_k) {
-  if (!proj || n_proj < 0 || n_inputs < 0 || n_inputs > 64) return XQ_ERR_ARG;
+  if (!proj || n_proj < 0 || n_proj > 64 || n_inputs < 0 || n_inputs > 64) return XQ_ERR_ARG;
   if (M < 0) return XQ_ERR_SHAPE;
   for (int i = 0; i < n_inputs; ++i) in_k[i] = 0;
   for (int p = 0; p < n_proj; ++p) {
@@ -317,6 +336,7 @@ xq_status xq_layer_mixed(const xq_proj* proj, int n_proj, const float* const* in
         it.K = q.K;
         it.M_total = M;
         it.chunk = 0;
+        it.nch = sc.nch[p];
       }
       if (n > 0 && (n == xq::kMaxProj || p == n_proj)) {
         if (xq::launch_gemv_mma(type, items, n, s, true, counter[g], arrive[g], partial[g]) != cudaSuccess)

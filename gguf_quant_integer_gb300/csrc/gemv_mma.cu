@@ -484,13 +484,36 @@ gemv_mma_kernel(const __grid_constant__ Group G) {
         }
         asm volatile("bar.sync 1, 128;" ::: "memory");
         if (*last_flag && rows_ok) {
+          // chunks added in chunk order (Q6_K, split into more chunks, issues
+          // the loads of 4 chunks at a time)
           float v[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-          for (int c = 0; c < P.nch; ++c) {
-            const float* pc = P.partial + static_cast<size_t>(c) * 8 * rows_pad;
-            v[0] += __ldcg(pc + static_cast<size_t>(c0) * rows_pad + r0);
-            v[1] += __ldcg(pc + static_cast<size_t>(c1) * rows_pad + r0);
-            v[2] += __ldcg(pc + static_cast<size_t>(c0) * rows_pad + r1);
-            v[3] += __ldcg(pc + static_cast<size_t>(c1) * rows_pad + r1);
+          if constexpr (TYPE == 12) {
+            for (int c = 0; c < P.nch; ++c) {
+              const float* pc = P.partial + static_cast<size_t>(c) * 8 * rows_pad;
+              v[0] += __ldcg(pc + static_cast<size_t>(c0) * rows_pad + r0);
+              v[1] += __ldcg(pc + static_cast<size_t>(c1) * rows_pad + r0);
+              v[2] += __ldcg(pc + static_cast<size_t>(c0) * rows_pad + r1);
+              v[3] += __ldcg(pc + static_cast<size_t>(c1) * rows_pad + r1);
+            }
+          } else {
+            for (int c0k = 0; c0k < P.nch; c0k += 4) {
+              float pv[4][4];
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                if (c0k + u < P.nch) {
+                  const float* pc = P.partial + static_cast<size_t>(c0k + u) * 8 * rows_pad;
+                  pv[u][0] = __ldcg(pc + static_cast<size_t>(c0) * rows_pad + r0);
+                  pv[u][1] = __ldcg(pc + static_cast<size_t>(c1) * rows_pad + r0);
+                  pv[u][2] = __ldcg(pc + static_cast<size_t>(c0) * rows_pad + r1);
+                  pv[u][3] = __ldcg(pc + static_cast<size_t>(c1) * rows_pad + r1);
+                }
+              }
+#pragma unroll
+              for (int u = 0; u < 4; ++u)
+                if (c0k + u < P.nch)
+#pragma unroll
+                  for (int e = 0; e < 4; ++e) v[e] += pv[u][e];
+            }
           }
           store_y(P, rg, n8, t, v[0], v[1], v[2], v[3]);
         }
@@ -577,7 +600,7 @@ cudaError_t launch_gemv_mma(int type, const MmaProj* projs, int n, cudaStream_t 
   const bool split = arrive_ws != nullptr && partial_ws != nullptr;
   int nch[kMaxProj], cost[kMaxProj];
   for (int k = 0; k < n; ++k) {
-    nch[k] = split ? gemv_split_chunks(projs[k].K, projs[k].M_total) : 1;
+    nch[k] = (split && projs[k].nch > 1) ? projs[k].nch : 1;
     cost[k] = ((projs[k].K >> 8) + nch[k] - 1) / nch[k];
   }
   // Most expensive tasks first (dynamic scheduling takes them in order).

@@ -157,6 +157,7 @@ cudaError_t launch_quantize_q8(const QuantJob* jobs, int n, cudaStream_t s, bool
                                unsigned int* zero_words = nullptr, int zero_count = 0);
 
 struct MmaProj {
+  int nch;             // K-chunks when split workspaces are given (0 or 1: none)
   const uint8_t* W;    // super-blocks [N][K/256]
   const uint8_t* xq;   // Q8 buffer of this projection's input (M_total tokens)
   float* y;            // [M_total][N]; this launch writes tokens 8*chunk .. 8*chunk+7
@@ -165,11 +166,17 @@ struct MmaProj {
 };
 
 // K-chunks a projection's rows are split into when a split workspace is
-// available: rows of more than 24 super-blocks go in chunks of ~16.
-__host__ __device__ inline int gemv_split_chunks(int K, int M_total) {
+// available, for a chunk length of `chunk` super-blocks: rows longer than
+// 24 super-blocks (or than `chunk`, once the chunk length drops below 16)
+// go in ceil(nsb / chunk) chunks.
+__host__ __device__ inline int gemv_split_chunks(int K, int M_total, int chunk = 16) {
   const int nsb = K >> 8;
-  return (M_total <= 8 && nsb > 24) ? (nsb + 15) / 16 : 1;
+  if (M_total > 8) return 1;
+  const int limit = chunk >= 16 ? 24 : chunk;
+  return nsb > limit ? (nsb + chunk - 1) / chunk : 1;
 }
+// Resident CTAs of the grouped GEMV (3 per SM for both weight types).
+constexpr int kGemvSlots = 3 * kNumSMs;
 // Workspace of a split projection: partial sums [nch][8][64 * row blocks]
 // and one arrival count per 64-row block (both rounded to 256 bytes).
 __host__ __device__ inline size_t gemv_split_partial_bytes(int N, int nch) {
