@@ -45,6 +45,10 @@ FALLBACK_HBM_GBS = 6800.0
 HEADLINE = "llama3-8b-32layer"
 
 
+# workloads --profile-workload runs (one launch per call)
+PROFILE_WORKLOADS = ("prefill512-up", "prefill512-down", "qwen3-q6k-layer", "llama3-layer")
+
+
 def parse_args(argv=None):
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
@@ -58,6 +62,8 @@ def parse_args(argv=None):
     p.add_argument("--cpu-sample-layers", type=int, default=8)
     p.add_argument("--layers", type=int, default=0,
                    help="run only the first L layers of the sweep (0 = all; small cases for ncu)")
+    p.add_argument("--profile-workload", choices=sorted(PROFILE_WORKLOADS), default=None,
+                   help="run one workload's launches (warmup + steps) without timing, for ncu captures")
     return p.parse_args(argv)
 
 
@@ -369,20 +375,29 @@ def per_layer_times(sweep, M, reps=3):
     return [t / reps for t in tot]
 
 
+# Sources the grouped GEMV kernel is built from: a recorded ncu traffic
+# figure stays valid only while these files are unchanged.
+GEMV_SOURCES = ("gemv_mma.cu", "xq_common.cuh", "xq_ptx.cuh")
+
+
+def kernel_source_hash(names=GEMV_SOURCES) -> str:
+    import hashlib
+    src = os.path.join(ROOT, "gguf_quant_integer_gb300", "csrc")
+    h = hashlib.sha256()
+    for name in names:
+        with open(os.path.join(src, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
 def read_ncu_traffic(kernel_key: str):
     """Per-launch DRAM bytes of `kernel_key` from the committed ncu summary,
-    valid only if the kernel source hash recorded there matches the current one."""
-    import hashlib
+    valid only if the hash of the kernel's sources recorded there matches the
+    current one."""
     path = os.path.join(ROOT, "profiles", "traffic.md")
     if not os.path.exists(path):
         return None
-    src = os.path.join(ROOT, "gguf_quant_integer_gb300", "csrc")
-    h = hashlib.sha256()
-    for name in sorted(os.listdir(src)):
-        if name.endswith((".cu", ".cuh")):
-            with open(os.path.join(src, name), "rb") as f:
-                h.update(f.read())
-    digest = h.hexdigest()[:16]
+    digest = kernel_source_hash()
     with open(path) as f:
         for line in f:
             parts = line.strip().strip("|").split("|")
@@ -444,10 +459,10 @@ def gpu_arm(args):
     layer_bytes = wl.layer_weight_bytes()
     avg = sum(lts) / len(lts)
     achieved = layer_bytes / avg / 1e9
-    tr = read_ncu_traffic(f"gemv_q4k_mma_layer_M{M}")
+    tr = read_ncu_traffic(f"gemv_mma_q4k_layer_M{M}")
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "peak_source": peak_kind,
-                "kernel": "gemv_q4k_mma_kernel, one grouped launch per layer (timed with its quantize launch)",
+                "kernel": "gemv_mma_kernel<Q4_K>, one grouped launch per layer (timed with its quantize launch)",
                 "bytes_per_launch": layer_bytes, "avg_launch_us": round(1e6 * avg, 3),
                 "traffic": (round(tr[0]) if tr else None),
                 "traffic_note": (tr[1] if tr else "no ncu capture of the current kernel source")}
@@ -592,10 +607,52 @@ def secondary_workloads(device, world):
     return out
 
 
+def profile_workload(args):
+    """Run the launches of one named workload `warmup + steps` times and exit.
+    No timing: the process exists to be captured by ncu (one launch per call
+    of the workload: one grouped layer GEMV, or one tile-kernel matmul)."""
+    import torch
+    from gguf_quant_integer_gb300 import xq
+    device = torch.device("cuda")
+    name = args.profile_workload
+    if name in ("prefill512-up", "prefill512-down"):
+        wl = synth.WORKLOADS["qwen3-8b-ffn-prefill512"]
+        p = wl.projs[0 if name.endswith("up") else 1]
+        t = wl.projs.index(p)
+        M = 512
+        W = torch.from_numpy(synth.gen_layer_weights(wl, 0)[t].reshape(-1)).to(device)
+        x = torch.from_numpy(synth.gen_layer_inputs(wl, M, 0)[p.input]).to(device)
+        buf = xq.quantize_q8(x)
+        y = torch.empty((M, p.N), dtype=torch.float32, device=device)
+        run = lambda: xq.matmul(p.qtype, W, buf, M, p.N, p.K, y=y)
+    else:
+        wl = synth.WORKLOADS["qwen3-8b-mixed-layer" if name == "qwen3-q6k-layer" else "llama3-8b-32layer"]
+        keep = [t for t, p in enumerate(wl.projs) if name != "qwen3-q6k-layer" or p.qtype == synth.Q6_K]
+        M = args.m
+        weights = synth.gen_layer_weights(wl, 0)
+        inputs = synth.gen_layer_inputs(wl, M, 0)
+        projs = [wl.projs[t] for t in keep]
+        used = sorted({p.input for p in projs})
+        remap = {i: k for k, i in enumerate(used)}
+        Wd = [torch.from_numpy(weights[t].reshape(-1)).to(device) for t in keep]
+        xs = [torch.from_numpy(inputs[i]).to(device) for i in used]
+        ys = [torch.empty((M, p.N), dtype=torch.float32, device=device) for p in projs]
+        desc = [(p.qtype, p.N, p.K, Wd[k], ys[k], remap[p.input]) for k, p in enumerate(projs)]
+        ws = torch.empty(xq.layer_workspace_bytes(desc, len(xs), M), dtype=torch.uint8, device=device)
+        run = lambda: xq.layer_mixed(desc, xs, M, ws)
+    for _ in range(args.warmup + args.steps):
+        run()
+    torch.cuda.synchronize()
+    print(f"profile workload {name}: {args.warmup + args.steps} calls done", flush=True)
+    return 0
+
+
 def main(argv=None):
     args = parse_args(argv)
     if args.impl == "reference":
         return reference_arm(args)
+    if args.profile_workload:
+        return profile_workload(args)
     return gpu_arm(args)
 
 
