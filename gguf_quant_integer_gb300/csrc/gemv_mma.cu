@@ -41,8 +41,11 @@
 // operands of that super-block (two 1D bulk copies, 4.6 KB), which all four
 // warps share. The producer writes each stage's task id and runs ahead
 // across tasks through a 4-stage ring guarded by mbarriers, with no
-// CTA-wide barrier. Tasks come from a static stride, or, when a work counter
-// is given, from an atomic counter over a list ordered by cost. Long rows
+// CTA-wide barrier. Each CTA's first task is its own index; later tasks come
+// from a static stride, or, when a work counter is given, from an atomic
+// counter over a list ordered by cost. The weight boxes of the first task's
+// first stages are requested before the kernel waits for the previous grid
+// on the stream (which writes the activation image and zeroes the counter). Long rows
 // (more than 24 super-blocks) can be split into K-chunks of about 16
 // super-blocks handled by different CTAs: each writes its partial sums to a
 // workspace, and the last CTA to finish a 64-row block (an atomic arrival
@@ -352,8 +355,10 @@ __device__ __forceinline__ void store_y(const Proj& P, int rg, int n8, int t, fl
   }
 }
 
+// Tasks after each CTA's first (its own index): from the counter, which
+// starts at zero, offset by the grid size; or strided by the grid size.
 __device__ __forceinline__ int next_task(const Group& G, int cur) {
-  if (G.counter) return static_cast<int>(atomicAdd(G.counter, 1u));
+  if (G.counter) return static_cast<int>(gridDim.x + atomicAdd(G.counter, 1u));
   return cur + static_cast<int>(gridDim.x);
 }
 
@@ -382,23 +387,57 @@ gemv_mma_kernel(const __grid_constant__ Group G) {
     mbar_init_fence();
   }
   __syncthreads();
-  // The activation image, the task counter and the arrival counts may be
-  // written by the previous grid on the stream: wait for it first.
-  cudaGridDependencySynchronize();
-  cudaTriggerProgrammaticLaunchCompletion();
-
   if (warp == 4) {
     // ------------------------------------------------------- producer
     if (lane != 0) return;
-    int task = G.counter ? static_cast<int>(atomicAdd(G.counter, 1u)) : static_cast<int>(blockIdx.x);
+    // Each CTA's first task is its own index; later tasks come from the
+    // counter (or a stride). The weights do not depend on the previous grid
+    // on the stream, so the weight boxes of the first task's first stages are
+    // requested before waiting for it; the activation image, the task
+    // counter and the arrival counts may be written by that grid.
+    int task = static_cast<int>(blockIdx.x);
     int slot = 0;
     unsigned fills = 0;  // completed passes over the ring
+    int bresume = -1;    // first super-block of the first task not yet requested
+    if (task < G.total) {
+      const TaskPos tp = task_pos(G, task);
+      const Proj& P = G.p[tp.p];
+      const int rows = P.N - tp.rb * 64;
+      const int nblk = rows >= 64 ? 4 : (rows + 15) / 16;
+      int b = tp.b0;
+      for (; b < tp.b1 && slot < kStages; ++b, ++slot) {
+        meta[slot] = make_int4(task, b, (b == tp.b1 - 1) ? 1 : 0, 0);
+        mbar_expect_tx(full_s + 8 * slot, static_cast<unsigned>(nblk * kBlockBytes + 8 * 512 + 8 * 64));
+        const uint32_t st = ring_s + slot * kStageBytes;
+        for (int w = 0; w < nblk; ++w)
+          tma_load_2d(st + w * kBlockBytes, &P.map, TYPE == 12 ? b * (kQ4kBytes / 8) : ((kQ6kBytes * b) & ~15),
+                      tp.rb * 64 + 16 * w, full_s + 8 * slot);
+      }
+      bresume = b;
+    }
+    cudaGridDependencySynchronize();
+    cudaTriggerProgrammaticLaunchCompletion();
+    if (task < G.total) {
+      const TaskPos tp = task_pos(G, task);
+      const Proj& P = G.p[tp.p];
+      for (int k = 0; k < slot; ++k) {
+        const uint32_t st = ring_s + k * kStageBytes;
+        bulk_load(st + kFragOff, P.frag + static_cast<size_t>(tp.b0 + k) * 8 * 512, 8 * 512, full_s + 8 * k);
+        bulk_load(st + kFscOff, P.fsc + static_cast<size_t>(tp.b0 + k) * 8 * 64, 8 * 64, full_s + 8 * k);
+      }
+    }
+    if (slot == kStages) {
+      slot = 0;
+      fills = 1;
+    }
     for (;;) {
       const bool valid = task < G.total;
       TaskPos tp = {0, 0, 0, 1, 0};
       if (valid) tp = task_pos(G, task);
       const int nxt = valid ? next_task(G, task) : task;
-      for (int b = tp.b0; b < tp.b1; ++b) {
+      const int bfirst = bresume >= 0 ? bresume : tp.b0;
+      bresume = -1;
+      for (int b = bfirst; b < tp.b1; ++b) {
         if (fills > 0 && !mbar_wait(empty_s + 8 * slot, (fills - 1) & 1, 1)) return;
         meta[slot] = make_int4(valid ? task : -1, b, (b == tp.b1 - 1) ? 1 : 0, 0);
         if (!valid) {
@@ -425,6 +464,8 @@ gemv_mma_kernel(const __grid_constant__ Group G) {
   }
 
   // --------------------------------------------------------- consumers
+  cudaGridDependencySynchronize();
+  cudaTriggerProgrammaticLaunchCompletion();
   const int n8 = lane >> 2, t = lane & 3;
   float4* dec = dec_all + warp * (kDecBytes / 16);
   f2 acc[2] = {0ull, 0ull};
