@@ -290,9 +290,24 @@ class Sweep:
             xq.layer_mixed(descs[l], ins[l], M, ws)
 
     def launches_per_step(self, M):
-        chunks = (M + 7) // 8
+        """Kernel launches of one step, following xq_layer_mixed's dispatch:
+        one quantize launch per 8 inputs; for M <= 8 one grouped GEMV launch
+        per weight type and 8 projections, plus one dp4a launch per Q6_K
+        projection whose rows are not 16-byte multiples; for M > 8 one tile
+        launch per projection."""
         used = len({p.input for p in self.wl.projs})
-        return len(self.W) * (used + chunks * len(self.wl.projs))
+        per_layer = -(-used // 8)
+        if M > 8:
+            per_layer += len(self.wl.projs)
+        else:
+            grouped = {synth.Q4_K: 0, synth.Q6_K: 0}
+            for p in self.wl.projs:
+                if p.qtype == synth.Q4_K or (p.K // 256) % 8 == 0:
+                    grouped[p.qtype] += 1
+                else:
+                    per_layer += 1
+            per_layer += sum(-(-n // 8) for n in grouped.values())
+        return len(self.W) * per_layer
 
     def bytes_per_step(self):
         return len(self.W) * self.wl.layer_weight_bytes()
