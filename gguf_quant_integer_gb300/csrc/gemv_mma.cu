@@ -147,14 +147,15 @@ __device__ __forceinline__ TaskPos task_pos(const Group& G, int task) {
 }
 
 // Decode the 16 rows' scales of one super-block into the warp's table:
-// lane l takes weight row l/2 and sub-blocks 4*(l&1) .. +3, writing
+// lane l takes weight row l%16 and sub-blocks 4*(l/16) .. +3, writing
 // (alpha, alpha, beta, beta) with alpha = d*sc*2^24 (low nibbles) or
 // d*sc*2^20 (high), beta = -dmin*m, each as (2^23 + byte)*x - 2^23*x: one
 // rounding of an exact product. Packed bytes (public Q4_K layout):
 //   j < 4 : sc = s[j] & 63, m = s[j+4] & 63
 //   j >= 4: sc = (s[j+4] & 15) | (s[j-4] >> 6) << 4, m = (s[j+4] >> 4) | (s[j] >> 6) << 4
+// Each half-warp's stores cover 256 consecutive bytes (no bank conflicts).
 __device__ __forceinline__ void decode_scales_q4(const uint8_t* blk, float4* dec, int lane) {
-  const int r = lane >> 1, half = lane & 1;
+  const int r = lane & 15, half = lane >> 4;
   const uint4 hd = *reinterpret_cast<const uint4*>(blk + r * kQ4kBytes);
   const unsigned scw = half ? ((hd.w & 0x0F0F0F0Fu) | ((hd.y >> 2) & 0x30303030u)) : (hd.y & 0x3F3F3F3Fu);
   const unsigned mnw = half ? (((hd.w >> 4) & 0x0F0F0F0Fu) | ((hd.z >> 2) & 0x30303030u)) : (hd.z & 0x3F3F3F3Fu);
@@ -189,12 +190,12 @@ __device__ __forceinline__ void load_words(const uint8_t* p, uint32_t (&out)[NW]
 
 // Q6_K (public layout: ql[128] @0, qh[64] @128, int8 scales[16] @192, d @208;
 // the super-block starts `off` bytes into the row's window). Lane l takes
-// weight row l/2 and 32-blocks 4*(l&1) .. +3, writing for each 32-block p
+// weight row l%16 and 32-blocks 4*(l/16) .. +3, writing for each 32-block p
 // (alpha_2p, alpha_2p, alpha_2p+1, alpha_2p+1), alpha_g = d * s_g (one
 // rounding of an exact product): the coefficients of the two 16-weight
-// groups of p.
+// groups of p. Each half-warp's stores cover 256 consecutive bytes.
 __device__ __forceinline__ void decode_scales_q6(const uint8_t* blk, int off, float4* dec, int lane) {
-  const int r = lane >> 1, half = lane & 1;
+  const int r = lane & 15, half = lane >> 4;
   const uint8_t* sb = blk + r * GLay<14>::kBoxRow + off;
   uint32_t sw[2];
   load_words<2>(sb + 192 + 8 * half, sw);
