@@ -31,24 +31,35 @@ __device__ __forceinline__ int tile_offset(int r, int ks) {
   return (r >> 3) * 512 + (ks >> 3) * 128 + (r & 7) * 16 + (ks & 7) * 2;
 }
 
+// One input of a grouped launch, with its buffer layout resolved on the host.
+struct QuantItem {
+  const float* x;
+  uint8_t* xq;
+  size_t d8, s8, frag, fsc, tile;  // byte offsets in xq (layout in xq_common.cuh)
+  int M, K, nsub, ttiles;
+};
+
 struct QuantGroup {
-  QuantJob job[kMaxProj];
-  long long blk0[kMaxProj + 1];  // prefix of padded 32-blocks per job
-  unsigned int* zero_words;      // optional: words set to 0 (the next matmul's scheduling state)
+  QuantItem job[kMaxProj];
+  unsigned blk0[kMaxProj + 1];  // prefix of padded 32-blocks per input
+  unsigned int* zero_words;     // optional: words set to 0 (the next matmul's scheduling state)
   int zero_count;
   int n;
 };
 
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(1024)
 quantize_q8_kernel(const __grid_constant__ QuantGroup G) {
-  // Inputs may be written by the previous kernel on the stream.
+  // Inputs may be written by the previous kernel on the stream. The next
+  // kernel may launch at once: it waits for this grid's completion before
+  // reading what it writes.
   cudaGridDependencySynchronize();
+  cudaTriggerProgrammaticLaunchCompletion();
   if (blockIdx.x == 0)
     for (int i = threadIdx.x; i < G.zero_count; i += blockDim.x) G.zero_words[i] = 0u;
   const int lane = threadIdx.x & 31;
-  const long long warp = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-  const long long nwarps = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
-  const long long total = G.blk0[G.n];
+  const unsigned warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const unsigned nwarps = (gridDim.x * blockDim.x) >> 5;
+  const unsigned total = G.blk0[G.n];
   // Position of this lane's element inside its lane's 8 operand slots:
   // slot order is perm = 0,2,1,3,4,6,5,7 (an involution), so slot = perm[l & 7].
   const int t = lane >> 3;
@@ -56,14 +67,14 @@ quantize_q8_kernel(const __grid_constant__ QuantGroup G) {
   const int slot = (i == 1 || i == 2 || i == 5 || i == 6) ? (i ^ 3) : i;
 
   int jb = 0;
-  for (long long blk = warp; blk < total; blk += nwarps) {
+  for (unsigned blk = warp; blk < total; blk += nwarps) {
     while (blk >= G.blk0[jb + 1]) ++jb;
-    const QuantJob& J = G.job[jb];
-    const long long local = blk - G.blk0[jb];
-    const int nsub = J.K >> 5;
-    const int m = static_cast<int>(local / nsub);
-    const int j = static_cast<int>(local - static_cast<long long>(m) * nsub);
-    const Q8Layout L = q8_layout(J.M, J.K);
+    const QuantItem& J = G.job[jb];
+    const unsigned local = blk - G.blk0[jb];
+    const int nsub = J.nsub;
+    const int m = static_cast<int>(local / static_cast<unsigned>(nsub));
+    const int j = static_cast<int>(local - static_cast<unsigned>(m) * nsub);
+    const QuantItem& L = J;
 
     float d = 0.0f, s = 0.0f;
     int q = 0;
@@ -82,7 +93,7 @@ quantize_q8_kernel(const __grid_constant__ QuantGroup G) {
       q = static_cast<int>(r);
       const int isum = __reduce_add_sync(0xffffffffu, q);
       s = __fmul_rn(d, static_cast<float>(isum));
-      J.xq[L.qs + static_cast<size_t>(m) * J.K + 32 * j + lane] = static_cast<uint8_t>(static_cast<int8_t>(q));
+      J.xq[static_cast<size_t>(m) * J.K + 32 * j + lane] = static_cast<uint8_t>(static_cast<int8_t>(q));
       if (lane == 0) {
         reinterpret_cast<float*>(J.xq + L.d8)[static_cast<size_t>(m) * nsub + j] = d;
         reinterpret_cast<float*>(J.xq + L.s8)[static_cast<size_t>(m) * nsub + j] = s;
@@ -122,7 +133,6 @@ quantize_q8_kernel(const __grid_constant__ QuantGroup G) {
       }
     }
   }
-  cudaTriggerProgrammaticLaunchCompletion();
 }
 
 cudaError_t launch_quantize_q8(const QuantJob* jobs, int n, cudaStream_t s, bool pdl, unsigned int* zero_words,
@@ -133,19 +143,34 @@ cudaError_t launch_quantize_q8(const QuantJob* jobs, int n, cudaStream_t s, bool
   G.zero_words = zero_words;
   G.zero_count = zero_words ? zero_count : 0;
   G.blk0[0] = 0;
+  long long nblocks = 0;
   for (int k = 0; k < n; ++k) {
-    G.job[k] = jobs[k];
+    const QuantJob& q = jobs[k];
+    const Q8Layout L = q8_layout(q.M, q.K);
+    QuantItem& it = G.job[k];
+    it.x = q.x;
+    it.xq = q.xq;
+    it.d8 = L.d8;
+    it.s8 = L.s8;
+    it.frag = L.frag;
+    it.fsc = L.fsc;
+    it.tile = L.tile;
+    it.M = q.M;
+    it.K = q.K;
+    it.nsub = q.K / 32;
+    it.ttiles = L.ttiles;
     // padded token count: the operand image's chunk (8) or tile (128)
-    const long long mp = jobs[k].M > 8 ? 128LL * ((jobs[k].M + 127) / 128) : 8LL * ((jobs[k].M + 7) / 8);
-    G.blk0[k + 1] = G.blk0[k] + mp * (jobs[k].K / 32);
+    const long long mp = q.M > 8 ? 128LL * ((q.M + 127) / 128) : 8LL * ((q.M + 7) / 8);
+    nblocks += mp * (q.K / 32);
+    if (nblocks >= (1LL << 31)) return cudaErrorInvalidValue;
+    G.blk0[k + 1] = static_cast<unsigned>(nblocks);
   }
-  const long long nblocks = G.blk0[n];
   if (nblocks == 0) return cudaSuccess;
-  long long want = (nblocks + 7) / 8;  // 8 warps per CTA, one block per warp
-  const long long cap = static_cast<long long>(kNumSMs) * 16;
+  long long want = (nblocks + 31) / 32;  // 32 warps per CTA, one block per warp
+  const long long cap = static_cast<long long>(kNumSMs) * 2;  // all resident
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(want < cap ? want : cap));
-  cfg.blockDim = dim3(256);
+  cfg.blockDim = dim3(1024);
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
