@@ -25,12 +25,14 @@ xq_status check_shape(int M, int N, int K) {
 // Enqueue y = x W^T. M > 8: the tensor-memory tile kernel (both types).
 // M <= 8: the warp-level MMA GEMV (8-token chunks, up to kMaxProj chunks per
 // launch) for Q4_K and for Q6_K rows that are 16-byte multiples; the dp4a
-// GEMV for the other Q6_K shapes.
+// GEMV for the other Q6_K shapes. invariant: every M in 8-token GEMV chunks
+// from the GEMV-image layout, never split over K, so that each token's row
+// of y is computed by the same operations whatever M is.
 xq_status run_matmul(int type, const void* W, const void* xq, int M, int N, int K, float* y,
-                     int32_t* isum, cudaStream_t s) {
-  const xq::Q8Layout L = xq::q8_layout(M, K);
+                     int32_t* isum, cudaStream_t s, bool invariant = false) {
+  const xq::Q8Layout L = xq::q8_layout(M, K, invariant);
   const uint8_t* base = static_cast<const uint8_t*>(xq);
-  if (M > kMaxGemvM) {
+  if (M > kMaxGemvM && !invariant) {
     const cudaError_t e = xq::launch_tile_mma(type, static_cast<const uint8_t*>(W), base, M, N, K, y, s, true);
     return e == cudaSuccess ? XQ_OK : XQ_ERR_CUDA;
   }
@@ -48,6 +50,7 @@ xq_status run_matmul(int type, const void* W, const void* xq, int M, int N, int 
       q.M_total = M;
       q.chunk = c;
       q.nch = 1;
+      q.gemv_image = invariant;
       if (n == xq::kMaxProj || c + 1 == L.chunks) {
         if (xq::launch_gemv_mma(type, items, n, s, true) != cudaSuccess) return XQ_ERR_CUDA;
         n = 0;
@@ -185,6 +188,37 @@ size_t xq_q8_bytes(int M, int K) {
   if (M < 0 || K <= 0 || (K % 32) != 0) return 0;
   if (M > kMaxGemvM && (K % 256) != 0) return 0;  // the tile image is per super-block
   return xq::q8_layout(M, K).total;
+}
+
+size_t xq_q8_bytes_invariant(int M, int K) {
+  if (M < 0 || K <= 0 || (K % 32) != 0) return 0;
+  return xq::q8_layout(M, K, true).total;
+}
+
+xq_status xq_quantize_q8_invariant(const float* x, int M, int K, void* xq, xq_stream stream) {
+  if (M < 0 || K <= 0 || (K % 256) != 0) return XQ_ERR_SHAPE;
+  if (M == 0) return XQ_OK;
+  if (!x || !xq) return XQ_ERR_ARG;
+  if (!aligned16(x) || !aligned16(xq)) return XQ_ERR_ALIGN;
+  xq::QuantJob job;
+  job.x = x;
+  job.xq = static_cast<uint8_t*>(xq);
+  job.M = M;
+  job.K = K;
+  job.gemv_image = true;
+  const cudaError_t e = xq::launch_quantize_q8(&job, 1, reinterpret_cast<cudaStream_t>(stream), true);
+  return e == cudaSuccess ? XQ_OK : XQ_ERR_CUDA;
+}
+
+xq_status xq_matmul_invariant(int type, const void* W, const void* xq, int M, int N, int K, float* y,
+                              xq_stream stream) {
+  if (block_bytes(type) == 0) return XQ_ERR_ARG;
+  xq_status st = check_shape(M, N, K);
+  if (st != XQ_OK) return st;
+  if (M == 0 || N == 0) return XQ_OK;
+  if (!W || !xq || !y) return XQ_ERR_ARG;
+  if (!aligned16(W) || !aligned16(xq) || !aligned16(y)) return XQ_ERR_ALIGN;
+  return run_matmul(type, W, xq, M, N, K, y, nullptr, reinterpret_cast<cudaStream_t>(stream), true);
 }
 
 size_t xq_weight_bytes(int type, int N, int K) {

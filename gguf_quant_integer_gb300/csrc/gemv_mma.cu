@@ -674,7 +674,7 @@ cudaError_t launch_gemv_mma(int type, const MmaProj* projs, int n, cudaStream_t 
   for (int k = 0; k < n; ++k) {
     const int src = order[k];
     const MmaProj& q = projs[src];
-    const Q8Layout L = q8_layout(q.M_total, q.K);
+    const Q8Layout L = q8_layout(q.M_total, q.K, q.gemv_image);
     const int m0 = 8 * q.chunk;
     Proj& P = G.p[k];
     if (!gemv_mma_supports(type, q.K) || !encode_weight_map(type, &P.map, q.W, q.N, q.K)) return cudaErrorInvalidValue;

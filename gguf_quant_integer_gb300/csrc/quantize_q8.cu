@@ -146,7 +146,7 @@ cudaError_t launch_quantize_q8(const QuantJob* jobs, int n, cudaStream_t s, bool
   long long nblocks = 0;
   for (int k = 0; k < n; ++k) {
     const QuantJob& q = jobs[k];
-    const Q8Layout L = q8_layout(q.M, q.K);
+    const Q8Layout L = q8_layout(q.M, q.K, q.gemv_image);
     QuantItem& it = G.job[k];
     it.x = q.x;
     it.xq = q.xq;
@@ -160,7 +160,7 @@ cudaError_t launch_quantize_q8(const QuantJob* jobs, int n, cudaStream_t s, bool
     it.nsub = q.K / 32;
     it.ttiles = L.ttiles;
     // padded token count: the operand image's chunk (8) or tile (128)
-    const long long mp = q.M > 8 ? 128LL * ((q.M + 127) / 128) : 8LL * ((q.M + 7) / 8);
+    const long long mp = (q.M > 8 && !q.gemv_image) ? 128LL * ((q.M + 127) / 128) : 8LL * ((q.M + 7) / 8);
     nblocks += mp * (q.K / 32);
     if (nblocks >= (1LL << 31)) return cudaErrorInvalidValue;
     G.blk0[k + 1] = static_cast<unsigned>(nblocks);

@@ -107,14 +107,16 @@ struct Q8Layout {
   int ttiles;  // 128-token tiles of the tile image (M > 8), else 0
 };
 
-__host__ __device__ inline Q8Layout q8_layout(int M, int K) {
+// gemv_image: the M <= 8 layout (8-token chunks of the GEMV image) for any M;
+// the batch-invariant entry points use it.
+__host__ __device__ inline Q8Layout q8_layout(int M, int K, bool gemv_image = false) {
   Q8Layout L;
   const size_t mk = static_cast<size_t>(M) * K;
   L.qs = 0;
   L.d8 = mk;
   L.s8 = mk + 4 * (mk / 32);
   const size_t F = (mk + 8 * (mk / 32) + 255) & ~static_cast<size_t>(255);
-  if (M <= 8) {
+  if (M <= 8 || gemv_image) {
     L.chunks = (M + 7) / 8;
     L.ttiles = 0;
     L.frag = F;
@@ -148,6 +150,7 @@ struct QuantJob {
   const float* x;   // fp32 [M][K]
   uint8_t* xq;      // Q8 buffer (layout above)
   int M, K;
+  bool gemv_image = false;  // 8-token GEMV image for any M (batch-invariant layout)
 };
 
 // One launch quantizing up to kMaxProj activations; also zeroes the
@@ -158,6 +161,7 @@ cudaError_t launch_quantize_q8(const QuantJob* jobs, int n, cudaStream_t s, bool
 
 struct MmaProj {
   int nch;             // K-chunks when split workspaces are given (0 or 1: none)
+  bool gemv_image = false;  // the Q8 buffer uses the GEMV image for M_total > 8 too
   const uint8_t* W;    // super-blocks [N][K/256]
   const uint8_t* xq;   // Q8 buffer of this projection's input (M_total tokens)
   float* y;            // [M_total][N]; this launch writes tokens 8*chunk .. 8*chunk+7

@@ -24,7 +24,8 @@ STATUS = {0: "XQ_OK", 1: "XQ_ERR_ARG", 2: "XQ_ERR_SHAPE", 3: "XQ_ERR_ALIGN",
 # Every symbol include/xq.h declares.
 SYMBOLS = ("xq_status_str", "xq_q8_bytes", "xq_weight_bytes", "xq_quantize_q8",
            "xq_matmul_q4k_q8", "xq_matmul_q6k_q8", "xq_layer_workspace_bytes",
-           "xq_layer_mixed", "xq_debug_isums_q4k", "xq_debug_isums_q6k", "xq_layer_mixed_static")
+           "xq_layer_mixed", "xq_debug_isums_q4k", "xq_debug_isums_q6k", "xq_layer_mixed_static",
+           "xq_q8_bytes_invariant", "xq_quantize_q8_invariant", "xq_matmul_invariant")
 
 
 class XQError(RuntimeError):
@@ -59,6 +60,12 @@ def lib(path: str | None = None):
     L.xq_weight_bytes.argtypes = [I, I, I]
     L.xq_weight_bytes.restype = S
     L.xq_quantize_q8.argtypes = [P, I, I, P, P]
+    L.xq_q8_bytes_invariant.argtypes = [I, I]
+    L.xq_q8_bytes_invariant.restype = S
+    L.xq_quantize_q8_invariant.argtypes = [P, I, I, P, P]
+    L.xq_quantize_q8_invariant.restype = I
+    L.xq_matmul_invariant.argtypes = [I, P, P, I, I, I, P, P]
+    L.xq_matmul_invariant.restype = I
     for fn in ("xq_matmul_q4k_q8", "xq_matmul_q6k_q8"):
         getattr(L, fn).argtypes = [P, P, I, I, I, P, P]
     for fn in ("xq_debug_isums_q4k", "xq_debug_isums_q6k"):
@@ -137,6 +144,31 @@ def matmul_q4k_q8(W, xq, M, N, K, y=None, stream=None):
 
 def matmul_q6k_q8(W, xq, M, N, K, y=None, stream=None):
     return matmul(XQ_TYPE_Q6_K, W, xq, M, N, K, y, stream)
+
+
+def q8_bytes_invariant(M: int, K: int) -> int:
+    return lib().xq_q8_bytes_invariant(M, K)
+
+
+def quantize_q8_invariant(x, out=None, stream=None):
+    """Q8-quantize fp32 x [M, K] into the 8-token GEMV image for any M (the
+    batch-invariant layout)."""
+    import torch
+    M, K = x.shape
+    if out is None:
+        out = torch.empty(q8_bytes_invariant(M, K), dtype=torch.uint8, device=x.device)
+    _check("xq_quantize_q8_invariant", lib().xq_quantize_q8_invariant(_ptr(x), M, K, _ptr(out), _stream(stream)))
+    return out
+
+
+def matmul_invariant(qtype: int, W, xq, M: int, N: int, K: int, y=None, stream=None):
+    """y [M, N] = x W^T with row m independent of M (batch-invariant mode)."""
+    import torch
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float32, device=W.device)
+    _check("xq_matmul_invariant",
+           lib().xq_matmul_invariant(qtype, _ptr(W), _ptr(xq), M, N, K, _ptr(y), _stream(stream)))
+    return y
 
 
 def debug_isums(qtype: int, W, xq, M: int, N: int, K: int, y=None, isum=None, stream=None):

@@ -135,6 +135,23 @@ XQ_API xq_status xq_matmul_q4k_q8(const void *W, const void *xq, int M, int N, i
 XQ_API xq_status xq_matmul_q6k_q8(const void *W, const void *xq, int M, int N, int K,
                            float *y, xq_stream stream);
 
+/* Batch-invariant mode (speculative-decoding verification: the rows of y for
+ * a batch of M tokens must equal those of decoding each token alone).
+ * xq_matmul_q4k_q8 / _q6k_q8 are invariant for M <= 8 (every token of an
+ * 8-token chunk goes through the same operations), but M > 8 switches to
+ * the tile kernel, whose fp32 combine runs in another order. These entry
+ * points keep the M <= 8 arithmetic for every M: the activations hold the
+ * 8-token GEMV image for all ceil(M/8) chunks (xq_q8_bytes_invariant bytes:
+ * the M <= 8 layout above with C = ceil(M/8)), and the matmul runs the GEMV
+ * chunk by chunk, never split over K. Row m of y is then bit-identical for
+ * every M >= m+1, and to xq_matmul_* at M <= 8 on the same activations.
+ * Arguments and errors as for xq_quantize_q8 and xq_matmul_*; type is
+ * XQ_TYPE_Q4_K or XQ_TYPE_Q6_K. */
+XQ_API size_t xq_q8_bytes_invariant(int M, int K);
+XQ_API xq_status xq_quantize_q8_invariant(const float *x, int M, int K, void *xq, xq_stream stream);
+XQ_API xq_status xq_matmul_invariant(int type, const void *W, const void *xq, int M, int N, int K,
+                                     float *y, xq_stream stream);
+
 /* One projection of a transformer layer for xq_layer_mixed. */
 typedef struct {
     int type;        /* XQ_TYPE_Q4_K or XQ_TYPE_Q6_K */

@@ -49,6 +49,12 @@ def test_sizes(L):
     assert L.xq_q8_bytes(1, 100) == 0
     assert L.xq_q8_bytes(8, 288) > 0      # M <= 8 needs K % 32 only
     assert L.xq_q8_bytes(9, 288) == 0     # the tile image is per 256-feature super-block
+    # batch-invariant layout: the GEMV image for every 8-token chunk, any M
+    for M, K in ((1, 2048), (8, 4096), (9, 256), (129, 1536), (512, 12288), (0, 256)):
+        base = -(-int(1.25 * M * K) // 256) * 256
+        assert xq.q8_bytes_invariant(M, K) == base + 18 * K * (-(-M // 8))
+    assert L.xq_q8_bytes_invariant(9, 288) > 0
+    assert L.xq_q8_bytes_invariant(1, 100) == 0
     assert xq.weight_bytes(12, 256, 2048) == 256 * 8 * 144
     assert xq.weight_bytes(14, 1024, 4096) == 1024 * 16 * 210
     assert xq.weight_bytes(99, 1, 256) == 0

@@ -364,3 +364,46 @@ def test_misaligned_device_pointer_rejected(xq):
     with pytest.raises(xq.XQError) as e:
         xq.matmul(synth.Q4_K, W[8:], buf, 1, 4, 256, y=y[:4])
     assert e.value.code == 3
+
+
+# ------------------------------------------------------------ batch invariance
+
+@pytest.mark.parametrize("qtype,N,K", [(synth.Q4_K, 200, 1536), (synth.Q6_K, 130, 2048), (synth.Q6_K, 70, 1024)])
+def test_batch_invariant_rows(xq, qtype, N, K):
+    """Row m of y from the batch-invariant entry points is bit-identical for
+    every batch that contains token m, equal to decoding the token alone with
+    xq_matmul_*, deterministic across runs, and within the oracle's bound."""
+    Mmax = 21
+    W = synth.gen_weight(qtype, 901 + K + qtype, N, K)
+    x = synth.gen_x(902 + N, Mmax, K)
+    Wd = dev(W.reshape(-1))
+    xd = dev(x)
+
+    def run(M):
+        buf = xq.quantize_q8_invariant(xd[:M].contiguous())
+        y = poisoned(M, N)
+        xq.matmul_invariant(qtype, Wd, buf, M, N, K, y=y)
+        torch.cuda.synchronize()
+        return buf, y.cpu().numpy()
+
+    buf_full, y_full = run(Mmax)
+    # the Q8 bytes of the invariant layout are the oracle's (qs / d8 / s8 regions)
+    rq, rd, rs = oracle.quantize_q8(x)
+    qs, d8, s8 = (t.cpu().numpy() for t in xq.q8_views(buf_full, Mmax, K))
+    assert np.array_equal(qs, rq)
+    assert np.array_equal(d8.view(np.uint32), rd.view(np.uint32))
+    assert np.array_equal(s8.view(np.uint32), rs.view(np.uint32))
+    y_ref, ab, _ = oracle.matmul(qtype, W, rq, rd, K, want_isum=False)
+    check_y(y_full, y_ref, ab)
+    for M in (1, 3, 8, 9, 16, 20):
+        _, y = run(M)
+        assert np.array_equal(y.view(np.uint32), y_full[:M].view(np.uint32)), M
+    _, y_again = run(Mmax)
+    assert np.array_equal(y_again.view(np.uint32), y_full.view(np.uint32))
+    # the plain entry point at M <= 8 computes the same rows
+    for m in (0, 7, 13):
+        buf1 = xq.quantize_q8(xd[m:m + 1].contiguous())
+        y1 = poisoned(1, N)
+        xq.matmul(qtype, Wd, buf1, 1, N, K, y=y1)
+        torch.cuda.synchronize()
+        assert np.array_equal(y1.cpu().numpy().view(np.uint32), y_full[m:m + 1].view(np.uint32)), m
