@@ -1,4 +1,4 @@
-"""Seeded synthetic inputs: GGUF Q4_K / Q6_K weight bytes and fp32 activations.
+"""Seeded synthetic inputs: GGUF Q4_K / Q6_K / Q8_0 weight bytes and fp32 activations.
 
 This module holds no arithmetic of the method: it only draws bytes and
 numbers. It is the one module that both the CUDA path's tests/bench and the
@@ -11,6 +11,8 @@ Distributions (the workload specification):
   4-bit quants uniform in 0..15.
   Q6_K super-block (210 B): 256 6-bit quants uniform in 0..63; 16 int8
   scales uniform in [-32, 31]; fp16 d uniform in [1e-4, 1e-3].
+  Q8_0 block (34 B per 32 weights): fp16 d uniform in [1e-4, 1e-3]; 32
+  int8 quants uniform over all 256 byte values.
   Activations: fp32 N(0, 1).
 
 The 12 packed scale/min bytes of Q4_K, its 128 nibble bytes, and the 192
@@ -18,7 +20,8 @@ ql/qh bytes of Q6_K use every bit of the fields they pack, one bit per bit,
 so drawing those bytes uniformly is the same as drawing each packed field
 uniformly and independently; the generator therefore draws the bytes and
 never packs anything. Byte offsets: Q4_K d at 0, dmin at 2, scales 4..15,
-quants 16..143; Q6_K ql 0..127, qh 128..191, scales 192..207, d at 208.
+quants 16..143; Q6_K ql 0..127, qh 128..191, scales 192..207, d at 208;
+Q8_0 d at 0, quants 2..33.
 
 RNG: numpy PCG64 via ``numpy.random.default_rng(seed)``.
 """
@@ -28,10 +31,11 @@ from dataclasses import dataclass, field
 
 import numpy as np
 
-Q4_K = 12  # GGUF type ids
+Q8_0 = 8  # GGUF type ids
+Q4_K = 12
 Q6_K = 14
-BLOCK_BYTES = {Q4_K: 144, Q6_K: 210}
-TYPE_NAME = {Q4_K: "Q4_K", Q6_K: "Q6_K"}
+BLOCK_BYTES = {Q4_K: 144, Q6_K: 210, Q8_0: 8 * 34}  # bytes per 256 weights
+TYPE_NAME = {Q4_K: "Q4_K", Q6_K: "Q6_K", Q8_0: "Q8_0"}
 
 
 def weight_bytes(qtype: int, N: int, K: int) -> int:
@@ -64,7 +68,19 @@ def gen_q6k(seed: int, N: int, K: int) -> np.ndarray:
     return raw.reshape(N, (K // 256) * 210)
 
 
+def gen_q8_0(seed: int, N: int, K: int) -> np.ndarray:
+    """Q8_0 weight bytes, shape [N, K/32*34], uint8."""
+    assert K % 256 == 0 and N >= 0
+    rng = np.random.default_rng(seed)
+    nblk = N * (K // 32)
+    raw = np.frombuffer(rng.bytes(nblk * 34), np.uint8).reshape(nblk, 34).copy()
+    raw[:, 0:2] = _fp16_uniform(rng, nblk).view(np.uint8).reshape(nblk, 2)
+    return raw.reshape(N, (K // 32) * 34)
+
+
 def gen_weight(qtype: int, seed: int, N: int, K: int) -> np.ndarray:
+    if qtype == Q8_0:
+        return gen_q8_0(seed, N, K)
     if qtype == Q4_K:
         return gen_q4k(seed, N, K)
     if qtype == Q6_K:
@@ -128,6 +144,12 @@ WORKLOADS = {
     "qwen2.5-1.5b-layer": Workload("qwen2.5-1.5b-layer", "Qwen2.5-1.5B-shaped layer, all Q4_K",
                                    _layer(1536, 8960, 256, {}), 1, (1, 2, 4, 8), 100, 7, 10100,
                                    (1536, 1536, 1536, 8960)),
+    # Qwen2.5-1.5B-shaped layer requantized to Q8_0 (the Q8_0 model of the
+    # xLLM v0.7 article, section B3 + B4).
+    "qwen2.5-1.5b-q8_0-layer": Workload("qwen2.5-1.5b-q8_0-layer", "Qwen2.5-1.5B-shaped layer, all Q8_0",
+                                        _layer(1536, 8960, 256, {n: Q8_0 for n in
+                                                                 ("q", "k", "v", "o", "gate", "up", "down")}),
+                                        1, (1, 2, 4, 8), 500, 7, 10500, (1536, 1536, 1536, 8960)),
     # Qwen3-8B-shaped mixed layer: attn_v and ffn_down Q6_K, the rest Q4_K.
     "qwen3-8b-mixed-layer": Workload("qwen3-8b-mixed-layer", "Qwen3-8B-shaped mixed Q4_K/Q6_K layer",
                                      _layer(4096, 12288, 1024, {"v": Q6_K, "down": Q6_K}), 1,

@@ -23,6 +23,7 @@ _LIB = os.path.join(_HERE, "_build", "liboracle.so")
 
 Q4K_BYTES = 144
 Q6K_BYTES = 210
+Q8_0_BYTES = 34
 
 _lib = None
 
@@ -56,6 +57,10 @@ def _load():
     lib.oracle_q4k_fields.restype = None
     lib.oracle_q6k_fields.argtypes = [P, P, P, P]
     lib.oracle_q6k_fields.restype = None
+    lib.oracle_q8_0_fields.argtypes = [P, P, P]
+    lib.oracle_q8_0_fields.restype = None
+    lib.oracle_dequant_q8_0.argtypes = [P, I, I, P]
+    lib.oracle_matmul_q8_0_q8.argtypes = [P, P, P, I, I, I, P, P, P]
     lib.oracle_dequant_q4k.argtypes = [P, I, I, P]
     lib.oracle_dequant_q6k.argtypes = [P, I, I, P]
     lib.oracle_dequant_q8.argtypes = [P, P, I, I, P]
@@ -64,7 +69,7 @@ def _load():
     lib.oracle_gemv_f64.argtypes = [P, P, I, I, I, P]
     for name in ("oracle_quantize_q8", "oracle_dequant_q4k", "oracle_dequant_q6k",
                  "oracle_dequant_q8", "oracle_matmul_q4k_q8", "oracle_matmul_q6k_q8",
-                 "oracle_gemv_f64"):
+                 "oracle_gemv_f64", "oracle_dequant_q8_0", "oracle_matmul_q8_0_q8"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -119,6 +124,16 @@ def q6k_fields(blk: np.ndarray):
     return d.value, s, q
 
 
+def q8_0_fields(blk: np.ndarray):
+    """Decoded fields of one 34-byte Q8_0 block: (d, q[32])."""
+    blk = np.ascontiguousarray(blk, dtype=np.uint8)
+    assert blk.size == Q8_0_BYTES
+    d = ctypes.c_double()
+    q = np.zeros(32, np.int32)
+    _load().oracle_q8_0_fields(_p(blk), ctypes.byref(d), _p(q))
+    return d.value, q
+
+
 def _weight_shape(W: np.ndarray, K: int, nbytes: int):
     W = np.ascontiguousarray(W, dtype=np.uint8)
     nsb = K // 256
@@ -137,6 +152,13 @@ def dequant_q6k(W: np.ndarray, K: int) -> np.ndarray:
     W, N = _weight_shape(W, K, Q6K_BYTES)
     w = np.zeros((N, K), np.float64)
     _check(_load().oracle_dequant_q6k(_p(W), N, K, _p(w)), "dequant_q6k")
+    return w
+
+
+def dequant_q8_0(W: np.ndarray, K: int) -> np.ndarray:
+    W, N = _weight_shape(W, K, 8 * Q8_0_BYTES)
+    w = np.zeros((N, K), np.float64)
+    _check(_load().oracle_dequant_q8_0(_p(W), N, K, _p(w)), "dequant_q8_0")
     return w
 
 
@@ -174,6 +196,11 @@ def matmul_q6k_q8(W, qs, d8, K, want_isum=False):
     return _matmul(_load().oracle_matmul_q6k_q8, W, qs, d8, K, Q6K_BYTES, want_isum, K // 16)
 
 
+def matmul_q8_0_q8(W, qs, d8, K, want_isum=False):
+    """Integer route: y [M][N] (double), sum|terms| [M][N], isums [M][N][K/32] or None."""
+    return _matmul(_load().oracle_matmul_q8_0_q8, W, qs, d8, K, 8 * Q8_0_BYTES, want_isum, K // 32)
+
+
 def gemv_f64(w: np.ndarray, x: np.ndarray) -> np.ndarray:
     """Plain definition y[m][n] = sum_k w[n][k] * x[m][k] in double."""
     w = np.ascontiguousarray(w, dtype=np.float64)
@@ -186,7 +213,9 @@ def gemv_f64(w: np.ndarray, x: np.ndarray) -> np.ndarray:
 
 
 def matmul(qtype: int, W, qs, d8, K, want_isum=False):
-    """Dispatch on the GGUF type id (12 = Q4_K, 14 = Q6_K)."""
+    """Dispatch on the GGUF type id (8 = Q8_0, 12 = Q4_K, 14 = Q6_K)."""
+    if qtype == 8:
+        return matmul_q8_0_q8(W, qs, d8, K, want_isum)
     if qtype == 12:
         return matmul_q4k_q8(W, qs, d8, K, want_isum)
     if qtype == 14:

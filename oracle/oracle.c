@@ -1,5 +1,5 @@
 /*
- * CPU oracle for GGUF Q4_K / Q6_K x Q8 integer matmul.
+ * CPU oracle for GGUF Q4_K / Q6_K / Q8_0 x Q8 integer matmul.
  *
  * TEST INFRASTRUCTURE. Only the tests, the smoke check and the bench's CPU
  * baseline leg may link, load or call this file. The CUDA library never does,
@@ -212,6 +212,32 @@ int oracle_dequant_q6k(const uint8_t *W, int N, int K, double *w)
     return 0;
 }
 
+/* Q8_0 (xLLM v0.7 long-context article, section B3 + B4: symmetric int8,
+ * one fp16 scale per 32 weights, no min term, 34-byte blocks). Public GGUF
+ * block layout: d (fp16, little endian) at byte 0, then the 32 weights as
+ * signed bytes at bytes 2..33; w = d * q. */
+void oracle_q8_0_fields(const uint8_t *blk, double *d, int q[32])
+{
+    *d = oracle_half_to_double(read_u16le(blk));
+    for (int i = 0; i < 32; i++) q[i] = (int8_t)blk[2 + i];
+}
+
+/* Dequantize Q8_0 rows to double. A row of K weights is K/32 blocks. */
+int oracle_dequant_q8_0(const uint8_t *W, int N, int K, double *w)
+{
+    if (N < 0 || K <= 0 || K % 32 != 0) return 1;
+    int nb = K / 32;
+    for (int n = 0; n < N; n++) {
+        for (int b = 0; b < nb; b++) {
+            double d;
+            int q[32];
+            oracle_q8_0_fields(W + ((size_t)n * nb + b) * ORACLE_Q8_0_BYTES, &d, q);
+            for (int i = 0; i < 32; i++) w[(size_t)n * K + (size_t)b * 32 + i] = d * q[i];
+        }
+    }
+    return 0;
+}
+
 /* ----------------------------------------------------- integer route */
 
 /* Q4_K x Q8 by integer sub-block sums (the route the kernels take).
@@ -297,6 +323,40 @@ int oracle_matmul_q6k_q8(const uint8_t *W, const int8_t *qs, const float *d8,
                     if (isum_out)
                         isum_out[((size_t)m * N + n) * ngrp + 16 * b + g] = (int32_t)isum;
                 }
+            }
+        }
+    }
+    return 0;
+}
+
+/* Q8_0 x Q8 by integer block sums:
+ *   isum = sum_i q[32j+i] * q8[m][32j+i]                   (exact, int64)
+ *   y[m][n] += d_j * d8[m][j] * isum                        (double)
+ * isum_out (optional) is [M][N][K/32]; absterm_out as for Q4_K. */
+int oracle_matmul_q8_0_q8(const uint8_t *W, const int8_t *qs, const float *d8,
+                          int M, int N, int K,
+                          double *y, double *absterm_out, int32_t *isum_out)
+{
+    if (M < 0 || N < 0 || K <= 0 || K % 32 != 0) return 1;
+    int nb = K / 32;
+    double d;
+    int q[32];
+    for (int m = 0; m < M; m++)
+        for (int n = 0; n < N; n++) {
+            y[(size_t)m * N + n] = 0.0;
+            if (absterm_out) absterm_out[(size_t)m * N + n] = 0.0;
+        }
+    for (int n = 0; n < N; n++) {
+        for (int j = 0; j < nb; j++) {
+            oracle_q8_0_fields(W + ((size_t)n * nb + j) * ORACLE_Q8_0_BYTES, &d, q);
+            for (int m = 0; m < M; m++) {
+                const int8_t *a = qs + (size_t)m * K + (size_t)j * 32;
+                int64_t isum = 0;
+                for (int i = 0; i < 32; i++) isum += (int64_t)q[i] * a[i];
+                double t = d * (double)d8[(size_t)m * nb + j] * (double)isum;
+                y[(size_t)m * N + n] += t;
+                if (absterm_out) absterm_out[(size_t)m * N + n] += fabs(t);
+                if (isum_out) isum_out[((size_t)m * N + n) * nb + j] = (int32_t)isum;
             }
         }
     }

@@ -394,3 +394,76 @@ def test_q8_overflowing_reciprocal_saturates():
     expect = np.zeros(32, np.int8)
     expect[0], expect[1] = 127, -127
     assert np.array_equal(qs[0], expect) and s8[0, 0] == 0.0
+
+
+# ------------------------------------------------------------ Q8_0
+
+def ref_q8_0_decode(blk: bytes):
+    """Independent Q8_0 reader: d from the first two bytes as binary16, then
+    each quant from its 8 bits as a two's-complement number."""
+    d = _f16(blk, 0)
+    q = []
+    for i in range(32):
+        u = _bits(blk, 8 * (2 + i), 8)
+        q.append(u - 256 if u >= 128 else u)
+    return d, q
+
+
+def test_q8_0_decode_matches_independent_reader():
+    W = synth.gen_q8_0(11, 3, 512)
+    assert W.shape == (3, 16 * 34)
+    for blk in W.reshape(-1, 34):
+        d, q = oracle.q8_0_fields(blk)
+        rd, rq = ref_q8_0_decode(bytes(blk))
+        assert d == rd and list(q) == rq
+    w = oracle.dequant_q8_0(W, 512)
+    for n in range(3):
+        for b in range(16):
+            rd, rq = ref_q8_0_decode(bytes(W[n, 34 * b:34 * (b + 1)]))
+            for i in range(32):
+                assert w[n, 32 * b + i] == rd * rq[i]
+
+
+def test_q8_0_extremes_and_hand_block():
+    # every byte value as a quant: w = d * (int8) byte, with d = 2^-11 exactly
+    blk = bytearray(34 * 8)
+    vals = np.arange(256, dtype=np.uint8)
+    for b in range(8):
+        blk[34 * b:34 * b + 2] = (0x1000).to_bytes(2, "little")   # binary16 2^-11
+        blk[34 * b + 2:34 * b + 34] = vals[32 * b:32 * (b + 1)].tobytes()
+    w = oracle.dequant_q8_0(np.frombuffer(bytes(blk), np.uint8), 256)[0]
+    assert np.array_equal(w, 2.0 ** -11 * vals.view(np.int8).astype(np.float64))
+    # the product route on one-hot activations picks single weights back out
+    qs = np.zeros((1, 256), np.int8)
+    qs[0, 200] = 1
+    d8 = np.ones((1, 8), np.float32)
+    y, ab, isum = oracle.matmul_q8_0_q8(np.frombuffer(bytes(blk), np.uint8), qs, d8, 256, want_isum=True)
+    assert y[0, 0] == 2.0 ** -11 * np.int8(200 - 256) and ab[0, 0] == abs(y[0, 0])
+    assert isum[0, 0, 6] == 200 - 256 and np.count_nonzero(isum) == 1
+
+
+def test_q8_0_integer_route_equals_dequant_gemv():
+    for M in (1, 3, 8):
+        N, K = 40, 1024
+        W = synth.gen_weight(synth.Q8_0, 88 + M, N, K)
+        x = synth.gen_x(600 + M, M, K)
+        qs, d8, _ = oracle.quantize_q8(x)
+        y, ab, _ = oracle.matmul(synth.Q8_0, W, qs, d8, K)
+        yd = oracle.gemv_f64(oracle.dequant_q8_0(W, K), oracle.dequant_q8(qs, d8))
+        assert np.all(np.abs(y - yd) <= 1e-12 * ab + 1e-300)
+        assert np.all(ab > 0)
+
+
+def test_q8_0_isums_brute_force():
+    N, K, M = 3, 512, 2
+    W = synth.gen_weight(synth.Q8_0, 12, N, K)
+    x = synth.gen_x(21, M, K)
+    qs, d8, _ = oracle.quantize_q8(x)
+    _, _, isum = oracle.matmul(synth.Q8_0, W, qs, d8, K, want_isum=True)
+    for n in range(N):
+        qrow = []
+        for b in range(K // 32):
+            qrow += ref_q8_0_decode(bytes(W[n, 34 * b:34 * (b + 1)]))[1]
+        qrow = np.array(qrow, np.int64)
+        for m in range(M):
+            assert np.array_equal(isum[m, n], (qrow * qs[m].astype(np.int64)).reshape(-1, 32).sum(1))
