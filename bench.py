@@ -557,7 +557,7 @@ def secondary_workloads(device, world):
     import torch
     from gguf_quant_integer_gb300 import xq
     out = {}
-    for name in ("qwen2.5-1.5b-layer", "qwen3-8b-mixed-layer"):
+    for name in ("qwen2.5-1.5b-layer", "qwen3-8b-mixed-layer", "qwen2.5-1.5b-q8_0-layer"):
         wl = synth.WORKLOADS[name]
         lw = synth.gen_layer_weights(wl, 0)
         copies = max(3, -(-3 * L2_BYTES // wl.layer_weight_bytes()))

@@ -14,7 +14,9 @@ constexpr int kMaxGemvM = 8;  // tokens per GEMV launch (the kernels' M template
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 int block_bytes(int type) {
-  return type == XQ_TYPE_Q4_K ? xq::kQ4kBytes : (type == XQ_TYPE_Q6_K ? xq::kQ6kBytes : 0);
+  // bytes per 256 weights
+  return type == XQ_TYPE_Q4_K ? xq::kQ4kBytes
+                              : (type == XQ_TYPE_Q6_K ? xq::kQ6kBytes : (type == XQ_TYPE_Q8_0 ? xq::kQ80Group : 0));
 }
 
 xq_status check_shape(int M, int N, int K) {
@@ -33,6 +35,7 @@ xq_status run_matmul(int type, const void* W, const void* xq, int M, int N, int 
   const xq::Q8Layout L = xq::q8_layout(M, K, invariant);
   const uint8_t* base = static_cast<const uint8_t*>(xq);
   if (M > kMaxGemvM && !invariant) {
+    if (type == XQ_TYPE_Q8_0) return XQ_ERR_UNSUPPORTED;  // the tile kernel takes Q4_K and Q6_K
     const cudaError_t e = xq::launch_tile_mma(type, static_cast<const uint8_t*>(W), base, M, N, K, y, s, true);
     return e == cudaSuccess ? XQ_OK : XQ_ERR_CUDA;
   }
@@ -98,9 +101,10 @@ size_t round256(size_t b) { return (b + 255) & ~static_cast<size_t>(255); }
 // from the same helpers the launcher uses). The counters and arrival counts
 // form one range that the quantize launch zeroes.
 constexpr size_t kCounterBytes = 256;
-constexpr int kTypes = 2;  // 0: Q4_K, 1: Q6_K
+constexpr int kTypes = 3;  // 0: Q4_K, 1: Q6_K, 2: Q8_0
+constexpr int kTypeIds[kTypes] = {XQ_TYPE_Q4_K, XQ_TYPE_Q6_K, XQ_TYPE_Q8_0};
 
-int type_index(int type) { return type == XQ_TYPE_Q4_K ? 0 : 1; }
+int type_index(int type) { return type == XQ_TYPE_Q4_K ? 0 : (type == XQ_TYPE_Q6_K ? 1 : 2); }
 
 struct Sched {
   bool dynamic[kTypes];  // the type's grouped GEMV fits one launch: counter and K-split
@@ -128,14 +132,14 @@ void choose_chunks(const xq_proj* proj, int n_proj, int M, int type, int* nch) {
 
 Sched sched_layout(const xq_proj* proj, int n_proj, int M) {
   Sched sc = {};
-  int items[kTypes] = {0, 0};
+  int items[kTypes] = {0, 0, 0};
   for (int p = 0; p < n_proj && p < 64; ++p) {
     sc.nch[p] = 1;
     if (in_group(proj[p], M)) ++items[type_index(proj[p].type)];
   }
   for (int g = 0; g < kTypes; ++g) {
     sc.dynamic[g] = items[g] > 0 && items[g] <= xq::kMaxProj;
-    if (sc.dynamic[g]) choose_chunks(proj, n_proj, M, g == 0 ? XQ_TYPE_Q4_K : XQ_TYPE_Q6_K, sc.nch);
+    if (sc.dynamic[g]) choose_chunks(proj, n_proj, M, kTypeIds[g], sc.nch);
   }
   for (int p = 0; p < n_proj; ++p) {
     if (!in_group(proj[p], M) || !sc.dynamic[type_index(proj[p].type)] || sc.nch[p] <= 1) continue;
@@ -147,7 +151,9 @@ Sched sched_layout(const xq_proj* proj, int n_proj, int M) {
 }
 
 size_t sched_bytes(const Sched& sc) {
-  return kTypes * kCounterBytes + sc.arrive[0] + sc.arrive[1] + sc.partial[0] + sc.partial[1];
+  size_t b = kTypes * kCounterBytes;
+  for (int g = 0; g < kTypes; ++g) b += sc.arrive[g] + sc.partial[g];
+  return b;
 }
 
 // Validate a layer description and find each input's K (0 = unused).
@@ -161,6 +167,7 @@ xq_status layer_inputs(const xq_proj* proj, int n_proj, int n_inputs, int M, int
     if (q.input < 0 || q.input >= n_inputs) return XQ_ERR_ARG;
     const xq_status st = check_shape(M, q.N, q.K);
     if (st != XQ_OK) return st;
+    if (q.type == XQ_TYPE_Q8_0 && M > kMaxGemvM) return XQ_ERR_UNSUPPORTED;
     if (in_k[q.input] == 0) in_k[q.input] = q.K;
     if (in_k[q.input] != q.K) return XQ_ERR_SHAPE;
   }
@@ -251,6 +258,17 @@ xq_status xq_matmul_q6k_q8(const void* W, const void* xq, int M, int N, int K, f
   return matmul_entry(XQ_TYPE_Q6_K, W, xq, M, N, K, y, nullptr, stream);
 }
 
+xq_status xq_matmul_q8_0_q8(const void* W, const void* xq, int M, int N, int K, float* y,
+                            xq_stream stream) {
+  return matmul_entry(XQ_TYPE_Q8_0, W, xq, M, N, K, y, nullptr, stream);
+}
+
+xq_status xq_debug_isums_q8_0(const void* W, const void* xq, int M, int N, int K, float* y,
+                              int32_t* isum, xq_stream stream) {
+  if (!isum) return XQ_ERR_ARG;
+  return matmul_entry(XQ_TYPE_Q8_0, W, xq, M, N, K, y, isum, stream);
+}
+
 xq_status xq_debug_isums_q4k(const void* W, const void* xq, int M, int N, int K, float* y,
                              int32_t* isum, xq_stream stream) {
   if (!isum) return XQ_ERR_ARG;
@@ -310,7 +328,8 @@ xq_status xq_layer_mixed(const xq_proj* proj, int n_proj, const float* const* in
   {
     uint8_t* c = ws + sched_off;
     uint8_t* a = c + kTypes * kCounterBytes;
-    uint8_t* pt = a + sc.arrive[0] + sc.arrive[1];
+    uint8_t* pt = a;
+    for (int g = 0; g < kTypes; ++g) pt += sc.arrive[g];
     for (int g = 0; g < kTypes; ++g) {
       counter[g] = sc.dynamic[g] ? reinterpret_cast<unsigned int*>(c + g * kCounterBytes) : nullptr;
       arrive[g] = sc.dynamic[g] ? a : nullptr;
@@ -319,8 +338,13 @@ xq_status xq_layer_mixed(const xq_proj* proj, int n_proj, const float* const* in
       pt += sc.partial[g];
     }
   }
-  const bool any_dynamic = sc.dynamic[0] || sc.dynamic[1];
-  const int zero_words = static_cast<int>((kTypes * kCounterBytes + sc.arrive[0] + sc.arrive[1]) / 4);
+  bool any_dynamic = false;
+  size_t zero_bytes = kTypes * kCounterBytes;
+  for (int g = 0; g < kTypes; ++g) {
+    any_dynamic = any_dynamic || sc.dynamic[g];
+    zero_bytes += sc.arrive[g];
+  }
+  const int zero_words = static_cast<int>(zero_bytes / 4);
   // One launch quantizes every input that is read (up to kMaxProj per launch).
   {
     xq::QuantJob jobs[xq::kMaxProj];
@@ -354,7 +378,7 @@ xq_status xq_layer_mixed(const xq_proj* proj, int n_proj, const float* const* in
   // One grouped tensor-core GEMV launch per weight type (kMaxProj items per
   // launch; M <= 8 is one chunk per projection), Q4_K first.
   for (int g = 0; g < kTypes; ++g) {
-    const int type = g == 0 ? XQ_TYPE_Q4_K : XQ_TYPE_Q6_K;
+    const int type = kTypeIds[g];
     xq::MmaProj items[xq::kMaxProj];
     int n = 0;
     for (int p = 0; p <= n_proj; ++p) {

@@ -90,7 +90,7 @@ constexpr int kDecBytes = 8 * 16 * 16;  // per warp: one float4 per (32-block, r
 // starting at the 16-byte boundary at or below the 210-byte super-block.
 template <int TYPE>
 struct GLay {
-  static constexpr int kBoxRow = TYPE == 12 ? kQ4kBytes : 240;
+  static constexpr int kBoxRow = TYPE == 12 ? kQ4kBytes : (TYPE == 8 ? kQ80Group : 240);
   static constexpr int kStages = TYPE == 12 ? 4 : 3;
   static constexpr int kBlockBytes = 16 * kBoxRow;  // 16 rows x one super-block
   static constexpr int kFragOff = 4 * kBlockBytes;
@@ -99,9 +99,18 @@ struct GLay {
   static constexpr int kSmemBytes = kStages * kStageBytes + 4 * kDecBytes + kStages * 16 + 2 * kStages * 8 + 16;
 };
 static_assert(GLay<12>::kStageBytes == 13824, "Q4_K stage layout");
+static_assert(3 * (GLay<8>::kSmemBytes + 1024) <= 228 * 1024, "Q8_0: three CTAs per SM");
 constexpr long long kWaitClocks = 1LL << 32;
 
 __device__ __forceinline__ int mma_row(int i) { return 8 * (i >> 3) + 2 * (i & 3) + ((i >> 2) & 1); }
+
+// TMA x coordinate of super-block (or 8-block group) b in the weight map.
+template <int TYPE>
+__device__ __forceinline__ int weight_box_x(int b) {
+  if constexpr (TYPE == 12) return b * (kQ4kBytes / 8);
+  else if constexpr (TYPE == 8) return b * (kQ80Group / 8);
+  else return (kQ6kBytes * b) & ~15;
+}
 
 // ---------------------------------------------------------------- PTX
 using namespace ptx;
@@ -343,6 +352,70 @@ __device__ __forceinline__ void compute_block_q6(const uint8_t* blk, int off, co
   }
 }
 
+// Q8_0 (xLLM v0.7 long-context article, section B3 + B4; public GGUF block:
+// fp16 d at byte 0, 32 int8 quants at bytes 2..33). A stage row holds 8
+// blocks (272 bytes, 16-byte aligned). Lane l takes row l%16 and blocks
+// 4*(l/16) .. +3, writing (d, d, 0, 0) into the warp's table (no min term).
+__device__ __forceinline__ void decode_scales_q8_0(const uint8_t* blk, float4* dec, int lane) {
+  const int r = lane & 15, half = lane >> 4;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int j = 4 * half + k;
+    const float d = half_bits_to_float(*reinterpret_cast<const unsigned short*>(blk + r * kQ80Group + 34 * j));
+    dec[j * 16 + r] = make_float4(d, d, 0.0f, 0.0f);
+  }
+}
+
+// Q8_0 block j of rows r0, r1: lane (n8, t) takes the quants of weights
+// 8t..8t+7 (the activation image's slot order, as for Q4_K). Each int8 q
+// becomes the exact fp16 integer q: the byte with its sign bit flipped is
+// q + 128, placed under the exponent of 1024 by a byte permute (1024 + q +
+// 128), then 1152 is subtracted. Products are at most 128*127 and a block
+// sum at most 520,192 in magnitude, so D = isum exactly. Combine:
+// acc += (d * d8) * D.
+template <bool ISUM>
+__device__ __forceinline__ void compute_block_q8_0(const uint8_t* blk, const uint8_t* act, const float4* dec,
+                                                   const Proj& P, int rg, int b, int n8, int t, int lane,
+                                                   f2 (&acc)[2]) {
+  const int r0 = mma_row(n8), r1 = r0 + 8;
+  const uint4* fp = reinterpret_cast<const uint4*>(act) + lane;
+  const ulonglong2* sp = reinterpret_cast<const ulonglong2*>(act + (GLay<8>::kFscOff - GLay<8>::kFragOff)) + t;
+  const ulonglong2* dp = reinterpret_cast<const ulonglong2*>(dec);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    uint32_t w0[2], w1[2];
+    load_words<2>(blk + r0 * kQ80Group + 34 * j + 2 + 8 * t, w0);
+    load_words<2>(blk + r1 * kQ80Group + 34 * j + 2 + 8 * t, w1);
+    uint32_t a[2][4];  // [k-half][a0..a3]
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const uint32_t x0 = w0[h] ^ 0x80808080u, x1 = w1[h] ^ 0x80808080u;
+      a[h][0] = hsub2(prmt(x0, 0x64646464u, 0x4240u), 0x64806480u);  // row r0, weights 4h', 4h'+2
+      a[h][1] = hsub2(prmt(x1, 0x64646464u, 0x4240u), 0x64806480u);  // row r1
+      a[h][2] = hsub2(prmt(x0, 0x64646464u, 0x4341u), 0x64806480u);  // row r0, weights 4h'+1, 4h'+3
+      a[h][3] = hsub2(prmt(x1, 0x64646464u, 0x4341u), 0x64806480u);  // row r1
+    }
+    const uint4 B = fp[j * 32];
+    float D[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    mma16816(D, a[0][0], a[0][1], a[0][2], a[0][3], B.x, B.y);
+    mma16816(D, a[1][0], a[1][1], a[1][2], a[1][3], B.z, B.w);
+    const ulonglong2 f = sp[j * 4];  // (d8 c0, d8 c1), (s8 c0, s8 c1)
+    const ulonglong2 e0 = dp[j * 16 + r0], e1 = dp[j * 16 + r1];
+    acc[0] = fma2(mul2(e0.x, f.x), pk(D[0], D[1]), acc[0]);
+    acc[1] = fma2(mul2(e1.x, f.x), pk(D[2], D[3]), acc[1]);
+    if (ISUM) {
+      const int nsub = P.K >> 5;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int row = rg * 16 + ((e >> 1) ? r1 : r0);
+        const int col = 2 * t + (e & 1);
+        if (row < P.N && col < P.M)
+          P.isum[(static_cast<size_t>(col) * P.N + row) * nsub + 8 * b + j] = static_cast<int32_t>(D[e]);
+      }
+    }
+  }
+}
+
 __device__ __forceinline__ void store_y(const Proj& P, int rg, int n8, int t, float v00, float v01, float v10,
                                         float v11) {
   const int r0 = rg * 16 + mma_row(n8), r1 = r0 + 8, c0 = 2 * t, c1 = c0 + 1;
@@ -411,7 +484,7 @@ gemv_mma_kernel(const __grid_constant__ Group G) {
         mbar_expect_tx(full_s + 8 * slot, static_cast<unsigned>(nblk * kBlockBytes + 8 * 512 + 8 * 64));
         const uint32_t st = ring_s + slot * kStageBytes;
         for (int w = 0; w < nblk; ++w)
-          tma_load_2d(st + w * kBlockBytes, &P.map, TYPE == 12 ? b * (kQ4kBytes / 8) : ((kQ6kBytes * b) & ~15),
+          tma_load_2d(st + w * kBlockBytes, &P.map, weight_box_x<TYPE>(b),
                       tp.rb * 64 + 16 * w, full_s + 8 * slot);
       }
       bresume = b;
@@ -451,7 +524,7 @@ gemv_mma_kernel(const __grid_constant__ Group G) {
         mbar_expect_tx(full_s + 8 * slot, static_cast<unsigned>(nblk * kBlockBytes + 8 * 512 + 8 * 64));
         const uint32_t st = ring_s + slot * kStageBytes;
         for (int w = 0; w < nblk; ++w)
-          tma_load_2d(st + w * kBlockBytes, &P.map, TYPE == 12 ? b * (kQ4kBytes / 8) : ((kQ6kBytes * b) & ~15),
+          tma_load_2d(st + w * kBlockBytes, &P.map, weight_box_x<TYPE>(b),
                       tp.rb * 64 + 16 * w, full_s + 8 * slot);
         bulk_load(st + kFragOff, P.frag + static_cast<size_t>(b) * 8 * 512, 8 * 512, full_s + 8 * slot);
         bulk_load(st + kFscOff, P.fsc + static_cast<size_t>(b) * 8 * 64, 8 * 64, full_s + 8 * slot);
@@ -487,10 +560,14 @@ gemv_mma_kernel(const __grid_constant__ Group G) {
     const uint8_t* st = ring + slot * kStageBytes;
     const bool rows_ok = rg * 16 < P.N;
     if (rows_ok) {
-      if (TYPE == 12) {
+      if constexpr (TYPE == 12) {
         decode_scales_q4(st + warp * kBlockBytes, dec, lane);
         __syncwarp();
         compute_block_q4<ISUM>(st + warp * kBlockBytes, st + kFragOff, dec, P, rg, m.y, n8, t, lane, acc);
+      } else if constexpr (TYPE == 8) {
+        decode_scales_q8_0(st + warp * kBlockBytes, dec, lane);
+        __syncwarp();
+        compute_block_q8_0<ISUM>(st + warp * kBlockBytes, st + kFragOff, dec, P, rg, m.y, n8, t, lane, acc);
       } else {
         const int off = (kQ6kBytes * m.y) & 15;  // the same for every row: rows are 16-byte multiples
         decode_scales_q6(st + warp * kBlockBytes, off, dec, lane);
@@ -529,7 +606,7 @@ gemv_mma_kernel(const __grid_constant__ Group G) {
           // chunks added in chunk order (Q6_K, split into more chunks, issues
           // the loads of 4 chunks at a time)
           float v[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-          if constexpr (TYPE == 12) {
+          if constexpr (TYPE != 14) {
             for (int c = 0; c < P.nch; ++c) {
               const float* pc = P.partial + static_cast<size_t>(c) * 8 * rows_pad;
               v[0] += __ldcg(pc + static_cast<size_t>(c0) * rows_pad + r0);
@@ -594,6 +671,9 @@ bool encode_weight_map(int type, CUtensorMap* map, const uint8_t* W, int N, int 
   if (type == 12)
     return encode_tma_2d(map, CU_TENSOR_MAP_DATA_TYPE_UINT64, W, nsb * kQ4kBytes / 8, static_cast<unsigned long long>(N),
                          nsb * kQ4kBytes, kQ4kBytes / 8, 16);
+  if (type == 8)
+    return encode_tma_2d(map, CU_TENSOR_MAP_DATA_TYPE_UINT64, W, nsb * kQ80Group / 8, static_cast<unsigned long long>(N),
+                         nsb * kQ80Group, kQ80Group / 8, 16);
   return encode_tma_2d(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, W, nsb * kQ6kBytes, static_cast<unsigned long long>(N),
                        nsb * kQ6kBytes, GLay<14>::kBoxRow, 16);
 }
@@ -632,12 +712,12 @@ bool encode_tma_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, u
 }
 
 bool gemv_mma_supports(int type, int K) {
-  return type == 12 || (type == 14 && ((K / 256) % 8) == 0);
+  return type == 12 || type == 8 || (type == 14 && ((K / 256) % 8) == 0);
 }
 
 cudaError_t launch_gemv_mma(int type, const MmaProj* projs, int n, cudaStream_t s, bool pdl, unsigned int* counter,
                             uint8_t* arrive_ws, uint8_t* partial_ws) {
-  if (n <= 0 || n > kMaxProj || (type != 12 && type != 14)) return cudaErrorInvalidValue;
+  if (n <= 0 || n > kMaxProj || (type != 12 && type != 14 && type != 8)) return cudaErrorInvalidValue;
   // Per-projection K-chunking (only with split workspaces) and task cost.
   const bool split = arrive_ws != nullptr && partial_ws != nullptr;
   int nch[kMaxProj], cost[kMaxProj];
@@ -699,18 +779,23 @@ cudaError_t launch_gemv_mma(int type, const MmaProj* projs, int n, cudaStream_t 
   }
   G.total = total;
   if (total == 0) return cudaSuccess;
-  const int cap = type == 12 ? (isum ? max_ctas<12, true>() : max_ctas<12, false>())
-                             : (isum ? max_ctas<14, true>() : max_ctas<14, false>());
+  const int cap = type == 12  ? (isum ? max_ctas<12, true>() : max_ctas<12, false>())
+                  : type == 8 ? (isum ? max_ctas<8, true>() : max_ctas<8, false>())
+                              : (isum ? max_ctas<14, true>() : max_ctas<14, false>());
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(total < cap ? total : cap));
   cfg.blockDim = dim3(160);
-  cfg.dynamicSmemBytes = type == 12 ? GLay<12>::kSmemBytes : GLay<14>::kSmemBytes;
+  cfg.dynamicSmemBytes =
+      type == 12 ? GLay<12>::kSmemBytes : (type == 8 ? GLay<8>::kSmemBytes : GLay<14>::kSmemBytes);
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
+  if (type == 8)
+    return isum ? cudaLaunchKernelEx(&cfg, gemv_mma_kernel<8, true>, G)
+                : cudaLaunchKernelEx(&cfg, gemv_mma_kernel<8, false>, G);
   if (type == 12)
     return isum ? cudaLaunchKernelEx(&cfg, gemv_mma_kernel<12, true>, G)
                 : cudaLaunchKernelEx(&cfg, gemv_mma_kernel<12, false>, G);

@@ -11,6 +11,8 @@ namespace xq {
 
 constexpr int kQ4kBytes = 144;  // GGUF Q4_K super-block: 256 weights
 constexpr int kQ6kBytes = 210;  // GGUF Q6_K super-block: 256 weights
+constexpr int kQ80Bytes = 34;   // GGUF Q8_0 block: 32 weights
+constexpr int kQ80Group = 8 * kQ80Bytes;  // 8 Q8_0 blocks: 256 weights, 16-byte multiple
 constexpr int kNumSMs = 152;    // GB300: 2 dies x 76 SMs
 
 // ---------------------------------------------------------------- loads

@@ -15,6 +15,7 @@ from . import synth
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_build", "libxq.so")
 
+XQ_TYPE_Q8_0 = 8
 XQ_TYPE_Q4_K = 12
 XQ_TYPE_Q6_K = 14
 
@@ -25,7 +26,8 @@ STATUS = {0: "XQ_OK", 1: "XQ_ERR_ARG", 2: "XQ_ERR_SHAPE", 3: "XQ_ERR_ALIGN",
 SYMBOLS = ("xq_status_str", "xq_q8_bytes", "xq_weight_bytes", "xq_quantize_q8",
            "xq_matmul_q4k_q8", "xq_matmul_q6k_q8", "xq_layer_workspace_bytes",
            "xq_layer_mixed", "xq_debug_isums_q4k", "xq_debug_isums_q6k", "xq_layer_mixed_static",
-           "xq_q8_bytes_invariant", "xq_quantize_q8_invariant", "xq_matmul_invariant")
+           "xq_q8_bytes_invariant", "xq_quantize_q8_invariant", "xq_matmul_invariant",
+           "xq_matmul_q8_0_q8", "xq_debug_isums_q8_0")
 
 
 class XQError(RuntimeError):
@@ -66,16 +68,17 @@ def lib(path: str | None = None):
     L.xq_quantize_q8_invariant.restype = I
     L.xq_matmul_invariant.argtypes = [I, P, P, I, I, I, P, P]
     L.xq_matmul_invariant.restype = I
-    for fn in ("xq_matmul_q4k_q8", "xq_matmul_q6k_q8"):
+    for fn in ("xq_matmul_q4k_q8", "xq_matmul_q6k_q8", "xq_matmul_q8_0_q8"):
         getattr(L, fn).argtypes = [P, P, I, I, I, P, P]
-    for fn in ("xq_debug_isums_q4k", "xq_debug_isums_q6k"):
+    for fn in ("xq_debug_isums_q4k", "xq_debug_isums_q6k", "xq_debug_isums_q8_0"):
         getattr(L, fn).argtypes = [P, P, I, I, I, P, P, P]
     L.xq_layer_workspace_bytes.argtypes = [ctypes.POINTER(xq_proj), I, I, I]
     L.xq_layer_workspace_bytes.restype = S
     L.xq_layer_mixed.argtypes = [ctypes.POINTER(xq_proj), I, ctypes.POINTER(ctypes.c_void_p), I, I, P, S, P]
     L.xq_layer_mixed_static.argtypes = [ctypes.POINTER(xq_proj), I, ctypes.POINTER(ctypes.c_void_p), I, I, P]
     for fn in ("xq_quantize_q8", "xq_matmul_q4k_q8", "xq_matmul_q6k_q8", "xq_debug_isums_q4k",
-               "xq_debug_isums_q6k", "xq_layer_mixed", "xq_layer_mixed_static"):
+               "xq_debug_isums_q6k", "xq_layer_mixed", "xq_layer_mixed_static", "xq_matmul_q8_0_q8",
+               "xq_debug_isums_q8_0"):
         getattr(L, fn).restype = I
     if path is None:
         _lib = L
@@ -133,7 +136,7 @@ def matmul(qtype: int, W, xq, M: int, N: int, K: int, y=None, stream=None):
     import torch
     if y is None:
         y = torch.empty((M, N), dtype=torch.float32, device=W.device)
-    fn = {XQ_TYPE_Q4_K: "xq_matmul_q4k_q8", XQ_TYPE_Q6_K: "xq_matmul_q6k_q8"}[qtype]
+    fn = {XQ_TYPE_Q4_K: "xq_matmul_q4k_q8", XQ_TYPE_Q6_K: "xq_matmul_q6k_q8", XQ_TYPE_Q8_0: "xq_matmul_q8_0_q8"}[qtype]
     _check(fn, getattr(lib(), fn)(_ptr(W), _ptr(xq), M, N, K, _ptr(y), _stream(stream)))
     return y
 
@@ -174,12 +177,13 @@ def matmul_invariant(qtype: int, W, xq, M: int, N: int, K: int, y=None, stream=N
 def debug_isums(qtype: int, W, xq, M: int, N: int, K: int, y=None, isum=None, stream=None):
     """Matmul that also writes the exact int32 sub-block sums (test hook)."""
     import torch
-    per = K // 32 if qtype == XQ_TYPE_Q4_K else K // 16
+    per = K // 16 if qtype == XQ_TYPE_Q6_K else K // 32
     if y is None:
         y = torch.empty((M, N), dtype=torch.float32, device=W.device)
     if isum is None:
         isum = torch.empty((M, N, per), dtype=torch.int32, device=W.device)
-    fn = {XQ_TYPE_Q4_K: "xq_debug_isums_q4k", XQ_TYPE_Q6_K: "xq_debug_isums_q6k"}[qtype]
+    fn = {XQ_TYPE_Q4_K: "xq_debug_isums_q4k", XQ_TYPE_Q6_K: "xq_debug_isums_q6k",
+          XQ_TYPE_Q8_0: "xq_debug_isums_q8_0"}[qtype]
     _check(fn, getattr(lib(), fn)(_ptr(W), _ptr(xq), M, N, K, _ptr(y), _ptr(isum), _stream(stream)))
     return y, isum
 

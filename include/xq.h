@@ -84,6 +84,7 @@ typedef enum {
 } xq_status;
 
 /* GGUF tensor type ids. */
+#define XQ_TYPE_Q8_0 8
 #define XQ_TYPE_Q4_K 12
 #define XQ_TYPE_Q6_K 14
 
@@ -135,6 +136,18 @@ XQ_API xq_status xq_matmul_q4k_q8(const void *W, const void *xq, int M, int N, i
 XQ_API xq_status xq_matmul_q6k_q8(const void *W, const void *xq, int M, int N, int K,
                            float *y, xq_stream stream);
 
+/* Same for a Q8_0 weight (xLLM v0.7 article, section B3 + B4: symmetric
+ * int8, one fp16 scale per 32 weights, no min term).
+ *   W  : Q8_0 bytes [N][K/32][34] (public GGUF block: fp16 d, then 32 int8
+ *        quants), device, read-only. Blocks are 2-byte aligned; only the base
+ *        pointer must be 16-byte aligned. K % 256 == 0 (rows of 8-block
+ *        groups, 272 bytes each, are 16-byte multiples).
+ * M <= 8 runs the tensor-core GEMV; M > 8 returns XQ_ERR_UNSUPPORTED (the
+ * tile kernel takes Q4_K and Q6_K): use the batch-invariant entry points,
+ * which run the GEMV per 8-token chunk for any M. */
+XQ_API xq_status xq_matmul_q8_0_q8(const void *W, const void *xq, int M, int N, int K,
+                            float *y, xq_stream stream);
+
 /* Batch-invariant mode (speculative-decoding verification: the rows of y for
  * a batch of M tokens must equal those of decoding each token alone).
  * xq_matmul_q4k_q8 / _q6k_q8 are invariant for M <= 8 (every token of an
@@ -146,7 +159,7 @@ XQ_API xq_status xq_matmul_q6k_q8(const void *W, const void *xq, int M, int N, i
  * chunk by chunk, never split over K. Row m of y is then bit-identical for
  * every M >= m+1, and to xq_matmul_* at M <= 8 on the same activations.
  * Arguments and errors as for xq_quantize_q8 and xq_matmul_*; type is
- * XQ_TYPE_Q4_K or XQ_TYPE_Q6_K. */
+ * XQ_TYPE_Q4_K, XQ_TYPE_Q6_K or XQ_TYPE_Q8_0. */
 XQ_API size_t xq_q8_bytes_invariant(int M, int K);
 XQ_API xq_status xq_quantize_q8_invariant(const float *x, int M, int K, void *xq, xq_stream stream);
 XQ_API xq_status xq_matmul_invariant(int type, const void *W, const void *xq, int M, int N, int K,
@@ -154,7 +167,7 @@ XQ_API xq_status xq_matmul_invariant(int type, const void *W, const void *xq, in
 
 /* One projection of a transformer layer for xq_layer_mixed. */
 typedef struct {
-    int type;        /* XQ_TYPE_Q4_K or XQ_TYPE_Q6_K */
+    int type;        /* XQ_TYPE_Q4_K, XQ_TYPE_Q6_K or XQ_TYPE_Q8_0 (M <= 8) */
     int N, K;        /* output and input features */
     const void *W;   /* weight bytes, device */
     float *y;        /* fp32 [M][N] output, device */
@@ -163,7 +176,7 @@ typedef struct {
 
 /* Workspace bytes xq_layer_mixed needs: the Q8 buffers of every input that
  * some projection reads, each rounded up to 256 bytes, then scheduling
- * state: one 256-byte task counter per weight type (Q4_K, Q6_K) and, for
+ * state: one 256-byte task counter per weight type (Q4_K, Q6_K, Q8_0) and, for
  * each projection with more than 24 super-blocks per row that the grouped
  * tensor-core GEMV splits over K across CTAs (M <= 8), its arrival counts
  * and partial sums. 0 on bad arguments. */
@@ -220,6 +233,9 @@ XQ_API xq_status xq_debug_isums_q4k(const void *W, const void *xq, int M, int N,
                              float *y, int32_t *isum, xq_stream stream);
 XQ_API xq_status xq_debug_isums_q6k(const void *W, const void *xq, int M, int N, int K,
                              float *y, int32_t *isum, xq_stream stream);
+/* Q8_0: isum int32 [M][N][K/32], block j at index j. */
+XQ_API xq_status xq_debug_isums_q8_0(const void *W, const void *xq, int M, int N, int K,
+                              float *y, int32_t *isum, xq_stream stream);
 
 #ifdef __cplusplus
 }

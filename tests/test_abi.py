@@ -56,6 +56,7 @@ def test_sizes(L):
     assert L.xq_q8_bytes_invariant(9, 288) > 0
     assert L.xq_q8_bytes_invariant(1, 100) == 0
     assert xq.weight_bytes(12, 256, 2048) == 256 * 8 * 144
+    assert xq.weight_bytes(8, 256, 2048) == 256 * 64 * 34   # Q8_0: 34 bytes per 32 weights
     assert xq.weight_bytes(14, 1024, 4096) == 1024 * 16 * 210
     assert xq.weight_bytes(99, 1, 256) == 0
     assert xq.weight_bytes(12, 1, 300) == 0
@@ -102,8 +103,9 @@ def test_layer_argument_errors(L):
 
     arr, n = projs((12, 16, 512, 0), (14, 8, 512, 0), (12, 16, 1024, 1))
     need = L.xq_layer_workspace_bytes(arr, n, 2, 4)
-    # Q8 buffers, then one 256-byte task counter per weight type (no split at these K)
-    expect = sum(((xq.q8_bytes(4, k) + 255) // 256) * 256 for k in (512, 1024)) + 2 * 256
+    # Q8 buffers, then one 256-byte task counter per weight type (Q4_K, Q6_K,
+    # Q8_0; no split at these K)
+    expect = sum(((xq.q8_bytes(4, k) + 255) // 256) * 256 for k in (512, 1024)) + 3 * 256
     assert need == expect
     # mismatched K on one input
     bad, nb = projs((12, 16, 512, 0), (12, 16, 768, 0))
@@ -119,3 +121,18 @@ def test_layer_argument_errors(L):
     assert L.xq_layer_mixed(arr, n, ins, 2, 4, P(FAKE), need - 1, None) == 4
     # missing weight pointer
     assert L.xq_layer_mixed(arr, n, ins, 2, 4, P(FAKE), need, None) == 1
+
+
+def test_q8_0_entry_points_reject_before_launch(L):
+    """Q8_0 at M > 8 (the tile kernel takes Q4_K and Q6_K) and Q8_0 in a
+    layer at M > 8 are refused before anything is enqueued."""
+    from gguf_quant_integer_gb300 import xq
+    P = ctypes.c_void_p
+    assert L.xq_matmul_q8_0_q8(P(FAKE), P(FAKE), 9, 16, 256, P(FAKE), None) == 6
+    assert L.xq_matmul_q8_0_q8(P(FAKE), P(FAKE), 8, 16, 300, P(FAKE), None) == 2
+    assert L.xq_debug_isums_q8_0(P(FAKE), P(FAKE), 2, 16, 256, P(FAKE), None, None) == 1
+    arr = xq._proj_array([(8, 16, 512, None, None, 0)])
+    assert L.xq_layer_workspace_bytes(arr, 1, 1, 9) == 0
+    assert L.xq_layer_workspace_bytes(arr, 1, 1, 8) > 0
+    ins = (ctypes.c_void_p * 1)(FAKE)
+    assert L.xq_layer_mixed(arr, 1, ins, 1, 9, P(FAKE), 1 << 20, None) == 6

@@ -168,7 +168,7 @@ def check_matmul(xq, qtype, W, x, want_isum=True):
     Wd = dev(W.reshape(-1))
     y = poisoned(M, N)
     if want_isum and M <= 8:
-        per = K // 32 if qtype == synth.Q4_K else K // 16
+        per = K // 16 if qtype == synth.Q6_K else K // 32
         isum = torch.full((M, N, per), -(2 ** 31), dtype=torch.int32, device="cuda")
         xq.debug_isums(qtype, Wd, buf, M, N, K, y=y, isum=isum)
         torch.cuda.synchronize()
@@ -304,6 +304,35 @@ def test_qwen3_mixed_layer(xq, M):
     assert layer_check(xq, synth.WORKLOADS["qwen3-8b-mixed-layer"], M, rows=rows) > 0
 
 
+Q80_SHAPES = [(1, 256), (5, 512), (37, 1536), (130, 4096), (3, 12288)]
+
+
+@pytest.mark.parametrize("N,K", Q80_SHAPES)
+def test_q8_0_shapes_all_m(xq, N, K):
+    # Q8_0 on the tensor-core GEMV: exact block sums (isum hook) and y for M = 1..8
+    errs = [run_and_check(xq, synth.Q8_0, N, K, M, 41 * N + K, 11 * M + N) for M in range(1, 9)]
+    assert max(errs) > 0.0
+
+
+@pytest.mark.parametrize("M", [1, 3, 8])
+def test_q8_0_layer(xq, M):
+    # a Qwen2.5-1.5B-shaped layer requantized to Q8_0, through xq_layer_mixed
+    # (one grouped Q8_0 launch; the 8960-wide down projection is split over K)
+    assert layer_check(xq, synth.WORKLOADS["qwen2.5-1.5b-q8_0-layer"], M) > 0
+
+
+def test_q8_0_extreme_bytes(xq):
+    # every int8 value as a weight, with large scales, against extreme activations
+    N, K, M = 64, 1024, 8
+    W = synth.gen_q8_0(5, N, K).reshape(N, K // 32, 34)
+    W[:, :, 2:] = (np.arange(N * (K // 32) * 32) % 256).astype(np.uint8).reshape(N, K // 32, 32)
+    W[:, :, 0:2] = np.frombuffer(np.float16(0.25).tobytes(), np.uint8)
+    x = synth.gen_x(6, M, K)
+    x[0] = 1000.0
+    x[1, ::2] = -1000.0
+    check_matmul(xq, synth.Q8_0, W.reshape(N, -1), x)
+
+
 def test_qwen3_mixed_layer_tiles(xq):
     # M > 8: every projection of the mixed layer (Q4_K and Q6_K) on the tile kernel
     assert layer_check(xq, synth.WORKLOADS["qwen3-8b-mixed-layer"], 40, rows=96) > 0
@@ -368,7 +397,8 @@ def test_misaligned_device_pointer_rejected(xq):
 
 # ------------------------------------------------------------ batch invariance
 
-@pytest.mark.parametrize("qtype,N,K", [(synth.Q4_K, 200, 1536), (synth.Q6_K, 130, 2048), (synth.Q6_K, 70, 1024)])
+@pytest.mark.parametrize("qtype,N,K", [(synth.Q4_K, 200, 1536), (synth.Q6_K, 130, 2048), (synth.Q6_K, 70, 1024),
+                                       (synth.Q8_0, 90, 1024)])
 def test_batch_invariant_rows(xq, qtype, N, K):
     """Row m of y from the batch-invariant entry points is bit-identical for
     every batch that contains token m, equal to decoding the token alone with
