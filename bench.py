@@ -580,6 +580,35 @@ def secondary_workloads(device, world):
             res[str(M)] = {"GBps": round(wl.layer_weight_bytes() / s / 1e9, 1), "us_per_layer": round(1e6 * s, 2),
                            "tokens_per_s": round(M / s, 1)}
         out[name] = {"rotated_copies": copies, "layer_bytes": wl.layer_weight_bytes(), "by_m": res}
+    # the Llama-3-8B-shaped layer with its down projection fed by
+    # silu(gate) * up of the same call (xq_layer_mixed_ffn), against the same
+    # layer with an independent down input (xq_layer_mixed)
+    wl = synth.WORKLOADS["llama3-8b-32layer"]
+    lw = synth.gen_layer_weights(wl, 0)
+    copies = max(3, -(-3 * L2_BYTES // wl.layer_weight_bytes()))
+    base = [torch.from_numpy(w.reshape(-1)).to(device) for w in lw]
+    reps = [base] + [[w.clone() for w in base] for _ in range(copies - 1)]
+    names = [p.name for p in wl.projs]
+    gi, ui, di = names.index("gate"), names.index("up"), names.index("down")
+    res = {}
+    for M in (1, 8):
+        ins = [torch.from_numpy(x).to(device) for x in synth.gen_layer_inputs(wl, M, 0)]
+        ys = [torch.empty((M, p.N), dtype=torch.float32, device=device) for p in wl.projs]
+        descs = [[(p.qtype, p.N, p.K, reps[c][t], ys[t], p.input) for t, p in enumerate(wl.projs)]
+                 for c in range(copies)]
+        ws = torch.empty(xq.layer_ffn_workspace_bytes(descs[0], 4, M, gi, ui, di), dtype=torch.uint8, device=device)
+        ws2 = torch.empty(xq.layer_workspace_bytes(descs[0], 4, M), dtype=torch.uint8, device=device)
+        row = {}
+        for label, call in (("ffn_chain", lambda c: xq.layer_mixed_ffn(descs[c], gi, ui, di, ins[:3], M, ws)),
+                            ("independent_down", lambda c: xq.layer_mixed(descs[c], ins, M, ws2))):
+            def step(call=call):
+                for c in range(copies):
+                    call(c)
+            sec = max_over_ranks(time_region(step, 5, 3, world, device), world, device) / (5 * copies)
+            row[label] = {"us_per_layer": round(1e6 * sec, 2), "GBps": round(wl.layer_weight_bytes() / sec / 1e9, 1)}
+        res[str(M)] = row
+    out["llama3-8b-layer-swiglu-down"] = {"rotated_copies": copies, "layer_bytes": wl.layer_weight_bytes(),
+                                          "by_m": res}
     # prefill tile M=512: up (Q4_K) then down (Q6_K), each launch timed on its own
     wl = synth.WORKLOADS["qwen3-8b-ffn-prefill512"]
     M = 512

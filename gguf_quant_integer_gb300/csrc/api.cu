@@ -174,9 +174,85 @@ xq_status layer_inputs(const xq_proj* proj, int n_proj, int n_inputs, int M, int
   return XQ_OK;
 }
 
+// The matmul launches of a layer whose inputs are already quantized: q8[p]
+// is projection p's Q8 buffer, sched the scheduling state sc describes
+// (zeroed by the kernel before). M <= 8: one grouped tensor-core GEMV launch
+// per weight type (kMaxProj items per launch), then the dp4a GEMV for the
+// Q6_K rows that are not 16-byte multiples; M > 8: the tile kernel per
+// projection, in the order given.
+xq_status layer_matmuls(const xq_proj* proj, int n_proj, const uint8_t* const* q8, int M, const Sched& sc,
+                        uint8_t* sched, cudaStream_t s) {
+  if (M > kMaxGemvM) {
+    for (int p = 0; p < n_proj; ++p) {
+      const xq_proj& q = proj[p];
+      if (q.N == 0) continue;
+      const xq_status st = run_matmul(q.type, q.W, q8[p], M, q.N, q.K, q.y, nullptr, s);
+      if (st != XQ_OK) return st;
+    }
+    return XQ_OK;
+  }
+  unsigned int* counter[kTypes];
+  uint8_t* arrive[kTypes];
+  uint8_t* partial[kTypes];
+  {
+    uint8_t* a = sched + kTypes * kCounterBytes;
+    uint8_t* pt = a;
+    for (int g = 0; g < kTypes; ++g) pt += sc.arrive[g];
+    for (int g = 0; g < kTypes; ++g) {
+      counter[g] = sc.dynamic[g] ? reinterpret_cast<unsigned int*>(sched + g * kCounterBytes) : nullptr;
+      arrive[g] = sc.dynamic[g] ? a : nullptr;
+      partial[g] = sc.dynamic[g] ? pt : nullptr;
+      a += sc.arrive[g];
+      pt += sc.partial[g];
+    }
+  }
+  for (int g = 0; g < kTypes; ++g) {
+    const int type = kTypeIds[g];
+    xq::MmaProj items[xq::kMaxProj];
+    int n = 0;
+    for (int p = 0; p <= n_proj; ++p) {
+      if (p < n_proj) {
+        const xq_proj& q = proj[p];
+        if (!in_group(q, M) || q.type != type) continue;
+        xq::MmaProj& it = items[n++];
+        it.W = static_cast<const uint8_t*>(q.W);
+        it.xq = q8[p];
+        it.y = q.y;
+        it.isum = nullptr;
+        it.N = q.N;
+        it.K = q.K;
+        it.M_total = M;
+        it.chunk = 0;
+        it.nch = sc.nch[p];
+      }
+      if (n > 0 && (n == xq::kMaxProj || p == n_proj)) {
+        if (xq::launch_gemv_mma(type, items, n, s, true, counter[g], arrive[g], partial[g]) != cudaSuccess)
+          return XQ_ERR_CUDA;
+        n = 0;
+      }
+    }
+  }
+  for (int p = 0; p < n_proj; ++p) {
+    const xq_proj& q = proj[p];
+    if (q.N == 0 || in_group(q, M)) continue;
+    const xq_status st = run_matmul(q.type, q.W, q8[p], M, q.N, q.K, q.y, nullptr, s);
+    if (st != XQ_OK) return st;
+  }
+  return XQ_OK;
+}
+
+// Bytes of the scheduling state sc describes, all of it zeroed before the
+// matmuls (counters and arrival counts) or written before it is read.
+size_t sched_zero_bytes(const Sched& sc) {
+  size_t z = kTypes * kCounterBytes;
+  for (int g = 0; g < kTypes; ++g) z += sc.arrive[g];
+  return z;
+}
+
 }  // namespace
 
 extern "C" {
+
 
 const char* xq_status_str(xq_status s) {
   switch (s) {
@@ -320,31 +396,11 @@ xq_status xq_layer_mixed(const xq_proj* proj, int n_proj, const float* const* in
   }
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  // scheduling state: counters, arrival counts (zeroed by the quantize
-  // launch; the matmuls leave them at zero), partial sums
-  unsigned int* counter[kTypes];
-  uint8_t* arrive[kTypes];
-  uint8_t* partial[kTypes];
-  {
-    uint8_t* c = ws + sched_off;
-    uint8_t* a = c + kTypes * kCounterBytes;
-    uint8_t* pt = a;
-    for (int g = 0; g < kTypes; ++g) pt += sc.arrive[g];
-    for (int g = 0; g < kTypes; ++g) {
-      counter[g] = sc.dynamic[g] ? reinterpret_cast<unsigned int*>(c + g * kCounterBytes) : nullptr;
-      arrive[g] = sc.dynamic[g] ? a : nullptr;
-      partial[g] = sc.dynamic[g] ? pt : nullptr;
-      a += sc.arrive[g];
-      pt += sc.partial[g];
-    }
-  }
+  // scheduling state: counters and arrival counts, zeroed by the quantize
+  // launch (the matmuls leave them at zero), then partial sums
   bool any_dynamic = false;
-  size_t zero_bytes = kTypes * kCounterBytes;
-  for (int g = 0; g < kTypes; ++g) {
-    any_dynamic = any_dynamic || sc.dynamic[g];
-    zero_bytes += sc.arrive[g];
-  }
-  const int zero_words = static_cast<int>(zero_bytes / 4);
+  for (int g = 0; g < kTypes; ++g) any_dynamic = any_dynamic || sc.dynamic[g];
+  const int zero_words = static_cast<int>(sched_zero_bytes(sc) / 4);
   // One launch quantizes every input that is read (up to kMaxProj per launch).
   {
     xq::QuantJob jobs[xq::kMaxProj];
@@ -365,52 +421,164 @@ xq_status xq_layer_mixed(const xq_proj* proj, int n_proj, const float* const* in
       }
     }
   }
-  if (M > kMaxGemvM) {
-    // every projection on the tile kernel, in the order given
-    for (int p = 0; p < n_proj; ++p) {
-      const xq_proj& q = proj[p];
-      if (q.N == 0) continue;
-      st = run_matmul(q.type, q.W, ws + off[q.input], M, q.N, q.K, q.y, nullptr, s);
-      if (st != XQ_OK) return st;
-    }
-    return XQ_OK;
+  const uint8_t* q8[64];
+  for (int p = 0; p < n_proj; ++p) q8[p] = ws + off[proj[p].input];
+  return layer_matmuls(proj, n_proj, q8, M, sc, ws + sched_off, s);
+}
+
+xq_status xq_silu_mul_quantize_q8(const float* gate, const float* up, int M, int K, void* xq, float* h_out,
+                                  xq_stream stream) {
+  if (M < 0 || K <= 0 || (K % 256) != 0) return XQ_ERR_SHAPE;
+  if (M == 0) return XQ_OK;
+  if (!gate || !up || !xq) return XQ_ERR_ARG;
+  if (!aligned16(gate) || !aligned16(up) || !aligned16(xq)) return XQ_ERR_ALIGN;
+  xq::QuantJob job;
+  job.x = gate;
+  job.up = up;
+  job.h_out = h_out;
+  job.xq = static_cast<uint8_t*>(xq);
+  job.M = M;
+  job.K = K;
+  const cudaError_t e = xq::launch_quantize_q8(&job, 1, reinterpret_cast<cudaStream_t>(stream), true);
+  return e == cudaSuccess ? XQ_OK : XQ_ERR_CUDA;
+}
+
+}  // extern "C"
+
+namespace {
+
+// The layer with a SwiGLU-fed down projection, in four launches: the Q8
+// quantization of every input; the gate and up projections (group A);
+// h = silu(y_gate) * y_up quantized to Q8; every other projection together
+// with down (group C), so that the projections that do not depend on gate
+// and up share down's grouped launch. Workspace: the inputs' Q8 buffers,
+// h's Q8 buffer, then the scheduling state of A and of C.
+struct FfnPlan {
+  xq_proj a[2], c[64];
+  int n_c;
+  int c_input[64];  // layer input of each C projection, -1 for down (reads h)
+  int in_k[64];
+  size_t off[64];
+  size_t h_off, sched_a, sched_c, total;
+  Sched sc_a, sc_c;
+};
+
+xq_status ffn_plan(const xq_proj* proj, int n_proj, int n_inputs, int M, int gate, int up, int down, FfnPlan* f) {
+  if (!proj || n_proj < 3 || n_proj > 64 || n_inputs < 0 || n_inputs > 64) return XQ_ERR_ARG;
+  if (gate < 0 || up < 0 || down < 0 || gate >= n_proj || up >= n_proj || down >= n_proj || gate == up ||
+      gate == down || up == down)
+    return XQ_ERR_ARG;
+  if (proj[gate].N != proj[up].N || proj[down].K != proj[gate].N) return XQ_ERR_SHAPE;
+  xq_proj rest[64];
+  int n_rest = 0;
+  for (int p = 0; p < n_proj; ++p)
+    if (p != down) rest[n_rest++] = proj[p];
+  xq_status st = layer_inputs(rest, n_rest, n_inputs, M, f->in_k);
+  if (st != XQ_OK) return st;
+  xq_proj d = proj[down];
+  d.input = 0;
+  int dk[1];
+  st = layer_inputs(&d, 1, 1, M, dk);
+  if (st != XQ_OK) return st;
+  f->a[0] = proj[gate];
+  f->a[1] = proj[up];
+  f->n_c = 0;
+  for (int p = 0; p < n_proj; ++p) {
+    if (p == gate || p == up) continue;
+    f->c_input[f->n_c] = p == down ? -1 : proj[p].input;
+    f->c[f->n_c++] = p == down ? d : proj[p];
   }
-  // One grouped tensor-core GEMV launch per weight type (kMaxProj items per
-  // launch; M <= 8 is one chunk per projection), Q4_K first.
-  for (int g = 0; g < kTypes; ++g) {
-    const int type = kTypeIds[g];
-    xq::MmaProj items[xq::kMaxProj];
-    int n = 0;
-    for (int p = 0; p <= n_proj; ++p) {
-      if (p < n_proj) {
-        const xq_proj& q = proj[p];
-        if (!in_group(q, M) || q.type != type) continue;
-        xq::MmaProj& it = items[n++];
-        it.W = static_cast<const uint8_t*>(q.W);
-        it.xq = ws + off[q.input];
-        it.y = q.y;
-        it.isum = nullptr;
-        it.N = q.N;
-        it.K = q.K;
-        it.M_total = M;
-        it.chunk = 0;
-        it.nch = sc.nch[p];
-      }
-      if (n > 0 && (n == xq::kMaxProj || p == n_proj)) {
-        if (xq::launch_gemv_mma(type, items, n, s, true, counter[g], arrive[g], partial[g]) != cudaSuccess)
+  size_t need = 0;
+  for (int i = 0; i < n_inputs; ++i) {
+    f->off[i] = need;
+    if (f->in_k[i]) need += round256(xq_q8_bytes(M, f->in_k[i]));
+  }
+  f->h_off = need;
+  need += round256(xq_q8_bytes(M, d.K));
+  f->sc_a = sched_layout(f->a, 2, M);
+  f->sc_c = sched_layout(f->c, f->n_c, M);
+  f->sched_a = need;
+  need += round256(sched_bytes(f->sc_a));
+  f->sched_c = need;
+  need += sched_bytes(f->sc_c);
+  f->total = need;
+  return XQ_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t xq_layer_ffn_workspace_bytes(const xq_proj* proj, int n_proj, int n_inputs, int M, int gate, int up,
+                                    int down) {
+  FfnPlan f;
+  if (ffn_plan(proj, n_proj, n_inputs, M, gate, up, down, &f) != XQ_OK) return 0;
+  return f.total;
+}
+
+xq_status xq_layer_mixed_ffn(const xq_proj* proj, int n_proj, int gate, int up, int down,
+                             const float* const* inputs, int n_inputs, int M, void* workspace, size_t ws_bytes,
+                             xq_stream stream) {
+  FfnPlan f;
+  xq_status st = ffn_plan(proj, n_proj, n_inputs, M, gate, up, down, &f);
+  if (st != XQ_OK) return st;
+  if (M == 0) return XQ_OK;
+  if (n_inputs > 0 && !inputs) return XQ_ERR_ARG;
+  for (int i = 0; i < n_inputs; ++i)
+    if (f.in_k[i]) {
+      if (!inputs[i]) return XQ_ERR_ARG;
+      if (!aligned16(inputs[i])) return XQ_ERR_ALIGN;
+    }
+  if (!workspace) return XQ_ERR_ARG;
+  if (ws_bytes < f.total) return XQ_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return XQ_ERR_ALIGN;
+  for (int p = 0; p < n_proj; ++p) {
+    if (proj[p].N == 0) continue;
+    if (!proj[p].W || !proj[p].y) return XQ_ERR_ARG;
+    if (!aligned16(proj[p].W) || !aligned16(proj[p].y)) return XQ_ERR_ALIGN;
+  }
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // 1. every input to Q8 (the last launch zeroes A's scheduling state)
+  {
+    xq::QuantJob jobs[xq::kMaxProj];
+    int n = 0, left = 0;
+    for (int i = 0; i < n_inputs; ++i) left += f.in_k[i] ? 1 : 0;
+    for (int i = 0; i < n_inputs; ++i) {
+      if (!f.in_k[i]) continue;
+      xq::QuantJob& j = jobs[n++];
+      j.x = inputs[i];
+      j.xq = ws + f.off[i];
+      j.M = M;
+      j.K = f.in_k[i];
+      --left;
+      if (n == xq::kMaxProj || left == 0) {
+        unsigned int* zero = left == 0 ? reinterpret_cast<unsigned int*>(ws + f.sched_a) : nullptr;
+        if (xq::launch_quantize_q8(jobs, n, s, true, zero, static_cast<int>(sched_zero_bytes(f.sc_a) / 4)) !=
+            cudaSuccess)
           return XQ_ERR_CUDA;
         n = 0;
       }
     }
   }
-  // the rest (Q6_K rows that are not 16-byte multiples) on the dp4a GEMV
-  for (int p = 0; p < n_proj; ++p) {
-    const xq_proj& q = proj[p];
-    if (q.N == 0 || in_group(q, M)) continue;
-    st = run_matmul(q.type, q.W, ws + off[q.input], M, q.N, q.K, q.y, nullptr, s);
-    if (st != XQ_OK) return st;
-  }
-  return XQ_OK;
+  // 2. gate and up
+  const uint8_t* q8a[2] = {ws + f.off[f.a[0].input], ws + f.off[f.a[1].input]};
+  st = layer_matmuls(f.a, 2, q8a, M, f.sc_a, ws + f.sched_a, s);
+  if (st != XQ_OK) return st;
+  // 3. h = silu(y_gate) * y_up -> Q8 (zeroing C's scheduling state)
+  xq::QuantJob job;
+  job.x = f.a[0].y;
+  job.up = f.a[1].y;
+  job.xq = ws + f.h_off;
+  job.M = M;
+  job.K = proj[down].K;
+  if (xq::launch_quantize_q8(&job, 1, s, true, reinterpret_cast<unsigned int*>(ws + f.sched_c),
+                             static_cast<int>(sched_zero_bytes(f.sc_c) / 4)) != cudaSuccess)
+    return XQ_ERR_CUDA;
+  // 4. the other projections and down
+  const uint8_t* q8c[64];
+  for (int k = 0; k < f.n_c; ++k) q8c[k] = f.c_input[k] < 0 ? ws + f.h_off : ws + f.off[f.c_input[k]];
+  return layer_matmuls(f.c, f.n_c, q8c, M, f.sc_c, ws + f.sched_c, s);
 }
 
 }  // extern "C"

@@ -34,6 +34,8 @@ __device__ __forceinline__ int tile_offset(int r, int ks) {
 // One input of a grouped launch, with its buffer layout resolved on the host.
 struct QuantItem {
   const float* x;
+  const float* up;  // non-null: quantize h = silu(x) * up
+  float* h_out;     // optional copy of h
   uint8_t* xq;
   size_t d8, s8, frag, fsc, tile;  // byte offsets in xq (layout in xq_common.cuh)
   int M, K, nsub, ttiles;
@@ -79,7 +81,16 @@ quantize_q8_kernel(const __grid_constant__ QuantGroup G) {
     float d = 0.0f, s = 0.0f;
     int q = 0;
     if (m < J.M) {
-      const float v = __ldg(J.x + static_cast<size_t>(m) * J.K + 32 * j + lane);
+      const size_t idx = static_cast<size_t>(m) * J.K + 32 * j + lane;
+      float v = __ldg(J.x + idx);
+      if (J.up) {
+        // SwiGLU feed of the down projection: h = silu(g) * u = g / (1 + e^-g) * u,
+        // each step one fp32 operation (CUDA's expf, IEEE add, divide and
+        // multiply); g -> -inf gives e^-g = inf and h = +-0.
+        const float e = expf(-v);
+        v = __fmul_rn(__fdiv_rn(v, __fadd_rn(1.0f, e)), __ldg(J.up + idx));
+        if (J.h_out) J.h_out[idx] = v;
+      }
       // |x| >= 0, so its IEEE bit pattern orders like the value itself.
       const unsigned amax_bits = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(v)));
       const float amax = __uint_as_float(amax_bits);
@@ -149,6 +160,8 @@ cudaError_t launch_quantize_q8(const QuantJob* jobs, int n, cudaStream_t s, bool
     const Q8Layout L = q8_layout(q.M, q.K, q.gemv_image);
     QuantItem& it = G.job[k];
     it.x = q.x;
+    it.up = q.up;
+    it.h_out = q.h_out;
     it.xq = q.xq;
     it.d8 = L.d8;
     it.s8 = L.s8;

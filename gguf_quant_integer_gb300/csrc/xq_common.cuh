@@ -153,6 +153,10 @@ struct QuantJob {
   uint8_t* xq;      // Q8 buffer (layout above)
   int M, K;
   bool gemv_image = false;  // 8-token GEMV image for any M (batch-invariant layout)
+  // With up: the quantized value is h = silu(x) * up (x the gate output, up
+  // the up output, both fp32 [M][K]), optionally written to h_out.
+  const float* up = nullptr;
+  float* h_out = nullptr;
 };
 
 // One launch quantizing up to kMaxProj activations; also zeroes the

@@ -27,7 +27,8 @@ SYMBOLS = ("xq_status_str", "xq_q8_bytes", "xq_weight_bytes", "xq_quantize_q8",
            "xq_matmul_q4k_q8", "xq_matmul_q6k_q8", "xq_layer_workspace_bytes",
            "xq_layer_mixed", "xq_debug_isums_q4k", "xq_debug_isums_q6k", "xq_layer_mixed_static",
            "xq_q8_bytes_invariant", "xq_quantize_q8_invariant", "xq_matmul_invariant",
-           "xq_matmul_q8_0_q8", "xq_debug_isums_q8_0")
+           "xq_matmul_q8_0_q8", "xq_debug_isums_q8_0", "xq_silu_mul_quantize_q8",
+           "xq_layer_ffn_workspace_bytes", "xq_layer_mixed_ffn")
 
 
 class XQError(RuntimeError):
@@ -62,6 +63,13 @@ def lib(path: str | None = None):
     L.xq_weight_bytes.argtypes = [I, I, I]
     L.xq_weight_bytes.restype = S
     L.xq_quantize_q8.argtypes = [P, I, I, P, P]
+    L.xq_silu_mul_quantize_q8.argtypes = [P, P, I, I, P, P, P]
+    L.xq_silu_mul_quantize_q8.restype = I
+    L.xq_layer_ffn_workspace_bytes.argtypes = [ctypes.POINTER(xq_proj), I, I, I, I, I, I]
+    L.xq_layer_ffn_workspace_bytes.restype = S
+    L.xq_layer_mixed_ffn.argtypes = [ctypes.POINTER(xq_proj), I, I, I, I, ctypes.POINTER(ctypes.c_void_p), I, I,
+                                     P, S, P]
+    L.xq_layer_mixed_ffn.restype = I
     L.xq_q8_bytes_invariant.argtypes = [I, I]
     L.xq_q8_bytes_invariant.restype = S
     L.xq_quantize_q8_invariant.argtypes = [P, I, I, P, P]
@@ -211,6 +219,30 @@ def layer_mixed(projs, inputs, M: int, workspace, stream=None):
     rc = lib().xq_layer_mixed(arr, len(projs), ins, len(inputs), M, _ptr(workspace),
                               workspace.numel() if workspace is not None else 0, _stream(stream))
     _check("xq_layer_mixed", rc)
+
+
+def silu_mul_quantize_q8(gate, up, out=None, h_out=None, stream=None):
+    """Q8 of h = silu(gate) * up (fp32 CUDA tensors [M, K]); h_out optional."""
+    import torch
+    M, K = gate.shape
+    if out is None:
+        out = torch.empty(q8_bytes(M, K), dtype=torch.uint8, device=gate.device)
+    _check("xq_silu_mul_quantize_q8",
+           lib().xq_silu_mul_quantize_q8(_ptr(gate), _ptr(up), M, K, _ptr(out), _ptr(h_out), _stream(stream)))
+    return out
+
+
+def layer_ffn_workspace_bytes(projs, n_inputs: int, M: int, gate: int, up: int, down: int) -> int:
+    return lib().xq_layer_ffn_workspace_bytes(_proj_array(projs), len(projs), n_inputs, M, gate, up, down)
+
+
+def layer_mixed_ffn(projs, gate: int, up: int, down: int, inputs, M: int, workspace, stream=None):
+    """layer_mixed with projs[down] fed by silu(y_gate) * y_up of the same call."""
+    arr = _proj_array(projs)
+    ins = (ctypes.c_void_p * max(1, len(inputs)))(*[t.data_ptr() for t in inputs])
+    rc = lib().xq_layer_mixed_ffn(arr, len(projs), gate, up, down, ins, len(inputs), M, _ptr(workspace),
+                                  workspace.numel() if workspace is not None else 0, _stream(stream))
+    _check("xq_layer_mixed_ffn", rc)
 
 
 def layer_mixed_static(projs, inputs, M: int, stream=None):

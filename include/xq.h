@@ -196,6 +196,36 @@ XQ_API xq_status xq_layer_mixed(const xq_proj *proj, int n_proj,
                          const float *const *inputs, int n_inputs, int M,
                          void *workspace, size_t ws_bytes, xq_stream stream);
 
+/* The SwiGLU feed of a down projection: h = silu(gate) * up, then the Q8
+ * quantization of h, in one launch (the step either side of the matmul
+ * path in the Agent Telemetry log's dispatch; silu(g) = g / (1 + e^-g)).
+ *   gate, up : fp32 [M][K], device (the gate and up projection outputs).
+ *   xq       : device buffer of xq_q8_bytes(M, K) bytes, written as by
+ *              xq_quantize_q8 from h.
+ *   h_out    : optional fp32 [M][K], device: receives h.
+ * Each step is one fp32 operation: e = expf(-g) (CUDA's expf, within its
+ * documented error bound, not correctly rounded), g / (1 + e) and the
+ * product with u rounded to nearest; h then goes through the Q8 rules of
+ * xq_quantize_q8. Shape and alignment rules as for xq_quantize_q8. */
+XQ_API xq_status xq_silu_mul_quantize_q8(const float *gate, const float *up, int M, int K, void *xq,
+                                  float *h_out, xq_stream stream);
+
+/* Workspace bytes of xq_layer_mixed_ffn (0 on bad arguments). */
+XQ_API size_t xq_layer_ffn_workspace_bytes(const xq_proj *proj, int n_proj, int n_inputs, int M,
+                                    int gate, int up, int down);
+
+/* xq_layer_mixed for a layer whose down projection reads silu(y_gate) * y_up
+ * of the same call (gate, up, down: indices into proj; proj[down].input is
+ * ignored; N of gate and up must equal K of down). Enqueues, in order on
+ * `stream`: the Q8 quantization of every input; the gate and up projections;
+ * one xq_silu_mul_quantize_q8 launch on their outputs; every other
+ * projection together with down (one grouped GEMV launch per weight type at
+ * M <= 8, split over K like the layer's; the tile kernel at M > 8). The
+ * projections that do not depend on gate and up thus share down's launch. */
+XQ_API xq_status xq_layer_mixed_ffn(const xq_proj *proj, int n_proj, int gate, int up, int down,
+                             const float *const *inputs, int n_inputs, int M,
+                             void *workspace, size_t ws_bytes, xq_stream stream);
+
 /* Fixed workspace size of xq_layer_mixed_static: 4 MiB per device. */
 #define XQ_LAYER_STATIC_SCRATCH_BYTES (4u << 20)
 

@@ -136,3 +136,24 @@ def test_q8_0_entry_points_reject_before_launch(L):
     assert L.xq_layer_workspace_bytes(arr, 1, 1, 8) > 0
     ins = (ctypes.c_void_p * 1)(FAKE)
     assert L.xq_layer_mixed(arr, 1, ins, 1, 9, P(FAKE), 1 << 20, None) == 6
+
+
+def test_ffn_entry_points_reject_before_launch(L):
+    from gguf_quant_integer_gb300 import xq
+    P = ctypes.c_void_p
+    # gate, up: N = 512; down: K = 512 -> N = 256
+    specs = [(12, 512, 256, 0), (12, 512, 256, 0), (12, 256, 512, 1)]
+    arr = xq._proj_array([(t, n, k, None, None, i) for (t, n, k, i) in specs])
+    good = L.xq_layer_ffn_workspace_bytes(arr, 3, 1, 4, 0, 1, 2)
+    assert good > L.xq_layer_workspace_bytes(arr, 2, 1, 4)   # + h's Q8 buffer and down's state
+    assert L.xq_layer_ffn_workspace_bytes(arr, 3, 1, 4, 0, 0, 2) == 0   # gate == up
+    assert L.xq_layer_ffn_workspace_bytes(arr, 3, 1, 4, 0, 1, 3) == 0   # index out of range
+    bad = xq._proj_array([(t, n, k, None, None, i) for (t, n, k, i) in [(12, 512, 256, 0), (12, 384, 256, 0),
+                                                                      (12, 256, 512, 1)]])
+    assert L.xq_layer_ffn_workspace_bytes(bad, 3, 1, 4, 0, 1, 2) == 0   # gate and up N differ
+    ins = (ctypes.c_void_p * 1)(FAKE)
+    assert L.xq_layer_mixed_ffn(bad, 3, 0, 1, 2, ins, 1, 4, P(FAKE), 1 << 20, None) == 2
+    assert L.xq_layer_mixed_ffn(arr, 3, 0, 1, 2, ins, 1, 4, P(FAKE), good - 1, None) == 4
+    assert L.xq_silu_mul_quantize_q8(P(FAKE), P(FAKE), 2, 300, P(FAKE), None, None) == 2
+    assert L.xq_silu_mul_quantize_q8(P(FAKE + 4), P(FAKE), 2, 256, P(FAKE), None, None) == 3
+    assert L.xq_silu_mul_quantize_q8(None, P(FAKE), 2, 256, P(FAKE), None, None) == 1

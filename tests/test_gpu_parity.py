@@ -437,3 +437,75 @@ def test_batch_invariant_rows(xq, qtype, N, K):
         xq.matmul(qtype, Wd, buf1, 1, N, K, y=y1)
         torch.cuda.synchronize()
         assert np.array_equal(y1.cpu().numpy().view(np.uint32), y_full[m:m + 1].view(np.uint32)), m
+
+
+# ------------------------------------------------------------ SwiGLU feed
+
+def silu_mul_ref(g, u):
+    g = g.astype(np.float64)
+    with np.errstate(over="ignore"):   # e^-g = inf for g << 0: h -> -0, as on the GPU
+        return g / (1.0 + np.exp(-g)) * u.astype(np.float64)
+
+
+def check_h(h_gpu, g, u):
+    # e = expf(-g) is within 2 ulp (CUDA's documented bound); 1 + e, the
+    # divide and the product are each rounded once: together within 8 ulp of
+    # the exact silu(g) * u (relative 2^-20), or tiny where h underflows.
+    h_ref = silu_mul_ref(g, u)
+    err = np.abs(h_gpu.astype(np.float64) - h_ref)
+    assert np.all(err <= 2.0 ** -20 * np.abs(h_ref) + 1e-37), float(np.max(err / (np.abs(h_ref) + 1e-37)))
+
+
+@pytest.mark.parametrize("M,K", [(1, 256), (5, 2048), (20, 512)])
+def test_silu_mul_quantize(xq, M, K):
+    rng = np.random.default_rng(M * 1000 + K)
+    g = (rng.standard_normal((M, K)) * 4).astype(np.float32)
+    u = rng.standard_normal((M, K)).astype(np.float32)
+    g[0, :32] = np.array([-100, -88, -87, 0, 88, 89, 100, -1e30, 1e30, -0.0] + [0.0] * 22, np.float32)
+    g[0, 32:64] = 0.0                                   # h = 0 block
+    h = torch.empty((M, K), dtype=torch.float32, device="cuda")
+    buf = xq.silu_mul_quantize_q8(dev(g), dev(u), h_out=h)
+    torch.cuda.synchronize()
+    h_gpu = h.cpu().numpy()
+    check_h(h_gpu, g, u)
+    # the Q8 of h is the oracle's quantization of the same fp32 values, bit for bit
+    qs, d8, s8 = (t.cpu().numpy() for t in xq.q8_views(buf, M, K))
+    rq, rd, rs = oracle.quantize_q8(h_gpu)
+    assert np.array_equal(qs, rq)
+    assert np.array_equal(d8.view(np.uint32), rd.view(np.uint32))
+    assert np.array_equal(s8.view(np.uint32), rs.view(np.uint32))
+
+
+@pytest.mark.parametrize("M", [1, 8, 20])
+def test_ffn_layer_down_fed_by_silu_gate_up(xq, M):
+    """xq_layer_mixed_ffn on a Qwen2.5-1.5B-shaped layer: every projection
+    but down checked as in xq_layer_mixed; down checked against the oracle on
+    the Q8 of h recomputed (same kernel, h exported) from the gate and up
+    outputs the call wrote."""
+    wl = synth.WORKLOADS["qwen2.5-1.5b-layer"]
+    weights = synth.gen_layer_weights(wl, 0)
+    inputs = synth.gen_layer_inputs(wl, M, 0)[:3]   # attn-in, o-in, ffn-in; down reads h
+    Wd = [dev(w.reshape(-1)) for w in weights]
+    ys = [poisoned(M, p.N) for p in wl.projs]
+    desc = [(p.qtype, p.N, p.K, Wd[t], ys[t], min(p.input, 2)) for t, p in enumerate(wl.projs)]
+    names = [p.name for p in wl.projs]
+    gi, ui, di = names.index("gate"), names.index("up"), names.index("down")
+    ws = torch.zeros(xq.layer_ffn_workspace_bytes(desc, 3, M, gi, ui, di), dtype=torch.uint8, device="cuda")
+    xq.layer_mixed_ffn(desc, gi, ui, di, [dev(x) for x in inputs], M, ws)
+    torch.cuda.synchronize()
+    q8 = [oracle.quantize_q8(x) for x in inputs]
+    for t, p in enumerate(wl.projs):
+        if t == di:
+            continue
+        rq, rd, _ = q8[p.input]
+        y_ref, ab, _ = oracle.matmul(p.qtype, weights[t], rq, rd, p.K)
+        check_y(ys[t].cpu().numpy(), y_ref, ab)
+    g, u = ys[gi], ys[ui]
+    h = torch.empty_like(g)
+    xq.silu_mul_quantize_q8(g, u, h_out=h)
+    torch.cuda.synchronize()
+    h_gpu = h.cpu().numpy()
+    check_h(h_gpu, g.cpu().numpy(), u.cpu().numpy())
+    rq, rd, _ = oracle.quantize_q8(h_gpu)
+    y_ref, ab, _ = oracle.matmul(wl.projs[di].qtype, weights[di], rq, rd, wl.projs[di].K)
+    check_y(ys[di].cpu().numpy(), y_ref, ab)
