@@ -18,7 +18,8 @@ Prints ONE JSON line (rank 0). Extra objects on it:
               Qwen3-8B FFN prefill tile;
   cpu_baseline the CPU oracle on a bounded sample of the same sweep;
   e2e         the same metric through the public API with pinned host
-              inputs/outputs copied inside the timed region.
+              inputs/outputs copied inside the timed region (the step's
+              activations and outputs packed, one copy per direction).
 
 `--impl reference` times the CPU oracle instead (rank 0 only).
 """
@@ -495,19 +496,39 @@ def gpu_arm(args):
     # ---- e2e through the public API: pinned host in/out copied in the timed region
     e2e = None
     if not args.no_e2e:
-        ins, ys, descs, ws = sweep.state[M]
-        h_in = [[x.cpu().pin_memory() for x in li] for li in ins]
-        h_out = [[torch.empty(y.shape, dtype=y.dtype).pin_memory() for y in ly] for ly in ys]
-        h2d = sum(x.numel() * 4 for li in h_in for x in li)
-        d2h = sum(y.numel() * 4 for ly in h_out for y in ly)
+        ins0, ys0, descs0, ws = sweep.state[M]
+        # The step's activations live in one pinned host buffer and its
+        # outputs in one device buffer, so each direction is one copy per
+        # step (the layer calls read and write views into them).
+        def pack(tensors, device_):
+            sizes = [t.numel() for lt in tensors for t in lt]
+            flat = torch.empty(sum(sizes), dtype=torch.float32, device=device_)
+            views, o = [], 0
+            for lt in tensors:
+                row = []
+                for t in lt:
+                    row.append(flat[o:o + t.numel()].view(t.shape))
+                    o += t.numel()
+                views.append(row)
+            return flat, views
+
+        d_in, ins = pack(ins0, device)
+        for li, l0 in zip(ins, ins0):
+            for v, x in zip(li, l0):
+                v.copy_(x)
+        h_in = d_in.cpu().pin_memory()
+        d_out, ys = pack(ys0, device)
+        h_out = torch.empty(d_out.shape, dtype=torch.float32).pin_memory()
+        descs = [[(t, n, k, w, ys[l][j], inp) for j, (t, n, k, w, _, inp) in enumerate(dl)]
+                 for l, dl in enumerate(descs0)]
+        h2d = h_in.numel() * 4
+        d2h = h_out.numel() * 4
 
         def e2e_step():
+            d_in.copy_(h_in, non_blocking=True)
             for l in range(len(sweep.W)):
-                for d, h in zip(ins[l], h_in[l]):
-                    d.copy_(h, non_blocking=True)
                 xq.layer_mixed(descs[l], ins[l], M, ws)
-                for h, d in zip(h_out[l], ys[l]):
-                    h.copy_(d, non_blocking=True)
+            h_out.copy_(d_out, non_blocking=True)
 
         s = time_region(e2e_step, args.steps, max(3, args.warmup), world, device)
         s = max_over_ranks(s, world, device) / args.steps
