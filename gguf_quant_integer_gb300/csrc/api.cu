@@ -206,6 +206,12 @@ xq_status layer_matmuls(const xq_proj* proj, int n_proj, const uint8_t* const* q
       pt += sc.partial[g];
     }
   }
+  // Only the first grouped launch waits for the previous grid on the stream
+  // (the quantizer). The later ones start as its CTAs drain: they read
+  // nothing it writes, and its CTAs trigger their launch only after their own
+  // wait for the quantizer. They wait for the earlier grids before exiting,
+  // which keeps the stream's order for the kernels that follow.
+  bool first_launch = true;
   for (int g = 0; g < kTypes; ++g) {
     const int type = kTypeIds[g];
     xq::MmaProj items[xq::kMaxProj];
@@ -226,8 +232,10 @@ xq_status layer_matmuls(const xq_proj* proj, int n_proj, const uint8_t* const* q
         it.nch = sc.nch[p];
       }
       if (n > 0 && (n == xq::kMaxProj || p == n_proj)) {
-        if (xq::launch_gemv_mma(type, items, n, s, true, counter[g], arrive[g], partial[g]) != cudaSuccess)
+        if (xq::launch_gemv_mma(type, items, n, s, true, counter[g], arrive[g], partial[g], first_launch) !=
+            cudaSuccess)
           return XQ_ERR_CUDA;
+        first_launch = false;
         n = 0;
       }
     }

@@ -80,6 +80,10 @@ struct Group {
   Proj p[kMaxProj];
   unsigned int* counter;  // dynamic task counter (zeroed before launch) or null
   int n, total;
+  // 0: the launch needs nothing the previous grid on the stream writes (it
+  // follows another grouped launch of the same layer, whose CTAs trigger only
+  // after their own wait for the quantizer): skip the dependency wait.
+  int wait_prev;
 };
 
 constexpr int kDecBytes = 8 * 16 * 16;  // per warp: one float4 per (32-block, row)
@@ -437,8 +441,9 @@ __device__ __forceinline__ int next_task(const Group& G, int cur) {
 }
 
 template <int TYPE, bool ISUM>
-__global__ void __launch_bounds__(160, 3)
-gemv_mma_kernel(const __grid_constant__ Group G) {
+__device__ __forceinline__ void gemv_mma_body(const Group& G) {
+  // Body of gemv_mma_kernel: a return here leaves through the kernel's
+  // deferred dependency wait.
   using Lay = GLay<TYPE>;
   constexpr int kStages = Lay::kStages, kStageBytes = Lay::kStageBytes, kBlockBytes = Lay::kBlockBytes;
   constexpr int kFragOff = Lay::kFragOff, kFscOff = Lay::kFscOff;
@@ -489,7 +494,7 @@ gemv_mma_kernel(const __grid_constant__ Group G) {
       }
       bresume = b;
     }
-    cudaGridDependencySynchronize();
+    if (G.wait_prev) cudaGridDependencySynchronize();
     cudaTriggerProgrammaticLaunchCompletion();
     if (task < G.total) {
       const TaskPos tp = task_pos(G, task);
@@ -538,7 +543,7 @@ gemv_mma_kernel(const __grid_constant__ Group G) {
   }
 
   // --------------------------------------------------------- consumers
-  cudaGridDependencySynchronize();
+  if (G.wait_prev) cudaGridDependencySynchronize();
   cudaTriggerProgrammaticLaunchCompletion();
   const int n8 = lane >> 2, t = lane & 3;
   float4* dec = dec_all + warp * (kDecBytes / 16);
@@ -649,6 +654,17 @@ gemv_mma_kernel(const __grid_constant__ Group G) {
 }
 
 template <int TYPE, bool ISUM>
+__global__ void __launch_bounds__(160, 3)
+gemv_mma_kernel(const __grid_constant__ Group G) {
+  gemv_mma_body<TYPE, ISUM>(G);
+  // A launch that did not wait for the previous grid on entry waits before
+  // its threads exit, so that its completion still implies the completion of
+  // every earlier kernel on the stream (the next kernel's dependency wait
+  // relies on that).
+  if (!G.wait_prev) cudaGridDependencySynchronize();
+}
+
+template <int TYPE, bool ISUM>
 int max_ctas() {
   static int per_sm = -1;
   if (per_sm < 0) {
@@ -716,7 +732,7 @@ bool gemv_mma_supports(int type, int K) {
 }
 
 cudaError_t launch_gemv_mma(int type, const MmaProj* projs, int n, cudaStream_t s, bool pdl, unsigned int* counter,
-                            uint8_t* arrive_ws, uint8_t* partial_ws) {
+                            uint8_t* arrive_ws, uint8_t* partial_ws, bool wait_prev) {
   if (n <= 0 || n > kMaxProj || (type != 12 && type != 14 && type != 8)) return cudaErrorInvalidValue;
   // Per-projection K-chunking (only with split workspaces) and task cost.
   const bool split = arrive_ws != nullptr && partial_ws != nullptr;
@@ -749,6 +765,7 @@ cudaError_t launch_gemv_mma(int type, const MmaProj* projs, int n, cudaStream_t 
   Group G;
   G.n = n;
   G.counter = counter;
+  G.wait_prev = (wait_prev || !pdl) ? 1 : 0;
   int total = 0;
   bool isum = false;
   for (int k = 0; k < n; ++k) {
