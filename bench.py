@@ -47,6 +47,8 @@ HEADLINE = "llama3-8b-32layer"
 
 
 # workloads --profile-workload runs (one launch per call)
+# The headline metric, the same string on both arms.
+METRIC = "Q4_K/Q6_K x Q8 matmul weight GB/s (M=%d) and %% of GB300 HBM roofline"
 PROFILE_WORKLOADS = ("prefill512-up", "prefill512-down", "qwen3-q6k-layer", "llama3-layer")
 
 
@@ -244,7 +246,7 @@ def reference_arm(args):
     sample_desc = (f"layer 0 of the 32-layer sweep per step (Q8 quantize of its 4 inputs + 7 Q4_K "
                    f"projections, {nbytes / 1e6:.1f} MB of weights) at M={M}")
     line = {
-        "impl": "reference", "metric": "Q4_K/Q6_K x Q8 matmul weight GB/s (M=%d)" % M,
+        "impl": "reference", "metric": METRIC % M,
         "value": round(value, 6), "unit": "GB/s", "n_gpus": args.gpus, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(1e3 * tot / args.steps, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
@@ -552,7 +554,7 @@ def gpu_arm(args):
 
     if rank == 0:
         line = {
-            "metric": "Q4_K/Q6_K x Q8 matmul weight GB/s (M=%d) and %% of GB300 HBM roofline" % M,
+            "metric": METRIC % M,
             "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "int8",
