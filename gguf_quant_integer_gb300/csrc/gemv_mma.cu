@@ -72,7 +72,7 @@ struct Proj {
   float* y;
   int32_t* isum;
   float* partial;      // split: [nch][8][64 * row blocks]
-  unsigned int* arrive;  // split: one arrival count per 64-row block
+  unsigned int* arrive;  // split: one arrival count per 16-row group
   int N, K, M, task0, nch;
 };
 
@@ -100,7 +100,7 @@ struct GLay {
   static constexpr int kFragOff = 4 * kBlockBytes;
   static constexpr int kFscOff = kFragOff + 8 * 512;
   static constexpr int kStageBytes = kFscOff + 8 * 64;
-  static constexpr int kSmemBytes = kStages * kStageBytes + 4 * kDecBytes + kStages * 16 + 2 * kStages * 8 + 16;
+  static constexpr int kSmemBytes = kStages * kStageBytes + 4 * kDecBytes + kStages * 16 + 2 * kStages * 8;
 };
 static_assert(GLay<12>::kStageBytes == 13824, "Q4_K stage layout");
 static_assert(3 * (GLay<8>::kSmemBytes + 1024) <= 228 * 1024, "Q8_0: three CTAs per SM");
@@ -433,6 +433,33 @@ __device__ __forceinline__ void store_y(const Proj& P, int rg, int n8, int t, fl
   }
 }
 
+// The last warp to finish a split 16-row group: y = the group's K-chunk
+// partials added in chunk order (the loads of 4 chunks issued together).
+__device__ __forceinline__ void reduce_chunks(const Proj& P, int rg, int n8, int t) {
+  const int rows_pad = ((P.N + 63) / 64) * 64;
+  const int r0 = rg * 16 + mma_row(n8), r1 = r0 + 8, c0 = 2 * t, c1 = c0 + 1;
+  float v[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+  for (int c0k = 0; c0k < P.nch; c0k += 4) {
+    float pv[4][4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      if (c0k + u < P.nch) {
+        const float* pc = P.partial + static_cast<size_t>(c0k + u) * 8 * rows_pad;
+        pv[u][0] = __ldcg(pc + static_cast<size_t>(c0) * rows_pad + r0);
+        pv[u][1] = __ldcg(pc + static_cast<size_t>(c1) * rows_pad + r0);
+        pv[u][2] = __ldcg(pc + static_cast<size_t>(c0) * rows_pad + r1);
+        pv[u][3] = __ldcg(pc + static_cast<size_t>(c1) * rows_pad + r1);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      if (c0k + u < P.nch)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) v[e] += pv[u][e];
+  }
+  store_y(P, rg, n8, t, v[0], v[1], v[2], v[3]);
+}
+
 // Tasks after each CTA's first (its own index): from the counter, which
 // starts at zero, offset by the grid size; or strided by the grid size.
 __device__ __forceinline__ int next_task(const Group& G, int cur) {
@@ -452,7 +479,6 @@ __device__ __forceinline__ void gemv_mma_body(const Group& G) {
   float4* dec_all = reinterpret_cast<float4*>(smem + kStages * kStageBytes);
   int4* meta = reinterpret_cast<int4*>(smem + kStages * kStageBytes + 4 * kDecBytes);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes + 4 * kDecBytes + kStages * 16);
-  int* last_flag = reinterpret_cast<int*>(smem + kStages * kStageBytes + 4 * kDecBytes + kStages * 16 + 2 * kStages * 8);
   const uint32_t ring_s = static_cast<uint32_t>(__cvta_generic_to_shared(ring));
   const uint32_t full_s = static_cast<uint32_t>(__cvta_generic_to_shared(bars));
   const uint32_t empty_s = full_s + kStages * 8;
@@ -552,10 +578,33 @@ __device__ __forceinline__ void gemv_mma_body(const Group& G) {
   unsigned fills = 0;
   int cur_task = -1;
   TaskPos tp = {0, 0, 0, 0, 0};
+  // Split tasks: each warp owns one arrival count per 16-row group. Lane 0
+  // increments it once the warp's partials are stored; the warp examines the
+  // count it got one stage later, so the atomic's round trip overlaps that
+  // stage's compute, and no barrier couples the four warps. pend_p >= 0
+  // marks a pending hand-off (projection and row group; pend_old is lane 0's
+  // count before the increment).
+  int pend_p = -1, pend_rg = 0;
+  unsigned pend_old = 0;
+  auto resolve = [&]() {
+    if (pend_p < 0) return;
+    const Proj& Q = G.p[pend_p];
+    const unsigned old = __shfl_sync(0xffffffffu, pend_old, 0);
+    if (old == static_cast<unsigned>(Q.nch - 1)) {  // every chunk has arrived
+      __threadfence();
+      __syncwarp();
+      if (lane == 0) Q.arrive[pend_rg] = 0u;  // ready for the next launch
+      reduce_chunks(Q, pend_rg, n8, t);
+    }
+    pend_p = -1;
+  };
   for (;;) {
     if (!mbar_wait(full_s + 8 * slot, fills & 1, 2)) return;
     const int4 m = meta[slot];
-    if (m.x < 0) return;
+    if (m.x < 0) {
+      resolve();
+      return;
+    }
     if (m.x != cur_task) {  // task geometry, once per task
       cur_task = m.x;
       tp = task_pos(G, m.x);
@@ -582,12 +631,15 @@ __device__ __forceinline__ void gemv_mma_body(const Group& G) {
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(empty_s + 8 * slot);
+    resolve();  // a split hand-off from an earlier task, one stage later
     if (m.z) {
       if (P.nch == 1) {
         if (rows_ok) store_y(P, rg, n8, t, lo32(acc[0]), hi32(acc[0]), lo32(acc[1]), hi32(acc[1]));
-      } else {
-        // K-chunk partial of a split task; the last CTA of the row block adds
-        // the chunks in chunk order.
+      } else if (rows_ok) {
+        // K-chunk partial of a split task; the last warp to finish the row
+        // group adds the chunks in chunk order. Lane 0's fence, after the
+        // warp barrier, publishes the warp's stores ahead of its relaxed
+        // increment; the last warp fences again before its reads.
         const int rows_pad = ((P.N + 63) / 64) * 64;
         float* part = P.partial + static_cast<size_t>(tp.c) * 8 * rows_pad;
         const int r0 = rg * 16 + mma_row(n8), r1 = r0 + 8, c0 = 2 * t, c1 = c0 + 1;
@@ -595,53 +647,13 @@ __device__ __forceinline__ void gemv_mma_body(const Group& G) {
         part[static_cast<size_t>(c1) * rows_pad + r0] = hi32(acc[0]);
         part[static_cast<size_t>(c0) * rows_pad + r1] = lo32(acc[1]);
         part[static_cast<size_t>(c1) * rows_pad + r1] = hi32(acc[1]);
-        __threadfence();
-        asm volatile("bar.sync 1, 128;" ::: "memory");
-        if (threadIdx.x == 0) {
-          const unsigned old = atomicAdd(P.arrive + tp.rb, 1u);
-          const int last = old == static_cast<unsigned>(P.nch - 1);
-          if (last) {
-            __threadfence();
-            P.arrive[tp.rb] = 0u;  // ready for the next launch
-          }
-          *last_flag = last;
+        __syncwarp();
+        if (lane == 0) {
+          __threadfence();
+          pend_old = atomicAdd(P.arrive + rg, 1u);
         }
-        asm volatile("bar.sync 1, 128;" ::: "memory");
-        if (*last_flag && rows_ok) {
-          // chunks added in chunk order (Q6_K, split into more chunks, issues
-          // the loads of 4 chunks at a time)
-          float v[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-          if constexpr (TYPE != 14) {
-            for (int c = 0; c < P.nch; ++c) {
-              const float* pc = P.partial + static_cast<size_t>(c) * 8 * rows_pad;
-              v[0] += __ldcg(pc + static_cast<size_t>(c0) * rows_pad + r0);
-              v[1] += __ldcg(pc + static_cast<size_t>(c1) * rows_pad + r0);
-              v[2] += __ldcg(pc + static_cast<size_t>(c0) * rows_pad + r1);
-              v[3] += __ldcg(pc + static_cast<size_t>(c1) * rows_pad + r1);
-            }
-          } else {
-            for (int c0k = 0; c0k < P.nch; c0k += 4) {
-              float pv[4][4];
-#pragma unroll
-              for (int u = 0; u < 4; ++u) {
-                if (c0k + u < P.nch) {
-                  const float* pc = P.partial + static_cast<size_t>(c0k + u) * 8 * rows_pad;
-                  pv[u][0] = __ldcg(pc + static_cast<size_t>(c0) * rows_pad + r0);
-                  pv[u][1] = __ldcg(pc + static_cast<size_t>(c1) * rows_pad + r0);
-                  pv[u][2] = __ldcg(pc + static_cast<size_t>(c0) * rows_pad + r1);
-                  pv[u][3] = __ldcg(pc + static_cast<size_t>(c1) * rows_pad + r1);
-                }
-              }
-#pragma unroll
-              for (int u = 0; u < 4; ++u)
-                if (c0k + u < P.nch)
-#pragma unroll
-                  for (int e = 0; e < 4; ++e) v[e] += pv[u][e];
-            }
-          }
-          store_y(P, rg, n8, t, v[0], v[1], v[2], v[3]);
-        }
-        asm volatile("bar.sync 1, 128;" ::: "memory");
+        pend_p = tp.p;
+        pend_rg = rg;
       }
       acc[0] = 0ull;
       acc[1] = 0ull;

@@ -188,12 +188,12 @@ __host__ __device__ inline int gemv_split_chunks(int K, int M_total, int chunk =
 // Resident CTAs of the grouped GEMV (3 per SM for both weight types).
 constexpr int kGemvSlots = 3 * kNumSMs;
 // Workspace of a split projection: partial sums [nch][8][64 * row blocks]
-// and one arrival count per 64-row block (both rounded to 256 bytes).
+// and one arrival count per 16-row group (both rounded to 256 bytes).
 __host__ __device__ inline size_t gemv_split_partial_bytes(int N, int nch) {
   return ((static_cast<size_t>(nch) * 8 * (((N + 63) / 64) * 64) * 4) + 255) & ~static_cast<size_t>(255);
 }
 __host__ __device__ inline size_t gemv_split_arrive_bytes(int N) {
-  return ((static_cast<size_t>((N + 63) / 64) * 4) + 255) & ~static_cast<size_t>(255);
+  return ((static_cast<size_t>((N + 63) / 64) * 4 * 4) + 255) & ~static_cast<size_t>(255);
 }
 
 // Whether the tensor-core GEMV takes this weight: every Q4_K shape; Q6_K
