@@ -526,14 +526,57 @@ def gpu_arm(args):
         h2d = h_in.numel() * 4
         d2h = h_out.numel() * 4
 
+        # Copies overlap the layers: a copy stream brings the inputs over in
+        # chunks of 1, 2, 4, 8, ... layers (each chunk lands long before its
+        # first layer starts) and takes the outputs back in chunks that
+        # shrink towards the last layer, so only the first chunk in and the
+        # last layer's outputs are exposed.
+        L = len(sweep.W)
+        in_off = [0]
+        for lt in ins0:
+            in_off.append(in_off[-1] + sum(t.numel() for t in lt))
+        out_off = [0]
+        for lt in ys0:
+            out_off.append(out_off[-1] + sum(t.numel() for t in lt))
+        in_chunks, a, n = [], 0, 1
+        while a < L:
+            in_chunks.append((a, min(L, a + n)))
+            a, n = min(L, a + n), 2 * n
+        out_chunks, b, n = [], L, 1
+        while b > 0:
+            out_chunks.append((max(0, b - n), b))
+            b, n = max(0, b - n), 2 * n
+        out_chunks.reverse()
+        copy_s = torch.cuda.Stream(device)
+
         def e2e_step():
-            d_in.copy_(h_in, non_blocking=True)
-            for l in range(len(sweep.W)):
+            cur = torch.cuda.current_stream()
+            copy_s.wait_stream(cur)  # the previous step is done with d_in and d_out
+            ev_in = []
+            with torch.cuda.stream(copy_s):
+                for a, b in in_chunks:
+                    d_in[in_off[a]:in_off[b]].copy_(h_in[in_off[a]:in_off[b]], non_blocking=True)
+                    ev_in.append(copy_s.record_event())
+            ci = 0
+            ev_out = []
+            for l in range(L):
+                if ci < len(in_chunks) and l == in_chunks[ci][0]:
+                    cur.wait_event(ev_in[ci])
+                    ci += 1
                 xq.layer_mixed(descs[l], ins[l], M, ws)
-            h_out.copy_(d_out, non_blocking=True)
+                if any(l == b - 1 for _, b in out_chunks):
+                    ev_out.append(cur.record_event())
+            with torch.cuda.stream(copy_s):
+                for (a, b), ev in zip(out_chunks, ev_out):
+                    copy_s.wait_event(ev)
+                    h_out[out_off[a]:out_off[b]].copy_(d_out[out_off[a]:out_off[b]], non_blocking=True)
+            cur.wait_stream(copy_s)
 
         s = time_region(e2e_step, args.steps, max(3, args.warmup), world, device)
         s = max_over_ranks(s, world, device) / args.steps
+        torch.cuda.synchronize()
+        if not torch.equal(h_out, d_out.cpu()):  # every output chunk came back after its layers
+            raise RuntimeError("e2e: host outputs differ from the device outputs")
         e2e = {"value": round(aggregate_value(nbytes, world, s), 1), "unit": "GB/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(1e3 * s, 4)}
 
