@@ -117,7 +117,8 @@ bool in_group(const xq_proj& q, int M) { return q.N > 0 && M <= kMaxGemvM && xq:
 
 // K-chunking of a grouped launch: chunks of ~16 super-blocks for long rows;
 // while the group has fewer 64-row tasks than resident CTAs, halve the chunk
-// length (down to 4) so that every CTA gets work.
+// length once, to 8 (4-super-block chunks cost more in hand-offs and pipeline
+// refills than the idle CTAs they put to work).
 void choose_chunks(const xq_proj* proj, int n_proj, int M, int type, int* nch) {
   for (int chunk = 16;; chunk /= 2) {
     long long tasks = 0;
@@ -126,7 +127,7 @@ void choose_chunks(const xq_proj* proj, int n_proj, int M, int type, int* nch) {
       nch[p] = xq::gemv_split_chunks(proj[p].K, M, chunk);
       tasks += static_cast<long long>((proj[p].N + 63) / 64) * nch[p];
     }
-    if (tasks >= xq::kGemvSlots || chunk <= 4) return;
+    if (tasks >= xq::kGemvSlots || chunk <= 8) return;
   }
 }
 
