@@ -125,7 +125,7 @@ void choose_chunks(const xq_proj* proj, int n_proj, int M, int type, int* nch) {
     for (int p = 0; p < n_proj; ++p) {
       if (!in_group(proj[p], M) || proj[p].type != type) continue;
       nch[p] = xq::gemv_split_chunks(proj[p].K, M, chunk);
-      tasks += static_cast<long long>((proj[p].N + 63) / 64) * nch[p];
+      tasks += static_cast<long long>(xq::gemv_row_blocks(proj[p].N)) * nch[p];
     }
     if (tasks >= xq::kGemvSlots || chunk <= 8) return;
   }

@@ -95,15 +95,17 @@ constexpr int kDecBytes = 8 * 16 * 16;  // per warp: one float4 per (32-block, r
 template <int TYPE>
 struct GLay {
   static constexpr int kBoxRow = TYPE == 12 ? kQ4kBytes : (TYPE == 8 ? kQ80Group : 240);
-  static constexpr int kStages = TYPE == 12 ? 4 : 3;
+  static constexpr int kStages = kGemvWarps == 4 ? (TYPE == 12 ? 4 : 3) : (TYPE == 12 ? 4 : 2);
   static constexpr int kBlockBytes = 16 * kBoxRow;  // 16 rows x one super-block
-  static constexpr int kFragOff = 4 * kBlockBytes;
+  static constexpr int kFragOff = kGemvWarps * kBlockBytes;
   static constexpr int kFscOff = kFragOff + 8 * 512;
   static constexpr int kStageBytes = kFscOff + 8 * 64;
-  static constexpr int kSmemBytes = kStages * kStageBytes + 4 * kDecBytes + kStages * 16 + 2 * kStages * 8;
+  static constexpr int kSmemBytes = kStages * kStageBytes + kGemvWarps * kDecBytes + kStages * 16 + 2 * kStages * 8;
 };
-static_assert(GLay<12>::kStageBytes == 13824, "Q4_K stage layout");
-static_assert(3 * (GLay<8>::kSmemBytes + 1024) <= 228 * 1024, "Q8_0: three CTAs per SM");
+static_assert(kGemvWarps != 4 || GLay<12>::kStageBytes == 13824, "Q4_K stage layout");
+static_assert(kGemvCtasPerSM * (GLay<12>::kSmemBytes + 1024) <= 228 * 1024, "Q4_K: resident CTAs per SM");
+static_assert(kGemvCtasPerSM * (GLay<14>::kSmemBytes + 1024) <= 228 * 1024, "Q6_K: resident CTAs per SM");
+static_assert(kGemvCtasPerSM * (GLay<8>::kSmemBytes + 1024) <= 228 * 1024, "Q8_0: resident CTAs per SM");
 constexpr long long kWaitClocks = 1LL << 32;
 
 __device__ __forceinline__ int mma_row(int i) { return 8 * (i >> 3) + 2 * (i & 3) + ((i >> 2) & 1); }
@@ -436,7 +438,7 @@ __device__ __forceinline__ void store_y(const Proj& P, int rg, int n8, int t, fl
 // The last warp to finish a split 16-row group: y = the group's K-chunk
 // partials added in chunk order (the loads of 4 chunks issued together).
 __device__ __forceinline__ void reduce_chunks(const Proj& P, int rg, int n8, int t) {
-  const int rows_pad = ((P.N + 63) / 64) * 64;
+  const int rows_pad = gemv_row_blocks(P.N) * kGemvRows;
   const int r0 = rg * 16 + mma_row(n8), r1 = r0 + 8, c0 = 2 * t, c1 = c0 + 1;
   float v[4] = {0.0f, 0.0f, 0.0f, 0.0f};
   for (int c0k = 0; c0k < P.nch; c0k += 4) {
@@ -477,8 +479,8 @@ __device__ __forceinline__ void gemv_mma_body(const Group& G) {
   extern __shared__ __align__(128) uint8_t smem[];
   uint8_t* ring = smem;
   float4* dec_all = reinterpret_cast<float4*>(smem + kStages * kStageBytes);
-  int4* meta = reinterpret_cast<int4*>(smem + kStages * kStageBytes + 4 * kDecBytes);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes + 4 * kDecBytes + kStages * 16);
+  int4* meta = reinterpret_cast<int4*>(smem + kStages * kStageBytes + kGemvWarps * kDecBytes);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes + kGemvWarps * kDecBytes + kStages * 16);
   const uint32_t ring_s = static_cast<uint32_t>(__cvta_generic_to_shared(ring));
   const uint32_t full_s = static_cast<uint32_t>(__cvta_generic_to_shared(bars));
   const uint32_t empty_s = full_s + kStages * 8;
@@ -487,12 +489,12 @@ __device__ __forceinline__ void gemv_mma_body(const Group& G) {
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(full_s + 8 * s, 1);
-      mbar_init(empty_s + 8 * s, 4);
+      mbar_init(empty_s + 8 * s, kGemvWarps);
     }
     mbar_init_fence();
   }
   __syncthreads();
-  if (warp == 4) {
+  if (warp == kGemvWarps) {
     // ------------------------------------------------------- producer
     if (lane != 0) return;
     // Each CTA's first task is its own index; later tasks come from the
@@ -507,8 +509,8 @@ __device__ __forceinline__ void gemv_mma_body(const Group& G) {
     if (task < G.total) {
       const TaskPos tp = task_pos(G, task);
       const Proj& P = G.p[tp.p];
-      const int rows = P.N - tp.rb * 64;
-      const int nblk = rows >= 64 ? 4 : (rows + 15) / 16;
+      const int rows = P.N - tp.rb * kGemvRows;
+      const int nblk = rows >= kGemvRows ? kGemvWarps : (rows + 15) / 16;
       int b = tp.b0;
       for (; b < tp.b1 && slot < kStages; ++b, ++slot) {
         meta[slot] = make_int4(task, b, (b == tp.b1 - 1) ? 1 : 0, 0);
@@ -516,7 +518,7 @@ __device__ __forceinline__ void gemv_mma_body(const Group& G) {
         const uint32_t st = ring_s + slot * kStageBytes;
         for (int w = 0; w < nblk; ++w)
           tma_load_2d(st + w * kBlockBytes, &P.map, weight_box_x<TYPE>(b),
-                      tp.rb * 64 + 16 * w, full_s + 8 * slot);
+                      tp.rb * kGemvRows + 16 * w, full_s + 8 * slot);
       }
       bresume = b;
     }
@@ -550,13 +552,13 @@ __device__ __forceinline__ void gemv_mma_body(const Group& G) {
           return;
         }
         const Proj& P = G.p[tp.p];
-        const int rows = P.N - tp.rb * 64;  // > 0
-        const int nblk = rows >= 64 ? 4 : (rows + 15) / 16;
+        const int rows = P.N - tp.rb * kGemvRows;  // > 0
+        const int nblk = rows >= kGemvRows ? kGemvWarps : (rows + 15) / 16;
         mbar_expect_tx(full_s + 8 * slot, static_cast<unsigned>(nblk * kBlockBytes + 8 * 512 + 8 * 64));
         const uint32_t st = ring_s + slot * kStageBytes;
         for (int w = 0; w < nblk; ++w)
           tma_load_2d(st + w * kBlockBytes, &P.map, weight_box_x<TYPE>(b),
-                      tp.rb * 64 + 16 * w, full_s + 8 * slot);
+                      tp.rb * kGemvRows + 16 * w, full_s + 8 * slot);
         bulk_load(st + kFragOff, P.frag + static_cast<size_t>(b) * 8 * 512, 8 * 512, full_s + 8 * slot);
         bulk_load(st + kFscOff, P.fsc + static_cast<size_t>(b) * 8 * 64, 8 * 64, full_s + 8 * slot);
         if (++slot == kStages) {
@@ -610,7 +612,7 @@ __device__ __forceinline__ void gemv_mma_body(const Group& G) {
       tp = task_pos(G, m.x);
     }
     const Proj& P = G.p[tp.p];
-    const int rg = tp.rb * 4 + warp;  // this warp's 16-row group
+    const int rg = tp.rb * kGemvWarps + warp;  // this warp's 16-row group
     const uint8_t* st = ring + slot * kStageBytes;
     const bool rows_ok = rg * 16 < P.N;
     if (rows_ok) {
@@ -640,7 +642,7 @@ __device__ __forceinline__ void gemv_mma_body(const Group& G) {
         // group adds the chunks in chunk order. Lane 0's fence, after the
         // warp barrier, publishes the warp's stores ahead of its relaxed
         // increment; the last warp fences again before its reads.
-        const int rows_pad = ((P.N + 63) / 64) * 64;
+        const int rows_pad = gemv_row_blocks(P.N) * kGemvRows;
         float* part = P.partial + static_cast<size_t>(tp.c) * 8 * rows_pad;
         const int r0 = rg * 16 + mma_row(n8), r1 = r0 + 8, c0 = 2 * t, c1 = c0 + 1;
         part[static_cast<size_t>(c0) * rows_pad + r0] = lo32(acc[0]);
@@ -666,7 +668,7 @@ __device__ __forceinline__ void gemv_mma_body(const Group& G) {
 }
 
 template <int TYPE, bool ISUM>
-__global__ void __launch_bounds__(160, 3)
+__global__ void __launch_bounds__(32 * (kGemvWarps + 1), kGemvCtasPerSM)
 gemv_mma_kernel(const __grid_constant__ Group G) {
   gemv_mma_body<TYPE, ISUM>(G);
   // A launch that did not wait for the previous grid on entry waits before
@@ -683,7 +685,7 @@ int max_ctas() {
     int n = 0;
     constexpr int kSmemBytes = GLay<TYPE>::kSmemBytes;
     cudaFuncSetAttribute(gemv_mma_kernel<TYPE, ISUM>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, gemv_mma_kernel<TYPE, ISUM>, 160, kSmemBytes) != cudaSuccess ||
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, gemv_mma_kernel<TYPE, ISUM>, 32 * (kGemvWarps + 1), kSmemBytes) != cudaSuccess ||
         n < 1)
       n = 1;
     per_sm = n;
@@ -797,7 +799,7 @@ cudaError_t launch_gemv_mma(int type, const MmaProj* projs, int n, cudaStream_t 
     P.nch = nch[src];
     P.partial = nullptr;
     P.arrive = nullptr;
-    const int rbs = (q.N + 63) / 64;
+    const int rbs = gemv_row_blocks(q.N);
     if (P.nch > 1) {
       P.partial = reinterpret_cast<float*>(partial_ws + partial_off[src]);
       P.arrive = reinterpret_cast<unsigned int*>(arrive_ws + arrive_off[src]);
@@ -813,7 +815,7 @@ cudaError_t launch_gemv_mma(int type, const MmaProj* projs, int n, cudaStream_t 
                               : (isum ? max_ctas<14, true>() : max_ctas<14, false>());
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(total < cap ? total : cap));
-  cfg.blockDim = dim3(160);
+  cfg.blockDim = dim3(32 * (kGemvWarps + 1));
   cfg.dynamicSmemBytes =
       type == 12 ? GLay<12>::kSmemBytes : (type == 8 ? GLay<8>::kSmemBytes : GLay<14>::kSmemBytes);
   cfg.stream = s;

@@ -185,15 +185,20 @@ __host__ __device__ inline int gemv_split_chunks(int K, int M_total, int chunk =
   const int limit = chunk >= 16 ? 24 : chunk;
   return nsb > limit ? (nsb + chunk - 1) / chunk : 1;
 }
-// Resident CTAs of the grouped GEMV (3 per SM for both weight types).
-constexpr int kGemvSlots = 3 * kNumSMs;
-// Workspace of a split projection: partial sums [nch][8][64 * row blocks]
-// and one arrival count per 16-row group (both rounded to 256 bytes).
+// Grouped GEMV geometry: consumer warps per CTA (16 weight rows each, so a
+// task covers kGemvRows rows), and resident CTAs per SM.
+constexpr int kGemvWarps = 4;
+constexpr int kGemvRows = 16 * kGemvWarps;
+constexpr int kGemvCtasPerSM = 3;
+constexpr int kGemvSlots = kGemvCtasPerSM * kNumSMs;
+// Workspace of a split projection: partial sums [nch][8][rows padded to
+// kGemvRows] and one arrival count per 16-row group (both rounded to 256 bytes).
+__host__ __device__ inline int gemv_row_blocks(int N) { return (N + kGemvRows - 1) / kGemvRows; }
 __host__ __device__ inline size_t gemv_split_partial_bytes(int N, int nch) {
-  return ((static_cast<size_t>(nch) * 8 * (((N + 63) / 64) * 64) * 4) + 255) & ~static_cast<size_t>(255);
+  return ((static_cast<size_t>(nch) * 8 * gemv_row_blocks(N) * kGemvRows * 4) + 255) & ~static_cast<size_t>(255);
 }
 __host__ __device__ inline size_t gemv_split_arrive_bytes(int N) {
-  return ((static_cast<size_t>((N + 63) / 64) * 4 * 4) + 255) & ~static_cast<size_t>(255);
+  return ((static_cast<size_t>(gemv_row_blocks(N)) * kGemvWarps * 4) + 255) & ~static_cast<size_t>(255);
 }
 
 // Whether the tensor-core GEMV takes this weight: every Q4_K shape; Q6_K
