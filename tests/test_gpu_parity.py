@@ -304,6 +304,27 @@ def test_qwen3_mixed_layer(xq, M):
     assert layer_check(xq, synth.WORKLOADS["qwen3-8b-mixed-layer"], M, rows=rows) > 0
 
 
+# Ragged projections whose rows are long enough to be split over K: output
+# counts that leave partial 16-row groups and empty warps in the last task,
+# a Q6_K and a Q8_0 projection next to Q4_K, and few enough tasks that the
+# chunk length drops to 8 super-blocks.
+RAGGED_SPLIT = synth.Workload(
+    key="ragged-split", title="ragged split-K layer",
+    projs=(synth.Proj("a", synth.Q4_K, 8192, 100, 0), synth.Proj("b", synth.Q6_K, 8192, 40, 0),
+           synth.Proj("c", synth.Q4_K, 6400, 1000, 1), synth.Proj("d", synth.Q4_K, 6400, 17, 1)),
+    seed_base=900, x_seed_base=19000, input_dims=(8192, 6400))
+RAGGED_SPLIT_Q80 = synth.Workload(
+    key="ragged-split-q8_0", title="ragged split-K Q8_0 layer",
+    projs=(synth.Proj("a", synth.Q8_0, 7168, 77, 0), synth.Proj("b", synth.Q8_0, 7168, 300, 0)),
+    seed_base=950, x_seed_base=19500, input_dims=(7168,))
+
+
+@pytest.mark.parametrize("M", [1, 5, 8])
+def test_ragged_split_layer(xq, M):
+    assert layer_check(xq, RAGGED_SPLIT, M) > 0
+    assert layer_check(xq, RAGGED_SPLIT_Q80, M) > 0
+
+
 Q80_SHAPES = [(1, 256), (5, 512), (37, 1536), (130, 4096), (3, 12288)]
 
 
