@@ -206,9 +206,10 @@ __device__ __forceinline__ void load_words(const uint8_t* p, uint32_t (&out)[NW]
 // Q6_K (public layout: ql[128] @0, qh[64] @128, int8 scales[16] @192, d @208;
 // the super-block starts `off` bytes into the row's window). Lane l takes
 // weight row l%16 and 32-blocks 4*(l/16) .. +3, writing for each 32-block p
-// (alpha_2p, alpha_2p, alpha_2p+1, alpha_2p+1), alpha_g = d * s_g (one
-// rounding of an exact product): the coefficients of the two 16-weight
-// groups of p. Each half-warp's stores cover 256 consecutive bytes.
+// (alpha_2p, alpha_2p, delta_p, delta_p) with alpha_2p = d * s_2p and
+// delta_p = d * (s_2p+1 - s_2p): exact products (11 x 9 significant bits),
+// so each is exact in fp32. Each half-warp's stores cover 256 consecutive
+// bytes.
 __device__ __forceinline__ void decode_scales_q6(const uint8_t* blk, int off, float4* dec, int lane) {
   const int r = lane & 15, half = lane >> 4;
   const uint8_t* sb = blk + r * GLay<14>::kBoxRow + off;
@@ -219,9 +220,11 @@ __device__ __forceinline__ void decode_scales_q6(const uint8_t* blk, int off, fl
   for (int k = 0; k < 4; ++k) {
     const uint32_t w = sw[k >> 1];
     const int b0 = 2 * (k & 1);
-    const float a0 = d * static_cast<float>(static_cast<int8_t>((w >> (8 * b0)) & 0xFFu));
-    const float a1 = d * static_cast<float>(static_cast<int8_t>((w >> (8 * b0 + 8)) & 0xFFu));
-    dec[(4 * half + k) * 16 + r] = make_float4(a0, a0, a1, a1);
+    const int s0 = static_cast<int8_t>((w >> (8 * b0)) & 0xFFu);
+    const int s1 = static_cast<int8_t>((w >> (8 * b0 + 8)) & 0xFFu);
+    const float a0 = d * static_cast<float>(s0);
+    const float dl = d * static_cast<float>(s1 - s0);
+    dec[(4 * half + k) * 16 + r] = make_float4(a0, a0, dl, dl);
   }
 }
 
@@ -288,9 +291,11 @@ __device__ __forceinline__ void compute_block_q4(const uint8_t* blk, const uint8
 // (the activation image's slot order, as for Q4_K). Each quant is
 // q = (ql nibble) | (qh 2 bits) << 4; the operand is q - 32 in fp16
 // (1024 + q from a byte permute, then an exact subtraction). Four MMAs per
-// 32-block: each group's accumulator gets the two k-halves with the other
-// group's lanes zeroed, so D_g = sum_{16} (q-32)*q8 = isum_g exactly
-// (|isum_g| <= 32*127*16). Combine: acc += (alpha_g * d8) * D_g per group.
+// 32-block: two give Da = isum_2p + isum_2p+1, and two more, with the
+// activation operands of group 2p's lanes zeroed, give D1 = isum_2p+1 (all
+// exact: |isum_g| <= 32*127*16). Since
+//   alpha_2p isum_2p + alpha_2p+1 isum_2p+1 = alpha_2p Da + delta_p D1,
+// the combine is acc += (alpha_2p d8) Da + (delta_p d8) D1.
 template <bool ISUM>
 __device__ __forceinline__ void compute_block_q6(const uint8_t* blk, int off, const uint8_t* act, const float4* dec,
                                                  const Proj& P, int rg, int b, int n8, int t, int lane,
@@ -331,16 +336,16 @@ __device__ __forceinline__ void compute_block_q6(const uint8_t* blk, int off, co
         a[w][3] = hsub2(prmt(q1, 0x64646464u, 0x4341u), 0x64206420u);
       }
       const uint4 B = fp[p * 32];
-      float D0[4] = {0.0f, 0.0f, 0.0f, 0.0f}, D1[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-      const uint32_t g0 = first ? 0xFFFFFFFFu : 0u, g1 = ~g0;
-      mma16816(D0, a[0][0] & g0, a[0][1] & g0, a[0][2] & g0, a[0][3] & g0, B.x, B.y);
-      mma16816(D0, a[1][0] & g0, a[1][1] & g0, a[1][2] & g0, a[1][3] & g0, B.z, B.w);
-      mma16816(D1, a[0][0] & g1, a[0][1] & g1, a[0][2] & g1, a[0][3] & g1, B.x, B.y);
-      mma16816(D1, a[1][0] & g1, a[1][1] & g1, a[1][2] & g1, a[1][3] & g1, B.z, B.w);
+      float Da[4] = {0.0f, 0.0f, 0.0f, 0.0f}, D1[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+      const uint32_t g1 = first ? 0u : 0xFFFFFFFFu;  // keeps group 2p+1's activations
+      mma16816(Da, a[0][0], a[0][1], a[0][2], a[0][3], B.x, B.y);
+      mma16816(Da, a[1][0], a[1][1], a[1][2], a[1][3], B.z, B.w);
+      mma16816(D1, a[0][0], a[0][1], a[0][2], a[0][3], B.x & g1, B.y & g1);
+      mma16816(D1, a[1][0], a[1][1], a[1][2], a[1][3], B.z & g1, B.w & g1);
       const ulonglong2 f = sp[p * 4];  // (d8 c0, d8 c1), (s8 c0, s8 c1)
       const ulonglong2 e0 = dp[p * 16 + r0], e1 = dp[p * 16 + r1];
-      acc[0] = fma2(mul2(e0.x, f.x), pk(D0[0], D0[1]), fma2(mul2(e0.y, f.x), pk(D1[0], D1[1]), acc[0]));
-      acc[1] = fma2(mul2(e1.x, f.x), pk(D0[2], D0[3]), fma2(mul2(e1.y, f.x), pk(D1[2], D1[3]), acc[1]));
+      acc[0] = fma2(mul2(e0.x, f.x), pk(Da[0], Da[1]), fma2(mul2(e0.y, f.x), pk(D1[0], D1[1]), acc[0]));
+      acc[1] = fma2(mul2(e1.x, f.x), pk(Da[2], Da[3]), fma2(mul2(e1.y, f.x), pk(D1[2], D1[3]), acc[1]));
       if (ISUM) {
         const int ngrp = P.K >> 4;
 #pragma unroll
@@ -351,7 +356,7 @@ __device__ __forceinline__ void compute_block_q6(const uint8_t* blk, int off, co
             const int col = 2 * t + (e & 1);
             if (row < P.N && col < P.M)
               P.isum[(static_cast<size_t>(col) * P.N + row) * ngrp + 16 * b + 2 * p + g] =
-                  static_cast<int32_t>(g ? D1[e] : D0[e]);
+                  static_cast<int32_t>(g ? D1[e] : Da[e] - D1[e]);
           }
       }
     }
