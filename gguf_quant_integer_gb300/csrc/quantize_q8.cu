@@ -51,17 +51,35 @@ struct QuantGroup {
 
 __global__ void __launch_bounds__(1024)
 quantize_q8_kernel(const __grid_constant__ QuantGroup G) {
-  // Inputs may be written by the previous kernel on the stream. The next
-  // kernel may launch at once: it waits for this grid's completion before
-  // reading what it writes.
-  cudaGridDependencySynchronize();
-  cudaTriggerProgrammaticLaunchCompletion();
-  if (blockIdx.x == 0)
-    for (int i = threadIdx.x; i < G.zero_count; i += blockDim.x) G.zero_words[i] = 0u;
   const int lane = threadIdx.x & 31;
   const unsigned warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const unsigned nwarps = (gridDim.x * blockDim.x) >> 5;
   const unsigned total = G.blk0[G.n];
+  // Inputs may be written by the previous kernel on the stream, so they are
+  // read only after the dependency wait. Before it, the lines they occupy
+  // are requested into L2 (L2 is coherent for the device, so a line the
+  // previous kernel writes afterwards is read with its new contents).
+  {
+    int jb = 0;
+    for (unsigned blk = warp; blk < total; blk += nwarps) {
+      while (blk >= G.blk0[jb + 1]) ++jb;
+      const QuantItem& J = G.job[jb];
+      const unsigned local = blk - G.blk0[jb];
+      const int m = static_cast<int>(local / static_cast<unsigned>(J.nsub));
+      const int j = static_cast<int>(local - static_cast<unsigned>(m) * J.nsub);
+      if (m < J.M && (lane == 0 || lane == 31)) {
+        const size_t idx = static_cast<size_t>(m) * J.K + 32 * j + lane;
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(J.x + idx));
+        if (J.up) asm volatile("prefetch.global.L2 [%0];" ::"l"(J.up + idx));
+      }
+    }
+  }
+  // The next kernel may launch at once: it waits for this grid's completion
+  // before reading what it writes.
+  cudaGridDependencySynchronize();
+  cudaTriggerProgrammaticLaunchCompletion();
+  if (blockIdx.x == 0)
+    for (int i = threadIdx.x; i < G.zero_count; i += blockDim.x) G.zero_words[i] = 0u;
   // Position of this lane's element inside its lane's 8 operand slots:
   // slot order is perm = 0,2,1,3,4,6,5,7 (an involution), so slot = perm[l & 7].
   const int t = lane >> 3;
