@@ -527,10 +527,12 @@ def gpu_arm(args):
         d2h = h_out.numel() * 4
 
         # Copies overlap the layers: a copy stream brings the inputs over in
-        # chunks of 1, 2, 4, 8, ... layers (each chunk lands long before its
-        # first layer starts) and takes the outputs back in chunks that
-        # shrink towards the last layer, so only the first chunk in and the
-        # last layer's outputs are exposed.
+        # three chunks (layer 0, layers 1-3, the rest; at about 200 GB/s each
+        # lands before its first layer starts) and takes the outputs back in
+        # four (all but the last 8 layers, the next 6, then one and one), so
+        # only layer 0's inputs and the last layer's outputs are exposed. A
+        # wait on a copy ends the early start of the next launch, hence few
+        # chunks.
         L = len(sweep.W)
         in_off = [0]
         for lt in ins0:
@@ -538,15 +540,11 @@ def gpu_arm(args):
         out_off = [0]
         for lt in ys0:
             out_off.append(out_off[-1] + sum(t.numel() for t in lt))
-        in_chunks, a, n = [], 0, 1
-        while a < L:
-            in_chunks.append((a, min(L, a + n)))
-            a, n = min(L, a + n), 2 * n
-        out_chunks, b, n = [], L, 1
-        while b > 0:
-            out_chunks.append((max(0, b - n), b))
-            b, n = max(0, b - n), 2 * n
-        out_chunks.reverse()
+        def spans(cuts):
+            cuts = sorted({min(max(c, 0), L) for c in cuts} | {0, L})
+            return [(a, b) for a, b in zip(cuts, cuts[1:]) if b > a]
+        in_chunks = spans([1, 4])
+        out_chunks = spans([L - 8, L - 2, L - 1])
         copy_s = torch.cuda.Stream(device)
 
         def e2e_step():
