@@ -394,17 +394,27 @@ def per_layer_times(sweep, M, reps=3):
 
 
 # Sources the grouped GEMV kernel is built from: a recorded ncu traffic
-# figure stays valid only while these files are unchanged.
+# figure stays valid only while their code is unchanged (comments and
+# whitespace are not part of the hash).
 GEMV_SOURCES = ("gemv_mma.cu", "xq_common.cuh", "xq_ptx.cuh")
 
 
-def kernel_source_hash(names=GEMV_SOURCES) -> str:
+def code_only(text: str) -> str:
+    """C/C++ source with comments removed and whitespace runs collapsed
+    (string literals are kept as they are)."""
+    import re
+    tok = re.compile(r'"(?:\\.|[^"\\])*"|/\*.*?\*/|//[^\n]*', re.S)
+    out = tok.sub(lambda m: m.group(0) if m.group(0).startswith('"') else " ", text)
+    return " ".join(out.split())
+
+
+def kernel_source_hash(names=GEMV_SOURCES, src=None) -> str:
     import hashlib
-    src = os.path.join(ROOT, "gguf_quant_integer_gb300", "csrc")
+    src = src or os.path.join(ROOT, "gguf_quant_integer_gb300", "csrc")
     h = hashlib.sha256()
     for name in names:
-        with open(os.path.join(src, name), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(src, name), encoding="utf-8") as f:
+            h.update(code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

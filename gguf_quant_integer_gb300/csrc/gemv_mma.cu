@@ -45,12 +45,14 @@
 // from a static stride, or, when a work counter is given, from an atomic
 // counter over a list ordered by cost. The weight boxes of the first task's
 // first stages are requested before the kernel waits for the previous grid
-// on the stream (which writes the activation image and zeroes the counter). Long rows
-// (more than 24 super-blocks) can be split into K-chunks of about 16
-// super-blocks handled by different CTAs: each writes its partial sums to a
-// workspace, and the last CTA to finish a 64-row block (an atomic arrival
-// count) adds the chunks in chunk order and writes y, so the result does
-// not depend on which CTA finishes last.
+// on the stream (which writes the activation image and zeroes the counter).
+// Long rows (more than 24 super-blocks) can be split into K-chunks of about
+// 16 super-blocks (8 when a launch has few tasks) handled by different CTAs:
+// each consumer warp writes its 16 rows' partial sums to a workspace and
+// bumps that 16-row group's arrival count, and the last warp to arrive adds
+// the chunks in chunk order and writes y, so the result does not depend on
+// which CTA finishes last. (The geometry constants kGemvWarps, kGemvRows and
+// kGemvCtasPerSM are in xq_common.cuh; the figures above are their values.)
 //
 // Every mbarrier wait is bounded (about 2^32 clocks); on expiry the kernel
 // records an error code and returns.
@@ -71,7 +73,7 @@ struct Proj {
   const uint8_t* fsc;  // [K/32][4][16 B]
   float* y;
   int32_t* isum;
-  float* partial;      // split: [nch][8][64 * row blocks]
+  float* partial;      // split: [nch][8][kGemvRows * row blocks]
   unsigned int* arrive;  // split: one arrival count per 16-row group
   int N, K, M, task0, nch;
 };
