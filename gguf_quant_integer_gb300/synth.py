@@ -34,8 +34,9 @@ import numpy as np
 Q8_0 = 8  # GGUF type ids
 Q4_K = 12
 Q6_K = 14
-BLOCK_BYTES = {Q4_K: 144, Q6_K: 210, Q8_0: 8 * 34}  # bytes per 256 weights
-TYPE_NAME = {Q4_K: "Q4_K", Q6_K: "Q6_K", Q8_0: "Q8_0"}
+IQ4_XS = 23
+BLOCK_BYTES = {Q4_K: 144, Q6_K: 210, Q8_0: 8 * 34, IQ4_XS: 136}  # bytes per 256 weights
+TYPE_NAME = {Q4_K: "Q4_K", Q6_K: "Q6_K", Q8_0: "Q8_0", IQ4_XS: "IQ4_XS"}
 
 
 def weight_bytes(qtype: int, N: int, K: int) -> int:
@@ -78,7 +79,34 @@ def gen_q8_0(seed: int, N: int, K: int) -> np.ndarray:
     return raw.reshape(N, (K // 32) * 34)
 
 
+def gen_iq4xs(seed: int, N: int, K: int) -> np.ndarray:
+    """IQ4_XS weight bytes, shape [N, K/256*136], uint8: d fp16 uniform in
+    [1e-4, 1e-3], every other byte (scale bits, 4-bit indices) uniform."""
+    assert K % 256 == 0 and N >= 0
+    rng = np.random.default_rng(seed)
+    nblk = N * (K // 256)
+    raw = np.frombuffer(rng.bytes(nblk * 136), np.uint8).reshape(nblk, 136).copy()
+    raw[:, 0:2] = _fp16_uniform(rng, nblk).view(np.uint8).reshape(nblk, 2)
+    return raw.reshape(N, (K // 256) * 136)
+
+
+def gen_codebook(seed: int) -> np.ndarray:
+    """A synthetic IQ4_XS codebook: 16 distinct int8 values in increasing
+    order, spread over the whole int8 range and denser near zero (a signed
+    cube of evenly spaced points, jittered). It stands in for the format's
+    table, which the pages name but do not print."""
+    rng = np.random.default_rng(seed)
+    t = np.linspace(-1.0, 1.0, 16) + rng.uniform(-0.02, 0.02, 16)
+    v = np.clip(np.round(127.0 * np.sign(t) * np.abs(t) ** 1.6), -128, 127).astype(np.int64)
+    v[0], v[-1] = -128, 127
+    for i in range(1, 16):  # strictly increasing
+        v[i] = max(v[i], v[i - 1] + 1)
+    return v.astype(np.int8)
+
+
 def gen_weight(qtype: int, seed: int, N: int, K: int) -> np.ndarray:
+    if qtype == IQ4_XS:
+        return gen_iq4xs(seed, N, K)
     if qtype == Q8_0:
         return gen_q8_0(seed, N, K)
     if qtype == Q4_K:

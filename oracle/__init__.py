@@ -1,4 +1,4 @@
-"""CPU oracle for GGUF Q4_K / Q6_K x Q8 integer matmul (ctypes over plain C).
+"""CPU oracle for GGUF Q4_K / Q6_K / Q8_0 / IQ4_XS x Q8 integer matmul (ctypes over plain C).
 
 TEST INFRASTRUCTURE. Only ``tests/``, ``__graft_entry__.smoke()`` and the
 ``cpu_baseline`` / reference leg of ``bench.py`` may import this package. The
@@ -24,6 +24,7 @@ _LIB = os.path.join(_HERE, "_build", "liboracle.so")
 Q4K_BYTES = 144
 Q6K_BYTES = 210
 Q8_0_BYTES = 34
+IQ4XS_BYTES = 136
 
 _lib = None
 
@@ -60,6 +61,10 @@ def _load():
     lib.oracle_q8_0_fields.argtypes = [P, P, P]
     lib.oracle_q8_0_fields.restype = None
     lib.oracle_dequant_q8_0.argtypes = [P, I, I, P]
+    lib.oracle_iq4xs_fields.argtypes = [P, P, P, P, P]
+    lib.oracle_iq4xs_fields.restype = None
+    lib.oracle_dequant_iq4xs.argtypes = [P, P, I, I, P]
+    lib.oracle_matmul_iq4xs_q8.argtypes = [P, P, P, P, I, I, I, P, P, P]
     lib.oracle_matmul_q8_0_q8.argtypes = [P, P, P, I, I, I, P, P, P]
     lib.oracle_dequant_q4k.argtypes = [P, I, I, P]
     lib.oracle_dequant_q6k.argtypes = [P, I, I, P]
@@ -69,7 +74,8 @@ def _load():
     lib.oracle_gemv_f64.argtypes = [P, P, I, I, I, P]
     for name in ("oracle_quantize_q8", "oracle_dequant_q4k", "oracle_dequant_q6k",
                  "oracle_dequant_q8", "oracle_matmul_q4k_q8", "oracle_matmul_q6k_q8",
-                 "oracle_gemv_f64", "oracle_dequant_q8_0", "oracle_matmul_q8_0_q8"):
+                 "oracle_gemv_f64", "oracle_dequant_q8_0", "oracle_matmul_q8_0_q8",
+                 "oracle_dequant_iq4xs", "oracle_matmul_iq4xs_q8"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -134,6 +140,25 @@ def q8_0_fields(blk: np.ndarray):
     return d.value, q
 
 
+def _codebook(codebook) -> np.ndarray:
+    cb = np.ascontiguousarray(codebook, dtype=np.int8)
+    assert cb.shape == (16,), "an IQ4_XS codebook is 16 int8 values"
+    return cb
+
+
+def iq4xs_fields(blk: np.ndarray, codebook):
+    """Decoded fields of one 136-byte IQ4_XS super-block: (d, ls[8], v[256]),
+    v the codebook value of each weight's index."""
+    blk = np.ascontiguousarray(blk, dtype=np.uint8)
+    assert blk.size == IQ4XS_BYTES
+    cb = _codebook(codebook)
+    d = ctypes.c_double()
+    ls = np.zeros(8, np.int32)
+    v = np.zeros(256, np.int32)
+    _load().oracle_iq4xs_fields(_p(blk), _p(cb), ctypes.byref(d), _p(ls), _p(v))
+    return d.value, ls, v
+
+
 def _weight_shape(W: np.ndarray, K: int, nbytes: int):
     W = np.ascontiguousarray(W, dtype=np.uint8)
     nsb = K // 256
@@ -159,6 +184,14 @@ def dequant_q8_0(W: np.ndarray, K: int) -> np.ndarray:
     W, N = _weight_shape(W, K, 8 * Q8_0_BYTES)
     w = np.zeros((N, K), np.float64)
     _check(_load().oracle_dequant_q8_0(_p(W), N, K, _p(w)), "dequant_q8_0")
+    return w
+
+
+def dequant_iq4xs(W: np.ndarray, K: int, codebook) -> np.ndarray:
+    W, N = _weight_shape(W, K, IQ4XS_BYTES)
+    cb = _codebook(codebook)
+    w = np.zeros((N, K), np.float64)
+    _check(_load().oracle_dequant_iq4xs(_p(W), _p(cb), N, K, _p(w)), "dequant_iq4xs")
     return w
 
 
@@ -201,6 +234,16 @@ def matmul_q8_0_q8(W, qs, d8, K, want_isum=False):
     return _matmul(_load().oracle_matmul_q8_0_q8, W, qs, d8, K, 8 * Q8_0_BYTES, want_isum, K // 32)
 
 
+def matmul_iq4xs_q8(W, qs, d8, K, codebook, want_isum=False):
+    """Integer route: y [M][N] (double), sum|terms| [M][N], isums [M][N][K/32] or None."""
+    cb = _codebook(codebook)
+    fn = _load().oracle_matmul_iq4xs_q8
+
+    def call(Wp, qp, dp, M, N, K_, yp, ap, ip):
+        return fn(Wp, _p(cb), qp, dp, M, N, K_, yp, ap, ip)
+    return _matmul(call, W, qs, d8, K, IQ4XS_BYTES, want_isum, K // 32)
+
+
 def gemv_f64(w: np.ndarray, x: np.ndarray) -> np.ndarray:
     """Plain definition y[m][n] = sum_k w[n][k] * x[m][k] in double."""
     w = np.ascontiguousarray(w, dtype=np.float64)
@@ -212,12 +255,15 @@ def gemv_f64(w: np.ndarray, x: np.ndarray) -> np.ndarray:
     return y
 
 
-def matmul(qtype: int, W, qs, d8, K, want_isum=False):
-    """Dispatch on the GGUF type id (8 = Q8_0, 12 = Q4_K, 14 = Q6_K)."""
+def matmul(qtype: int, W, qs, d8, K, want_isum=False, codebook=None):
+    """Dispatch on the GGUF type id (8 = Q8_0, 12 = Q4_K, 14 = Q6_K,
+    23 = IQ4_XS, which needs its codebook)."""
     if qtype == 8:
         return matmul_q8_0_q8(W, qs, d8, K, want_isum)
     if qtype == 12:
         return matmul_q4k_q8(W, qs, d8, K, want_isum)
     if qtype == 14:
         return matmul_q6k_q8(W, qs, d8, K, want_isum)
+    if qtype == 23:
+        return matmul_iq4xs_q8(W, qs, d8, K, codebook, want_isum)
     raise ValueError(f"unsupported type {qtype}")

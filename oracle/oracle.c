@@ -1,5 +1,5 @@
 /*
- * CPU oracle for GGUF Q4_K / Q6_K / Q8_0 x Q8 integer matmul.
+ * CPU oracle for GGUF Q4_K / Q6_K / Q8_0 / IQ4_XS x Q8 integer matmul.
  *
  * TEST INFRASTRUCTURE. Only the tests, the smoke check and the bench's CPU
  * baseline leg may link, load or call this file. The CUDA library never does,
@@ -238,6 +238,51 @@ int oracle_dequant_q8_0(const uint8_t *W, int N, int K, double *w)
     return 0;
 }
 
+/* IQ4_XS (Agent Telemetry log, entries "找到" and "再一輪": 4-bit indices into
+ * a 16-entry int8 codebook, kvalues_iq4nl, and a 32-weight sub-block laid out
+ * like a Q4_0 block, low nibbles holding elements 0..15). The pages name the
+ * codebook but do not print it, so it is an argument here (16 int8 values,
+ * index order), not a table in this file. Public GGUF block layout, 136 bytes
+ * per 256 weights:
+ *   d (fp16, little endian) at byte 0; scales_h (uint16, little endian) at 2;
+ *   scales_l[4] at 4; qs[128] at 8.
+ * Sub-block j = 0..7 (32 weights) has the 6-bit scale
+ *   ls_j = ((scales_l[j/2] >> 4*(j%2)) & 15) | (((scales_h >> 2j) & 3) << 4)
+ * and weight i = 0..31 of it the index
+ *   idx = (qs[16j + i%16] >> 4*(i/16)) & 15,
+ * so w = d * (ls_j - 32) * codebook[idx]. */
+void oracle_iq4xs_fields(const uint8_t *blk, const int8_t *codebook, double *d, int ls[8], int v[256])
+{
+    *d = oracle_half_to_double(read_u16le(blk));
+    int sh = read_u16le(blk + 2);
+    for (int j = 0; j < 8; j++) {
+        int lo = (blk[4 + j / 2] >> (4 * (j % 2))) & 15;
+        int hi = (sh >> (2 * j)) & 3;
+        ls[j] = lo | (hi << 4);
+        for (int i = 0; i < 32; i++) {
+            int idx = (blk[8 + 16 * j + i % 16] >> (4 * (i / 16))) & 15;
+            v[32 * j + i] = codebook[idx];
+        }
+    }
+}
+
+/* Dequantize IQ4_XS rows to double. */
+int oracle_dequant_iq4xs(const uint8_t *W, const int8_t *codebook, int N, int K, double *w)
+{
+    if (N < 0 || K <= 0 || K % 256 != 0) return 1;
+    int nsb = K / 256;
+    double d;
+    int ls[8], v[256];
+    for (int n = 0; n < N; n++) {
+        for (int b = 0; b < nsb; b++) {
+            oracle_iq4xs_fields(W + ((size_t)n * nsb + b) * ORACLE_IQ4XS_BYTES, codebook, &d, ls, v);
+            for (int i = 0; i < 256; i++)
+                w[(size_t)n * K + (size_t)b * 256 + i] = d * (ls[i / 32] - 32) * v[i];
+        }
+    }
+    return 0;
+}
+
 /* ----------------------------------------------------- integer route */
 
 /* Q4_K x Q8 by integer sub-block sums (the route the kernels take).
@@ -357,6 +402,43 @@ int oracle_matmul_q8_0_q8(const uint8_t *W, const int8_t *qs, const float *d8,
                 y[(size_t)m * N + n] += t;
                 if (absterm_out) absterm_out[(size_t)m * N + n] += fabs(t);
                 if (isum_out) isum_out[((size_t)m * N + n) * nb + j] = (int32_t)isum;
+            }
+        }
+    }
+    return 0;
+}
+
+/* IQ4_XS x Q8 by integer sub-block sums:
+ *   isum_j = sum_i codebook[idx(32j+i)] * q8[m][256b+32j+i]   (exact, int64)
+ *   y[m][n] += d * (ls_j - 32) * d8[m][8b+j] * isum_j          (double)
+ * isum_out (optional) is [M][N][K/32]; absterm_out as for Q4_K. */
+int oracle_matmul_iq4xs_q8(const uint8_t *W, const int8_t *codebook, const int8_t *qs, const float *d8,
+                           int M, int N, int K,
+                           double *y, double *absterm_out, int32_t *isum_out)
+{
+    if (M < 0 || N < 0 || K <= 0 || K % 256 != 0) return 1;
+    int nsb = K / 256;
+    int nsub = K / 32;
+    double d;
+    int ls[8], v[256];
+    for (int m = 0; m < M; m++)
+        for (int n = 0; n < N; n++) {
+            y[(size_t)m * N + n] = 0.0;
+            if (absterm_out) absterm_out[(size_t)m * N + n] = 0.0;
+        }
+    for (int n = 0; n < N; n++) {
+        for (int b = 0; b < nsb; b++) {
+            oracle_iq4xs_fields(W + ((size_t)n * nsb + b) * ORACLE_IQ4XS_BYTES, codebook, &d, ls, v);
+            for (int m = 0; m < M; m++) {
+                const int8_t *a = qs + (size_t)m * K + (size_t)b * 256;
+                for (int j = 0; j < 8; j++) {
+                    int64_t isum = 0;
+                    for (int i = 0; i < 32; i++) isum += (int64_t)v[32 * j + i] * a[32 * j + i];
+                    double t = d * (ls[j] - 32) * (double)d8[(size_t)m * nsub + 8 * b + j] * (double)isum;
+                    y[(size_t)m * N + n] += t;
+                    if (absterm_out) absterm_out[(size_t)m * N + n] += fabs(t);
+                    if (isum_out) isum_out[((size_t)m * N + n) * nsub + 8 * b + j] = (int32_t)isum;
+                }
             }
         }
     }

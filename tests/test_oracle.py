@@ -467,3 +467,99 @@ def test_q8_0_isums_brute_force():
         qrow = np.array(qrow, np.int64)
         for m in range(M):
             assert np.array_equal(isum[m, n], (qrow * qs[m].astype(np.int64)).reshape(-1, 32).sum(1))
+
+
+# ------------------------------------------------------------ IQ4_XS
+
+def ref_iq4xs_decode(blk: bytes, codebook):
+    """Independent IQ4_XS reader (bit offsets, not masks), from the block
+    description: d fp16 at 0, scales_h (16 bits) at 2, scales_l (4 bytes) at
+    4, 128 index bytes at 8; sub-block j's 6-bit scale takes 4 bits from
+    scales_l at bit 4j and 2 bits from scales_h at bit 2j; weight i of
+    sub-block j is the low (i < 16) or high nibble of index byte 16j + i%16."""
+    d = _f16(blk, 0)
+    ls = [_bits(blk, 32 + 4 * j, 4) | (_bits(blk, 16 + 2 * j, 2) << 4) for j in range(8)]
+    v = []
+    for i in range(256):
+        j, r = divmod(i, 32)
+        byte = 8 + 16 * j + (r % 16)
+        v.append(int(codebook[_bits(blk, 8 * byte + (4 if r >= 16 else 0), 4)]))
+    return d, ls, v
+
+
+def test_iq4xs_decode_matches_independent_reader():
+    cb = synth.gen_codebook(3)
+    W = synth.gen_iq4xs(31, 3, 512)
+    assert W.shape == (3, 2 * 136)
+    for blk in W.reshape(-1, 136):
+        d, ls, v = oracle.iq4xs_fields(blk, cb)
+        rd, rls, rv = ref_iq4xs_decode(bytes(blk), cb)
+        assert d == rd and list(ls) == rls and list(v) == rv
+    w = oracle.dequant_iq4xs(W, 512, cb)
+    for n in range(3):
+        for b in range(2):
+            rd, rls, rv = ref_iq4xs_decode(bytes(W[n, 136 * b:136 * (b + 1)]), cb)
+            for i in range(256):
+                assert w[n, 256 * b + i] == rd * (rls[i // 32] - 32) * rv[i]
+
+
+def test_iq4xs_one_hot_and_scale_extremes():
+    cb = np.arange(-8, 8, dtype=np.int8) * 3 + 1      # index k -> 3k - 23, all distinct
+    blk = bytearray(136)
+    blk[0:2] = (0x3C00).to_bytes(2, "little")         # d = 1
+    # sub-block scales: ls = 0, 63, 33, 32, 1, 62, 17, 48 through both bit fields
+    ls = [0, 63, 33, 32, 1, 62, 17, 48]
+    sh = 0
+    for j, l in enumerate(ls):
+        blk[4 + j // 2] |= (l & 15) << (4 * (j % 2))
+        sh |= (l >> 4) << (2 * j)
+    blk[2:4] = sh.to_bytes(2, "little")
+    # every index 8 (value 1) except one high and one low nibble per sub-block
+    for k in range(128):
+        blk[8 + k] = 0x88
+    for j in range(8):
+        blk[8 + 16 * j + j] = (blk[8 + 16 * j + j] & 0xF0) | j          # weight 32j + j: index j
+        blk[8 + 16 * j + 15 - j] = (blk[8 + 16 * j + 15 - j] & 0x0F) | ((15 - j) << 4)  # weight 32j + 31 - j
+    w = oracle.dequant_iq4xs(np.frombuffer(bytes(blk), np.uint8), 256, cb)[0]
+    for j in range(8):
+        s = ls[j] - 32
+        for i in range(32):
+            idx = j if i == j else (15 - j if i == 31 - j else 8)
+            assert w[32 * j + i] == s * (3 * idx - 23), (j, i)
+    assert w[0] == -32 * -23 and w[32 + 30] == 31 * (3 * 14 - 23)
+
+
+@pytest.mark.parametrize("M", [1, 3, 8])
+def test_iq4xs_integer_route_equals_dequant_gemv(M):
+    cb = synth.gen_codebook(M)
+    N, K = 40, 1024
+    W = synth.gen_iq4xs(90 + M, N, K)
+    x = synth.gen_x(700 + M, M, K)
+    qs, d8, _ = oracle.quantize_q8(x)
+    y, ab, _ = oracle.matmul(synth.IQ4_XS, W, qs, d8, K, codebook=cb)
+    yd = oracle.gemv_f64(oracle.dequant_iq4xs(W, K, cb), oracle.dequant_q8(qs, d8))
+    assert np.all(np.abs(y - yd) <= 1e-12 * ab + 1e-300)
+    assert np.all(ab > 0)
+
+
+def test_iq4xs_isums_brute_force():
+    cb = synth.gen_codebook(9)
+    N, K, M = 3, 512, 2
+    W = synth.gen_iq4xs(13, N, K)
+    x = synth.gen_x(22, M, K)
+    qs, d8, _ = oracle.quantize_q8(x)
+    _, _, isum = oracle.matmul(synth.IQ4_XS, W, qs, d8, K, want_isum=True, codebook=cb)
+    for n in range(N):
+        vrow = []
+        for b in range(K // 256):
+            vrow += ref_iq4xs_decode(bytes(W[n, 136 * b:136 * (b + 1)]), cb)[2]
+        vrow = np.array(vrow, np.int64)
+        for m in range(M):
+            assert np.array_equal(isum[m, n], (vrow * qs[m].astype(np.int64)).reshape(-1, 32).sum(1))
+
+
+def test_gen_codebook_is_sixteen_increasing_int8():
+    for seed in range(5):
+        cb = synth.gen_codebook(seed)
+        assert cb.dtype == np.int8 and cb.shape == (16,)
+        assert np.all(np.diff(cb.astype(np.int64)) > 0) and cb[0] == -128 and cb[-1] == 127
