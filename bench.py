@@ -683,6 +683,30 @@ def secondary_workloads(device, world):
         res[str(M)] = row
     out["llama3-8b-layer-swiglu-down"] = {"rotated_copies": copies, "layer_bytes": wl.layer_weight_bytes(),
                                           "by_m": res}
+    # IQ4_XS: the 17408 x 5120 ffn_up shape whose batch cost the IQ4_XS
+    # entries of the Agent Telemetry log measure, with a synthetic codebook;
+    # quantize + matmul per copy, weights rotated past L2
+    N, K = 17408, 5120
+    cb = synth.gen_codebook(0)
+    w0 = torch.from_numpy(synth.gen_iq4xs(17, N, K).reshape(-1)).to(device)
+    wbytes = synth.weight_bytes(synth.IQ4_XS, N, K)
+    copies = max(3, -(-3 * L2_BYTES // wbytes))
+    Ws = [w0] + [w0.clone() for _ in range(copies - 1)]
+    res = {}
+    for M in (1, 8):
+        x = torch.from_numpy(synth.gen_x(18, M, K)).to(device)
+        buf = xq.quantize_q8(x)
+        y = torch.empty((M, N), dtype=torch.float32, device=device)
+
+        def step():
+            for c in range(copies):
+                xq.quantize_q8(x, out=buf)
+                xq.matmul_iq4xs_q8(Ws[c], cb, buf, M, N, K, y=y)
+
+        sec = max_over_ranks(time_region(step, 5, 3, world, device), world, device) / (5 * copies)
+        res[str(M)] = {"us": round(1e6 * sec, 2), "GBps": round(wbytes / sec / 1e9, 1)}
+    out["iq4xs-ffn_up-17408x5120"] = {"rotated_copies": copies, "weight_bytes": wbytes, "by_m": res,
+                                      "codebook": "synthetic (the pages do not print the format's table)"}
     # prefill tile M=512: up (Q4_K) then down (Q6_K), each launch timed on its own
     wl = synth.WORKLOADS["qwen3-8b-ffn-prefill512"]
     M = 512

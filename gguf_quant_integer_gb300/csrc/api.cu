@@ -15,8 +15,11 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 int block_bytes(int type) {
   // bytes per 256 weights
-  return type == XQ_TYPE_Q4_K ? xq::kQ4kBytes
-                              : (type == XQ_TYPE_Q6_K ? xq::kQ6kBytes : (type == XQ_TYPE_Q8_0 ? xq::kQ80Group : 0));
+  return type == XQ_TYPE_Q4_K    ? xq::kQ4kBytes
+         : type == XQ_TYPE_Q6_K  ? xq::kQ6kBytes
+         : type == XQ_TYPE_Q8_0  ? xq::kQ80Group
+         : type == XQ_TYPE_IQ4_XS ? xq::kIq4xsBytes
+                                 : 0;
 }
 
 xq_status check_shape(int M, int N, int K) {
@@ -31,7 +34,7 @@ xq_status check_shape(int M, int N, int K) {
 // from the GEMV-image layout, never split over K, so that each token's row
 // of y is computed by the same operations whatever M is.
 xq_status run_matmul(int type, const void* W, const void* xq, int M, int N, int K, float* y,
-                     int32_t* isum, cudaStream_t s, bool invariant = false) {
+                     int32_t* isum, cudaStream_t s, bool invariant = false, const uint32_t* codebook = nullptr) {
   const xq::Q8Layout L = xq::q8_layout(M, K, invariant);
   const uint8_t* base = static_cast<const uint8_t*>(xq);
   if (M > kMaxGemvM && !invariant) {
@@ -54,6 +57,8 @@ xq_status run_matmul(int type, const void* W, const void* xq, int M, int N, int 
       q.chunk = c;
       q.nch = 1;
       q.gemv_image = invariant;
+      if (codebook)
+        for (int i = 0; i < 4; ++i) q.codebook[i] = codebook[i];
       if (n == xq::kMaxProj || c + 1 == L.chunks) {
         if (xq::launch_gemv_mma(type, items, n, s, true) != cudaSuccess) return XQ_ERR_CUDA;
         n = 0;
@@ -165,6 +170,7 @@ xq_status layer_inputs(const xq_proj* proj, int n_proj, int n_inputs, int M, int
   for (int p = 0; p < n_proj; ++p) {
     const xq_proj& q = proj[p];
     if (block_bytes(q.type) == 0) return XQ_ERR_ARG;
+    if (q.type == XQ_TYPE_IQ4_XS) return XQ_ERR_UNSUPPORTED;  // its codebook has no place in xq_proj
     if (q.input < 0 || q.input >= n_inputs) return XQ_ERR_ARG;
     const xq_status st = check_shape(M, q.N, q.K);
     if (st != XQ_OK) return st;
@@ -305,6 +311,7 @@ xq_status xq_quantize_q8_invariant(const float* x, int M, int K, void* xq, xq_st
 xq_status xq_matmul_invariant(int type, const void* W, const void* xq, int M, int N, int K, float* y,
                               xq_stream stream) {
   if (block_bytes(type) == 0) return XQ_ERR_ARG;
+  if (type == XQ_TYPE_IQ4_XS) return XQ_ERR_UNSUPPORTED;  // no codebook argument here
   xq_status st = check_shape(M, N, K);
   if (st != XQ_OK) return st;
   if (M == 0 || N == 0) return XQ_OK;
@@ -352,6 +359,37 @@ xq_status xq_debug_isums_q8_0(const void* W, const void* xq, int M, int N, int K
                               int32_t* isum, xq_stream stream) {
   if (!isum) return XQ_ERR_ARG;
   return matmul_entry(XQ_TYPE_Q8_0, W, xq, M, N, K, y, isum, stream);
+}
+
+// IQ4_XS: M <= 8 on the tensor-core GEMV, rows that are 16-byte multiples
+// (K a multiple of 512); the codebook is read from the host during the call.
+static xq_status iq4xs_entry(const void* W, const int8_t* codebook, const void* xq, int M, int N, int K, float* y,
+                             int32_t* isum, xq_stream stream) {
+  xq_status st = check_shape(M, N, K);
+  if (st != XQ_OK) return st;
+  if ((K % 512) != 0) return XQ_ERR_SHAPE;
+  if (M == 0 || N == 0) return XQ_OK;
+  if (!W || !xq || !y || !codebook) return XQ_ERR_ARG;
+  if (!aligned16(W) || !aligned16(xq) || !aligned16(y) || (isum && !aligned16(isum))) return XQ_ERR_ALIGN;
+  if (M > kMaxGemvM) return XQ_ERR_UNSUPPORTED;
+  uint32_t cb[4];
+  for (int i = 0; i < 4; ++i)
+    cb[i] = static_cast<uint32_t>(static_cast<uint8_t>(codebook[4 * i])) |
+            (static_cast<uint32_t>(static_cast<uint8_t>(codebook[4 * i + 1])) << 8) |
+            (static_cast<uint32_t>(static_cast<uint8_t>(codebook[4 * i + 2])) << 16) |
+            (static_cast<uint32_t>(static_cast<uint8_t>(codebook[4 * i + 3])) << 24);
+  return run_matmul(XQ_TYPE_IQ4_XS, W, xq, M, N, K, y, isum, reinterpret_cast<cudaStream_t>(stream), false, cb);
+}
+
+xq_status xq_matmul_iq4xs_q8(const void* W, const int8_t* codebook, const void* xq, int M, int N, int K, float* y,
+                             xq_stream stream) {
+  return iq4xs_entry(W, codebook, xq, M, N, K, y, nullptr, stream);
+}
+
+xq_status xq_debug_isums_iq4xs(const void* W, const int8_t* codebook, const void* xq, int M, int N, int K, float* y,
+                               int32_t* isum, xq_stream stream) {
+  if (!isum) return XQ_ERR_ARG;
+  return iq4xs_entry(W, codebook, xq, M, N, K, y, isum, stream);
 }
 
 xq_status xq_debug_isums_q4k(const void* W, const void* xq, int M, int N, int K, float* y,

@@ -75,6 +75,7 @@ struct Proj {
   int32_t* isum;
   float* partial;      // split: [nch][8][kGemvRows * row blocks]
   unsigned int* arrive;  // split: one arrival count per 16-row group
+  uint32_t cb[4];        // IQ4_XS: codebook bytes with their sign bits flipped
   int N, K, M, task0, nch;
 };
 
@@ -96,8 +97,8 @@ constexpr int kDecBytes = 8 * 16 * 16;  // per warp: one float4 per (32-block, r
 // starting at the 16-byte boundary at or below the 210-byte super-block.
 template <int TYPE>
 struct GLay {
-  static constexpr int kBoxRow = TYPE == 12 ? kQ4kBytes : (TYPE == 8 ? kQ80Group : 240);
-  static constexpr int kStages = kGemvWarps == 4 ? (TYPE == 12 ? 4 : 3) : (TYPE == 12 ? 4 : 2);
+  static constexpr int kBoxRow = TYPE == 12 ? kQ4kBytes : (TYPE == 8 ? kQ80Group : (TYPE == 23 ? 144 : 240));
+  static constexpr int kStages = kGemvWarps == 4 ? ((TYPE == 12 || TYPE == 23) ? 4 : 3) : ((TYPE == 12 || TYPE == 23) ? 4 : 2);
   static constexpr int kBlockBytes = 16 * kBoxRow;  // 16 rows x one super-block
   static constexpr int kFragOff = kGemvWarps * kBlockBytes;
   static constexpr int kFscOff = kFragOff + 8 * 512;
@@ -108,6 +109,7 @@ static_assert(kGemvWarps != 4 || GLay<12>::kStageBytes == 13824, "Q4_K stage lay
 static_assert(kGemvCtasPerSM * (GLay<12>::kSmemBytes + 1024) <= 228 * 1024, "Q4_K: resident CTAs per SM");
 static_assert(kGemvCtasPerSM * (GLay<14>::kSmemBytes + 1024) <= 228 * 1024, "Q6_K: resident CTAs per SM");
 static_assert(kGemvCtasPerSM * (GLay<8>::kSmemBytes + 1024) <= 228 * 1024, "Q8_0: resident CTAs per SM");
+static_assert(kGemvCtasPerSM * (GLay<23>::kSmemBytes + 1024) <= 228 * 1024, "IQ4_XS: resident CTAs per SM");
 constexpr long long kWaitClocks = 1LL << 32;
 
 __device__ __forceinline__ int mma_row(int i) { return 8 * (i >> 3) + 2 * (i & 3) + ((i >> 2) & 1); }
@@ -117,6 +119,7 @@ template <int TYPE>
 __device__ __forceinline__ int weight_box_x(int b) {
   if constexpr (TYPE == 12) return b * (kQ4kBytes / 8);
   else if constexpr (TYPE == 8) return b * (kQ80Group / 8);
+  else if constexpr (TYPE == 23) return (kIq4xsBytes * b) & ~15;
   else return (kQ6kBytes * b) & ~15;
 }
 
@@ -429,6 +432,91 @@ __device__ __forceinline__ void compute_block_q8_0(const uint8_t* blk, const uin
   }
 }
 
+// IQ4_XS (Agent Telemetry log, entries on the IQ4_XS batch kernels: 4-bit
+// indices into a 16-entry int8 codebook; public GGUF block, 136 bytes: fp16 d
+// at 0, scales_h at 2, scales_l[4] at 4, 128 index bytes at 8). A stage row
+// is the 144-byte window from the 16-byte boundary at or below the
+// super-block, which begins `off` = 0 or 8 bytes in (136 b mod 16). Lane l
+// takes weight row l%16 and sub-blocks 4*(l/16) .. +3, writing (alpha, alpha,
+// 0, 0) with alpha = d * (ls_j - 32), an exact product: ls_j is 4 bits of
+// scales_l at bit 4j and 2 bits of scales_h at bit 2j.
+__device__ __forceinline__ void decode_scales_iq4xs(const uint8_t* blk, int off, float4* dec, int lane) {
+  const int r = lane & 15, half = lane >> 4;
+  const uint2 h = *reinterpret_cast<const uint2*>(blk + r * GLay<23>::kBoxRow + off);  // d | scales_h, scales_l
+  const float d = half_bits_to_float(h.x);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int j = 4 * half + k;
+    const int ls = static_cast<int>(((h.y >> (4 * j)) & 15u) | (((h.x >> (16 + 2 * j)) & 3u) << 4));
+    const float a = d * static_cast<float>(ls - 32);
+    dec[j * 16 + r] = make_float4(a, a, 0.0f, 0.0f);
+  }
+}
+
+// Codebook bytes (sign bits flipped) of four 4-bit indices, one index per
+// byte of x: two byte permutes over the codebook halves, chosen per byte by
+// index bit 3 (a sign-replicating permute of x << 4 makes the byte mask).
+__device__ __forceinline__ uint32_t iq4_lookup(uint32_t x, const uint32_t (&cb)[4]) {
+  const uint32_t sel = prmt(x | (x >> 4), 0u, 0x4420u) & 0x7777u;  // the four indices' low 3 bits, as selectors
+  const uint32_t lo = prmt(cb[0], cb[1], sel), hi = prmt(cb[2], cb[3], sel);
+  const uint32_t m = prmt(x << 4, 0u, 0xBA98u);
+  return (hi & m) | (lo & ~m);
+}
+
+// IQ4_XS sub-block j of rows r0, r1: lane (n8, t) takes weights 8t..8t+7
+// (the activation image's slot order): low nibbles of index bytes
+// 16j + 8t .. +7 for t < 2, high nibbles of bytes 16j + 8(t-2) .. +7 for
+// t >= 2. Each index becomes its codebook value, then the exact fp16 integer
+// as for Q8_0 (sign bit flipped, placed under the exponent of 1024, 1152
+// subtracted). |value| <= 128, so a sub-block sum is at most 128*127*32 in
+// magnitude and D = isum exactly. Combine: acc += (alpha * d8) * D.
+template <bool ISUM>
+__device__ __forceinline__ void compute_block_iq4xs(const uint8_t* blk, int off, const uint8_t* act, const float4* dec,
+                                                    const Proj& P, int rg, int b, int n8, int t, int lane,
+                                                    f2 (&acc)[2]) {
+  const int r0 = mma_row(n8), r1 = r0 + 8;
+  const uint8_t* q0 = blk + r0 * GLay<23>::kBoxRow + off + 8 + 8 * (t & 1);
+  const uint8_t* q1 = blk + r1 * GLay<23>::kBoxRow + off + 8 + 8 * (t & 1);
+  const unsigned sh = 4u * static_cast<unsigned>(t >> 1);
+  const uint32_t cb[4] = {P.cb[0], P.cb[1], P.cb[2], P.cb[3]};
+  const uint4* fp = reinterpret_cast<const uint4*>(act) + lane;
+  const ulonglong2* sp = reinterpret_cast<const ulonglong2*>(act + (GLay<23>::kFscOff - GLay<23>::kFragOff)) + t;
+  const ulonglong2* dp = reinterpret_cast<const ulonglong2*>(dec);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const uint2 w0 = *reinterpret_cast<const uint2*>(q0 + 16 * j);
+    const uint2 w1 = *reinterpret_cast<const uint2*>(q1 + 16 * j);
+    uint32_t a[2][4];  // [k-half][a0..a3]
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const uint32_t x0 = iq4_lookup(((h ? w0.y : w0.x) >> sh) & 0x0F0F0F0Fu, cb);
+      const uint32_t x1 = iq4_lookup(((h ? w1.y : w1.x) >> sh) & 0x0F0F0F0Fu, cb);
+      a[h][0] = hsub2(prmt(x0, 0x64646464u, 0x4240u), 0x64806480u);  // row r0, weights 4h', 4h'+2
+      a[h][1] = hsub2(prmt(x1, 0x64646464u, 0x4240u), 0x64806480u);  // row r1
+      a[h][2] = hsub2(prmt(x0, 0x64646464u, 0x4341u), 0x64806480u);  // row r0, weights 4h'+1, 4h'+3
+      a[h][3] = hsub2(prmt(x1, 0x64646464u, 0x4341u), 0x64806480u);  // row r1
+    }
+    const uint4 B = fp[j * 32];
+    float D[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    mma16816(D, a[0][0], a[0][1], a[0][2], a[0][3], B.x, B.y);
+    mma16816(D, a[1][0], a[1][1], a[1][2], a[1][3], B.z, B.w);
+    const ulonglong2 f = sp[j * 4];  // (d8 c0, d8 c1), (s8 c0, s8 c1)
+    const ulonglong2 e0 = dp[j * 16 + r0], e1 = dp[j * 16 + r1];
+    acc[0] = fma2(mul2(e0.x, f.x), pk(D[0], D[1]), acc[0]);
+    acc[1] = fma2(mul2(e1.x, f.x), pk(D[2], D[3]), acc[1]);
+    if (ISUM) {
+      const int nsub = P.K >> 5;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int row = rg * 16 + ((e >> 1) ? r1 : r0);
+        const int col = 2 * t + (e & 1);
+        if (row < P.N && col < P.M)
+          P.isum[(static_cast<size_t>(col) * P.N + row) * nsub + 8 * b + j] = static_cast<int32_t>(D[e]);
+      }
+    }
+  }
+}
+
 __device__ __forceinline__ void store_y(const Proj& P, int rg, int n8, int t, float v00, float v01, float v10,
                                         float v11) {
   const int r0 = rg * 16 + mma_row(n8), r1 = r0 + 8, c0 = 2 * t, c1 = c0 + 1;
@@ -631,6 +719,11 @@ __device__ __forceinline__ void gemv_mma_body(const Group& G) {
         decode_scales_q8_0(st + warp * kBlockBytes, dec, lane);
         __syncwarp();
         compute_block_q8_0<ISUM>(st + warp * kBlockBytes, st + kFragOff, dec, P, rg, m.y, n8, t, lane, acc);
+      } else if constexpr (TYPE == 23) {
+        const int off = (kIq4xsBytes * m.y) & 15;  // 0 or 8, the same for every row (rows are 16-byte multiples)
+        decode_scales_iq4xs(st + warp * kBlockBytes, off, dec, lane);
+        __syncwarp();
+        compute_block_iq4xs<ISUM>(st + warp * kBlockBytes, off, st + kFragOff, dec, P, rg, m.y, n8, t, lane, acc);
       } else {
         const int off = (kQ6kBytes * m.y) & 15;  // the same for every row: rows are 16-byte multiples
         decode_scales_q6(st + warp * kBlockBytes, off, dec, lane);
@@ -701,8 +794,9 @@ int max_ctas() {
 }
 
 // Weight rows as a 2D tensor, boxes of 16 rows: Q4_K as 8-byte elements
-// {row_bytes/8, N} with one super-block per box row; Q6_K as bytes
-// {row_bytes, N} with 240-byte box rows (rows must be 16-byte multiples).
+// {row_bytes/8, N} with one super-block per box row; Q6_K and IQ4_XS as
+// bytes {row_bytes, N} with 240- and 144-byte box rows (rows must be 16-byte
+// multiples).
 bool encode_weight_map(int type, CUtensorMap* map, const uint8_t* W, int N, int K) {
   const unsigned long long nsb = static_cast<unsigned long long>(K / 256);
   if (type == 12)
@@ -711,6 +805,9 @@ bool encode_weight_map(int type, CUtensorMap* map, const uint8_t* W, int N, int 
   if (type == 8)
     return encode_tma_2d(map, CU_TENSOR_MAP_DATA_TYPE_UINT64, W, nsb * kQ80Group / 8, static_cast<unsigned long long>(N),
                          nsb * kQ80Group, kQ80Group / 8, 16);
+  if (type == 23)
+    return encode_tma_2d(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, W, nsb * kIq4xsBytes, static_cast<unsigned long long>(N),
+                         nsb * kIq4xsBytes, GLay<23>::kBoxRow, 16);
   return encode_tma_2d(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, W, nsb * kQ6kBytes, static_cast<unsigned long long>(N),
                        nsb * kQ6kBytes, GLay<14>::kBoxRow, 16);
 }
@@ -749,12 +846,12 @@ bool encode_tma_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, u
 }
 
 bool gemv_mma_supports(int type, int K) {
-  return type == 12 || type == 8 || (type == 14 && ((K / 256) % 8) == 0);
+  return type == 12 || type == 8 || (type == 14 && ((K / 256) % 8) == 0) || (type == 23 && ((K / 256) % 2) == 0);
 }
 
 cudaError_t launch_gemv_mma(int type, const MmaProj* projs, int n, cudaStream_t s, bool pdl, unsigned int* counter,
                             uint8_t* arrive_ws, uint8_t* partial_ws, bool wait_prev) {
-  if (n <= 0 || n > kMaxProj || (type != 12 && type != 14 && type != 8)) return cudaErrorInvalidValue;
+  if (n <= 0 || n > kMaxProj || (type != 12 && type != 14 && type != 8 && type != 23)) return cudaErrorInvalidValue;
   // Per-projection K-chunking (only with split workspaces) and task cost.
   const bool split = arrive_ws != nullptr && partial_ws != nullptr;
   int nch[kMaxProj], cost[kMaxProj];
@@ -806,6 +903,7 @@ cudaError_t launch_gemv_mma(int type, const MmaProj* projs, int n, cudaStream_t 
     P.nch = nch[src];
     P.partial = nullptr;
     P.arrive = nullptr;
+    for (int i = 0; i < 4; ++i) P.cb[i] = q.codebook[i] ^ 0x80808080u;  // IQ4_XS operand bias
     const int rbs = gemv_row_blocks(q.N);
     if (P.nch > 1) {
       P.partial = reinterpret_cast<float*>(partial_ws + partial_off[src]);
@@ -817,14 +915,16 @@ cudaError_t launch_gemv_mma(int type, const MmaProj* projs, int n, cudaStream_t 
   }
   G.total = total;
   if (total == 0) return cudaSuccess;
-  const int cap = type == 12  ? (isum ? max_ctas<12, true>() : max_ctas<12, false>())
-                  : type == 8 ? (isum ? max_ctas<8, true>() : max_ctas<8, false>())
-                              : (isum ? max_ctas<14, true>() : max_ctas<14, false>());
+  const int cap = type == 12   ? (isum ? max_ctas<12, true>() : max_ctas<12, false>())
+                  : type == 8  ? (isum ? max_ctas<8, true>() : max_ctas<8, false>())
+                  : type == 23 ? (isum ? max_ctas<23, true>() : max_ctas<23, false>())
+                               : (isum ? max_ctas<14, true>() : max_ctas<14, false>());
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(total < cap ? total : cap));
   cfg.blockDim = dim3(32 * (kGemvWarps + 1));
   cfg.dynamicSmemBytes =
-      type == 12 ? GLay<12>::kSmemBytes : (type == 8 ? GLay<8>::kSmemBytes : GLay<14>::kSmemBytes);
+      type == 12 ? GLay<12>::kSmemBytes
+                 : (type == 8 ? GLay<8>::kSmemBytes : (type == 23 ? GLay<23>::kSmemBytes : GLay<14>::kSmemBytes));
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -834,6 +934,9 @@ cudaError_t launch_gemv_mma(int type, const MmaProj* projs, int n, cudaStream_t 
   if (type == 8)
     return isum ? cudaLaunchKernelEx(&cfg, gemv_mma_kernel<8, true>, G)
                 : cudaLaunchKernelEx(&cfg, gemv_mma_kernel<8, false>, G);
+  if (type == 23)
+    return isum ? cudaLaunchKernelEx(&cfg, gemv_mma_kernel<23, true>, G)
+                : cudaLaunchKernelEx(&cfg, gemv_mma_kernel<23, false>, G);
   if (type == 12)
     return isum ? cudaLaunchKernelEx(&cfg, gemv_mma_kernel<12, true>, G)
                 : cudaLaunchKernelEx(&cfg, gemv_mma_kernel<12, false>, G);

@@ -11,6 +11,7 @@ namespace xq {
 
 constexpr int kQ4kBytes = 144;  // GGUF Q4_K super-block: 256 weights
 constexpr int kQ6kBytes = 210;  // GGUF Q6_K super-block: 256 weights
+constexpr int kIq4xsBytes = 136;  // GGUF IQ4_XS super-block: 256 weights
 constexpr int kQ80Bytes = 34;   // GGUF Q8_0 block: 32 weights
 constexpr int kQ80Group = 8 * kQ80Bytes;  // 8 Q8_0 blocks: 256 weights, 16-byte multiple
 constexpr int kNumSMs = 152;    // GB300: 2 dies x 76 SMs
@@ -173,6 +174,7 @@ struct MmaProj {
   float* y;            // [M_total][N]; this launch writes tokens 8*chunk .. 8*chunk+7
   int32_t* isum;       // optional [M_total][N][K/32], only with M_total <= 8
   int N, K, M_total, chunk;
+  uint32_t codebook[4] = {0u, 0u, 0u, 0u};  // IQ4_XS: the 16 int8 values, little-endian bytes
 };
 
 // K-chunks a projection's rows are split into when a split workspace is

@@ -18,6 +18,7 @@ LIB_PATH = os.path.join(_HERE, "_build", "libxq.so")
 XQ_TYPE_Q8_0 = 8
 XQ_TYPE_Q4_K = 12
 XQ_TYPE_Q6_K = 14
+XQ_TYPE_IQ4_XS = 23
 
 STATUS = {0: "XQ_OK", 1: "XQ_ERR_ARG", 2: "XQ_ERR_SHAPE", 3: "XQ_ERR_ALIGN",
           4: "XQ_ERR_WORKSPACE", 5: "XQ_ERR_CUDA", 6: "XQ_ERR_UNSUPPORTED"}
@@ -28,7 +29,8 @@ SYMBOLS = ("xq_status_str", "xq_q8_bytes", "xq_weight_bytes", "xq_quantize_q8",
            "xq_layer_mixed", "xq_debug_isums_q4k", "xq_debug_isums_q6k", "xq_layer_mixed_static",
            "xq_q8_bytes_invariant", "xq_quantize_q8_invariant", "xq_matmul_invariant",
            "xq_matmul_q8_0_q8", "xq_debug_isums_q8_0", "xq_silu_mul_quantize_q8",
-           "xq_layer_ffn_workspace_bytes", "xq_layer_mixed_ffn")
+           "xq_layer_ffn_workspace_bytes", "xq_layer_mixed_ffn", "xq_matmul_iq4xs_q8",
+           "xq_debug_isums_iq4xs")
 
 
 class XQError(RuntimeError):
@@ -80,6 +82,10 @@ def lib(path: str | None = None):
         getattr(L, fn).argtypes = [P, P, I, I, I, P, P]
     for fn in ("xq_debug_isums_q4k", "xq_debug_isums_q6k", "xq_debug_isums_q8_0"):
         getattr(L, fn).argtypes = [P, P, I, I, I, P, P, P]
+    L.xq_matmul_iq4xs_q8.argtypes = [P, P, P, I, I, I, P, P]
+    L.xq_matmul_iq4xs_q8.restype = I
+    L.xq_debug_isums_iq4xs.argtypes = [P, P, P, I, I, I, P, P, P]
+    L.xq_debug_isums_iq4xs.restype = I
     L.xq_layer_workspace_bytes.argtypes = [ctypes.POINTER(xq_proj), I, I, I]
     L.xq_layer_workspace_bytes.restype = S
     L.xq_layer_mixed.argtypes = [ctypes.POINTER(xq_proj), I, ctypes.POINTER(ctypes.c_void_p), I, I, P, S, P]
@@ -155,6 +161,40 @@ def matmul_q4k_q8(W, xq, M, N, K, y=None, stream=None):
 
 def matmul_q6k_q8(W, xq, M, N, K, y=None, stream=None):
     return matmul(XQ_TYPE_Q6_K, W, xq, M, N, K, y, stream)
+
+
+def _codebook(codebook):
+    """16 int8 codebook values as a host buffer (read by the C call)."""
+    import numpy as np
+    cb = np.ascontiguousarray(codebook, dtype=np.int8)
+    if cb.shape != (16,):
+        raise ValueError("an IQ4_XS codebook is 16 int8 values")
+    return cb
+
+
+def matmul_iq4xs_q8(W, codebook, xq, M: int, N: int, K: int, y=None, stream=None):
+    """y [M, N] fp32 = x W^T for IQ4_XS weight bytes W and its 16-value int8
+    codebook (host array), M <= 8."""
+    import torch
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float32, device=W.device)
+    cb = _codebook(codebook)
+    _check("xq_matmul_iq4xs_q8", lib().xq_matmul_iq4xs_q8(_ptr(W), cb.ctypes.data, _ptr(xq), M, N, K, _ptr(y),
+                                                         _stream(stream)))
+    return y
+
+
+def debug_isums_iq4xs(W, codebook, xq, M: int, N: int, K: int, y=None, isum=None, stream=None):
+    """IQ4_XS matmul that also writes the exact int32 sub-block sums [M, N, K/32]."""
+    import torch
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float32, device=W.device)
+    if isum is None:
+        isum = torch.empty((M, N, K // 32), dtype=torch.int32, device=W.device)
+    cb = _codebook(codebook)
+    _check("xq_debug_isums_iq4xs", lib().xq_debug_isums_iq4xs(_ptr(W), cb.ctypes.data, _ptr(xq), M, N, K, _ptr(y),
+                                                             _ptr(isum), _stream(stream)))
+    return y, isum
 
 
 def q8_bytes_invariant(M: int, K: int) -> int:

@@ -87,6 +87,7 @@ typedef enum {
 #define XQ_TYPE_Q8_0 8
 #define XQ_TYPE_Q4_K 12
 #define XQ_TYPE_Q6_K 14
+#define XQ_TYPE_IQ4_XS 23
 
 /* Human-readable name of a status code (static string, never NULL). */
 XQ_API const char *xq_status_str(xq_status s);
@@ -99,7 +100,8 @@ XQ_API const char *xq_status_str(xq_status s);
 XQ_API size_t xq_q8_bytes(int M, int K);
 
 /* Bytes of an N x K weight of GGUF type `type` (N*(K/256)*144 for Q4_K,
- * N*(K/256)*210 for Q6_K). Returns 0 for an unknown type or a bad shape. */
+ * N*(K/256)*210 for Q6_K, N*(K/256)*272 for Q8_0, N*(K/256)*136 for
+ * IQ4_XS). Returns 0 for an unknown type or a bad shape. */
 XQ_API size_t xq_weight_bytes(int type, int N, int K);
 
 /* Q8 activation quantization (xLLM v0.7 article, sections B1.3 and C.1:
@@ -147,6 +149,25 @@ XQ_API xq_status xq_matmul_q6k_q8(const void *W, const void *xq, int M, int N, i
  * which run the GEMV per 8-token chunk for any M. */
 XQ_API xq_status xq_matmul_q8_0_q8(const void *W, const void *xq, int M, int N, int K,
                             float *y, xq_stream stream);
+
+/* Same for an IQ4_XS weight (Agent Telemetry log, entries on the IQ4_XS
+ * batch kernels: 4-bit indices into a 16-entry int8 codebook, a 6-bit scale
+ * per 32 weights).
+ *   W        : IQ4_XS bytes [N][K/256][136] (public GGUF block: fp16 d,
+ *              uint16 scales_h, 4 bytes scales_l, 128 index bytes), device,
+ *              read-only; only the base pointer must be 16-byte aligned.
+ *              Sub-block j's scale is ls = (4 bits of scales_l at bit 4j) |
+ *              (2 bits of scales_h at bit 2j) << 4; weight i of sub-block j
+ *              is index byte 16j + i%16, low nibble for i < 16, else high;
+ *              w = d * (ls - 32) * codebook[index].
+ *   codebook : HOST pointer to the format's 16 int8 values in index order,
+ *              read during the call (the launch carries a copy).
+ * K must be a multiple of 512 (rows of 16-byte multiples for the tensor
+ * map; other K return XQ_ERR_SHAPE). M <= 8 runs the tensor-core GEMV;
+ * M > 8 returns XQ_ERR_UNSUPPORTED. xq_layer_mixed and the batch-invariant
+ * entry points take no codebook and return XQ_ERR_UNSUPPORTED for IQ4_XS. */
+XQ_API xq_status xq_matmul_iq4xs_q8(const void *W, const int8_t *codebook, const void *xq, int M, int N,
+                             int K, float *y, xq_stream stream);
 
 /* Batch-invariant mode (speculative-decoding verification: the rows of y for
  * a batch of M tokens must equal those of decoding each token alone).
@@ -266,6 +287,10 @@ XQ_API xq_status xq_debug_isums_q6k(const void *W, const void *xq, int M, int N,
 /* Q8_0: isum int32 [M][N][K/32], block j at index j. */
 XQ_API xq_status xq_debug_isums_q8_0(const void *W, const void *xq, int M, int N, int K,
                               float *y, int32_t *isum, xq_stream stream);
+/* IQ4_XS: isum int32 [M][N][K/32] (sums of codebook value x Q8 quant),
+ * sub-block j of super-block b at 8b+j. */
+XQ_API xq_status xq_debug_isums_iq4xs(const void *W, const int8_t *codebook, const void *xq, int M,
+                               int N, int K, float *y, int32_t *isum, xq_stream stream);
 
 #ifdef __cplusplus
 }

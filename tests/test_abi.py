@@ -157,3 +157,21 @@ def test_ffn_entry_points_reject_before_launch(L):
     assert L.xq_silu_mul_quantize_q8(P(FAKE), P(FAKE), 2, 300, P(FAKE), None, None) == 2
     assert L.xq_silu_mul_quantize_q8(P(FAKE + 4), P(FAKE), 2, 256, P(FAKE), None, None) == 3
     assert L.xq_silu_mul_quantize_q8(None, P(FAKE), 2, 256, P(FAKE), None, None) == 1
+
+
+def test_iq4xs_entry_points_reject_before_launch(L):
+    from gguf_quant_integer_gb300 import xq
+    P = ctypes.c_void_p
+    cb = (ctypes.c_int8 * 16)(*range(-8, 8))
+    assert xq.weight_bytes(23, 10, 1024) == 10 * 4 * 136
+    assert L.xq_matmul_iq4xs_q8(P(FAKE), cb, P(FAKE), 2, 16, 768, P(FAKE), None) == 2   # K % 512
+    assert L.xq_matmul_iq4xs_q8(P(FAKE), cb, P(FAKE), 9, 16, 1024, P(FAKE), None) == 6  # M > 8
+    assert L.xq_matmul_iq4xs_q8(P(FAKE), None, P(FAKE), 2, 16, 1024, P(FAKE), None) == 1
+    assert L.xq_matmul_iq4xs_q8(P(FAKE + 8), cb, P(FAKE), 2, 16, 1024, P(FAKE), None) == 3
+    assert L.xq_matmul_iq4xs_q8(None, None, None, 0, 16, 1024, None, None) == 0         # empty
+    assert L.xq_debug_isums_iq4xs(P(FAKE), cb, P(FAKE), 2, 16, 1024, P(FAKE), None, None) == 1
+    # no codebook travels with xq_proj or the batch-invariant matmul
+    arr = xq._proj_array([(23, 16, 1024, None, None, 0)])
+    ins = (ctypes.c_void_p * 1)(FAKE)
+    assert L.xq_layer_mixed(arr, 1, ins, 1, 4, P(FAKE), 1 << 20, None) == 6
+    assert L.xq_matmul_invariant(23, P(FAKE), P(FAKE), 2, 16, 1024, P(FAKE), None) == 6

@@ -530,3 +530,63 @@ def test_ffn_layer_down_fed_by_silu_gate_up(xq, M):
     rq, rd, _ = oracle.quantize_q8(h_gpu)
     y_ref, ab, _ = oracle.matmul(wl.projs[di].qtype, weights[di], rq, rd, wl.projs[di].K)
     check_y(ys[di].cpu().numpy(), y_ref, ab)
+
+
+# ------------------------------------------------------------ IQ4_XS
+
+def check_iq4xs(xq, W, x, codebook):
+    """xq_matmul_iq4xs_q8 and its isum hook against the oracle (M <= 8)."""
+    M, K = x.shape
+    N = W.shape[0]
+    buf, rq, rd = assert_q8_exact(xq, x)
+    y_ref, ab, isum_ref = oracle.matmul(synth.IQ4_XS, W, rq, rd, K, want_isum=True, codebook=codebook)
+    Wd = dev(W.reshape(-1))
+    y = poisoned(M, N)
+    isum = torch.full((M, N, K // 32), -(2 ** 31), dtype=torch.int32, device="cuda")
+    xq.debug_isums_iq4xs(Wd, codebook, buf, M, N, K, y=y, isum=isum)
+    torch.cuda.synchronize()
+    assert np.array_equal(isum.cpu().numpy(), isum_ref)
+    y_isum = y.cpu().numpy()
+    y = poisoned(M, N)
+    xq.matmul_iq4xs_q8(Wd, codebook, buf, M, N, K, y=y)
+    torch.cuda.synchronize()
+    assert np.array_equal(y.cpu().numpy().view(np.uint32), y_isum.view(np.uint32))
+    return check_y(y.cpu().numpy(), y_ref, ab)
+
+
+IQ4XS_SHAPES = [(1, 512), (5, 1024), (37, 1536), (130, 5120), (64, 4096)]
+
+
+@pytest.mark.parametrize("N,K", IQ4XS_SHAPES)
+def test_iq4xs_shapes_all_m(xq, N, K):
+    # IQ4_XS on the tensor-core GEMV: exact codebook-value sums and y for M = 1..8,
+    # a different synthetic codebook per M
+    errs = []
+    for M in range(1, 9):
+        cb = synth.gen_codebook(100 * M + N)
+        W = synth.gen_iq4xs(43 * N + K + M, N, K)
+        errs.append(check_iq4xs(xq, W, synth.gen_x(13 * M + N, M, K), cb))
+    assert max(errs) > 0.0
+
+
+def test_iq4xs_extremes(xq):
+    # codebook ends (-128, 127) on every index, scales 0 and 63, large d,
+    # against +-1000 activations
+    N, K, M = 64, 1024, 8
+    W = synth.gen_iq4xs(7, N, K).reshape(N, K // 256, 136)
+    W[:, :, 0:2] = np.frombuffer(np.float16(0.5).tobytes(), np.uint8)
+    W[: N // 2, :, 2:8] = 0x00                # ls = 0 -> -32
+    W[N // 2:, :, 2:8] = 0xFF                 # ls = 63 -> 31
+    cb = np.array([-128, 127] * 8, dtype=np.int8)
+    x = synth.gen_x(8, M, K)
+    x[0] = 1000.0
+    x[1, ::2] = -1000.0
+    check_iq4xs(xq, W.reshape(N, -1), x, cb)
+
+
+def test_iq4xs_rows_of_a_ragged_tail(xq):
+    # N not a multiple of 16, one super-block pair, a codebook with zero in it
+    cb = synth.gen_codebook(4)
+    cb[7] = 0
+    W = synth.gen_iq4xs(9, 19, 512)
+    assert check_iq4xs(xq, W, synth.gen_x(10, 3, 512), cb) > 0.0
