@@ -38,8 +38,8 @@ xq_status run_matmul(int type, const void* W, const void* xq, int M, int N, int 
   const xq::Q8Layout L = xq::q8_layout(M, K, invariant);
   const uint8_t* base = static_cast<const uint8_t*>(xq);
   if (M > kMaxGemvM && !invariant) {
-    if (type == XQ_TYPE_Q8_0) return XQ_ERR_UNSUPPORTED;  // the tile kernel takes Q4_K and Q6_K
-    const cudaError_t e = xq::launch_tile_mma(type, static_cast<const uint8_t*>(W), base, M, N, K, y, s, true);
+    if (type == XQ_TYPE_Q8_0) return XQ_ERR_UNSUPPORTED;  // the tile kernel takes Q4_K, Q6_K and IQ4_XS
+    const cudaError_t e = xq::launch_tile_mma(type, static_cast<const uint8_t*>(W), base, M, N, K, y, s, true, codebook);
     return e == cudaSuccess ? XQ_OK : XQ_ERR_CUDA;
   }
   if (xq::gemv_mma_supports(type, K)) {
@@ -361,8 +361,9 @@ xq_status xq_debug_isums_q8_0(const void* W, const void* xq, int M, int N, int K
   return matmul_entry(XQ_TYPE_Q8_0, W, xq, M, N, K, y, isum, stream);
 }
 
-// IQ4_XS: M <= 8 on the tensor-core GEMV, rows that are 16-byte multiples
-// (K a multiple of 512); the codebook is read from the host during the call.
+// IQ4_XS: M <= 8 on the tensor-core GEMV, M > 8 on the tile kernel; rows
+// that are 16-byte multiples (K a multiple of 512); the codebook is read
+// from the host during the call.
 static xq_status iq4xs_entry(const void* W, const int8_t* codebook, const void* xq, int M, int N, int K, float* y,
                              int32_t* isum, xq_stream stream) {
   xq_status st = check_shape(M, N, K);
@@ -371,7 +372,7 @@ static xq_status iq4xs_entry(const void* W, const int8_t* codebook, const void* 
   if (M == 0 || N == 0) return XQ_OK;
   if (!W || !xq || !y || !codebook) return XQ_ERR_ARG;
   if (!aligned16(W) || !aligned16(xq) || !aligned16(y) || (isum && !aligned16(isum))) return XQ_ERR_ALIGN;
-  if (M > kMaxGemvM) return XQ_ERR_UNSUPPORTED;
+  if (isum && M > kMaxGemvM) return XQ_ERR_UNSUPPORTED;
   uint32_t cb[4];
   for (int i = 0; i < 4; ++i)
     cb[i] = static_cast<uint32_t>(static_cast<uint8_t>(codebook[4 * i])) |

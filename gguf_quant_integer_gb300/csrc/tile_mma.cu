@@ -84,6 +84,12 @@ struct Fmt<14> {
   static constexpr int kItems = 8;
   static constexpr int kWBytes = 2 * kOpBytes;  // high and low operands
 };
+template <>
+struct Fmt<23> {
+  static constexpr int kRawRow = 144, kRawStages = 3;  // the 136-byte super-block's 16-byte-aligned window
+  static constexpr int kItems = 8;
+  static constexpr int kWBytes = 2 * kOpBytes;  // high and low operands
+};
 
 template <int TYPE>
 struct Smem {
@@ -117,6 +123,7 @@ struct TileArgs {
   float* y;                    // [M][N]
   unsigned long long w_bytes;  // N * row_bytes
   int N, K, M, nsb, row_bytes, ttiles;
+  uint32_t cb[4];              // IQ4_XS: codebook bytes with their sign bits flipped
 };
 
 // Waits of the producer, unpack and epilogue warps suspend between polls;
@@ -160,6 +167,17 @@ __device__ __forceinline__ void load_words(const uint8_t* p, uint32_t (&out)[NW]
 __device__ __forceinline__ uint32_t half2_of(float v) {
   const uint32_t h = __half_as_ushort(__float2half_rn(v));
   return h | (h << 16);
+}
+
+// IQ4_XS: the codebook bytes (sign bits flipped) of four 4-bit indices, one
+// per byte of x. The indices' low 3 bits, compacted into permute selectors,
+// pick from each codebook half; a sign-replicating permute of x << 4 turns
+// index bit 3 into a byte mask that chooses between the halves.
+__device__ __forceinline__ uint32_t iq4_codes(uint32_t x, const uint32_t (&cb)[4]) {
+  const uint32_t sel = prmt(x | (x >> 4), 0u, 0x4420u) & 0x7777u;
+  const uint32_t lo = prmt(cb[0], cb[1], sel), hi = prmt(cb[2], cb[3], sel);
+  const uint32_t m = prmt(x << 4, 0u, 0xBA98u);
+  return (hi & m) | (lo & ~m);
 }
 
 // Store one row's 32 k-slots (16 words: word c holds slots 2c, 2c+1) into a
@@ -240,10 +258,11 @@ __global__ void __launch_bounds__(kThreads, 1) tile_mma_kernel(const __grid_cons
       const int rs = b % RS;
       if (b >= RS && !warp_wait(BAR(B::kRawEmpty + rs), ((b / RS) - 1) & 1, 1)) break;
       const uint32_t dst = smem_addr(raw_ring + rs * kRawBytes);
-      if (TYPE == 12) {
+      if (TYPE == 12 || TYPE == 23) {
         if (lane == 0) {
           mbar_expect_tx(BAR(B::kRawFull + rs), kRawBytes);  // rows past N arrive zero-filled
-          tma_load_2d(dst, &A.map, b * (kQ4kBytes / 8), row0, BAR(B::kRawFull + rs));
+          tma_load_2d(dst, &A.map, TYPE == 12 ? b * (kQ4kBytes / 8) : (kIq4xsBytes * b) & ~15, row0,
+                      BAR(B::kRawFull + rs));
         }
       } else {
         unsigned mine = 0;
@@ -347,6 +366,71 @@ __global__ void __launch_bounds__(kThreads, 1) tile_mma_kernel(const __grid_cons
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) mbar_arrive(BAR(B::kWFull + ws));
+        }
+      } else if (TYPE == 23) {
+        // IQ4_XS: d at 0, scales_h at 2, scales_l[4] at 4, 128 index bytes
+        // at 8, starting off = 136b mod 16 (0 or 8) bytes into the window.
+        // Sub-block j's weight is codebook[index] * s_j, s_j = ls_j - 32 in
+        // [-32, 31]; |value * s| reaches 4096, so as for Q6_K the operand is
+        // split into 2*(s>>1)*value (even, exact) and (s&1)*value when some
+        // row of the tile has |s| > 16, and the tile then reads both.
+        const uint8_t* sb = raw + ((kIq4xsBytes * b) & 15);
+        const uint2 h = *reinterpret_cast<const uint2*>(sb);  // d | scales_h, scales_l (zero past N)
+        coef_ring[cs * kRows + r] = make_float2(half_bits_to_float(h.x), 0.0f);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(BAR(B::kCoefFull + cs));
+        int sj[8];
+        bool big = false;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          sj[j] = static_cast<int>(((h.y >> (4 * j)) & 15u) | (((h.x >> (16 + 2 * j)) & 3u) << 4)) - 32;
+          big = big || (row_ok && (sj[j] > 16 || sj[j] < -16));
+        }
+        const bool any = __any_sync(0xffffffffu, big);
+        int* vote = split_vote + 4 * (b & 1);
+        if (lane == 0) {
+          vote[warp] = any ? 1 : 0;
+          mbar_arrive(BAR(B::kVote + (b & 1)));
+        }
+        if (!warp_wait(BAR(B::kVote + (b & 1)), (b >> 1) & 1, 15)) break;
+        const bool split = (vote[0] | vote[1] | vote[2] | vote[3]) != 0;
+        const uint32_t cb[4] = {A.cb[0], A.cb[1], A.cb[2], A.cb[3]};
+#pragma unroll
+        for (int it = 0; it < 8; ++it, ++wf) {
+          const int ws = wf % kWStages;
+          if (wf >= kWStages && !warp_wait(BAR(B::kWEmpty + ws), ((wf / kWStages) - 1) & 1, 5)) {
+            ok = false;
+            break;
+          }
+          const int s = sj[it];
+          const bool wide = s > 16 || s < -16;
+          const uint32_t Shi = half2_of(static_cast<float>(wide ? 2 * (s >> 1) : s));
+          const uint32_t Slo = half2_of(static_cast<float>(wide ? (s & 1) : 0));
+          // 16 index bytes, 8-byte aligned only (the window offset is 0 or 8)
+          const uint2 qa = *reinterpret_cast<const uint2*>(sb + 8 + 16 * it);
+          const uint2 qc = *reinterpret_cast<const uint2*>(sb + 16 + 16 * it);
+          const uint32_t qw[4] = {qa.x, qa.y, qc.x, qc.y};
+          uint32_t v[16], u[16];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            // weights 4i..4i+3: low nibbles of bytes 4i.. for i < 4, high nibbles of bytes 4(i-4).. after
+            const uint32_t x = iq4_codes((i < 4 ? qw[i] : (qw[i - 4] >> 4)) & 0x0F0F0F0Fu, cb);
+            const uint32_t x0 = hsub2(prmt(x, 0x64646464u, 0x4240u), 0x64806480u);  // weights 4i, 4i+2
+            const uint32_t x1 = hsub2(prmt(x, 0x64646464u, 0x4341u), 0x64806480u);  // weights 4i+1, 4i+3
+            v[2 * i] = row_ok ? hmul2(x0, Shi) : 0u;
+            v[2 * i + 1] = row_ok ? hmul2(x1, Shi) : 0u;
+            u[2 * i] = row_ok ? hmul2(x0, Slo) : 0u;
+            u[2 * i + 1] = row_ok ? hmul2(x1, Slo) : 0u;
+          }
+          uint8_t* op = w_ring + ws * F::kWBytes;
+          store_row(op, r, v);
+          if (split) store_row(op + kOpBytes, r, u);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            if (warp == 0) split_flag[ws] = split ? 1 : 0;
+            mbar_arrive(BAR(B::kWFull + ws));
+          }
         }
       } else {
         // Q6_K: ql[128] at 0, qh[64] at 128, scales int8[16] at 192, d at
@@ -464,7 +548,7 @@ __global__ void __launch_bounds__(kThreads, 1) tile_mma_kernel(const __grid_cons
         const uint32_t id = (TYPE == 12 && it == 8) ? kIdB : kIdH;
         mma_f16_ss(dt, a0, smem_desc(bs, 128, 512), id, false);
         mma_f16_ss(dt, a1, smem_desc(bs + 256, 128, 512), id, true);
-        if (TYPE == 14 && split_flag[ws]) {
+        if (TYPE != 12 && split_flag[ws]) {
           mma_f16_ss(dt, a0, smem_desc(bs + kOpBytes, 128, 512), id, true);
           mma_f16_ss(dt, a1, smem_desc(bs + kOpBytes + 256, 128, 512), id, true);
         }
@@ -623,8 +707,10 @@ cudaError_t launch_tile(const TileArgs& A, int grid, cudaStream_t s, bool pdl) {
 }  // namespace
 
 cudaError_t launch_tile_mma(int type, const uint8_t* W, const uint8_t* xq, int M, int N, int K, float* y,
-                            cudaStream_t s, bool pdl) {
-  if (M <= 8 || N <= 0 || K <= 0 || (K & 255) != 0 || (type != 12 && type != 14)) return cudaErrorInvalidValue;
+                            cudaStream_t s, bool pdl, const uint32_t* codebook) {
+  if (M <= 8 || N <= 0 || K <= 0 || (K & 255) != 0 || (type != 12 && type != 14 && type != 23))
+    return cudaErrorInvalidValue;
+  if (type == 23 && (!codebook || (K & 511) != 0)) return cudaErrorInvalidValue;
   const Q8Layout L = q8_layout(M, K);
   TileArgs A = {};
   A.W = W;
@@ -634,7 +720,8 @@ cudaError_t launch_tile_mma(int type, const uint8_t* W, const uint8_t* xq, int M
   A.K = K;
   A.M = M;
   A.nsb = K >> 8;
-  A.row_bytes = A.nsb * (type == 12 ? kQ4kBytes : kQ6kBytes);
+  A.row_bytes = A.nsb * (type == 12 ? kQ4kBytes : (type == 23 ? kIq4xsBytes : kQ6kBytes));
+  for (int i = 0; i < 4; ++i) A.cb[i] = codebook ? (codebook[i] ^ 0x80808080u) : 0u;
   A.w_bytes = static_cast<unsigned long long>(N) * A.row_bytes;
   A.ttiles = L.ttiles;
   const int grid = ((N + kRows - 1) / kRows) * L.ttiles;
@@ -643,6 +730,12 @@ cudaError_t launch_tile_mma(int type, const uint8_t* W, const uint8_t* xq, int M
                        A.row_bytes, kQ4kBytes / 8, kRows))
       return cudaErrorInvalidValue;
     return launch_tile<12>(A, grid, s, pdl);
+  }
+  if (type == 23) {
+    if (!encode_tma_2d(&A.map, CU_TENSOR_MAP_DATA_TYPE_UINT8, W, A.row_bytes, static_cast<unsigned long long>(N),
+                       A.row_bytes, Fmt<23>::kRawRow, kRows))
+      return cudaErrorInvalidValue;
+    return launch_tile<23>(A, grid, s, pdl);
   }
   return launch_tile<14>(A, grid, s, pdl);
 }

@@ -163,9 +163,10 @@ XQ_API xq_status xq_matmul_q8_0_q8(const void *W, const void *xq, int M, int N, 
  *   codebook : HOST pointer to the format's 16 int8 values in index order,
  *              read during the call (the launch carries a copy).
  * K must be a multiple of 512 (rows of 16-byte multiples for the tensor
- * map; other K return XQ_ERR_SHAPE). M <= 8 runs the tensor-core GEMV;
- * M > 8 returns XQ_ERR_UNSUPPORTED. xq_layer_mixed and the batch-invariant
- * entry points take no codebook and return XQ_ERR_UNSUPPORTED for IQ4_XS. */
+ * map; other K return XQ_ERR_SHAPE). M <= 8 runs the tensor-core GEMV,
+ * M > 8 the tile kernel (the codebook lookup done once per weight tile and
+ * reused by its 128 tokens). xq_layer_mixed and the batch-invariant entry
+ * points take no codebook and return XQ_ERR_UNSUPPORTED for IQ4_XS. */
 XQ_API xq_status xq_matmul_iq4xs_q8(const void *W, const int8_t *codebook, const void *xq, int M, int N,
                              int K, float *y, xq_stream stream);
 

@@ -165,7 +165,7 @@ def test_iq4xs_entry_points_reject_before_launch(L):
     cb = (ctypes.c_int8 * 16)(*range(-8, 8))
     assert xq.weight_bytes(23, 10, 1024) == 10 * 4 * 136
     assert L.xq_matmul_iq4xs_q8(P(FAKE), cb, P(FAKE), 2, 16, 768, P(FAKE), None) == 2   # K % 512
-    assert L.xq_matmul_iq4xs_q8(P(FAKE), cb, P(FAKE), 9, 16, 1024, P(FAKE), None) == 6  # M > 8
+    assert L.xq_debug_isums_iq4xs(P(FAKE), cb, P(FAKE), 9, 16, 1024, P(FAKE), P(FAKE), None) == 6  # hook: M <= 8
     assert L.xq_matmul_iq4xs_q8(P(FAKE), None, P(FAKE), 2, 16, 1024, P(FAKE), None) == 1
     assert L.xq_matmul_iq4xs_q8(P(FAKE + 8), cb, P(FAKE), 2, 16, 1024, P(FAKE), None) == 3
     assert L.xq_matmul_iq4xs_q8(None, None, None, 0, 16, 1024, None, None) == 0         # empty

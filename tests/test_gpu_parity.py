@@ -590,3 +590,43 @@ def test_iq4xs_rows_of_a_ragged_tail(xq):
     cb[7] = 0
     W = synth.gen_iq4xs(9, 19, 512)
     assert check_iq4xs(xq, W, synth.gen_x(10, 3, 512), cb) > 0.0
+
+
+def check_iq4xs_tile(xq, W, x, codebook, rows=None):
+    """M > 8: xq_matmul_iq4xs_q8 on the tile kernel against the oracle (all
+    rows, or `rows` sampled rows)."""
+    M, K = x.shape
+    N = W.shape[0]
+    buf, rq, rd = assert_q8_exact(xq, x)
+    sel = np.arange(N) if rows is None else np.sort(np.random.default_rng(N + M).choice(N, rows, replace=False))
+    y_ref, ab, _ = oracle.matmul(synth.IQ4_XS, W[sel], rq, rd, K, codebook=codebook)
+    y = poisoned(M, N)
+    xq.matmul_iq4xs_q8(dev(W.reshape(-1)), codebook, buf, M, N, K, y=y)
+    torch.cuda.synchronize()
+    return check_y(y.cpu().numpy()[:, sel], y_ref, ab)
+
+
+@pytest.mark.parametrize("N,K,M", [(130, 1024, 9), (64, 4096, 40), (17, 512, 200), (300, 5120, 130)])
+def test_iq4xs_tile_shapes(xq, N, K, M):
+    cb = synth.gen_codebook(N + M)
+    W = synth.gen_iq4xs(57 * N + K, N, K)
+    assert check_iq4xs_tile(xq, W, synth.gen_x(3 * M + N, M, K), cb, rows=None if N * M <= 20000 else 96) > 0.0
+
+
+def test_iq4xs_tile_scale_forms(xq):
+    # |s| <= 16 everywhere (one operand per tile) and the extremes s = -32, 31
+    # (the two-operand form), with the codebook ends on every index
+    N, K, M = 256, 1024, 24
+    cb = np.array([-128, 127] * 8, dtype=np.int8)
+    x = synth.gen_x(5, M, K)
+    x[0] = 1000.0
+    W = synth.gen_iq4xs(6, N, K).reshape(N, K // 256, 136)
+    W[:, :, 0:2] = np.frombuffer(np.float16(0.5).tobytes(), np.uint8)
+    narrow = W.copy()
+    narrow[:, :, 2:4] = 0x55                     # scales_h bits 01 -> ls in 16..31
+    narrow[:, :, 4:8] = 0x00                     # ls = 16 -> s = -16
+    check_iq4xs_tile(xq, narrow.reshape(N, -1), x, cb)
+    wide = W.copy()
+    wide[: N // 2, :, 2:8] = 0x00                # s = -32
+    wide[N // 2:, :, 2:8] = 0xFF                 # s = 31
+    check_iq4xs_tile(xq, wide.reshape(N, -1), x, cb)
