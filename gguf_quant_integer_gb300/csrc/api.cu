@@ -27,17 +27,18 @@ xq_status check_shape(int M, int N, int K) {
   return XQ_OK;
 }
 
-// Enqueue y = x W^T. M > 8: the tensor-memory tile kernel (both types).
-// M <= 8: the warp-level MMA GEMV (8-token chunks, up to kMaxProj chunks per
-// launch) for Q4_K and for Q6_K rows that are 16-byte multiples; the dp4a
-// GEMV for the other Q6_K shapes. invariant: every M in 8-token GEMV chunks
-// from the GEMV-image layout, never split over K, so that each token's row
-// of y is computed by the same operations whatever M is.
+// Enqueue y = x W^T. M > 64 (the buffer holds the tile image): the
+// tensor-memory tile kernel. M <= 64: the warp-level MMA GEMV in 8-token
+// chunks (up to kMaxProj chunks per launch, which share each weight tile
+// through L2) for Q4_K, Q8_0, IQ4_XS and Q6_K rows that are 16-byte
+// multiples; the dp4a GEMV for the other Q6_K shapes. invariant: every M in
+// 8-token GEMV chunks from the GEMV-image layout, never split over K, so
+// that each token's row of y is computed by the same operations whatever M.
 xq_status run_matmul(int type, const void* W, const void* xq, int M, int N, int K, float* y,
                      int32_t* isum, cudaStream_t s, bool invariant = false, const uint32_t* codebook = nullptr) {
   const xq::Q8Layout L = xq::q8_layout(M, K, invariant);
   const uint8_t* base = static_cast<const uint8_t*>(xq);
-  if (M > kMaxGemvM && !invariant) {
+  if (L.ttiles > 0) {
     if (type == XQ_TYPE_Q8_0) return XQ_ERR_UNSUPPORTED;  // the tile kernel takes Q4_K, Q6_K and IQ4_XS
     const cudaError_t e = xq::launch_tile_mma(type, static_cast<const uint8_t*>(W), base, M, N, K, y, s, true, codebook);
     return e == cudaSuccess ? XQ_OK : XQ_ERR_CUDA;
@@ -174,7 +175,7 @@ xq_status layer_inputs(const xq_proj* proj, int n_proj, int n_inputs, int M, int
     if (q.input < 0 || q.input >= n_inputs) return XQ_ERR_ARG;
     const xq_status st = check_shape(M, q.N, q.K);
     if (st != XQ_OK) return st;
-    if (q.type == XQ_TYPE_Q8_0 && M > kMaxGemvM) return XQ_ERR_UNSUPPORTED;
+    if (q.type == XQ_TYPE_Q8_0 && M > xq::kGemvMaxTokens) return XQ_ERR_UNSUPPORTED;
     if (in_k[q.input] == 0) in_k[q.input] = q.K;
     if (in_k[q.input] != q.K) return XQ_ERR_SHAPE;
   }
@@ -185,8 +186,9 @@ xq_status layer_inputs(const xq_proj* proj, int n_proj, int n_inputs, int M, int
 // is projection p's Q8 buffer, sched the scheduling state sc describes
 // (zeroed by the kernel before). M <= 8: one grouped tensor-core GEMV launch
 // per weight type (kMaxProj items per launch), then the dp4a GEMV for the
-// Q6_K rows that are not 16-byte multiples; M > 8: the tile kernel per
-// projection, in the order given.
+// Q6_K rows that are not 16-byte multiples; M > 8: each projection on its
+// own (GEMV chunks up to 64 tokens, the tile kernel above), in the order
+// given.
 xq_status layer_matmuls(const xq_proj* proj, int n_proj, const uint8_t* const* q8, int M, const Sched& sc,
                         uint8_t* sched, cudaStream_t s) {
   if (M > kMaxGemvM) {
@@ -284,7 +286,7 @@ const char* xq_status_str(xq_status s) {
 
 size_t xq_q8_bytes(int M, int K) {
   if (M < 0 || K <= 0 || (K % 32) != 0) return 0;
-  if (M > kMaxGemvM && (K % 256) != 0) return 0;  // the tile image is per super-block
+  if (M > xq::kGemvMaxTokens && (K % 256) != 0) return 0;  // the tile image is per super-block
   return xq::q8_layout(M, K).total;
 }
 
@@ -361,7 +363,7 @@ xq_status xq_debug_isums_q8_0(const void* W, const void* xq, int M, int N, int K
   return matmul_entry(XQ_TYPE_Q8_0, W, xq, M, N, K, y, isum, stream);
 }
 
-// IQ4_XS: M <= 8 on the tensor-core GEMV, M > 8 on the tile kernel; rows
+// IQ4_XS: M <= 64 on the tensor-core GEMV, M > 64 on the tile kernel; rows
 // that are 16-byte multiples (K a multiple of 512); the codebook is read
 // from the host during the call.
 static xq_status iq4xs_entry(const void* W, const int8_t* codebook, const void* xq, int M, int N, int K, float* y,

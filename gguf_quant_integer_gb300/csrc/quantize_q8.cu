@@ -15,8 +15,8 @@
 // performs the same steps.
 //
 // The same pass writes the tensor-core operand image of the quants, so that
-// the matmuls never convert activations themselves: for M <= 8 fp16 copies
-// in m16n8k16 B-fragment order plus per-32-block scale quads; for M > 8 the
+// the matmuls never convert activations themselves: for M <= 64 fp16 copies
+// in m16n8k16 B-fragment order plus per-32-block scale quads; for M > 64 the
 // 128-token tiles of the tcgen05 B operand, their d8 rows and the three-piece
 // bf16 split of s8 (layouts in xq_common.cuh). One launch serves all inputs
 // of a layer.
@@ -191,7 +191,7 @@ cudaError_t launch_quantize_q8(const QuantJob* jobs, int n, cudaStream_t s, bool
     it.nsub = q.K / 32;
     it.ttiles = L.ttiles;
     // padded token count: the operand image's chunk (8) or tile (128)
-    const long long mp = (q.M > 8 && !q.gemv_image) ? 128LL * ((q.M + 127) / 128) : 8LL * ((q.M + 7) / 8);
+    const long long mp = (q.M > kGemvMaxTokens && !q.gemv_image) ? 128LL * ((q.M + 127) / 128) : 8LL * ((q.M + 7) / 8);
     nblocks += mp * (q.K / 32);
     if (nblocks >= (1LL << 31)) return cudaErrorInvalidValue;
     G.blk0[k + 1] = static_cast<unsigned>(nblocks);

@@ -708,7 +708,7 @@ cudaError_t launch_tile(const TileArgs& A, int grid, cudaStream_t s, bool pdl) {
 
 cudaError_t launch_tile_mma(int type, const uint8_t* W, const uint8_t* xq, int M, int N, int K, float* y,
                             cudaStream_t s, bool pdl, const uint32_t* codebook) {
-  if (M <= 8 || N <= 0 || K <= 0 || (K & 255) != 0 || (type != 12 && type != 14 && type != 23))
+  if (M <= kGemvMaxTokens || N <= 0 || K <= 0 || (K & 255) != 0 || (type != 12 && type != 14 && type != 23))
     return cudaErrorInvalidValue;
   if (type == 23 && (!codebook || (K & 511) != 0)) return cudaErrorInvalidValue;
   const Q8Layout L = q8_layout(M, K);

@@ -76,7 +76,7 @@ __device__ __forceinline__ float half_bits_to_float(unsigned bits16) {
 // followed, at F = round_up(1.25*M*K, 256), by the tensor-core operand image
 // of the matmul path that serves this M.
 //
-// M <= 8 (warp-level MMA GEMV):
+// M <= kGemvMaxTokens (warp-level MMA GEMV, 8-token chunks):
 //   frag fp16 [C][K/32][32][8]            at F
 //   fsc  fp32 [C][K/32][4][4]             at F + C*16*K
 // with C = ceil(M/8) chunks of 8 tokens, laid out as the B operand of an
@@ -85,7 +85,7 @@ __device__ __forceinline__ float half_bits_to_float(unsigned bits16) {
 // perm = 0,2,1,3,4,6,5,7; fsc[c][j][t] = (d8[8c+2t][j], d8[8c+2t+1][j],
 // s8[8c+2t][j], s8[8c+2t+1][j]). Tokens past M in the last chunk are zero.
 //
-// M > 8 (tensor-memory tile kernel), T = ceil(M/128) token tiles:
+// M > kGemvMaxTokens (tensor-memory tile kernel), T = ceil(M/128) token tiles:
 //   tile [T][K/256] records of kTileRecord bytes at F. Record (t, b) holds,
 //   for the 128 tokens 128t .. 128t+127 and super-block b:
 //     8 items, one per 32-block j = 8b + i (kTileItem bytes each):
@@ -106,12 +106,20 @@ constexpr int kTileRecord = 8 * kTileItem + kTileItemOp;  // 77824
 
 struct Q8Layout {
   size_t qs, d8, s8, frag, fsc, tile, total;
-  int chunks;  // 8-token chunks of the GEMV image (M <= 8), else 0
-  int ttiles;  // 128-token tiles of the tile image (M > 8), else 0
+  int chunks;  // 8-token chunks of the GEMV image (M <= kGemvMaxTokens), else 0
+  int ttiles;  // 128-token tiles of the tile image (M > kGemvMaxTokens), else 0
 };
 
-// gemv_image: the M <= 8 layout (8-token chunks of the GEMV image) for any M;
-// the batch-invariant entry points use it.
+// Up to this many tokens a matmul runs the GEMV over 8-token chunks (up to 8
+// chunks in one launch, which then read each weight tile from HBM about once),
+// above it the tile kernel. Measured on GB300 (weights past L2): a Q4_K
+// 12288 x 4096 matmul takes 18 us at M = 9..16, 34 us at 32 and 65 us at 64
+// as GEMV chunks against 80 us on the tile kernel at any M <= 128; a Q6_K
+// 4096 x 12288 one 45 / 82 / 118 us against 323 us.
+constexpr int kGemvMaxTokens = 64;
+
+// gemv_image: the GEMV layout (8-token chunks) for any M; the batch-invariant
+// entry points use it.
 __host__ __device__ inline Q8Layout q8_layout(int M, int K, bool gemv_image = false) {
   Q8Layout L;
   const size_t mk = static_cast<size_t>(M) * K;
@@ -119,7 +127,7 @@ __host__ __device__ inline Q8Layout q8_layout(int M, int K, bool gemv_image = fa
   L.d8 = mk;
   L.s8 = mk + 4 * (mk / 32);
   const size_t F = (mk + 8 * (mk / 32) + 255) & ~static_cast<size_t>(255);
-  if (M <= 8 || gemv_image) {
+  if (M <= kGemvMaxTokens || gemv_image) {
     L.chunks = (M + 7) / 8;
     L.ttiles = 0;
     L.frag = F;

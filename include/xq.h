@@ -39,12 +39,12 @@
  *          matmul that serves this M. d8 = amax/127 of the 32-block,
  *          q = round-half-away(x * (1/d8)) clamped to +-127, s8 = d8*sum(q)
  *          (q8_1 kind: scale and sum).
- *          M <= 8: frag fp16 [C][K/32][32][8] at F and fsc fp32 [C][K/32][4][4]
+ *          M <= 64: frag fp16 [C][K/32][32][8] at F and fsc fp32 [C][K/32][4][4]
  *          at F + 16*C*K, C = ceil(M/8): the same numbers in the operand
  *          order of the warp-level tensor-core GEMV (8-token chunks:
  *          frag[c][j][4n+t][s] = qs[8c+n][32j+8t+p(s)], p = 0,2,1,3,4,6,5,7;
  *          fsc[c][j][t] = d8,d8,s8,s8 of tokens 8c+2t, 8c+2t+1).
- *          M > 8: T = ceil(M/128) tiles of 128 tokens; for tile t and
+ *          M > 64: T = ceil(M/128) tiles of 128 tokens; for tile t and
  *          super-block b a record of 77,824 bytes at F + (t*K/256 + b)*77824:
  *          for each 32-block 8b+i an 8,704-byte item (fp16 q of the 128
  *          tokens as a K-major tensor-core operand, 8x8 core matrices, then
@@ -93,10 +93,10 @@ typedef enum {
 XQ_API const char *xq_status_str(xq_status s);
 
 /* Bytes of the Q8 activation buffer for M tokens of K features:
- * round_up(1.25*M*K, 256) + 18*K*ceil(M/8) for M <= 8,
- * round_up(1.25*M*K, 256) + 77824*(K/256)*ceil(M/128) for M > 8.
+ * round_up(1.25*M*K, 256) + 18*K*ceil(M/8) for M <= 64,
+ * round_up(1.25*M*K, 256) + 77824*(K/256)*ceil(M/128) for M > 64.
  * Returns 0 when M < 0, when K is not a positive multiple of 32, or when
- * M > 8 and K is not a multiple of 256. */
+ * M > 64 and K is not a multiple of 256. */
 XQ_API size_t xq_q8_bytes(int M, int K);
 
 /* Bytes of an N x K weight of GGUF type `type` (N*(K/256)*144 for Q4_K,
@@ -122,9 +122,11 @@ XQ_API xq_status xq_quantize_q8(const float *x, int M, int K, void *xq, xq_strea
  *   xq : Q8 activations from xq_quantize_q8(.., M, K, ..), device, read-only.
  *   y  : fp32 [M][N], device, overwritten.
  * Any M >= 0. Dispatch: M <= 8 runs a GEMV that streams every weight byte
- * once for all M tokens; M > 8 runs the tile kernel (128 weight rows x 128
- * tokens per CTA on the tcgen05 tensor cores, tile MMQ of section B2), whose
- * operand image xq_quantize_q8 writes for that M. */
+ * once for all M tokens; 8 < M <= 64 runs it on 8-token chunks, up to 8 in
+ * one launch (they share each weight tile through L2); M > 64 runs the tile
+ * kernel (128 weight rows x 128 tokens per CTA on the tcgen05 tensor cores,
+ * tile MMQ of section B2), whose operand image xq_quantize_q8 writes for
+ * that M. */
 XQ_API xq_status xq_matmul_q4k_q8(const void *W, const void *xq, int M, int N, int K,
                            float *y, xq_stream stream);
 
@@ -133,8 +135,8 @@ XQ_API xq_status xq_matmul_q4k_q8(const void *W, const void *xq, int M, int N, i
  *   W  : Q6_K bytes [N][K/256][210], device, read-only. Individual blocks are
  *        2-byte aligned (210 is not a multiple of 4); only the base pointer
  *        must be 16-byte aligned.
- * Dispatch at M <= 8: the tensor-core GEMV when rows are 16-byte multiples
- * (K a multiple of 2048), else a dp4a GEMV; M > 8: the tile kernel. */
+ * Dispatch at M <= 64: the tensor-core GEMV when rows are 16-byte multiples
+ * (K a multiple of 2048), else a dp4a GEMV; M > 64: the tile kernel. */
 XQ_API xq_status xq_matmul_q6k_q8(const void *W, const void *xq, int M, int N, int K,
                            float *y, xq_stream stream);
 
@@ -144,7 +146,7 @@ XQ_API xq_status xq_matmul_q6k_q8(const void *W, const void *xq, int M, int N, i
  *        quants), device, read-only. Blocks are 2-byte aligned; only the base
  *        pointer must be 16-byte aligned. K % 256 == 0 (rows of 8-block
  *        groups, 272 bytes each, are 16-byte multiples).
- * M <= 8 runs the tensor-core GEMV; M > 8 returns XQ_ERR_UNSUPPORTED (the
+ * M <= 64 runs the tensor-core GEMV; M > 64 returns XQ_ERR_UNSUPPORTED (the
  * tile kernel takes Q4_K and Q6_K): use the batch-invariant entry points,
  * which run the GEMV per 8-token chunk for any M. */
 XQ_API xq_status xq_matmul_q8_0_q8(const void *W, const void *xq, int M, int N, int K,
@@ -163,8 +165,8 @@ XQ_API xq_status xq_matmul_q8_0_q8(const void *W, const void *xq, int M, int N, 
  *   codebook : HOST pointer to the format's 16 int8 values in index order,
  *              read during the call (the launch carries a copy).
  * K must be a multiple of 512 (rows of 16-byte multiples for the tensor
- * map; other K return XQ_ERR_SHAPE). M <= 8 runs the tensor-core GEMV,
- * M > 8 the tile kernel (the codebook lookup done once per weight tile and
+ * map; other K return XQ_ERR_SHAPE). M <= 64 runs the tensor-core GEMV,
+ * M > 64 the tile kernel (the codebook lookup done once per weight tile and
  * reused by its 128 tokens). xq_layer_mixed and the batch-invariant entry
  * points take no codebook and return XQ_ERR_UNSUPPORTED for IQ4_XS. */
 XQ_API xq_status xq_matmul_iq4xs_q8(const void *W, const int8_t *codebook, const void *xq, int M, int N,
@@ -172,8 +174,8 @@ XQ_API xq_status xq_matmul_iq4xs_q8(const void *W, const int8_t *codebook, const
 
 /* Batch-invariant mode (speculative-decoding verification: the rows of y for
  * a batch of M tokens must equal those of decoding each token alone).
- * xq_matmul_q4k_q8 / _q6k_q8 are invariant for M <= 8 (every token of an
- * 8-token chunk goes through the same operations), but M > 8 switches to
+ * xq_matmul_q4k_q8 / _q6k_q8 are invariant for M <= 64 (every token of an
+ * 8-token chunk goes through the same operations), but M > 64 switches to
  * the tile kernel, whose fp32 combine runs in another order. These entry
  * points keep the M <= 8 arithmetic for every M: the activations hold the
  * 8-token GEMV image for all ceil(M/8) chunks (xq_q8_bytes_invariant bytes:
@@ -189,7 +191,7 @@ XQ_API xq_status xq_matmul_invariant(int type, const void *W, const void *xq, in
 
 /* One projection of a transformer layer for xq_layer_mixed. */
 typedef struct {
-    int type;        /* XQ_TYPE_Q4_K, XQ_TYPE_Q6_K or XQ_TYPE_Q8_0 (M <= 8) */
+    int type;        /* XQ_TYPE_Q4_K, XQ_TYPE_Q6_K or XQ_TYPE_Q8_0 (M <= 64) */
     int N, K;        /* output and input features */
     const void *W;   /* weight bytes, device */
     float *y;        /* fp32 [M][N] output, device */
@@ -242,7 +244,8 @@ XQ_API size_t xq_layer_ffn_workspace_bytes(const xq_proj *proj, int n_proj, int 
  * `stream`: the Q8 quantization of every input; the gate and up projections;
  * one xq_silu_mul_quantize_q8 launch on their outputs; every other
  * projection together with down (one grouped GEMV launch per weight type at
- * M <= 8, split over K like the layer's; the tile kernel at M > 8). The
+ * M <= 8, split over K like the layer's; per projection above, GEMV chunks
+ * up to M = 64 and the tile kernel beyond). The
  * projections that do not depend on gate and up thus share down's launch. */
 XQ_API xq_status xq_layer_mixed_ffn(const xq_proj *proj, int n_proj, int gate, int up, int down,
                              const float *const *inputs, int n_inputs, int M,

@@ -40,15 +40,16 @@ def test_sizes(L):
     from gguf_quant_integer_gb300 import xq
     def layout(M, K):
         base = -(-int(1.25 * M * K) // 256) * 256
-        if M <= 8:   # GEMV operand image: 18 bytes per feature per 8-token chunk
+        if M <= 64:  # GEMV operand image: 18 bytes per feature per 8-token chunk
             return base + 18 * K * (-(-M // 8))
         # tile image: one 77,824-byte record per 128-token tile and super-block
         return base + 77824 * (K // 256) * (-(-M // 128))
-    for M, K in ((1, 2048), (8, 4096), (9, 256), (129, 1536), (512, 12288), (0, 256)):
+    for M, K in ((1, 2048), (8, 4096), (9, 256), (64, 512), (65, 512), (129, 1536), (512, 12288), (0, 256)):
         assert xq.q8_bytes(M, K) == layout(M, K)
     assert L.xq_q8_bytes(1, 100) == 0
-    assert L.xq_q8_bytes(8, 288) > 0      # M <= 8 needs K % 32 only
-    assert L.xq_q8_bytes(9, 288) == 0     # the tile image is per 256-feature super-block
+    assert L.xq_q8_bytes(8, 288) > 0      # the GEMV image needs K % 32 only
+    assert L.xq_q8_bytes(64, 288) > 0
+    assert L.xq_q8_bytes(65, 288) == 0    # the tile image is per 256-feature super-block
     # batch-invariant layout: the GEMV image for every 8-token chunk, any M
     for M, K in ((1, 2048), (8, 4096), (9, 256), (129, 1536), (512, 12288), (0, 256)):
         base = -(-int(1.25 * M * K) // 256) * 256
@@ -124,18 +125,20 @@ def test_layer_argument_errors(L):
 
 
 def test_q8_0_entry_points_reject_before_launch(L):
-    """Q8_0 at M > 8 (the tile kernel takes Q4_K and Q6_K) and Q8_0 in a
-    layer at M > 8 are refused before anything is enqueued."""
+    """Q8_0 at M > 64 (the tile kernel takes Q4_K, Q6_K and IQ4_XS) and Q8_0
+    in a layer at M > 64 are refused before anything is enqueued."""
     from gguf_quant_integer_gb300 import xq
     P = ctypes.c_void_p
-    assert L.xq_matmul_q8_0_q8(P(FAKE), P(FAKE), 9, 16, 256, P(FAKE), None) == 6
+    assert L.xq_matmul_q8_0_q8(P(FAKE), P(FAKE), 65, 16, 256, P(FAKE), None) == 6
     assert L.xq_matmul_q8_0_q8(P(FAKE), P(FAKE), 8, 16, 300, P(FAKE), None) == 2
     assert L.xq_debug_isums_q8_0(P(FAKE), P(FAKE), 2, 16, 256, P(FAKE), None, None) == 1
+    assert L.xq_debug_isums_q8_0(P(FAKE), P(FAKE), 9, 16, 256, P(FAKE), P(FAKE), None) == 6  # hook: M <= 8
     arr = xq._proj_array([(8, 16, 512, None, None, 0)])
-    assert L.xq_layer_workspace_bytes(arr, 1, 1, 9) == 0
+    assert L.xq_layer_workspace_bytes(arr, 1, 1, 65) == 0
+    assert L.xq_layer_workspace_bytes(arr, 1, 1, 64) > 0
     assert L.xq_layer_workspace_bytes(arr, 1, 1, 8) > 0
     ins = (ctypes.c_void_p * 1)(FAKE)
-    assert L.xq_layer_mixed(arr, 1, ins, 1, 9, P(FAKE), 1 << 20, None) == 6
+    assert L.xq_layer_mixed(arr, 1, ins, 1, 65, P(FAKE), 1 << 20, None) == 6
 
 
 def test_ffn_entry_points_reject_before_launch(L):

@@ -106,7 +106,7 @@ def expected_operand_image(qs, d8, s8):
     return frag, fsc
 
 
-@pytest.mark.parametrize("M,K", [(1, 256), (3, 2048), (8, 4096)])
+@pytest.mark.parametrize("M,K", [(1, 256), (3, 2048), (8, 4096), (20, 512), (64, 256)])
 def test_quantize_operand_image(xq, M, K):
     x = synth.gen_x(300 + M, M, K)
     buf, rq, rd = assert_q8_exact(xq, x)
@@ -121,7 +121,7 @@ def test_quantize_operand_image(xq, M, K):
     assert np.array_equal(got_s.view(np.uint32), fsc.view(np.uint32))
 
 
-@pytest.mark.parametrize("M,K", [(9, 256), (13, 1536), (130, 512)])
+@pytest.mark.parametrize("M,K", [(65, 256), (100, 1536), (130, 512)])
 def test_quantize_tile_image(xq, M, K):
     x = synth.gen_x(310 + M, M, K)
     buf, rq, rd = assert_q8_exact(xq, x)
@@ -202,17 +202,19 @@ def test_shapes_all_m(xq, qtype, N, K):
     assert max(errs) > 0.0
 
 
-@pytest.mark.parametrize("qtype", [synth.Q4_K, synth.Q6_K])
-@pytest.mark.parametrize("M", [9, 13, 64])
+# 8 < M <= 64: the GEMV over 8-token chunks (several chunks per launch).
+@pytest.mark.parametrize("qtype", [synth.Q4_K, synth.Q6_K, synth.Q8_0])
+@pytest.mark.parametrize("M", [9, 13, 40, 64])
 def test_more_than_eight_tokens(xq, qtype, M):
-    run_and_check(xq, qtype, 48, 1024, M, 900 + M, 901 + M, want_isum=False)
+    run_and_check(xq, qtype, 48, 2048, M, 900 + M, 901 + M, want_isum=False)
+    run_and_check(xq, qtype, 130, 4096, M, 910 + M, 911 + M, want_isum=False)
 
 
-# M > 8: the tcgen05 tile kernel. Ragged N and M, one-super-block rows, and
+# M > 64: the tcgen05 tile kernel. Ragged N and M, one-super-block rows, and
 # Q6_K rows whose byte length is not a multiple of 16 (row windows start at
 # varying offsets; for (37, 256) and (130, 1536) the last window is cut at
 # the end of the weight buffer).
-TILE_SHAPES = [(37, 256, 20), (130, 1536, 200), (300, 4096, 129), (128, 2304, 64), (48, 1024, 9)]
+TILE_SHAPES = [(37, 256, 70), (130, 1536, 200), (300, 4096, 129), (128, 2304, 65), (48, 1024, 128)]
 
 
 @pytest.mark.parametrize("qtype", [synth.Q4_K, synth.Q6_K])
@@ -355,7 +357,12 @@ def test_q8_0_extreme_bytes(xq):
 
 
 def test_qwen3_mixed_layer_tiles(xq):
-    # M > 8: every projection of the mixed layer (Q4_K and Q6_K) on the tile kernel
+    # M > 64: every projection of the mixed layer (Q4_K and Q6_K) on the tile kernel
+    assert layer_check(xq, synth.WORKLOADS["qwen3-8b-mixed-layer"], 80, rows=96) > 0
+
+
+def test_qwen3_mixed_layer_gemv_chunks(xq):
+    # 8 < M <= 64: every projection of the mixed layer as GEMV chunks
     assert layer_check(xq, synth.WORKLOADS["qwen3-8b-mixed-layer"], 40, rows=96) > 0
 
 
@@ -606,8 +613,9 @@ def check_iq4xs_tile(xq, W, x, codebook, rows=None):
     return check_y(y.cpu().numpy()[:, sel], y_ref, ab)
 
 
+# 9 and 40 tokens run as GEMV chunks, 130 and 200 on the tile kernel
 @pytest.mark.parametrize("N,K,M", [(130, 1024, 9), (64, 4096, 40), (17, 512, 200), (300, 5120, 130)])
-def test_iq4xs_tile_shapes(xq, N, K, M):
+def test_iq4xs_more_than_eight_tokens(xq, N, K, M):
     cb = synth.gen_codebook(N + M)
     W = synth.gen_iq4xs(57 * N + K, N, K)
     assert check_iq4xs_tile(xq, W, synth.gen_x(3 * M + N, M, K), cb, rows=None if N * M <= 20000 else 96) > 0.0
@@ -616,7 +624,7 @@ def test_iq4xs_tile_shapes(xq, N, K, M):
 def test_iq4xs_tile_scale_forms(xq):
     # |s| <= 16 everywhere (one operand per tile) and the extremes s = -32, 31
     # (the two-operand form), with the codebook ends on every index
-    N, K, M = 256, 1024, 24
+    N, K, M = 256, 1024, 80
     cb = np.array([-128, 127] * 8, dtype=np.int8)
     x = synth.gen_x(5, M, K)
     x[0] = 1000.0
