@@ -683,6 +683,30 @@ def secondary_workloads(device, world):
         res[str(M)] = row
     out["llama3-8b-layer-swiglu-down"] = {"rotated_copies": copies, "layer_bytes": wl.layer_weight_bytes(),
                                           "by_m": res}
+    # batched decode: the Qwen3-8B mixed layer at 16, 32 and 64 tokens (GEMV
+    # over 8-token chunks) and 128 (the tile kernel)
+    wl = synth.WORKLOADS["qwen3-8b-mixed-layer"]
+    lw = synth.gen_layer_weights(wl, 0)
+    copies = max(3, -(-3 * L2_BYTES // wl.layer_weight_bytes()))
+    base = [torch.from_numpy(w.reshape(-1)).to(device) for w in lw]
+    reps = [base] + [[w.clone() for w in base] for _ in range(copies - 1)]
+    res = {}
+    for M in (16, 32, 64, 128):
+        ins = [torch.from_numpy(x).to(device) for x in synth.gen_layer_inputs(wl, M, 0)]
+        ys = [torch.empty((M, p.N), dtype=torch.float32, device=device) for p in wl.projs]
+        descs = [[(p.qtype, p.N, p.K, reps[c][t], ys[t], p.input) for t, p in enumerate(wl.projs)]
+                 for c in range(copies)]
+        ws = torch.empty(max(256, xq.layer_workspace_bytes(descs[0], 4, M)), dtype=torch.uint8, device=device)
+
+        def step():
+            for c in range(copies):
+                xq.layer_mixed(descs[c], ins, M, ws)
+
+        sec = max_over_ranks(time_region(step, 3, 2, world, device), world, device) / (3 * copies)
+        res[str(M)] = {"us_per_layer": round(1e6 * sec, 2), "GBps": round(wl.layer_weight_bytes() / sec / 1e9, 1),
+                       "tokens_per_s": round(M / sec, 1)}
+    out["qwen3-8b-mixed-layer-batched"] = {"rotated_copies": copies, "layer_bytes": wl.layer_weight_bytes(),
+                                           "by_m": res, "path": "GEMV over 8-token chunks up to 64 tokens, tile above"}
     # IQ4_XS: the 17408 x 5120 ffn_up shape whose batch cost the IQ4_XS
     # entries of the Agent Telemetry log measure, with a synthetic codebook;
     # quantize + matmul per copy, weights rotated past L2
@@ -705,6 +729,20 @@ def secondary_workloads(device, world):
 
         sec = max_over_ranks(time_region(step, 5, 3, world, device), world, device) / (5 * copies)
         res[str(M)] = {"us": round(1e6 * sec, 2), "GBps": round(wbytes / sec / 1e9, 1)}
+    # M > 8 on the tile kernel (the same quantize + matmul per copy)
+    for M in (16, 64, 512):
+        x = torch.from_numpy(synth.gen_x(19, M, K)).to(device)
+        buf = xq.quantize_q8(x)
+        y = torch.empty((M, N), dtype=torch.float32, device=device)
+
+        def step():
+            for c in range(copies):
+                xq.quantize_q8(x, out=buf)
+                xq.matmul_iq4xs_q8(Ws[c], cb, buf, M, N, K, y=y)
+
+        sec = max_over_ranks(time_region(step, 3, 2, world, device), world, device) / (3 * copies)
+        res[str(M)] = {"us": round(1e6 * sec, 2), "GBps": round(wbytes / sec / 1e9, 1),
+                       "TOPS_int": round(2.0 * M * N * K / sec / 1e12, 1)}
     out["iq4xs-ffn_up-17408x5120"] = {"rotated_copies": copies, "weight_bytes": wbytes, "by_m": res,
                                       "codebook": "synthetic (the pages do not print the format's table)"}
     # prefill tile M=512: up (Q4_K) then down (Q6_K), each launch timed on its own

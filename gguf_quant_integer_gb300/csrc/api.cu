@@ -186,15 +186,55 @@ xq_status layer_inputs(const xq_proj* proj, int n_proj, int n_inputs, int M, int
 // is projection p's Q8 buffer, sched the scheduling state sc describes
 // (zeroed by the kernel before). M <= 8: one grouped tensor-core GEMV launch
 // per weight type (kMaxProj items per launch), then the dp4a GEMV for the
-// Q6_K rows that are not 16-byte multiples; M > 8: each projection on its
-// own (GEMV chunks up to 64 tokens, the tile kernel above), in the order
-// given.
+// Q6_K rows that are not 16-byte multiples; 8 < M <= 64: grouped launches
+// over (projection, 8-token chunk) pairs; M > 64: the tile kernel per
+// projection, in the order given.
 xq_status layer_matmuls(const xq_proj* proj, int n_proj, const uint8_t* const* q8, int M, const Sched& sc,
                         uint8_t* sched, cudaStream_t s) {
   if (M > kMaxGemvM) {
+    // 8 < M <= 64: per weight type, grouped GEMV launches over every
+    // (projection, 8-token chunk) pair, kMaxProj pairs per launch, the chunks
+    // of one projection side by side so that they share its weight tiles
+    // through L2 (no counter, no K-split). The other projections (and all
+    // of them above 64 tokens) run on their own.
+    const bool chunked = M <= xq::kGemvMaxTokens;
+    const int chunks = (M + 7) / 8;
+    bool first_launch = true;
+    for (int g = 0; chunked && g < kTypes; ++g) {
+      const int type = kTypeIds[g];
+      xq::MmaProj items[xq::kMaxProj];
+      int n = 0;
+      for (int p = 0; p < n_proj; ++p) {
+        const xq_proj& q = proj[p];
+        if (q.N == 0 || q.type != type || !xq::gemv_mma_supports(q.type, q.K)) continue;
+        for (int c = 0; c < chunks; ++c) {
+          xq::MmaProj& it = items[n++];
+          it.W = static_cast<const uint8_t*>(q.W);
+          it.xq = q8[p];
+          it.y = q.y;
+          it.isum = nullptr;
+          it.N = q.N;
+          it.K = q.K;
+          it.M_total = M;
+          it.chunk = c;
+          it.nch = 1;
+          if (n == xq::kMaxProj) {
+            if (xq::launch_gemv_mma(type, items, n, s, true, nullptr, nullptr, nullptr, first_launch) != cudaSuccess)
+              return XQ_ERR_CUDA;
+            first_launch = false;
+            n = 0;
+          }
+        }
+      }
+      if (n > 0) {
+        if (xq::launch_gemv_mma(type, items, n, s, true, nullptr, nullptr, nullptr, first_launch) != cudaSuccess)
+          return XQ_ERR_CUDA;
+        first_launch = false;
+      }
+    }
     for (int p = 0; p < n_proj; ++p) {
       const xq_proj& q = proj[p];
-      if (q.N == 0) continue;
+      if (q.N == 0 || (chunked && xq::gemv_mma_supports(q.type, q.K))) continue;
       const xq_status st = run_matmul(q.type, q.W, q8[p], M, q.N, q.K, q.y, nullptr, s);
       if (st != XQ_OK) return st;
     }
