@@ -139,6 +139,24 @@ void choose_chunks(const xq_proj* proj, int n_proj, int M, int type, int* nch) {
 
 Sched sched_layout(const xq_proj* proj, int n_proj, int M) {
   Sched sc = {};
+  if (M > kMaxGemvM) {
+    // 8 < M <= 64: every (projection, 8-token chunk) pair of a long row is
+    // split over K with its own arrival counts and partial sums (the pairs
+    // are spread over several launches that may run at once); no counters.
+    for (int p = 0; p < n_proj && p < 64; ++p) sc.nch[p] = 1;
+    if (M > xq::kGemvMaxTokens) return sc;
+    const int chunks = (M + 7) / 8;
+    for (int p = 0; p < n_proj && p < 64; ++p) {
+      const xq_proj& q = proj[p];
+      if (q.N <= 0 || !xq::gemv_mma_supports(q.type, q.K)) continue;
+      sc.nch[p] = xq::gemv_split_chunks(q.K, kMaxGemvM, 16);
+      if (sc.nch[p] <= 1) continue;
+      const int g = type_index(q.type);
+      sc.arrive[g] += chunks * xq::gemv_split_arrive_bytes(q.N);
+      sc.partial[g] += chunks * xq::gemv_split_partial_bytes(q.N, sc.nch[p]);
+    }
+    return sc;
+  }
   int items[kTypes] = {0, 0, 0};
   for (int p = 0; p < n_proj && p < 64; ++p) {
     sc.nch[p] = 1;
@@ -195,15 +213,48 @@ xq_status layer_matmuls(const xq_proj* proj, int n_proj, const uint8_t* const* q
     // 8 < M <= 64: per weight type, grouped GEMV launches over every
     // (projection, 8-token chunk) pair, kMaxProj pairs per launch, the chunks
     // of one projection side by side so that they share its weight tiles
-    // through L2 (no counter, no K-split). The other projections (and all
-    // of them above 64 tokens) run on their own.
+    // through L2; rows longer than 24 super-blocks split over K (no task
+    // counter). The other projections (and all of them above 64 tokens) run
+    // on their own.
     const bool chunked = M <= xq::kGemvMaxTokens;
     const int chunks = (M + 7) / 8;
+    // split workspaces: per type, the arrival counts (zeroed by the quantize
+    // launch), then the partial sums, consumed launch by launch in item order
+    uint8_t* arr_cur[kTypes];
+    uint8_t* part_cur[kTypes];
+    {
+      uint8_t* a = sched + kTypes * kCounterBytes;
+      uint8_t* pt = a;
+      for (int g = 0; g < kTypes; ++g) pt += sc.arrive[g];
+      for (int g = 0; g < kTypes; ++g) {
+        arr_cur[g] = a;
+        part_cur[g] = pt;
+        a += sc.arrive[g];
+        pt += sc.partial[g];
+      }
+    }
     bool first_launch = true;
     for (int g = 0; chunked && g < kTypes; ++g) {
       const int type = kTypeIds[g];
       xq::MmaProj items[xq::kMaxProj];
       int n = 0;
+      auto launch = [&]() -> bool {
+        size_t ab = 0, pb = 0;
+        for (int k = 0; k < n; ++k)
+          if (items[k].nch > 1) {
+            ab += xq::gemv_split_arrive_bytes(items[k].N);
+            pb += xq::gemv_split_partial_bytes(items[k].N, items[k].nch);
+          }
+        const bool split = ab > 0;
+        if (xq::launch_gemv_mma(type, items, n, s, true, nullptr, split ? arr_cur[g] : nullptr,
+                                split ? part_cur[g] : nullptr, first_launch) != cudaSuccess)
+          return false;
+        arr_cur[g] += ab;
+        part_cur[g] += pb;
+        first_launch = false;
+        n = 0;
+        return true;
+      };
       for (int p = 0; p < n_proj; ++p) {
         const xq_proj& q = proj[p];
         if (q.N == 0 || q.type != type || !xq::gemv_mma_supports(q.type, q.K)) continue;
@@ -217,20 +268,11 @@ xq_status layer_matmuls(const xq_proj* proj, int n_proj, const uint8_t* const* q
           it.K = q.K;
           it.M_total = M;
           it.chunk = c;
-          it.nch = 1;
-          if (n == xq::kMaxProj) {
-            if (xq::launch_gemv_mma(type, items, n, s, true, nullptr, nullptr, nullptr, first_launch) != cudaSuccess)
-              return XQ_ERR_CUDA;
-            first_launch = false;
-            n = 0;
-          }
+          it.nch = sc.nch[p];
+          if (n == xq::kMaxProj && !launch()) return XQ_ERR_CUDA;
         }
       }
-      if (n > 0) {
-        if (xq::launch_gemv_mma(type, items, n, s, true, nullptr, nullptr, nullptr, first_launch) != cudaSuccess)
-          return XQ_ERR_CUDA;
-        first_launch = false;
-      }
+      if (n > 0 && !launch()) return XQ_ERR_CUDA;
     }
     for (int p = 0; p < n_proj; ++p) {
       const xq_proj& q = proj[p];
@@ -488,8 +530,6 @@ xq_status xq_layer_mixed(const xq_proj* proj, int n_proj, const float* const* in
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   // scheduling state: counters and arrival counts, zeroed by the quantize
   // launch (the matmuls leave them at zero), then partial sums
-  bool any_dynamic = false;
-  for (int g = 0; g < kTypes; ++g) any_dynamic = any_dynamic || sc.dynamic[g];
   const int zero_words = static_cast<int>(sched_zero_bytes(sc) / 4);
   // One launch quantizes every input that is read (up to kMaxProj per launch).
   {
@@ -505,7 +545,7 @@ xq_status xq_layer_mixed(const xq_proj* proj, int n_proj, const float* const* in
       j.K = in_k[i];
       --left;
       if (n == xq::kMaxProj || left == 0) {
-        unsigned int* zero = (left == 0 && any_dynamic) ? reinterpret_cast<unsigned int*>(ws + sched_off) : nullptr;
+        unsigned int* zero = left == 0 ? reinterpret_cast<unsigned int*>(ws + sched_off) : nullptr;
         if (xq::launch_quantize_q8(jobs, n, s, true, zero, zero_words) != cudaSuccess) return XQ_ERR_CUDA;
         n = 0;
       }

@@ -321,8 +321,10 @@ RAGGED_SPLIT_Q80 = synth.Workload(
     seed_base=950, x_seed_base=19500, input_dims=(7168,))
 
 
-@pytest.mark.parametrize("M", [1, 5, 8])
+@pytest.mark.parametrize("M", [1, 5, 8, 20, 40, 64])
 def test_ragged_split_layer(xq, M):
+    # M > 8: (projection, 8-token chunk) pairs over several grouped launches,
+    # each pair of a long row with its own split workspace
     assert layer_check(xq, RAGGED_SPLIT, M) > 0
     assert layer_check(xq, RAGGED_SPLIT_Q80, M) > 0
 
