@@ -202,8 +202,9 @@ typedef struct {
  * some projection reads, each rounded up to 256 bytes, then scheduling
  * state: one 256-byte task counter per weight type (Q4_K, Q6_K, Q8_0) and, for
  * each projection with more than 24 super-blocks per row that the grouped
- * tensor-core GEMV splits over K across CTAs (M <= 8), its arrival counts
- * and partial sums. 0 on bad arguments. */
+ * tensor-core GEMV splits over K across CTAs (M <= 64; above 8 tokens once
+ * per 8-token chunk), its arrival counts and partial sums. 0 on bad
+ * arguments. */
 XQ_API size_t xq_layer_workspace_bytes(const xq_proj *proj, int n_proj, int n_inputs, int M);
 
 /* One layer's projections with a quant type per tensor (xLLM v0.7 article,
@@ -215,7 +216,9 @@ XQ_API size_t xq_layer_workspace_bytes(const xq_proj *proj, int n_proj, int n_in
  *   workspace: device buffer of at least xq_layer_workspace_bytes() bytes;
  *              receives the Q8 activations, one region per input.
  * Enqueues one quantization per used input and the projections, in order,
- * on `stream`. */
+ * on `stream`: at M <= 8 one grouped GEMV launch per weight type; at
+ * 8 < M <= 64 grouped GEMV launches over (projection, 8-token chunk) pairs,
+ * 8 per launch; above 64 tokens the tile kernel per projection. */
 XQ_API xq_status xq_layer_mixed(const xq_proj *proj, int n_proj,
                          const float *const *inputs, int n_inputs, int M,
                          void *workspace, size_t ws_bytes, xq_stream stream);
@@ -243,9 +246,9 @@ XQ_API size_t xq_layer_ffn_workspace_bytes(const xq_proj *proj, int n_proj, int 
  * ignored; N of gate and up must equal K of down). Enqueues, in order on
  * `stream`: the Q8 quantization of every input; the gate and up projections;
  * one xq_silu_mul_quantize_q8 launch on their outputs; every other
- * projection together with down (one grouped GEMV launch per weight type at
- * M <= 8, split over K like the layer's; per projection above, GEMV chunks
- * up to M = 64 and the tile kernel beyond). The
+ * projection together with down (grouped GEMV launches as in
+ * xq_layer_mixed, split over K like the layer's; the tile kernel per
+ * projection above 64 tokens). The
  * projections that do not depend on gate and up thus share down's launch. */
 XQ_API xq_status xq_layer_mixed_ffn(const xq_proj *proj, int n_proj, int gate, int up, int down,
                              const float *const *inputs, int n_inputs, int M,
