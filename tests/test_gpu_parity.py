@@ -295,7 +295,7 @@ def layer_check(xq, wl, M, layer=0, rows=None):
     return max(errs)
 
 
-@pytest.mark.parametrize("M", [1, 2, 4, 8])
+@pytest.mark.parametrize("M", [1, 2, 4, 8, 16, 33])
 def test_qwen25_layer_full(xq, M):
     assert layer_check(xq, synth.WORKLOADS["qwen2.5-1.5b-layer"], M) > 0
 
@@ -339,7 +339,7 @@ def test_q8_0_shapes_all_m(xq, N, K):
     assert max(errs) > 0.0
 
 
-@pytest.mark.parametrize("M", [1, 3, 8])
+@pytest.mark.parametrize("M", [1, 3, 8, 20, 64])
 def test_q8_0_layer(xq, M):
     # a Qwen2.5-1.5B-shaped layer requantized to Q8_0, through xq_layer_mixed
     # (one grouped Q8_0 launch; the 8960-wide down projection is split over K)
