@@ -226,7 +226,6 @@ bool gemv_mma_supports(int type, int K);
 cudaError_t launch_gemv_mma(int type, const MmaProj* projs, int n, cudaStream_t s, bool pdl,
                             unsigned int* counter = nullptr, uint8_t* arrive_ws = nullptr,
                             uint8_t* partial_ws = nullptr, bool wait_prev = true);
-cudaError_t launch_gemv_q4k(const GemvArgs& a, cudaStream_t s);
 
 // 2D tensor map (no interleave, no swizzle, zero fill): dims {dim0, dim1}
 // elements of type dt, rows stride1 bytes apart, boxes box0 x box1. False
