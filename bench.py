@@ -46,10 +46,11 @@ FALLBACK_HBM_GBS = 6800.0
 HEADLINE = "llama3-8b-32layer"
 
 
-# workloads --profile-workload runs (one launch per call)
 # The headline metric, the same string on both arms.
 METRIC = "Q4_K/Q6_K x Q8 matmul weight GB/s (M=%d) and %% of GB300 HBM roofline"
-PROFILE_WORKLOADS = ("prefill512-up", "prefill512-down", "qwen3-q6k-layer", "llama3-layer")
+# workloads --profile-workload runs (one launch per call)
+PROFILE_WORKLOADS = ("prefill512-up", "prefill512-down", "qwen3-q6k-layer", "llama3-layer", "iq4xs-ffn-up",
+                     "q8_0-qwen25-layer")
 
 
 def parse_args(argv=None):
@@ -805,8 +806,17 @@ def profile_workload(args):
         buf = xq.quantize_q8(x)
         y = torch.empty((M, p.N), dtype=torch.float32, device=device)
         run = lambda: xq.matmul(p.qtype, W, buf, M, p.N, p.K, y=y)
+    elif name == "iq4xs-ffn-up":
+        # IQ4_XS 17408 x 5120 (47.3 MB), synthetic codebook, M from --m
+        N, K, M = 17408, 5120, args.m
+        W = torch.from_numpy(synth.gen_iq4xs(17, N, K).reshape(-1)).to(device)
+        cb = synth.gen_codebook(0)
+        buf = xq.quantize_q8(torch.from_numpy(synth.gen_x(18, M, K)).to(device))
+        y = torch.empty((M, N), dtype=torch.float32, device=device)
+        run = lambda: xq.matmul_iq4xs_q8(W, cb, buf, M, N, K, y=y)
     else:
-        wl = synth.WORKLOADS["qwen3-8b-mixed-layer" if name == "qwen3-q6k-layer" else "llama3-8b-32layer"]
+        wl = synth.WORKLOADS[{"qwen3-q6k-layer": "qwen3-8b-mixed-layer",
+                              "q8_0-qwen25-layer": "qwen2.5-1.5b-q8_0-layer"}.get(name, "llama3-8b-32layer")]
         keep = [t for t, p in enumerate(wl.projs) if name != "qwen3-q6k-layer" or p.qtype == synth.Q6_K]
         M = args.m
         weights = synth.gen_layer_weights(wl, 0)
