@@ -107,10 +107,30 @@ size_t round256(size_t b) { return (b + 255) & ~static_cast<size_t>(255); }
 // from the same helpers the launcher uses). The counters and arrival counts
 // form one range that the quantize launch zeroes.
 constexpr size_t kCounterBytes = 256;
-constexpr int kTypes = 3;  // 0: Q4_K, 1: Q6_K, 2: Q8_0
-constexpr int kTypeIds[kTypes] = {XQ_TYPE_Q4_K, XQ_TYPE_Q6_K, XQ_TYPE_Q8_0};
+constexpr int kTypes = 4;  // 0: Q4_K, 1: Q6_K, 2: Q8_0, 3: IQ4_XS
+constexpr int kTypeIds[kTypes] = {XQ_TYPE_Q4_K, XQ_TYPE_Q6_K, XQ_TYPE_Q8_0, XQ_TYPE_IQ4_XS};
 
-int type_index(int type) { return type == XQ_TYPE_Q4_K ? 0 : (type == XQ_TYPE_Q6_K ? 1 : 2); }
+int type_index(int type) {
+  return type == XQ_TYPE_Q4_K ? 0 : (type == XQ_TYPE_Q6_K ? 1 : (type == XQ_TYPE_Q8_0 ? 2 : 3));
+}
+
+// The 16 int8 codebook values of an IQ4_XS weight as 4 little-endian words.
+void pack_codebook(const int8_t* codebook, uint32_t (&cb)[4]) {
+  for (int i = 0; i < 4; ++i)
+    cb[i] = static_cast<uint32_t>(static_cast<uint8_t>(codebook[4 * i])) |
+            (static_cast<uint32_t>(static_cast<uint8_t>(codebook[4 * i + 1])) << 8) |
+            (static_cast<uint32_t>(static_cast<uint8_t>(codebook[4 * i + 2])) << 16) |
+            (static_cast<uint32_t>(static_cast<uint8_t>(codebook[4 * i + 3])) << 24);
+}
+
+// A projection's MmaProj fields that do not depend on the chunk.
+void set_codebook(const xq_proj& q, xq::MmaProj& it) {
+  if (q.type == XQ_TYPE_IQ4_XS && q.codebook) {
+    uint32_t cb[4];
+    pack_codebook(q.codebook, cb);
+    for (int i = 0; i < 4; ++i) it.codebook[i] = cb[i];
+  }
+}
 
 struct Sched {
   bool dynamic[kTypes];  // the type's grouped GEMV fits one launch: counter and K-split
@@ -157,7 +177,7 @@ Sched sched_layout(const xq_proj* proj, int n_proj, int M) {
     }
     return sc;
   }
-  int items[kTypes] = {0, 0, 0};
+  int items[kTypes] = {0, 0, 0, 0};
   for (int p = 0; p < n_proj && p < 64; ++p) {
     sc.nch[p] = 1;
     if (in_group(proj[p], M)) ++items[type_index(proj[p].type)];
@@ -189,11 +209,12 @@ xq_status layer_inputs(const xq_proj* proj, int n_proj, int n_inputs, int M, int
   for (int p = 0; p < n_proj; ++p) {
     const xq_proj& q = proj[p];
     if (block_bytes(q.type) == 0) return XQ_ERR_ARG;
-    if (q.type == XQ_TYPE_IQ4_XS) return XQ_ERR_UNSUPPORTED;  // its codebook has no place in xq_proj
+    if (q.type == XQ_TYPE_IQ4_XS && !q.codebook) return XQ_ERR_ARG;
     if (q.input < 0 || q.input >= n_inputs) return XQ_ERR_ARG;
     const xq_status st = check_shape(M, q.N, q.K);
     if (st != XQ_OK) return st;
     if (q.type == XQ_TYPE_Q8_0 && M > xq::kGemvMaxTokens) return XQ_ERR_UNSUPPORTED;
+    if (q.type == XQ_TYPE_IQ4_XS && (q.K % 512) != 0) return XQ_ERR_SHAPE;
     if (in_k[q.input] == 0) in_k[q.input] = q.K;
     if (in_k[q.input] != q.K) return XQ_ERR_SHAPE;
   }
@@ -207,6 +228,17 @@ xq_status layer_inputs(const xq_proj* proj, int n_proj, int n_inputs, int M, int
 // Q6_K rows that are not 16-byte multiples; 8 < M <= 64: grouped launches
 // over (projection, 8-token chunk) pairs; M > 64: the tile kernel per
 // projection, in the order given.
+// One projection on its own (run_matmul), with its codebook for IQ4_XS.
+xq_status run_one(const xq_proj& q, const uint8_t* q8, int M, cudaStream_t s) {
+  uint32_t cb[4];
+  const uint32_t* cbp = nullptr;
+  if (q.type == XQ_TYPE_IQ4_XS) {
+    pack_codebook(q.codebook, cb);
+    cbp = cb;
+  }
+  return run_matmul(q.type, q.W, q8, M, q.N, q.K, q.y, nullptr, s, false, cbp);
+}
+
 xq_status layer_matmuls(const xq_proj* proj, int n_proj, const uint8_t* const* q8, int M, const Sched& sc,
                         uint8_t* sched, cudaStream_t s) {
   if (M > kMaxGemvM) {
@@ -269,6 +301,7 @@ xq_status layer_matmuls(const xq_proj* proj, int n_proj, const uint8_t* const* q
           it.M_total = M;
           it.chunk = c;
           it.nch = sc.nch[p];
+          set_codebook(q, it);
           if (n == xq::kMaxProj && !launch()) return XQ_ERR_CUDA;
         }
       }
@@ -277,7 +310,7 @@ xq_status layer_matmuls(const xq_proj* proj, int n_proj, const uint8_t* const* q
     for (int p = 0; p < n_proj; ++p) {
       const xq_proj& q = proj[p];
       if (q.N == 0 || (chunked && xq::gemv_mma_supports(q.type, q.K))) continue;
-      const xq_status st = run_matmul(q.type, q.W, q8[p], M, q.N, q.K, q.y, nullptr, s);
+      const xq_status st = run_one(q, q8[p], M, s);
       if (st != XQ_OK) return st;
     }
     return XQ_OK;
@@ -321,6 +354,7 @@ xq_status layer_matmuls(const xq_proj* proj, int n_proj, const uint8_t* const* q
         it.M_total = M;
         it.chunk = 0;
         it.nch = sc.nch[p];
+        set_codebook(q, it);
       }
       if (n > 0 && (n == xq::kMaxProj || p == n_proj)) {
         if (xq::launch_gemv_mma(type, items, n, s, true, counter[g], arrive[g], partial[g], first_launch) !=
@@ -334,7 +368,7 @@ xq_status layer_matmuls(const xq_proj* proj, int n_proj, const uint8_t* const* q
   for (int p = 0; p < n_proj; ++p) {
     const xq_proj& q = proj[p];
     if (q.N == 0 || in_group(q, M)) continue;
-    const xq_status st = run_matmul(q.type, q.W, q8[p], M, q.N, q.K, q.y, nullptr, s);
+    const xq_status st = run_one(q, q8[p], M, s);
     if (st != XQ_OK) return st;
   }
   return XQ_OK;
@@ -458,11 +492,7 @@ static xq_status iq4xs_entry(const void* W, const int8_t* codebook, const void* 
   if (!aligned16(W) || !aligned16(xq) || !aligned16(y) || (isum && !aligned16(isum))) return XQ_ERR_ALIGN;
   if (isum && M > kMaxGemvM) return XQ_ERR_UNSUPPORTED;
   uint32_t cb[4];
-  for (int i = 0; i < 4; ++i)
-    cb[i] = static_cast<uint32_t>(static_cast<uint8_t>(codebook[4 * i])) |
-            (static_cast<uint32_t>(static_cast<uint8_t>(codebook[4 * i + 1])) << 8) |
-            (static_cast<uint32_t>(static_cast<uint8_t>(codebook[4 * i + 2])) << 16) |
-            (static_cast<uint32_t>(static_cast<uint8_t>(codebook[4 * i + 3])) << 24);
+  pack_codebook(codebook, cb);
   return run_matmul(XQ_TYPE_IQ4_XS, W, xq, M, N, K, y, isum, reinterpret_cast<cudaStream_t>(stream), false, cb);
 }
 

@@ -41,7 +41,8 @@ class XQError(RuntimeError):
 
 class xq_proj(ctypes.Structure):
     _fields_ = [("type", ctypes.c_int), ("N", ctypes.c_int), ("K", ctypes.c_int),
-                ("W", ctypes.c_void_p), ("y", ctypes.c_void_p), ("input", ctypes.c_int)]
+                ("W", ctypes.c_void_p), ("y", ctypes.c_void_p), ("input", ctypes.c_int),
+                ("codebook", ctypes.c_void_p)]
 
 
 _lib = None
@@ -237,12 +238,21 @@ def debug_isums(qtype: int, W, xq, M: int, N: int, K: int, y=None, isum=None, st
 
 
 def _proj_array(projs):
+    """projs: (type, N, K, W, y, input[, codebook]) tuples; an IQ4_XS entry
+    carries its 16-value int8 codebook (host array) as the 7th element."""
     arr = (xq_proj * max(1, len(projs)))()
+    keep = []
     for i, p in enumerate(projs):
         arr[i].type, arr[i].N, arr[i].K = int(p[0]), int(p[1]), int(p[2])
         arr[i].W = p[3].data_ptr() if p[3] is not None else None
         arr[i].y = p[4].data_ptr() if p[4] is not None else None
         arr[i].input = int(p[5])
+        cb = p[6] if len(p) > 6 else None
+        if cb is not None:
+            cb = _codebook(cb)
+            keep.append(cb)
+            arr[i].codebook = cb.ctypes.data
+    arr._codebooks = keep  # host codebooks live as long as the array
     return arr
 
 
@@ -300,7 +310,7 @@ class Layer:
     dequantized) and `forward` runs xq_layer_mixed on the current stream.
     """
 
-    def __init__(self, projs, weights, M: int, device="cuda"):
+    def __init__(self, projs, weights, M: int, device="cuda", codebooks=None):
         import torch
         self.projs = projs
         self.M = M
@@ -308,7 +318,8 @@ class Layer:
         self.y = [torch.empty((M, p.N), dtype=torch.float32, device=device) for p in projs]
         n_in = 1 + max(p.input for p in projs)
         self.n_inputs = n_in
-        self.desc = [(p.qtype, p.N, p.K, self.W[i], self.y[i], p.input) for i, p in enumerate(projs)]
+        cbs = codebooks or [None] * len(projs)  # per projection; IQ4_XS needs one
+        self.desc = [(p.qtype, p.N, p.K, self.W[i], self.y[i], p.input, cbs[i]) for i, p in enumerate(projs)]
         nb = layer_workspace_bytes(self.desc, n_in, M)
         self.workspace = torch.empty(max(nb, 256), dtype=torch.uint8, device=device)
 

@@ -167,8 +167,9 @@ XQ_API xq_status xq_matmul_q8_0_q8(const void *W, const void *xq, int M, int N, 
  * K must be a multiple of 512 (rows of 16-byte multiples for the tensor
  * map; other K return XQ_ERR_SHAPE). M <= 64 runs the tensor-core GEMV,
  * M > 64 the tile kernel (the codebook lookup done once per weight tile and
- * reused by its 128 tokens). xq_layer_mixed and the batch-invariant entry
- * points take no codebook and return XQ_ERR_UNSUPPORTED for IQ4_XS. */
+ * reused by its 128 tokens). xq_layer_mixed takes IQ4_XS projections with
+ * their codebook in xq_proj; the batch-invariant entry points take no
+ * codebook and return XQ_ERR_UNSUPPORTED for IQ4_XS. */
 XQ_API xq_status xq_matmul_iq4xs_q8(const void *W, const int8_t *codebook, const void *xq, int M, int N,
                              int K, float *y, xq_stream stream);
 
@@ -191,16 +192,21 @@ XQ_API xq_status xq_matmul_invariant(int type, const void *W, const void *xq, in
 
 /* One projection of a transformer layer for xq_layer_mixed. */
 typedef struct {
-    int type;        /* XQ_TYPE_Q4_K, XQ_TYPE_Q6_K or XQ_TYPE_Q8_0 (M <= 64) */
+    int type;        /* XQ_TYPE_Q4_K, XQ_TYPE_Q6_K, XQ_TYPE_Q8_0 (M <= 64) or
+                        XQ_TYPE_IQ4_XS (K a multiple of 512) */
     int N, K;        /* output and input features */
     const void *W;   /* weight bytes, device */
     float *y;        /* fp32 [M][N] output, device */
     int input;       /* index into the layer's inputs[] */
+    const int8_t *codebook;  /* IQ4_XS: HOST pointer to its 16 int8 codebook
+                                values, read during the call; ignored (may be
+                                NULL) for the other types */
 } xq_proj;
 
 /* Workspace bytes xq_layer_mixed needs: the Q8 buffers of every input that
  * some projection reads, each rounded up to 256 bytes, then scheduling
- * state: one 256-byte task counter per weight type (Q4_K, Q6_K, Q8_0) and, for
+ * state: one 256-byte task counter per weight type (Q4_K, Q6_K, Q8_0,
+ * IQ4_XS) and, for
  * each projection with more than 24 super-blocks per row that the grouped
  * tensor-core GEMV splits over K across CTAs (M <= 64; above 8 tokens once
  * per 8-token chunk), its arrival counts and partial sums. 0 on bad

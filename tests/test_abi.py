@@ -105,8 +105,8 @@ def test_layer_argument_errors(L):
     arr, n = projs((12, 16, 512, 0), (14, 8, 512, 0), (12, 16, 1024, 1))
     need = L.xq_layer_workspace_bytes(arr, n, 2, 4)
     # Q8 buffers, then one 256-byte task counter per weight type (Q4_K, Q6_K,
-    # Q8_0; no split at these K)
-    expect = sum(((xq.q8_bytes(4, k) + 255) // 256) * 256 for k in (512, 1024)) + 3 * 256
+    # Q8_0, IQ4_XS; no split at these K)
+    expect = sum(((xq.q8_bytes(4, k) + 255) // 256) * 256 for k in (512, 1024)) + 4 * 256
     assert need == expect
     # mismatched K on one input
     bad, nb = projs((12, 16, 512, 0), (12, 16, 768, 0))
@@ -173,8 +173,13 @@ def test_iq4xs_entry_points_reject_before_launch(L):
     assert L.xq_matmul_iq4xs_q8(P(FAKE + 8), cb, P(FAKE), 2, 16, 1024, P(FAKE), None) == 3
     assert L.xq_matmul_iq4xs_q8(None, None, None, 0, 16, 1024, None, None) == 0         # empty
     assert L.xq_debug_isums_iq4xs(P(FAKE), cb, P(FAKE), 2, 16, 1024, P(FAKE), None, None) == 1
-    # no codebook travels with xq_proj or the batch-invariant matmul
-    arr = xq._proj_array([(23, 16, 1024, None, None, 0)])
+    # the layer takes the codebook through xq_proj; the batch-invariant matmul has none
+    import numpy as np
     ins = (ctypes.c_void_p * 1)(FAKE)
-    assert L.xq_layer_mixed(arr, 1, ins, 1, 4, P(FAKE), 1 << 20, None) == 6
+    arr = xq._proj_array([(23, 16, 1024, None, None, 0)])
+    assert L.xq_layer_mixed(arr, 1, ins, 1, 4, P(FAKE), 1 << 20, None) == 1      # no codebook
+    arr = xq._proj_array([(23, 16, 768, None, None, 0, np.arange(-8, 8, dtype=np.int8))])
+    assert L.xq_layer_mixed(arr, 1, ins, 1, 4, P(FAKE), 1 << 20, None) == 2      # K % 512
+    arr = xq._proj_array([(23, 16, 1024, None, None, 0, np.arange(-8, 8, dtype=np.int8))])
+    assert L.xq_layer_workspace_bytes(arr, 1, 1, 4) > 0
     assert L.xq_matmul_invariant(23, P(FAKE), P(FAKE), 2, 16, 1024, P(FAKE), None) == 6

@@ -271,12 +271,14 @@ def test_row_split_is_bit_identical(xq, qtype):
 
 # ------------------------------------------------------------ layers
 
-def layer_check(xq, wl, M, layer=0, rows=None):
+def layer_check(xq, wl, M, layer=0, rows=None, codebooks=None):
     """Run one layer through xq_layer_mixed and check every projection
-    (all rows, or `rows` sampled rows per projection) against the oracle."""
+    (all rows, or `rows` sampled rows per projection) against the oracle.
+    codebooks: per projection, the IQ4_XS codebook (None for other types)."""
     weights = synth.gen_layer_weights(wl, layer)
     inputs = synth.gen_layer_inputs(wl, M, layer)
-    L = xq.Layer(wl.projs, weights, M)
+    codebooks = codebooks or [None] * len(wl.projs)
+    L = xq.Layer(wl.projs, weights, M, codebooks=codebooks)
     for y in L.y:
         y.fill_(float("nan"))
     L.forward([dev(x) for x in inputs])
@@ -289,7 +291,7 @@ def layer_check(xq, wl, M, layer=0, rows=None):
         rq, rd, _ = q8[p.input]
         W = weights[t]
         sel = np.arange(p.N) if rows is None else np.sort(rng.choice(p.N, size=min(rows, p.N), replace=False))
-        y_ref, ab, _ = oracle.matmul(p.qtype, W[sel], rq, rd, p.K)
+        y_ref, ab, _ = oracle.matmul(p.qtype, W[sel], rq, rd, p.K, codebook=codebooks[t])
         y = L.y[t].cpu().numpy()[:, sel]
         errs.append(check_y(y, y_ref, ab))
     return max(errs)
@@ -640,3 +642,19 @@ def test_iq4xs_tile_scale_forms(xq):
     wide[: N // 2, :, 2:8] = 0x00                # s = -32
     wide[N // 2:, :, 2:8] = 0xFF                 # s = 31
     check_iq4xs_tile(xq, wide.reshape(N, -1), x, cb)
+
+
+# A layer mixing IQ4_XS (two codebooks) with Q4_K and Q6_K: ragged output
+# counts, a long IQ4_XS row that splits over K, through every path by M.
+IQ4XS_LAYER = synth.Workload(
+    key="iq4xs-layer", title="IQ4_XS mixed layer",
+    projs=(synth.Proj("q", synth.IQ4_XS, 2048, 300, 0), synth.Proj("k", synth.Q4_K, 2048, 70, 0),
+           synth.Proj("v", synth.IQ4_XS, 2048, 64, 0), synth.Proj("up", synth.Q6_K, 2048, 200, 0),
+           synth.Proj("down", synth.IQ4_XS, 8192, 130, 1)),
+    seed_base=960, x_seed_base=19700, input_dims=(2048, 8192))
+
+
+@pytest.mark.parametrize("M", [1, 8, 20, 80])
+def test_iq4xs_layer(xq, M):
+    cbs = [synth.gen_codebook(1), None, synth.gen_codebook(2), None, synth.gen_codebook(3)]
+    assert layer_check(xq, IQ4XS_LAYER, M, codebooks=cbs) > 0
