@@ -39,7 +39,6 @@ xq_status run_matmul(int type, const void* W, const void* xq, int M, int N, int 
   const xq::Q8Layout L = xq::q8_layout(M, K, invariant);
   const uint8_t* base = static_cast<const uint8_t*>(xq);
   if (L.ttiles > 0) {
-    if (type == XQ_TYPE_Q8_0) return XQ_ERR_UNSUPPORTED;  // the tile kernel takes Q4_K, Q6_K and IQ4_XS
     const cudaError_t e = xq::launch_tile_mma(type, static_cast<const uint8_t*>(W), base, M, N, K, y, s, true, codebook);
     return e == cudaSuccess ? XQ_OK : XQ_ERR_CUDA;
   }
@@ -213,7 +212,6 @@ xq_status layer_inputs(const xq_proj* proj, int n_proj, int n_inputs, int M, int
     if (q.input < 0 || q.input >= n_inputs) return XQ_ERR_ARG;
     const xq_status st = check_shape(M, q.N, q.K);
     if (st != XQ_OK) return st;
-    if (q.type == XQ_TYPE_Q8_0 && M > xq::kGemvMaxTokens) return XQ_ERR_UNSUPPORTED;
     if (q.type == XQ_TYPE_IQ4_XS && (q.K % 512) != 0) return XQ_ERR_SHAPE;
     if (in_k[q.input] == 0) in_k[q.input] = q.K;
     if (in_k[q.input] != q.K) return XQ_ERR_SHAPE;

@@ -85,6 +85,12 @@ struct Fmt<14> {
   static constexpr int kWBytes = 2 * kOpBytes;  // high and low operands
 };
 template <>
+struct Fmt<8> {
+  static constexpr int kRawRow = kQ80Group, kRawStages = 2;  // 8 Q8_0 blocks (272 bytes) per row and stage
+  static constexpr int kItems = 8;
+  static constexpr int kWBytes = kOpBytes;
+};
+template <>
 struct Fmt<23> {
   static constexpr int kRawRow = 144, kRawStages = 3;  // the 136-byte super-block's 16-byte-aligned window
   static constexpr int kItems = 8;
@@ -97,8 +103,11 @@ struct Smem {
   static constexpr int kTok = kTokStages * kTileItem;
   static constexpr int kW = kWStages * Fmt<TYPE>::kWBytes;
   static constexpr int kCoef = kCoefStages * kRows * 8;
+  // Q8_0: the scale of every 32-block of every row, [stage][block][row]
+  static constexpr int kDs = TYPE == 8 ? kCoefStages * 8 * kRows * 4 : 0;
   static constexpr int kRawOff = 0, kTokOff = kRaw, kWOff = kTokOff + kTok, kCoefOff = kWOff + kW;
-  static constexpr int kBarOff = kCoefOff + kCoef;
+  static constexpr int kDsOff = kCoefOff + kCoef;
+  static constexpr int kBarOff = kDsOff + kDs;
 };
 
 // barrier indices (raw ring first; its size depends on the type)
@@ -203,6 +212,7 @@ __global__ void __launch_bounds__(kThreads, 1) tile_mma_kernel(const __grid_cons
   uint8_t* tok_ring = smem + S::kTokOff;
   uint8_t* w_ring = smem + S::kWOff;
   float2* coef_ring = reinterpret_cast<float2*>(smem + S::kCoefOff);
+  float* ds_ring = reinterpret_cast<float*>(smem + S::kDsOff);  // Q8_0 only
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::kBarOff);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + B::kCount);
   int* split_flag = reinterpret_cast<int*>(tmem_slot + 4);  // [kWStages]: tile uses the two-operand form
@@ -258,11 +268,11 @@ __global__ void __launch_bounds__(kThreads, 1) tile_mma_kernel(const __grid_cons
       const int rs = b % RS;
       if (b >= RS && !warp_wait(BAR(B::kRawEmpty + rs), ((b / RS) - 1) & 1, 1)) break;
       const uint32_t dst = smem_addr(raw_ring + rs * kRawBytes);
-      if (TYPE == 12 || TYPE == 23) {
+      if (TYPE == 12 || TYPE == 23 || TYPE == 8) {
         if (lane == 0) {
           mbar_expect_tx(BAR(B::kRawFull + rs), kRawBytes);  // rows past N arrive zero-filled
-          tma_load_2d(dst, &A.map, TYPE == 12 ? b * (kQ4kBytes / 8) : (kIq4xsBytes * b) & ~15, row0,
-                      BAR(B::kRawFull + rs));
+          const int x = TYPE == 12 ? b * (kQ4kBytes / 8) : (TYPE == 8 ? b * (kQ80Group / 8) : (kIq4xsBytes * b) & ~15);
+          tma_load_2d(dst, &A.map, x, row0, BAR(B::kRawFull + rs));
         }
       } else {
         unsigned mine = 0;
@@ -361,6 +371,39 @@ __global__ void __launch_bounds__(kThreads, 1) tile_mma_kernel(const __grid_cons
               }
               v[c] = pair;
             }
+          }
+          store_row(w_ring + ws * F::kWBytes, r, v);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(BAR(B::kWFull + ws));
+        }
+      } else if (TYPE == 8) {
+        // Q8_0: 8 blocks of 34 bytes (fp16 d, 32 int8 quants). Each block's
+        // d goes to the scale ring for the epilogue (it scales that block's
+        // accumulator per row); the super-block coefficient is 1.
+        coef_ring[cs * kRows + r] = make_float2(1.0f, 0.0f);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          ds_ring[(cs * 8 + i) * kRows + r] = half_bits_to_float(*reinterpret_cast<const unsigned short*>(raw + 34 * i));
+        __syncwarp();
+        if (lane == 0) mbar_arrive(BAR(B::kCoefFull + cs));
+#pragma unroll
+        for (int it = 0; it < 8; ++it, ++wf) {
+          const int ws = wf % kWStages;
+          if (wf >= kWStages && !warp_wait(BAR(B::kWEmpty + ws), ((wf / kWStages) - 1) & 1, 5)) {
+            ok = false;
+            break;
+          }
+          uint32_t qw[8];
+          load_words<8>(raw + 34 * it + 2, qw);  // 2-byte aligned quants
+          uint32_t v[16];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            // weights 4i..4i+3: the int8 q with its sign bit flipped under the
+            // exponent of 1024, minus 1152, is the exact fp16 q
+            const uint32_t x = qw[i] ^ 0x80808080u;
+            v[2 * i] = hsub2(prmt(x, 0x64646464u, 0x4240u), 0x64806480u);      // weights 4i, 4i+2
+            v[2 * i + 1] = hsub2(prmt(x, 0x64646464u, 0x4341u), 0x64806480u);  // weights 4i+1, 4i+3
           }
           store_row(w_ring + ws * F::kWBytes, r, v);
           fence_proxy_async_smem();
@@ -548,7 +591,7 @@ __global__ void __launch_bounds__(kThreads, 1) tile_mma_kernel(const __grid_cons
         const uint32_t id = (TYPE == 12 && it == 8) ? kIdB : kIdH;
         mma_f16_ss(dt, a0, smem_desc(bs, 128, 512), id, false);
         mma_f16_ss(dt, a1, smem_desc(bs + 256, 128, 512), id, true);
-        if (TYPE != 12 && split_flag[ws]) {
+        if ((TYPE == 14 || TYPE == 23) && split_flag[ws]) {
           mma_f16_ss(dt, a0, smem_desc(bs + kOpBytes, 128, 512), id, true);
           mma_f16_ss(dt, a1, smem_desc(bs + kOpBytes + 256, 128, 512), id, true);
         }
@@ -596,9 +639,15 @@ __global__ void __launch_bounds__(kThreads, 1) tile_mma_kernel(const __grid_cons
         }
         tc_fence_after();
         const uint32_t dcol = tl + kColD + 128u * d + 64u * half;
+        if (TYPE == 8 && it == 0 && !warp_wait(BAR(B::kCoefFull + b % kCoefStages), (b / kCoefStages) & 1, 14)) {
+          ok = false;
+          break;
+        }
         if (it < 8) {
           const float d8 = reinterpret_cast<const float*>(tok_ring + ts * kTileItem + kTileItemOp)[r];
           const f2 d82 = pk(d8, d8);
+          // Q8_0: this block's per-row scales (pairs of this thread's rows)
+          const float2* dsp = reinterpret_cast<const float2*>(ds_ring + ((b % kCoefStages) * 8 + it) * kRows + 64 * half);
           // two 16-column loads in flight per wait
 #pragma unroll
           for (int c = 0; c < 4; c += 2) {
@@ -608,16 +657,22 @@ __global__ void __launch_bounds__(kThreads, 1) tile_mma_kernel(const __grid_cons
             tmem_wait_ld();
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
-              acc[8 * c + k] = fma2(d82, pk(__uint_as_float(v[2 * k]), __uint_as_float(v[2 * k + 1])), acc[8 * c + k]);
+              f2 s0 = d82, s1 = d82;
+              if (TYPE == 8) {
+                const float2 a = dsp[8 * c + k], e = dsp[8 * c + 8 + k];
+                s0 = mul2(d82, pk(a.x, a.y));
+                s1 = mul2(d82, pk(e.x, e.y));
+              }
+              acc[8 * c + k] = fma2(s0, pk(__uint_as_float(v[2 * k]), __uint_as_float(v[2 * k + 1])), acc[8 * c + k]);
               acc[8 * c + 8 + k] =
-                  fma2(d82, pk(__uint_as_float(w[2 * k]), __uint_as_float(w[2 * k + 1])), acc[8 * c + 8 + k]);
+                  fma2(s1, pk(__uint_as_float(w[2 * k]), __uint_as_float(w[2 * k + 1])), acc[8 * c + 8 + k]);
             }
           }
         }
         if (it == kItems - 1) {
           // super-block end: run += d' * acc (- dmin * Dmin)
           const int cs = b % kCoefStages;
-          if (!warp_wait(BAR(B::kCoefFull + cs), (b / kCoefStages) & 1, 14)) {
+          if (TYPE != 8 && !warp_wait(BAR(B::kCoefFull + cs), (b / kCoefStages) & 1, 14)) {  // Q8_0 waited at item 0
             ok = false;
             break;
           }
@@ -708,7 +763,8 @@ cudaError_t launch_tile(const TileArgs& A, int grid, cudaStream_t s, bool pdl) {
 
 cudaError_t launch_tile_mma(int type, const uint8_t* W, const uint8_t* xq, int M, int N, int K, float* y,
                             cudaStream_t s, bool pdl, const uint32_t* codebook) {
-  if (M <= kGemvMaxTokens || N <= 0 || K <= 0 || (K & 255) != 0 || (type != 12 && type != 14 && type != 23))
+  if (M <= kGemvMaxTokens || N <= 0 || K <= 0 || (K & 255) != 0 ||
+      (type != 12 && type != 14 && type != 23 && type != 8))
     return cudaErrorInvalidValue;
   if (type == 23 && (!codebook || (K & 511) != 0)) return cudaErrorInvalidValue;
   const Q8Layout L = q8_layout(M, K);
@@ -720,7 +776,7 @@ cudaError_t launch_tile_mma(int type, const uint8_t* W, const uint8_t* xq, int M
   A.K = K;
   A.M = M;
   A.nsb = K >> 8;
-  A.row_bytes = A.nsb * (type == 12 ? kQ4kBytes : (type == 23 ? kIq4xsBytes : kQ6kBytes));
+  A.row_bytes = A.nsb * (type == 12 ? kQ4kBytes : (type == 23 ? kIq4xsBytes : (type == 8 ? kQ80Group : kQ6kBytes)));
   for (int i = 0; i < 4; ++i) A.cb[i] = codebook ? (codebook[i] ^ 0x80808080u) : 0u;
   A.w_bytes = static_cast<unsigned long long>(N) * A.row_bytes;
   A.ttiles = L.ttiles;
@@ -736,6 +792,12 @@ cudaError_t launch_tile_mma(int type, const uint8_t* W, const uint8_t* xq, int M
                        A.row_bytes, Fmt<23>::kRawRow, kRows))
       return cudaErrorInvalidValue;
     return launch_tile<23>(A, grid, s, pdl);
+  }
+  if (type == 8) {
+    if (!encode_tma_2d(&A.map, CU_TENSOR_MAP_DATA_TYPE_UINT64, W, A.row_bytes / 8, static_cast<unsigned long long>(N),
+                       A.row_bytes, kQ80Group / 8, kRows))
+      return cudaErrorInvalidValue;
+    return launch_tile<8>(A, grid, s, pdl);
   }
   return launch_tile<14>(A, grid, s, pdl);
 }

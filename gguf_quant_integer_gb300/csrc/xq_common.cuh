@@ -233,10 +233,10 @@ cudaError_t launch_gemv_mma(int type, const MmaProj* projs, int n, cudaStream_t 
 bool encode_tma_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, unsigned long long dim0,
                    unsigned long long dim1, unsigned long long stride1, unsigned box0, unsigned box1);
 
-// y = x W^T for M > 8 tokens on the tensor-memory tile kernel; type is 12
-// (Q4_K), 14 (Q6_K) or 23 (IQ4_XS, with its codebook as 4 little-endian
-// words; K a multiple of 512), xq the Q8 buffer of M tokens (tile image
-// present).
+// y = x W^T for M > 64 tokens on the tensor-memory tile kernel; type is 12
+// (Q4_K), 14 (Q6_K), 8 (Q8_0) or 23 (IQ4_XS, with its codebook as 4
+// little-endian words; K a multiple of 512), xq the Q8 buffer of M tokens
+// (tile image present).
 cudaError_t launch_tile_mma(int type, const uint8_t* W, const uint8_t* xq, int M, int N, int K, float* y,
                             cudaStream_t s, bool pdl, const uint32_t* codebook = nullptr);
 cudaError_t launch_gemv_q6k(const GemvArgs& a, cudaStream_t s);

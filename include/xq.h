@@ -146,9 +146,9 @@ XQ_API xq_status xq_matmul_q6k_q8(const void *W, const void *xq, int M, int N, i
  *        quants), device, read-only. Blocks are 2-byte aligned; only the base
  *        pointer must be 16-byte aligned. K % 256 == 0 (rows of 8-block
  *        groups, 272 bytes each, are 16-byte multiples).
- * M <= 64 runs the tensor-core GEMV; M > 64 returns XQ_ERR_UNSUPPORTED (the
- * tile kernel takes Q4_K and Q6_K): use the batch-invariant entry points,
- * which run the GEMV per 8-token chunk for any M. */
+ * M <= 64 runs the tensor-core GEMV; M > 64 the tile kernel (each block's
+ * int8 quants as an exact fp16 operand, its scale applied per row to the
+ * block's accumulator). */
 XQ_API xq_status xq_matmul_q8_0_q8(const void *W, const void *xq, int M, int N, int K,
                             float *y, xq_stream stream);
 
@@ -192,7 +192,7 @@ XQ_API xq_status xq_matmul_invariant(int type, const void *W, const void *xq, in
 
 /* One projection of a transformer layer for xq_layer_mixed. */
 typedef struct {
-    int type;        /* XQ_TYPE_Q4_K, XQ_TYPE_Q6_K, XQ_TYPE_Q8_0 (M <= 64) or
+    int type;        /* XQ_TYPE_Q4_K, XQ_TYPE_Q6_K, XQ_TYPE_Q8_0 or
                         XQ_TYPE_IQ4_XS (K a multiple of 512) */
     int N, K;        /* output and input features */
     const void *W;   /* weight bytes, device */

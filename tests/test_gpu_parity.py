@@ -202,6 +202,24 @@ def test_shapes_all_m(xq, qtype, N, K):
     assert max(errs) > 0.0
 
 
+# Q8_0 above 64 tokens: the tile kernel with per-block row scales, ragged N
+# and M, every int8 value as a quant against +-1000 activations.
+@pytest.mark.parametrize("N,K,M", [(130, 1024, 65), (37, 256, 200), (300, 2048, 129)])
+def test_q8_0_tile(xq, N, K, M):
+    assert run_and_check(xq, synth.Q8_0, N, K, M, 51 * N + K, 5 * M + K, want_isum=False) > 0.0
+
+
+def test_q8_0_tile_extremes(xq):
+    N, K, M = 64, 1024, 96
+    W = synth.gen_q8_0(5, N, K).reshape(N, K // 32, 34)
+    W[:, :, 2:] = (np.arange(N * (K // 32) * 32) % 256).astype(np.uint8).reshape(N, K // 32, 32)
+    W[:, :, 0:2] = np.frombuffer(np.float16(0.25).tobytes(), np.uint8)
+    x = synth.gen_x(6, M, K)
+    x[0] = 1000.0
+    x[1, ::2] = -1000.0
+    check_matmul(xq, synth.Q8_0, W.reshape(N, -1), x, want_isum=False)
+
+
 # 8 < M <= 64: the GEMV over 8-token chunks (several chunks per launch).
 @pytest.mark.parametrize("qtype", [synth.Q4_K, synth.Q6_K, synth.Q8_0])
 @pytest.mark.parametrize("M", [9, 13, 40, 64])
@@ -341,7 +359,7 @@ def test_q8_0_shapes_all_m(xq, N, K):
     assert max(errs) > 0.0
 
 
-@pytest.mark.parametrize("M", [1, 3, 8, 20, 64])
+@pytest.mark.parametrize("M", [1, 3, 8, 20, 64, 80])
 def test_q8_0_layer(xq, M):
     # a Qwen2.5-1.5B-shaped layer requantized to Q8_0, through xq_layer_mixed
     # (one grouped Q8_0 launch; the 8960-wide down projection is split over K)
