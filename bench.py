@@ -744,6 +744,16 @@ def secondary_workloads(device, world):
         sec = max_over_ranks(time_region(step, 3, 2, world, device), world, device) / (3 * copies)
         res[str(M)] = {"us": round(1e6 * sec, 2), "GBps": round(wbytes / sec / 1e9, 1),
                        "TOPS_int": round(2.0 * M * N * K / sec / 1e12, 1)}
+    # Q8_0 on the tile kernel: the Qwen3-8B ffn_up shape (12288 x 4096) as Q8_0 at 512 tokens
+    N, K, M = 12288, 4096, 512
+    wq = torch.from_numpy(synth.gen_q8_0(23, N, K).reshape(-1)).to(device)
+    x = torch.from_numpy(synth.gen_x(24, M, K)).to(device)
+    bq = xq.quantize_q8(x)
+    y = torch.empty((M, N), dtype=torch.float32, device=device)
+    sec = max_over_ranks(time_region(lambda: xq.matmul(synth.Q8_0, wq, bq, M, N, K, y=y), 5, 3, world, device),
+                         world, device) / 5
+    out["q8_0-ffn_up-prefill512"] = {"ms": round(1e3 * sec, 4), "TOPS_int": round(2.0 * M * N * K / sec / 1e12, 1),
+                                     "weight_bytes": synth.weight_bytes(synth.Q8_0, N, K)}
     out["iq4xs-ffn_up-17408x5120"] = {"rotated_copies": copies, "weight_bytes": wbytes, "by_m": res,
                                       "codebook": "synthetic (the pages do not print the format's table)"}
     # prefill tile M=512: up (Q4_K) then down (Q6_K), each launch timed on its own
