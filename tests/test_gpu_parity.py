@@ -526,7 +526,7 @@ def test_silu_mul_quantize(xq, M, K):
     assert np.array_equal(s8.view(np.uint32), rs.view(np.uint32))
 
 
-@pytest.mark.parametrize("M", [1, 8, 20])
+@pytest.mark.parametrize("M", [1, 8, 20, 80])
 def test_ffn_layer_down_fed_by_silu_gate_up(xq, M):
     """xq_layer_mixed_ffn on a Qwen2.5-1.5B-shaped layer: every projection
     but down checked as in xq_layer_mixed; down checked against the oracle on
