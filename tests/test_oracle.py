@@ -1,8 +1,8 @@
 """Pins for the CPU oracle, checked against things other than itself.
 
 - hand-derived decode and Q8 fixtures (tests/golden/*.txt);
-- an independent bit-offset reader for Q4_K / Q6_K written from the format
-  description, compared on every position of random blocks;
+- an independent bit-offset reader for Q4_K / Q6_K / Q8_0 / IQ4_XS written
+  from the format description, compared on every position of random blocks;
 - one-hot blocks with closed-form weights;
 - the integer route (exact sub-block sums + fp64 combine) against the plain
   dequantize-then-fp64-GEMV definition (they are one sum, rearranged);
