@@ -1,5 +1,5 @@
 /*
- * xq — GGUF Q4_K / Q6_K x Q8 integer matmul on GB300 (sm_103a).
+ * xq — GGUF Q4_K / Q6_K / Q8_0 / IQ4_XS x Q8 integer matmul on GB300 (sm_103a).
  *
  * The operation (xLLM v0.7 long-context article, Tencent Cloud, section 一
  * "背景"): weights stay in their GGUF k-quant super-blocks; activations are
@@ -9,8 +9,9 @@
  *
  *   y[m][n] = sum_k w[n][k] * (d8[m][k/32] * q8[m][k])
  *
- * with w from the super-block formulas (Q4_K: w = d*sc*q - dmin*m;
- * Q6_K: w = d*s*(q-32)), rearranged as sums of integer sub-block dot products.
+ * with w from the block formulas (Q4_K: w = d*sc*q - dmin*m; Q6_K:
+ * w = d*s*(q-32); Q8_0: w = d*q; IQ4_XS: w = d*(ls-32)*codebook[q]),
+ * rearranged as sums of integer sub-block dot products.
  *
  * Conventions for every entry point:
  *  - Every pointer argument is a DEVICE pointer, owned by the caller. The
@@ -29,8 +30,9 @@
  *
  * Data layouts (all row-major):
  *  - x   : fp32 [M][K].
- *  - W   : GGUF super-blocks, row n is K/256 consecutive blocks;
- *          Q4_K 144 B per block, Q6_K 210 B per block (public GGUF layout).
+ *  - W   : GGUF blocks, row n is K/256 consecutive super-blocks (Q4_K 144 B,
+ *          Q6_K 210 B, IQ4_XS 136 B) or K/32 Q8_0 blocks of 34 B (public
+ *          GGUF layouts).
  *  - xq  : one buffer of xq_q8_bytes(M, K) bytes holding
  *            qs   int8 [M][K]          at byte 0
  *            d8   fp32 [M][K/32]       at byte M*K
