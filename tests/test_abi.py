@@ -179,3 +179,29 @@ def test_iq4xs_entry_points_reject_before_launch(L):
     arr = xq._proj_array([(23, 16, 1024, None, None, 0, np.arange(-8, 8, dtype=np.int8))])
     assert L.xq_layer_workspace_bytes(arr, 1, 1, 4) > 0
     assert L.xq_matmul_invariant(23, P(FAKE), P(FAKE), 2, 16, 1024, P(FAKE), None) == 6
+
+
+def test_layer_workspace_for_chunked_split(L):
+    """8 < M <= 64: every (projection, 8-token chunk) pair of a row longer
+    than 24 super-blocks gets its own arrival counts and partial sums, sized
+    as the launcher consumes them."""
+    from gguf_quant_integer_gb300 import xq
+
+    def r256(b):
+        return -(-b // 256) * 256
+
+    def split_bytes(N, nch):
+        rb = -(-N // 64)
+        return r256(rb * 4 * 4) + r256(nch * 8 * rb * 64 * 4)
+
+    # q: 16 super-blocks (no split); down: 56 super-blocks (4 chunks of 14)
+    specs = [(12, 300, 4096, 0), (12, 130, 14336, 1)]
+    arr = xq._proj_array([(t, n, k, None, None, i) for (t, n, k, i) in specs])
+    for M in (9, 20, 64):
+        chunks = -(-M // 8)
+        q8 = r256(xq.q8_bytes(M, 4096)) + r256(xq.q8_bytes(M, 14336))
+        want = q8 + 4 * 256 + chunks * split_bytes(130, 4)
+        assert L.xq_layer_workspace_bytes(arr, 2, 2, M) == want, M
+    # above 64 tokens (the tile kernel) there is no split state
+    q8 = r256(xq.q8_bytes(80, 4096)) + r256(xq.q8_bytes(80, 14336))
+    assert L.xq_layer_workspace_bytes(arr, 2, 2, 80) == q8 + 4 * 256
