@@ -30,7 +30,8 @@ _lib = None
 
 
 def build(force: bool = False) -> str:
-    """Compile oracle.c into a shared library (gcc, -O2, no FP contraction)."""
+    """Compile oracle.c into a shared library (gcc, -O2, no FP contraction,
+    pthreads for sharing output rows among threads, see set_threads)."""
     os.makedirs(os.path.dirname(_LIB), exist_ok=True)
     deps = [_SRC, os.path.join(_HERE, "oracle.h")]
     if (not force and os.path.exists(_LIB)
@@ -38,10 +39,17 @@ def build(force: bool = False) -> str:
         return _LIB
     tmp = _LIB + f".tmp{os.getpid()}"
     cmd = ["gcc", "-O2", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared",
-           "-std=c99", "-Wall", "-o", tmp, _SRC, "-lm"]
+           "-std=c99", "-Wall", "-pthread", "-o", tmp, _SRC, "-lm"]
     subprocess.run(cmd, check=True)
     os.replace(tmp, _LIB)
     return _LIB
+
+
+def set_threads(n: int) -> int:
+    """Threads the matmul routines may use (output rows are shared out; every
+    output is still computed by one thread in the same order, so results do
+    not depend on it). Returns the count in use."""
+    return int(_load().oracle_set_threads(int(n)))
 
 
 def _load():
@@ -72,11 +80,14 @@ def _load():
     lib.oracle_matmul_q4k_q8.argtypes = [P, P, P, I, I, I, P, P, P]
     lib.oracle_matmul_q6k_q8.argtypes = [P, P, P, I, I, I, P, P, P]
     lib.oracle_gemv_f64.argtypes = [P, P, I, I, I, P]
+    lib.oracle_set_threads.argtypes = [I]
+    lib.oracle_set_threads.restype = I
     for name in ("oracle_quantize_q8", "oracle_dequant_q4k", "oracle_dequant_q6k",
                  "oracle_dequant_q8", "oracle_matmul_q4k_q8", "oracle_matmul_q6k_q8",
                  "oracle_gemv_f64", "oracle_dequant_q8_0", "oracle_matmul_q8_0_q8",
                  "oracle_dequant_iq4xs", "oracle_matmul_iq4xs_q8"):
         getattr(lib, name).restype = ctypes.c_int
+    lib.oracle_set_threads(1)
     _lib = lib
     return lib
 

@@ -38,6 +38,83 @@
 #include <math.h>
 #include <stdint.h>
 #include <string.h>
+#include <pthread.h>
+
+/* Threads for the matmul routines. Output rows n are independent, so they
+ * may be shared out among threads, row n to thread n mod T; every output is
+ * still computed by one thread in the order written below, so the results
+ * do not depend on the thread count. Returns the count in use. */
+static int g_threads = 1;
+
+int oracle_set_threads(int n)
+{
+    g_threads = n < 1 ? 1 : (n > 256 ? 256 : n);
+    return g_threads;
+}
+
+struct mm_args {
+    const uint8_t *W;
+    const int8_t *codebook; /* IQ4_XS only */
+    const int8_t *qs;
+    const float *d8;
+    int M, N, K;
+    double *y, *absterm_out;
+    int32_t *isum_out;
+};
+
+typedef void (*row_fn)(const struct mm_args *a, int n);
+
+struct row_job {
+    row_fn fn;
+    const struct mm_args *a;
+    int t, T;
+};
+
+static void *row_worker(void *p)
+{
+    const struct row_job *j = (const struct row_job *)p;
+    for (int n = j->t; n < j->a->N; n += j->T) j->fn(j->a, n);
+    return NULL;
+}
+
+/* fn(a, n) for every row n: on the calling thread, plus up to g_threads - 1
+ * helper threads (a helper that cannot be started leaves its rows to the
+ * calling thread). */
+static void for_rows(row_fn fn, const struct mm_args *a)
+{
+    int T = g_threads < a->N ? g_threads : a->N;
+    if (T <= 1) {
+        for (int n = 0; n < a->N; n++) fn(a, n);
+        return;
+    }
+    pthread_t th[256];
+    int started[256];
+    struct row_job jobs[256];
+    for (int t = 0; t < T; t++) {
+        jobs[t].fn = fn;
+        jobs[t].a = a;
+        jobs[t].t = t;
+        jobs[t].T = T;
+        started[t] = 0;
+    }
+    for (int t = 1; t < T; t++) started[t] = pthread_create(&th[t], NULL, row_worker, &jobs[t]) == 0;
+    row_worker(&jobs[0]);
+    for (int t = 1; t < T; t++) {
+        if (started[t])
+            pthread_join(th[t], NULL);
+        else
+            row_worker(&jobs[t]);
+    }
+}
+
+static void zero_outputs(const struct mm_args *a)
+{
+    for (int m = 0; m < a->M; m++)
+        for (int n = 0; n < a->N; n++) {
+            a->y[(size_t)m * a->N + n] = 0.0;
+            if (a->absterm_out) a->absterm_out[(size_t)m * a->N + n] = 0.0;
+        }
+}
 
 /* IEEE 754 binary16 -> double, from the definition of the format:
  * 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits; exponent 0 is
@@ -293,43 +370,41 @@ int oracle_dequant_iq4xs(const uint8_t *W, const int8_t *codebook, int N, int K,
  * All in double. isum_out (optional, [M][N][K/32]) receives isum.
  * absterm_out (optional, [M][N]) receives the sum of the absolute values of
  * every scaled term above, both the d-term and the dmin-term. */
+static void q4k_row(const struct mm_args *A, int n)
+{
+    const int M = A->M, N = A->N, K = A->K;
+    const int nsb = K / 256, nsub = K / 32;
+    double d, dmin;
+    int sc[8], mn[8], q[256];
+    for (int b = 0; b < nsb; b++) {
+        oracle_q4k_fields(A->W + ((size_t)n * nsb + b) * ORACLE_Q4K_BYTES, &d, &dmin, sc, mn, q);
+        for (int m = 0; m < M; m++) {
+            const int8_t *a = A->qs + (size_t)m * K + (size_t)b * 256;
+            for (int j = 0; j < 8; j++) {
+                int64_t isum = 0, isum8 = 0;
+                for (int i = 0; i < 32; i++) {
+                    isum += (int64_t)q[32 * j + i] * a[32 * j + i];
+                    isum8 += a[32 * j + i];
+                }
+                double da = (double)A->d8[(size_t)m * nsub + 8 * b + j];
+                double t1 = d * sc[j] * da * (double)isum;
+                double t2 = dmin * mn[j] * da * (double)isum8;
+                A->y[(size_t)m * N + n] += t1 - t2;
+                if (A->absterm_out) A->absterm_out[(size_t)m * N + n] += fabs(t1) + fabs(t2);
+                if (A->isum_out) A->isum_out[((size_t)m * N + n) * nsub + 8 * b + j] = (int32_t)isum;
+            }
+        }
+    }
+}
+
 int oracle_matmul_q4k_q8(const uint8_t *W, const int8_t *qs, const float *d8,
                          int M, int N, int K,
                          double *y, double *absterm_out, int32_t *isum_out)
 {
     if (M < 0 || N < 0 || K <= 0 || K % 256 != 0) return 1;
-    int nsb = K / 256;
-    int nsub = K / 32;
-    double d, dmin;
-    int sc[8], mn[8], q[256];
-    for (int m = 0; m < M; m++)
-        for (int n = 0; n < N; n++) {
-            y[(size_t)m * N + n] = 0.0;
-            if (absterm_out) absterm_out[(size_t)m * N + n] = 0.0;
-        }
-    for (int n = 0; n < N; n++) {
-        for (int b = 0; b < nsb; b++) {
-            oracle_q4k_fields(W + ((size_t)n * nsb + b) * ORACLE_Q4K_BYTES,
-                              &d, &dmin, sc, mn, q);
-            for (int m = 0; m < M; m++) {
-                const int8_t *a = qs + (size_t)m * K + (size_t)b * 256;
-                for (int j = 0; j < 8; j++) {
-                    int64_t isum = 0, isum8 = 0;
-                    for (int i = 0; i < 32; i++) {
-                        isum += (int64_t)q[32 * j + i] * a[32 * j + i];
-                        isum8 += a[32 * j + i];
-                    }
-                    double da = (double)d8[(size_t)m * nsub + 8 * b + j];
-                    double t1 = d * sc[j] * da * (double)isum;
-                    double t2 = dmin * mn[j] * da * (double)isum8;
-                    y[(size_t)m * N + n] += t1 - t2;
-                    if (absterm_out) absterm_out[(size_t)m * N + n] += fabs(t1) + fabs(t2);
-                    if (isum_out)
-                        isum_out[((size_t)m * N + n) * nsub + 8 * b + j] = (int32_t)isum;
-                }
-            }
-        }
-    }
+    struct mm_args A = {W, NULL, qs, d8, M, N, K, y, absterm_out, isum_out};
+    zero_outputs(&A);
+    for_rows(q4k_row, &A);
     return 0;
 }
 
@@ -337,40 +412,38 @@ int oracle_matmul_q4k_q8(const uint8_t *W, const int8_t *qs, const float *d8,
  *   isum_g = sum_i (q[16g+i] - 32) * q8[m][256b+16g+i]     (exact, int64)
  *   y[m][n] += d * s_g * d8[m][(256b+16g)/32] * isum_g     (double)
  * isum_out (optional) is [M][N][K/16]; absterm_out as for Q4_K. */
+static void q6k_row(const struct mm_args *A, int n)
+{
+    const int M = A->M, N = A->N, K = A->K;
+    const int nsb = K / 256, nsub = K / 32, ngrp = K / 16;
+    double d;
+    int s[16], q[256];
+    for (int b = 0; b < nsb; b++) {
+        oracle_q6k_fields(A->W + ((size_t)n * nsb + b) * ORACLE_Q6K_BYTES, &d, s, q);
+        for (int m = 0; m < M; m++) {
+            const int8_t *a = A->qs + (size_t)m * K + (size_t)b * 256;
+            for (int g = 0; g < 16; g++) {
+                int64_t isum = 0;
+                for (int i = 0; i < 16; i++)
+                    isum += (int64_t)(q[16 * g + i] - 32) * a[16 * g + i];
+                double da = (double)A->d8[(size_t)m * nsub + 8 * b + g / 2];
+                double t = d * s[g] * da * (double)isum;
+                A->y[(size_t)m * N + n] += t;
+                if (A->absterm_out) A->absterm_out[(size_t)m * N + n] += fabs(t);
+                if (A->isum_out) A->isum_out[((size_t)m * N + n) * ngrp + 16 * b + g] = (int32_t)isum;
+            }
+        }
+    }
+}
+
 int oracle_matmul_q6k_q8(const uint8_t *W, const int8_t *qs, const float *d8,
                          int M, int N, int K,
                          double *y, double *absterm_out, int32_t *isum_out)
 {
     if (M < 0 || N < 0 || K <= 0 || K % 256 != 0) return 1;
-    int nsb = K / 256;
-    int nsub = K / 32;
-    int ngrp = K / 16;
-    double d;
-    int s[16], q[256];
-    for (int m = 0; m < M; m++)
-        for (int n = 0; n < N; n++) {
-            y[(size_t)m * N + n] = 0.0;
-            if (absterm_out) absterm_out[(size_t)m * N + n] = 0.0;
-        }
-    for (int n = 0; n < N; n++) {
-        for (int b = 0; b < nsb; b++) {
-            oracle_q6k_fields(W + ((size_t)n * nsb + b) * ORACLE_Q6K_BYTES, &d, s, q);
-            for (int m = 0; m < M; m++) {
-                const int8_t *a = qs + (size_t)m * K + (size_t)b * 256;
-                for (int g = 0; g < 16; g++) {
-                    int64_t isum = 0;
-                    for (int i = 0; i < 16; i++)
-                        isum += (int64_t)(q[16 * g + i] - 32) * a[16 * g + i];
-                    double da = (double)d8[(size_t)m * nsub + 8 * b + g / 2];
-                    double t = d * s[g] * da * (double)isum;
-                    y[(size_t)m * N + n] += t;
-                    if (absterm_out) absterm_out[(size_t)m * N + n] += fabs(t);
-                    if (isum_out)
-                        isum_out[((size_t)m * N + n) * ngrp + 16 * b + g] = (int32_t)isum;
-                }
-            }
-        }
-    }
+    struct mm_args A = {W, NULL, qs, d8, M, N, K, y, absterm_out, isum_out};
+    zero_outputs(&A);
+    for_rows(q6k_row, &A);
     return 0;
 }
 
@@ -378,33 +451,34 @@ int oracle_matmul_q6k_q8(const uint8_t *W, const int8_t *qs, const float *d8,
  *   isum = sum_i q[32j+i] * q8[m][32j+i]                   (exact, int64)
  *   y[m][n] += d_j * d8[m][j] * isum                        (double)
  * isum_out (optional) is [M][N][K/32]; absterm_out as for Q4_K. */
+static void q8_0_row(const struct mm_args *A, int n)
+{
+    const int M = A->M, N = A->N, K = A->K;
+    const int nb = K / 32;
+    double d;
+    int q[32];
+    for (int j = 0; j < nb; j++) {
+        oracle_q8_0_fields(A->W + ((size_t)n * nb + j) * ORACLE_Q8_0_BYTES, &d, q);
+        for (int m = 0; m < M; m++) {
+            const int8_t *a = A->qs + (size_t)m * K + (size_t)j * 32;
+            int64_t isum = 0;
+            for (int i = 0; i < 32; i++) isum += (int64_t)q[i] * a[i];
+            double t = d * (double)A->d8[(size_t)m * nb + j] * (double)isum;
+            A->y[(size_t)m * N + n] += t;
+            if (A->absterm_out) A->absterm_out[(size_t)m * N + n] += fabs(t);
+            if (A->isum_out) A->isum_out[((size_t)m * N + n) * nb + j] = (int32_t)isum;
+        }
+    }
+}
+
 int oracle_matmul_q8_0_q8(const uint8_t *W, const int8_t *qs, const float *d8,
                           int M, int N, int K,
                           double *y, double *absterm_out, int32_t *isum_out)
 {
     if (M < 0 || N < 0 || K <= 0 || K % 32 != 0) return 1;
-    int nb = K / 32;
-    double d;
-    int q[32];
-    for (int m = 0; m < M; m++)
-        for (int n = 0; n < N; n++) {
-            y[(size_t)m * N + n] = 0.0;
-            if (absterm_out) absterm_out[(size_t)m * N + n] = 0.0;
-        }
-    for (int n = 0; n < N; n++) {
-        for (int j = 0; j < nb; j++) {
-            oracle_q8_0_fields(W + ((size_t)n * nb + j) * ORACLE_Q8_0_BYTES, &d, q);
-            for (int m = 0; m < M; m++) {
-                const int8_t *a = qs + (size_t)m * K + (size_t)j * 32;
-                int64_t isum = 0;
-                for (int i = 0; i < 32; i++) isum += (int64_t)q[i] * a[i];
-                double t = d * (double)d8[(size_t)m * nb + j] * (double)isum;
-                y[(size_t)m * N + n] += t;
-                if (absterm_out) absterm_out[(size_t)m * N + n] += fabs(t);
-                if (isum_out) isum_out[((size_t)m * N + n) * nb + j] = (int32_t)isum;
-            }
-        }
-    }
+    struct mm_args A = {W, NULL, qs, d8, M, N, K, y, absterm_out, isum_out};
+    zero_outputs(&A);
+    for_rows(q8_0_row, &A);
     return 0;
 }
 
@@ -412,36 +486,36 @@ int oracle_matmul_q8_0_q8(const uint8_t *W, const int8_t *qs, const float *d8,
  *   isum_j = sum_i codebook[idx(32j+i)] * q8[m][256b+32j+i]   (exact, int64)
  *   y[m][n] += d * (ls_j - 32) * d8[m][8b+j] * isum_j          (double)
  * isum_out (optional) is [M][N][K/32]; absterm_out as for Q4_K. */
+static void iq4xs_row(const struct mm_args *A, int n)
+{
+    const int M = A->M, N = A->N, K = A->K;
+    const int nsb = K / 256, nsub = K / 32;
+    double d;
+    int ls[8], v[256];
+    for (int b = 0; b < nsb; b++) {
+        oracle_iq4xs_fields(A->W + ((size_t)n * nsb + b) * ORACLE_IQ4XS_BYTES, A->codebook, &d, ls, v);
+        for (int m = 0; m < M; m++) {
+            const int8_t *a = A->qs + (size_t)m * K + (size_t)b * 256;
+            for (int j = 0; j < 8; j++) {
+                int64_t isum = 0;
+                for (int i = 0; i < 32; i++) isum += (int64_t)v[32 * j + i] * a[32 * j + i];
+                double t = d * (ls[j] - 32) * (double)A->d8[(size_t)m * nsub + 8 * b + j] * (double)isum;
+                A->y[(size_t)m * N + n] += t;
+                if (A->absterm_out) A->absterm_out[(size_t)m * N + n] += fabs(t);
+                if (A->isum_out) A->isum_out[((size_t)m * N + n) * nsub + 8 * b + j] = (int32_t)isum;
+            }
+        }
+    }
+}
+
 int oracle_matmul_iq4xs_q8(const uint8_t *W, const int8_t *codebook, const int8_t *qs, const float *d8,
                            int M, int N, int K,
                            double *y, double *absterm_out, int32_t *isum_out)
 {
     if (M < 0 || N < 0 || K <= 0 || K % 256 != 0) return 1;
-    int nsb = K / 256;
-    int nsub = K / 32;
-    double d;
-    int ls[8], v[256];
-    for (int m = 0; m < M; m++)
-        for (int n = 0; n < N; n++) {
-            y[(size_t)m * N + n] = 0.0;
-            if (absterm_out) absterm_out[(size_t)m * N + n] = 0.0;
-        }
-    for (int n = 0; n < N; n++) {
-        for (int b = 0; b < nsb; b++) {
-            oracle_iq4xs_fields(W + ((size_t)n * nsb + b) * ORACLE_IQ4XS_BYTES, codebook, &d, ls, v);
-            for (int m = 0; m < M; m++) {
-                const int8_t *a = qs + (size_t)m * K + (size_t)b * 256;
-                for (int j = 0; j < 8; j++) {
-                    int64_t isum = 0;
-                    for (int i = 0; i < 32; i++) isum += (int64_t)v[32 * j + i] * a[32 * j + i];
-                    double t = d * (ls[j] - 32) * (double)d8[(size_t)m * nsub + 8 * b + j] * (double)isum;
-                    y[(size_t)m * N + n] += t;
-                    if (absterm_out) absterm_out[(size_t)m * N + n] += fabs(t);
-                    if (isum_out) isum_out[((size_t)m * N + n) * nsub + 8 * b + j] = (int32_t)isum;
-                }
-            }
-        }
-    }
+    struct mm_args A = {W, codebook, qs, d8, M, N, K, y, absterm_out, isum_out};
+    zero_outputs(&A);
+    for_rows(iq4xs_row, &A);
     return 0;
 }
 

@@ -63,6 +63,10 @@ int oracle_matmul_iq4xs_q8(const uint8_t *W, const int8_t *codebook, const int8_
 
 int oracle_gemv_f64(const double *w, const double *x, int M, int N, int K, double *y);
 
+/* Threads for the matmul routines (OpenMP over output rows when built with
+ * it; results do not depend on the count). Returns the count in use. */
+int oracle_set_threads(int n);
+
 #ifdef __cplusplus
 }
 #endif

@@ -563,3 +563,96 @@ def test_gen_codebook_is_sixteen_increasing_int8():
         cb = synth.gen_codebook(seed)
         assert cb.dtype == np.int8 and cb.shape == (16,)
         assert np.all(np.diff(cb.astype(np.int64)) > 0) and cb[0] == -128 and cb[-1] == 127
+
+
+# ------------------------------------------------------------ sum|terms| pins
+
+def _absterm_fixture():
+    """tests/golden/absterm_hand.txt: key -> list of value strings."""
+    out = {}
+    with open(os.path.join(GOLD, "absterm_hand.txt")) as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if line:
+                key, *vals = line.split()
+                out[key] = vals
+    return out
+
+
+def _hand_activation(fx):
+    """The fixture's token: 32 copies of a_j per 32-block, d8_j = 2^e."""
+    a = [int(v) for v in fx["a"]]
+    qs = np.repeat(np.array(a, np.int8), 32).reshape(1, 256)
+    d8 = np.full((1, 8), np.float32(2.0 ** int(fx["d8_log2"][0])), np.float32)
+    return qs, d8
+
+
+def _hex_bytes(vals):
+    return [int(v, 16) for v in vals]
+
+
+def test_absterm_q4k_hand_block():
+    # Both the d-term and the dmin-term enter sum|terms| with their absolute
+    # values: the fixture's terms alternate in sign, so a missing fabs, a
+    # doubled or dropped min term changes the value.
+    fx = _absterm_fixture()
+    qs, d8 = _hand_activation(fx)
+    blk = np.zeros(144, np.uint8)
+    blk[0:2] = np.frombuffer(int(fx["q4k_d_hex"][0], 16).to_bytes(2, "little"), np.uint8)
+    blk[2:4] = np.frombuffer(int(fx["q4k_dmin_hex"][0], 16).to_bytes(2, "little"), np.uint8)
+    blk[4:16] = _hex_bytes(fx["q4k_scales_hex"])
+    blk[16:] = int(fx["q4k_quant_byte"][0], 16)
+    y, ab, _ = oracle.matmul(synth.Q4_K, blk.reshape(1, 144), qs, d8, 256)
+    scale = 2.0 ** int(fx["q4k_log2"][0])
+    assert y[0, 0] == int(fx["q4k_y_num"][0]) * scale
+    assert ab[0, 0] == int(fx["q4k_abs_num"][0]) * scale
+
+
+def test_absterm_q6k_hand_block():
+    # y cancels to a small value while sum|terms| stays large: the pin of the
+    # tolerance denominator is independent of y.
+    fx = _absterm_fixture()
+    qs, d8 = _hand_activation(fx)
+    blk = np.zeros(210, np.uint8)
+    blk[0:128] = int(fx["q6k_ql_byte"][0], 16)
+    blk[128:192] = int(fx["q6k_qh_byte"][0], 16)
+    blk[192:208] = np.array([int(v) for v in fx["q6k_scales"]], np.int8).view(np.uint8)
+    blk[208:210] = np.frombuffer(int(fx["q6k_d_hex"][0], 16).to_bytes(2, "little"), np.uint8)
+    y, ab, _ = oracle.matmul(synth.Q6_K, blk.reshape(1, 210), qs, d8, 256)
+    scale = 2.0 ** int(fx["q6k_log2"][0])
+    assert y[0, 0] == int(fx["q6k_y_num"][0]) * scale
+    assert ab[0, 0] == int(fx["q6k_abs_num"][0]) * scale
+
+
+def test_absterm_iq4xs_hand_block():
+    fx = _absterm_fixture()
+    qs, d8 = _hand_activation(fx)
+    cb = np.array([int(v) for v in fx["iq4xs_codebook"]], np.int8)
+    blk = np.zeros(136, np.uint8)
+    blk[0:2] = np.frombuffer(int(fx["iq4xs_d_hex"][0], 16).to_bytes(2, "little"), np.uint8)
+    blk[2:4] = np.frombuffer(int(fx["iq4xs_scales_h_hex"][0], 16).to_bytes(2, "little"), np.uint8)
+    blk[4:8] = _hex_bytes(fx["iq4xs_scales_l_hex"])
+    blk[8:] = int(fx["iq4xs_index_byte"][0], 16)
+    y, ab, _ = oracle.matmul(synth.IQ4_XS, blk.reshape(1, 136), qs, d8, 256, codebook=cb)
+    scale = 2.0 ** int(fx["iq4xs_log2"][0])
+    assert y[0, 0] == int(fx["iq4xs_y_num"][0]) * scale
+    assert ab[0, 0] == int(fx["iq4xs_abs_num"][0]) * scale
+
+
+def test_threads_do_not_change_results():
+    # output rows shared out among threads: every output is still computed by
+    # one thread in the same order, so the results are bit-identical
+    N, K, M = 37, 1024, 3
+    x = synth.gen_x(61, M, K)
+    qs, d8, _ = oracle.quantize_q8(x)
+    cb = synth.gen_codebook(2)
+    for qtype in (synth.Q4_K, synth.Q6_K, synth.Q8_0, synth.IQ4_XS):
+        W = synth.gen_weight(qtype, 62, N, K) if qtype != synth.IQ4_XS else synth.gen_iq4xs(62, N, K)
+        oracle.set_threads(1)
+        one = oracle.matmul(qtype, W, qs, d8, K, want_isum=True, codebook=cb)
+        used = oracle.set_threads(4)
+        many = oracle.matmul(qtype, W, qs, d8, K, want_isum=True, codebook=cb)
+        oracle.set_threads(1)
+        assert used >= 1
+        for a, b in zip(one, many):
+            assert np.array_equal(a, b)
