@@ -12,11 +12,14 @@
 // loading the library holds until the process exits.
 //
 // Host code cannot use the array's name as a device address (on the host it
-// is only a stand-in symbol). The first call on each device, with that
-// device current, asks the runtime for the real address with
-// cudaGetSymbolAddress, checks the result and caches it; later calls reuse
-// it. That first call may load the module, so make it before any stream
-// capture on that device.
+// is only a stand-in symbol). Every call asks the runtime for the real
+// address with cudaGetSymbolAddress, with the caller's device current, and
+// checks the result. The address belongs to the current context (the
+// module instance loaded into it), so it is not cached across calls: after
+// cudaDeviceReset, or under a caller's own driver-API context, a cached
+// address could point into a module that is gone. Once the module is loaded
+// the lookup is a host-side table lookup; the first call on a device may
+// load it, so make that first call before any stream capture on the device.
 //
 // Nothing here allocates: no cudaMalloc, no cudaFree, no library allocator.
 // Every call on a device shares the one array and leaves its contents
@@ -24,8 +27,6 @@
 // cleared by the quantize kernel of every call. Calls whose work overlaps on
 // the GPU (different streams, or different host threads without ordering)
 // race on the array: order them on one stream or synchronize between them.
-#include <mutex>
-
 #include "xq.h"
 #include "xq_common.cuh"
 
@@ -35,24 +36,14 @@ namespace {
 // 8B-class model at M <= 8 (the Llama-3-8B-shaped layer needs about
 // 1.3 MB); larger requests are refused.
 constexpr size_t kStaticScratchBytes = XQ_LAYER_STATIC_SCRATCH_BYTES;
-constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) uint8_t g_layer_scratch[kStaticScratchBytes];
 
-std::mutex g_mu;
-void* g_scratch_addr[kMaxDevices];  // device address of g_layer_scratch, per device
-
-// Device address of the scratch array on the current device (set up once).
+// Device address of the scratch array in the current context.
 xq_status scratch_address(void** out) {
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return XQ_ERR_CUDA;
-  std::lock_guard<std::mutex> lock(g_mu);
-  if (!g_scratch_addr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_layer_scratch) != cudaSuccess || !p) return XQ_ERR_CUDA;
-    g_scratch_addr[dev] = p;
-  }
-  *out = g_scratch_addr[dev];
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_layer_scratch) != cudaSuccess || !p) return XQ_ERR_CUDA;
+  *out = p;
   return XQ_OK;
 }
 
