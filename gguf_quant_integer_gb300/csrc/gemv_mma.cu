@@ -670,7 +670,11 @@ __device__ __forceinline__ void gemv_mma_body(const Group& G) {
   cudaTriggerProgrammaticLaunchCompletion();
   const int n8 = lane >> 2, t = lane & 3;
   float4* dec = dec_all + warp * (kDecBytes / 16);
-  f2 acc[2] = {0ull, 0ull};
+  // Accumulation bounded by construction: one super-block's terms (at most
+  // 16 fp32 roundings) go into a fresh accumulator, added once to a running
+  // sum; every 32 super-blocks the running sum is added to a total.
+  f2 run[2] = {0ull, 0ull}, tot[2] = {0ull, 0ull};
+  int nrun = 0;
   int slot = 0;
   unsigned fills = 0;
   int cur_task = -1;
@@ -710,6 +714,7 @@ __device__ __forceinline__ void gemv_mma_body(const Group& G) {
     const int rg = tp.rb * kGemvWarps + warp;  // this warp's 16-row group
     const uint8_t* st = ring + slot * kStageBytes;
     const bool rows_ok = rg * 16 < P.N;
+    f2 acc[2] = {0ull, 0ull};
     if (rows_ok) {
       if constexpr (TYPE == 12) {
         decode_scales_q4(st + warp * kBlockBytes, dec, lane);
@@ -733,8 +738,20 @@ __device__ __forceinline__ void gemv_mma_body(const Group& G) {
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(empty_s + 8 * slot);
+    run[0] = add2(run[0], acc[0]);
+    run[1] = add2(run[1], acc[1]);
+    if (++nrun == 32) {
+      tot[0] = add2(tot[0], run[0]);
+      tot[1] = add2(tot[1], run[1]);
+      run[0] = run[1] = 0ull;
+      nrun = 0;
+    }
     resolve();  // a split hand-off from an earlier task, one stage later
     if (m.z) {
+      acc[0] = add2(tot[0], run[0]);
+      acc[1] = add2(tot[1], run[1]);
+      run[0] = run[1] = tot[0] = tot[1] = 0ull;
+      nrun = 0;
       if (P.nch == 1) {
         if (rows_ok) store_y(P, rg, n8, t, lo32(acc[0]), hi32(acc[0]), lo32(acc[1]), hi32(acc[1]));
       } else if (rows_ok) {
@@ -757,8 +774,6 @@ __device__ __forceinline__ void gemv_mma_body(const Group& G) {
         pend_p = tp.p;
         pend_rg = rg;
       }
-      acc[0] = 0ull;
-      acc[1] = 0ull;
     }
     if (++slot == kStages) {
       slot = 0;
@@ -813,6 +828,14 @@ bool encode_weight_map(int type, CUtensorMap* map, const uint8_t* W, int N, int 
 }
 
 }  // namespace
+
+cudaError_t take_gemv_error(unsigned int* code) {
+  unsigned int v = 0, z = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&v, g_gemv_error, sizeof(v));
+  if (e == cudaSuccess) e = cudaMemcpyToSymbol(g_gemv_error, &z, sizeof(z));
+  *code = v;
+  return e;
+}
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,

@@ -761,6 +761,14 @@ cudaError_t launch_tile(const TileArgs& A, int grid, cudaStream_t s, bool pdl) {
 
 }  // namespace
 
+cudaError_t take_tile_error(unsigned int* code) {
+  unsigned int v = 0, z = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&v, g_tile_error, sizeof(v));
+  if (e == cudaSuccess) e = cudaMemcpyToSymbol(g_tile_error, &z, sizeof(z));
+  *code = v;
+  return e;
+}
+
 cudaError_t launch_tile_mma(int type, const uint8_t* W, const uint8_t* xq, int M, int N, int K, float* y,
                             cudaStream_t s, bool pdl, const uint32_t* codebook) {
   if (M <= kGemvMaxTokens || N <= 0 || K <= 0 || (K & 255) != 0 ||

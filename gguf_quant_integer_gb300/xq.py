@@ -30,7 +30,7 @@ SYMBOLS = ("xq_status_str", "xq_q8_bytes", "xq_weight_bytes", "xq_quantize_q8",
            "xq_q8_bytes_invariant", "xq_quantize_q8_invariant", "xq_matmul_invariant",
            "xq_matmul_q8_0_q8", "xq_debug_isums_q8_0", "xq_silu_mul_quantize_q8",
            "xq_layer_ffn_workspace_bytes", "xq_layer_mixed_ffn", "xq_matmul_iq4xs_q8",
-           "xq_debug_isums_iq4xs")
+           "xq_debug_isums_iq4xs", "xq_device_error", "xq_debug_stalled_matmul_q4k")
 
 
 class XQError(RuntimeError):
@@ -87,6 +87,10 @@ def lib(path: str | None = None):
     L.xq_matmul_iq4xs_q8.restype = I
     L.xq_debug_isums_iq4xs.argtypes = [P, P, P, I, I, I, P, P, P]
     L.xq_debug_isums_iq4xs.restype = I
+    L.xq_device_error.argtypes = [P, ctypes.POINTER(ctypes.c_uint)]
+    L.xq_device_error.restype = I
+    L.xq_debug_stalled_matmul_q4k.argtypes = [P, P, I, I, I, P, P]
+    L.xq_debug_stalled_matmul_q4k.restype = I
     L.xq_layer_workspace_bytes.argtypes = [ctypes.POINTER(xq_proj), I, I, I]
     L.xq_layer_workspace_bytes.restype = S
     L.xq_layer_mixed.argtypes = [ctypes.POINTER(xq_proj), I, ctypes.POINTER(ctypes.c_void_p), I, I, P, S, P]
@@ -235,6 +239,22 @@ def debug_isums(qtype: int, W, xq, M: int, N: int, K: int, y=None, isum=None, st
           XQ_TYPE_Q8_0: "xq_debug_isums_q8_0"}[qtype]
     _check(fn, getattr(lib(), fn)(_ptr(W), _ptr(xq), M, N, K, _ptr(y), _ptr(isum), _stream(stream)))
     return y, isum
+
+
+def device_error(stream=None) -> int:
+    """Read and clear the kernels' timed-out-wait record (xq_device_error):
+    0 if no bounded device wait ran out since the last read, else
+    (kernel << 8) | wait."""
+    code = ctypes.c_uint(0)
+    _check("xq_device_error", lib().xq_device_error(_stream(stream), ctypes.byref(code)))
+    return code.value
+
+
+def debug_stalled_matmul_q4k(W, xq, M: int, N: int, K: int, y, stream=None):
+    """Test hook: the Q4_K tensor-memory GEMV with no stage issued and short
+    waits, so that its waits run out (y stays unwritten)."""
+    _check("xq_debug_stalled_matmul_q4k",
+           lib().xq_debug_stalled_matmul_q4k(_ptr(W), _ptr(xq), M, N, K, _ptr(y), _stream(stream)))
 
 
 def _proj_array(projs):

@@ -278,9 +278,12 @@ XQ_API xq_status xq_layer_mixed_ffn(const xq_proj *proj, int n_proj, int gate, i
  *  - Requests whose xq_layer_workspace_bytes() exceeds the fixed size return
  *    XQ_ERR_WORKSPACE before anything is enqueued (one decode layer of an
  *    8B-class model at M <= 8 needs about 1.3 MB).
- *  - The first call on a device, with that device current, looks up the
- *    array's device address (cudaGetSymbolAddress); make it before any
- *    stream capture. A failed lookup returns XQ_ERR_CUDA.
+ *  - Every call looks up the array's device address in the current context
+ *    (cudaGetSymbolAddress, with the caller's device current); the address
+ *    is valid per context and is not cached, so a context created after
+ *    cudaDeviceReset gets its own. The first call on a device may load the
+ *    module: make it before any stream capture. A failed lookup returns
+ *    XQ_ERR_CUDA.
  *  - All calls on a device share the array; the state that must start at
  *    zero is cleared by every call. Calls whose work overlaps on the GPU
  *    (other streams, or unordered host threads) race on it: order them on
@@ -289,6 +292,29 @@ XQ_API xq_status xq_layer_mixed_ffn(const xq_proj *proj, int n_proj, int gate, i
 XQ_API xq_status xq_layer_mixed_static(const xq_proj *proj, int n_proj,
                                 const float *const *inputs, int n_inputs, int M,
                                 xq_stream stream);
+
+/* Failure detection. Every mbarrier wait of the TMA / tensor-core kernels is
+ * bounded (about 2^32 clocks). A wait that runs out records an error code in
+ * a device word; the kernel then leaves its loops, waits for its own copies
+ * and tensor-core work, frees tensor memory and exits, leaving some outputs
+ * unwritten although the call that launched it already returned XQ_OK.
+ * xq_device_error waits until `stream` is idle, then reads and clears those
+ * words. *code_out = 0 if no wait ran out since the last read, else
+ * (kernel << 8) | wait: kernel 1 = the warp-level MMA GEMV, 2 = the
+ * tensor-memory GEMV (Q4_K, M <= 8), 3 = the tile kernel (M > 64); wait = the
+ * kernel's number of the wait that gave up. If several kernels recorded one,
+ * the lowest kernel number is reported and all are cleared. The reads and
+ * writes are synchronous. XQ_ERR_ARG for a null code_out, XQ_ERR_CUDA if the
+ * stream or the reads fail. */
+XQ_API xq_status xq_device_error(xq_stream stream, unsigned int *code_out);
+
+/* Test hook for the failure detection above: the Q4_K tensor-memory GEMV
+ * (1 <= M <= 8) launched with its producer issuing no stage and every wait
+ * limited to about 10^5 clocks, so that the other roles' first waits run out
+ * and record their codes; y is left unwritten and xq_device_error then
+ * reports kernel 2. Arguments and errors as xq_matmul_q4k_q8. */
+XQ_API xq_status xq_debug_stalled_matmul_q4k(const void *W, const void *xq, int M, int N, int K, float *y,
+                                             xq_stream stream);
 
 /* Test hooks: the same matmul kernels with their exact int32 sub-block sums
  * written out instead of only consumed.
