@@ -42,20 +42,6 @@ xq_status run_matmul(int type, const void* W, const void* xq, int M, int N, int 
     const cudaError_t e = xq::launch_tile_mma(type, static_cast<const uint8_t*>(W), base, M, N, K, y, s, true, codebook);
     return e == cudaSuccess ? XQ_OK : XQ_ERR_CUDA;
   }
-  if (type == XQ_TYPE_Q4_K && L.tcb != 0) {
-    // M <= 8, Q4_K: the tensor-memory GEMV (rows on TMEM lanes)
-    xq::MmaProj q;
-    q.W = static_cast<const uint8_t*>(W);
-    q.xq = base;
-    q.y = y;
-    q.isum = isum;
-    q.N = N;
-    q.K = K;
-    q.M_total = M;
-    q.chunk = 0;
-    q.nch = 1;
-    return xq::launch_gemv_tc(&q, 1, s, true) == cudaSuccess ? XQ_OK : XQ_ERR_CUDA;
-  }
   if (xq::gemv_mma_supports(type, K)) {
     xq::MmaProj items[xq::kMaxProj];
     int n = 0;
@@ -154,16 +140,6 @@ struct Sched {
 // Projections that go to the grouped tensor-core GEMV at M <= 8.
 bool in_group(const xq_proj& q, int M) { return q.N > 0 && M <= kMaxGemvM && xq::gemv_mma_supports(q.type, q.K); }
 
-// Whether a type's grouped launch at M <= 8 is the tensor-memory GEMV (Q4_K:
-// 128-row tasks, one CTA per SM) rather than the warp-level MMA GEMV.
-bool uses_tc(int type) { return type == XQ_TYPE_Q4_K; }
-int row_blocks(int type, int N) { return uses_tc(type) ? xq::tc_row_blocks(N) : xq::gemv_row_blocks(N); }
-size_t split_arrive_bytes(int type, int N) {
-  return uses_tc(type) ? xq::tc_split_arrive_bytes(N) : xq::gemv_split_arrive_bytes(N);
-}
-size_t split_partial_bytes(int type, int N, int nch) {
-  return uses_tc(type) ? xq::tc_split_partial_bytes(N, nch) : xq::gemv_split_partial_bytes(N, nch);
-}
 
 // K-chunking of a grouped launch: chunks of ~16 super-blocks for long rows;
 // while the group has fewer 64-row tasks than resident CTAs, halve the chunk
@@ -175,9 +151,9 @@ void choose_chunks(const xq_proj* proj, int n_proj, int M, int type, int* nch) {
     for (int p = 0; p < n_proj; ++p) {
       if (!in_group(proj[p], M) || proj[p].type != type) continue;
       nch[p] = xq::gemv_split_chunks(proj[p].K, M, chunk);
-      tasks += static_cast<long long>(row_blocks(type, proj[p].N)) * nch[p];
+      tasks += static_cast<long long>(xq::gemv_row_blocks(proj[p].N)) * nch[p];
     }
-    if (tasks >= (uses_tc(type) ? xq::kNumSMs : xq::kGemvSlots) || chunk <= 8) return;
+    if (tasks >= xq::kGemvSlots || chunk <= 8) return;
   }
 }
 
@@ -213,8 +189,8 @@ Sched sched_layout(const xq_proj* proj, int n_proj, int M) {
   for (int p = 0; p < n_proj; ++p) {
     if (!in_group(proj[p], M) || !sc.dynamic[type_index(proj[p].type)] || sc.nch[p] <= 1) continue;
     const int g = type_index(proj[p].type);
-    sc.arrive[g] += split_arrive_bytes(proj[p].type, proj[p].N);
-    sc.partial[g] += split_partial_bytes(proj[p].type, proj[p].N, sc.nch[p]);
+    sc.arrive[g] += xq::gemv_split_arrive_bytes(proj[p].N);
+    sc.partial[g] += xq::gemv_split_partial_bytes(proj[p].N, sc.nch[p]);
   }
   return sc;
 }
@@ -380,10 +356,9 @@ xq_status layer_matmuls(const xq_proj* proj, int n_proj, const uint8_t* const* q
         set_codebook(q, it);
       }
       if (n > 0 && (n == xq::kMaxProj || p == n_proj)) {
-        const cudaError_t e =
-            uses_tc(type) ? xq::launch_gemv_tc(items, n, s, true, counter[g], arrive[g], partial[g], first_launch)
-                          : xq::launch_gemv_mma(type, items, n, s, true, counter[g], arrive[g], partial[g], first_launch);
-        if (e != cudaSuccess) return XQ_ERR_CUDA;
+        if (xq::launch_gemv_mma(type, items, n, s, true, counter[g], arrive[g], partial[g], first_launch) !=
+            cudaSuccess)
+          return XQ_ERR_CUDA;
         first_launch = false;
         n = 0;
       }
@@ -614,12 +589,11 @@ xq_status xq_device_error(xq_stream stream, unsigned int* code_out) {
   if (!code_out) return XQ_ERR_ARG;
   *code_out = 0;
   if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return XQ_ERR_CUDA;
-  unsigned int c[3] = {0u, 0u, 0u};
+  unsigned int c[2] = {0u, 0u};
   const cudaError_t e0 = xq::take_gemv_error(&c[0]);
-  const cudaError_t e1 = xq::take_gemv_tc_error(&c[1]);
-  const cudaError_t e2 = xq::take_tile_error(&c[2]);
-  if (e0 != cudaSuccess || e1 != cudaSuccess || e2 != cudaSuccess) return XQ_ERR_CUDA;
-  for (int k = 0; k < 3; ++k)
+  const cudaError_t e1 = xq::take_tile_error(&c[1]);
+  if (e0 != cudaSuccess || e1 != cudaSuccess) return XQ_ERR_CUDA;
+  for (int k = 0; k < 2; ++k)
     if (c[k]) {
       *code_out = (static_cast<unsigned int>(k + 1) << 8) | (c[k] & 0xFFu);
       break;
@@ -644,8 +618,8 @@ xq_status xq_debug_stalled_matmul_q4k(const void* W, const void* xq, int M, int 
   q.M_total = M;
   q.chunk = 0;
   q.nch = 1;
-  const cudaError_t e = xq::launch_gemv_tc(&q, 1, reinterpret_cast<cudaStream_t>(stream), true, nullptr, nullptr,
-                                           nullptr, true, true);
+  const cudaError_t e = xq::launch_gemv_mma(XQ_TYPE_Q4_K, &q, 1, reinterpret_cast<cudaStream_t>(stream), true, nullptr,
+                                            nullptr, nullptr, true, true);
   return e == cudaSuccess ? XQ_OK : XQ_ERR_CUDA;
 }
 

@@ -82,6 +82,8 @@ struct Proj {
 struct Group {
   Proj p[kMaxProj];
   unsigned int* counter;  // dynamic task counter (zeroed before launch) or null
+  long long wait_limit;   // clocks a wait may take before it records an error and gives up
+  int stall;              // test hook: the producer issues no stage, so the consumers' first waits run out
   int n, total;
   // 0: the launch needs nothing the previous grid on the stream writes (it
   // follows another grouped launch of the same layer, whose CTAs trigger only
@@ -111,6 +113,7 @@ static_assert(kGemvCtasPerSM * (GLay<14>::kSmemBytes + 1024) <= 228 * 1024, "Q6_
 static_assert(kGemvCtasPerSM * (GLay<8>::kSmemBytes + 1024) <= 228 * 1024, "Q8_0: resident CTAs per SM");
 static_assert(kGemvCtasPerSM * (GLay<23>::kSmemBytes + 1024) <= 228 * 1024, "IQ4_XS: resident CTAs per SM");
 constexpr long long kWaitClocks = 1LL << 32;
+constexpr long long kStallWaitClocks = 100000;  // the test hook's short limit (about 50 us)
 
 __device__ __forceinline__ int mma_row(int i) { return 8 * (i >> 3) + 2 * (i & 3) + ((i >> 2) & 1); }
 
@@ -126,9 +129,10 @@ __device__ __forceinline__ int weight_box_x(int b) {
 // ---------------------------------------------------------------- PTX
 using namespace ptx;
 
-// Bounded wait: false (and an error code recorded) if the phase never completes.
-__device__ __forceinline__ bool mbar_wait(uint32_t a, unsigned parity, unsigned code) {
-  return ptx::mbar_wait(a, parity, &g_gemv_error, code, kWaitClocks);
+// Bounded wait: false (and an error code recorded) if the phase does not
+// complete within `limit` clocks.
+__device__ __forceinline__ bool mbar_wait(uint32_t a, unsigned parity, unsigned code, long long limit) {
+  return ptx::mbar_wait(a, parity, &g_gemv_error, code, limit);
 }
 
 __device__ __forceinline__ void mma16816(float (&d)[4], unsigned a0, unsigned a1, unsigned a2,
@@ -592,6 +596,11 @@ __device__ __forceinline__ void gemv_mma_body(const Group& G) {
   if (warp == kGemvWarps) {
     // ------------------------------------------------------- producer
     if (lane != 0) return;
+    if (G.stall) {
+      if (G.wait_prev) cudaGridDependencySynchronize();
+      cudaTriggerProgrammaticLaunchCompletion();
+      return;
+    }
     // Each CTA's first task is its own index; later tasks come from the
     // counter (or a stride). The weights do not depend on the previous grid
     // on the stream, so the weight boxes of the first task's first stages are
@@ -640,7 +649,7 @@ __device__ __forceinline__ void gemv_mma_body(const Group& G) {
       const int bfirst = bresume >= 0 ? bresume : tp.b0;
       bresume = -1;
       for (int b = bfirst; b < tp.b1; ++b) {
-        if (fills > 0 && !mbar_wait(empty_s + 8 * slot, (fills - 1) & 1, 1)) return;
+        if (fills > 0 && !mbar_wait(empty_s + 8 * slot, (fills - 1) & 1, 1, G.wait_limit)) return;
         meta[slot] = make_int4(valid ? task : -1, b, (b == tp.b1 - 1) ? 1 : 0, 0);
         if (!valid) {
           mbar_arrive(full_s + 8 * slot);
@@ -700,7 +709,7 @@ __device__ __forceinline__ void gemv_mma_body(const Group& G) {
     pend_p = -1;
   };
   for (;;) {
-    if (!mbar_wait(full_s + 8 * slot, fills & 1, 2)) return;
+    if (!mbar_wait(full_s + 8 * slot, fills & 1, 2, G.wait_limit)) return;
     const int4 m = meta[slot];
     if (m.x < 0) {
       resolve();
@@ -873,7 +882,7 @@ bool gemv_mma_supports(int type, int K) {
 }
 
 cudaError_t launch_gemv_mma(int type, const MmaProj* projs, int n, cudaStream_t s, bool pdl, unsigned int* counter,
-                            uint8_t* arrive_ws, uint8_t* partial_ws, bool wait_prev) {
+                            uint8_t* arrive_ws, uint8_t* partial_ws, bool wait_prev, bool stall_test) {
   if (n <= 0 || n > kMaxProj || (type != 12 && type != 14 && type != 8 && type != 23)) return cudaErrorInvalidValue;
   // Per-projection K-chunking (only with split workspaces) and task cost.
   const bool split = arrive_ws != nullptr && partial_ws != nullptr;
@@ -907,6 +916,8 @@ cudaError_t launch_gemv_mma(int type, const MmaProj* projs, int n, cudaStream_t 
   G.n = n;
   G.counter = counter;
   G.wait_prev = (wait_prev || !pdl) ? 1 : 0;
+  G.stall = stall_test ? 1 : 0;
+  G.wait_limit = stall_test ? kStallWaitClocks : kWaitClocks;
   int total = 0;
   bool isum = false;
   for (int k = 0; k < n; ++k) {

@@ -37,7 +37,7 @@ struct QuantItem {
   const float* up;  // non-null: quantize h = silu(x) * up
   float* h_out;     // optional copy of h
   uint8_t* xq;
-  size_t d8, s8, frag, fsc, tile, tcb;  // byte offsets in xq (layout in xq_common.cuh); tcb 0 if absent
+  size_t d8, s8, frag, fsc, tile;  // byte offsets in xq (layout in xq_common.cuh)
   int M, K, nsub, ttiles;
 };
 
@@ -139,15 +139,6 @@ quantize_q8_kernel(const __grid_constant__ QuantGroup G) {
         fsc[base + (n & 1)] = d;
         fsc[base + 2 + (n & 1)] = s;
       }
-      if (L.tcb) {
-        // tensor-memory GEMV operand (M <= 8, so c = 0): slice 2*(j%8) + h of
-        // super-block j/8, the lane's k-slot s inside its 16-slot half h
-        const int h = lane >> 4, l16 = lane & 15, u = l16 & 3;
-        const int s16 = (l16 & ~3) | ((u == 1 || u == 2) ? (u ^ 3) : u);
-        uint8_t* dst = J.xq + L.tcb + (static_cast<size_t>(j >> 3) * 16 + 2 * (j & 7) + h) * 256 + (s16 >> 3) * 128 +
-                       n * 16 + (s16 & 7) * 2;
-        *reinterpret_cast<__half*>(dst) = __int2half_rn(q);
-      }
     } else {
       // tile image: token r of tile tt, 32-block j = 8b + ib
       const int tt = m >> 7, r = m & 127, b = j >> 3, ib = j & 7;
@@ -195,7 +186,6 @@ cudaError_t launch_quantize_q8(const QuantJob* jobs, int n, cudaStream_t s, bool
     it.frag = L.frag;
     it.fsc = L.fsc;
     it.tile = L.tile;
-    it.tcb = L.tcb;
     it.M = q.M;
     it.K = q.K;
     it.nsub = q.K / 32;

@@ -85,13 +85,6 @@ __device__ __forceinline__ float half_bits_to_float(unsigned bits16) {
 // perm = 0,2,1,3,4,6,5,7; fsc[c][j][t] = (d8[8c+2t][j], d8[8c+2t+1][j],
 // s8[8c+2t][j], s8[8c+2t+1][j]). Tokens past M in the last chunk are zero.
 //
-// M <= 8 only, after fsc: the B operand of the tensor-memory GEMV
-//   tcb  fp16 [K/256][16 slices][2][8][8]  at F + 18*K
-// Slice i = 2*jj + h of super-block b holds k-slots 16h .. 16h+15 of its
-// 32-block jj (feature 256b + 32jj + 16h + 4(s/4) + pr[s%4] in slot s,
-// pr = 0,2,1,3) for tokens n = 0..7 as two 8x8 K-major core matrices: slot
-// s of token n at byte (s/8)*128 + n*16 + (s%8)*2. Tokens past M are zero.
-//
 // M > kGemvMaxTokens (tensor-memory tile kernel), T = ceil(M/128) token tiles:
 //   tile [T][K/256] records of kTileRecord bytes at F. Record (t, b) holds,
 //   for the 128 tokens 128t .. 128t+127 and super-block b:
@@ -111,11 +104,8 @@ constexpr int kTileItemOp = 8192;                         // 128 tokens x 32 slo
 constexpr int kTileItem = kTileItemOp + 4 * kTileTokens;  // 8704
 constexpr int kTileRecord = 8 * kTileItem + kTileItemOp;  // 77824
 
-constexpr int kTcImgSb = 16 * 256;  // tcb bytes per super-block (8 tokens)
-
 struct Q8Layout {
   size_t qs, d8, s8, frag, fsc, tile, total;
-  size_t tcb;  // the tensor-memory GEMV's B operand (M <= 8, standard layout), else 0
   int chunks;  // 8-token chunks of the GEMV image (M <= kGemvMaxTokens), else 0
   int ttiles;  // 128-token tiles of the tile image (M > kGemvMaxTokens), else 0
 };
@@ -143,16 +133,10 @@ __host__ __device__ inline Q8Layout q8_layout(int M, int K, bool gemv_image = fa
     L.frag = F;
     L.fsc = L.frag + static_cast<size_t>(L.chunks) * 16 * K;
     L.tile = L.total = L.fsc + static_cast<size_t>(L.chunks) * 2 * K;
-    L.tcb = 0;
-    if (M >= 1 && M <= 8 && !gemv_image && (K & 255) == 0) {
-      L.tcb = L.total;
-      L.tile = L.total = L.tcb + static_cast<size_t>(K / 256) * kTcImgSb;
-    }
   } else {
     L.chunks = 0;
     L.ttiles = (M + kTileTokens - 1) / kTileTokens;
     L.frag = L.fsc = L.tile = F;
-    L.tcb = 0;
     L.total = F + static_cast<size_t>(L.ttiles) * (K / 256) * kTileRecord;
   }
   return L;
@@ -227,18 +211,6 @@ __host__ __device__ inline size_t gemv_split_arrive_bytes(int N) {
   return ((static_cast<size_t>(gemv_row_blocks(N)) * kGemvWarps * 4) + 255) & ~static_cast<size_t>(255);
 }
 
-// Tensor-memory GEMV (M <= 8, Q4_K): tasks of kTcRows weight rows (the TMEM
-// lanes); split workspaces of partial sums [nch][8][rows padded to kTcRows]
-// and one arrival count per 32-row group (both rounded to 256 bytes).
-constexpr int kTcRows = 128;
-__host__ __device__ inline int tc_row_blocks(int N) { return (N + kTcRows - 1) / kTcRows; }
-__host__ __device__ inline size_t tc_split_partial_bytes(int N, int nch) {
-  return ((static_cast<size_t>(nch) * 8 * tc_row_blocks(N) * kTcRows * 4) + 255) & ~static_cast<size_t>(255);
-}
-__host__ __device__ inline size_t tc_split_arrive_bytes(int N) {
-  return ((static_cast<size_t>(tc_row_blocks(N)) * 4 * 4) + 255) & ~static_cast<size_t>(255);
-}
-
 // Whether the tensor-core GEMV takes this weight: every Q4_K shape; Q6_K
 // when its rows are 16-byte multiples (K/256 a multiple of 8), which the
 // tensor map needs.
@@ -251,25 +223,16 @@ bool gemv_mma_supports(int type, int K);
 // split workspace (arrival counts, zeroed before the first use, at arrive_ws;
 // partial sums at partial_ws; sizes from the gemv_split_* helpers in item
 // order) long rows are split into K-chunks across CTAs.
+// stall_test (a test hook): the producer issues no stage and every wait is
+// limited to about 10^5 clocks, so the consumers' first waits run out,
+// record their error code and return; y is left unwritten.
 cudaError_t launch_gemv_mma(int type, const MmaProj* projs, int n, cudaStream_t s, bool pdl,
                             unsigned int* counter = nullptr, uint8_t* arrive_ws = nullptr,
-                            uint8_t* partial_ws = nullptr, bool wait_prev = true);
-
-// One launch of the tensor-memory GEMV for up to kMaxProj Q4_K projections of
-// M_total <= 8 tokens (chunk 0, the standard layout with its tcb region),
-// with the same counter and split-workspace conventions as launch_gemv_mma
-// (sizes from the tc_split_* helpers, in item order).
-// stall_test (a test hook): the producer issues no stage and every wait is
-// limited to about 10^5 clocks, so the consumers' first waits run out, record
-// their error code and return; y is left unwritten.
-cudaError_t launch_gemv_tc(const MmaProj* projs, int n, cudaStream_t s, bool pdl, unsigned int* counter = nullptr,
-                           uint8_t* arrive_ws = nullptr, uint8_t* partial_ws = nullptr, bool wait_prev = true,
-                           bool stall_test = false);
+                            uint8_t* partial_ws = nullptr, bool wait_prev = true, bool stall_test = false);
 
 // Read and clear the error word each waiting kernel sets when a bounded wait
 // runs out (0: none since the last read). Synchronous device reads/writes.
 cudaError_t take_gemv_error(unsigned int* code);
-cudaError_t take_gemv_tc_error(unsigned int* code);
 cudaError_t take_tile_error(unsigned int* code);
 
 // 2D tensor map (no interleave, no swizzle, zero fill): dims {dim0, dim1}

@@ -251,7 +251,7 @@ def device_error(stream=None) -> int:
 
 
 def debug_stalled_matmul_q4k(W, xq, M: int, N: int, K: int, y, stream=None):
-    """Test hook: the Q4_K tensor-memory GEMV with no stage issued and short
+    """Test hook: the Q4_K warp-level MMA GEMV with no stage issued and short
     waits, so that its waits run out (y stays unwritten)."""
     _check("xq_debug_stalled_matmul_q4k",
            lib().xq_debug_stalled_matmul_q4k(_ptr(W), _ptr(xq), M, N, K, _ptr(y), _stream(stream)))

@@ -300,19 +300,20 @@ XQ_API xq_status xq_layer_mixed_static(const xq_proj *proj, int n_proj,
  * unwritten although the call that launched it already returned XQ_OK.
  * xq_device_error waits until `stream` is idle, then reads and clears those
  * words. *code_out = 0 if no wait ran out since the last read, else
- * (kernel << 8) | wait: kernel 1 = the warp-level MMA GEMV, 2 = the
- * tensor-memory GEMV (Q4_K, M <= 8), 3 = the tile kernel (M > 64); wait = the
- * kernel's number of the wait that gave up. If several kernels recorded one,
+ * (kernel << 8) | wait: kernel 1 = the warp-level MMA GEMV (M <= 64), 2 =
+ * the tile kernel (M > 64); wait = the kernel's number of the wait that gave
+ * up (GEMV: 1 the producer waiting for a free stage, 2 a consumer waiting for
+ * a full one). If several kernels recorded one,
  * the lowest kernel number is reported and all are cleared. The reads and
  * writes are synchronous. XQ_ERR_ARG for a null code_out, XQ_ERR_CUDA if the
  * stream or the reads fail. */
 XQ_API xq_status xq_device_error(xq_stream stream, unsigned int *code_out);
 
-/* Test hook for the failure detection above: the Q4_K tensor-memory GEMV
+/* Test hook for the failure detection above: the Q4_K warp-level MMA GEMV
  * (1 <= M <= 8) launched with its producer issuing no stage and every wait
- * limited to about 10^5 clocks, so that the other roles' first waits run out
- * and record their codes; y is left unwritten and xq_device_error then
- * reports kernel 2. Arguments and errors as xq_matmul_q4k_q8. */
+ * limited to about 10^5 clocks, so that the consumers' first waits run out
+ * and record their code; y is left unwritten and xq_device_error then
+ * reports kernel 1, wait 2. Arguments and errors as xq_matmul_q4k_q8. */
 XQ_API xq_status xq_debug_stalled_matmul_q4k(const void *W, const void *xq, int M, int N, int K, float *y,
                                              xq_stream stream);
 

@@ -40,10 +40,6 @@ def test_sizes(L):
     from gguf_quant_integer_gb300 import xq
     def layout(M, K):
         base = -(-int(1.25 * M * K) // 256) * 256
-        if 1 <= M <= 8 and K % 256 == 0:
-            # GEMV operand image (18 bytes per feature) and the tensor-memory
-            # GEMV's B operand (4096 bytes per super-block)
-            return base + 18 * K + 16 * K
         if M <= 64:  # GEMV operand image: 18 bytes per feature per 8-token chunk
             return base + 18 * K * (-(-M // 8))
         # tile image: one 77,824-byte record per 128-token tile and super-block
@@ -209,25 +205,6 @@ def test_layer_workspace_for_chunked_split(L):
     # above 64 tokens (the tile kernel) there is no split state
     q8 = r256(xq.q8_bytes(80, 4096)) + r256(xq.q8_bytes(80, 14336))
     assert L.xq_layer_workspace_bytes(arr, 2, 2, 80) == q8 + 4 * 256
-
-
-def test_layer_workspace_for_tensor_memory_gemv_split(L):
-    """M <= 8: the Q4_K projections go to the tensor-memory GEMV (128-row
-    tasks); a row longer than 24 super-blocks is split over K with one arrival
-    count per 32-row group and partial sums [nch][8][rows padded to 128]."""
-    from gguf_quant_integer_gb300 import xq
-
-    def r256(b):
-        return -(-b // 256) * 256
-
-    # Llama-3-8B-shaped layer: 432 tasks of 128 rows, down in 4 chunks of 14
-    specs = [(12, 4096, 4096, 0), (12, 1024, 4096, 0), (12, 1024, 4096, 0), (12, 4096, 4096, 1),
-             (12, 14336, 4096, 2), (12, 14336, 4096, 2), (12, 4096, 14336, 3)]
-    arr = xq._proj_array([(t, n, k, None, None, i) for (t, n, k, i) in specs])
-    for M in (1, 8):
-        q8 = 3 * r256(xq.q8_bytes(M, 4096)) + r256(xq.q8_bytes(M, 14336))
-        want = q8 + 4 * 256 + r256(32 * 4 * 4) + r256(4 * 8 * 4096 * 4)
-        assert L.xq_layer_workspace_bytes(arr, 7, 4, M) == want, M
 
 
 def test_failure_detection_entry_points_reject_before_launch(L):
