@@ -585,6 +585,24 @@ xq_status xq_layer_mixed(const xq_proj* proj, int n_proj, const float* const* in
   return layer_matmuls(proj, n_proj, q8, M, sc, ws + sched_off, s);
 }
 
+xq_status xq_debug_tile_sums(int type, const void* W, const int8_t* codebook, const void* xq, int M, int N, int K,
+                             float* y, int32_t* sums, xq_stream stream) {
+  if (block_bytes(type) == 0) return XQ_ERR_ARG;
+  xq_status st = check_shape(M, N, K);
+  if (st != XQ_OK) return st;
+  if (M <= xq::kGemvMaxTokens) return XQ_ERR_UNSUPPORTED;  // the tile kernel serves M > 64
+  if (type == XQ_TYPE_IQ4_XS && (K % 512) != 0) return XQ_ERR_SHAPE;
+  if (N == 0) return XQ_OK;
+  if (!W || !xq || !y || !sums || (type == XQ_TYPE_IQ4_XS && !codebook)) return XQ_ERR_ARG;
+  if (!aligned16(W) || !aligned16(xq) || !aligned16(y) || !aligned16(sums)) return XQ_ERR_ALIGN;
+  uint32_t cb[4];
+  if (type == XQ_TYPE_IQ4_XS) pack_codebook(codebook, cb);
+  const cudaError_t e =
+      xq::launch_tile_mma(type, static_cast<const uint8_t*>(W), static_cast<const uint8_t*>(xq), M, N, K, y,
+                          reinterpret_cast<cudaStream_t>(stream), true, type == XQ_TYPE_IQ4_XS ? cb : nullptr, sums);
+  return e == cudaSuccess ? XQ_OK : XQ_ERR_CUDA;
+}
+
 xq_status xq_device_error(xq_stream stream, unsigned int* code_out) {
   if (!code_out) return XQ_ERR_ARG;
   *code_out = 0;

@@ -130,6 +130,7 @@ struct TileArgs {
   const uint8_t* W;
   const uint8_t* img;          // tile image of the Q8 buffer
   float* y;                    // [M][N]
+  int32_t* sums;               // test hook: [M][N][K/32] per-32-block integer sums, or null
   unsigned long long w_bytes;  // N * row_bytes
   int N, K, M, nsb, row_bytes, ttiles;
   uint32_t cb[4];              // IQ4_XS: codebook bytes with their sign bits flipped
@@ -199,7 +200,7 @@ __device__ __forceinline__ void store_row(uint8_t* op, int r, const uint32_t (&v
     *reinterpret_cast<uint4*>(p + q * 128) = make_uint4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
 }
 
-template <int TYPE>
+template <int TYPE, bool SUMS>
 __global__ void __launch_bounds__(kThreads, 1) tile_mma_kernel(const __grid_constant__ TileArgs A) {
   using F = Fmt<TYPE>;
   using S = Smem<TYPE>;
@@ -655,6 +656,23 @@ __global__ void __launch_bounds__(kThreads, 1) tile_mma_kernel(const __grid_cons
             tmem_ld16(dcol + 16 * c, v);
             tmem_ld16(dcol + 16 * c + 16, w);
             tmem_wait_ld();
+            if (SUMS && m < A.M) {
+              // test hook: the 32-block's exact integer (Q4_K sc*isum, from
+              // the operand's 2^-14 scale; Q6_K and IQ4_XS scale*isum summed
+              // over the block's groups; Q8_0 isum)
+              const int nsub = A.K >> 5;
+              const float sc = TYPE == 12 ? 16384.0f : 1.0f;
+#pragma unroll
+              for (int e = 0; e < 16; ++e) {
+                const int n1 = n0 + 16 * c + e, n2 = n1 + 16;
+                if (n1 < A.N)
+                  A.sums[(static_cast<size_t>(m) * A.N + n1) * nsub + 8 * b + it] =
+                      static_cast<int32_t>(__uint_as_float(v[e]) * sc);
+                if (n2 < A.N)
+                  A.sums[(static_cast<size_t>(m) * A.N + n2) * nsub + 8 * b + it] =
+                      static_cast<int32_t>(__uint_as_float(w[e]) * sc);
+              }
+            }
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
               f2 s0 = d82, s1 = d82;
@@ -737,12 +755,12 @@ __global__ void __launch_bounds__(kThreads, 1) tile_mma_kernel(const __grid_cons
   }
 }
 
-template <int TYPE>
+template <int TYPE, bool SUMS>
 cudaError_t launch_tile(const TileArgs& A, int grid, cudaStream_t s, bool pdl) {
   static bool smem_set = false;
   if (!smem_set) {
-    const cudaError_t e =
-        cudaFuncSetAttribute(tile_mma_kernel<TYPE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes<TYPE>());
+    const cudaError_t e = cudaFuncSetAttribute(tile_mma_kernel<TYPE, SUMS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               smem_bytes<TYPE>());
     if (e != cudaSuccess) return e;
     smem_set = true;
   }
@@ -756,7 +774,7 @@ cudaError_t launch_tile(const TileArgs& A, int grid, cudaStream_t s, bool pdl) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, tile_mma_kernel<TYPE>, A);
+  return cudaLaunchKernelEx(&cfg, tile_mma_kernel<TYPE, SUMS>, A);
 }
 
 }  // namespace
@@ -770,7 +788,7 @@ cudaError_t take_tile_error(unsigned int* code) {
 }
 
 cudaError_t launch_tile_mma(int type, const uint8_t* W, const uint8_t* xq, int M, int N, int K, float* y,
-                            cudaStream_t s, bool pdl, const uint32_t* codebook) {
+                            cudaStream_t s, bool pdl, const uint32_t* codebook, int32_t* sums) {
   if (M <= kGemvMaxTokens || N <= 0 || K <= 0 || (K & 255) != 0 ||
       (type != 12 && type != 14 && type != 23 && type != 8))
     return cudaErrorInvalidValue;
@@ -780,6 +798,7 @@ cudaError_t launch_tile_mma(int type, const uint8_t* W, const uint8_t* xq, int M
   A.W = W;
   A.img = xq + L.tile;
   A.y = y;
+  A.sums = sums;
   A.N = N;
   A.K = K;
   A.M = M;
@@ -793,21 +812,21 @@ cudaError_t launch_tile_mma(int type, const uint8_t* W, const uint8_t* xq, int M
     if (!encode_tma_2d(&A.map, CU_TENSOR_MAP_DATA_TYPE_UINT64, W, A.row_bytes / 8, static_cast<unsigned long long>(N),
                        A.row_bytes, kQ4kBytes / 8, kRows))
       return cudaErrorInvalidValue;
-    return launch_tile<12>(A, grid, s, pdl);
+    return sums ? launch_tile<12, true>(A, grid, s, pdl) : launch_tile<12, false>(A, grid, s, pdl);
   }
   if (type == 23) {
     if (!encode_tma_2d(&A.map, CU_TENSOR_MAP_DATA_TYPE_UINT8, W, A.row_bytes, static_cast<unsigned long long>(N),
                        A.row_bytes, Fmt<23>::kRawRow, kRows))
       return cudaErrorInvalidValue;
-    return launch_tile<23>(A, grid, s, pdl);
+    return sums ? launch_tile<23, true>(A, grid, s, pdl) : launch_tile<23, false>(A, grid, s, pdl);
   }
   if (type == 8) {
     if (!encode_tma_2d(&A.map, CU_TENSOR_MAP_DATA_TYPE_UINT64, W, A.row_bytes / 8, static_cast<unsigned long long>(N),
                        A.row_bytes, kQ80Group / 8, kRows))
       return cudaErrorInvalidValue;
-    return launch_tile<8>(A, grid, s, pdl);
+    return sums ? launch_tile<8, true>(A, grid, s, pdl) : launch_tile<8, false>(A, grid, s, pdl);
   }
-  return launch_tile<14>(A, grid, s, pdl);
+  return sums ? launch_tile<14, true>(A, grid, s, pdl) : launch_tile<14, false>(A, grid, s, pdl);
 }
 
 }  // namespace xq

@@ -245,8 +245,11 @@ bool encode_tma_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, u
 // (Q4_K), 14 (Q6_K), 8 (Q8_0) or 23 (IQ4_XS, with its codebook as 4
 // little-endian words; K a multiple of 512), xq the Q8 buffer of M tokens
 // (tile image present).
+// sums (test hook, or null): [M][N][K/32] int32, each 32-block's exact
+// integer as the kernel accumulates it (Q4_K sc_j * isum_j; Q6_K
+// s_2p * isum_2p + s_2p+1 * isum_2p+1; Q8_0 isum_j; IQ4_XS (ls_j - 32) * isum_j).
 cudaError_t launch_tile_mma(int type, const uint8_t* W, const uint8_t* xq, int M, int N, int K, float* y,
-                            cudaStream_t s, bool pdl, const uint32_t* codebook = nullptr);
+                            cudaStream_t s, bool pdl, const uint32_t* codebook = nullptr, int32_t* sums = nullptr);
 cudaError_t launch_gemv_q6k(const GemvArgs& a, cudaStream_t s);
 
 }  // namespace xq

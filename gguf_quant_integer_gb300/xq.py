@@ -30,7 +30,7 @@ SYMBOLS = ("xq_status_str", "xq_q8_bytes", "xq_weight_bytes", "xq_quantize_q8",
            "xq_q8_bytes_invariant", "xq_quantize_q8_invariant", "xq_matmul_invariant",
            "xq_matmul_q8_0_q8", "xq_debug_isums_q8_0", "xq_silu_mul_quantize_q8",
            "xq_layer_ffn_workspace_bytes", "xq_layer_mixed_ffn", "xq_matmul_iq4xs_q8",
-           "xq_debug_isums_iq4xs", "xq_device_error", "xq_debug_stalled_matmul_q4k")
+           "xq_debug_isums_iq4xs", "xq_device_error", "xq_debug_stalled_matmul_q4k", "xq_debug_tile_sums")
 
 
 class XQError(RuntimeError):
@@ -91,6 +91,8 @@ def lib(path: str | None = None):
     L.xq_device_error.restype = I
     L.xq_debug_stalled_matmul_q4k.argtypes = [P, P, I, I, I, P, P]
     L.xq_debug_stalled_matmul_q4k.restype = I
+    L.xq_debug_tile_sums.argtypes = [I, P, P, P, I, I, I, P, P, P]
+    L.xq_debug_tile_sums.restype = I
     L.xq_layer_workspace_bytes.argtypes = [ctypes.POINTER(xq_proj), I, I, I]
     L.xq_layer_workspace_bytes.restype = S
     L.xq_layer_mixed.argtypes = [ctypes.POINTER(xq_proj), I, ctypes.POINTER(ctypes.c_void_p), I, I, P, S, P]
@@ -255,6 +257,20 @@ def debug_stalled_matmul_q4k(W, xq, M: int, N: int, K: int, y, stream=None):
     waits, so that its waits run out (y stays unwritten)."""
     _check("xq_debug_stalled_matmul_q4k",
            lib().xq_debug_stalled_matmul_q4k(_ptr(W), _ptr(xq), M, N, K, _ptr(y), _stream(stream)))
+
+
+def debug_tile_sums(qtype: int, W, xq, M: int, N: int, K: int, codebook=None, y=None, sums=None, stream=None):
+    """Tile-kernel matmul (M > 64) that also writes each 32-block's exact
+    integer as the kernel accumulates it, int32 [M, N, K/32] (test hook)."""
+    import torch
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float32, device=W.device)
+    if sums is None:
+        sums = torch.empty((M, N, K // 32), dtype=torch.int32, device=W.device)
+    cb = _codebook(codebook) if codebook is not None else None
+    _check("xq_debug_tile_sums", lib().xq_debug_tile_sums(qtype, _ptr(W), cb.ctypes.data if cb is not None else None,
+                                                         _ptr(xq), M, N, K, _ptr(y), _ptr(sums), _stream(stream)))
+    return y, sums
 
 
 def _proj_array(projs):

@@ -334,6 +334,19 @@ XQ_API xq_status xq_debug_isums_q8_0(const void *W, const void *xq, int M, int N
 XQ_API xq_status xq_debug_isums_iq4xs(const void *W, const int8_t *codebook, const void *xq, int M,
                                int N, int K, float *y, int32_t *isum, xq_stream stream);
 
+/* Test hook of the tile kernel (M > 64): the same launch as the matmul of
+ * `type` (8, 12, 14 or 23; IQ4_XS with its codebook, K a multiple of 512),
+ * writing y and, into sums int32 [M][N][K/32], each 32-block's exact integer
+ * as the kernel accumulates it before any scale is applied:
+ *   Q4_K   sc_j * isum_j              (the 6-bit scale is folded into the operand)
+ *   Q6_K   s_2p * isum_2p + s_2p+1 * isum_2p+1   (both 16-weight groups)
+ *   Q8_0   isum_j
+ *   IQ4_XS (ls_j - 32) * isum_j
+ * with isum the integer sub-block sums of xq_debug_isums_*. XQ_ERR_UNSUPPORTED
+ * for M <= 64 (those token counts run the GEMV, whose hooks are above). */
+XQ_API xq_status xq_debug_tile_sums(int type, const void *W, const int8_t *codebook, const void *xq, int M,
+                                    int N, int K, float *y, int32_t *sums, xq_stream stream);
+
 #ifdef __cplusplus
 }
 #endif
