@@ -50,7 +50,7 @@ HEADLINE = "llama3-8b-32layer"
 METRIC = "Q4_K/Q6_K x Q8 matmul weight GB/s (M=%d) and %% of GB300 HBM roofline"
 # workloads --profile-workload runs (one launch per call)
 PROFILE_WORKLOADS = ("prefill512-up", "prefill512-down", "qwen3-q6k-layer", "llama3-layer", "iq4xs-ffn-up",
-                     "q8_0-qwen25-layer")
+                     "q8_0-qwen25-layer", "qwen25-layer")
 
 
 def parse_args(argv=None):
@@ -874,7 +874,7 @@ def profile_workload(args):
         y = torch.empty((M, N), dtype=torch.float32, device=device)
         run = lambda: xq.matmul_iq4xs_q8(W, cb, buf, M, N, K, y=y)
     else:
-        wl = synth.WORKLOADS[{"qwen3-q6k-layer": "qwen3-8b-mixed-layer",
+        wl = synth.WORKLOADS[{"qwen3-q6k-layer": "qwen3-8b-mixed-layer", "qwen25-layer": "qwen2.5-1.5b-layer",
                               "q8_0-qwen25-layer": "qwen2.5-1.5b-q8_0-layer"}.get(name, "llama3-8b-32layer")]
         keep = [t for t, p in enumerate(wl.projs) if name != "qwen3-q6k-layer" or p.qtype == synth.Q6_K]
         M = args.m
