@@ -76,6 +76,9 @@ struct Proj {
   float* partial;      // split: [nch][8][kGemvRows * row blocks]
   unsigned int* arrive;  // split: one arrival count per 16-row group
   uint32_t cb[4];        // IQ4_XS: codebook bytes with their sign bits flipped
+  const uint8_t* aq;     // small-M form: int8 quants [M][K] of the Q8 buffer
+  const float* ad8;      // small-M form: d8 [M][K/32]
+  const float* as8;      // small-M form: s8 [M][K/32]
   int N, K, M, task0, nch;
 };
 
@@ -568,13 +571,245 @@ __device__ __forceinline__ int next_task(const Group& G, int cur) {
   return cur + static_cast<int>(gridDim.x);
 }
 
-template <int TYPE, bool ISUM>
+// ------------------------------------------------- small-M (M <= 2) form
+//
+// At one or two tokens the m16n8k16 MMA uses 1/8 or 2/8 of its columns but
+// still pays the full fp16 unpack of every weight. The small form keeps the
+// producer, ring, tasks and K-split of the grouped GEMV and replaces the
+// consumer arithmetic with exact integer dot products on the CUDA cores
+// (dp4a: four unsigned nibbles times four signed int8 activations):
+//   - a stage holds, besides the weight boxes, each token's 256 int8
+//     quants, 8 d8 and 8 s8 of the super-block (plain Q8 buffer regions,
+//     bulk-copied), not the 8-token fp16 operand image;
+//   - lane l of a consumer warp takes weight row l/2 of the warp's 16 and
+//     half l%2 of the super-block (quant bytes 64h..64h+63: sub-blocks
+//     4h..4h+3) and forms each sub-block's isum with 8 dp4a per token.
+// The fp32 arithmetic is the MMA consumer's, operation for operation, so the
+// two forms give bit-identical y (batch invariance across M holds):
+//   - the dp4a accumulator starts at the bit pattern of 0.75f (low nibbles)
+//     or 12.0f (high nibbles); the int32 result is that float plus isum
+//     units in the last place, which are 2^-24 and 2^-20 there, so
+//     subtracting the float leaves exactly the MMA's D (isum * 2^-24, or
+//     isum * 2^-20 for the in-place high nibble); |isum| <= 15*127*32 < 2^22
+//     keeps the sum inside the float's binade;
+//   - the coefficients carry the same 2^24 / 2^20 factors as
+//     decode_scales_q4, and each sub-block adds
+//     fma(RN(a*d8), D, fma(-dmin*m, s8, acc)) as compute_block_q4 does;
+//   - a super-block's eight terms go into its fresh accumulator in sub-block
+//     order: half 0 adds sub-blocks 0..3 from zero, passes the result to
+//     half 1 (one shuffle), which adds 4..7; the running sum and total then
+//     follow the MMA consumer, and half 1 stores.
+// Only Q4_K takes it, at M <= 2 outside the batch-invariant entry points
+// (whose activations are the 8-token operand image).
+
+template <bool SMALL>
+__device__ __forceinline__ unsigned act_bytes(const Proj& P) {
+  return SMALL ? 320u * static_cast<unsigned>(P.M) : 8u * 512u + 8u * 64u;
+}
+
+// The activation part of a stage for super-block b: the operand image (fp16
+// fragments and scale quads), or in the small form each token's quants
+// (256 bytes at +256m), d8 (32 bytes at +512+32m) and s8 (at +576+32m).
+template <int TYPE, bool SMALL>
+__device__ __forceinline__ void act_load(uint32_t st, const Proj& P, int b, uint32_t bar) {
+  constexpr int kFragOff = GLay<TYPE>::kFragOff, kFscOff = GLay<TYPE>::kFscOff;
+  if (SMALL) {
+    const int nsub = P.K >> 5;
+    for (int m = 0; m < P.M; ++m) {
+      bulk_load(st + kFragOff + 256 * m, P.aq + static_cast<size_t>(m) * P.K + 256 * static_cast<size_t>(b), 256, bar);
+      bulk_load(st + kFragOff + 512 + 32 * m, P.ad8 + static_cast<size_t>(m) * nsub + 8 * b, 32, bar);
+      bulk_load(st + kFragOff + 576 + 32 * m, P.as8 + static_cast<size_t>(m) * nsub + 8 * b, 32, bar);
+    }
+  } else {
+    bulk_load(st + kFragOff, P.frag + static_cast<size_t>(b) * 8 * 512, 8 * 512, bar);
+    bulk_load(st + kFscOff, P.fsc + static_cast<size_t>(b) * 8 * 64, 8 * 64, bar);
+  }
+}
+
+constexpr int kMagicLo = 0x3F400000;  // 0.75f: unit in the last place 2^-24
+constexpr int kMagicHi = 0x41400000;  // 12.0f: unit in the last place 2^-20
+
+// One super-block of the lane's row (small form): acc[m] = the super-block's
+// fresh accumulator for token m < P.M, complete in the lanes of half 1.
+template <bool ISUM>
+__device__ __forceinline__ void compute_small_q4(const uint8_t* blk, const uint8_t* act, const Proj& P, int row, int b,
+                                                 int r, int h, int lane, float (&acc)[2]) {
+  const uint8_t* rp = blk + r * kQ4kBytes;
+  const uint4 hd = *reinterpret_cast<const uint4*>(rp);
+  const uint4* qp = reinterpret_cast<const uint4*>(rp + 16 + 64 * h);
+  const uint4 q0 = qp[0], q1 = qp[1], q2 = qp[2], q3 = qp[3];
+  const uint32_t w[16] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w,
+                          q2.x, q2.y, q2.z, q2.w, q3.x, q3.y, q3.z, q3.w};
+  // (sc, m) of sub-blocks 4h..4h+3 (public Q4_K packing) and the MMA form's
+  // coefficients: a = d*sc*2^24 (even sub-blocks) or d*sc*2^20 (odd), and
+  // -dmin*m, each an exact product
+  const unsigned scw = h ? ((hd.w & 0x0F0F0F0Fu) | ((hd.y >> 2) & 0x30303030u)) : (hd.y & 0x3F3F3F3Fu);
+  const unsigned mnw = h ? (((hd.w >> 4) & 0x0F0F0F0Fu) | ((hd.z >> 2) & 0x30303030u)) : (hd.z & 0x3F3F3F3Fu);
+  const float d = half_bits_to_float(hd.x);
+  const float dl = d * 16777216.0f, dh = d * 1048576.0f;
+  const float dm = -half_bits_to_float(hd.x >> 16);
+  const float cl = -8388608.0f * dl, ch = -8388608.0f * dh, cm = -8388608.0f * dm;
+  float al[4], be[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    al[k] = (k & 1) ? fmaf(byte_plus_2p23(scw, k), dh, ch) : fmaf(byte_plus_2p23(scw, k), dl, cl);
+    be[k] = fmaf(byte_plus_2p23(mnw, k), dm, cm);
+  }
+  // sub-block 4h+k: group k/2 of the lane's 64 bytes, low nibbles for even k
+  uint32_t nib[4][8];
+#pragma unroll
+  for (int k = 0; k < 4; ++k)
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const uint32_t x = w[8 * (k >> 1) + i];
+      nib[k][i] = ((k & 1) ? (x >> 4) : x) & 0x0F0F0F0Fu;
+    }
+  const int nsub = P.K >> 5;
+#pragma unroll
+  for (int m = 0; m < 2; ++m) {
+    if (m < P.M) {
+      const uint4* ap = reinterpret_cast<const uint4*>(act + 256 * m + 128 * h);
+      const float4 dv = *reinterpret_cast<const float4*>(act + 512 + 32 * m + 16 * h);
+      const float4 sv = *reinterpret_cast<const float4*>(act + 576 + 32 * m + 16 * h);
+      const float d8[4] = {dv.x, dv.y, dv.z, dv.w}, s8[4] = {sv.x, sv.y, sv.z, sv.w};
+      float D[4], cf[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const uint4 a0 = ap[2 * k], a1 = ap[2 * k + 1];
+        const int magic = (k & 1) ? kMagicHi : kMagicLo;
+        int v = dp4a_us(nib[k][0], a0.x, magic);
+        v = dp4a_us(nib[k][1], a0.y, v);
+        v = dp4a_us(nib[k][2], a0.z, v);
+        v = dp4a_us(nib[k][3], a0.w, v);
+        v = dp4a_us(nib[k][4], a1.x, v);
+        v = dp4a_us(nib[k][5], a1.y, v);
+        v = dp4a_us(nib[k][6], a1.z, v);
+        v = dp4a_us(nib[k][7], a1.w, v);
+        if (ISUM && row < P.N)
+          P.isum[(static_cast<size_t>(m) * P.N + row) * nsub + 8 * b + 4 * h + k] = v - magic;
+        D[k] = __int_as_float(v) - ((k & 1) ? 12.0f : 0.75f);
+        cf[k] = al[k] * d8[k];
+      }
+      // sub-blocks 0..3 from zero (half 0), then 4..7 from half 0's result
+      float c = 0.0f;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) c = fmaf(cf[k], D[k], fmaf(be[k], s8[k], c));
+      const float c0 = __shfl_sync(0xffffffffu, c, lane & ~1);
+      if (h) {
+        c = c0;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) c = fmaf(cf[k], D[k], fmaf(be[k], s8[k], c));
+      }
+      acc[m] = c;
+    }
+  }
+}
+
+// The last warp to finish a split 16-row group (small form): lane 2r+1 adds
+// row r's chunk partials in chunk order (as reduce_chunks does).
+__device__ __forceinline__ void reduce_chunks_small(const Proj& P, int rg, int r, int h) {
+  const int rows_pad = gemv_row_blocks(P.N) * kGemvRows;
+  const int row = rg * 16 + r;
+  if (h == 0 || row >= P.N) return;
+  for (int m = 0; m < P.M; ++m) {
+    float v = 0.0f;
+    for (int c = 0; c < P.nch; ++c) v += __ldcg(P.partial + (static_cast<size_t>(c) * 8 + m) * rows_pad + row);
+    P.y[static_cast<size_t>(m) * P.N + row] = v;
+  }
+}
+
+__device__ __forceinline__ TaskPos task_pos(const Group& G, int task);
+
+// Consumer loop of the small form (the same ring, meta, task and split
+// protocol as the MMA consumers).
+template <bool ISUM>
+__device__ __forceinline__ void small_consumer(const Group& G, const uint8_t* ring, const int4* meta, uint32_t full_s,
+                                               uint32_t empty_s, int kStages, int kStageBytes, int kBlockBytes,
+                                               int kFragOff, int warp, int lane) {
+  const int r = lane >> 1, h = lane & 1;
+  float run[2] = {0.0f, 0.0f}, tot[2] = {0.0f, 0.0f};
+  int nrun = 0;
+  int slot = 0;
+  unsigned fills = 0;
+  int cur_task = -1;
+  TaskPos tp = {0, 0, 0, 0, 0};
+  int pend_p = -1, pend_rg = 0;
+  unsigned pend_old = 0;
+  auto resolve = [&]() {
+    if (pend_p < 0) return;
+    const Proj& Q = G.p[pend_p];
+    const unsigned old = __shfl_sync(0xffffffffu, pend_old, 0);
+    if (old == static_cast<unsigned>(Q.nch - 1)) {
+      __threadfence();
+      __syncwarp();
+      if (lane == 0) Q.arrive[pend_rg] = 0u;
+      reduce_chunks_small(Q, pend_rg, r, h);
+    }
+    pend_p = -1;
+  };
+  for (;;) {
+    if (!mbar_wait(full_s + 8 * slot, fills & 1, 2, G.wait_limit)) return;
+    const int4 m = meta[slot];
+    if (m.x < 0) {
+      resolve();
+      return;
+    }
+    if (m.x != cur_task) {
+      cur_task = m.x;
+      tp = task_pos(G, m.x);
+    }
+    const Proj& P = G.p[tp.p];
+    const int rg = tp.rb * kGemvWarps + warp;
+    const int row = rg * 16 + r;
+    const uint8_t* st = ring + slot * kStageBytes;
+    float acc[2] = {0.0f, 0.0f};
+    if (rg * 16 < P.N) compute_small_q4<ISUM>(st + warp * kBlockBytes, st + kFragOff, P, row, m.y, r, h, lane, acc);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty_s + 8 * slot);
+    run[0] += acc[0];
+    run[1] += acc[1];
+    if (++nrun == 32) {
+      tot[0] += run[0];
+      tot[1] += run[1];
+      run[0] = run[1] = 0.0f;
+      nrun = 0;
+    }
+    resolve();
+    if (m.z) {
+      const float v[2] = {tot[0] + run[0], tot[1] + run[1]};
+      run[0] = run[1] = tot[0] = tot[1] = 0.0f;
+      nrun = 0;
+      if (P.nch == 1) {
+        if (h == 1 && row < P.N)
+          for (int t = 0; t < P.M; ++t) P.y[static_cast<size_t>(t) * P.N + row] = v[t];
+      } else if (rg * 16 < P.N) {
+        const int rows_pad = gemv_row_blocks(P.N) * kGemvRows;
+        float* part = P.partial + static_cast<size_t>(tp.c) * 8 * rows_pad;
+        if (h == 1)
+          for (int t = 0; t < P.M; ++t) part[static_cast<size_t>(t) * rows_pad + row] = v[t];
+        __syncwarp();
+        if (lane == 0) {
+          __threadfence();
+          pend_old = atomicAdd(P.arrive + rg, 1u);
+        }
+        pend_p = tp.p;
+        pend_rg = rg;
+      }
+    }
+    if (++slot == kStages) {
+      slot = 0;
+      ++fills;
+    }
+  }
+}
+
+template <int TYPE, bool ISUM, bool SMALL>
 __device__ __forceinline__ void gemv_mma_body(const Group& G) {
   // Body of gemv_mma_kernel: a return here leaves through the kernel's
   // deferred dependency wait.
   using Lay = GLay<TYPE>;
   constexpr int kStages = Lay::kStages, kStageBytes = Lay::kStageBytes, kBlockBytes = Lay::kBlockBytes;
-  constexpr int kFragOff = Lay::kFragOff, kFscOff = Lay::kFscOff;
+  constexpr int kFragOff = Lay::kFragOff;
   extern __shared__ __align__(128) uint8_t smem[];
   uint8_t* ring = smem;
   float4* dec_all = reinterpret_cast<float4*>(smem + kStages * kStageBytes);
@@ -618,7 +853,7 @@ __device__ __forceinline__ void gemv_mma_body(const Group& G) {
       int b = tp.b0;
       for (; b < tp.b1 && slot < kStages; ++b, ++slot) {
         meta[slot] = make_int4(task, b, (b == tp.b1 - 1) ? 1 : 0, 0);
-        mbar_expect_tx(full_s + 8 * slot, static_cast<unsigned>(nblk * kBlockBytes + 8 * 512 + 8 * 64));
+        mbar_expect_tx(full_s + 8 * slot, static_cast<unsigned>(nblk * kBlockBytes) + act_bytes<SMALL>(P));
         const uint32_t st = ring_s + slot * kStageBytes;
         for (int w = 0; w < nblk; ++w)
           tma_load_2d(st + w * kBlockBytes, &P.map, weight_box_x<TYPE>(b),
@@ -633,8 +868,7 @@ __device__ __forceinline__ void gemv_mma_body(const Group& G) {
       const Proj& P = G.p[tp.p];
       for (int k = 0; k < slot; ++k) {
         const uint32_t st = ring_s + k * kStageBytes;
-        bulk_load(st + kFragOff, P.frag + static_cast<size_t>(tp.b0 + k) * 8 * 512, 8 * 512, full_s + 8 * k);
-        bulk_load(st + kFscOff, P.fsc + static_cast<size_t>(tp.b0 + k) * 8 * 64, 8 * 64, full_s + 8 * k);
+        act_load<TYPE, SMALL>(st, P, tp.b0 + k, full_s + 8 * k);
       }
     }
     if (slot == kStages) {
@@ -658,13 +892,12 @@ __device__ __forceinline__ void gemv_mma_body(const Group& G) {
         const Proj& P = G.p[tp.p];
         const int rows = P.N - tp.rb * kGemvRows;  // > 0
         const int nblk = rows >= kGemvRows ? kGemvWarps : (rows + 15) / 16;
-        mbar_expect_tx(full_s + 8 * slot, static_cast<unsigned>(nblk * kBlockBytes + 8 * 512 + 8 * 64));
+        mbar_expect_tx(full_s + 8 * slot, static_cast<unsigned>(nblk * kBlockBytes) + act_bytes<SMALL>(P));
         const uint32_t st = ring_s + slot * kStageBytes;
         for (int w = 0; w < nblk; ++w)
           tma_load_2d(st + w * kBlockBytes, &P.map, weight_box_x<TYPE>(b),
                       tp.rb * kGemvRows + 16 * w, full_s + 8 * slot);
-        bulk_load(st + kFragOff, P.frag + static_cast<size_t>(b) * 8 * 512, 8 * 512, full_s + 8 * slot);
-        bulk_load(st + kFscOff, P.fsc + static_cast<size_t>(b) * 8 * 64, 8 * 64, full_s + 8 * slot);
+        act_load<TYPE, SMALL>(st, P, b, full_s + 8 * slot);
         if (++slot == kStages) {
           slot = 0;
           ++fills;
@@ -677,6 +910,10 @@ __device__ __forceinline__ void gemv_mma_body(const Group& G) {
   // --------------------------------------------------------- consumers
   if (G.wait_prev) cudaGridDependencySynchronize();
   cudaTriggerProgrammaticLaunchCompletion();
+  if constexpr (SMALL) {
+    small_consumer<ISUM>(G, ring, meta, full_s, empty_s, kStages, kStageBytes, kBlockBytes, kFragOff, warp, lane);
+    return;
+  }
   const int n8 = lane >> 2, t = lane & 3;
   float4* dec = dec_all + warp * (kDecBytes / 16);
   // Accumulation bounded by construction: one super-block's terms (at most
@@ -791,10 +1028,10 @@ __device__ __forceinline__ void gemv_mma_body(const Group& G) {
   }
 }
 
-template <int TYPE, bool ISUM>
+template <int TYPE, bool ISUM, bool SMALL>
 __global__ void __launch_bounds__(32 * (kGemvWarps + 1), kGemvCtasPerSM)
 gemv_mma_kernel(const __grid_constant__ Group G) {
-  gemv_mma_body<TYPE, ISUM>(G);
+  gemv_mma_body<TYPE, ISUM, SMALL>(G);
   // A launch that did not wait for the previous grid on entry waits before
   // its threads exit, so that its completion still implies the completion of
   // every earlier kernel on the stream (the next kernel's dependency wait
@@ -802,14 +1039,15 @@ gemv_mma_kernel(const __grid_constant__ Group G) {
   if (!G.wait_prev) cudaGridDependencySynchronize();
 }
 
-template <int TYPE, bool ISUM>
+template <int TYPE, bool ISUM, bool SMALL = false>
 int max_ctas() {
   static int per_sm = -1;
   if (per_sm < 0) {
     int n = 0;
     constexpr int kSmemBytes = GLay<TYPE>::kSmemBytes;
-    cudaFuncSetAttribute(gemv_mma_kernel<TYPE, ISUM>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, gemv_mma_kernel<TYPE, ISUM>, 32 * (kGemvWarps + 1), kSmemBytes) != cudaSuccess ||
+    cudaFuncSetAttribute(gemv_mma_kernel<TYPE, ISUM, SMALL>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, gemv_mma_kernel<TYPE, ISUM, SMALL>, 32 * (kGemvWarps + 1),
+                                                      kSmemBytes) != cudaSuccess ||
         n < 1)
       n = 1;
     per_sm = n;
@@ -920,6 +1158,11 @@ cudaError_t launch_gemv_mma(int type, const MmaProj* projs, int n, cudaStream_t 
   G.wait_limit = stall_test ? kStallWaitClocks : kWaitClocks;
   int total = 0;
   bool isum = false;
+  // Q4_K at one or two tokens takes the small-M (dp4a) form, except in the
+  // batch-invariant layout.
+  bool small = type == 12;
+  for (int k = 0; k < n; ++k)
+    small = small && projs[k].M_total <= 2 && projs[k].chunk == 0 && !projs[k].gemv_image;
   for (int k = 0; k < n; ++k) {
     const int src = order[k];
     const MmaProj& q = projs[src];
@@ -929,6 +1172,9 @@ cudaError_t launch_gemv_mma(int type, const MmaProj* projs, int n, cudaStream_t 
     if (!gemv_mma_supports(type, q.K) || !encode_weight_map(type, &P.map, q.W, q.N, q.K)) return cudaErrorInvalidValue;
     P.frag = q.xq + L.frag + static_cast<size_t>(q.chunk) * 16 * q.K;
     P.fsc = q.xq + L.fsc + static_cast<size_t>(q.chunk) * 2 * q.K;
+    P.aq = q.xq + L.qs;
+    P.ad8 = reinterpret_cast<const float*>(q.xq + L.d8);
+    P.as8 = reinterpret_cast<const float*>(q.xq + L.s8);
     P.y = q.y + static_cast<size_t>(m0) * q.N;
     P.isum = q.isum;
     P.N = q.N;
@@ -949,7 +1195,8 @@ cudaError_t launch_gemv_mma(int type, const MmaProj* projs, int n, cudaStream_t 
   }
   G.total = total;
   if (total == 0) return cudaSuccess;
-  const int cap = type == 12   ? (isum ? max_ctas<12, true>() : max_ctas<12, false>())
+  const int cap = small        ? (isum ? max_ctas<12, true, true>() : max_ctas<12, false, true>())
+                  : type == 12 ? (isum ? max_ctas<12, true>() : max_ctas<12, false>())
                   : type == 8  ? (isum ? max_ctas<8, true>() : max_ctas<8, false>())
                   : type == 23 ? (isum ? max_ctas<23, true>() : max_ctas<23, false>())
                                : (isum ? max_ctas<14, true>() : max_ctas<14, false>());
@@ -966,16 +1213,19 @@ cudaError_t launch_gemv_mma(int type, const MmaProj* projs, int n, cudaStream_t 
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
   if (type == 8)
-    return isum ? cudaLaunchKernelEx(&cfg, gemv_mma_kernel<8, true>, G)
-                : cudaLaunchKernelEx(&cfg, gemv_mma_kernel<8, false>, G);
+    return isum ? cudaLaunchKernelEx(&cfg, gemv_mma_kernel<8, true, false>, G)
+                : cudaLaunchKernelEx(&cfg, gemv_mma_kernel<8, false, false>, G);
   if (type == 23)
-    return isum ? cudaLaunchKernelEx(&cfg, gemv_mma_kernel<23, true>, G)
-                : cudaLaunchKernelEx(&cfg, gemv_mma_kernel<23, false>, G);
+    return isum ? cudaLaunchKernelEx(&cfg, gemv_mma_kernel<23, true, false>, G)
+                : cudaLaunchKernelEx(&cfg, gemv_mma_kernel<23, false, false>, G);
+  if (small)
+    return isum ? cudaLaunchKernelEx(&cfg, gemv_mma_kernel<12, true, true>, G)
+                : cudaLaunchKernelEx(&cfg, gemv_mma_kernel<12, false, true>, G);
   if (type == 12)
-    return isum ? cudaLaunchKernelEx(&cfg, gemv_mma_kernel<12, true>, G)
-                : cudaLaunchKernelEx(&cfg, gemv_mma_kernel<12, false>, G);
-  return isum ? cudaLaunchKernelEx(&cfg, gemv_mma_kernel<14, true>, G)
-              : cudaLaunchKernelEx(&cfg, gemv_mma_kernel<14, false>, G);
+    return isum ? cudaLaunchKernelEx(&cfg, gemv_mma_kernel<12, true, false>, G)
+                : cudaLaunchKernelEx(&cfg, gemv_mma_kernel<12, false, false>, G);
+  return isum ? cudaLaunchKernelEx(&cfg, gemv_mma_kernel<14, true, false>, G)
+              : cudaLaunchKernelEx(&cfg, gemv_mma_kernel<14, false, false>, G);
 }
 
 }  // namespace xq
