@@ -410,6 +410,40 @@ def per_layer_times(sweep, M, reps=3):
     return [t / reps for t in tot]
 
 
+def per_layer_gemv_times(sweep, M, reps=3):
+    """CUDA-event duration of every layer's grouped matmul launch on its own
+    (the dominant kernel), on the stream the kernels run on. Each layer gets
+    its own workspace, which one xq_layer_mixed call fills with the layer's
+    Q8 activations; then xq_debug_layer_matmuls re-runs just the matmul
+    launch (one grouped launch for an all-Q4_K layer), layer after layer in
+    sweep order, so every layer's weights were last read 31 layers (3.8 GB)
+    earlier and stream from HBM. Returns seconds per layer, averaged over
+    reps sweeps."""
+    import torch
+    from gguf_quant_integer_gb300 import xq
+    ins, ys, descs, ws = sweep.state[M]
+    wss = [torch.empty_like(ws) for _ in sweep.W]
+    for l in range(len(sweep.W)):
+        xq.layer_mixed(descs[l], ins[l], M, wss[l])
+    s = torch.cuda.current_stream()
+    tot = [0.0] * len(sweep.W)
+    for _ in range(reps + 1):  # the first pass is a warm-up
+        evs = []
+        for l in range(len(sweep.W)):
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(s)
+            xq.debug_layer_matmuls(descs[l], sweep.n_inputs, M, wss[l])
+            b.record(s)
+            evs.append((a, b))
+        torch.cuda.synchronize()
+        if _ == 0:
+            continue
+        for l, (a, b) in enumerate(evs):
+            tot[l] += a.elapsed_time(b) / 1e3
+    return [t / reps for t in tot]
+
+
 # Sources the grouped GEMV kernel is built from: a recorded ncu traffic
 # figure stays valid only while their code is unchanged (comments and
 # whitespace are not part of the hash).
@@ -497,18 +531,23 @@ def gpu_arm(args):
         by_m[str(m)] = {"GBps": round(nbytes / s / 1e9, 1), "ms_per_step": round(1e3 * s, 4),
                         "tokens_per_s": round(m / s, 1)}
 
-    # ---- dominant kernel: CUDA events around every layer's launches (the
-    # grouped Q4_K matmul is ~90% of each layer's GPU time per the ncu list)
+    # ---- dominant kernel: CUDA events around every layer's grouped Q4_K
+    # matmul launch on its own (about 90% of each layer's GPU time per the
+    # ncu launch list); the layer call with its quantize launch for context
     peak, peak_kind = measured_peaks()
+    gts = per_layer_gemv_times(sweep, M)
     lts = per_layer_times(sweep, M)
     layer_bytes = wl.layer_weight_bytes()
-    avg = sum(lts) / len(lts)
+    avg = sum(gts) / len(gts)
+    avg_call = sum(lts) / len(lts)
     achieved = layer_bytes / avg / 1e9
     tr = read_ncu_traffic(f"gemv_mma_q4k_layer_M{M}")
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "peak_source": peak_kind,
-                "kernel": "gemv_mma_kernel<Q4_K>, one grouped launch per layer (timed with its quantize launch)",
+                "kernel": "gemv_mma_kernel<Q4_K>, the grouped launch of one layer, timed alone",
                 "bytes_per_launch": layer_bytes, "avg_launch_us": round(1e6 * avg, 3),
+                "layer_call_us": round(1e6 * avg_call, 3),
+                "layer_call_note": "xq_layer_mixed per layer (quantize launch + GEMV launch), CUDA events per call",
                 "traffic": (round(tr[0]) if tr else None),
                 "traffic_note": (tr[1] if tr else "no ncu capture of the current kernel source")}
     # Context: every projection launched on its own (small projections get

@@ -585,6 +585,37 @@ xq_status xq_layer_mixed(const xq_proj* proj, int n_proj, const float* const* in
   return layer_matmuls(proj, n_proj, q8, M, sc, ws + sched_off, s);
 }
 
+xq_status xq_debug_layer_matmuls(const xq_proj* proj, int n_proj, int n_inputs, int M, void* workspace,
+                                 size_t ws_bytes, xq_stream stream) {
+  int in_k[64];
+  const xq_status st = layer_inputs(proj, n_proj, n_inputs, M, in_k);
+  if (st != XQ_OK) return st;
+  if (M == 0) return XQ_OK;
+  // the workspace layout of xq_layer_mixed: the used inputs' Q8 buffers in
+  // input order, then the scheduling state
+  size_t off[64];
+  size_t need = 0;
+  for (int i = 0; i < n_inputs; ++i) {
+    off[i] = need;
+    if (in_k[i]) need += round256(xq_q8_bytes(M, in_k[i]));
+  }
+  const size_t sched_off = need;
+  const Sched sc = sched_layout(proj, n_proj, M);
+  need += sched_bytes(sc);
+  if (!workspace) return XQ_ERR_ARG;
+  if (ws_bytes < need) return XQ_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return XQ_ERR_ALIGN;
+  for (int p = 0; p < n_proj; ++p) {
+    if (proj[p].N == 0) continue;
+    if (!proj[p].W || !proj[p].y) return XQ_ERR_ARG;
+    if (!aligned16(proj[p].W) || !aligned16(proj[p].y)) return XQ_ERR_ALIGN;
+  }
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const uint8_t* q8[64];
+  for (int p = 0; p < n_proj; ++p) q8[p] = ws + off[proj[p].input];
+  return layer_matmuls(proj, n_proj, q8, M, sc, ws + sched_off, reinterpret_cast<cudaStream_t>(stream));
+}
+
 xq_status xq_debug_tile_sums(int type, const void* W, const int8_t* codebook, const void* xq, int M, int N, int K,
                              float* y, int32_t* sums, xq_stream stream) {
   if (block_bytes(type) == 0) return XQ_ERR_ARG;

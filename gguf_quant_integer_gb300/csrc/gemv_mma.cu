@@ -566,8 +566,16 @@ __device__ __forceinline__ void reduce_chunks(const Proj& P, int rg, int n8, int
 
 // Tasks after each CTA's first (its own index): from the counter, which
 // starts at zero, offset by the grid size; or strided by the grid size.
+// A producer fetches once per task it runs, so a launch makes exactly
+// G.total fetches and the one that returns G.total - 1 is the last to touch
+// the counter: it puts the counter back to zero, and a later launch on the
+// same workspace finds it as the quantize launch leaves it.
 __device__ __forceinline__ int next_task(const Group& G, int cur) {
-  if (G.counter) return static_cast<int>(gridDim.x + atomicAdd(G.counter, 1u));
+  if (G.counter) {
+    const unsigned old = atomicAdd(G.counter, 1u);
+    if (old == static_cast<unsigned>(G.total - 1)) atomicExch(G.counter, 0u);
+    return static_cast<int>(gridDim.x + old);
+  }
   return cur + static_cast<int>(gridDim.x);
 }
 

@@ -30,7 +30,8 @@ SYMBOLS = ("xq_status_str", "xq_q8_bytes", "xq_weight_bytes", "xq_quantize_q8",
            "xq_q8_bytes_invariant", "xq_quantize_q8_invariant", "xq_matmul_invariant",
            "xq_matmul_q8_0_q8", "xq_debug_isums_q8_0", "xq_silu_mul_quantize_q8",
            "xq_layer_ffn_workspace_bytes", "xq_layer_mixed_ffn", "xq_matmul_iq4xs_q8",
-           "xq_debug_isums_iq4xs", "xq_device_error", "xq_debug_stalled_matmul_q4k", "xq_debug_tile_sums")
+           "xq_debug_isums_iq4xs", "xq_device_error", "xq_debug_stalled_matmul_q4k", "xq_debug_tile_sums",
+           "xq_debug_layer_matmuls")
 
 
 class XQError(RuntimeError):
@@ -97,9 +98,10 @@ def lib(path: str | None = None):
     L.xq_layer_workspace_bytes.restype = S
     L.xq_layer_mixed.argtypes = [ctypes.POINTER(xq_proj), I, ctypes.POINTER(ctypes.c_void_p), I, I, P, S, P]
     L.xq_layer_mixed_static.argtypes = [ctypes.POINTER(xq_proj), I, ctypes.POINTER(ctypes.c_void_p), I, I, P]
+    L.xq_debug_layer_matmuls.argtypes = [ctypes.POINTER(xq_proj), I, I, I, P, S, P]
     for fn in ("xq_quantize_q8", "xq_matmul_q4k_q8", "xq_matmul_q6k_q8", "xq_debug_isums_q4k",
                "xq_debug_isums_q6k", "xq_layer_mixed", "xq_layer_mixed_static", "xq_matmul_q8_0_q8",
-               "xq_debug_isums_q8_0"):
+               "xq_debug_isums_q8_0", "xq_debug_layer_matmuls"):
         getattr(L, fn).restype = I
     if path is None:
         _lib = L
@@ -305,6 +307,15 @@ def layer_mixed(projs, inputs, M: int, workspace, stream=None):
     rc = lib().xq_layer_mixed(arr, len(projs), ins, len(inputs), M, _ptr(workspace),
                               workspace.numel() if workspace is not None else 0, _stream(stream))
     _check("xq_layer_mixed", rc)
+
+
+def debug_layer_matmuls(projs, n_inputs: int, M: int, workspace, stream=None):
+    """The matmul launches of layer_mixed alone, on the Q8 activations the last
+    layer_mixed call with the same projs, input count and M left in workspace."""
+    arr = _proj_array(projs)
+    rc = lib().xq_debug_layer_matmuls(arr, len(projs), n_inputs, M, _ptr(workspace),
+                                      workspace.numel() if workspace is not None else 0, _stream(stream))
+    _check("xq_debug_layer_matmuls", rc)
 
 
 def silu_mul_quantize_q8(gate, up, out=None, h_out=None, stream=None):

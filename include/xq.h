@@ -347,6 +347,18 @@ XQ_API xq_status xq_debug_isums_iq4xs(const void *W, const int8_t *codebook, con
 XQ_API xq_status xq_debug_tile_sums(int type, const void *W, const int8_t *codebook, const void *xq, int M,
                                     int N, int K, float *y, int32_t *sums, xq_stream stream);
 
+/* Timing hook: the matmul launches of xq_layer_mixed alone, without its
+ * quantize launch, reading the Q8 activations that the last xq_layer_mixed
+ * call with the same proj, n_proj, n_inputs and M left in `workspace`. Each
+ * launch leaves the workspace's scheduling state (task counters, split-K
+ * arrival counts) at zero, as it found it, so the call can be repeated; it
+ * rewrites every projection's y with the same values, bit for bit. Errors as
+ * xq_layer_mixed (XQ_ERR_WORKSPACE if ws_bytes is below
+ * xq_layer_workspace_bytes). The result is undefined if the workspace does
+ * not hold the state of such a call. */
+XQ_API xq_status xq_debug_layer_matmuls(const xq_proj *proj, int n_proj, int n_inputs, int M, void *workspace,
+                                        size_t ws_bytes, xq_stream stream);
+
 #ifdef __cplusplus
 }
 #endif

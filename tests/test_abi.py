@@ -124,6 +124,22 @@ def test_layer_argument_errors(L):
     assert L.xq_layer_mixed(arr, n, ins, 2, 4, P(FAKE), need, None) == 1
 
 
+def test_layer_matmuls_timing_hook_argument_errors(L):
+    """xq_debug_layer_matmuls validates like xq_layer_mixed (it takes no
+    inputs: the activations are the workspace's)."""
+    from gguf_quant_integer_gb300 import xq
+    P = ctypes.c_void_p
+    specs = [(12, 16, 512, 0), (14, 8, 512, 0), (12, 16, 1024, 1)]
+    arr = xq._proj_array([(t, n, k, None, None, i) for (t, n, k, i) in specs])
+    need = L.xq_layer_workspace_bytes(arr, 3, 2, 4)
+    assert L.xq_debug_layer_matmuls(arr, 3, 2, 4, P(FAKE), need - 1, None) == 4     # workspace too small
+    assert L.xq_debug_layer_matmuls(arr, 3, 2, 4, None, need, None) == 1            # no workspace
+    assert L.xq_debug_layer_matmuls(arr, 3, 2, 4, P(FAKE + 8), need, None) == 3     # misaligned
+    assert L.xq_debug_layer_matmuls(arr, 3, 2, 4, P(FAKE), need, None) == 1         # no weight pointers
+    assert L.xq_debug_layer_matmuls(arr, 3, 1, 4, P(FAKE), need, None) == 1         # input 1 out of range
+    assert L.xq_debug_layer_matmuls(arr, 3, 2, 0, None, 0, None) == 0               # M = 0: nothing to do
+
+
 def test_q8_0_entry_points_reject_before_launch(L):
     """Q8_0 shape and argument errors are refused before anything is
     enqueued; the layer sizes Q8_0 at every M."""
