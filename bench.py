@@ -279,6 +279,17 @@ def reference_arm(args):
 
 # ------------------------------------------------------------ GPU arm
 
+def q6k_on_gemv(N, K):
+    """Whether a Q6_K projection runs on the tensor-core GEMV (the rest run
+    on the dp4a kernel): rows of 16-byte multiples, or N a multiple of 16
+    times the count of consecutive rows whose bytes are (2, 4 or 8)."""
+    row = (K // 256) * 210
+    g = 1
+    while g < 8 and (row * g) % 16:
+        g *= 2
+    return g == 1 or N % (16 * g) == 0
+
+
 class Sweep:
     """All layers of a workload resident on the device, with per-M outputs."""
 
@@ -322,7 +333,7 @@ class Sweep:
         else:
             grouped = {synth.Q4_K: 0, synth.Q6_K: 0}
             for p in self.wl.projs:
-                if p.qtype == synth.Q4_K or (p.K // 256) % 8 == 0:
+                if p.qtype == synth.Q4_K or q6k_on_gemv(p.N, p.K):
                     grouped[p.qtype] += 1
                 else:
                     per_layer += 1
@@ -717,7 +728,31 @@ def secondary_workloads(device, world):
     out["tiny-gemv"] = {"M": 1, "N": p.N, "K": p.K, "rotated_copies": copies, "weight_bytes": wbytes,
                         "us_per_call": round(1e6 * sec, 3), "GBps": round(wbytes / sec / 1e9, 2),
                         "tokens_per_s": round(1 / sec, 1), "note": "quantize + matmul per call; launch-bound"}
-    for name in ("qwen2.5-1.5b-layer", "qwen3-8b-mixed-layer", "qwen2.5-1.5b-q8_0-layer"):
+    # Q6_K rows that are not 16-byte multiples (the 8960 -> 1536 ffn_down of
+    # the Qwen2.5-1.5B shape, 7350-byte rows): quantize + matmul per call
+    N6, K6 = 1536, 8960
+    wb6 = synth.weight_bytes(synth.Q6_K, N6, K6)
+    copies = max(3, -(-3 * L2_BYTES // wb6))
+    W6 = torch.from_numpy(synth.gen_q6k(61, N6, K6).reshape(-1)).to(device)
+    W6s = [W6] + [W6.clone() for _ in range(copies - 1)]
+    res6 = {}
+    for M in (1, 8):
+        x6 = torch.from_numpy(synth.gen_x(62 + M, M, K6)).to(device)
+        buf6 = xq.quantize_q8(x6)
+        y6 = torch.empty((M, N6), dtype=torch.float32, device=device)
+
+        def q6_step():
+            for c in range(copies):
+                xq.quantize_q8(x6, out=buf6)
+                xq.matmul(synth.Q6_K, W6s[c], buf6, M, N6, K6, y=y6)
+
+        sec = max_over_ranks(time_region(q6_step, 5, 3, world, device), world, device) / (5 * copies)
+        res6[str(M)] = {"us_per_call": round(1e6 * sec, 2), "GBps": round(wb6 / sec / 1e9, 1)}
+    out["q6k-ffn_down-1536x8960"] = {"rotated_copies": copies, "weight_bytes": wb6, "by_m": res6,
+                                     "path": "dp4a kernel (a single matmul of fewer than 128 row blocks; in a "
+                                             "layer this projection runs on the tensor-core GEMV, split over K)",
+                                     "note": "quantize + matmul per call"}
+    for name in ("qwen2.5-1.5b-layer", "qwen2.5-1.5b-q4km-layer", "qwen3-8b-mixed-layer", "qwen2.5-1.5b-q8_0-layer"):
         wl = synth.WORKLOADS[name]
         lw = synth.gen_layer_weights(wl, 0)
         copies = max(3, -(-3 * L2_BYTES // wl.layer_weight_bytes()))

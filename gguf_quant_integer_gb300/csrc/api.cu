@@ -34,6 +34,19 @@ xq_status check_shape(int M, int N, int K) {
 // multiples; the dp4a GEMV for the other Q6_K shapes. invariant: every M in
 // 8-token GEMV chunks from the GEMV-image layout, never split over K, so
 // that each token's row of y is computed by the same operations whatever M.
+//
+// A single matmul has no workspace for split-K partial sums, so its GEMV
+// launch has one task per 64 rows over the whole of K. Q6_K weights in the
+// grouped view (rows that are not 16-byte multiples) take the tensor-core
+// GEMV only when that gives at least 128 tasks; narrower ones run faster on
+// the dp4a kernel, whose warps take a few rows each (measured on GB300, M = 8,
+// weights past L2: 1536 x 8960 24.7 us on dp4a against 35.1 us; 8960 x 1536
+// 16.5 us against 9.9 us). The choice depends on the shape only, never on M.
+bool single_gemv(int type, int N, int K) {
+  if (!xq::gemv_mma_supports(type, N, K)) return false;
+  return type != XQ_TYPE_Q6_K || xq::q6k_row_shift(K) == 0 || xq::gemv_row_blocks(N) >= 128;
+}
+
 xq_status run_matmul(int type, const void* W, const void* xq, int M, int N, int K, float* y,
                      int32_t* isum, cudaStream_t s, bool invariant = false, const uint32_t* codebook = nullptr) {
   const xq::Q8Layout L = xq::q8_layout(M, K, invariant);
@@ -42,7 +55,7 @@ xq_status run_matmul(int type, const void* W, const void* xq, int M, int N, int 
     const cudaError_t e = xq::launch_tile_mma(type, static_cast<const uint8_t*>(W), base, M, N, K, y, s, true, codebook);
     return e == cudaSuccess ? XQ_OK : XQ_ERR_CUDA;
   }
-  if (xq::gemv_mma_supports(type, K)) {
+  if (single_gemv(type, N, K)) {
     xq::MmaProj items[xq::kMaxProj];
     int n = 0;
     for (int c = 0; c < L.chunks; ++c) {
@@ -138,7 +151,9 @@ struct Sched {
 };
 
 // Projections that go to the grouped tensor-core GEMV at M <= 8.
-bool in_group(const xq_proj& q, int M) { return q.N > 0 && M <= kMaxGemvM && xq::gemv_mma_supports(q.type, q.K); }
+bool in_group(const xq_proj& q, int M) {
+  return q.N > 0 && M <= kMaxGemvM && xq::gemv_mma_supports(q.type, q.N, q.K);
+}
 
 
 // K-chunking of a grouped launch: chunks of ~16 super-blocks for long rows;
@@ -168,7 +183,7 @@ Sched sched_layout(const xq_proj* proj, int n_proj, int M) {
     const int chunks = (M + 7) / 8;
     for (int p = 0; p < n_proj && p < 64; ++p) {
       const xq_proj& q = proj[p];
-      if (q.N <= 0 || !xq::gemv_mma_supports(q.type, q.K)) continue;
+      if (q.N <= 0 || !xq::gemv_mma_supports(q.type, q.N, q.K)) continue;
       sc.nch[p] = xq::gemv_split_chunks(q.K, kMaxGemvM, 16);
       if (sc.nch[p] <= 1) continue;
       const int g = type_index(q.type);
@@ -288,7 +303,7 @@ xq_status layer_matmuls(const xq_proj* proj, int n_proj, const uint8_t* const* q
       };
       for (int p = 0; p < n_proj; ++p) {
         const xq_proj& q = proj[p];
-        if (q.N == 0 || q.type != type || !xq::gemv_mma_supports(q.type, q.K)) continue;
+        if (q.N == 0 || q.type != type || !xq::gemv_mma_supports(q.type, q.N, q.K)) continue;
         for (int c = 0; c < chunks; ++c) {
           xq::MmaProj& it = items[n++];
           it.W = static_cast<const uint8_t*>(q.W);
@@ -308,7 +323,7 @@ xq_status layer_matmuls(const xq_proj* proj, int n_proj, const uint8_t* const* q
     }
     for (int p = 0; p < n_proj; ++p) {
       const xq_proj& q = proj[p];
-      if (q.N == 0 || (chunked && xq::gemv_mma_supports(q.type, q.K))) continue;
+      if (q.N == 0 || (chunked && xq::gemv_mma_supports(q.type, q.N, q.K))) continue;
       const xq_status st = run_one(q, q8[p], M, s);
       if (st != XQ_OK) return st;
     }

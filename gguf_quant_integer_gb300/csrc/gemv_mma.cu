@@ -80,6 +80,7 @@ struct Proj {
   const float* ad8;      // small-M form: d8 [M][K/32]
   const float* as8;      // small-M form: s8 [M][K/32]
   int N, K, M, task0, nch;
+  int gs;                // Q6_K grouped view: 2^gs consecutive rows form one tensor-map row (else 0)
 };
 
 struct Group {
@@ -127,6 +128,30 @@ __device__ __forceinline__ int weight_box_x(int b) {
   else if constexpr (TYPE == 8) return b * (kQ80Group / 8);
   else if constexpr (TYPE == 23) return (kIq4xsBytes * b) & ~15;
   else return (kQ6kBytes * b) & ~15;
+}
+
+// Weight row of row k (0..15) of the 16-row group rg. Without the grouped
+// view (gs = 0) the group holds rows 16rg .. 16rg+15. Q6_K rows that are not
+// 16-byte multiples are mapped 2^gs rows to a tensor-map row (the smallest
+// count whose bytes are a multiple of 16); group rg then holds rows
+// i, i + g, ..., i + 15g of the block of 16g rows starting at 16g(rg >> gs),
+// with g = 2^gs and i = rg mod g, so all its rows share one position i in
+// their tensor-map rows and one in-window offset.
+__device__ __forceinline__ int group_row(const Proj& P, int rg, int k) {
+  return ((16 * (rg >> P.gs) + k) << P.gs) + (rg & ((1 << P.gs) - 1));
+}
+
+// TMA coordinates of the 16-row box of group rg at super-block b.
+template <int TYPE>
+__device__ __forceinline__ void weight_box(const Proj& P, int rg, int b, int& x, int& y) {
+  if constexpr (TYPE == 14) {
+    const int i = rg & ((1 << P.gs) - 1);
+    x = (kQ6kBytes * ((P.K >> 8) * i + b)) & ~15;
+    y = 16 * (rg >> P.gs);
+  } else {
+    x = weight_box_x<TYPE>(b);
+    y = 16 * rg;
+  }
 }
 
 // ---------------------------------------------------------------- PTX
@@ -287,7 +312,7 @@ __device__ __forceinline__ void compute_block_q4(const uint8_t* blk, const uint8
         const int sb = 8 * b + j;
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const int row = rg * 16 + ((e >> 1) ? r1 : r0);
+          const int row = group_row(P, rg, (e >> 1) ? r1 : r0);
           const int col = 2 * t + (e & 1);
           if (row < P.N && col < P.M)
             P.isum[(static_cast<size_t>(col) * P.N + row) * nsub + sb] = static_cast<int32_t>(D[e] * scale);
@@ -364,7 +389,7 @@ __device__ __forceinline__ void compute_block_q6(const uint8_t* blk, int off, co
         for (int g = 0; g < 2; ++g)
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            const int row = rg * 16 + ((e >> 1) ? r1 : r0);
+            const int row = group_row(P, rg, (e >> 1) ? r1 : r0);
             const int col = 2 * t + (e & 1);
             if (row < P.N && col < P.M)
               P.isum[(static_cast<size_t>(col) * P.N + row) * ngrp + 16 * b + 2 * p + g] =
@@ -430,7 +455,7 @@ __device__ __forceinline__ void compute_block_q8_0(const uint8_t* blk, const uin
       const int nsub = P.K >> 5;
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const int row = rg * 16 + ((e >> 1) ? r1 : r0);
+        const int row = group_row(P, rg, (e >> 1) ? r1 : r0);
         const int col = 2 * t + (e & 1);
         if (row < P.N && col < P.M)
           P.isum[(static_cast<size_t>(col) * P.N + row) * nsub + 8 * b + j] = static_cast<int32_t>(D[e]);
@@ -515,7 +540,7 @@ __device__ __forceinline__ void compute_block_iq4xs(const uint8_t* blk, int off,
       const int nsub = P.K >> 5;
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const int row = rg * 16 + ((e >> 1) ? r1 : r0);
+        const int row = group_row(P, rg, (e >> 1) ? r1 : r0);
         const int col = 2 * t + (e & 1);
         if (row < P.N && col < P.M)
           P.isum[(static_cast<size_t>(col) * P.N + row) * nsub + 8 * b + j] = static_cast<int32_t>(D[e]);
@@ -526,7 +551,7 @@ __device__ __forceinline__ void compute_block_iq4xs(const uint8_t* blk, int off,
 
 __device__ __forceinline__ void store_y(const Proj& P, int rg, int n8, int t, float v00, float v01, float v10,
                                         float v11) {
-  const int r0 = rg * 16 + mma_row(n8), r1 = r0 + 8, c0 = 2 * t, c1 = c0 + 1;
+  const int r0 = group_row(P, rg, mma_row(n8)), r1 = group_row(P, rg, mma_row(n8) + 8), c0 = 2 * t, c1 = c0 + 1;
   if (r0 < P.N) {
     if (c0 < P.M) P.y[static_cast<size_t>(c0) * P.N + r0] = v00;
     if (c1 < P.M) P.y[static_cast<size_t>(c1) * P.N + r0] = v01;
@@ -863,9 +888,11 @@ __device__ __forceinline__ void gemv_mma_body(const Group& G) {
         meta[slot] = make_int4(task, b, (b == tp.b1 - 1) ? 1 : 0, 0);
         mbar_expect_tx(full_s + 8 * slot, static_cast<unsigned>(nblk * kBlockBytes) + act_bytes<SMALL>(P));
         const uint32_t st = ring_s + slot * kStageBytes;
-        for (int w = 0; w < nblk; ++w)
-          tma_load_2d(st + w * kBlockBytes, &P.map, weight_box_x<TYPE>(b),
-                      tp.rb * kGemvRows + 16 * w, full_s + 8 * slot);
+        for (int w = 0; w < nblk; ++w) {
+          int bx, by;
+          weight_box<TYPE>(P, tp.rb * kGemvWarps + w, b, bx, by);
+          tma_load_2d(st + w * kBlockBytes, &P.map, bx, by, full_s + 8 * slot);
+        }
       }
       bresume = b;
     }
@@ -902,9 +929,11 @@ __device__ __forceinline__ void gemv_mma_body(const Group& G) {
         const int nblk = rows >= kGemvRows ? kGemvWarps : (rows + 15) / 16;
         mbar_expect_tx(full_s + 8 * slot, static_cast<unsigned>(nblk * kBlockBytes) + act_bytes<SMALL>(P));
         const uint32_t st = ring_s + slot * kStageBytes;
-        for (int w = 0; w < nblk; ++w)
-          tma_load_2d(st + w * kBlockBytes, &P.map, weight_box_x<TYPE>(b),
-                      tp.rb * kGemvRows + 16 * w, full_s + 8 * slot);
+        for (int w = 0; w < nblk; ++w) {
+          int bx, by;
+          weight_box<TYPE>(P, tp.rb * kGemvWarps + w, b, bx, by);
+          tma_load_2d(st + w * kBlockBytes, &P.map, bx, by, full_s + 8 * slot);
+        }
         act_load<TYPE, SMALL>(st, P, b, full_s + 8 * slot);
         if (++slot == kStages) {
           slot = 0;
@@ -984,7 +1013,9 @@ __device__ __forceinline__ void gemv_mma_body(const Group& G) {
         __syncwarp();
         compute_block_iq4xs<ISUM>(st + warp * kBlockBytes, off, st + kFragOff, dec, P, rg, m.y, n8, t, lane, acc);
       } else {
-        const int off = (kQ6kBytes * m.y) & 15;  // the same for every row: rows are 16-byte multiples
+        // the same for every row of the group: rows are 16-byte multiples, or
+        // (grouped view) the group's rows share their position in the view
+        const int off = (kQ6kBytes * ((P.K >> 8) * (rg & ((1 << P.gs) - 1)) + m.y)) & 15;
         decode_scales_q6(st + warp * kBlockBytes, off, dec, lane);
         __syncwarp();
         compute_block_q6<ISUM>(st + warp * kBlockBytes, off, st + kFragOff, dec, P, rg, m.y, n8, t, lane, acc);
@@ -1069,6 +1100,13 @@ int max_ctas() {
 // multiples).
 bool encode_weight_map(int type, CUtensorMap* map, const uint8_t* W, int N, int K) {
   const unsigned long long nsb = static_cast<unsigned long long>(K / 256);
+  if (type == 14 && q6k_row_shift(K) > 0) {
+    // grouped view: 2^gs rows per tensor-map row
+    const int gs = q6k_row_shift(K);
+    const unsigned long long vrow = (nsb * kQ6kBytes) << gs;
+    return encode_tma_2d(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, W, vrow, static_cast<unsigned long long>(N >> gs), vrow,
+                         GLay<14>::kBoxRow, 16);
+  }
   if (type == 12)
     return encode_tma_2d(map, CU_TENSOR_MAP_DATA_TYPE_UINT64, W, nsb * kQ4kBytes / 8, static_cast<unsigned long long>(N),
                          nsb * kQ4kBytes, kQ4kBytes / 8, 16);
@@ -1123,8 +1161,19 @@ bool encode_tma_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, u
          CUDA_SUCCESS;
 }
 
-bool gemv_mma_supports(int type, int K) {
-  return type == 12 || type == 8 || (type == 14 && ((K / 256) % 8) == 0) || (type == 23 && ((K / 256) % 2) == 0);
+int q6k_row_shift(int K) {
+  const int row = (K / 256) * kQ6kBytes;
+  int gs = 0;
+  while (gs < 3 && ((row << gs) & 15) != 0) ++gs;
+  return gs;
+}
+
+bool gemv_mma_supports(int type, int N, int K) {
+  if (type == 14) {
+    const int gs = q6k_row_shift(K);
+    return gs == 0 || (N % (16 << gs)) == 0;
+  }
+  return type == 12 || type == 8 || (type == 23 && ((K / 256) % 2) == 0);
 }
 
 cudaError_t launch_gemv_mma(int type, const MmaProj* projs, int n, cudaStream_t s, bool pdl, unsigned int* counter,
@@ -1177,7 +1226,8 @@ cudaError_t launch_gemv_mma(int type, const MmaProj* projs, int n, cudaStream_t 
     const Q8Layout L = q8_layout(q.M_total, q.K, q.gemv_image);
     const int m0 = 8 * q.chunk;
     Proj& P = G.p[k];
-    if (!gemv_mma_supports(type, q.K) || !encode_weight_map(type, &P.map, q.W, q.N, q.K)) return cudaErrorInvalidValue;
+    if (!gemv_mma_supports(type, q.N, q.K) || !encode_weight_map(type, &P.map, q.W, q.N, q.K)) return cudaErrorInvalidValue;
+    P.gs = type == 14 ? q6k_row_shift(q.K) : 0;
     P.frag = q.xq + L.frag + static_cast<size_t>(q.chunk) * 16 * q.K;
     P.fsc = q.xq + L.fsc + static_cast<size_t>(q.chunk) * 2 * q.K;
     P.aq = q.xq + L.qs;

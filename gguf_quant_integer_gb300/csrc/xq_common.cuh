@@ -211,10 +211,14 @@ __host__ __device__ inline size_t gemv_split_arrive_bytes(int N) {
   return ((static_cast<size_t>(gemv_row_blocks(N)) * kGemvWarps * 4) + 255) & ~static_cast<size_t>(255);
 }
 
-// Whether the tensor-core GEMV takes this weight: every Q4_K shape; Q6_K
-// when its rows are 16-byte multiples (K/256 a multiple of 8), which the
-// tensor map needs.
-bool gemv_mma_supports(int type, int K);
+// Whether the tensor-core GEMV takes this weight: every Q4_K and Q8_0
+// shape; IQ4_XS when K is a multiple of 512; Q6_K when its rows are 16-byte
+// multiples (K/256 a multiple of 8), or else when N is a multiple of 16 * 2^gs
+// with 2^gs (2, 4 or 8) the number of consecutive rows whose bytes are a
+// multiple of 16 (q6k_row_shift): the tensor map then takes 2^gs rows per
+// map row.
+int q6k_row_shift(int K);
+bool gemv_mma_supports(int type, int N, int K);
 
 // One launch for up to kMaxProj projection chunks of <= 8 tokens, all of one
 // type (12 = Q4_K, 14 = Q6_K, the latter only where gemv_mma_supports). With

@@ -172,6 +172,12 @@ WORKLOADS = {
     "qwen2.5-1.5b-layer": Workload("qwen2.5-1.5b-layer", "Qwen2.5-1.5B-shaped layer, all Q4_K",
                                    _layer(1536, 8960, 256, {}), 1, (1, 2, 4, 8), 100, 7, 10100,
                                    (1536, 1536, 1536, 8960)),
+    # Qwen2.5-1.5B-shaped layer in the Q4_K_M mix: attn_v and ffn_down Q6_K
+    # (rows of 6 and 35 super-blocks: 1260 and 7350 bytes, not 16-byte
+    # multiples), the rest Q4_K.
+    "qwen2.5-1.5b-q4km-layer": Workload("qwen2.5-1.5b-q4km-layer", "Qwen2.5-1.5B-shaped layer, Q4_K with Q6_K v/down",
+                                        _layer(1536, 8960, 256, {"v": Q6_K, "down": Q6_K}), 1, (1, 2, 4, 8),
+                                        600, 7, 10600, (1536, 1536, 1536, 8960)),
     # Qwen2.5-1.5B-shaped layer requantized to Q8_0 (the Q8_0 model of the
     # xLLM v0.7 article, section B3 + B4).
     "qwen2.5-1.5b-q8_0-layer": Workload("qwen2.5-1.5b-q8_0-layer", "Qwen2.5-1.5B-shaped layer, all Q8_0",

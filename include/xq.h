@@ -137,8 +137,13 @@ XQ_API xq_status xq_matmul_q4k_q8(const void *W, const void *xq, int M, int N, i
  *   W  : Q6_K bytes [N][K/256][210], device, read-only. Individual blocks are
  *        2-byte aligned (210 is not a multiple of 4); only the base pointer
  *        must be 16-byte aligned.
- * Dispatch at M <= 64: the tensor-core GEMV when rows are 16-byte multiples
- * (K a multiple of 2048), else a dp4a GEMV; M > 64: the tile kernel. */
+ * Dispatch at M <= 64, by shape only (never by M): the tensor-core GEMV when
+ * rows are 16-byte multiples (K a multiple of 2048); otherwise, with g = 8, 4
+ * or 2 the smallest count of consecutive rows whose bytes are a multiple of
+ * 16, the tensor-core GEMV over g rows per tensor-map row when N is a
+ * multiple of 16g and N >= 8192, else a dp4a GEMV. (xq_layer_mixed, which
+ * splits long rows over K in its workspace, takes the tensor-core GEMV
+ * whenever N is a multiple of 16g.) M > 64: the tile kernel. */
 XQ_API xq_status xq_matmul_q6k_q8(const void *W, const void *xq, int M, int N, int K,
                            float *y, xq_stream stream);
 

@@ -203,6 +203,28 @@ def test_shapes_all_m(xq, qtype, N, K):
     assert max(errs) > 0.0
 
 
+# Q6_K rows that are not 16-byte multiples on the tensor-core GEMV: the
+# tensor map takes 2^gs consecutive rows per map row (g = 8 for an odd
+# super-block count, 4 for 2 mod 4, 2 for 4 mod 8), N a multiple of 16g. A
+# single matmul takes that path from 128 row blocks of 64 (N >= 8192); the
+# narrower shapes above run on the dp4a kernel. The layer test below takes it
+# at N = 256 and 1536 with split-K.
+Q6K_GROUPED = [(8192, 2304), (8192, 1536), (8192, 1024), (8448, 4864)]
+
+
+@pytest.mark.parametrize("N,K", Q6K_GROUPED)
+def test_q6k_grouped_rows_all_m(xq, N, K):
+    errs = [run_and_check(xq, synth.Q6_K, N, K, M, 61 * N + K, 13 * M + N) for M in range(1, 9)]
+    assert max(errs) > 0.0
+
+
+@pytest.mark.parametrize("M", [1, 2, 8, 20, 80])
+def test_qwen25_q4km_layer(xq, M):
+    # Q6_K attn_v (K = 1536) and ffn_down (K = 8960, split over K at M <= 8)
+    # beside Q4_K, through every path by M
+    assert layer_check(xq, synth.WORKLOADS["qwen2.5-1.5b-q4km-layer"], M) > 0
+
+
 # Q8_0 above 64 tokens: the tile kernel with per-block row scales, ragged N
 # and M, every int8 value as a quant against +-1000 activations.
 @pytest.mark.parametrize("N,K,M", [(130, 1024, 65), (37, 256, 200), (300, 2048, 129)])
