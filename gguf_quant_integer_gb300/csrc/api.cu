@@ -253,8 +253,19 @@ xq_status run_one(const xq_proj& q, const uint8_t* q8, int M, cudaStream_t s) {
   return run_matmul(q.type, q.W, q8, M, q.N, q.K, q.y, nullptr, s, false, cbp);
 }
 
+// The SwiGLU feed fused into a layer's matmul launches (M <= 8): gate, up and
+// down index proj; arrive and ready are zeroed counters (F/32 and F/256
+// words), hq is h's Q8 buffer, which down reads.
+struct FfnSpec {
+  int gate, up, down;
+  unsigned int* arrive;
+  unsigned int* ready;
+  uint8_t* hq;
+  int F;
+};
+
 xq_status layer_matmuls(const xq_proj* proj, int n_proj, const uint8_t* const* q8, int M, const Sched& sc,
-                        uint8_t* sched, cudaStream_t s) {
+                        uint8_t* sched, cudaStream_t s, const FfnSpec* ffn = nullptr) {
   if (M > kMaxGemvM) {
     // 8 < M <= 64: per weight type, grouped GEMV launches over every
     // (projection, 8-token chunk) pair, kMaxProj pairs per launch, the chunks
@@ -349,15 +360,29 @@ xq_status layer_matmuls(const xq_proj* proj, int n_proj, const uint8_t* const* q
   // nothing it writes, and its CTAs trigger their launch only after their own
   // wait for the quantizer. They wait for the earlier grids before exiting,
   // which keeps the stream's order for the kernels that follow.
+  // With a fused SwiGLU feed, gate and up's weight type launches first; the
+  // launch that holds them writes h, and a down projection of another type
+  // waits for that grid.
+  int type_order[kTypes];
+  {
+    int k = 0;
+    const int first = ffn ? type_index(proj[ffn->gate].type) : 0;
+    type_order[k++] = first;
+    for (int g = 0; g < kTypes; ++g)
+      if (g != first) type_order[k++] = g;
+  }
   bool first_launch = true;
-  for (int g = 0; g < kTypes; ++g) {
+  for (int gi = 0; gi < kTypes; ++gi) {
+    const int g = type_order[gi];
     const int type = kTypeIds[g];
     xq::MmaProj items[xq::kMaxProj];
+    int item_proj[xq::kMaxProj];
     int n = 0;
     for (int p = 0; p <= n_proj; ++p) {
       if (p < n_proj) {
         const xq_proj& q = proj[p];
         if (!in_group(q, M) || q.type != type) continue;
+        item_proj[n] = p;
         xq::MmaProj& it = items[n++];
         it.W = static_cast<const uint8_t*>(q.W);
         it.xq = q8[p];
@@ -371,7 +396,33 @@ xq_status layer_matmuls(const xq_proj* proj, int n_proj, const uint8_t* const* q
         set_codebook(q, it);
       }
       if (n > 0 && (n == xq::kMaxProj || p == n_proj)) {
-        if (xq::launch_gemv_mma(type, items, n, s, true, counter[g], arrive[g], partial[g], first_launch) !=
+        xq::FfnFuse fz;
+        const xq::FfnFuse* fzp = nullptr;
+        bool wait = first_launch;
+        if (ffn) {
+          int ig = -1, iu = -1, id = -1;
+          for (int k = 0; k < n; ++k) {
+            if (item_proj[k] == ffn->gate) ig = k;
+            if (item_proj[k] == ffn->up) iu = k;
+            if (item_proj[k] == ffn->down) id = k;
+          }
+          if ((ig >= 0) != (iu >= 0)) return XQ_ERR_UNSUPPORTED;  // excluded by the plan
+          if (ig >= 0) {
+            fz.gate = ig;
+            fz.up = iu;
+            fz.down = id;
+            fz.arrive = ffn->arrive;
+            fz.ready = ffn->ready;
+            fz.hq = ffn->hq;
+            fz.h_out = nullptr;
+            fz.F = ffn->F;
+            fz.M = M;
+            fzp = &fz;
+          } else if (id >= 0) {
+            wait = true;  // h comes from an earlier grid
+          }
+        }
+        if (xq::launch_gemv_mma(type, items, n, s, true, counter[g], arrive[g], partial[g], wait, false, fzp) !=
             cudaSuccess)
           return XQ_ERR_CUDA;
         first_launch = false;
@@ -714,6 +765,14 @@ namespace {
 // with down (group C), so that the projections that do not depend on gate
 // and up share down's grouped launch. Workspace: the inputs' Q8 buffers,
 // h's Q8 buffer, then the scheduling state of A and of C.
+//
+// At M <= 8, when gate and up share one grouped launch, the feed is fused
+// instead: the Q8 quantization of every input, then the layer's grouped
+// launches (gate and up's type first), whose gate/up warps write h's Q8
+// themselves; a down projection in the same launch waits per super-block
+// for h, one in a later launch for the grid. Workspace: the inputs' Q8
+// buffers, h's Q8 buffer, h's block counters, then the layer's scheduling
+// state (the quantize launch zeroes the counters and the state).
 struct FfnPlan {
   xq_proj a[2], c[64];
   int n_c;
@@ -722,6 +781,10 @@ struct FfnPlan {
   size_t off[64];
   size_t h_off, sched_a, sched_c, total;
   Sched sc_a, sc_c;
+  bool fused;
+  xq_proj all[64];  // fused: the layer with down as it is (its input unused)
+  Sched sc_all;
+  size_t ffn_off, ffn_bytes, sched_all;
 };
 
 xq_status ffn_plan(const xq_proj* proj, int n_proj, int n_inputs, int M, int gate, int up, int down, FfnPlan* f) {
@@ -756,6 +819,25 @@ xq_status ffn_plan(const xq_proj* proj, int n_proj, int n_inputs, int M, int gat
   }
   f->h_off = need;
   need += round256(xq_q8_bytes(M, d.K));
+  // fused feed: gate and up in the GEMV group, in one launch of their type
+  f->fused = false;
+  if (M >= 1 && M <= kMaxGemvM && in_group(proj[gate], M) && in_group(proj[up], M) &&
+      proj[gate].type == proj[up].type) {
+    int same = 0;
+    for (int p = 0; p < n_proj; ++p) same += (in_group(proj[p], M) && proj[p].type == proj[gate].type) ? 1 : 0;
+    f->fused = same <= xq::kMaxProj;
+  }
+  if (f->fused) {
+    for (int p = 0; p < n_proj; ++p) f->all[p] = proj[p];
+    f->sc_all = sched_layout(f->all, n_proj, M);
+    f->ffn_off = need;
+    f->ffn_bytes = round256(4 * static_cast<size_t>(d.K / 32 + d.K / 256));
+    need += f->ffn_bytes;
+    f->sched_all = need;
+    need += sched_bytes(f->sc_all);
+    f->total = need;
+    return XQ_OK;
+  }
   f->sc_a = sched_layout(f->a, 2, M);
   f->sc_c = sched_layout(f->c, f->n_c, M);
   f->sched_a = need;
@@ -800,6 +882,41 @@ xq_status xq_layer_mixed_ffn(const xq_proj* proj, int n_proj, int gate, int up, 
   }
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (f.fused) {
+    // 1. every input to Q8 (the last launch zeroes h's counters and the
+    // layer's scheduling state, which follow one another)
+    xq::QuantJob jobs[xq::kMaxProj];
+    int n = 0, left = 0;
+    for (int i = 0; i < n_inputs; ++i) left += f.in_k[i] ? 1 : 0;
+    const int zero_words = static_cast<int>((f.ffn_bytes + sched_zero_bytes(f.sc_all)) / 4);
+    for (int i = 0; i < n_inputs; ++i) {
+      if (!f.in_k[i]) continue;
+      xq::QuantJob& j = jobs[n++];
+      j.x = inputs[i];
+      j.xq = ws + f.off[i];
+      j.M = M;
+      j.K = f.in_k[i];
+      --left;
+      if (n == xq::kMaxProj || left == 0) {
+        unsigned int* zero = left == 0 ? reinterpret_cast<unsigned int*>(ws + f.ffn_off) : nullptr;
+        if (xq::launch_quantize_q8(jobs, n, s, true, zero, zero_words) != cudaSuccess) return XQ_ERR_CUDA;
+        n = 0;
+      }
+    }
+    // 2. the layer's matmuls, h written by the gate and up warps
+    const uint8_t* q8[64];
+    for (int p = 0; p < n_proj; ++p) q8[p] = p == down ? ws + f.h_off : ws + f.off[proj[p].input];
+    const int F = proj[down].K;
+    FfnSpec spec;
+    spec.gate = gate;
+    spec.up = up;
+    spec.down = down;
+    spec.arrive = reinterpret_cast<unsigned int*>(ws + f.ffn_off);
+    spec.ready = spec.arrive + F / 32;
+    spec.hq = ws + f.h_off;
+    spec.F = F;
+    return layer_matmuls(f.all, n_proj, q8, M, f.sc_all, ws + f.sched_all, s, &spec);
+  }
   // 1. every input to Q8 (the last launch zeroes A's scheduling state)
   {
     xq::QuantJob jobs[xq::kMaxProj];

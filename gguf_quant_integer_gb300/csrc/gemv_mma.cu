@@ -58,6 +58,7 @@
 // records an error code and returns.
 #include <cuda.h>
 
+#include "q8_block.cuh"
 #include "xq_common.cuh"
 #include "xq_ptx.cuh"
 
@@ -83,8 +84,25 @@ struct Proj {
   int gs;                // Q6_K grouped view: 2^gs consecutive rows form one tensor-map row (else 0)
 };
 
+// The SwiGLU feed of a down projection computed inside the launch that runs
+// gate and up: h = silu(y_gate) * y_up, quantized to Q8 (qs, d8, s8 and the
+// GEMV operand image) by the warp that completes a 32-row block of gate and
+// up, then counted ready per super-block. A down projection in the same
+// launch waits, per super-block, for those counts before copying its
+// activations; one in a later launch reads h after this grid completes.
+struct Ffn {
+  unsigned int* arrive;  // per 32-block of h: gate and up warps done with its rows (4 = all); null: no feed
+  unsigned int* ready;   // per super-block of h: 32-blocks written (8 = all)
+  uint8_t* hq;           // h's Q8 buffer
+  float* h_out;          // optional fp32 copy of h [M][F]
+  unsigned long long qs, d8, s8, frag, fsc;  // region offsets in hq
+  int gate, up, down;    // slots in Group::p (down -1: not in this launch)
+  int F, M;              // h features (N of gate and up, K of down), tokens (<= 8)
+};
+
 struct Group {
   Proj p[kMaxProj];
+  Ffn ffn;
   unsigned int* counter;  // dynamic task counter (zeroed before launch) or null
   long long wait_limit;   // clocks a wait may take before it records an error and gives up
   int stall;              // test hook: the producer issues no stage, so the consumers' first waits run out
@@ -589,6 +607,137 @@ __device__ __forceinline__ void reduce_chunks(const Proj& P, int rg, int n8, int
   store_y(P, rg, n8, t, v[0], v[1], v[2], v[3]);
 }
 
+// A consumer warp has written the final y of 16-row group rg of gate or up.
+// The warp that completes a 32-row block (the fourth of the two gate and two
+// up warps to arrive) computes that block of h for every token and writes
+// its Q8 bytes and operand image, then counts the block ready. Writers publish
+// with a fence before their relaxed increment (as the split hand-off does);
+// the fourth warp fences again before it reads the others' y. The proxy fence
+// makes the generic-proxy writes of h visible to the bulk copies (async
+// proxy) that read them.
+__device__ __noinline__ void ffn_arrive(const Group& G, int rg, int lane) {
+  const Ffn& F = G.ffn;
+  __syncwarp();
+  unsigned old = 0;
+  if (lane == 0) {
+    __threadfence();
+    old = atomicAdd(F.arrive + (rg >> 1), 1u);
+  }
+  old = __shfl_sync(0xffffffffu, old, 0);
+  if (old != 3u) return;
+  __threadfence();
+  // All tokens at once: lane l takes token n = l/4 and elements 8g..8g+7,
+  // g = l%4, of the block. The steps are those of q8_quantize_lane and
+  // swiglu (the same fp32 operations, the block max and quant sum taken over
+  // the token's 4 lanes instead of 32), so the bytes equal the quantize
+  // kernel's.
+  const int j = rg >> 1, nsub = F.F >> 5;
+  const int n = lane >> 2, g = lane & 3;
+  const bool live = n < F.M;
+  float v[8];
+  if (live) {
+    const size_t idx = static_cast<size_t>(n) * F.F + 32 * j + 8 * g;
+    const float4* gp = reinterpret_cast<const float4*>(G.p[F.gate].y + idx);
+    const float4* up = reinterpret_cast<const float4*>(G.p[F.up].y + idx);
+    const float4 g0 = __ldcg(gp), g1 = __ldcg(gp + 1), u0 = __ldcg(up), u1 = __ldcg(up + 1);
+    v[0] = swiglu(g0.x, u0.x);
+    v[1] = swiglu(g0.y, u0.y);
+    v[2] = swiglu(g0.z, u0.z);
+    v[3] = swiglu(g0.w, u0.w);
+    v[4] = swiglu(g1.x, u1.x);
+    v[5] = swiglu(g1.y, u1.y);
+    v[6] = swiglu(g1.z, u1.z);
+    v[7] = swiglu(g1.w, u1.w);
+    if (F.h_out) {
+      float4* hp = reinterpret_cast<float4*>(F.h_out + idx);
+      hp[0] = make_float4(v[0], v[1], v[2], v[3]);
+      hp[1] = make_float4(v[4], v[5], v[6], v[7]);
+    }
+  } else {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) v[e] = 0.0f;
+  }
+  // amax over the token's 32 values: IEEE bit patterns of |x| order like the values
+  unsigned ab = 0;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) ab = max(ab, __float_as_uint(fabsf(v[e])));
+  ab = max(ab, __shfl_xor_sync(0xffffffffu, ab, 1));
+  ab = max(ab, __shfl_xor_sync(0xffffffffu, ab, 2));
+  const float d = __fdiv_rn(__uint_as_float(ab), 127.0f);
+  const float id = (d != 0.0f) ? __frcp_rn(d) : 0.0f;
+  int q[8], isum = 0;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    float x = roundf(__fmul_rn(v[e], id));
+    x = (x != x) ? 0.0f : x;
+    x = x > 127.0f ? 127.0f : (x < -127.0f ? -127.0f : x);
+    q[e] = static_cast<int>(x);
+    isum += q[e];
+  }
+  isum += __shfl_xor_sync(0xffffffffu, isum, 1);
+  isum += __shfl_xor_sync(0xffffffffu, isum, 2);
+  const float sc = __fmul_rn(d, static_cast<float>(isum));
+  if (live) {
+    uint2 qb;
+    qb.x = (q[0] & 255) | (q[1] & 255) << 8 | (q[2] & 255) << 16 | static_cast<unsigned>(q[3] & 255) << 24;
+    qb.y = (q[4] & 255) | (q[5] & 255) << 8 | (q[6] & 255) << 16 | static_cast<unsigned>(q[7] & 255) << 24;
+    *reinterpret_cast<uint2*>(F.hq + F.qs + static_cast<size_t>(n) * F.F + 32 * j + 8 * g) = qb;
+    if (g == 0) {
+      reinterpret_cast<float*>(F.hq + F.d8)[static_cast<size_t>(n) * nsub + j] = d;
+      reinterpret_cast<float*>(F.hq + F.s8)[static_cast<size_t>(n) * nsub + j] = sc;
+    }
+  }
+  // GEMV image (chunk 0): the lane's 8 fp16 quants fill operand slots
+  // 0..7 of (token n, quad g), slot s holding element perm(s), perm =
+  // 0,2,1,3,4,6,5,7 (write_gemv_image's order); padding tokens write zeros.
+  {
+    const __half2 h01 = __halves2half2(__int2half_rn(q[0]), __int2half_rn(q[2]));
+    const __half2 h23 = __halves2half2(__int2half_rn(q[1]), __int2half_rn(q[3]));
+    const __half2 h45 = __halves2half2(__int2half_rn(q[4]), __int2half_rn(q[6]));
+    const __half2 h67 = __halves2half2(__int2half_rn(q[5]), __int2half_rn(q[7]));
+    uint4 w;
+    w.x = *reinterpret_cast<const unsigned*>(&h01);
+    w.y = *reinterpret_cast<const unsigned*>(&h23);
+    w.z = *reinterpret_cast<const unsigned*>(&h45);
+    w.w = *reinterpret_cast<const unsigned*>(&h67);
+    reinterpret_cast<uint4*>(F.hq + F.frag)[static_cast<size_t>(j) * 32 + 4 * n + g] = w;
+    if (g == 0) {
+      float* fsc = reinterpret_cast<float*>(F.hq + F.fsc);
+      const size_t base = (static_cast<size_t>(j) * 4 + (n >> 1)) * 4;
+      fsc[base + (n & 1)] = d;
+      fsc[base + 2 + (n & 1)] = sc;
+    }
+  }
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+  __syncwarp();
+  if (lane == 0) {
+    __threadfence();
+    atomicAdd(F.ready + (j >> 3), 1u);
+  }
+}
+
+// The down projection's producer before copying super-block b of h: wait
+// (bounded) until its eight 32-blocks are written.
+__device__ __forceinline__ bool ffn_wait_ready(const Group& G, int b) {
+  const unsigned int* f = G.ffn.ready + b;
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(f) : "memory");
+  if (v < 8u) {
+    const long long t0 = clock64();
+    for (;;) {
+      __nanosleep(100);
+      asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(f) : "memory");
+      if (v >= 8u) break;
+      if (clock64() - t0 > G.wait_limit) {
+        atomicExch(&g_gemv_error, 3u);
+        return false;
+      }
+    }
+  }
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+  return true;
+}
+
 // Tasks after each CTA's first (its own index): from the counter, which
 // starts at zero, offset by the grid size; or strided by the grid size.
 // A producer fetches once per task it runs, so a launch makes exactly
@@ -755,7 +904,7 @@ __device__ __forceinline__ TaskPos task_pos(const Group& G, int task);
 
 // Consumer loop of the small form (the same ring, meta, task and split
 // protocol as the MMA consumers).
-template <bool ISUM>
+template <bool ISUM, bool FFN>
 __device__ __forceinline__ void small_consumer(const Group& G, const uint8_t* ring, const int4* meta, uint32_t full_s,
                                                uint32_t empty_s, int kStages, int kStageBytes, int kBlockBytes,
                                                int kFragOff, int warp, int lane) {
@@ -777,6 +926,7 @@ __device__ __forceinline__ void small_consumer(const Group& G, const uint8_t* ri
       __syncwarp();
       if (lane == 0) Q.arrive[pend_rg] = 0u;
       reduce_chunks_small(Q, pend_rg, r, h);
+      if (FFN && (pend_p == G.ffn.gate || pend_p == G.ffn.up)) ffn_arrive(G, pend_rg, lane);
     }
     pend_p = -1;
   };
@@ -815,6 +965,7 @@ __device__ __forceinline__ void small_consumer(const Group& G, const uint8_t* ri
       if (P.nch == 1) {
         if (h == 1 && row < P.N)
           for (int t = 0; t < P.M; ++t) P.y[static_cast<size_t>(t) * P.N + row] = v[t];
+        if (FFN && rg * 16 < P.N && (tp.p == G.ffn.gate || tp.p == G.ffn.up)) ffn_arrive(G, rg, lane);
       } else if (rg * 16 < P.N) {
         const int rows_pad = gemv_row_blocks(P.N) * kGemvRows;
         float* part = P.partial + static_cast<size_t>(tp.c) * 8 * rows_pad;
@@ -836,7 +987,7 @@ __device__ __forceinline__ void small_consumer(const Group& G, const uint8_t* ri
   }
 }
 
-template <int TYPE, bool ISUM, bool SMALL>
+template <int TYPE, bool ISUM, bool SMALL, bool FFN>
 __device__ __forceinline__ void gemv_mma_body(const Group& G) {
   // Body of gemv_mma_kernel: a return here leaves through the kernel's
   // deferred dependency wait.
@@ -903,6 +1054,7 @@ __device__ __forceinline__ void gemv_mma_body(const Group& G) {
       const Proj& P = G.p[tp.p];
       for (int k = 0; k < slot; ++k) {
         const uint32_t st = ring_s + k * kStageBytes;
+        if (FFN && tp.p == G.ffn.down && !ffn_wait_ready(G, tp.b0 + k)) return;
         act_load<TYPE, SMALL>(st, P, tp.b0 + k, full_s + 8 * k);
       }
     }
@@ -934,6 +1086,7 @@ __device__ __forceinline__ void gemv_mma_body(const Group& G) {
           weight_box<TYPE>(P, tp.rb * kGemvWarps + w, b, bx, by);
           tma_load_2d(st + w * kBlockBytes, &P.map, bx, by, full_s + 8 * slot);
         }
+        if (FFN && tp.p == G.ffn.down && !ffn_wait_ready(G, b)) return;
         act_load<TYPE, SMALL>(st, P, b, full_s + 8 * slot);
         if (++slot == kStages) {
           slot = 0;
@@ -948,7 +1101,7 @@ __device__ __forceinline__ void gemv_mma_body(const Group& G) {
   if (G.wait_prev) cudaGridDependencySynchronize();
   cudaTriggerProgrammaticLaunchCompletion();
   if constexpr (SMALL) {
-    small_consumer<ISUM>(G, ring, meta, full_s, empty_s, kStages, kStageBytes, kBlockBytes, kFragOff, warp, lane);
+    small_consumer<ISUM, FFN>(G, ring, meta, full_s, empty_s, kStages, kStageBytes, kBlockBytes, kFragOff, warp, lane);
     return;
   }
   const int n8 = lane >> 2, t = lane & 3;
@@ -979,6 +1132,7 @@ __device__ __forceinline__ void gemv_mma_body(const Group& G) {
       __syncwarp();
       if (lane == 0) Q.arrive[pend_rg] = 0u;  // ready for the next launch
       reduce_chunks(Q, pend_rg, n8, t);
+      if (FFN && (pend_p == G.ffn.gate || pend_p == G.ffn.up)) ffn_arrive(G, pend_rg, lane);
     }
     pend_p = -1;
   };
@@ -1038,7 +1192,10 @@ __device__ __forceinline__ void gemv_mma_body(const Group& G) {
       run[0] = run[1] = tot[0] = tot[1] = 0ull;
       nrun = 0;
       if (P.nch == 1) {
-        if (rows_ok) store_y(P, rg, n8, t, lo32(acc[0]), hi32(acc[0]), lo32(acc[1]), hi32(acc[1]));
+        if (rows_ok) {
+          store_y(P, rg, n8, t, lo32(acc[0]), hi32(acc[0]), lo32(acc[1]), hi32(acc[1]));
+          if (FFN && (tp.p == G.ffn.gate || tp.p == G.ffn.up)) ffn_arrive(G, rg, lane);
+        }
       } else if (rows_ok) {
         // K-chunk partial of a split task; the last warp to finish the row
         // group adds the chunks in chunk order. Lane 0's fence, after the
@@ -1067,10 +1224,10 @@ __device__ __forceinline__ void gemv_mma_body(const Group& G) {
   }
 }
 
-template <int TYPE, bool ISUM, bool SMALL>
+template <int TYPE, bool ISUM, bool SMALL, bool FFN>
 __global__ void __launch_bounds__(32 * (kGemvWarps + 1), kGemvCtasPerSM)
 gemv_mma_kernel(const __grid_constant__ Group G) {
-  gemv_mma_body<TYPE, ISUM, SMALL>(G);
+  gemv_mma_body<TYPE, ISUM, SMALL, FFN>(G);
   // A launch that did not wait for the previous grid on entry waits before
   // its threads exit, so that its completion still implies the completion of
   // every earlier kernel on the stream (the next kernel's dependency wait
@@ -1078,14 +1235,15 @@ gemv_mma_kernel(const __grid_constant__ Group G) {
   if (!G.wait_prev) cudaGridDependencySynchronize();
 }
 
-template <int TYPE, bool ISUM, bool SMALL = false>
+template <int TYPE, bool ISUM, bool SMALL = false, bool FFN = false>
 int max_ctas() {
   static int per_sm = -1;
   if (per_sm < 0) {
     int n = 0;
     constexpr int kSmemBytes = GLay<TYPE>::kSmemBytes;
-    cudaFuncSetAttribute(gemv_mma_kernel<TYPE, ISUM, SMALL>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, gemv_mma_kernel<TYPE, ISUM, SMALL>, 32 * (kGemvWarps + 1),
+    cudaFuncSetAttribute(gemv_mma_kernel<TYPE, ISUM, SMALL, FFN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         kSmemBytes);
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, gemv_mma_kernel<TYPE, ISUM, SMALL, FFN>, 32 * (kGemvWarps + 1),
                                                       kSmemBytes) != cudaSuccess ||
         n < 1)
       n = 1;
@@ -1177,14 +1335,31 @@ bool gemv_mma_supports(int type, int N, int K) {
 }
 
 cudaError_t launch_gemv_mma(int type, const MmaProj* projs, int n, cudaStream_t s, bool pdl, unsigned int* counter,
-                            uint8_t* arrive_ws, uint8_t* partial_ws, bool wait_prev, bool stall_test) {
+                            uint8_t* arrive_ws, uint8_t* partial_ws, bool wait_prev, bool stall_test,
+                            const FfnFuse* ffn) {
   if (n <= 0 || n > kMaxProj || (type != 12 && type != 14 && type != 8 && type != 23)) return cudaErrorInvalidValue;
+  if (ffn) {
+    const bool ok = ffn->gate >= 0 && ffn->gate < n && ffn->up >= 0 && ffn->up < n && ffn->gate != ffn->up &&
+                    ffn->down < n && ffn->down != ffn->gate && ffn->down != ffn->up && ffn->arrive && ffn->ready &&
+                    ffn->hq && ffn->M >= 1 && ffn->M <= 8 && (ffn->F % 256) == 0 && projs[ffn->gate].N == ffn->F &&
+                    projs[ffn->up].N == ffn->F && projs[ffn->gate].M_total == ffn->M &&
+                    projs[ffn->up].M_total == ffn->M && projs[ffn->gate].chunk == 0 && projs[ffn->up].chunk == 0 &&
+                    (ffn->down < 0 || (projs[ffn->down].K == ffn->F && projs[ffn->down].xq == ffn->hq &&
+                                       projs[ffn->down].M_total == ffn->M));
+    if (!ok) return cudaErrorInvalidValue;
+  }
   // Per-projection K-chunking (only with split workspaces) and task cost.
   const bool split = arrive_ws != nullptr && partial_ws != nullptr;
   int nch[kMaxProj], cost[kMaxProj];
   for (int k = 0; k < n; ++k) {
     nch[k] = (split && projs[k].nch > 1) ? projs[k].nch : 1;
     cost[k] = ((projs[k].K >> 8) + nch[k] - 1) / nch[k];
+  }
+  // With a fused feed, gate and up go first, so that h is complete about when
+  // the first wave of tasks ends, and down goes last: its tasks wait for h.
+  if (ffn) {
+    cost[ffn->gate] = cost[ffn->up] = 1 << 30;
+    if (ffn->down >= 0) cost[ffn->down] = -1;
   }
   // Most expensive tasks first (dynamic scheduling takes them in order).
   int order[kMaxProj];
@@ -1210,6 +1385,27 @@ cudaError_t launch_gemv_mma(int type, const MmaProj* projs, int n, cudaStream_t 
   Group G;
   G.n = n;
   G.counter = counter;
+  G.ffn = Ffn{};
+  G.ffn.gate = G.ffn.up = G.ffn.down = -1;
+  if (ffn) {
+    const Q8Layout H = q8_layout(ffn->M, ffn->F, false);
+    G.ffn.arrive = ffn->arrive;
+    G.ffn.ready = ffn->ready;
+    G.ffn.hq = ffn->hq;
+    G.ffn.h_out = ffn->h_out;
+    G.ffn.qs = H.qs;
+    G.ffn.d8 = H.d8;
+    G.ffn.s8 = H.s8;
+    G.ffn.frag = H.frag;
+    G.ffn.fsc = H.fsc;
+    G.ffn.F = ffn->F;
+    G.ffn.M = ffn->M;
+    for (int k = 0; k < n; ++k) {
+      if (order[k] == ffn->gate) G.ffn.gate = k;
+      if (order[k] == ffn->up) G.ffn.up = k;
+      if (order[k] == ffn->down) G.ffn.down = k;
+    }
+  }
   G.wait_prev = (wait_prev || !pdl) ? 1 : 0;
   G.stall = stall_test ? 1 : 0;
   G.wait_limit = stall_test ? kStallWaitClocks : kWaitClocks;
@@ -1253,7 +1449,16 @@ cudaError_t launch_gemv_mma(int type, const MmaProj* projs, int n, cudaStream_t 
   }
   G.total = total;
   if (total == 0) return cudaSuccess;
-  const int cap = small        ? (isum ? max_ctas<12, true, true>() : max_ctas<12, false, true>())
+  // The fused SwiGLU feed has its own instantiations (without the isum
+  // hook), so that other launches carry none of its code.
+  const bool fz = ffn != nullptr;
+  if (fz && isum) return cudaErrorInvalidValue;
+  const int cap = fz ? (small ? max_ctas<12, false, true, true>()
+                       : type == 12 ? max_ctas<12, false, false, true>()
+                       : type == 8  ? max_ctas<8, false, false, true>()
+                       : type == 23 ? max_ctas<23, false, false, true>()
+                                    : max_ctas<14, false, false, true>())
+                  : small      ? (isum ? max_ctas<12, true, true>() : max_ctas<12, false, true>())
                   : type == 12 ? (isum ? max_ctas<12, true>() : max_ctas<12, false>())
                   : type == 8  ? (isum ? max_ctas<8, true>() : max_ctas<8, false>())
                   : type == 23 ? (isum ? max_ctas<23, true>() : max_ctas<23, false>())
@@ -1270,20 +1475,27 @@ cudaError_t launch_gemv_mma(int type, const MmaProj* projs, int n, cudaStream_t 
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
+  if (fz) {
+    if (small) return cudaLaunchKernelEx(&cfg, gemv_mma_kernel<12, false, true, true>, G);
+    if (type == 12) return cudaLaunchKernelEx(&cfg, gemv_mma_kernel<12, false, false, true>, G);
+    if (type == 8) return cudaLaunchKernelEx(&cfg, gemv_mma_kernel<8, false, false, true>, G);
+    if (type == 23) return cudaLaunchKernelEx(&cfg, gemv_mma_kernel<23, false, false, true>, G);
+    return cudaLaunchKernelEx(&cfg, gemv_mma_kernel<14, false, false, true>, G);
+  }
   if (type == 8)
-    return isum ? cudaLaunchKernelEx(&cfg, gemv_mma_kernel<8, true, false>, G)
-                : cudaLaunchKernelEx(&cfg, gemv_mma_kernel<8, false, false>, G);
+    return isum ? cudaLaunchKernelEx(&cfg, gemv_mma_kernel<8, true, false, false>, G)
+                : cudaLaunchKernelEx(&cfg, gemv_mma_kernel<8, false, false, false>, G);
   if (type == 23)
-    return isum ? cudaLaunchKernelEx(&cfg, gemv_mma_kernel<23, true, false>, G)
-                : cudaLaunchKernelEx(&cfg, gemv_mma_kernel<23, false, false>, G);
+    return isum ? cudaLaunchKernelEx(&cfg, gemv_mma_kernel<23, true, false, false>, G)
+                : cudaLaunchKernelEx(&cfg, gemv_mma_kernel<23, false, false, false>, G);
   if (small)
-    return isum ? cudaLaunchKernelEx(&cfg, gemv_mma_kernel<12, true, true>, G)
-                : cudaLaunchKernelEx(&cfg, gemv_mma_kernel<12, false, true>, G);
+    return isum ? cudaLaunchKernelEx(&cfg, gemv_mma_kernel<12, true, true, false>, G)
+                : cudaLaunchKernelEx(&cfg, gemv_mma_kernel<12, false, true, false>, G);
   if (type == 12)
-    return isum ? cudaLaunchKernelEx(&cfg, gemv_mma_kernel<12, true, false>, G)
-                : cudaLaunchKernelEx(&cfg, gemv_mma_kernel<12, false, false>, G);
-  return isum ? cudaLaunchKernelEx(&cfg, gemv_mma_kernel<14, true, false>, G)
-              : cudaLaunchKernelEx(&cfg, gemv_mma_kernel<14, false, false>, G);
+    return isum ? cudaLaunchKernelEx(&cfg, gemv_mma_kernel<12, true, false, false>, G)
+                : cudaLaunchKernelEx(&cfg, gemv_mma_kernel<12, false, false, false>, G);
+  return isum ? cudaLaunchKernelEx(&cfg, gemv_mma_kernel<14, true, false, false>, G)
+              : cudaLaunchKernelEx(&cfg, gemv_mma_kernel<14, false, false, false>, G);
 }
 
 }  // namespace xq

@@ -2,16 +2,9 @@
 // scale*sum per block of 32 (the q8_1 kind; xLLM v0.7 article, sections B1.3
 // and C.1; Agent Telemetry log, "批次化 MMVQ").
 //
-// One warp per 32-block, one element per lane:
-//   amax = max |x|          (warp max over the IEEE bit patterns of |x|)
-//   d8   = amax / 127       (IEEE round-to-nearest divide)
-//   id   = 1 / d8, 0 if d8 == 0 (IEEE round-to-nearest reciprocal)
-//   q    = clamp(roundf(x * id), -127, 127), roundf = half away from zero,
-//          clamped in float (NaN -> 0) before the int conversion
-//   s8   = d8 * (float)sum(q)
-// Each step is one correctly rounded fp32 operation, written with explicit
-// _rn intrinsics so that no contraction or fast-math substitution can change
-// a bit. The result is therefore the same on any IEEE implementation that
+// One warp per 32-block, one element per lane, by the steps of
+// q8_quantize_lane (q8_block.cuh): each one correctly rounded fp32
+// operation, so the result is the same on any IEEE implementation that
 // performs the same steps.
 //
 // The same pass writes the tensor-core operand image of the quants, so that
@@ -20,6 +13,7 @@
 // 128-token tiles of the tcgen05 B operand, their d8 rows and the three-piece
 // bf16 split of s8 (layouts in xq_common.cuh). One launch serves all inputs
 // of a layer.
+#include "q8_block.cuh"
 #include "xq_common.cuh"
 
 namespace xq {
@@ -80,11 +74,8 @@ quantize_q8_kernel(const __grid_constant__ QuantGroup G) {
   cudaTriggerProgrammaticLaunchCompletion();
   if (blockIdx.x == 0)
     for (int i = threadIdx.x; i < G.zero_count; i += blockDim.x) G.zero_words[i] = 0u;
-  // Position of this lane's element inside its lane's 8 operand slots:
-  // slot order is perm = 0,2,1,3,4,6,5,7 (an involution), so slot = perm[l & 7].
-  const int t = lane >> 3;
-  const int i = lane & 7;
-  const int slot = (i == 1 || i == 2 || i == 5 || i == 6) ? (i ^ 3) : i;
+  // Position of this lane's element inside its lane's 8 operand slots.
+  const int slot = gemv_image_slot(lane);
 
   int jb = 0;
   for (unsigned blk = warp; blk < total; blk += nwarps) {
@@ -102,26 +93,14 @@ quantize_q8_kernel(const __grid_constant__ QuantGroup G) {
       const size_t idx = static_cast<size_t>(m) * J.K + 32 * j + lane;
       float v = __ldg(J.x + idx);
       if (J.up) {
-        // SwiGLU feed of the down projection: h = silu(g) * u = g / (1 + e^-g) * u,
-        // each step one fp32 operation (CUDA's expf, IEEE add, divide and
-        // multiply); g -> -inf gives e^-g = inf and h = +-0.
-        const float e = expf(-v);
-        v = __fmul_rn(__fdiv_rn(v, __fadd_rn(1.0f, e)), __ldg(J.up + idx));
+        // SwiGLU feed of the down projection
+        v = swiglu(v, __ldg(J.up + idx));
         if (J.h_out) J.h_out[idx] = v;
       }
-      // |x| >= 0, so its IEEE bit pattern orders like the value itself.
-      const unsigned amax_bits = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(v)));
-      const float amax = __uint_as_float(amax_bits);
-      d = __fdiv_rn(amax, 127.0f);
-      const float id = (d != 0.0f) ? __frcp_rn(d) : 0.0f;
-      float r = roundf(__fmul_rn(v, id));
-      // Saturate in float: if 1/d8 overflowed (amax below ~1.5e-36), x*id is
-      // +-inf (-> +-127) or 0*inf = NaN (-> 0).
-      r = (r != r) ? 0.0f : r;
-      r = r > 127.0f ? 127.0f : (r < -127.0f ? -127.0f : r);
-      q = static_cast<int>(r);
-      const int isum = __reduce_add_sync(0xffffffffu, q);
-      s = __fmul_rn(d, static_cast<float>(isum));
+      const Q8Lane r = q8_quantize_lane(v);
+      q = r.q;
+      d = r.d;
+      s = r.s;
       J.xq[static_cast<size_t>(m) * J.K + 32 * j + lane] = static_cast<uint8_t>(static_cast<int8_t>(q));
       if (lane == 0) {
         reinterpret_cast<float*>(J.xq + L.d8)[static_cast<size_t>(m) * nsub + j] = d;
@@ -130,15 +109,7 @@ quantize_q8_kernel(const __grid_constant__ QuantGroup G) {
     }
     if (L.ttiles == 0) {
       // GEMV operand image (zeros for padding tokens)
-      const int c = m >> 3, n = m & 7;
-      __half* frag = reinterpret_cast<__half*>(J.xq + L.frag);
-      frag[((static_cast<size_t>(c) * nsub + j) * 32 + 4 * n + t) * 8 + slot] = __int2half_rn(q);
-      if (lane == 0) {
-        float* fsc = reinterpret_cast<float*>(J.xq + L.fsc);
-        const size_t base = ((static_cast<size_t>(c) * nsub + j) * 4 + (n >> 1)) * 4;
-        fsc[base + (n & 1)] = d;
-        fsc[base + 2 + (n & 1)] = s;
-      }
+      write_gemv_image(J.xq + L.frag, J.xq + L.fsc, nsub, m, j, lane, q, d, s);
     } else {
       // tile image: token r of tile tt, 32-block j = 8b + ib
       const int tt = m >> 7, r = m & 127, b = j >> 3, ib = j & 7;

@@ -230,9 +230,28 @@ bool gemv_mma_supports(int type, int N, int K);
 // stall_test (a test hook): the producer issues no stage and every wait is
 // limited to about 10^5 clocks, so the consumers' first waits run out,
 // record their error code and return; y is left unwritten.
+//
+// ffn (optional): the launch runs the gate and up projections of a SwiGLU
+// FFN (items ffn->gate and ffn->up, N = F, M <= 8, one chunk) and writes
+// h = silu(y_gate) * y_up as Q8 (layout q8_layout(M, F, false)) at ffn->hq,
+// counting each completed 32-block in ffn->arrive (F/32 words) and each
+// completed super-block's blocks in ffn->ready (F/256 words), both zero
+// before the launch. ffn->down >= 0: that item is the down projection (K =
+// F, reading ffn->hq); its tasks are placed after every other task, and its
+// activation copies wait for the ready counts. ffn->down < 0: down runs in a
+// later launch, which must wait for this grid's completion.
+struct FfnFuse {
+  int gate, up, down;
+  unsigned int* arrive;
+  unsigned int* ready;
+  uint8_t* hq;
+  float* h_out;  // optional fp32 copy of h [M][F]
+  int F, M;
+};
 cudaError_t launch_gemv_mma(int type, const MmaProj* projs, int n, cudaStream_t s, bool pdl,
                             unsigned int* counter = nullptr, uint8_t* arrive_ws = nullptr,
-                            uint8_t* partial_ws = nullptr, bool wait_prev = true, bool stall_test = false);
+                            uint8_t* partial_ws = nullptr, bool wait_prev = true, bool stall_test = false,
+                            const FfnFuse* ffn = nullptr);
 
 // Read and clear the error word each waiting kernel sets when a bounded wait
 // runs out (0: none since the last read). Synchronous device reads/writes.

@@ -257,12 +257,24 @@ XQ_API size_t xq_layer_ffn_workspace_bytes(const xq_proj *proj, int n_proj, int 
 /* xq_layer_mixed for a layer whose down projection reads silu(y_gate) * y_up
  * of the same call (gate, up, down: indices into proj; proj[down].input is
  * ignored; N of gate and up must equal K of down). Enqueues, in order on
- * `stream`: the Q8 quantization of every input; the gate and up projections;
- * one xq_silu_mul_quantize_q8 launch on their outputs; every other
- * projection together with down (grouped GEMV launches as in
- * xq_layer_mixed, split over K like the layer's; the tile kernel per
- * projection above 64 tokens). The
- * projections that do not depend on gate and up thus share down's launch. */
+ * `stream`, first the Q8 quantization of every input, then:
+ *  - at M <= 8, when gate and up fall in one grouped GEMV launch (the same
+ *    weight type, at most 8 projections of that type in the GEMV group):
+ *    the layer's grouped launches, gate and up's type first. The warps that
+ *    finish a 32-row block of gate and up compute that block of
+ *    h = silu(y_gate) * y_up and its Q8 bytes (the operations of
+ *    xq_silu_mul_quantize_q8, bit for bit). A down projection in the same
+ *    launch runs after every other task of it and waits for h per
+ *    256-feature super-block (bounded; see xq_device_error); one in a later
+ *    launch reads h after the grid completes.
+ *  - otherwise: the gate and up projections; one xq_silu_mul_quantize_q8
+ *    launch on their outputs; every other projection together with down
+ *    (grouped GEMV launches as in xq_layer_mixed, split over K like the
+ *    layer's; the tile kernel per projection above 64 tokens).
+ * Either way the workspace begins with the Q8 buffers of the inputs that
+ * are read (in input order, each padded to a multiple of 256 bytes),
+ * followed by h's Q8 buffer (xq_q8_bytes(M, K of down) bytes in the layout
+ * xq_quantize_q8 writes), which the call leaves there. */
 XQ_API xq_status xq_layer_mixed_ffn(const xq_proj *proj, int n_proj, int gate, int up, int down,
                              const float *const *inputs, int n_inputs, int M,
                              void *workspace, size_t ws_bytes, xq_stream stream);
@@ -308,7 +320,8 @@ XQ_API xq_status xq_layer_mixed_static(const xq_proj *proj, int n_proj,
  * (kernel << 8) | wait: kernel 1 = the warp-level MMA GEMV (M <= 64), 2 =
  * the tile kernel (M > 64); wait = the kernel's number of the wait that gave
  * up (GEMV: 1 the producer waiting for a free stage, 2 a consumer waiting for
- * a full one). If several kernels recorded one,
+ * a full one, 3 a down projection's producer waiting for h in the fused
+ * feed of xq_layer_mixed_ffn). If several kernels recorded one,
  * the lowest kernel number is reported and all are cleared. The reads and
  * writes are synchronous. XQ_ERR_ARG for a null code_out, XQ_ERR_CUDA if the
  * stream or the reads fail. */

@@ -62,6 +62,7 @@ def _load():
     lib.oracle_half_to_double.argtypes = [ctypes.c_uint16]
     lib.oracle_half_to_double.restype = ctypes.c_double
     lib.oracle_quantize_q8.argtypes = [P, I, I, P, P, P]
+    lib.oracle_silu_mul.argtypes = [P, P, I, P]
     lib.oracle_q4k_fields.argtypes = [P, P, P, P, P, P]
     lib.oracle_q4k_fields.restype = None
     lib.oracle_q6k_fields.argtypes = [P, P, P, P]
@@ -85,7 +86,7 @@ def _load():
     for name in ("oracle_quantize_q8", "oracle_dequant_q4k", "oracle_dequant_q6k",
                  "oracle_dequant_q8", "oracle_matmul_q4k_q8", "oracle_matmul_q6k_q8",
                  "oracle_gemv_f64", "oracle_dequant_q8_0", "oracle_matmul_q8_0_q8",
-                 "oracle_dequant_iq4xs", "oracle_matmul_iq4xs_q8"):
+                 "oracle_dequant_iq4xs", "oracle_matmul_iq4xs_q8", "oracle_silu_mul"):
         getattr(lib, name).restype = ctypes.c_int
     lib.oracle_set_threads(1)
     _lib = lib
@@ -115,6 +116,16 @@ def quantize_q8(x: np.ndarray):
     s8 = np.zeros((M, K // 32), np.float32)
     _check(_load().oracle_quantize_q8(_p(x), M, K, _p(qs), _p(d8), _p(s8)), "quantize_q8")
     return qs, d8, s8
+
+
+def silu_mul(g: np.ndarray, u: np.ndarray) -> np.ndarray:
+    """h = silu(g) * u = g / (1 + e^-g) * u in fp64, from fp32 g and u of one shape."""
+    g = np.ascontiguousarray(g, dtype=np.float32)
+    u = np.ascontiguousarray(u, dtype=np.float32)
+    assert g.shape == u.shape
+    h = np.zeros(g.shape, np.float64)
+    _check(_load().oracle_silu_mul(_p(g), _p(u), g.size, _p(h)), "silu_mul")
+    return h
 
 
 def q4k_fields(blk: np.ndarray):

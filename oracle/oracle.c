@@ -181,6 +181,23 @@ int oracle_quantize_q8(const float *x, int M, int K,
     return 0;
 }
 
+/* ------------------------------------------------------------ SwiGLU */
+
+/* The SwiGLU feed of the down projection, element by element in fp64 from
+ * fp32 inputs: h = silu(g) * u, silu(g) = g * sigma(g) = g / (1 + e^-g)
+ * (the gated activation between the gate/up and down matmuls of the layer
+ * dispatch in the Agent Telemetry log). g -> -inf gives e^-g = inf and
+ * h = +-0; g -> +inf gives h -> g * u. */
+int oracle_silu_mul(const float *g, const float *u, int n, double *h)
+{
+    if (n < 0) return 1;
+    for (int i = 0; i < n; i++) {
+        double gi = (double)g[i];
+        h[i] = gi / (1.0 + exp(-gi)) * (double)u[i];
+    }
+    return 0;
+}
+
 /* -------------------------------------------------------------- Q4_K */
 
 /* Decode one Q4_K super-block (144 bytes, 256 weights) into its fields.

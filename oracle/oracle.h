@@ -34,6 +34,9 @@ double oracle_half_to_double(uint16_t h);
 int oracle_quantize_q8(const float *x, int M, int K,
                        int8_t *qs, float *d8, float *s8);
 
+/* h[i] = silu(g[i]) * u[i] in fp64, silu(g) = g / (1 + e^-g). */
+int oracle_silu_mul(const float *g, const float *u, int n, double *h);
+
 void oracle_q4k_fields(const uint8_t *blk, double *d, double *dmin,
                        int sc[8], int mn[8], int q[256]);
 void oracle_q6k_fields(const uint8_t *blk, double *d, int s[16], int q[256]);

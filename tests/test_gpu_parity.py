@@ -514,17 +514,11 @@ def test_batch_invariant_rows(xq, qtype, N, K):
 
 # ------------------------------------------------------------ SwiGLU feed
 
-def silu_mul_ref(g, u):
-    g = g.astype(np.float64)
-    with np.errstate(over="ignore"):   # e^-g = inf for g << 0: h -> -0, as on the GPU
-        return g / (1.0 + np.exp(-g)) * u.astype(np.float64)
-
-
 def check_h(h_gpu, g, u):
     # e = expf(-g) is within 2 ulp (CUDA's documented bound); 1 + e, the
     # divide and the product are each rounded once: together within 8 ulp of
     # the exact silu(g) * u (relative 2^-20), or tiny where h underflows.
-    h_ref = silu_mul_ref(g, u)
+    h_ref = oracle.silu_mul(g, u)
     err = np.abs(h_gpu.astype(np.float64) - h_ref)
     assert np.all(err <= 2.0 ** -20 * np.abs(h_ref) + 1e-37), float(np.max(err / (np.abs(h_ref) + 1e-37)))
 
@@ -549,13 +543,26 @@ def test_silu_mul_quantize(xq, M, K):
     assert np.array_equal(s8.view(np.uint32), rs.view(np.uint32))
 
 
-@pytest.mark.parametrize("M", [1, 8, 20, 80])
-def test_ffn_layer_down_fed_by_silu_gate_up(xq, M):
-    """xq_layer_mixed_ffn on a Qwen2.5-1.5B-shaped layer: every projection
-    but down checked as in xq_layer_mixed; down checked against the oracle on
-    the Q8 of h recomputed (same kernel, h exported) from the gate and up
-    outputs the call wrote."""
-    wl = synth.WORKLOADS["qwen2.5-1.5b-layer"]
+# xq_layer_mixed_ffn. At M <= 8 the gate/up warps of the grouped launch write
+# h's Q8 themselves: down in the same launch (all-Q4_K layers: Qwen2.5-1.5B,
+# F = 8960, and Llama-3-8B, F = 14336 with down split over K) or in a later
+# launch (the Q4_K_M mix, down in Q6_K). Above 8 tokens the feed is a
+# separate launch.
+FFN_CASES = [("qwen2.5-1.5b-layer", None), ("qwen2.5-1.5b-q4km-layer", None), ("llama3-8b-32layer", 384)]
+
+
+@pytest.mark.parametrize("key,rows", FFN_CASES)
+@pytest.mark.parametrize("M", [1, 2, 8, 20, 80])
+def test_ffn_layer_down_fed_by_silu_gate_up(xq, key, rows, M):
+    """Every projection but down checked as in xq_layer_mixed (all rows, or
+    `rows` sampled rows); h recomputed from the call's gate and up outputs by
+    xq_silu_mul_quantize_q8 checked against the oracle's silu_mul; the Q8 of
+    h the call left in its workspace equal to that launch's Q8, bit for bit,
+    and to the oracle's quantization of the same fp32 h; down checked against
+    the oracle on that Q8."""
+    wl = synth.WORKLOADS[key]
+    if rows is not None and M == 80:
+        pytest.skip("the Llama-3-8B layer is covered at M <= 20")
     weights = synth.gen_layer_weights(wl, 0)
     inputs = synth.gen_layer_inputs(wl, M, 0)[:3]   # attn-in, o-in, ffn-in; down reads h
     Wd = [dev(w.reshape(-1)) for w in weights]
@@ -566,22 +573,37 @@ def test_ffn_layer_down_fed_by_silu_gate_up(xq, M):
     ws = torch.zeros(xq.layer_ffn_workspace_bytes(desc, 3, M, gi, ui, di), dtype=torch.uint8, device="cuda")
     xq.layer_mixed_ffn(desc, gi, ui, di, [dev(x) for x in inputs], M, ws)
     torch.cuda.synchronize()
+    assert xq.device_error() == 0
     q8 = [oracle.quantize_q8(x) for x in inputs]
+    rng = np.random.default_rng(M)
     for t, p in enumerate(wl.projs):
         if t == di:
             continue
         rq, rd, _ = q8[p.input]
-        y_ref, ab, _ = oracle.matmul(p.qtype, weights[t], rq, rd, p.K)
-        check_y(ys[t].cpu().numpy(), y_ref, ab)
+        sel = np.arange(p.N) if rows is None else np.sort(rng.choice(p.N, size=min(rows, p.N), replace=False))
+        y_ref, ab, _ = oracle.matmul(p.qtype, weights[t][sel], rq, rd, p.K)
+        check_y(ys[t].cpu().numpy()[:, sel], y_ref, ab)
     g, u = ys[gi], ys[ui]
+    F = wl.projs[di].K
     h = torch.empty_like(g)
-    xq.silu_mul_quantize_q8(g, u, h_out=h)
+    # zero-filled, like the workspace: the layout's padding bytes stay zero on both
+    hbuf = xq.silu_mul_quantize_q8(g, u, out=torch.zeros(xq.q8_bytes(M, F), dtype=torch.uint8, device="cuda"),
+                                   h_out=h)
     torch.cuda.synchronize()
     h_gpu = h.cpu().numpy()
     check_h(h_gpu, g.cpu().numpy(), u.cpu().numpy())
-    rq, rd, _ = oracle.quantize_q8(h_gpu)
-    y_ref, ab, _ = oracle.matmul(wl.projs[di].qtype, weights[di], rq, rd, wl.projs[di].K)
-    check_y(ys[di].cpu().numpy(), y_ref, ab)
+    # the workspace: the read inputs' Q8 buffers (256-byte padded), then h's
+    h_off = sum(-(-xq.q8_bytes(M, x.shape[1]) // 256) * 256 for x in inputs)
+    nb = xq.q8_bytes(M, F)
+    assert torch.equal(ws[h_off:h_off + nb], hbuf[:nb])
+    rq, rd, rs = oracle.quantize_q8(h_gpu)
+    qs, d8, s8 = (t.cpu().numpy() for t in xq.q8_views(ws[h_off:h_off + nb], M, F))
+    assert np.array_equal(qs, rq)
+    assert np.array_equal(d8.view(np.uint32), rd.view(np.uint32))
+    assert np.array_equal(s8.view(np.uint32), rs.view(np.uint32))
+    sel = np.arange(wl.projs[di].N) if rows is None else np.sort(rng.choice(wl.projs[di].N, size=rows, replace=False))
+    y_ref, ab, _ = oracle.matmul(wl.projs[di].qtype, weights[di][sel], rq, rd, F)
+    check_y(ys[di].cpu().numpy()[:, sel], y_ref, ab)
 
 
 # ------------------------------------------------------------ IQ4_XS

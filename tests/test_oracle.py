@@ -656,3 +656,39 @@ def test_threads_do_not_change_results():
         assert used >= 1
         for a, b in zip(one, many):
             assert np.array_equal(a, b)
+
+
+# ------------------------------------------------------------ SwiGLU feed
+
+def test_silu_mul_pins():
+    """oracle.silu_mul against what the definition silu(g) = g * sigma(g)
+    fixes without retyping it:
+    - sigma(ln 3) = 3/4 and sigma(-ln 3) = 1/4, so at the fp32 values nearest
+      +-ln 3, h = 0.75 g u and 0.25 g u up to sigma's slope times the fp32
+      rounding of ln 3 (relative 1e-7); this tells sigma(g) from sigma(-g);
+    - silu(g) - silu(-g) = g for every g (sigma(g) + sigma(-g) = 1);
+    - the limits: h = g u once e^-g is below fp64 resolution (g = 40, 100),
+      h = +-0 once e^-g overflows (g = -800, -1e30), h = 0 at g = 0;
+    - h is linear in u (u used once, as a factor)."""
+    ln3 = np.float32(np.log(3.0))
+    g = np.array([ln3, -ln3], np.float32)
+    u = np.array([1.0, 1.0], np.float32)
+    h = oracle.silu_mul(g, u)
+    assert abs(h[0] - 0.75 * float(g[0])) <= 1e-7 * abs(float(g[0]))
+    assert abs(h[1] - 0.25 * float(g[1])) <= 1e-7 * abs(float(g[1]))
+    rng = np.random.default_rng(5)
+    gs = (rng.standard_normal(2000) * 6).astype(np.float32)
+    one = np.ones_like(gs)
+    diff = oracle.silu_mul(gs, one) - oracle.silu_mul(-gs, one)
+    assert np.all(np.abs(diff - gs.astype(np.float64)) <= 4e-16 * np.abs(gs) + 1e-300)
+    lim = np.array([40.0, 100.0, -800.0, -1e30, 0.0], np.float32)
+    ul = np.array([3.0, -2.0, 5.0, 7.0, 9.0], np.float32)
+    hl = oracle.silu_mul(lim, ul)
+    assert hl[0] == 120.0 and hl[1] == -200.0
+    assert hl[2] == 0.0 and hl[3] == 0.0 and hl[4] == 0.0
+    # u on a 2^-10 grid, so that u1 + u2 is exact in fp32
+    u1 = (rng.integers(-4096, 4096, 2000) / 1024.0).astype(np.float32)
+    u2 = (rng.integers(-4096, 4096, 2000) / 1024.0).astype(np.float32)
+    h12 = oracle.silu_mul(gs, u1 + u2)
+    lin = oracle.silu_mul(gs, u1) + oracle.silu_mul(gs, u2)
+    assert np.all(np.abs(h12 - lin) <= 1e-15 * (np.abs(oracle.silu_mul(gs, u1)) + np.abs(oracle.silu_mul(gs, u2))))
