@@ -713,7 +713,49 @@ xq_status xq_device_error(xq_stream stream, unsigned int* code_out) {
       *code_out = (static_cast<unsigned int>(k + 1) << 8) | (c[k] & 0xFFu);
       break;
     }
+  // checked builds: the first failed bounds check of each kernel file
+  unsigned int chk[4] = {0u, 0u, 0u, 0u};
+  const cudaError_t c0 = xq::take_gemv_check(&chk[0]);
+  const cudaError_t c1 = xq::take_tile_check(&chk[1]);
+  const cudaError_t c2 = xq::take_quant_check(&chk[2]);
+  const cudaError_t c3 = xq::take_q6k_check(&chk[3]);
+  if (c0 != cudaSuccess || c1 != cudaSuccess || c2 != cudaSuccess || c3 != cudaSuccess) return XQ_ERR_CUDA;
+  for (int k = 0; k < 4 && *code_out == 0; ++k)
+    if (chk[k]) *code_out = (9u << 8) | (chk[k] & 0xFFu);
   return XQ_OK;
+}
+
+xq_status xq_debug_check_probe(const void* W, const void* xq, int M, int N, int K, float* y, xq_stream stream) {
+#ifdef XQ_CHECK
+  if (M < 2 || M > kMaxGemvM) return XQ_ERR_SHAPE;
+  const xq_status st = check_shape(M, N, K);
+  if (st != XQ_OK) return st;
+  if (!W || !xq || !y) return XQ_ERR_ARG;
+  if (!aligned16(W) || !aligned16(xq) || !aligned16(y)) return XQ_ERR_ALIGN;
+  xq::MmaProj q;
+  q.W = static_cast<const uint8_t*>(W);
+  q.xq = static_cast<const uint8_t*>(xq);
+  q.y = y;
+  q.isum = nullptr;
+  q.N = N;
+  q.K = K;
+  q.M_total = M;
+  q.chunk = 0;
+  q.nch = 1;
+  q.y_limit = static_cast<long long>(M - 1) * N;  // one token row short of what the launch writes
+  return xq::launch_gemv_mma(XQ_TYPE_Q4_K, &q, 1, reinterpret_cast<cudaStream_t>(stream), true) == cudaSuccess
+             ? XQ_OK
+             : XQ_ERR_CUDA;
+#else
+  (void)W;
+  (void)xq;
+  (void)M;
+  (void)N;
+  (void)K;
+  (void)y;
+  (void)stream;
+  return XQ_ERR_UNSUPPORTED;
+#endif
 }
 
 xq_status xq_debug_stalled_matmul_q4k(const void* W, const void* xq, int M, int N, int K, float* y,

@@ -59,6 +59,7 @@
 #include <cuda.h>
 
 #include "q8_block.cuh"
+#include "xq_check.cuh"
 #include "xq_common.cuh"
 #include "xq_ptx.cuh"
 
@@ -82,6 +83,9 @@ struct Proj {
   const float* as8;      // small-M form: s8 [M][K/32]
   int N, K, M, task0, nch;
   int gs;                // Q6_K grouped view: 2^gs consecutive rows form one tensor-map row (else 0)
+  const uint8_t* xq0;    // the Q8 buffer and its size (bounds checks of checked builds)
+  unsigned long long xq_bytes;
+  unsigned long long y_elems;  // elements of y from P.y on that the launch may write (checked builds)
 };
 
 // The SwiGLU feed of a down projection computed inside the launch that runs
@@ -96,6 +100,7 @@ struct Ffn {
   uint8_t* hq;           // h's Q8 buffer
   float* h_out;          // optional fp32 copy of h [M][F]
   unsigned long long qs, d8, s8, frag, fsc;  // region offsets in hq
+  unsigned long long hq_bytes;               // size of h's Q8 buffer
   int gate, up, down;    // slots in Group::p (down -1: not in this launch)
   int F, M;              // h features (N of gate and up, K of down), tokens (<= 8)
 };
@@ -170,6 +175,9 @@ __device__ __forceinline__ void weight_box(const Proj& P, int rg, int b, int& x,
     x = weight_box_x<TYPE>(b);
     y = 16 * rg;
   }
+  // x in map elements (8 bytes for Q4_K and Q8_0, 1 byte otherwise)
+  const int xb = (TYPE == 12 || TYPE == 8) ? 8 * x : x;
+  (void)XQ_CHECKED((xb & 15) == 0 && x >= 0 && y >= 0 && y < (P.N >> P.gs), kChkGemvBox);
 }
 
 // ---------------------------------------------------------------- PTX
@@ -332,8 +340,9 @@ __device__ __forceinline__ void compute_block_q4(const uint8_t* blk, const uint8
         for (int e = 0; e < 4; ++e) {
           const int row = group_row(P, rg, (e >> 1) ? r1 : r0);
           const int col = 2 * t + (e & 1);
-          if (row < P.N && col < P.M)
-            P.isum[(static_cast<size_t>(col) * P.N + row) * nsub + sb] = static_cast<int32_t>(D[e] * scale);
+          const size_t ii = (static_cast<size_t>(col) * P.N + row) * nsub + sb;
+          if (row < P.N && col < P.M && XQ_IN(ii, static_cast<size_t>(P.M) * P.N * nsub, kChkGemvIsum))
+            P.isum[ii] = static_cast<int32_t>(D[e] * scale);
         }
       }
     }
@@ -409,9 +418,9 @@ __device__ __forceinline__ void compute_block_q6(const uint8_t* blk, int off, co
           for (int e = 0; e < 4; ++e) {
             const int row = group_row(P, rg, (e >> 1) ? r1 : r0);
             const int col = 2 * t + (e & 1);
-            if (row < P.N && col < P.M)
-              P.isum[(static_cast<size_t>(col) * P.N + row) * ngrp + 16 * b + 2 * p + g] =
-                  static_cast<int32_t>(g ? D1[e] : Da[e] - D1[e]);
+            const size_t ii = (static_cast<size_t>(col) * P.N + row) * ngrp + 16 * b + 2 * p + g;
+            if (row < P.N && col < P.M && XQ_IN(ii, static_cast<size_t>(P.M) * P.N * ngrp, kChkGemvIsum))
+              P.isum[ii] = static_cast<int32_t>(g ? D1[e] : Da[e] - D1[e]);
           }
       }
     }
@@ -475,8 +484,9 @@ __device__ __forceinline__ void compute_block_q8_0(const uint8_t* blk, const uin
       for (int e = 0; e < 4; ++e) {
         const int row = group_row(P, rg, (e >> 1) ? r1 : r0);
         const int col = 2 * t + (e & 1);
-        if (row < P.N && col < P.M)
-          P.isum[(static_cast<size_t>(col) * P.N + row) * nsub + 8 * b + j] = static_cast<int32_t>(D[e]);
+        const size_t ii = (static_cast<size_t>(col) * P.N + row) * nsub + 8 * b + j;
+        if (row < P.N && col < P.M && XQ_IN(ii, static_cast<size_t>(P.M) * P.N * nsub, kChkGemvIsum))
+          P.isum[ii] = static_cast<int32_t>(D[e]);
       }
     }
   }
@@ -560,8 +570,9 @@ __device__ __forceinline__ void compute_block_iq4xs(const uint8_t* blk, int off,
       for (int e = 0; e < 4; ++e) {
         const int row = group_row(P, rg, (e >> 1) ? r1 : r0);
         const int col = 2 * t + (e & 1);
-        if (row < P.N && col < P.M)
-          P.isum[(static_cast<size_t>(col) * P.N + row) * nsub + 8 * b + j] = static_cast<int32_t>(D[e]);
+        const size_t ii = (static_cast<size_t>(col) * P.N + row) * nsub + 8 * b + j;
+        if (row < P.N && col < P.M && XQ_IN(ii, static_cast<size_t>(P.M) * P.N * nsub, kChkGemvIsum))
+          P.isum[ii] = static_cast<int32_t>(D[e]);
       }
     }
   }
@@ -570,14 +581,14 @@ __device__ __forceinline__ void compute_block_iq4xs(const uint8_t* blk, int off,
 __device__ __forceinline__ void store_y(const Proj& P, int rg, int n8, int t, float v00, float v01, float v10,
                                         float v11) {
   const int r0 = group_row(P, rg, mma_row(n8)), r1 = group_row(P, rg, mma_row(n8) + 8), c0 = 2 * t, c1 = c0 + 1;
-  if (r0 < P.N) {
-    if (c0 < P.M) P.y[static_cast<size_t>(c0) * P.N + r0] = v00;
-    if (c1 < P.M) P.y[static_cast<size_t>(c1) * P.N + r0] = v01;
-  }
-  if (r1 < P.N) {
-    if (c0 < P.M) P.y[static_cast<size_t>(c0) * P.N + r1] = v10;
-    if (c1 < P.M) P.y[static_cast<size_t>(c1) * P.N + r1] = v11;
-  }
+  auto put = [&](int c, int r, float v) {
+    const size_t i = static_cast<size_t>(c) * P.N + r;
+    if (c < P.M && r < P.N && XQ_IN(i, P.y_elems, kChkGemvY)) P.y[i] = v;
+  };
+  put(c0, r0, v00);
+  put(c1, r0, v01);
+  put(c0, r1, v10);
+  put(c1, r1, v11);
 }
 
 // The last warp to finish a split 16-row group: y = the group's K-chunk
@@ -596,6 +607,9 @@ __device__ __forceinline__ void reduce_chunks(const Proj& P, int rg, int n8, int
         pv[u][1] = __ldcg(pc + static_cast<size_t>(c1) * rows_pad + r0);
         pv[u][2] = __ldcg(pc + static_cast<size_t>(c0) * rows_pad + r1);
         pv[u][3] = __ldcg(pc + static_cast<size_t>(c1) * rows_pad + r1);
+        // (checked builds: the highest of the four reads inside the partial sums)
+        (void)XQ_IN((static_cast<size_t>(c0k + u) * 8 + c1) * rows_pad + (r0 > r1 ? r0 : r1),
+                    static_cast<size_t>(P.nch) * 8 * rows_pad, kChkGemvPartial);
       }
     }
 #pragma unroll
@@ -635,6 +649,11 @@ __device__ __noinline__ void ffn_arrive(const Group& G, int rg, int lane) {
   const int n = lane >> 2, g = lane & 3;
   const bool live = n < F.M;
   float v[8];
+  // (checked builds: the block inside h, and h's Q8 regions inside its buffer)
+  const bool ffn_ok = XQ_CHECKED(j >= 0 && 32 * j + 32 <= F.F && F.fsc + static_cast<size_t>(F.F / 32) * 64 <= F.hq_bytes &&
+                                     F.s8 + 4ull * F.M * (F.F / 32) <= F.hq_bytes && F.qs + 1ull * F.M * F.F <= F.hq_bytes,
+                                 kChkGemvFfn);
+  if (!ffn_ok) return;
   if (live) {
     const size_t idx = static_cast<size_t>(n) * F.F + 32 * j + 8 * g;
     const float4* gp = reinterpret_cast<const float4*>(G.p[F.gate].y + idx);
@@ -795,16 +814,27 @@ __device__ __forceinline__ unsigned act_bytes(const Proj& P) {
 template <int TYPE, bool SMALL>
 __device__ __forceinline__ void act_load(uint32_t st, const Proj& P, int b, uint32_t bar) {
   constexpr int kFragOff = GLay<TYPE>::kFragOff, kFscOff = GLay<TYPE>::kFscOff;
+  // (checked builds: every source range inside the Q8 buffer, 16-byte aligned)
+  auto in_q8 = [&](const void* src, unsigned n) {
+    const uint8_t* p = static_cast<const uint8_t*>(src);
+    return XQ_CHECKED(p >= P.xq0 && p + n <= P.xq0 + P.xq_bytes && (reinterpret_cast<uintptr_t>(p) & 15) == 0,
+                      kChkGemvAct);
+  };
   if (SMALL) {
     const int nsub = P.K >> 5;
     for (int m = 0; m < P.M; ++m) {
-      bulk_load(st + kFragOff + 256 * m, P.aq + static_cast<size_t>(m) * P.K + 256 * static_cast<size_t>(b), 256, bar);
-      bulk_load(st + kFragOff + 512 + 32 * m, P.ad8 + static_cast<size_t>(m) * nsub + 8 * b, 32, bar);
-      bulk_load(st + kFragOff + 576 + 32 * m, P.as8 + static_cast<size_t>(m) * nsub + 8 * b, 32, bar);
+      const uint8_t* q = P.aq + static_cast<size_t>(m) * P.K + 256 * static_cast<size_t>(b);
+      const float* d = P.ad8 + static_cast<size_t>(m) * nsub + 8 * b;
+      const float* s8 = P.as8 + static_cast<size_t>(m) * nsub + 8 * b;
+      if (in_q8(q, 256)) bulk_load(st + kFragOff + 256 * m, q, 256, bar);
+      if (in_q8(d, 32)) bulk_load(st + kFragOff + 512 + 32 * m, d, 32, bar);
+      if (in_q8(s8, 32)) bulk_load(st + kFragOff + 576 + 32 * m, s8, 32, bar);
     }
   } else {
-    bulk_load(st + kFragOff, P.frag + static_cast<size_t>(b) * 8 * 512, 8 * 512, bar);
-    bulk_load(st + kFscOff, P.fsc + static_cast<size_t>(b) * 8 * 64, 8 * 64, bar);
+    const uint8_t* f = P.frag + static_cast<size_t>(b) * 8 * 512;
+    const uint8_t* c = P.fsc + static_cast<size_t>(b) * 8 * 64;
+    if (in_q8(f, 8 * 512)) bulk_load(st + kFragOff, f, 8 * 512, bar);
+    if (in_q8(c, 8 * 64)) bulk_load(st + kFscOff, c, 8 * 64, bar);
   }
 }
 
@@ -867,8 +897,10 @@ __device__ __forceinline__ void compute_small_q4(const uint8_t* blk, const uint8
         v = dp4a_us(nib[k][5], a1.y, v);
         v = dp4a_us(nib[k][6], a1.z, v);
         v = dp4a_us(nib[k][7], a1.w, v);
-        if (ISUM && row < P.N)
-          P.isum[(static_cast<size_t>(m) * P.N + row) * nsub + 8 * b + 4 * h + k] = v - magic;
+        if (ISUM && row < P.N) {
+          const size_t ii = (static_cast<size_t>(m) * P.N + row) * nsub + 8 * b + 4 * h + k;
+          if (XQ_IN(ii, static_cast<size_t>(P.M) * P.N * nsub, kChkGemvIsum)) P.isum[ii] = v - magic;
+        }
         D[k] = __int_as_float(v) - ((k & 1) ? 12.0f : 0.75f);
         cf[k] = al[k] * d8[k];
       }
@@ -895,8 +927,12 @@ __device__ __forceinline__ void reduce_chunks_small(const Proj& P, int rg, int r
   if (h == 0 || row >= P.N) return;
   for (int m = 0; m < P.M; ++m) {
     float v = 0.0f;
-    for (int c = 0; c < P.nch; ++c) v += __ldcg(P.partial + (static_cast<size_t>(c) * 8 + m) * rows_pad + row);
-    P.y[static_cast<size_t>(m) * P.N + row] = v;
+    for (int c = 0; c < P.nch; ++c) {
+      const size_t i = (static_cast<size_t>(c) * 8 + m) * rows_pad + row;
+      if (XQ_IN(i, static_cast<size_t>(P.nch) * 8 * rows_pad, kChkGemvPartial)) v += __ldcg(P.partial + i);
+    }
+    if (XQ_IN(static_cast<size_t>(m) * P.N + row, P.y_elems, kChkGemvY))
+      P.y[static_cast<size_t>(m) * P.N + row] = v;
   }
 }
 
@@ -964,17 +1000,22 @@ __device__ __forceinline__ void small_consumer(const Group& G, const uint8_t* ri
       nrun = 0;
       if (P.nch == 1) {
         if (h == 1 && row < P.N)
-          for (int t = 0; t < P.M; ++t) P.y[static_cast<size_t>(t) * P.N + row] = v[t];
+          for (int t = 0; t < P.M; ++t)
+            if (XQ_IN(static_cast<size_t>(t) * P.N + row, P.y_elems, kChkGemvY))
+              P.y[static_cast<size_t>(t) * P.N + row] = v[t];
         if (FFN && rg * 16 < P.N && (tp.p == G.ffn.gate || tp.p == G.ffn.up)) ffn_arrive(G, rg, lane);
       } else if (rg * 16 < P.N) {
         const int rows_pad = gemv_row_blocks(P.N) * kGemvRows;
         float* part = P.partial + static_cast<size_t>(tp.c) * 8 * rows_pad;
         if (h == 1)
-          for (int t = 0; t < P.M; ++t) part[static_cast<size_t>(t) * rows_pad + row] = v[t];
+          for (int t = 0; t < P.M; ++t)
+            if (XQ_IN((static_cast<size_t>(tp.c) * 8 + t) * rows_pad + row, static_cast<size_t>(P.nch) * 8 * rows_pad,
+                      kChkGemvPartial))
+              part[static_cast<size_t>(t) * rows_pad + row] = v[t];
         __syncwarp();
         if (lane == 0) {
           __threadfence();
-          pend_old = atomicAdd(P.arrive + rg, 1u);
+          if (XQ_IN(rg, gemv_row_blocks(P.N) * kGemvWarps, kChkGemvArrive)) pend_old = atomicAdd(P.arrive + rg, 1u);
         }
         pend_p = tp.p;
         pend_rg = rg;
@@ -1204,14 +1245,17 @@ __device__ __forceinline__ void gemv_mma_body(const Group& G) {
         const int rows_pad = gemv_row_blocks(P.N) * kGemvRows;
         float* part = P.partial + static_cast<size_t>(tp.c) * 8 * rows_pad;
         const int r0 = rg * 16 + mma_row(n8), r1 = r0 + 8, c0 = 2 * t, c1 = c0 + 1;
-        part[static_cast<size_t>(c0) * rows_pad + r0] = lo32(acc[0]);
-        part[static_cast<size_t>(c1) * rows_pad + r0] = hi32(acc[0]);
-        part[static_cast<size_t>(c0) * rows_pad + r1] = lo32(acc[1]);
-        part[static_cast<size_t>(c1) * rows_pad + r1] = hi32(acc[1]);
+        if (XQ_IN((static_cast<size_t>(tp.c) * 8 + c1) * rows_pad + (r0 > r1 ? r0 : r1),
+                  static_cast<size_t>(P.nch) * 8 * rows_pad, kChkGemvPartial)) {
+          part[static_cast<size_t>(c0) * rows_pad + r0] = lo32(acc[0]);
+          part[static_cast<size_t>(c1) * rows_pad + r0] = hi32(acc[0]);
+          part[static_cast<size_t>(c0) * rows_pad + r1] = lo32(acc[1]);
+          part[static_cast<size_t>(c1) * rows_pad + r1] = hi32(acc[1]);
+        }
         __syncwarp();
         if (lane == 0) {
           __threadfence();
-          pend_old = atomicAdd(P.arrive + rg, 1u);
+          if (XQ_IN(rg, gemv_row_blocks(P.N) * kGemvWarps, kChkGemvArrive)) pend_old = atomicAdd(P.arrive + rg, 1u);
         }
         pend_p = tp.p;
         pend_rg = rg;
@@ -1279,6 +1323,8 @@ bool encode_weight_map(int type, CUtensorMap* map, const uint8_t* W, int N, int 
 }
 
 }  // namespace
+
+cudaError_t take_gemv_check(unsigned int* code) { return take_check_word(code); }
 
 cudaError_t take_gemv_error(unsigned int* code) {
   unsigned int v = 0, z = 0;
@@ -1400,6 +1446,7 @@ cudaError_t launch_gemv_mma(int type, const MmaProj* projs, int n, cudaStream_t 
     G.ffn.fsc = H.fsc;
     G.ffn.F = ffn->F;
     G.ffn.M = ffn->M;
+    G.ffn.hq_bytes = H.total;
     for (int k = 0; k < n; ++k) {
       if (order[k] == ffn->gate) G.ffn.gate = k;
       if (order[k] == ffn->up) G.ffn.up = k;
@@ -1442,6 +1489,13 @@ cudaError_t launch_gemv_mma(int type, const MmaProj* projs, int n, cudaStream_t 
     if (P.nch > 1) {
       P.partial = reinterpret_cast<float*>(partial_ws + partial_off[src]);
       P.arrive = reinterpret_cast<unsigned int*>(arrive_ws + arrive_off[src]);
+    }
+    P.xq0 = q.xq;
+    P.xq_bytes = L.total;
+    {
+      const long long full = static_cast<long long>(P.M) * q.N;
+      const long long lim = q.y_limit >= 0 ? q.y_limit - static_cast<long long>(m0) * q.N : full;
+      P.y_elems = static_cast<unsigned long long>(lim < 0 ? 0 : (lim < full ? lim : full));
     }
     P.task0 = total;
     total += rbs * P.nch;

@@ -19,6 +19,7 @@
 //
 // The -32 offset: sum (q-32)*a = dot(q, a) - 32*sum(a). The activation sums
 // are computed once per token and reused for all R rows of the warp.
+#include "xq_check.cuh"
 #include "xq_common.cuh"
 
 namespace xq {
@@ -70,7 +71,9 @@ gemv_q6k_dp4a_kernel(GemvArgs a, int kw) {
 #pragma unroll
     for (int r = 0; r < R; ++r) {
       const long long row = row0 + r;
-      if (row < N) {
+      if (row < N && XQ_CHECKED(row >= 0 && b >= 0 && (static_cast<size_t>(row) * nsb + b + 1) * kQ6kBytes <=
+                                                          static_cast<size_t>(N) * nsb * kQ6kBytes,
+                                kChkQ6W)) {
         const uint8_t* blk = a.W + (static_cast<size_t>(row) * nsb + b) * kQ6kBytes;
         l0[r] = load16_a2(blk + 64 * h + 16 * p);
         l1[r] = load16_a2(blk + 64 * h + 32 + 16 * p);
@@ -105,6 +108,11 @@ gemv_q6k_dp4a_kernel(GemvArgs a, int kw) {
 #pragma unroll
     for (int m = 0; m < M; ++m) {
       const int8_t* xa = a.qs + static_cast<size_t>(m) * K + static_cast<size_t>(b) * 256 + 128 * h + 16 * p;
+      // (checked builds: the token's quants and scales of this super-block inside [M][K] and [M][K/32])
+      if (!XQ_CHECKED(static_cast<size_t>(m) * K + static_cast<size_t>(b) * 256 + 256 <= static_cast<size_t>(a.M) * K &&
+                          static_cast<size_t>(m) * nsub + 8 * b + 8 <= static_cast<size_t>(a.M) * nsub,
+                      kChkQ6Act))
+        continue;
       const float4 dd = __ldg(reinterpret_cast<const float4*>(a.d8 + static_cast<size_t>(m) * nsub + 8 * b + 4 * h));
       const float dq[4] = {dd.x, dd.y, dd.z, dd.w};
 #pragma unroll
@@ -127,8 +135,8 @@ gemv_q6k_dp4a_kernel(GemvArgs a, int kw) {
           acc[r][m] = fmaf(sd[r][qq] * dq[qq], static_cast<float>(isum), acc[r][m]);
           if (ISUM) {
             const long long row = row0 + r;
-            if (row < N)
-              a.isum[(static_cast<size_t>(m) * N + row) * ngrp + 16 * b + 8 * h + 2 * qq + p] = isum;
+            const size_t ii = (static_cast<size_t>(m) * N + row) * ngrp + 16 * b + 8 * h + 2 * qq + p;
+            if (row < N && XQ_IN(ii, static_cast<size_t>(a.M) * N * ngrp, kChkQ6Isum)) a.isum[ii] = isum;
           }
         }
       }
@@ -152,7 +160,8 @@ gemv_q6k_dp4a_kernel(GemvArgs a, int kw) {
         const long long row = row0 + r;
         if (row < N)
 #pragma unroll
-          for (int m = 0; m < M; ++m) a.y[m * a.ldy + row] = acc[r][m];
+          for (int m = 0; m < M; ++m)
+            if (XQ_IN(m * a.ldy + row, (a.M - 1) * a.ldy + N, kChkQ6Y)) a.y[m * a.ldy + row] = acc[r][m];
       }
     }
     return;
@@ -170,7 +179,7 @@ gemv_q6k_dp4a_kernel(GemvArgs a, int kw) {
     float v = red[wib][lane];
     for (int w = 1; w < kw; ++w) v += red[wib + w][lane];
     const long long row = row0 + r;
-    if (row < N) a.y[m * a.ldy + row] = v;
+    if (row < N && XQ_IN(m * a.ldy + row, (a.M - 1) * a.ldy + N, kChkQ6Y)) a.y[m * a.ldy + row] = v;
   }
 }
 
@@ -210,6 +219,8 @@ static cudaError_t dispatch(const GemvArgs& a, cudaStream_t s) {
     default: return cudaErrorInvalidValue;
   }
 }
+
+cudaError_t take_q6k_check(unsigned int* code) { return take_check_word(code); }
 
 cudaError_t launch_gemv_q6k(const GemvArgs& a, cudaStream_t s) {
   return a.isum ? dispatch<true>(a, s) : dispatch<false>(a, s);

@@ -14,6 +14,7 @@
 // bf16 split of s8 (layouts in xq_common.cuh). One launch serves all inputs
 // of a layer.
 #include "q8_block.cuh"
+#include "xq_check.cuh"
 #include "xq_common.cuh"
 
 namespace xq {
@@ -32,6 +33,7 @@ struct QuantItem {
   float* h_out;     // optional copy of h
   uint8_t* xq;
   size_t d8, s8, frag, fsc, tile;  // byte offsets in xq (layout in xq_common.cuh)
+  size_t total;                    // bytes of xq (bounds checks of checked builds)
   int M, K, nsub, ttiles;
 };
 
@@ -89,6 +91,16 @@ quantize_q8_kernel(const __grid_constant__ QuantGroup G) {
 
     float d = 0.0f, s = 0.0f;
     int q = 0;
+    // (checked builds: the block inside [M][K] and every region of xq this
+    // block writes inside the buffer)
+    const bool blk_ok = XQ_CHECKED(j >= 0 && 32 * j + 32 <= J.K, kChkQuantX) &&
+                        XQ_CHECKED(L.s8 + 4 * (static_cast<size_t>(J.M) * nsub) <= J.total, kChkQuantQ8) &&
+                        XQ_CHECKED(L.ttiles != 0 || L.fsc + static_cast<size_t>((m >> 3) + 1) * nsub * 64 <= J.total,
+                                   kChkQuantImage) &&
+                        XQ_CHECKED(L.ttiles == 0 || L.tile + (static_cast<size_t>(m >> 7) + 1) * (J.K >> 8) *
+                                                                   kTileRecord <= J.total,
+                                   kChkQuantImage);
+    if (!blk_ok) continue;
     if (m < J.M) {
       const size_t idx = static_cast<size_t>(m) * J.K + 32 * j + lane;
       float v = __ldg(J.x + idx);
@@ -135,6 +147,8 @@ quantize_q8_kernel(const __grid_constant__ QuantGroup G) {
   }
 }
 
+cudaError_t take_quant_check(unsigned int* code) { return take_check_word(code); }
+
 cudaError_t launch_quantize_q8(const QuantJob* jobs, int n, cudaStream_t s, bool pdl, unsigned int* zero_words,
                                int zero_count) {
   if (n <= 0 || n > kMaxProj) return cudaErrorInvalidValue;
@@ -157,6 +171,7 @@ cudaError_t launch_quantize_q8(const QuantJob* jobs, int n, cudaStream_t s, bool
     it.frag = L.frag;
     it.fsc = L.fsc;
     it.tile = L.tile;
+    it.total = L.total;
     it.M = q.M;
     it.K = q.K;
     it.nsub = q.K / 32;

@@ -46,6 +46,7 @@
 // its own tensor-core work and frees TMEM.
 #include <cuda.h>
 
+#include "xq_check.cuh"
 #include "xq_common.cuh"
 #include "xq_ptx.cuh"
 
@@ -132,6 +133,7 @@ struct TileArgs {
   float* y;                    // [M][N]
   int32_t* sums;               // test hook: [M][N][K/32] per-32-block integer sums, or null
   unsigned long long w_bytes;  // N * row_bytes
+  unsigned long long img_bytes;  // bytes of the tile image (bounds checks of checked builds)
   int N, K, M, nsb, row_bytes, ttiles;
   uint32_t cb[4];              // IQ4_XS: codebook bytes with their sign bits flipped
 };
@@ -273,7 +275,9 @@ __global__ void __launch_bounds__(kThreads, 1) tile_mma_kernel(const __grid_cons
         if (lane == 0) {
           mbar_expect_tx(BAR(B::kRawFull + rs), kRawBytes);  // rows past N arrive zero-filled
           const int x = TYPE == 12 ? b * (kQ4kBytes / 8) : (TYPE == 8 ? b * (kQ80Group / 8) : (kIq4xsBytes * b) & ~15);
-          tma_load_2d(dst, &A.map, x, row0, BAR(B::kRawFull + rs));
+          // x in map elements: 8 bytes for Q4_K and Q8_0, 1 byte for IQ4_XS
+          if (XQ_CHECKED((((TYPE == 23) ? x : 8 * x) & 15) == 0 && x >= 0, kChkTileBox))
+            tma_load_2d(dst, &A.map, x, row0, BAR(B::kRawFull + rs));
         }
       } else {
         unsigned mine = 0;
@@ -283,7 +287,11 @@ __global__ void __launch_bounds__(kThreads, 1) tile_mma_kernel(const __grid_cons
         __syncwarp();
         for (int r = lane; r < rows; r += 32) {
           const unsigned long long start = static_cast<unsigned long long>(row0 + r) * A.row_bytes + 210ull * b;
-          bulk_load(dst + r * kQ6Pitch, A.W + (start & ~15ull), q6_window(A, row0 + r, b), BAR(B::kRawFull + rs));
+          const unsigned win = q6_window(A, row0 + r, b);
+          if (XQ_CHECKED((start & ~15ull) + win <= A.w_bytes && (win & 15) == 0 &&
+                             ((reinterpret_cast<uintptr_t>(A.W) + (start & ~15ull)) & 15) == 0,
+                         kChkTileQ6Window))
+            bulk_load(dst + r * kQ6Pitch, A.W + (start & ~15ull), win, BAR(B::kRawFull + rs));
         }
       }
       for (int it = 0; it < kItems; ++it, ++tf) {
@@ -295,8 +303,11 @@ __global__ void __launch_bounds__(kThreads, 1) tile_mma_kernel(const __grid_cons
         if (lane == 0) {
           const unsigned bytes = it < 8 ? kTileItem : kTileItemOp;
           mbar_expect_tx(BAR(B::kTokFull + ts), bytes);
-          bulk_load(smem_addr(tok_ring + ts * kTileItem), rec + static_cast<size_t>(b) * kTileRecord + it * kTileItem,
-                    bytes, BAR(B::kTokFull + ts));
+          const size_t off = (static_cast<size_t>(tt) * A.nsb + b) * kTileRecord + static_cast<size_t>(it) * kTileItem;
+          if (XQ_CHECKED(off + bytes <= A.img_bytes && ((reinterpret_cast<uintptr_t>(A.img) + off) & 15) == 0,
+                         kChkTileItem))
+            bulk_load(smem_addr(tok_ring + ts * kTileItem), rec + static_cast<size_t>(b) * kTileRecord + it * kTileItem,
+                      bytes, BAR(B::kTokFull + ts));
         }
       }
     }
@@ -489,7 +500,7 @@ __global__ void __launch_bounds__(kThreads, 1) tile_mma_kernel(const __grid_cons
           if (!cut) {
             load_words<4>(sb + 192, sw);
             d = half_bits_to_float(*reinterpret_cast<const unsigned short*>(sb + 208));
-          } else {
+          } else if (XQ_CHECKED(start + 210 <= A.w_bytes, kChkTileQ6Cut)) {
             const unsigned short* gs = reinterpret_cast<const unsigned short*>(A.W + start + 192);
 #pragma unroll
             for (int k = 0; k < 4; ++k)
@@ -665,12 +676,11 @@ __global__ void __launch_bounds__(kThreads, 1) tile_mma_kernel(const __grid_cons
 #pragma unroll
               for (int e = 0; e < 16; ++e) {
                 const int n1 = n0 + 16 * c + e, n2 = n1 + 16;
-                if (n1 < A.N)
-                  A.sums[(static_cast<size_t>(m) * A.N + n1) * nsub + 8 * b + it] =
-                      static_cast<int32_t>(__uint_as_float(v[e]) * sc);
-                if (n2 < A.N)
-                  A.sums[(static_cast<size_t>(m) * A.N + n2) * nsub + 8 * b + it] =
-                      static_cast<int32_t>(__uint_as_float(w[e]) * sc);
+                const size_t ns = static_cast<size_t>(A.M) * A.N * nsub;
+                const size_t i1 = (static_cast<size_t>(m) * A.N + n1) * nsub + 8 * b + it;
+                const size_t i2 = (static_cast<size_t>(m) * A.N + n2) * nsub + 8 * b + it;
+                if (n1 < A.N && XQ_IN(i1, ns, kChkTileSums)) A.sums[i1] = static_cast<int32_t>(__uint_as_float(v[e]) * sc);
+                if (n2 < A.N && XQ_IN(i2, ns, kChkTileSums)) A.sums[i2] = static_cast<int32_t>(__uint_as_float(w[e]) * sc);
               }
             }
 #pragma unroll
@@ -718,7 +728,9 @@ __global__ void __launch_bounds__(kThreads, 1) tile_mma_kernel(const __grid_cons
               if (m < A.M) {
                 const int nc = n0 + 16 * c;
                 float* yr = A.y + static_cast<size_t>(m) * A.N;
-                if ((A.N & 3) == 0 && nc + 16 <= A.N) {
+                if (!XQ_IN(static_cast<size_t>(m) * A.N + (nc < A.N ? nc : 0), static_cast<size_t>(A.M) * A.N,
+                           kChkTileY)) {
+                } else if ((A.N & 3) == 0 && nc + 16 <= A.N) {
 #pragma unroll
                   for (int k = 0; k < 4; ++k)
                     *reinterpret_cast<uint4*>(yr + nc + 4 * k) =
@@ -779,6 +791,8 @@ cudaError_t launch_tile(const TileArgs& A, int grid, cudaStream_t s, bool pdl) {
 
 }  // namespace
 
+cudaError_t take_tile_check(unsigned int* code) { return take_check_word(code); }
+
 cudaError_t take_tile_error(unsigned int* code) {
   unsigned int v = 0, z = 0;
   cudaError_t e = cudaMemcpyFromSymbol(&v, g_tile_error, sizeof(v));
@@ -806,6 +820,7 @@ cudaError_t launch_tile_mma(int type, const uint8_t* W, const uint8_t* xq, int M
   A.row_bytes = A.nsb * (type == 12 ? kQ4kBytes : (type == 23 ? kIq4xsBytes : (type == 8 ? kQ80Group : kQ6kBytes)));
   for (int i = 0; i < 4; ++i) A.cb[i] = codebook ? (codebook[i] ^ 0x80808080u) : 0u;
   A.w_bytes = static_cast<unsigned long long>(N) * A.row_bytes;
+  A.img_bytes = L.total - L.tile;
   A.ttiles = L.ttiles;
   const int grid = ((N + kRows - 1) / kRows) * L.ttiles;
   if (type == 12) {

@@ -183,6 +183,9 @@ struct MmaProj {
   int32_t* isum;       // optional [M_total][N][K/32], only with M_total <= 8
   int N, K, M_total, chunk;
   uint32_t codebook[4] = {0u, 0u, 0u, 0u};  // IQ4_XS: the 16 int8 values, little-endian bytes
+  // Elements of y [M_total][N] the launch may write (bounds checks of checked
+  // builds; -1: all of them). The check probe declares fewer.
+  long long y_limit = -1;
 };
 
 // K-chunks a projection's rows are split into when a split workspace is
@@ -257,6 +260,12 @@ cudaError_t launch_gemv_mma(int type, const MmaProj* projs, int n, cudaStream_t 
 // runs out (0: none since the last read). Synchronous device reads/writes.
 cudaError_t take_gemv_error(unsigned int* code);
 cudaError_t take_tile_error(unsigned int* code);
+// Checked builds: read and clear the bounds-check word of each kernel file
+// (the site number of the first failed check; always 0 in normal builds).
+cudaError_t take_gemv_check(unsigned int* code);
+cudaError_t take_tile_check(unsigned int* code);
+cudaError_t take_quant_check(unsigned int* code);
+cudaError_t take_q6k_check(unsigned int* code);
 
 // 2D tensor map (no interleave, no swizzle, zero fill): dims {dim0, dim1}
 // elements of type dt, rows stride1 bytes apart, boxes box0 x box1. False

@@ -31,7 +31,7 @@ SYMBOLS = ("xq_status_str", "xq_q8_bytes", "xq_weight_bytes", "xq_quantize_q8",
            "xq_matmul_q8_0_q8", "xq_debug_isums_q8_0", "xq_silu_mul_quantize_q8",
            "xq_layer_ffn_workspace_bytes", "xq_layer_mixed_ffn", "xq_matmul_iq4xs_q8",
            "xq_debug_isums_iq4xs", "xq_device_error", "xq_debug_stalled_matmul_q4k", "xq_debug_tile_sums",
-           "xq_debug_layer_matmuls")
+           "xq_debug_layer_matmuls", "xq_debug_check_probe")
 
 
 class XQError(RuntimeError):
@@ -99,9 +99,10 @@ def lib(path: str | None = None):
     L.xq_layer_mixed.argtypes = [ctypes.POINTER(xq_proj), I, ctypes.POINTER(ctypes.c_void_p), I, I, P, S, P]
     L.xq_layer_mixed_static.argtypes = [ctypes.POINTER(xq_proj), I, ctypes.POINTER(ctypes.c_void_p), I, I, P]
     L.xq_debug_layer_matmuls.argtypes = [ctypes.POINTER(xq_proj), I, I, I, P, S, P]
+    L.xq_debug_check_probe.argtypes = [P, P, I, I, I, P, P]
     for fn in ("xq_quantize_q8", "xq_matmul_q4k_q8", "xq_matmul_q6k_q8", "xq_debug_isums_q4k",
                "xq_debug_isums_q6k", "xq_layer_mixed", "xq_layer_mixed_static", "xq_matmul_q8_0_q8",
-               "xq_debug_isums_q8_0", "xq_debug_layer_matmuls"):
+               "xq_debug_isums_q8_0", "xq_debug_layer_matmuls", "xq_debug_check_probe"):
         getattr(L, fn).restype = I
     if path is None:
         _lib = L

@@ -321,7 +321,12 @@ XQ_API xq_status xq_layer_mixed_static(const xq_proj *proj, int n_proj,
  * the tile kernel (M > 64); wait = the kernel's number of the wait that gave
  * up (GEMV: 1 the producer waiting for a free stage, 2 a consumer waiting for
  * a full one, 3 a down projection's producer waiting for h in the fused
- * feed of xq_layer_mixed_ffn). If several kernels recorded one,
+ * feed of xq_layer_mixed_ffn). Checked builds (the library compiled with
+ * -DXQ_CHECK) also test the index, range or 16-byte alignment of each global
+ * access whose address comes from nontrivial arithmetic, skip an access that
+ * fails and record the site: kernel 9, wait = site (10-16 the GEMV, 20-25
+ * the tile kernel, 30-32 the quantizer, 40-43 the dp4a Q6_K GEMV), reported
+ * after any wait code. If several kernels recorded one,
  * the lowest kernel number is reported and all are cleared. The reads and
  * writes are synchronous. XQ_ERR_ARG for a null code_out, XQ_ERR_CUDA if the
  * stream or the reads fail. */
@@ -334,6 +339,14 @@ XQ_API xq_status xq_device_error(xq_stream stream, unsigned int *code_out);
  * reports kernel 1, wait 2. Arguments and errors as xq_matmul_q4k_q8. */
 XQ_API xq_status xq_debug_stalled_matmul_q4k(const void *W, const void *xq, int M, int N, int K, float *y,
                                              xq_stream stream);
+
+/* Test hook of checked builds: the Q4_K GEMV (2 <= M <= 8, y [M][N] fully
+ * allocated) launched with its y extent declared one token row short, so
+ * that the stores of token M-1 fail their bounds check (site 10), are
+ * skipped (that row of y is left as it was) and are recorded for
+ * xq_device_error. Normal builds: XQ_ERR_UNSUPPORTED, nothing launched. */
+XQ_API xq_status xq_debug_check_probe(const void *W, const void *xq, int M, int N, int K, float *y,
+                                      xq_stream stream);
 
 /* Test hooks: the same matmul kernels with their exact int32 sub-block sums
  * written out instead of only consumed.

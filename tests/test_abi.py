@@ -140,6 +140,12 @@ def test_layer_matmuls_timing_hook_argument_errors(L):
     assert L.xq_debug_layer_matmuls(arr, 3, 2, 0, None, 0, None) == 0               # M = 0: nothing to do
 
 
+def test_check_probe_needs_the_checked_build(L):
+    """The normal library refuses the checked build's probe before any CUDA call."""
+    P = ctypes.c_void_p
+    assert L.xq_debug_check_probe(P(FAKE), P(FAKE), 4, 64, 512, P(FAKE), None) == 6
+
+
 def test_q8_0_entry_points_reject_before_launch(L):
     """Q8_0 shape and argument errors are refused before anything is
     enqueued; the layer sizes Q8_0 at every M."""
