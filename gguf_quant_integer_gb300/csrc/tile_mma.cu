@@ -64,12 +64,36 @@ constexpr int kWStages = 4;     // unpacked weight operand ring
 constexpr int kNumD = 3;        // accumulators in TMEM
 constexpr int kCoefStages = 4;  // per-super-block row coefficients
 constexpr uint32_t kColRun = 0, kColD = 128;
-constexpr int kThreads = 512;
-constexpr int kWarpEpi0 = 4, kWarpProd = 12, kWarpMma = 13;  // MMA warps 13..15
 constexpr long long kWaitClocks = 1LL << 32;
 constexpr int kQ6Window = 224;  // bytes copied per Q6_K row and super-block
 constexpr int kQ6Pitch = 240;   // their pitch in shared memory (conflict-free 16-byte reads)
 constexpr int kOpBytes = kRows * 32 * 2;  // one 128-row x 32-slot fp16 operand
+
+// Warp roles: warps 0-3 unpack, then kEpi epilogue warps (kEpi / 4 per TMEM
+// lane quarter, each thread taking kCols = 512 / kEpi weight columns of its
+// token), the producer, then kMma MMA issuers. The epilogue holds a
+// kCols-wide fp32 accumulator per thread; at 64 columns (8 warps) it fills
+// the 128-register cap of a 512-thread CTA and bounds the Q4_K tile. Sixteen
+// epilogue warps of 32 columns would halve that, but 22 warps leave 80
+// registers a thread, and the spills cost more than the parallelism gains
+// (measured on the 12288 x 4096 x 512 up projection: 270 us against 241).
+template <int TYPE>
+struct Roles {
+  static constexpr int kEpi = 8;
+  static constexpr int kMma = 3;
+  static constexpr int kCols = 512 / kEpi;
+  static constexpr int kEpi0 = 4, kProd = 4 + kEpi, kMma0 = 5 + kEpi;
+  static constexpr int kThreads = 32 * (5 + kEpi + kMma);
+};
+
+// Register split between the warpgroups (setmaxnreg): the kernel is built
+// for 128 registers a thread (the cap of a 512-thread CTA, checked on the host
+// before every launch), the producer and MMA warpgroup (warps 12-15) gives
+// back down to kRegsCtl, and the two epilogue warpgroups (warps 4-11) take
+// kRegsEpi, for their kCols-wide accumulators. The sum stays inside the CTA's
+// launch allocation: (128 + 2 * kRegsEpi + kRegsCtl) * 128 <= 512 * 128.
+constexpr int kRegsLaunch = 128, kRegsCtl = 56, kRegsEpi = 152;
+static_assert(128 * (kRegsLaunch + 2 * kRegsEpi + kRegsCtl) <= 512 * kRegsLaunch, "register split exceeds the CTA");
 
 template <int TYPE>
 struct Fmt;
@@ -134,6 +158,7 @@ struct TileArgs {
   int32_t* sums;               // test hook: [M][N][K/32] per-32-block integer sums, or null
   unsigned long long w_bytes;  // N * row_bytes
   unsigned long long img_bytes;  // bytes of the tile image (bounds checks of checked builds)
+  int q6_tma;                  // Q6_K rows of 16-byte multiples: map {row_bytes, N} of u8, box {240, 128}
   int N, K, M, nsb, row_bytes, ttiles;
   uint32_t cb[4];              // IQ4_XS: codebook bytes with their sign bits flipped
 };
@@ -203,7 +228,8 @@ __device__ __forceinline__ void store_row(uint8_t* op, int r, const uint32_t (&v
 }
 
 template <int TYPE, bool SUMS>
-__global__ void __launch_bounds__(kThreads, 1) tile_mma_kernel(const __grid_constant__ TileArgs A) {
+__global__ void __launch_bounds__(Roles<TYPE>::kThreads, 1) tile_mma_kernel(const __grid_constant__ TileArgs A) {
+  using R = Roles<TYPE>;
   using F = Fmt<TYPE>;
   using S = Smem<TYPE>;
   using B = Bars<TYPE>;
@@ -233,7 +259,7 @@ __global__ void __launch_bounds__(kThreads, 1) tile_mma_kernel(const __grid_cons
     }
     for (int s = 0; s < kTokStages; ++s) {
       mbar_init(BAR(B::kTokFull + s), 1);
-      mbar_init(BAR(B::kTokEmpty + s), 8);
+      mbar_init(BAR(B::kTokEmpty + s), R::kEpi);
     }
     for (int s = 0; s < kWStages; ++s) {
       mbar_init(BAR(B::kWFull + s), 4);
@@ -241,17 +267,17 @@ __global__ void __launch_bounds__(kThreads, 1) tile_mma_kernel(const __grid_cons
     }
     for (int s = 0; s < kNumD; ++s) {
       mbar_init(BAR(B::kDFull + s), 1);
-      mbar_init(BAR(B::kDEmpty + s), 8);
+      mbar_init(BAR(B::kDEmpty + s), R::kEpi);
     }
     for (int s = 0; s < kCoefStages; ++s) {
       mbar_init(BAR(B::kCoefFull + s), 4);
-      mbar_init(BAR(B::kCoefEmpty + s), 8);
+      mbar_init(BAR(B::kCoefEmpty + s), R::kEpi);
     }
     for (int s = 0; s < 2; ++s) mbar_init(BAR(B::kVote + s), 4);
     for (int s = 0; s < kNumD; ++s) mbar_init(BAR(B::kDone + s), 1);
     mbar_init_fence();
   }
-  if (warp == kWarpMma) tmem_alloc(smem_addr(tmem_slot), 512);
+  if (warp == R::kMma0) tmem_alloc(smem_addr(tmem_slot), 512);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -260,66 +286,121 @@ __global__ void __launch_bounds__(kThreads, 1) tile_mma_kernel(const __grid_cons
   cudaGridDependencySynchronize();
   cudaTriggerProgrammaticLaunchCompletion();
 
-  if (warp == kWarpProd) {
-    // ------------------------------------------------------- producer
-    const uint8_t* rec = A.img + static_cast<size_t>(tt) * A.nsb * kTileRecord;
-    const int row0 = wt * kRows;
-    const int rows = min(kRows, A.N - row0);
-    unsigned tf = 0;  // token items issued
-    bool ok = true;
-    for (int b = 0; b < A.nsb && ok; ++b) {
-      const int rs = b % RS;
-      if (b >= RS && !warp_wait(BAR(B::kRawEmpty + rs), ((b / RS) - 1) & 1, 1)) break;
-      const uint32_t dst = smem_addr(raw_ring + rs * kRawBytes);
-      if (TYPE == 12 || TYPE == 23 || TYPE == 8) {
-        if (lane == 0) {
-          mbar_expect_tx(BAR(B::kRawFull + rs), kRawBytes);  // rows past N arrive zero-filled
-          const int x = TYPE == 12 ? b * (kQ4kBytes / 8) : (TYPE == 8 ? b * (kQ80Group / 8) : (kIq4xsBytes * b) & ~15);
-          // x in map elements: 8 bytes for Q4_K and Q8_0, 1 byte for IQ4_XS
-          if (XQ_CHECKED((((TYPE == 23) ? x : 8 * x) & 15) == 0 && x >= 0, kChkTileBox))
-            tma_load_2d(dst, &A.map, x, row0, BAR(B::kRawFull + rs));
+  // Register split (setmaxnreg): warpgroup 3 (producer and MMA issuers,
+  // warps 12-15) gives registers back at one instruction before its roles
+  // split; the epilogue warpgroups (warps 4-11) then take them.
+  static_assert(R::kProd == 12 && R::kThreads == 512, "the register split assumes warpgroups 0 / 1-2 / 3");
+  if (warp >= R::kProd) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsCtl));
+    if (warp == R::kProd) {
+      // ------------------------------------------------------- producer
+      const uint8_t* rec = A.img + static_cast<size_t>(tt) * A.nsb * kTileRecord;
+      const int row0 = wt * kRows;
+      const int rows = min(kRows, A.N - row0);
+      unsigned tf = 0;  // token items issued
+      bool ok = true;
+      for (int b = 0; b < A.nsb && ok; ++b) {
+        const int rs = b % RS;
+        if (b >= RS && !warp_wait(BAR(B::kRawEmpty + rs), ((b / RS) - 1) & 1, 1)) break;
+        const uint32_t dst = smem_addr(raw_ring + rs * kRawBytes);
+        if (TYPE == 12 || TYPE == 23 || TYPE == 8) {
+          if (lane == 0) {
+            mbar_expect_tx(BAR(B::kRawFull + rs), kRawBytes);  // rows past N arrive zero-filled
+            const int x = TYPE == 12 ? b * (kQ4kBytes / 8) : (TYPE == 8 ? b * (kQ80Group / 8) : (kIq4xsBytes * b) & ~15);
+            // x in map elements: 8 bytes for Q4_K and Q8_0, 1 byte for IQ4_XS
+            if (XQ_CHECKED((((TYPE == 23) ? x : 8 * x) & 15) == 0 && x >= 0, kChkTileBox))
+              tma_load_2d(dst, &A.map, x, row0, BAR(B::kRawFull + rs));
+          }
+        } else if (A.q6_tma) {
+          // Q6_K rows of 16-byte multiples: one box of 128 rows x 240 bytes
+          // from the 16-byte boundary at or below the super-block (the same
+          // offset in every row); rows past N and bytes past the row arrive
+          // zero-filled
+          if (lane == 0) {
+            mbar_expect_tx(BAR(B::kRawFull + rs), kRawBytes);
+            const int x = (kQ6kBytes * b) & ~15;
+            if (XQ_CHECKED((x & 15) == 0 && x >= 0, kChkTileBox))
+              tma_load_2d(dst, &A.map, x, row0, BAR(B::kRawFull + rs));
+          }
+        } else {
+          unsigned mine = 0;
+          for (int r = lane; r < rows; r += 32) mine += q6_window(A, row0 + r, b);
+          const unsigned total = __reduce_add_sync(0xffffffffu, mine);
+          if (lane == 0) mbar_expect_tx(BAR(B::kRawFull + rs), total);
+          __syncwarp();
+          for (int r = lane; r < rows; r += 32) {
+            const unsigned long long start = static_cast<unsigned long long>(row0 + r) * A.row_bytes + 210ull * b;
+            const unsigned win = q6_window(A, row0 + r, b);
+            if (XQ_CHECKED((start & ~15ull) + win <= A.w_bytes && (win & 15) == 0 &&
+                               ((reinterpret_cast<uintptr_t>(A.W) + (start & ~15ull)) & 15) == 0,
+                           kChkTileQ6Window))
+              bulk_load(dst + r * kQ6Pitch, A.W + (start & ~15ull), win, BAR(B::kRawFull + rs));
+          }
         }
-      } else {
-        unsigned mine = 0;
-        for (int r = lane; r < rows; r += 32) mine += q6_window(A, row0 + r, b);
-        const unsigned total = __reduce_add_sync(0xffffffffu, mine);
-        if (lane == 0) mbar_expect_tx(BAR(B::kRawFull + rs), total);
-        __syncwarp();
-        for (int r = lane; r < rows; r += 32) {
-          const unsigned long long start = static_cast<unsigned long long>(row0 + r) * A.row_bytes + 210ull * b;
-          const unsigned win = q6_window(A, row0 + r, b);
-          if (XQ_CHECKED((start & ~15ull) + win <= A.w_bytes && (win & 15) == 0 &&
-                             ((reinterpret_cast<uintptr_t>(A.W) + (start & ~15ull)) & 15) == 0,
-                         kChkTileQ6Window))
-            bulk_load(dst + r * kQ6Pitch, A.W + (start & ~15ull), win, BAR(B::kRawFull + rs));
+        for (int it = 0; it < kItems; ++it, ++tf) {
+          const int ts = tf % kTokStages;
+          if (tf >= kTokStages && !warp_wait(BAR(B::kTokEmpty + ts), ((tf / kTokStages) - 1) & 1, 2)) {
+            ok = false;
+            break;
+          }
+          if (lane == 0) {
+            const unsigned bytes = it < 8 ? kTileItem : kTileItemOp;
+            mbar_expect_tx(BAR(B::kTokFull + ts), bytes);
+            const size_t off = (static_cast<size_t>(tt) * A.nsb + b) * kTileRecord + static_cast<size_t>(it) * kTileItem;
+            if (XQ_CHECKED(off + bytes <= A.img_bytes && ((reinterpret_cast<uintptr_t>(A.img) + off) & 15) == 0,
+                           kChkTileItem))
+              bulk_load(smem_addr(tok_ring + ts * kTileItem), rec + static_cast<size_t>(b) * kTileRecord + it * kTileItem,
+                        bytes, BAR(B::kTokFull + ts));
+          }
         }
       }
-      for (int it = 0; it < kItems; ++it, ++tf) {
-        const int ts = tf % kTokStages;
-        if (tf >= kTokStages && !warp_wait(BAR(B::kTokEmpty + ts), ((tf / kTokStages) - 1) & 1, 2)) {
-          ok = false;
-          break;
-        }
-        if (lane == 0) {
-          const unsigned bytes = it < 8 ? kTileItem : kTileItemOp;
-          mbar_expect_tx(BAR(B::kTokFull + ts), bytes);
-          const size_t off = (static_cast<size_t>(tt) * A.nsb + b) * kTileRecord + static_cast<size_t>(it) * kTileItem;
-          if (XQ_CHECKED(off + bytes <= A.img_bytes && ((reinterpret_cast<uintptr_t>(A.img) + off) & 15) == 0,
-                         kChkTileItem))
-            bulk_load(smem_addr(tok_ring + ts * kTileItem), rec + static_cast<size_t>(b) * kTileRecord + it * kTileItem,
-                      bytes, BAR(B::kTokFull + ts));
+      // No copy may still be landing when the CTA exits: wait for the last
+      // fill of every stage (already complete on the normal path).
+      if (lane == 0) {
+        const int nb = A.nsb;
+        for (int b = nb > RS ? nb - RS : 0; b < nb; ++b) wait_bar(BAR(B::kRawFull + b % RS), (b / RS) & 1, 11);
+        for (unsigned f = tf > kTokStages ? tf - kTokStages : 0; f < tf; ++f)
+          wait_bar(BAR(B::kTokFull + f % kTokStages), (f / kTokStages) & 1, 12);
+      }
+      __syncwarp();
+    } else {
+      // ------------------------------------------------------------- MMA
+      // kMma issuing threads: thread k issues items f = k, k + kMma, ... in
+      // order, item f into accumulator f % kNumD. Each thread's chain of waits,
+      // MMAs and commits is serial; the epilogue frees the accumulators in item
+      // order, so one issuer keeps the same order as several.
+      const int k = warp - R::kMma0;
+      if (lane == 0 && k < nitems) {
+        constexpr uint32_t kIdH = idesc_f16(kTileTokens, kRows, false);
+        constexpr uint32_t kIdB = idesc_f16(kTileTokens, kRows, true);
+        const uint32_t tok0 = smem_addr(tok_ring), w0 = smem_addr(w_ring);
+        for (int f = k; f < nitems; f += R::kMma) {
+          const int ts = f % kTokStages, ws = f % kWStages, d = f % kNumD, it = f % kItems;
+          if (!wait_bar_spin(BAR(B::kTokFull + ts), (f / kTokStages) & 1, 6)) break;
+          if (!wait_bar_spin(BAR(B::kWFull + ws), (f / kWStages) & 1, 7)) break;
+          if (f >= kNumD && !wait_bar_spin(BAR(B::kDEmpty + d), ((f / kNumD) - 1) & 1, 8)) break;
+          tc_fence_after();
+          const uint32_t dt = tmem + kColD + 128u * d;
+          const uint32_t as = tok0 + ts * kTileItem, bs = w0 + ws * F::kWBytes;
+          const uint64_t a0 = smem_desc(as, 128, 512), a1 = smem_desc(as + 256, 128, 512);
+          const uint32_t id = (TYPE == 12 && it == 8) ? kIdB : kIdH;
+          mma_f16_ss(dt, a0, smem_desc(bs, 128, 512), id, false);
+          mma_f16_ss(dt, a1, smem_desc(bs + 256, 128, 512), id, true);
+          if ((TYPE == 14 || TYPE == 23) && split_flag[ws]) {
+            mma_f16_ss(dt, a0, smem_desc(bs + kOpBytes, 128, 512), id, true);
+            mma_f16_ss(dt, a1, smem_desc(bs + kOpBytes + 256, 128, 512), id, true);
+          }
+          tc_commit(BAR(B::kWEmpty + ws));
+          tc_commit(BAR(B::kDFull + d));
         }
       }
+      // all issued MMAs complete before TMEM is freed
+      if (lane == 0) {
+        tc_commit(BAR(B::kDone + k));
+        wait_bar_spin(BAR(B::kDone + k), 0, 9);
+      }
+      __syncwarp();
     }
-    // No copy may still be landing when the CTA exits: wait for the last
-    // fill of every stage (already complete on the normal path).
-    if (lane == 0) {
-      const int nb = A.nsb;
-      for (int b = nb > RS ? nb - RS : 0; b < nb; ++b) wait_bar(BAR(B::kRawFull + b % RS), (b / RS) & 1, 11);
-      for (unsigned f = tf > kTokStages ? tf - kTokStages : 0; f < tf; ++f)
-        wait_bar(BAR(B::kTokFull + f % kTokStages), (f / kTokStages) & 1, 12);
-    }
-    __syncwarp();
   } else if (warp < 4) {
     // ---------------------------------------------------------- unpack
     const int r = threadIdx.x;  // tile row
@@ -579,66 +660,18 @@ __global__ void __launch_bounds__(kThreads, 1) tile_mma_kernel(const __grid_cons
       __syncwarp();
       if (lane == 0) mbar_arrive(BAR(B::kRawEmpty + rs));
     }
-  } else if (warp >= kWarpMma) {
-    // ------------------------------------------------------------- MMA
-    // Three issuing threads, one per accumulator: thread k issues the items
-    // f = k, k+3, k+6, ... into accumulator k. Each thread's chain of waits,
-    // MMAs and commits is serial; three of them keep the tensor core fed.
-    const int k = warp - kWarpMma;
-    if (lane == 0 && k < nitems) {
-      constexpr uint32_t kIdH = idesc_f16(kTileTokens, kRows, false);
-      constexpr uint32_t kIdB = idesc_f16(kTileTokens, kRows, true);
-      const uint32_t dt = tmem + kColD + 128u * k;
-      const uint32_t tok0 = smem_addr(tok_ring), w0 = smem_addr(w_ring);
-      // ring positions of item f, advanced by kNumD per step
-      int it = k, ts = k, ws = k;
-      unsigned tpar = 0, wpar = 0;
-      for (int f = k, step = 0; f < nitems; f += kNumD, ++step) {
-        if (!wait_bar_spin(BAR(B::kTokFull + ts), tpar, 6)) break;
-        if (!wait_bar_spin(BAR(B::kWFull + ws), wpar, 7)) break;
-        if (step > 0 && !wait_bar_spin(BAR(B::kDEmpty + k), (step - 1) & 1, 8)) break;
-        tc_fence_after();
-        const uint32_t as = tok0 + ts * kTileItem, bs = w0 + ws * F::kWBytes;
-        const uint64_t a0 = smem_desc(as, 128, 512), a1 = smem_desc(as + 256, 128, 512);
-        const uint32_t id = (TYPE == 12 && it == 8) ? kIdB : kIdH;
-        mma_f16_ss(dt, a0, smem_desc(bs, 128, 512), id, false);
-        mma_f16_ss(dt, a1, smem_desc(bs + 256, 128, 512), id, true);
-        if ((TYPE == 14 || TYPE == 23) && split_flag[ws]) {
-          mma_f16_ss(dt, a0, smem_desc(bs + kOpBytes, 128, 512), id, true);
-          mma_f16_ss(dt, a1, smem_desc(bs + kOpBytes + 256, 128, 512), id, true);
-        }
-        tc_commit(BAR(B::kWEmpty + ws));
-        tc_commit(BAR(B::kDFull + k));
-        it += kNumD;
-        if (it >= kItems) it -= kItems;
-        ts += kNumD;
-        if (ts >= kTokStages) {
-          ts -= kTokStages;
-          tpar ^= 1u;
-        }
-        ws += kNumD;
-        if (ws >= kWStages) {
-          ws -= kWStages;
-          wpar ^= 1u;
-        }
-      }
-    }
-    // all issued MMAs complete before TMEM is freed
-    if (lane == 0) {
-      tc_commit(BAR(B::kDone + k));
-      wait_bar_spin(BAR(B::kDone + k), 0, 9);
-    }
-    __syncwarp();
   } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsEpi));
     // -------------------------------------------------------- epilogue
-    const int quarter = warp & 3, half = (warp - kWarpEpi0) >> 2;
+    const int quarter = warp & 3, part = (warp - R::kEpi0) >> 2;
+    constexpr int kCols = R::kCols;           // weight columns of this thread
     const int r = quarter * 32 + lane;        // token of the tile = TMEM lane
     const int m = tt * kTileTokens + r;
-    const int n0 = wt * kRows + 64 * half;    // first weight row of this thread's columns
+    const int n0 = wt * kRows + kCols * part;  // first weight row of this thread's columns
     const uint32_t tl = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-    f2 acc[32];                               // weight-row pairs (2i, 2i+1) of the current super-block
+    f2 acc[kCols / 2];                        // weight-row pairs (2i, 2i+1) of the current super-block
 #pragma unroll
-    for (int i = 0; i < 32; ++i) acc[i] = 0ull;
+    for (int i = 0; i < kCols / 2; ++i) acc[i] = 0ull;
     bool ok = true;
     int f = 0;
     for (int b = 0; b < A.nsb && ok; ++b) {
@@ -650,7 +683,7 @@ __global__ void __launch_bounds__(kThreads, 1) tile_mma_kernel(const __grid_cons
           break;
         }
         tc_fence_after();
-        const uint32_t dcol = tl + kColD + 128u * d + 64u * half;
+        const uint32_t dcol = tl + kColD + 128u * d + static_cast<uint32_t>(kCols * part);
         if (TYPE == 8 && it == 0 && !warp_wait(BAR(B::kCoefFull + b % kCoefStages), (b / kCoefStages) & 1, 14)) {
           ok = false;
           break;
@@ -659,10 +692,11 @@ __global__ void __launch_bounds__(kThreads, 1) tile_mma_kernel(const __grid_cons
           const float d8 = reinterpret_cast<const float*>(tok_ring + ts * kTileItem + kTileItemOp)[r];
           const f2 d82 = pk(d8, d8);
           // Q8_0: this block's per-row scales (pairs of this thread's rows)
-          const float2* dsp = reinterpret_cast<const float2*>(ds_ring + ((b % kCoefStages) * 8 + it) * kRows + 64 * half);
+          const float2* dsp =
+              reinterpret_cast<const float2*>(ds_ring + ((b % kCoefStages) * 8 + it) * kRows + kCols * part);
           // two 16-column loads in flight per wait
 #pragma unroll
-          for (int c = 0; c < 4; c += 2) {
+          for (int c = 0; c < kCols / 16; c += 2) {
             uint32_t v[16], w[16];
             tmem_ld16(dcol + 16 * c, v);
             tmem_ld16(dcol + 16 * c + 16, w);
@@ -704,12 +738,12 @@ __global__ void __launch_bounds__(kThreads, 1) tile_mma_kernel(const __grid_cons
             ok = false;
             break;
           }
-          const float4* cf = reinterpret_cast<const float4*>(coef_ring + cs * kRows + 64 * half);
+          const float4* cf = reinterpret_cast<const float4*>(coef_ring + cs * kRows + kCols * part);
           const bool last = b == A.nsb - 1;
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
+          for (int c = 0; c < kCols / 16; ++c) {
             uint32_t run[16], dmin[16];
-            if (b > 0) tmem_ld16(tl + kColRun + 64u * half + 16u * c, run);
+            if (b > 0) tmem_ld16(tl + kColRun + static_cast<uint32_t>(kCols * part) + 16u * c, run);
             if (TYPE == 12) tmem_ld16(dcol + 16 * c, dmin);
             tmem_wait_ld();
             uint32_t out[16];
@@ -742,7 +776,7 @@ __global__ void __launch_bounds__(kThreads, 1) tile_mma_kernel(const __grid_cons
                 }
               }
             } else {
-              tmem_st16(tl + kColRun + 64u * half + 16u * c, out);
+              tmem_st16(tl + kColRun + static_cast<uint32_t>(kCols * part) + 16u * c, out);
             }
           }
           if (!last) tmem_wait_st();
@@ -761,7 +795,7 @@ __global__ void __launch_bounds__(kThreads, 1) tile_mma_kernel(const __grid_cons
 #undef BAR
   tc_fence_before();
   __syncthreads();
-  if (warp == kWarpMma) {
+  if (warp == R::kMma0) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
@@ -769,6 +803,17 @@ __global__ void __launch_bounds__(kThreads, 1) tile_mma_kernel(const __grid_cons
 
 template <int TYPE, bool SUMS>
 cudaError_t launch_tile(const TileArgs& A, int grid, cudaStream_t s, bool pdl) {
+  // The register split inside the kernel is sized for a launch allocation
+  // of exactly kRegsLaunch registers a thread; anything else is refused
+  // before launch (a split larger than the allocation would never complete).
+  static int regs_ok = -1;
+  if (regs_ok < 0) {
+    cudaFuncAttributes fa;
+    regs_ok = (cudaFuncGetAttributes(&fa, tile_mma_kernel<TYPE, SUMS>) == cudaSuccess && fa.numRegs == kRegsLaunch)
+                  ? 1
+                  : 0;
+  }
+  if (!regs_ok) return cudaErrorInvalidConfiguration;
   static bool smem_set = false;
   if (!smem_set) {
     const cudaError_t e = cudaFuncSetAttribute(tile_mma_kernel<TYPE, SUMS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -778,7 +823,7 @@ cudaError_t launch_tile(const TileArgs& A, int grid, cudaStream_t s, bool pdl) {
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid));
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(Roles<TYPE>::kThreads);
   cfg.dynamicSmemBytes = smem_bytes<TYPE>();
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
@@ -841,6 +886,12 @@ cudaError_t launch_tile_mma(int type, const uint8_t* W, const uint8_t* xq, int M
       return cudaErrorInvalidValue;
     return sums ? launch_tile<8, true>(A, grid, s, pdl) : launch_tile<8, false>(A, grid, s, pdl);
   }
+  // Q6_K: one tensor-map box per super-block when rows are 16-byte multiples
+  // (K a multiple of 2048), else a bulk copy per row
+  A.q6_tma = (A.row_bytes % 16) == 0 ? 1 : 0;
+  if (A.q6_tma && !encode_tma_2d(&A.map, CU_TENSOR_MAP_DATA_TYPE_UINT8, W, A.row_bytes,
+                                 static_cast<unsigned long long>(N), A.row_bytes, kQ6Pitch, kRows))
+    return cudaErrorInvalidValue;
   return sums ? launch_tile<14, true>(A, grid, s, pdl) : launch_tile<14, false>(A, grid, s, pdl);
 }
 
