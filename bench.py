@@ -534,6 +534,22 @@ def gpu_arm(args):
     ms_per_step = 1e3 * secs / args.steps
     value = aggregate_value(nbytes, world, secs / args.steps)
 
+    # ---- per-step distribution (context; outside the timed region): each of
+    # 50 steps timed on its own with CUDA events
+    import torch
+    s_cur = torch.cuda.current_stream()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(50)]
+    for a, b in evs:
+        a.record(s_cur)
+        sweep.step(M)
+        b.record(s_cur)
+    torch.cuda.synchronize()
+    per_step = sorted(a.elapsed_time(b) for a, b in evs)
+    step_dist = {"n": len(per_step), "median_ms": round(statistics.median(per_step), 4),
+                 "p10_ms": round(per_step[len(per_step) // 10], 4),
+                 "p90_ms": round(per_step[(9 * len(per_step)) // 10], 4),
+                 "note": "each step timed alone (events between steps), so adjacent layers of two steps do not overlap"}
+
     # ---- the same sweep at other M
     by_m = {}
     for m in ms_list:
@@ -694,7 +710,7 @@ def gpu_arm(args):
             "hbm_frac": round(value / world / peak, 4), "hbm_peak_GBps": peak, "hbm_peak_source": peak_kind,
             "tokens_per_s": round(M * world / (secs / args.steps), 1),
             "gpu_launches": sweep.launches_per_step(M) * args.steps,
-            "clocks": clocks, "roofline": roofline, "by_m": by_m,
+            "clocks": clocks, "roofline": roofline, "by_m": by_m, "step_distribution": step_dist,
             "e2e": e2e, "secondary": secondary, "cpu_baseline": cpu,
         }
         print(json.dumps(line), flush=True)
@@ -774,6 +790,16 @@ def secondary_workloads(device, world):
             s = max_over_ranks(s, world, device) / (5 * copies)
             res[str(M)] = {"GBps": round(wl.layer_weight_bytes() / s / 1e9, 1), "us_per_layer": round(1e6 * s, 2),
                            "tokens_per_s": round(M / s, 1)}
+            if wl.layer_weight_bytes() < L2_BYTES:
+                # context only: the same layer repeated on one copy, its
+                # weights resident in L2 ("hot")
+                def hot():
+                    for _ in range(copies):
+                        xq.layer_mixed(descs[0], ins, M, ws)
+
+                sh = max_over_ranks(time_region(hot, 5, 3, world, device), world, device) / (5 * copies)
+                res[str(M)]["hot_l2_resident"] = {"GBps": round(wl.layer_weight_bytes() / sh / 1e9, 1),
+                                                  "us_per_layer": round(1e6 * sh, 2)}
         out[name] = {"rotated_copies": copies, "layer_bytes": wl.layer_weight_bytes(), "by_m": res}
     # the Llama-3-8B-shaped layer with its down projection fed by
     # silu(gate) * up of the same call (xq_layer_mixed_ffn), against the same
