@@ -787,12 +787,12 @@ __device__ __forceinline__ int next_task(const Group& G, int cur) {
 //     4h..4h+3) and forms each sub-block's isum with 8 dp4a per token.
 // The fp32 arithmetic is the MMA consumer's, operation for operation, so the
 // two forms give bit-identical y (batch invariance across M holds):
-//   - the dp4a accumulator starts at the bit pattern of 0.75f (low nibbles)
-//     or 12.0f (high nibbles); the int32 result is that float plus isum
-//     units in the last place, which are 2^-24 and 2^-20 there, so
-//     subtracting the float leaves exactly the MMA's D (isum * 2^-24, or
-//     isum * 2^-20 for the in-place high nibble); |isum| <= 15*127*32 < 2^22
-//     keeps the sum inside the float's binade;
+//   - high nibbles stay in place (16q, one mask per word), as in the MMA
+//     operand; the dp4a accumulator starts at the bit pattern of 0.75f,
+//     whose unit in the last place is 2^-24, so the int32 result is 0.75f
+//     plus isum (low nibbles) or 16 isum (high) units, and subtracting 0.75f
+//     leaves exactly the MMA's D (isum * 2^-24, or isum * 2^-20);
+//     |16 isum| <= 16*15*127*32 < 2^22 keeps the sum inside the binade;
 //   - the coefficients carry the same 2^24 / 2^20 factors as
 //     decode_scales_q4, and each sub-block adds
 //     fma(RN(a*d8), D, fma(-dmin*m, s8, acc)) as compute_block_q4 does;
@@ -839,7 +839,6 @@ __device__ __forceinline__ void act_load(uint32_t st, const Proj& P, int b, uint
 }
 
 constexpr int kMagicLo = 0x3F400000;  // 0.75f: unit in the last place 2^-24
-constexpr int kMagicHi = 0x41400000;  // 12.0f: unit in the last place 2^-20
 
 // One super-block of the lane's row (small form): acc[m] = the super-block's
 // fresh accumulator for token m < P.M, complete in the lanes of half 1.
@@ -874,7 +873,8 @@ __device__ __forceinline__ void compute_small_q4(const uint8_t* blk, const uint8
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const uint32_t x = w[8 * (k >> 1) + i];
-      nib[k][i] = ((k & 1) ? (x >> 4) : x) & 0x0F0F0F0Fu;
+      // high nibbles stay in place (16q): one mask, no shift
+      nib[k][i] = x & ((k & 1) ? 0xF0F0F0F0u : 0x0F0F0F0Fu);
     }
   const int nsub = P.K >> 5;
 #pragma unroll
@@ -888,7 +888,7 @@ __device__ __forceinline__ void compute_small_q4(const uint8_t* blk, const uint8
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         const uint4 a0 = ap[2 * k], a1 = ap[2 * k + 1];
-        const int magic = (k & 1) ? kMagicHi : kMagicLo;
+        const int magic = kMagicLo;
         int v = dp4a_us(nib[k][0], a0.x, magic);
         v = dp4a_us(nib[k][1], a0.y, v);
         v = dp4a_us(nib[k][2], a0.z, v);
@@ -899,9 +899,10 @@ __device__ __forceinline__ void compute_small_q4(const uint8_t* blk, const uint8
         v = dp4a_us(nib[k][7], a1.w, v);
         if (ISUM && row < P.N) {
           const size_t ii = (static_cast<size_t>(m) * P.N + row) * nsub + 8 * b + 4 * h + k;
-          if (XQ_IN(ii, static_cast<size_t>(P.M) * P.N * nsub, kChkGemvIsum)) P.isum[ii] = v - magic;
+          if (XQ_IN(ii, static_cast<size_t>(P.M) * P.N * nsub, kChkGemvIsum))
+            P.isum[ii] = (k & 1) ? (v - magic) >> 4 : v - magic;
         }
-        D[k] = __int_as_float(v) - ((k & 1) ? 12.0f : 0.75f);
+        D[k] = __int_as_float(v) - 0.75f;
         cf[k] = al[k] * d8[k];
       }
       // sub-blocks 0..3 from zero (half 0), then 4..7 from half 0's result
