@@ -147,6 +147,124 @@ quantize_q8_kernel(const __grid_constant__ QuantGroup G) {
   }
 }
 
+// The same quantization for inputs whose Q8 buffer holds the tile image
+// (M > 64 tokens): one warp per (token, 256-feature super-block), lane l
+// taking feature l of each of its eight 32-blocks, so that eight 128-byte
+// loads are in flight per warp and each block's max and quant sum come from
+// warp reductions. Every element goes through the steps of q8_quantize_lane
+// (the max and the integer sum do not depend on their order), so the bytes
+// equal quantize_q8_kernel's. Padding tokens of the last 128-token tile get
+// zeros in the image, as there.
+__global__ void __launch_bounds__(256)
+quantize_q8_tile_kernel(const __grid_constant__ QuantGroup G) {
+  const int lane = threadIdx.x & 31;
+  const unsigned warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const unsigned nwarps = (gridDim.x * blockDim.x) >> 5;
+  const unsigned total = G.blk0[G.n] >> 3;  // super-block units (blk0 counts padded 32-blocks)
+  {
+    int jb = 0;
+    for (unsigned u = warp; u < total; u += nwarps) {
+      while (u >= (G.blk0[jb + 1] >> 3)) ++jb;
+      const QuantItem& J = G.job[jb];
+      const unsigned local = u - (G.blk0[jb] >> 3);
+      const int nsb = J.K >> 8;
+      const int m = static_cast<int>(local / static_cast<unsigned>(nsb));
+      const int b = static_cast<int>(local - static_cast<unsigned>(m) * nsb);
+      if (m < J.M && lane < 8) {
+        const size_t idx = static_cast<size_t>(m) * J.K + 256 * b + 32 * lane;
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(J.x + idx));
+        if (J.up) asm volatile("prefetch.global.L2 [%0];" ::"l"(J.up + idx));
+      }
+    }
+  }
+  cudaGridDependencySynchronize();
+  cudaTriggerProgrammaticLaunchCompletion();
+  if (blockIdx.x == 0)
+    for (int i = threadIdx.x; i < G.zero_count; i += blockDim.x) G.zero_words[i] = 0u;
+  const int ks = (lane & ~7) | gemv_image_slot(lane);  // k-slot of this lane's feature in a tile item
+
+  int jb = 0;
+  for (unsigned u = warp; u < total; u += nwarps) {
+    while (u >= (G.blk0[jb + 1] >> 3)) ++jb;
+    const QuantItem& J = G.job[jb];
+    const unsigned local = u - (G.blk0[jb] >> 3);
+    const int nsb = J.K >> 8, nsub = J.nsub;
+    const int m = static_cast<int>(local / static_cast<unsigned>(nsb));
+    const int b = static_cast<int>(local - static_cast<unsigned>(m) * nsb);
+    const bool live = m < J.M;
+    if (!XQ_CHECKED(J.ttiles > 0 && J.tile + (static_cast<size_t>(m >> 7) + 1) * nsb * kTileRecord <= J.total &&
+                        J.s8 + 4 * (static_cast<size_t>(J.M) * nsub) <= J.total,
+                    kChkQuantImage))
+      continue;
+    float v[8];
+    const size_t base = static_cast<size_t>(m) * J.K + 256 * b + lane;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = live ? __ldg(J.x + base + 32 * i) : 0.0f;
+    if (J.up && live) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        v[i] = swiglu(v[i], __ldg(J.up + base + 32 * i));
+        if (J.h_out) J.h_out[base + 32 * i] = v[i];
+      }
+    }
+    float d[8], sc[8];
+    int q[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      // the steps of q8_quantize_lane, block i
+      const unsigned amax_bits = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(v[i])));
+      d[i] = __fdiv_rn(__uint_as_float(amax_bits), 127.0f);
+      const float id = (d[i] != 0.0f) ? __frcp_rn(d[i]) : 0.0f;
+      float x = roundf(__fmul_rn(v[i], id));
+      x = (x != x) ? 0.0f : x;
+      x = x > 127.0f ? 127.0f : (x < -127.0f ? -127.0f : x);
+      q[i] = static_cast<int>(x);
+      sc[i] = __fmul_rn(d[i], static_cast<float>(__reduce_add_sync(0xffffffffu, q[i])));
+    }
+    if (live) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) J.xq[base + 32 * i] = static_cast<uint8_t>(static_cast<int8_t>(q[i]));
+      if (lane < 8) {
+        float dl = d[0], sl = sc[0];
+#pragma unroll
+        for (int i = 1; i < 8; ++i)
+          if (lane == i) {
+            dl = d[i];
+            sl = sc[i];
+          }
+        reinterpret_cast<float*>(J.xq + J.d8)[static_cast<size_t>(m) * nsub + 8 * b + lane] = dl;
+        reinterpret_cast<float*>(J.xq + J.s8)[static_cast<size_t>(m) * nsub + 8 * b + lane] = sl;
+      }
+    }
+    // tile image record (tile m / 128, super-block b), token r = m % 128
+    const int r = m & 127;
+    uint8_t* rec = J.xq + J.tile + (static_cast<size_t>(m >> 7) * nsb + b) * kTileRecord;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      uint8_t* item = rec + i * kTileItem;
+      *reinterpret_cast<__half*>(item + tile_offset(r, ks)) = __int2half_rn(q[i]);
+      if (lane == i) reinterpret_cast<float*>(item + kTileItemOp)[r] = d[i];
+    }
+    // min-term operand: slot 3i + p holds bf16 piece p of s8 of block i
+    // (s8 = p0 + p1 + p2, each the upper 16 bits of an fp32), slots 24-31 zero
+    uint16_t piece = 0;
+    if (lane < 24) {
+      const int i = lane / 3, pc = lane - 3 * i;
+      float sv = sc[0];
+#pragma unroll
+      for (int k = 1; k < 8; ++k)
+        if (i == k) sv = sc[k];
+      const float p0 = __uint_as_float(__float_as_uint(sv) & 0xFFFF0000u);
+      const float r1 = __fsub_rn(sv, p0);
+      const float p1 = __uint_as_float(__float_as_uint(r1) & 0xFFFF0000u);
+      const float p2 = __fsub_rn(r1, p1);
+      const float pv = pc == 0 ? p0 : (pc == 1 ? p1 : p2);
+      piece = static_cast<uint16_t>(__float_as_uint(pv) >> 16);
+    }
+    *reinterpret_cast<uint16_t*>(rec + 8 * kTileItem + tile_offset(r, lane)) = piece;
+  }
+}
+
 cudaError_t take_quant_check(unsigned int* code) { return take_check_word(code); }
 
 cudaError_t launch_quantize_q8(const QuantJob* jobs, int n, cudaStream_t s, bool pdl, unsigned int* zero_words,
@@ -183,6 +301,23 @@ cudaError_t launch_quantize_q8(const QuantJob* jobs, int n, cudaStream_t s, bool
     G.blk0[k + 1] = static_cast<unsigned>(nblocks);
   }
   if (nblocks == 0) return cudaSuccess;
+  bool tiles = true;  // every input in the tile layout: the super-block quantizer
+  for (int k = 0; k < n; ++k) tiles = tiles && G.job[k].ttiles > 0;
+  if (tiles) {
+    const long long units = nblocks / 8;
+    long long want = (units + 7) / 8;  // 8 warps per CTA, one super-block per warp and pass
+    const long long cap = static_cast<long long>(kNumSMs) * 8;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(want < cap ? want : cap));
+    cfg.blockDim = dim3(256);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, quantize_q8_tile_kernel, G);
+  }
   long long want = (nblocks + 31) / 32;  // 32 warps per CTA, one block per warp
   const long long cap = static_cast<long long>(kNumSMs) * 2;  // all resident
   cudaLaunchConfig_t cfg = {};
