@@ -863,8 +863,11 @@ xq_status ffn_plan(const xq_proj* proj, int n_proj, int n_inputs, int M, int gat
   need += round256(xq_q8_bytes(M, d.K));
   // fused feed: gate and up in the GEMV group, in one launch of their type
   f->fused = false;
+  // (h's blocks are counted per pair of 16-row groups of consecutive rows, so
+  // Q6_K gate/up rows in the grouped view keep the separate feed launch)
+  const bool grouped_rows = proj[gate].type == XQ_TYPE_Q6_K && xq::q6k_row_shift(proj[gate].K) > 0;
   if (M >= 1 && M <= kMaxGemvM && in_group(proj[gate], M) && in_group(proj[up], M) &&
-      proj[gate].type == proj[up].type) {
+      proj[gate].type == proj[up].type && !grouped_rows) {
     int same = 0;
     for (int p = 0; p < n_proj; ++p) same += (in_group(proj[p], M) && proj[p].type == proj[gate].type) ? 1 : 0;
     f->fused = same <= xq::kMaxProj;

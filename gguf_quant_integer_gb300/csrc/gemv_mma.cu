@@ -920,11 +920,103 @@ __device__ __forceinline__ void compute_small_q4(const uint8_t* blk, const uint8
   }
 }
 
+// Q6_K in the small form: one super-block of the lane's row, half h (weights
+// 128h..128h+127: 32-blocks p = 4h + k, ql bytes 64h.., qh bytes 128 + 32h..,
+// scales 192 + 8h..), the super-block starting `off` bytes into its window.
+// The MMA form's arithmetic, operation for operation:
+//   - a byte's 6-bit q (low nibble from ql, two bits from qh) becomes
+//     4 (q - 32) as a signed byte, (q ^ 0x20) << 2, and one dp4a per word
+//     sums 4 (q - 32) * a;
+//   - the dp4a accumulator starts at the bits of 3145728.0f, whose unit in
+//     the last place is 0.25, so subtracting that float leaves each 16-group's
+//     exact integer sum (|4 isum| < 2^22 keeps it in the binade): Da = the
+//     32-block's sum, D1 = its second group's, as the MMA form's D;
+//   - alpha = d * s_2p and delta = d * (s_2p+1 - s_2p) as decode_scales_q6,
+//     and acc = fma(alpha d8, Da, fma(delta d8, D1, acc)) in 32-block order.
+constexpr int kMagicQ6 = 0x4A400000;  // 3145728.0f: unit in the last place 0.25
+
+template <bool ISUM>
+__device__ __forceinline__ void compute_small_q6(const uint8_t* blk, int off, const uint8_t* act, const Proj& P, int row,
+                                                 int b, int r, int h, int lane, float (&acc)[2]) {
+  const uint8_t* sb = blk + r * GLay<14>::kBoxRow + off;
+  uint32_t ql[16], qh[8], sw[2];
+  load_words<16>(sb + 64 * h, ql);
+  load_words<8>(sb + 128 + 32 * h, qh);
+  load_words<2>(sb + 192 + 8 * h, sw);
+  const float d = half_bits_to_float(*reinterpret_cast<const unsigned short*>(sb + 208));
+  float al[4], de[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const uint32_t w = sw[k >> 1];
+    const int b0 = 2 * (k & 1);
+    const int s0 = static_cast<int8_t>((w >> (8 * b0)) & 0xFFu);
+    const int s1 = static_cast<int8_t>((w >> (8 * b0 + 8)) & 0xFFu);
+    al[k] = d * static_cast<float>(s0);
+    de[k] = d * static_cast<float>(s1 - s0);
+  }
+  // 4 (q - 32) of weights 4i..4i+3 of 32-block k
+  uint32_t y[4][8];
+#pragma unroll
+  for (int k = 0; k < 4; ++k)
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const uint32_t Lw = (k & 1) ? ql[8 + i] : ql[i];
+      const uint32_t L = ((k >> 1) ? (Lw >> 4) : Lw) & 0x0F0F0F0Fu;
+      const uint32_t H = (k == 0 ? (qh[i] << 4) : (k == 1 ? (qh[i] << 2) : (k == 2 ? qh[i] : (qh[i] >> 2)))) & 0x30303030u;
+      y[k][i] = ((L | H) ^ 0x20202020u) << 2;
+    }
+  const int ngrp = P.K >> 4;
+#pragma unroll
+  for (int m = 0; m < 2; ++m) {
+    if (m < P.M) {
+      const uint4* ap = reinterpret_cast<const uint4*>(act + 256 * m + 128 * h);
+      const float4 dv = *reinterpret_cast<const float4*>(act + 512 + 32 * m + 16 * h);
+      const float d8[4] = {dv.x, dv.y, dv.z, dv.w};
+      float Da[4], D1[4], ca[4], cd[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const uint4 a0 = ap[2 * k], a1 = ap[2 * k + 1];
+        int v0 = dp4a_ss(y[k][0], a0.x, kMagicQ6);
+        v0 = dp4a_ss(y[k][1], a0.y, v0);
+        v0 = dp4a_ss(y[k][2], a0.z, v0);
+        v0 = dp4a_ss(y[k][3], a0.w, v0);
+        int v1 = dp4a_ss(y[k][4], a1.x, kMagicQ6);
+        v1 = dp4a_ss(y[k][5], a1.y, v1);
+        v1 = dp4a_ss(y[k][6], a1.z, v1);
+        v1 = dp4a_ss(y[k][7], a1.w, v1);
+        const float g0 = __int_as_float(v0) - 3145728.0f, g1 = __int_as_float(v1) - 3145728.0f;
+        D1[k] = g1;
+        Da[k] = g0 + g1;
+        if (ISUM && row < P.N) {
+          const size_t ii = (static_cast<size_t>(m) * P.N + row) * ngrp + 16 * b + 8 * h + 2 * k;
+          if (XQ_IN(ii + 1, static_cast<size_t>(P.M) * P.N * ngrp, kChkGemvIsum)) {
+            P.isum[ii] = static_cast<int32_t>(g0);
+            P.isum[ii + 1] = static_cast<int32_t>(g1);
+          }
+        }
+        ca[k] = al[k] * d8[k];
+        cd[k] = de[k] * d8[k];
+      }
+      // 32-blocks 0..3 from zero (half 0), then 4..7 from half 0's result
+      float c = 0.0f;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) c = fmaf(ca[k], Da[k], fmaf(cd[k], D1[k], c));
+      const float c0 = __shfl_sync(0xffffffffu, c, lane & ~1);
+      if (h) {
+        c = c0;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) c = fmaf(ca[k], Da[k], fmaf(cd[k], D1[k], c));
+      }
+      acc[m] = c;
+    }
+  }
+}
+
 // The last warp to finish a split 16-row group (small form): lane 2r+1 adds
 // row r's chunk partials in chunk order (as reduce_chunks does).
 __device__ __forceinline__ void reduce_chunks_small(const Proj& P, int rg, int r, int h) {
   const int rows_pad = gemv_row_blocks(P.N) * kGemvRows;
-  const int row = rg * 16 + r;
+  const int row = group_row(P, rg, r);
   if (h == 0 || row >= P.N) return;
   for (int m = 0; m < P.M; ++m) {
     float v = 0.0f;
@@ -941,7 +1033,7 @@ __device__ __forceinline__ TaskPos task_pos(const Group& G, int task);
 
 // Consumer loop of the small form (the same ring, meta, task and split
 // protocol as the MMA consumers).
-template <bool ISUM, bool FFN>
+template <int TYPE, bool ISUM, bool FFN>
 __device__ __forceinline__ void small_consumer(const Group& G, const uint8_t* ring, const int4* meta, uint32_t full_s,
                                                uint32_t empty_s, int kStages, int kStageBytes, int kBlockBytes,
                                                int kFragOff, int warp, int lane) {
@@ -980,10 +1072,18 @@ __device__ __forceinline__ void small_consumer(const Group& G, const uint8_t* ri
     }
     const Proj& P = G.p[tp.p];
     const int rg = tp.rb * kGemvWarps + warp;
-    const int row = rg * 16 + r;
+    const int row = group_row(P, rg, r);
     const uint8_t* st = ring + slot * kStageBytes;
     float acc[2] = {0.0f, 0.0f};
-    if (rg * 16 < P.N) compute_small_q4<ISUM>(st + warp * kBlockBytes, st + kFragOff, P, row, m.y, r, h, lane, acc);
+    if (rg * 16 < P.N) {
+      if constexpr (TYPE == 12) {
+        compute_small_q4<ISUM>(st + warp * kBlockBytes, st + kFragOff, P, row, m.y, r, h, lane, acc);
+      } else {
+        // the same in-window offset for every row of the group (as the MMA form)
+        const int off = (kQ6kBytes * ((P.K >> 8) * (rg & ((1 << P.gs) - 1)) + m.y)) & 15;
+        compute_small_q6<ISUM>(st + warp * kBlockBytes, off, st + kFragOff, P, row, m.y, r, h, lane, acc);
+      }
+    }
     __syncwarp();
     if (lane == 0) mbar_arrive(empty_s + 8 * slot);
     run[0] += acc[0];
@@ -1143,7 +1243,8 @@ __device__ __forceinline__ void gemv_mma_body(const Group& G) {
   if (G.wait_prev) cudaGridDependencySynchronize();
   cudaTriggerProgrammaticLaunchCompletion();
   if constexpr (SMALL) {
-    small_consumer<ISUM, FFN>(G, ring, meta, full_s, empty_s, kStages, kStageBytes, kBlockBytes, kFragOff, warp, lane);
+    small_consumer<TYPE, ISUM, FFN>(G, ring, meta, full_s, empty_s, kStages, kStageBytes, kBlockBytes, kFragOff, warp,
+                                    lane);
     return;
   }
   const int n8 = lane >> 2, t = lane & 3;
@@ -1459,9 +1560,9 @@ cudaError_t launch_gemv_mma(int type, const MmaProj* projs, int n, cudaStream_t 
   G.wait_limit = stall_test ? kStallWaitClocks : kWaitClocks;
   int total = 0;
   bool isum = false;
-  // Q4_K at one or two tokens takes the small-M (dp4a) form, except in the
-  // batch-invariant layout.
-  bool small = type == 12;
+  // Q4_K and Q6_K at one or two tokens take the small-M (dp4a) form, except
+  // in the batch-invariant layout.
+  bool small = type == 12 || type == 14;
   for (int k = 0; k < n; ++k)
     small = small && projs[k].M_total <= 2 && projs[k].chunk == 0 && !projs[k].gemv_image;
   for (int k = 0; k < n; ++k) {
@@ -1508,12 +1609,15 @@ cudaError_t launch_gemv_mma(int type, const MmaProj* projs, int n, cudaStream_t 
   // hook), so that other launches carry none of its code.
   const bool fz = ffn != nullptr;
   if (fz && isum) return cudaErrorInvalidValue;
-  const int cap = fz ? (small ? max_ctas<12, false, true, true>()
+  const bool s12 = small && type == 12, s14 = small && type == 14;
+  const int cap = fz ? (s12 ? max_ctas<12, false, true, true>()
+                       : s14 ? max_ctas<14, false, true, true>()
                        : type == 12 ? max_ctas<12, false, false, true>()
                        : type == 8  ? max_ctas<8, false, false, true>()
                        : type == 23 ? max_ctas<23, false, false, true>()
                                     : max_ctas<14, false, false, true>())
-                  : small      ? (isum ? max_ctas<12, true, true>() : max_ctas<12, false, true>())
+                  : s12        ? (isum ? max_ctas<12, true, true>() : max_ctas<12, false, true>())
+                  : s14        ? (isum ? max_ctas<14, true, true>() : max_ctas<14, false, true>())
                   : type == 12 ? (isum ? max_ctas<12, true>() : max_ctas<12, false>())
                   : type == 8  ? (isum ? max_ctas<8, true>() : max_ctas<8, false>())
                   : type == 23 ? (isum ? max_ctas<23, true>() : max_ctas<23, false>())
@@ -1531,7 +1635,8 @@ cudaError_t launch_gemv_mma(int type, const MmaProj* projs, int n, cudaStream_t 
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
   if (fz) {
-    if (small) return cudaLaunchKernelEx(&cfg, gemv_mma_kernel<12, false, true, true>, G);
+    if (s12) return cudaLaunchKernelEx(&cfg, gemv_mma_kernel<12, false, true, true>, G);
+    if (s14) return cudaLaunchKernelEx(&cfg, gemv_mma_kernel<14, false, true, true>, G);
     if (type == 12) return cudaLaunchKernelEx(&cfg, gemv_mma_kernel<12, false, false, true>, G);
     if (type == 8) return cudaLaunchKernelEx(&cfg, gemv_mma_kernel<8, false, false, true>, G);
     if (type == 23) return cudaLaunchKernelEx(&cfg, gemv_mma_kernel<23, false, false, true>, G);
@@ -1543,9 +1648,12 @@ cudaError_t launch_gemv_mma(int type, const MmaProj* projs, int n, cudaStream_t 
   if (type == 23)
     return isum ? cudaLaunchKernelEx(&cfg, gemv_mma_kernel<23, true, false, false>, G)
                 : cudaLaunchKernelEx(&cfg, gemv_mma_kernel<23, false, false, false>, G);
-  if (small)
+  if (s12)
     return isum ? cudaLaunchKernelEx(&cfg, gemv_mma_kernel<12, true, true, false>, G)
                 : cudaLaunchKernelEx(&cfg, gemv_mma_kernel<12, false, true, false>, G);
+  if (s14)
+    return isum ? cudaLaunchKernelEx(&cfg, gemv_mma_kernel<14, true, true, false>, G)
+                : cudaLaunchKernelEx(&cfg, gemv_mma_kernel<14, false, true, false>, G);
   if (type == 12)
     return isum ? cudaLaunchKernelEx(&cfg, gemv_mma_kernel<12, true, false, false>, G)
                 : cudaLaunchKernelEx(&cfg, gemv_mma_kernel<12, false, false, false>, G);

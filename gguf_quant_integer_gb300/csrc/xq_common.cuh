@@ -55,6 +55,12 @@ __device__ __forceinline__ int dp4a_us(unsigned a, unsigned b, int c) {
   asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
   return d;
 }
+// Four signed bytes of a times four signed bytes of b, plus c.
+__device__ __forceinline__ int dp4a_ss(unsigned a, unsigned b, int c) {
+  int d;
+  asm("dp4a.s32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
 
 // Byte permute of the 8-byte pair (hi:lo).
 __device__ __forceinline__ unsigned prmt(unsigned lo, unsigned hi, unsigned sel) {
