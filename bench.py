@@ -744,6 +744,28 @@ def secondary_workloads(device, world):
     out["tiny-gemv"] = {"M": 1, "N": p.N, "K": p.K, "rotated_copies": copies, "weight_bytes": wbytes,
                         "us_per_call": round(1e6 * sec, 3), "GBps": round(wbytes / sec / 1e9, 2),
                         "tokens_per_s": round(1 / sec, 1), "note": "quantize + matmul per call; launch-bound"}
+    # the same calls replayed from CUDA graphs (slices of 172 calls, weights
+    # still rotated): the GPU-side cost of a call without the host's launch
+    # overhead, for context
+    try:
+        graphs = []
+        for g0 in range(0, copies, 172):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                for c in range(g0, min(copies, g0 + 172)):
+                    xq.quantize_q8(x, out=buf)
+                    xq.matmul(p.qtype, Ws[c], buf, 1, p.N, p.K, y=y)
+            graphs.append(g)
+
+        def graph_step():
+            for g in graphs:
+                g.replay()
+
+        sg = max_over_ranks(time_region(graph_step, 3, 2, world, device), world, device) / (3 * copies)
+        out["tiny-gemv"]["from_cuda_graph"] = {"us_per_call": round(1e6 * sg, 3), "GBps": round(wbytes / sg / 1e9, 2)}
+        del graphs
+    except Exception as e:  # capture is context, not the measurement
+        out["tiny-gemv"]["from_cuda_graph"] = {"error": str(e)[:200]}
     # Q6_K rows that are not 16-byte multiples (the 8960 -> 1536 ffn_down of
     # the Qwen2.5-1.5B shape, 7350-byte rows): quantize + matmul per call
     N6, K6 = 1536, 8960
