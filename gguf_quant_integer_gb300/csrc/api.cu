@@ -262,6 +262,7 @@ struct FfnSpec {
   unsigned int* ready;
   uint8_t* hq;
   int F;
+  bool stall;  // test hook (xq_debug_stalled_ffn_layer)
 };
 
 xq_status layer_matmuls(const xq_proj* proj, int n_proj, const uint8_t* const* q8, int M, const Sched& sc,
@@ -417,6 +418,7 @@ xq_status layer_matmuls(const xq_proj* proj, int n_proj, const uint8_t* const* q
             fz.h_out = nullptr;
             fz.F = ffn->F;
             fz.M = M;
+            fz.stall = ffn->stall;
             fzp = &fz;
           } else if (id >= 0) {
             wait = true;  // h comes from an earlier grid
@@ -893,24 +895,13 @@ xq_status ffn_plan(const xq_proj* proj, int n_proj, int n_inputs, int M, int gat
   return XQ_OK;
 }
 
-}  // namespace
-
-extern "C" {
-
-size_t xq_layer_ffn_workspace_bytes(const xq_proj* proj, int n_proj, int n_inputs, int M, int gate, int up,
-                                    int down) {
-  FfnPlan f;
-  if (ffn_plan(proj, n_proj, n_inputs, M, gate, up, down, &f) != XQ_OK) return 0;
-  return f.total;
-}
-
-xq_status xq_layer_mixed_ffn(const xq_proj* proj, int n_proj, int gate, int up, int down,
-                             const float* const* inputs, int n_inputs, int M, void* workspace, size_t ws_bytes,
-                             xq_stream stream) {
+xq_status layer_ffn(const xq_proj* proj, int n_proj, int gate, int up, int down, const float* const* inputs,
+                    int n_inputs, int M, void* workspace, size_t ws_bytes, xq_stream stream, bool stall) {
   FfnPlan f;
   xq_status st = ffn_plan(proj, n_proj, n_inputs, M, gate, up, down, &f);
   if (st != XQ_OK) return st;
   if (M == 0) return XQ_OK;
+  if (stall && !f.fused) return XQ_ERR_UNSUPPORTED;
   if (n_inputs > 0 && !inputs) return XQ_ERR_ARG;
   for (int i = 0; i < n_inputs; ++i)
     if (f.in_k[i]) {
@@ -960,6 +951,7 @@ xq_status xq_layer_mixed_ffn(const xq_proj* proj, int n_proj, int gate, int up, 
     spec.ready = spec.arrive + F / 32;
     spec.hq = ws + f.h_off;
     spec.F = F;
+    spec.stall = stall;
     return layer_matmuls(f.all, n_proj, q8, M, f.sc_all, ws + f.sched_all, s, &spec);
   }
   // 1. every input to Q8 (the last launch zeroes A's scheduling state)
@@ -1002,6 +994,29 @@ xq_status xq_layer_mixed_ffn(const xq_proj* proj, int n_proj, int gate, int up, 
   const uint8_t* q8c[64];
   for (int k = 0; k < f.n_c; ++k) q8c[k] = f.c_input[k] < 0 ? ws + f.h_off : ws + f.off[f.c_input[k]];
   return layer_matmuls(f.c, f.n_c, q8c, M, f.sc_c, ws + f.sched_c, s);
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t xq_layer_ffn_workspace_bytes(const xq_proj* proj, int n_proj, int n_inputs, int M, int gate, int up,
+                                    int down) {
+  FfnPlan f;
+  if (ffn_plan(proj, n_proj, n_inputs, M, gate, up, down, &f) != XQ_OK) return 0;
+  return f.total;
+}
+
+xq_status xq_layer_mixed_ffn(const xq_proj* proj, int n_proj, int gate, int up, int down,
+                             const float* const* inputs, int n_inputs, int M, void* workspace, size_t ws_bytes,
+                             xq_stream stream) {
+  return layer_ffn(proj, n_proj, gate, up, down, inputs, n_inputs, M, workspace, ws_bytes, stream, false);
+}
+
+xq_status xq_debug_stalled_ffn_layer(const xq_proj* proj, int n_proj, int gate, int up, int down,
+                                     const float* const* inputs, int n_inputs, int M, void* workspace,
+                                     size_t ws_bytes, xq_stream stream) {
+  return layer_ffn(proj, n_proj, gate, up, down, inputs, n_inputs, M, workspace, ws_bytes, stream, true);
 }
 
 }  // extern "C"

@@ -103,6 +103,8 @@ struct Ffn {
   unsigned long long hq_bytes;               // size of h's Q8 buffer
   int gate, up, down;    // slots in Group::p (down -1: not in this launch)
   int F, M;              // h features (N of gate and up, K of down), tokens (<= 8)
+  int stall;             // test hook: h is written but never counted ready, so down's waits run out
+  long long ready_limit; // clocks down's producer waits for a super-block of h
 };
 
 struct Group {
@@ -729,7 +731,7 @@ __device__ __noinline__ void ffn_arrive(const Group& G, int rg, int lane) {
   }
   asm volatile("fence.proxy.async.global;" ::: "memory");
   __syncwarp();
-  if (lane == 0) {
+  if (lane == 0 && !F.stall) {
     __threadfence();
     atomicAdd(F.ready + (j >> 3), 1u);
   }
@@ -747,8 +749,8 @@ __device__ __forceinline__ bool ffn_wait_ready(const Group& G, int b) {
       __nanosleep(100);
       asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(f) : "memory");
       if (v >= 8u) break;
-      if (clock64() - t0 > G.wait_limit) {
-        atomicExch(&g_gemv_error, 3u);
+      if (clock64() - t0 > G.ffn.ready_limit) {
+        atomicCAS(&g_gemv_error, 0u, 3u);
         return false;
       }
     }
@@ -1549,6 +1551,8 @@ cudaError_t launch_gemv_mma(int type, const MmaProj* projs, int n, cudaStream_t 
     G.ffn.F = ffn->F;
     G.ffn.M = ffn->M;
     G.ffn.hq_bytes = H.total;
+    G.ffn.stall = ffn->stall ? 1 : 0;
+    G.ffn.ready_limit = ffn->stall ? kStallWaitClocks : kWaitClocks;
     for (int k = 0; k < n; ++k) {
       if (order[k] == ffn->gate) G.ffn.gate = k;
       if (order[k] == ffn->up) G.ffn.up = k;
@@ -1558,6 +1562,9 @@ cudaError_t launch_gemv_mma(int type, const MmaProj* projs, int n, cudaStream_t 
   G.wait_prev = (wait_prev || !pdl) ? 1 : 0;
   G.stall = stall_test ? 1 : 0;
   G.wait_limit = stall_test ? kStallWaitClocks : kWaitClocks;
+  // With h withheld, down's stage waits outlast the producer's wait for h,
+  // so that code 3 is the first error recorded.
+  if (ffn && ffn->stall) G.wait_limit = 4 * kStallWaitClocks;
   int total = 0;
   bool isum = false;
   // Q4_K and Q6_K at one or two tokens take the small-M (dp4a) form, except

@@ -256,6 +256,7 @@ struct FfnFuse {
   uint8_t* hq;
   float* h_out;  // optional fp32 copy of h [M][F]
   int F, M;
+  bool stall = false;  // test hook: h never counted ready; every wait limited to about 10^5 clocks
 };
 cudaError_t launch_gemv_mma(int type, const MmaProj* projs, int n, cudaStream_t s, bool pdl,
                             unsigned int* counter = nullptr, uint8_t* arrive_ws = nullptr,

@@ -42,7 +42,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t a, unsigned parity, unsigned 
   const long long t0 = clock64();
   while (!mbar_try_wait(a, parity)) {
     if (clock64() - t0 > limit) {
-      atomicExch(err, code);
+      atomicCAS(err, 0u, code);  // the first wait to run out is the one reported
       return false;
     }
   }
@@ -68,7 +68,7 @@ __device__ __forceinline__ bool mbar_wait_sleep(uint32_t a, unsigned parity, uns
   const long long t0 = clock64();
   while (!mbar_try_wait_sleep(a, parity, 20000u)) {
     if (clock64() - t0 > limit) {
-      atomicExch(err, code);
+      atomicCAS(err, 0u, code);  // the first wait to run out is the one reported
       return false;
     }
   }

@@ -31,7 +31,7 @@ SYMBOLS = ("xq_status_str", "xq_q8_bytes", "xq_weight_bytes", "xq_quantize_q8",
            "xq_matmul_q8_0_q8", "xq_debug_isums_q8_0", "xq_silu_mul_quantize_q8",
            "xq_layer_ffn_workspace_bytes", "xq_layer_mixed_ffn", "xq_matmul_iq4xs_q8",
            "xq_debug_isums_iq4xs", "xq_device_error", "xq_debug_stalled_matmul_q4k", "xq_debug_tile_sums",
-           "xq_debug_layer_matmuls", "xq_debug_check_probe")
+           "xq_debug_layer_matmuls", "xq_debug_check_probe", "xq_debug_stalled_ffn_layer")
 
 
 class XQError(RuntimeError):
@@ -74,6 +74,8 @@ def lib(path: str | None = None):
     L.xq_layer_mixed_ffn.argtypes = [ctypes.POINTER(xq_proj), I, I, I, I, ctypes.POINTER(ctypes.c_void_p), I, I,
                                      P, S, P]
     L.xq_layer_mixed_ffn.restype = I
+    L.xq_debug_stalled_ffn_layer.argtypes = L.xq_layer_mixed_ffn.argtypes
+    L.xq_debug_stalled_ffn_layer.restype = I
     L.xq_q8_bytes_invariant.argtypes = [I, I]
     L.xq_q8_bytes_invariant.restype = S
     L.xq_quantize_q8_invariant.argtypes = [P, I, I, P, P]
@@ -334,13 +336,18 @@ def layer_ffn_workspace_bytes(projs, n_inputs: int, M: int, gate: int, up: int, 
     return lib().xq_layer_ffn_workspace_bytes(_proj_array(projs), len(projs), n_inputs, M, gate, up, down)
 
 
-def layer_mixed_ffn(projs, gate: int, up: int, down: int, inputs, M: int, workspace, stream=None):
+def layer_mixed_ffn(projs, gate: int, up: int, down: int, inputs, M: int, workspace, stream=None, _fn="xq_layer_mixed_ffn"):
     """layer_mixed with projs[down] fed by silu(y_gate) * y_up of the same call."""
     arr = _proj_array(projs)
     ins = (ctypes.c_void_p * max(1, len(inputs)))(*[t.data_ptr() for t in inputs])
-    rc = lib().xq_layer_mixed_ffn(arr, len(projs), gate, up, down, ins, len(inputs), M, _ptr(workspace),
-                                  workspace.numel() if workspace is not None else 0, _stream(stream))
-    _check("xq_layer_mixed_ffn", rc)
+    rc = getattr(lib(), _fn)(arr, len(projs), gate, up, down, ins, len(inputs), M, _ptr(workspace),
+                             workspace.numel() if workspace is not None else 0, _stream(stream))
+    _check(_fn, rc)
+
+
+def debug_stalled_ffn_layer(projs, gate: int, up: int, down: int, inputs, M: int, workspace, stream=None):
+    """Test hook: layer_mixed_ffn's fused form with h never counted ready."""
+    layer_mixed_ffn(projs, gate, up, down, inputs, M, workspace, stream, _fn="xq_debug_stalled_ffn_layer")
 
 
 def layer_mixed_static(projs, inputs, M: int, stream=None):

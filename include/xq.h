@@ -312,7 +312,8 @@ XQ_API xq_status xq_layer_mixed_static(const xq_proj *proj, int n_proj,
 
 /* Failure detection. Every mbarrier wait of the TMA / tensor-core kernels is
  * bounded (about 2^32 clocks). A wait that runs out records an error code in
- * a device word; the kernel then leaves its loops, waits for its own copies
+ * a device word (the first such wait of a kernel's launches since the last
+ * read is the one kept); the kernel then leaves its loops, waits for its own copies
  * and tensor-core work, frees tensor memory and exits, leaving some outputs
  * unwritten although the call that launched it already returned XQ_OK.
  * xq_device_error waits until `stream` is idle, then reads and clears those
@@ -339,6 +340,18 @@ XQ_API xq_status xq_device_error(xq_stream stream, unsigned int *code_out);
  * reports kernel 1, wait 2. Arguments and errors as xq_matmul_q4k_q8. */
 XQ_API xq_status xq_debug_stalled_matmul_q4k(const void *W, const void *xq, int M, int N, int K, float *y,
                                              xq_stream stream);
+
+/* Test hook for wait 3 above: xq_layer_mixed_ffn's fused form (gate and up
+ * warps write h's Q8 themselves) with h written but its super-blocks never
+ * counted ready. Down's producers wait about 10^5 clocks for each, record
+ * kernel 1, wait 3 and leave; down's stage waits are given four times that,
+ * so wait 3 is the record xq_device_error reads. Down's y is left unwritten,
+ * the other projections are computed as usual. Arguments, workspace and
+ * errors as xq_layer_mixed_ffn, plus XQ_ERR_UNSUPPORTED (nothing launched)
+ * when the call would not take the fused form. */
+XQ_API xq_status xq_debug_stalled_ffn_layer(const xq_proj *proj, int n_proj, int gate, int up, int down,
+                                            const float *const *inputs, int n_inputs, int M, void *workspace,
+                                            size_t ws_bytes, xq_stream stream);
 
 /* Test hook of checked builds: the Q4_K GEMV (2 <= M <= 8, y [M][N] fully
  * allocated) launched with its y extent declared one token row short, so

@@ -175,6 +175,11 @@ def test_ffn_entry_points_reject_before_launch(L):
     ins = (ctypes.c_void_p * 1)(FAKE)
     assert L.xq_layer_mixed_ffn(bad, 3, 0, 1, 2, ins, 1, 4, P(FAKE), 1 << 20, None) == 2
     assert L.xq_layer_mixed_ffn(arr, 3, 0, 1, 2, ins, 1, 4, P(FAKE), good - 1, None) == 4
+    # the wait-3 hook: the same checks; the unfused form (M > 8) is not hooked
+    stalled = L.xq_debug_stalled_ffn_layer
+    assert stalled(bad, 3, 0, 1, 2, ins, 1, 4, P(FAKE), 1 << 20, None) == 2
+    assert stalled(arr, 3, 0, 1, 2, ins, 1, 4, P(FAKE), good - 1, None) == 4
+    assert stalled(arr, 3, 0, 1, 2, ins, 1, 20, P(FAKE), 1 << 30, None) == 6
     assert L.xq_silu_mul_quantize_q8(P(FAKE), P(FAKE), 2, 300, P(FAKE), None, None) == 2
     assert L.xq_silu_mul_quantize_q8(P(FAKE + 4), P(FAKE), 2, 256, P(FAKE), None, None) == 3
     assert L.xq_silu_mul_quantize_q8(None, P(FAKE), 2, 256, P(FAKE), None, None) == 1
