@@ -205,6 +205,17 @@ __device__ __forceinline__ float byte_plus_2p23(unsigned w, int k) {
   return __uint_as_float(prmt(w, 0x4B000000u, 0x7540u | static_cast<unsigned>(k)));
 }
 
+// Arrival count increment of a split hand-off: an acquire-release atomic,
+// executed by lane 0 after a warp barrier. As a release it publishes the
+// stores every lane made before the barrier; as an acquire it makes the
+// stores published by earlier arrivals visible to this warp, so the warp
+// that arrives last can read every chunk's partial sums with no other fence.
+__device__ __forceinline__ unsigned arrive_acq_rel(unsigned int* count) {
+  unsigned old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(old) : "l"(count) : "memory");
+  return old;
+}
+
 // ---------------------------------------------------------------- tasks
 struct TaskPos {
   int p, rb, b0, b1, c;
@@ -626,22 +637,18 @@ __device__ __forceinline__ void reduce_chunks(const Proj& P, int rg, int n8, int
 // A consumer warp has written the final y of 16-row group rg of gate or up.
 // The warp that completes a 32-row block (the fourth of the two gate and two
 // up warps to arrive) computes that block of h for every token and writes
-// its Q8 bytes and operand image, then counts the block ready. Writers publish
-// with a fence before their relaxed increment (as the split hand-off does);
-// the fourth warp fences again before it reads the others' y. The proxy fence
-// makes the generic-proxy writes of h visible to the bulk copies (async
-// proxy) that read them.
+// its Q8 bytes and operand image, then counts the block ready. The arrival
+// is an acquire-release increment (arrive_acq_rel, as in the split hand-off),
+// so the fourth warp reads the others' y with no further fence. The proxy
+// fence makes the generic-proxy writes of h visible to the bulk copies
+// (async proxy) that read them.
 __device__ __noinline__ void ffn_arrive(const Group& G, int rg, int lane) {
   const Ffn& F = G.ffn;
   __syncwarp();
   unsigned old = 0;
-  if (lane == 0) {
-    __threadfence();
-    old = atomicAdd(F.arrive + (rg >> 1), 1u);
-  }
+  if (lane == 0) old = arrive_acq_rel(F.arrive + (rg >> 1));
   old = __shfl_sync(0xffffffffu, old, 0);
   if (old != 3u) return;
-  __threadfence();
   // All tokens at once: lane l takes token n = l/4 and elements 8g..8g+7,
   // g = l%4, of the block. The steps are those of q8_quantize_lane and
   // swiglu (the same fp32 operations, the block max and quant sum taken over
@@ -1053,8 +1060,7 @@ __device__ __forceinline__ void small_consumer(const Group& G, const uint8_t* ri
     const Proj& Q = G.p[pend_p];
     const unsigned old = __shfl_sync(0xffffffffu, pend_old, 0);
     if (old == static_cast<unsigned>(Q.nch - 1)) {
-      __threadfence();
-      __syncwarp();
+      __syncwarp();  // lane 0's acquiring increment, a stage ago, covers the partials
       if (lane == 0) Q.arrive[pend_rg] = 0u;
       reduce_chunks_small(Q, pend_rg, r, h);
       if (FFN && (pend_p == G.ffn.gate || pend_p == G.ffn.up)) ffn_arrive(G, pend_rg, lane);
@@ -1116,10 +1122,8 @@ __device__ __forceinline__ void small_consumer(const Group& G, const uint8_t* ri
                       kChkGemvPartial))
               part[static_cast<size_t>(t) * rows_pad + row] = v[t];
         __syncwarp();
-        if (lane == 0) {
-          __threadfence();
-          if (XQ_IN(rg, gemv_row_blocks(P.N) * kGemvWarps, kChkGemvArrive)) pend_old = atomicAdd(P.arrive + rg, 1u);
-        }
+        if (lane == 0 && XQ_IN(rg, gemv_row_blocks(P.N) * kGemvWarps, kChkGemvArrive))
+          pend_old = arrive_acq_rel(P.arrive + rg);
         pend_p = tp.p;
         pend_rg = rg;
       }
@@ -1273,8 +1277,7 @@ __device__ __forceinline__ void gemv_mma_body(const Group& G) {
     const Proj& Q = G.p[pend_p];
     const unsigned old = __shfl_sync(0xffffffffu, pend_old, 0);
     if (old == static_cast<unsigned>(Q.nch - 1)) {  // every chunk has arrived
-      __threadfence();
-      __syncwarp();
+      __syncwarp();  // lane 0's acquiring increment, a stage ago, covers the partials
       if (lane == 0) Q.arrive[pend_rg] = 0u;  // ready for the next launch
       reduce_chunks(Q, pend_rg, n8, t);
       if (FFN && (pend_p == G.ffn.gate || pend_p == G.ffn.up)) ffn_arrive(G, pend_rg, lane);
@@ -1343,9 +1346,8 @@ __device__ __forceinline__ void gemv_mma_body(const Group& G) {
         }
       } else if (rows_ok) {
         // K-chunk partial of a split task; the last warp to finish the row
-        // group adds the chunks in chunk order. Lane 0's fence, after the
-        // warp barrier, publishes the warp's stores ahead of its relaxed
-        // increment; the last warp fences again before its reads.
+        // group adds the chunks in chunk order (arrive_acq_rel orders the
+        // stores and the reads).
         const int rows_pad = gemv_row_blocks(P.N) * kGemvRows;
         float* part = P.partial + static_cast<size_t>(tp.c) * 8 * rows_pad;
         const int r0 = rg * 16 + mma_row(n8), r1 = r0 + 8, c0 = 2 * t, c1 = c0 + 1;
@@ -1357,10 +1359,8 @@ __device__ __forceinline__ void gemv_mma_body(const Group& G) {
           part[static_cast<size_t>(c1) * rows_pad + r1] = hi32(acc[1]);
         }
         __syncwarp();
-        if (lane == 0) {
-          __threadfence();
-          if (XQ_IN(rg, gemv_row_blocks(P.N) * kGemvWarps, kChkGemvArrive)) pend_old = atomicAdd(P.arrive + rg, 1u);
-        }
+        if (lane == 0 && XQ_IN(rg, gemv_row_blocks(P.N) * kGemvWarps, kChkGemvArrive))
+          pend_old = arrive_acq_rel(P.arrive + rg);
         pend_p = tp.p;
         pend_rg = rg;
       }
