@@ -148,6 +148,7 @@ struct Sched {
   bool dynamic[kTypes];  // the type's grouped GEMV fits one launch: counter and K-split
   size_t arrive[kTypes], partial[kTypes];
   int nch[64];           // K-chunks per projection (1: not split)
+  int tsplit[64];        // M > 64: K ranges per tile of each projection's tile launch (1: not split)
 };
 
 // Projections that go to the grouped tensor-core GEMV at M <= 8.
@@ -178,8 +179,21 @@ Sched sched_layout(const xq_proj* proj, int n_proj, int M) {
     // 8 < M <= 64: every (projection, 8-token chunk) pair of a long row is
     // split over K with its own arrival counts and partial sums (the pairs
     // are spread over several launches that may run at once); no counters.
-    for (int p = 0; p < n_proj && p < 64; ++p) sc.nch[p] = 1;
-    if (M > xq::kGemvMaxTokens) return sc;
+    for (int p = 0; p < n_proj && p < 64; ++p) sc.nch[p] = sc.tsplit[p] = 1;
+    if (M > xq::kGemvMaxTokens) {
+      // tile launches: K-split where a projection's tiles leave SMs idle,
+      // with one arrival count per tile and the partial sums of every range
+      for (int p = 0; p < n_proj && p < 64; ++p) {
+        const xq_proj& q = proj[p];
+        if (q.N <= 0) continue;
+        sc.tsplit[p] = xq::tile_split_count(q.N, q.K, M);
+        if (sc.tsplit[p] <= 1) continue;
+        const int g = type_index(q.type);
+        sc.arrive[g] += xq::tile_split_arrive_bytes(q.N, M);
+        sc.partial[g] += xq::tile_split_partial_bytes(q.N, M, sc.tsplit[p]);
+      }
+      return sc;
+    }
     const int chunks = (M + 7) / 8;
     for (int p = 0; p < n_proj && p < 64; ++p) {
       const xq_proj& q = proj[p];
@@ -278,6 +292,7 @@ xq_status layer_matmuls(const xq_proj* proj, int n_proj, const uint8_t* const* q
     const int chunks = (M + 7) / 8;
     // split workspaces: per type, the arrival counts (zeroed by the quantize
     // launch), then the partial sums, consumed launch by launch in item order
+    // (8 < M <= 64: GEMV chunks; M > 64: tile K ranges)
     uint8_t* arr_cur[kTypes];
     uint8_t* part_cur[kTypes];
     {
@@ -333,9 +348,41 @@ xq_status layer_matmuls(const xq_proj* proj, int n_proj, const uint8_t* const* q
       }
       if (n > 0 && !launch()) return XQ_ERR_CUDA;
     }
+    if (!chunked) {
+      // M > 64: one tile launch per projection, in order, K-split where its
+      // tiles would leave SMs idle. Only the first launch waits for the
+      // previous grid (the quantizer) on entry: the later ones read nothing
+      // an earlier one writes and start as its CTAs drain, and wait for it
+      // before their threads exit, which keeps the stream's order.
+      bool first = true;
+      for (int p = 0; p < n_proj; ++p) {
+        const xq_proj& q = proj[p];
+        if (q.N == 0) continue;
+        uint32_t cb[4];
+        const uint32_t* cbp = nullptr;
+        if (q.type == XQ_TYPE_IQ4_XS) {
+          pack_codebook(q.codebook, cb);
+          cbp = cb;
+        }
+        const int g = type_index(q.type);
+        xq::TileSplit ts;
+        ts.splits = sc.tsplit[p];
+        ts.partial = reinterpret_cast<float*>(part_cur[g]);
+        ts.arrive = reinterpret_cast<unsigned int*>(arr_cur[g]);
+        if (xq::launch_tile_mma(q.type, static_cast<const uint8_t*>(q.W), q8[p], M, q.N, q.K, q.y, s, true, cbp,
+                                nullptr, ts.splits > 1 ? &ts : nullptr, first) != cudaSuccess)
+          return XQ_ERR_CUDA;
+        if (ts.splits > 1) {
+          arr_cur[g] += xq::tile_split_arrive_bytes(q.N, M);
+          part_cur[g] += xq::tile_split_partial_bytes(q.N, M, ts.splits);
+        }
+        first = false;
+      }
+      return XQ_OK;
+    }
     for (int p = 0; p < n_proj; ++p) {
       const xq_proj& q = proj[p];
-      if (q.N == 0 || (chunked && xq::gemv_mma_supports(q.type, q.N, q.K))) continue;
+      if (q.N == 0 || xq::gemv_mma_supports(q.type, q.N, q.K)) continue;
       const xq_status st = run_one(q, q8[p], M, s);
       if (st != XQ_OK) return st;
     }

@@ -161,6 +161,18 @@ struct TileArgs {
   int q6_tma;                  // Q6_K rows of 16-byte multiples: map {row_bytes, N} of u8, box {240, 128}
   int N, K, M, nsb, row_bytes, ttiles;
   uint32_t cb[4];              // IQ4_XS: codebook bytes with their sign bits flipped
+  // K-split (layer calls that would leave SMs idle): each tile's super-blocks
+  // in `splits` ranges, one CTA each; a CTA stores its sums in partial
+  // [splits][M][N] and the last CTA of the tile to arrive (count in
+  // arrive[tile], zero before the launch and left zero) adds the ranges in
+  // order into y. splits = 1: y directly.
+  int splits;
+  float* partial;
+  unsigned int* arrive;
+  // 0: the launch reads nothing the previous grid on the stream writes (a
+  // later launch of the same layer): it waits for that grid only before its
+  // threads exit, so that its completion still implies the earlier ones.
+  int wait_prev;
 };
 
 // Waits of the producer, unpack and epilogue warps suspend between polls;
@@ -248,8 +260,13 @@ __global__ void __launch_bounds__(Roles<TYPE>::kThreads, 1) tile_mma_kernel(cons
   int* split_vote = split_flag + kWStages;                  // [2][4 unpack warps]
   const uint32_t bar0 = smem_addr(bars);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int tt = blockIdx.x % A.ttiles, wt = blockIdx.x / A.ttiles;
-  const int nitems = A.nsb * kItems;
+  // CTA = (weight tile, K range, token tile), token tile fastest so that the
+  // CTAs of one weight tile run side by side
+  const int tt = blockIdx.x % A.ttiles, wks = blockIdx.x / A.ttiles;
+  const int ks = wks % A.splits, wt = wks / A.splits;
+  const int kb0 = A.nsb * ks / A.splits;           // first super-block of this CTA
+  const int nb = A.nsb * (ks + 1) / A.splits - kb0;  // super-blocks of this CTA
+  const int nitems = nb * kItems;
 #define BAR(i) (bar0 + 8u * static_cast<uint32_t>(i))
 
   if (threadIdx.x == 0) {
@@ -282,8 +299,9 @@ __global__ void __launch_bounds__(Roles<TYPE>::kThreads, 1) tile_mma_kernel(cons
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  // The tile image is written by the previous kernel on the stream.
-  cudaGridDependencySynchronize();
+  // The tile image is written by the previous kernel on the stream (or, for
+  // a later launch of a layer, before the first launch's wait).
+  if (A.wait_prev) cudaGridDependencySynchronize();
   cudaTriggerProgrammaticLaunchCompletion();
 
   // Register split (setmaxnreg): warpgroup 3 (producer and MMA issuers,
@@ -299,14 +317,15 @@ __global__ void __launch_bounds__(Roles<TYPE>::kThreads, 1) tile_mma_kernel(cons
       const int rows = min(kRows, A.N - row0);
       unsigned tf = 0;  // token items issued
       bool ok = true;
-      for (int b = 0; b < A.nsb && ok; ++b) {
+      for (int b = 0; b < nb && ok; ++b) {
+        const int gb = kb0 + b;  // super-block in the row
         const int rs = b % RS;
         if (b >= RS && !warp_wait(BAR(B::kRawEmpty + rs), ((b / RS) - 1) & 1, 1)) break;
         const uint32_t dst = smem_addr(raw_ring + rs * kRawBytes);
         if (TYPE == 12 || TYPE == 23 || TYPE == 8) {
           if (lane == 0) {
             mbar_expect_tx(BAR(B::kRawFull + rs), kRawBytes);  // rows past N arrive zero-filled
-            const int x = TYPE == 12 ? b * (kQ4kBytes / 8) : (TYPE == 8 ? b * (kQ80Group / 8) : (kIq4xsBytes * b) & ~15);
+            const int x = TYPE == 12 ? gb * (kQ4kBytes / 8) : (TYPE == 8 ? gb * (kQ80Group / 8) : (kIq4xsBytes * gb) & ~15);
             // x in map elements: 8 bytes for Q4_K and Q8_0, 1 byte for IQ4_XS
             if (XQ_CHECKED((((TYPE == 23) ? x : 8 * x) & 15) == 0 && x >= 0, kChkTileBox))
               tma_load_2d(dst, &A.map, x, row0, BAR(B::kRawFull + rs));
@@ -318,19 +337,19 @@ __global__ void __launch_bounds__(Roles<TYPE>::kThreads, 1) tile_mma_kernel(cons
           // zero-filled
           if (lane == 0) {
             mbar_expect_tx(BAR(B::kRawFull + rs), kRawBytes);
-            const int x = (kQ6kBytes * b) & ~15;
+            const int x = (kQ6kBytes * gb) & ~15;
             if (XQ_CHECKED((x & 15) == 0 && x >= 0, kChkTileBox))
               tma_load_2d(dst, &A.map, x, row0, BAR(B::kRawFull + rs));
           }
         } else {
           unsigned mine = 0;
-          for (int r = lane; r < rows; r += 32) mine += q6_window(A, row0 + r, b);
+          for (int r = lane; r < rows; r += 32) mine += q6_window(A, row0 + r, gb);
           const unsigned total = __reduce_add_sync(0xffffffffu, mine);
           if (lane == 0) mbar_expect_tx(BAR(B::kRawFull + rs), total);
           __syncwarp();
           for (int r = lane; r < rows; r += 32) {
-            const unsigned long long start = static_cast<unsigned long long>(row0 + r) * A.row_bytes + 210ull * b;
-            const unsigned win = q6_window(A, row0 + r, b);
+            const unsigned long long start = static_cast<unsigned long long>(row0 + r) * A.row_bytes + 210ull * gb;
+            const unsigned win = q6_window(A, row0 + r, gb);
             if (XQ_CHECKED((start & ~15ull) + win <= A.w_bytes && (win & 15) == 0 &&
                                ((reinterpret_cast<uintptr_t>(A.W) + (start & ~15ull)) & 15) == 0,
                            kChkTileQ6Window))
@@ -346,10 +365,10 @@ __global__ void __launch_bounds__(Roles<TYPE>::kThreads, 1) tile_mma_kernel(cons
           if (lane == 0) {
             const unsigned bytes = it < 8 ? kTileItem : kTileItemOp;
             mbar_expect_tx(BAR(B::kTokFull + ts), bytes);
-            const size_t off = (static_cast<size_t>(tt) * A.nsb + b) * kTileRecord + static_cast<size_t>(it) * kTileItem;
+            const size_t off = (static_cast<size_t>(tt) * A.nsb + gb) * kTileRecord + static_cast<size_t>(it) * kTileItem;
             if (XQ_CHECKED(off + bytes <= A.img_bytes && ((reinterpret_cast<uintptr_t>(A.img) + off) & 15) == 0,
                            kChkTileItem))
-              bulk_load(smem_addr(tok_ring + ts * kTileItem), rec + static_cast<size_t>(b) * kTileRecord + it * kTileItem,
+              bulk_load(smem_addr(tok_ring + ts * kTileItem), rec + static_cast<size_t>(gb) * kTileRecord + it * kTileItem,
                         bytes, BAR(B::kTokFull + ts));
           }
         }
@@ -357,7 +376,6 @@ __global__ void __launch_bounds__(Roles<TYPE>::kThreads, 1) tile_mma_kernel(cons
       // No copy may still be landing when the CTA exits: wait for the last
       // fill of every stage (already complete on the normal path).
       if (lane == 0) {
-        const int nb = A.nsb;
         for (int b = nb > RS ? nb - RS : 0; b < nb; ++b) wait_bar(BAR(B::kRawFull + b % RS), (b / RS) & 1, 11);
         for (unsigned f = tf > kTokStages ? tf - kTokStages : 0; f < tf; ++f)
           wait_bar(BAR(B::kTokFull + f % kTokStages), (f / kTokStages) & 1, 12);
@@ -408,7 +426,8 @@ __global__ void __launch_bounds__(Roles<TYPE>::kThreads, 1) tile_mma_kernel(cons
     const bool row_ok = n < A.N;
     unsigned wf = 0;  // weight operands filled
     bool ok = true;
-    for (int b = 0; b < A.nsb && ok; ++b) {
+    for (int b = 0; b < nb && ok; ++b) {
+      const int gb = kb0 + b;  // super-block in the row
       const int rs = b % RS, cs = b % kCoefStages;
       if (!warp_wait(BAR(B::kRawFull + rs), (b / RS) & 1, 3)) break;
       if (b >= kCoefStages && !warp_wait(BAR(B::kCoefEmpty + cs), ((b / kCoefStages) - 1) & 1, 4)) break;
@@ -510,7 +529,7 @@ __global__ void __launch_bounds__(Roles<TYPE>::kThreads, 1) tile_mma_kernel(cons
         // [-32, 31]; |value * s| reaches 4096, so as for Q6_K the operand is
         // split into 2*(s>>1)*value (even, exact) and (s&1)*value when some
         // row of the tile has |s| > 16, and the tile then reads both.
-        const uint8_t* sb = raw + ((kIq4xsBytes * b) & 15);
+        const uint8_t* sb = raw + ((kIq4xsBytes * gb) & 15);
         const uint2 h = *reinterpret_cast<const uint2*>(sb);  // d | scales_h, scales_l (zero past N)
         coef_ring[cs * kRows + r] = make_float2(half_bits_to_float(h.x), 0.0f);
         __syncwarp();
@@ -572,7 +591,7 @@ __global__ void __launch_bounds__(Roles<TYPE>::kThreads, 1) tile_mma_kernel(cons
         // Q6_K: ql[128] at 0, qh[64] at 128, scales int8[16] at 192, d at
         // 208. The row's window starts `off` (even, 0..14) bytes before the
         // super-block.
-        const unsigned long long start = static_cast<unsigned long long>(n) * A.row_bytes + 210ull * b;
+        const unsigned long long start = static_cast<unsigned long long>(n) * A.row_bytes + 210ull * gb;
         const uint8_t* sb = raw + (start & 15);
         const bool cut = (start & ~15ull) + kQ6Window > A.w_bytes;  // scales and d not all in the window
         uint32_t sw[4] = {0u, 0u, 0u, 0u};
@@ -674,7 +693,8 @@ __global__ void __launch_bounds__(Roles<TYPE>::kThreads, 1) tile_mma_kernel(cons
     for (int i = 0; i < kCols / 2; ++i) acc[i] = 0ull;
     bool ok = true;
     int f = 0;
-    for (int b = 0; b < A.nsb && ok; ++b) {
+    for (int b = 0; b < nb && ok; ++b) {
+      const int gb = kb0 + b;  // super-block in the row
       for (int it = 0; it < kItems; ++it, ++f) {
         const int d = f % kNumD, ts = f % kTokStages;
         if (!warp_wait(BAR(B::kDFull + d), (f / kNumD) & 1, 10) ||
@@ -711,8 +731,8 @@ __global__ void __launch_bounds__(Roles<TYPE>::kThreads, 1) tile_mma_kernel(cons
               for (int e = 0; e < 16; ++e) {
                 const int n1 = n0 + 16 * c + e, n2 = n1 + 16;
                 const size_t ns = static_cast<size_t>(A.M) * A.N * nsub;
-                const size_t i1 = (static_cast<size_t>(m) * A.N + n1) * nsub + 8 * b + it;
-                const size_t i2 = (static_cast<size_t>(m) * A.N + n2) * nsub + 8 * b + it;
+                const size_t i1 = (static_cast<size_t>(m) * A.N + n1) * nsub + 8 * gb + it;
+                const size_t i2 = (static_cast<size_t>(m) * A.N + n2) * nsub + 8 * gb + it;
                 if (n1 < A.N && XQ_IN(i1, ns, kChkTileSums)) A.sums[i1] = static_cast<int32_t>(__uint_as_float(v[e]) * sc);
                 if (n2 < A.N && XQ_IN(i2, ns, kChkTileSums)) A.sums[i2] = static_cast<int32_t>(__uint_as_float(w[e]) * sc);
               }
@@ -739,7 +759,7 @@ __global__ void __launch_bounds__(Roles<TYPE>::kThreads, 1) tile_mma_kernel(cons
             break;
           }
           const float4* cf = reinterpret_cast<const float4*>(coef_ring + cs * kRows + kCols * part);
-          const bool last = b == A.nsb - 1;
+          const bool last = b == nb - 1;
 #pragma unroll
           for (int c = 0; c < kCols / 16; ++c) {
             uint32_t run[16], dmin[16];
@@ -761,7 +781,9 @@ __global__ void __launch_bounds__(Roles<TYPE>::kThreads, 1) tile_mma_kernel(cons
             if (last) {
               if (m < A.M) {
                 const int nc = n0 + 16 * c;
-                float* yr = A.y + static_cast<size_t>(m) * A.N;
+                // y, or this K range's partial sums (same [M][N] layout)
+                float* yr = (A.splits > 1 ? A.partial + static_cast<size_t>(ks) * A.M * A.N : A.y) +
+                            static_cast<size_t>(m) * A.N;
                 if (!XQ_IN(static_cast<size_t>(m) * A.N + (nc < A.N ? nc : 0), static_cast<size_t>(A.M) * A.N,
                            kChkTileY)) {
                 } else if ((A.N & 3) == 0 && nc + 16 <= A.N) {
@@ -791,6 +813,50 @@ __global__ void __launch_bounds__(Roles<TYPE>::kThreads, 1) tile_mma_kernel(cons
         }
       }
     }
+    if (A.splits > 1) {
+      // K-split: once every epilogue thread has stored its partial sums
+      // (named barrier 1, the epilogue warps only), one thread counts the CTA
+      // in with an acquire-release increment (its release publishes the
+      // stores the barrier ordered before it; its acquire, in the last CTA,
+      // covers every other CTA's). The last CTA of the tile adds the K
+      // ranges in order into y and leaves the count at zero.
+      asm volatile("bar.sync 1, %0;" ::"n"(32 * R::kEpi) : "memory");
+      const int tile = wt * A.ttiles + tt;
+      if (threadIdx.x == 32 * R::kEpi0) {
+        unsigned old = 0;
+        if (XQ_IN(tile, (A.N + kRows - 1) / kRows * A.ttiles, kChkTileSplit))
+          asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(old) : "l"(A.arrive + tile) : "memory");
+        const bool last_cta = old == static_cast<unsigned>(A.splits - 1);
+        if (last_cta) A.arrive[tile] = 0u;
+        tmem_slot[1] = last_cta ? 1u : 0u;
+      }
+      asm volatile("bar.sync 1, %0;" ::"n"(32 * R::kEpi) : "memory");
+      if (tmem_slot[1] != 0u && m < A.M) {
+        const size_t plane = static_cast<size_t>(A.M) * A.N;
+        const size_t row = static_cast<size_t>(m) * A.N;
+        for (int c = 0; c < kCols; c += 4) {
+          const int nc = n0 + c;
+          if (nc >= A.N) break;
+          if ((A.N & 3) == 0) {
+            float4 v = __ldcg(reinterpret_cast<const float4*>(A.partial + row + nc));
+            for (int k = 1; k < A.splits; ++k) {
+              const float4 w = __ldcg(reinterpret_cast<const float4*>(A.partial + k * plane + row + nc));
+              v.x += w.x;
+              v.y += w.y;
+              v.z += w.z;
+              v.w += w.w;
+            }
+            if (XQ_IN(row + nc + 3, plane, kChkTileY)) *reinterpret_cast<float4*>(A.y + row + nc) = v;
+          } else {
+            for (int e = 0; e < 4 && nc + e < A.N; ++e) {
+              float v = __ldcg(A.partial + row + nc + e);
+              for (int k = 1; k < A.splits; ++k) v += __ldcg(A.partial + k * plane + row + nc + e);
+              if (XQ_IN(row + nc + e, plane, kChkTileY)) A.y[row + nc + e] = v;
+            }
+          }
+        }
+      }
+    }
   }
 #undef BAR
   tc_fence_before();
@@ -799,6 +865,9 @@ __global__ void __launch_bounds__(Roles<TYPE>::kThreads, 1) tile_mma_kernel(cons
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
+  // A launch that did not wait for the previous grid on entry waits before
+  // its threads exit (the next kernel's dependency wait relies on that).
+  if (!A.wait_prev) cudaGridDependencySynchronize();
 }
 
 template <int TYPE, bool SUMS>
@@ -847,9 +916,14 @@ cudaError_t take_tile_error(unsigned int* code) {
 }
 
 cudaError_t launch_tile_mma(int type, const uint8_t* W, const uint8_t* xq, int M, int N, int K, float* y,
-                            cudaStream_t s, bool pdl, const uint32_t* codebook, int32_t* sums) {
+                            cudaStream_t s, bool pdl, const uint32_t* codebook, int32_t* sums, const TileSplit* split,
+                            bool wait_prev) {
   if (M <= kGemvMaxTokens || N <= 0 || K <= 0 || (K & 255) != 0 ||
       (type != 12 && type != 14 && type != 23 && type != 8))
+    return cudaErrorInvalidValue;
+  const int splits = split ? split->splits : 1;
+  if (splits < 1 || splits > (K >> 8) || (splits > 1 && (!split->partial || !split->arrive || sums)) ||
+      (!wait_prev && !pdl))
     return cudaErrorInvalidValue;
   if (type == 23 && (!codebook || (K & 511) != 0)) return cudaErrorInvalidValue;
   const Q8Layout L = q8_layout(M, K);
@@ -867,7 +941,11 @@ cudaError_t launch_tile_mma(int type, const uint8_t* W, const uint8_t* xq, int M
   A.w_bytes = static_cast<unsigned long long>(N) * A.row_bytes;
   A.img_bytes = L.total - L.tile;
   A.ttiles = L.ttiles;
-  const int grid = ((N + kRows - 1) / kRows) * L.ttiles;
+  A.splits = splits;
+  A.partial = splits > 1 ? split->partial : nullptr;
+  A.arrive = splits > 1 ? split->arrive : nullptr;
+  A.wait_prev = wait_prev ? 1 : 0;
+  const int grid = ((N + kRows - 1) / kRows) * L.ttiles * splits;
   if (type == 12) {
     if (!encode_tma_2d(&A.map, CU_TENSOR_MAP_DATA_TYPE_UINT64, W, A.row_bytes / 8, static_cast<unsigned long long>(N),
                        A.row_bytes, kQ4kBytes / 8, kRows))

@@ -64,6 +64,7 @@ enum CheckSite : unsigned {
   kChkTileItem = 23,      // token item copy inside the tile image
   kChkTileBox = 24,       // weight box x on a 16-byte boundary
   kChkTileQ6Cut = 25,     // Q6_K scales read from global memory inside the weights
+  kChkTileSplit = 26,     // K-split arrival count inside the tile counts
   // quantize_q8.cu
   kChkQuantX = 30,     // input read inside [M][K]
   kChkQuantQ8 = 31,    // qs / d8 / s8 store inside the Q8 buffer

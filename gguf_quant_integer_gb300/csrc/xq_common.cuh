@@ -287,8 +287,38 @@ bool encode_tma_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, u
 // sums (test hook, or null): [M][N][K/32] int32, each 32-block's exact
 // integer as the kernel accumulates it (Q4_K sc_j * isum_j; Q6_K
 // s_2p * isum_2p + s_2p+1 * isum_2p+1; Q8_0 isum_j; IQ4_XS (ls_j - 32) * isum_j).
+// split (layer calls, or null): the K-split of tile_split_count, with
+// partial [splits][M][N] fp32 and one arrival count per 128 x 128 tile,
+// zeroed before the launch (the kernel leaves them zero). wait_prev false:
+// a later launch of a layer, which reads nothing the previous grid writes
+// and waits for it only before exiting (needs pdl).
+struct TileSplit {
+  int splits;
+  float* partial;
+  unsigned int* arrive;
+};
+// K ranges per tile for a layer's tile launch: 1 when the launch's 128 x 128
+// tiles already cover the SMs, else as many as fill them (one CTA per SM),
+// at most 8 and at most one per two super-blocks.
+inline int tile_split_count(int N, int K, int M) {
+  const long long tiles = static_cast<long long>((N + 127) / 128) * ((M + kTileTokens - 1) / kTileTokens);
+  if (tiles <= 0 || tiles >= kNumSMs) return 1;
+  long long s = kNumSMs / tiles;
+  const int nsb = K >> 8;
+  if (s > nsb / 2) s = nsb / 2;
+  if (s > 8) s = 8;
+  return s < 1 ? 1 : static_cast<int>(s);
+}
+inline size_t tile_split_arrive_bytes(int N, int M) {
+  return ((static_cast<size_t>((N + 127) / 128) * ((M + kTileTokens - 1) / kTileTokens) * 4) + 255) &
+         ~static_cast<size_t>(255);
+}
+inline size_t tile_split_partial_bytes(int N, int M, int splits) {
+  return ((static_cast<size_t>(splits) * M * N * 4) + 255) & ~static_cast<size_t>(255);
+}
 cudaError_t launch_tile_mma(int type, const uint8_t* W, const uint8_t* xq, int M, int N, int K, float* y,
-                            cudaStream_t s, bool pdl, const uint32_t* codebook = nullptr, int32_t* sums = nullptr);
+                            cudaStream_t s, bool pdl, const uint32_t* codebook = nullptr, int32_t* sums = nullptr,
+                            const TileSplit* split = nullptr, bool wait_prev = true);
 cudaError_t launch_gemv_q6k(const GemvArgs& a, cudaStream_t s);
 
 }  // namespace xq

@@ -216,8 +216,10 @@ typedef struct {
  * IQ4_XS) and, for
  * each projection with more than 24 super-blocks per row that the grouped
  * tensor-core GEMV splits over K across CTAs (M <= 64; above 8 tokens once
- * per 8-token chunk), its arrival counts and partial sums. 0 on bad
- * arguments. */
+ * per 8-token chunk), its arrival counts and partial sums; above 64 tokens,
+ * for each projection whose 128 x 128 tiles number fewer than the SMs and
+ * whose tile launch is therefore split over K, one arrival count per tile
+ * and the [ranges][M][N] fp32 partial sums. 0 on bad arguments. */
 XQ_API size_t xq_layer_workspace_bytes(const xq_proj *proj, int n_proj, int n_inputs, int M);
 
 /* One layer's projections with a quant type per tensor (xLLM v0.7 article,
@@ -231,7 +233,11 @@ XQ_API size_t xq_layer_workspace_bytes(const xq_proj *proj, int n_proj, int n_in
  * Enqueues one quantization per used input and the projections, in order,
  * on `stream`: at M <= 8 one grouped GEMV launch per weight type; at
  * 8 < M <= 64 grouped GEMV launches over (projection, 8-token chunk) pairs,
- * 8 per launch; above 64 tokens the tile kernel per projection. */
+ * 8 per launch; above 64 tokens the tile kernel per projection, split over
+ * K (ranges added in order by the last CTA of each tile: deterministic)
+ * where its tiles number fewer than the SMs; only the first of these tile
+ * launches waits for the quantizer, the later ones start as the earlier
+ * ones drain. */
 XQ_API xq_status xq_layer_mixed(const xq_proj *proj, int n_proj,
                          const float *const *inputs, int n_inputs, int M,
                          void *workspace, size_t ws_bytes, xq_stream stream);
@@ -325,7 +331,7 @@ XQ_API xq_status xq_layer_mixed_static(const xq_proj *proj, int n_proj,
  * feed of xq_layer_mixed_ffn). Checked builds (the library compiled with
  * -DXQ_CHECK) also test the index, range or 16-byte alignment of each global
  * access whose address comes from nontrivial arithmetic, skip an access that
- * fails and record the site: kernel 9, wait = site (10-16 the GEMV, 20-25
+ * fails and record the site: kernel 9, wait = site (10-16 the GEMV, 20-26
  * the tile kernel, 30-32 the quantizer, 40-43 the dp4a Q6_K GEMV), reported
  * after any wait code. If several kernels recorded one,
  * the lowest kernel number is reported and all are cleared. The reads and

@@ -229,9 +229,20 @@ def test_layer_workspace_for_chunked_split(L):
         q8 = r256(xq.q8_bytes(M, 4096)) + r256(xq.q8_bytes(M, 14336))
         want = q8 + 4 * 256 + chunks * split_bytes(130, 4)
         assert L.xq_layer_workspace_bytes(arr, 2, 2, M) == want, M
-    # above 64 tokens (the tile kernel) there is no split state
-    q8 = r256(xq.q8_bytes(80, 4096)) + r256(xq.q8_bytes(80, 14336))
-    assert L.xq_layer_workspace_bytes(arr, 2, 2, 80) == q8 + 4 * 256
+    # above 64 tokens (the tile kernel): where a projection's 128 x 128 tiles
+    # leave the 152 SMs idle, K ranges per tile (at most 8, at most one per
+    # two super-blocks), with an arrival count per tile and [ranges][M][N]
+    # partial sums
+    def tile_split_bytes(N, K, M):
+        tiles = -(-N // 128) * -(-M // 128)
+        splits = 1 if tiles >= 152 else max(1, min(152 // tiles, (K // 256) // 2, 8))
+        return 0 if splits == 1 else r256(tiles * 4) + r256(splits * M * N * 4)
+    for M in (80, 200, 512):
+        q8 = r256(xq.q8_bytes(M, 4096)) + r256(xq.q8_bytes(M, 14336))
+        want = q8 + 4 * 256 + tile_split_bytes(300, 4096, M) + tile_split_bytes(130, 14336, M)
+        assert L.xq_layer_workspace_bytes(arr, 2, 2, M) == want, M
+    # 80 tokens: 8 ranges for both projections (3 and 2 tiles)
+    assert tile_split_bytes(300, 4096, 80) == 256 + 8 * 80 * 300 * 4
 
 
 def test_failure_detection_entry_points_reject_before_launch(L):

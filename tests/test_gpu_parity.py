@@ -406,6 +406,33 @@ def test_q8_0_extreme_bytes(xq):
     check_matmul(xq, synth.Q8_0, W.reshape(N, -1), x)
 
 
+@pytest.mark.parametrize("M", [100, 128, 200, 300])
+def test_tile_layer_k_split(xq, M):
+    """M > 64 inside a layer: projections whose 128 x 128 tiles leave SMs
+    idle are split into K ranges whose partial sums the last CTA of each tile
+    adds in range order (ragged N, N not a multiple of 4, Q4_K and Q6_K), and
+    later tile launches of the layer start without waiting for the earlier
+    ones. Every row against the oracle; two calls give the same bits."""
+    assert layer_check(xq, RAGGED_SPLIT, M) > 0
+    wl = RAGGED_SPLIT
+    weights = synth.gen_layer_weights(wl, 0)
+    inputs = [dev(x) for x in synth.gen_layer_inputs(wl, M, 0)]
+    L = xq.Layer(wl.projs, weights, M)
+    L.forward(inputs)
+    first = [y.clone() for y in L.y]
+    L.forward(inputs)
+    torch.cuda.synchronize()
+    assert xq.device_error() == 0
+    for a, b in zip(first, L.y):
+        assert torch.equal(a, b)
+
+
+def test_qwen3_mixed_layer_tiles_128(xq):
+    # the mixed layer at 128 tokens: q/k/v/o and down split over K, gate and
+    # up (96 tiles) not; sampled rows of every projection
+    assert layer_check(xq, synth.WORKLOADS["qwen3-8b-mixed-layer"], 128, rows=96) > 0
+
+
 def test_qwen3_mixed_layer_tiles(xq):
     # M > 64: every row of every projection of the mixed layer (Q4_K and
     # Q6_K) on the tile kernel
