@@ -148,32 +148,46 @@ quantize_q8_kernel(const __grid_constant__ QuantGroup G) {
 }
 
 // The same quantization for inputs whose Q8 buffer holds the tile image
-// (M > 64 tokens): one warp per (token, 256-feature super-block), lane l
-// taking feature l of each of its eight 32-blocks, so that eight 128-byte
-// loads are in flight per warp and each block's max and quant sum come from
-// warp reductions. Every element goes through the steps of q8_quantize_lane
-// (the max and the integer sum do not depend on their order), so the bytes
-// equal quantize_q8_kernel's. Padding tokens of the last 128-token tile get
-// zeros in the image, as there.
+// (M > 64 tokens): one warp per 8 tokens x one 256-feature super-block.
+// Lane l takes token 8u + l/4 and features 8g..8g+7 (g = l%4) of each of the
+// eight 32-blocks, so each lane keeps its 16 16-byte loads in flight and
+// stores whole 16-byte chunks: 8 fp16 quants of the tile operand (k-slots
+// 8g..8g+7 of its token, in operand slot order), 8 int8 quants of qs, and 8
+// bf16 pieces of the min-term operand. Every element goes through the steps
+// of q8_quantize_lane, the block max and quant sum taken over the token's 4
+// lanes (neither depends on its order), so the bytes equal
+// quantize_q8_kernel's. Padding tokens of the last 128-token tile get zeros
+// in the image, as there.
 __global__ void __launch_bounds__(256)
 quantize_q8_tile_kernel(const __grid_constant__ QuantGroup G) {
   const int lane = threadIdx.x & 31;
+  const int t = lane >> 2, g = lane & 3;
   const unsigned warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const unsigned nwarps = (gridDim.x * blockDim.x) >> 5;
-  const unsigned total = G.blk0[G.n] >> 3;  // super-block units (blk0 counts padded 32-blocks)
+  // units: (8-token group, super-block) of every job; blk0 counts padded
+  // 32-blocks, 64 of them per unit
+  const unsigned total = G.blk0[G.n] >> 6;
   {
     int jb = 0;
     for (unsigned u = warp; u < total; u += nwarps) {
-      while (u >= (G.blk0[jb + 1] >> 3)) ++jb;
+      while (u >= (G.blk0[jb + 1] >> 6)) ++jb;
       const QuantItem& J = G.job[jb];
-      const unsigned local = u - (G.blk0[jb] >> 3);
+      const unsigned local = u - (G.blk0[jb] >> 6);
       const int nsb = J.K >> 8;
-      const int m = static_cast<int>(local / static_cast<unsigned>(nsb));
-      const int b = static_cast<int>(local - static_cast<unsigned>(m) * nsb);
-      if (m < J.M && lane < 8) {
-        const size_t idx = static_cast<size_t>(m) * J.K + 256 * b + 32 * lane;
+      const int m = 8 * static_cast<int>(local / static_cast<unsigned>(nsb)) + t;
+      const int b = static_cast<int>(local % static_cast<unsigned>(nsb));
+      if (m < J.M && g < 2) {  // the token's 1 KB of the super-block: 8 lines over its 4 lanes
+        const size_t idx = static_cast<size_t>(m) * J.K + 256 * b + 128 * g;
         asm volatile("prefetch.global.L2 [%0];" ::"l"(J.x + idx));
-        if (J.up) asm volatile("prefetch.global.L2 [%0];" ::"l"(J.up + idx));
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(J.x + idx + 32));
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(J.x + idx + 64));
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(J.x + idx + 96));
+        if (J.up) {
+          asm volatile("prefetch.global.L2 [%0];" ::"l"(J.up + idx));
+          asm volatile("prefetch.global.L2 [%0];" ::"l"(J.up + idx + 32));
+          asm volatile("prefetch.global.L2 [%0];" ::"l"(J.up + idx + 64));
+          asm volatile("prefetch.global.L2 [%0];" ::"l"(J.up + idx + 96));
+        }
       }
     }
   }
@@ -181,87 +195,120 @@ quantize_q8_tile_kernel(const __grid_constant__ QuantGroup G) {
   cudaTriggerProgrammaticLaunchCompletion();
   if (blockIdx.x == 0)
     for (int i = threadIdx.x; i < G.zero_count; i += blockDim.x) G.zero_words[i] = 0u;
-  const int ks = (lane & ~7) | gemv_image_slot(lane);  // k-slot of this lane's feature in a tile item
 
   int jb = 0;
   for (unsigned u = warp; u < total; u += nwarps) {
-    while (u >= (G.blk0[jb + 1] >> 3)) ++jb;
+    while (u >= (G.blk0[jb + 1] >> 6)) ++jb;
     const QuantItem& J = G.job[jb];
-    const unsigned local = u - (G.blk0[jb] >> 3);
+    const unsigned local = u - (G.blk0[jb] >> 6);
     const int nsb = J.K >> 8, nsub = J.nsub;
-    const int m = static_cast<int>(local / static_cast<unsigned>(nsb));
-    const int b = static_cast<int>(local - static_cast<unsigned>(m) * nsb);
+    const int m = 8 * static_cast<int>(local / static_cast<unsigned>(nsb)) + t;
+    const int b = static_cast<int>(local % static_cast<unsigned>(nsb));
     const bool live = m < J.M;
     if (!XQ_CHECKED(J.ttiles > 0 && J.tile + (static_cast<size_t>(m >> 7) + 1) * nsb * kTileRecord <= J.total &&
                         J.s8 + 4 * (static_cast<size_t>(J.M) * nsub) <= J.total,
                     kChkQuantImage))
       continue;
-    float v[8];
-    const size_t base = static_cast<size_t>(m) * J.K + 256 * b + lane;
+    // this lane's 64 features: 8 per 32-block, all loads issued first
+    const size_t base = static_cast<size_t>(m) * J.K + 256 * b + 8 * g;
+    float4 v[16];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) v[i] = live ? __ldg(J.x + base + 32 * i) : 0.0f;
+    for (int k = 0; k < 16; ++k) {
+      const size_t at = base + 32 * (k >> 1) + 4 * (k & 1);
+      v[k] = live ? __ldg(reinterpret_cast<const float4*>(J.x + at)) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    }
     if (J.up && live) {
+      // SwiGLU feed of the down projection
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        v[i] = swiglu(v[i], __ldg(J.up + base + 32 * i));
-        if (J.h_out) J.h_out[base + 32 * i] = v[i];
+      for (int k = 0; k < 16; ++k) {
+        const size_t at = base + 32 * (k >> 1) + 4 * (k & 1);
+        const float4 w = __ldg(reinterpret_cast<const float4*>(J.up + at));
+        v[k] = make_float4(swiglu(v[k].x, w.x), swiglu(v[k].y, w.y), swiglu(v[k].z, w.z), swiglu(v[k].w, w.w));
+        if (J.h_out) *reinterpret_cast<float4*>(J.h_out + at) = v[k];
       }
     }
-    float d[8], sc[8];
-    int q[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      // the steps of q8_quantize_lane, block i
-      const unsigned amax_bits = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(v[i])));
-      d[i] = __fdiv_rn(__uint_as_float(amax_bits), 127.0f);
-      const float id = (d[i] != 0.0f) ? __frcp_rn(d[i]) : 0.0f;
-      float x = roundf(__fmul_rn(v[i], id));
-      x = (x != x) ? 0.0f : x;
-      x = x > 127.0f ? 127.0f : (x < -127.0f ? -127.0f : x);
-      q[i] = static_cast<int>(x);
-      sc[i] = __fmul_rn(d[i], static_cast<float>(__reduce_add_sync(0xffffffffu, q[i])));
-    }
-    if (live) {
-#pragma unroll
-      for (int i = 0; i < 8; ++i) J.xq[base + 32 * i] = static_cast<uint8_t>(static_cast<int8_t>(q[i]));
-      if (lane < 8) {
-        float dl = d[0], sl = sc[0];
-#pragma unroll
-        for (int i = 1; i < 8; ++i)
-          if (lane == i) {
-            dl = d[i];
-            sl = sc[i];
-          }
-        reinterpret_cast<float*>(J.xq + J.d8)[static_cast<size_t>(m) * nsub + 8 * b + lane] = dl;
-        reinterpret_cast<float*>(J.xq + J.s8)[static_cast<size_t>(m) * nsub + 8 * b + lane] = sl;
-      }
-    }
-    // tile image record (tile m / 128, super-block b), token r = m % 128
-    const int r = m & 127;
+    const int r = m & 127;  // token of its 128-token tile
     uint8_t* rec = J.xq + J.tile + (static_cast<size_t>(m >> 7) * nsb + b) * kTileRecord;
+    float sblk[8];  // s8 of the token's eight 32-blocks
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
+      const float e[8] = {v[2 * i].x, v[2 * i].y, v[2 * i].z, v[2 * i].w,
+                          v[2 * i + 1].x, v[2 * i + 1].y, v[2 * i + 1].z, v[2 * i + 1].w};
+      // the steps of q8_quantize_lane over the token's 4 lanes
+      unsigned ab = 0;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) ab = max(ab, __float_as_uint(fabsf(e[k])));
+      ab = max(ab, __shfl_xor_sync(0xffffffffu, ab, 1));
+      ab = max(ab, __shfl_xor_sync(0xffffffffu, ab, 2));
+      const float d = __fdiv_rn(__uint_as_float(ab), 127.0f);
+      const float id = (d != 0.0f) ? __frcp_rn(d) : 0.0f;
+      int q[8], isum = 0;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        float x = roundf(__fmul_rn(e[k], id));
+        x = (x != x) ? 0.0f : x;
+        x = x > 127.0f ? 127.0f : (x < -127.0f ? -127.0f : x);
+        q[k] = static_cast<int>(x);
+        isum += q[k];
+      }
+      isum += __shfl_xor_sync(0xffffffffu, isum, 1);
+      isum += __shfl_xor_sync(0xffffffffu, isum, 2);
+      const float sc = __fmul_rn(d, static_cast<float>(isum));
+      sblk[i] = sc;
+      if (live) {
+        uint2 qb;
+        qb.x = (q[0] & 255) | (q[1] & 255) << 8 | (q[2] & 255) << 16 | static_cast<unsigned>(q[3] & 255) << 24;
+        qb.y = (q[4] & 255) | (q[5] & 255) << 8 | (q[6] & 255) << 16 | static_cast<unsigned>(q[7] & 255) << 24;
+        *reinterpret_cast<uint2*>(J.xq + base + 32 * i) = qb;
+        if (g == 0) {
+          reinterpret_cast<float*>(J.xq + J.d8)[static_cast<size_t>(m) * nsub + 8 * b + i] = d;
+          reinterpret_cast<float*>(J.xq + J.s8)[static_cast<size_t>(m) * nsub + 8 * b + i] = sc;
+        }
+      }
+      // tile operand of 32-block i: k-slots 8g..8g+7 of token r, slot s
+      // holding feature perm(s) of the lane's 8 (perm = 0,2,1,3,4,6,5,7)
       uint8_t* item = rec + i * kTileItem;
-      *reinterpret_cast<__half*>(item + tile_offset(r, ks)) = __int2half_rn(q[i]);
-      if (lane == i) reinterpret_cast<float*>(item + kTileItemOp)[r] = d[i];
+      const __half2 h01 = __halves2half2(__int2half_rn(q[0]), __int2half_rn(q[2]));
+      const __half2 h23 = __halves2half2(__int2half_rn(q[1]), __int2half_rn(q[3]));
+      const __half2 h45 = __halves2half2(__int2half_rn(q[4]), __int2half_rn(q[6]));
+      const __half2 h67 = __halves2half2(__int2half_rn(q[5]), __int2half_rn(q[7]));
+      uint4 w;
+      w.x = *reinterpret_cast<const unsigned*>(&h01);
+      w.y = *reinterpret_cast<const unsigned*>(&h23);
+      w.z = *reinterpret_cast<const unsigned*>(&h45);
+      w.w = *reinterpret_cast<const unsigned*>(&h67);
+      *reinterpret_cast<uint4*>(item + tile_offset(r, 8 * g)) = w;
+      if (g == 0) reinterpret_cast<float*>(item + kTileItemOp)[r] = d;
     }
     // min-term operand: slot 3i + p holds bf16 piece p of s8 of block i
-    // (s8 = p0 + p1 + p2, each the upper 16 bits of an fp32), slots 24-31 zero
-    uint16_t piece = 0;
-    if (lane < 24) {
-      const int i = lane / 3, pc = lane - 3 * i;
-      float sv = sc[0];
+    // (s8 = p0 + p1 + p2, each the upper 16 bits of an fp32), slots 24-31
+    // zero; this lane writes slots 8g..8g+7
+    uint32_t pk[4];
 #pragma unroll
-      for (int k = 1; k < 8; ++k)
-        if (i == k) sv = sc[k];
-      const float p0 = __uint_as_float(__float_as_uint(sv) & 0xFFFF0000u);
-      const float r1 = __fsub_rn(sv, p0);
-      const float p1 = __uint_as_float(__float_as_uint(r1) & 0xFFFF0000u);
-      const float p2 = __fsub_rn(r1, p1);
-      const float pv = pc == 0 ? p0 : (pc == 1 ? p1 : p2);
-      piece = static_cast<uint16_t>(__float_as_uint(pv) >> 16);
+    for (int h = 0; h < 4; ++h) {
+      uint32_t pair = 0;
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int slot = 8 * g + 2 * h + e;
+        uint32_t piece = 0;
+        if (slot < 24) {
+          const int i = slot / 3, pc = slot - 3 * i;
+          float sv = sblk[0];
+#pragma unroll
+          for (int k = 1; k < 8; ++k)
+            if (i == k) sv = sblk[k];
+          const float p0 = __uint_as_float(__float_as_uint(sv) & 0xFFFF0000u);
+          const float r1 = __fsub_rn(sv, p0);
+          const float p1 = __uint_as_float(__float_as_uint(r1) & 0xFFFF0000u);
+          const float p2 = __fsub_rn(r1, p1);
+          const float pv = pc == 0 ? p0 : (pc == 1 ? p1 : p2);
+          piece = __float_as_uint(pv) >> 16;
+        }
+        pair |= piece << (16 * e);
+      }
+      pk[h] = pair;
     }
-    *reinterpret_cast<uint16_t*>(rec + 8 * kTileItem + tile_offset(r, lane)) = piece;
+    *reinterpret_cast<uint4*>(rec + 8 * kTileItem + tile_offset(r, 8 * g)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
   }
 }
 
@@ -304,8 +351,8 @@ cudaError_t launch_quantize_q8(const QuantJob* jobs, int n, cudaStream_t s, bool
   bool tiles = true;  // every input in the tile layout: the super-block quantizer
   for (int k = 0; k < n; ++k) tiles = tiles && G.job[k].ttiles > 0;
   if (tiles) {
-    const long long units = nblocks / 8;
-    long long want = (units + 7) / 8;  // 8 warps per CTA, one super-block per warp and pass
+    const long long units = nblocks / 64;
+    long long want = (units + 7) / 8;  // 8 warps per CTA, 8 tokens x one super-block per warp and pass
     const long long cap = static_cast<long long>(kNumSMs) * 8;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(want < cap ? want : cap));
