@@ -986,7 +986,7 @@ def profile_workload(args):
         wl = synth.WORKLOADS["qwen3-8b-ffn-prefill512"]
         p = wl.projs[0 if name.endswith("up") else 1]
         t = wl.projs.index(p)
-        M = 512
+        M = args.m if args.m > 64 else 512  # the workload's 512 tokens unless --m gives a tile-sized count
         W = torch.from_numpy(synth.gen_layer_weights(wl, 0)[t].reshape(-1)).to(device)
         x = torch.from_numpy(synth.gen_layer_inputs(wl, M, 0)[p.input]).to(device)
         buf = xq.quantize_q8(x)
