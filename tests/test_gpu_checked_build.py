@@ -69,9 +69,10 @@ def test_checked_iq4xs(xq, M):
     no_check_failed(xq)
 
 
-@pytest.mark.parametrize("M", [1, 8, 40, 80])
+@pytest.mark.parametrize("M", [1, 8, 40, 80, 200])
 def test_checked_layers(xq, M):
-    # split-K hand-offs, mixed weight types and the grouped Q6_K view
+    # split-K hand-offs, mixed weight types and the grouped Q6_K view; above
+    # 64 tokens the tile launches' K ranges (two token tiles at 200)
     assert par.layer_check(xq, par.RAGGED_SPLIT, M) > 0
     assert par.layer_check(xq, synth.WORKLOADS["qwen2.5-1.5b-q4km-layer"], M, rows=128) > 0
     no_check_failed(xq)
