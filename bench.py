@@ -457,6 +457,30 @@ def per_layer_gemv_times(sweep, M, reps=3):
     return [t / reps for t in tot]
 
 
+def gemv_back_to_back_time(sweep, M, steps, warmup, world, device):
+    """Mean duration of one layer's grouped matmul launch when the launches
+    run back to back as in the sweep: every layer gets its own workspace,
+    which one xq_layer_mixed call fills with its Q8 activations, then the
+    timed region runs xq_debug_layer_matmuls layer after layer, `steps`
+    sweeps, CUDA events only at its ends (events between launches would
+    break the programmatic-launch overlap the sweep runs with). Each layer's
+    weights were last read 31 layers earlier and stream from HBM. Returns
+    seconds per launch (one grouped launch per all-Q4_K layer)."""
+    import torch
+    from gguf_quant_integer_gb300 import xq
+    ins, ys, descs, ws = sweep.state[M]
+    wss = [torch.empty_like(ws) for _ in sweep.W]
+    for l in range(len(sweep.W)):
+        xq.layer_mixed(descs[l], ins[l], M, wss[l])
+
+    def run():
+        for l in range(len(sweep.W)):
+            xq.debug_layer_matmuls(descs[l], sweep.n_inputs, M, wss[l])
+
+    secs = time_region(run, steps, warmup, world, device)
+    return max_over_ranks(secs, world, device) / (steps * len(sweep.W))
+
+
 # Sources the grouped GEMV kernel is built from: a recorded ncu traffic
 # figure stays valid only while their code is unchanged (comments and
 # whitespace are not part of the hash).
@@ -560,14 +584,16 @@ def gpu_arm(args):
         by_m[str(m)] = {"GBps": round(nbytes / s / 1e9, 1), "ms_per_step": round(1e3 * s, 4),
                         "tokens_per_s": round(m / s, 1)}
 
-    # ---- dominant kernel: CUDA events around every layer's grouped Q4_K
-    # matmul launch on its own (about 90% of each layer's GPU time per the
-    # ncu launch list); the layer call with its quantize launch for context
+    # ---- dominant kernel: every layer's grouped Q4_K matmul launch (about
+    # 90% of each layer's GPU time per the ncu launch list), timed alone and
+    # back to back over a region; for context the same launches with events
+    # around each, and the layer call with its quantize launch
     peak, peak_kind = measured_peaks()
+    avg = gemv_back_to_back_time(sweep, M, args.steps, max(3, args.warmup), world, device)
     gts = per_layer_gemv_times(sweep, M)
     lts = per_layer_times(sweep, M)
     layer_bytes = wl.layer_weight_bytes()
-    avg = sum(gts) / len(gts)
+    avg_each = sum(gts) / len(gts)
     avg_call = sum(lts) / len(lts)
     achieved = layer_bytes / avg / 1e9
     tr = read_ncu_traffic(f"gemv_mma_q4k_layer_M{M}")
@@ -575,6 +601,9 @@ def gpu_arm(args):
                 "frac": round(achieved / peak, 4), "peak_source": peak_kind,
                 "kernel": "gemv_mma_kernel<Q4_K>, the grouped launch of one layer, timed alone",
                 "bytes_per_launch": layer_bytes, "avg_launch_us": round(1e6 * avg, 3),
+                "avg_launch_note": "the 32 layers' grouped launches back to back (xq_debug_layer_matmuls, no quantize "
+                                   "launches), CUDA events at the ends of the timed region, mean per launch",
+                "avg_launch_us_events_each": round(1e6 * avg_each, 3),
                 "layer_call_us": round(1e6 * avg_call, 3),
                 "layer_call_note": "xq_layer_mixed per layer (quantize launch + GEMV launch), CUDA events per call",
                 "traffic": (round(tr[0]) if tr else None),
