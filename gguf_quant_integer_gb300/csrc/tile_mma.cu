@@ -36,6 +36,11 @@
 // for Q6_K, with run kept in TMEM and written to y after the last
 // super-block. d' and -dmin reach the epilogue through a shared-memory ring.
 //
+// Grid: one CTA per (128-row weight tile, K range, 128-token tile). A launch
+// inside a layer call may split K into ranges (TileArgs::splits); each CTA
+// then writes its range's sums as a partial, and the tile's last CTA adds
+// the ranges in order into y.
+//
 // Warp roles (512 threads): warps 0-3 unpack, warps 4-11 epilogue (warp w
 // reads TMEM lane quarter w%4, weight-row half (w-4)/4), warp 12 producer
 // (raw weights by TMA or row copies, token items by bulk copy), warps 13-15
