@@ -110,7 +110,8 @@ struct Fmt<12> {
 };
 template <>
 struct Fmt<14> {
-  static constexpr int kRawRow = kQ6Pitch, kRawStages = 2;
+  // (kRawPad: room for the 128-byte gaps between the boxes of a grouped view)
+  static constexpr int kRawRow = kQ6Pitch, kRawStages = 2, kRawPad = 1024;
   static constexpr int kItems = 8;
   static constexpr int kWBytes = 2 * kOpBytes;  // high and low operands
 };
@@ -127,9 +128,16 @@ struct Fmt<23> {
   static constexpr int kWBytes = 2 * kOpBytes;  // high and low operands
 };
 
+// Bytes of one raw-weight stage: the 128 rows, plus the Q6_K gaps.
+template <int TYPE>
+constexpr int raw_stage_bytes() {
+  if constexpr (TYPE == 14) return kRows * Fmt<14>::kRawRow + Fmt<14>::kRawPad;
+  else return kRows * Fmt<TYPE>::kRawRow;
+}
+
 template <int TYPE>
 struct Smem {
-  static constexpr int kRaw = Fmt<TYPE>::kRawStages * kRows * Fmt<TYPE>::kRawRow;
+  static constexpr int kRaw = Fmt<TYPE>::kRawStages * raw_stage_bytes<TYPE>();
   static constexpr int kTok = kTokStages * kTileItem;
   static constexpr int kW = kWStages * Fmt<TYPE>::kWBytes;
   static constexpr int kCoef = kCoefStages * kRows * 8;
@@ -163,7 +171,10 @@ struct TileArgs {
   int32_t* sums;               // test hook: [M][N][K/32] per-32-block integer sums, or null
   unsigned long long w_bytes;  // N * row_bytes
   unsigned long long img_bytes;  // bytes of the tile image (bounds checks of checked builds)
-  int q6_tma;                  // Q6_K rows of 16-byte multiples: map {row_bytes, N} of u8, box {240, 128}
+  // Q6_K by tensor map: rows of 16-byte multiples (q6_gs = 0: map {row_bytes, N} of u8, one box of 240 x 128),
+  // or 2^q6_gs consecutive rows per map row (map {row_bytes << gs, N >> gs}, 2^gs boxes of 240 x (128 >> gs),
+  // box i holding rows i, i + 2^gs, ... of the tile, each box at its own 128-byte-aligned place in the stage)
+  int q6_tma, q6_gs;
   int N, K, M, nsb, row_bytes, ttiles;
   uint32_t cb[4];              // IQ4_XS: codebook bytes with their sign bits flipped
   // K-split (layer calls that would leave SMs idle): each tile's super-blocks
@@ -250,7 +261,8 @@ __global__ void __launch_bounds__(Roles<TYPE>::kThreads, 1) tile_mma_kernel(cons
   using F = Fmt<TYPE>;
   using S = Smem<TYPE>;
   using B = Bars<TYPE>;
-  constexpr int kRawBytes = kRows * F::kRawRow;
+  constexpr int kRawBytes = kRows * F::kRawRow;     // bytes a stage's copies deliver
+  constexpr int kRawStage = raw_stage_bytes<TYPE>();  // stage stride in the ring
   constexpr int kItems = F::kItems;
   constexpr int RS = F::kRawStages;
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -326,7 +338,7 @@ __global__ void __launch_bounds__(Roles<TYPE>::kThreads, 1) tile_mma_kernel(cons
         const int gb = kb0 + b;  // super-block in the row
         const int rs = b % RS;
         if (b >= RS && !warp_wait(BAR(B::kRawEmpty + rs), ((b / RS) - 1) & 1, 1)) break;
-        const uint32_t dst = smem_addr(raw_ring + rs * kRawBytes);
+        const uint32_t dst = smem_addr(raw_ring + rs * kRawStage);
         if (TYPE == 12 || TYPE == 23 || TYPE == 8) {
           if (lane == 0) {
             mbar_expect_tx(BAR(B::kRawFull + rs), kRawBytes);  // rows past N arrive zero-filled
@@ -336,15 +348,20 @@ __global__ void __launch_bounds__(Roles<TYPE>::kThreads, 1) tile_mma_kernel(cons
               tma_load_2d(dst, &A.map, x, row0, BAR(B::kRawFull + rs));
           }
         } else if (A.q6_tma) {
-          // Q6_K rows of 16-byte multiples: one box of 128 rows x 240 bytes
-          // from the 16-byte boundary at or below the super-block (the same
-          // offset in every row); rows past N and bytes past the row arrive
-          // zero-filled
+          // Q6_K by tensor map: boxes of 240 bytes from the 16-byte boundary
+          // at or below the super-block. Rows of 16-byte multiples: one box
+          // of the 128 rows (the same offset in every row). Grouped view
+          // (2^gs rows per map row): box i takes rows i, i + 2^gs, ... of the
+          // tile, whose windows all start at the same position in their map
+          // rows. Rows past N and bytes past a map row arrive zero-filled.
           if (lane == 0) {
             mbar_expect_tx(BAR(B::kRawFull + rs), kRawBytes);
-            const int x = (kQ6kBytes * gb) & ~15;
-            if (XQ_CHECKED((x & 15) == 0 && x >= 0, kChkTileBox))
-              tma_load_2d(dst, &A.map, x, row0, BAR(B::kRawFull + rs));
+            const int gs = A.q6_gs, rb = kRows >> gs;
+            for (int i = 0; i < (1 << gs); ++i) {
+              const int x = (i * A.row_bytes + kQ6kBytes * gb) & ~15;
+              if (XQ_CHECKED((x & 15) == 0 && x >= 0, kChkTileBox))
+                tma_load_2d(dst + i * (rb * kQ6Pitch + 128), &A.map, x, row0 >> gs, BAR(B::kRawFull + rs));
+            }
           }
         } else {
           unsigned mine = 0;
@@ -436,7 +453,13 @@ __global__ void __launch_bounds__(Roles<TYPE>::kThreads, 1) tile_mma_kernel(cons
       const int rs = b % RS, cs = b % kCoefStages;
       if (!warp_wait(BAR(B::kRawFull + rs), (b / RS) & 1, 3)) break;
       if (b >= kCoefStages && !warp_wait(BAR(B::kCoefEmpty + cs), ((b / kCoefStages) - 1) & 1, 4)) break;
-      const uint8_t* raw = raw_ring + rs * kRawBytes + r * F::kRawRow;
+      // this row's window: row r of the stage, or in a Q6_K grouped view row
+      // r >> gs of box r mod 2^gs (boxes 128-byte aligned, see the producer)
+      const uint8_t* raw = (TYPE == 14 && A.q6_tma && A.q6_gs)
+                               ? raw_ring + rs * kRawStage +
+                                     (r & ((1 << A.q6_gs) - 1)) * ((kRows >> A.q6_gs) * F::kRawRow + 128) +
+                                     (r >> A.q6_gs) * F::kRawRow
+                               : raw_ring + rs * kRawStage + r * F::kRawRow;
       if (TYPE == 12) {
         // Scales and mins (public Q4_K packing): j < 4: sc = s[j] & 63,
         // m = s[j+4] & 63; j >= 4: sc = (s[j+4] & 15) | (s[j-4] >> 6) << 4,
@@ -969,12 +992,18 @@ cudaError_t launch_tile_mma(int type, const uint8_t* W, const uint8_t* xq, int M
       return cudaErrorInvalidValue;
     return sums ? launch_tile<8, true>(A, grid, s, pdl) : launch_tile<8, false>(A, grid, s, pdl);
   }
-  // Q6_K: one tensor-map box per super-block when rows are 16-byte multiples
-  // (K a multiple of 2048), else a bulk copy per row
-  A.q6_tma = (A.row_bytes % 16) == 0 ? 1 : 0;
-  if (A.q6_tma && !encode_tma_2d(&A.map, CU_TENSOR_MAP_DATA_TYPE_UINT8, W, A.row_bytes,
-                                 static_cast<unsigned long long>(N), A.row_bytes, kQ6Pitch, kRows))
-    return cudaErrorInvalidValue;
+  // Q6_K by tensor map: one box per super-block when rows are 16-byte
+  // multiples (K a multiple of 2048); else 2^gs rows per map row (the fewest
+  // whose bytes are a multiple of 16) and 2^gs boxes, when N is a multiple of
+  // 2^gs; else a bulk copy per row
+  A.q6_gs = q6k_row_shift(K);
+  A.q6_tma = (N % (1 << A.q6_gs)) == 0 ? 1 : 0;
+  if (A.q6_tma) {
+    const unsigned long long vrow = static_cast<unsigned long long>(A.row_bytes) << A.q6_gs;
+    if (!encode_tma_2d(&A.map, CU_TENSOR_MAP_DATA_TYPE_UINT8, W, vrow, static_cast<unsigned long long>(N >> A.q6_gs),
+                       vrow, kQ6Pitch, kRows >> A.q6_gs))
+      return cudaErrorInvalidValue;
+  }
   return sums ? launch_tile<14, true>(A, grid, s, pdl) : launch_tile<14, false>(A, grid, s, pdl);
 }
 
