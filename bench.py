@@ -883,8 +883,8 @@ def secondary_workloads(device, world):
         res[str(M)] = row
     out["llama3-8b-layer-swiglu-down"] = {"rotated_copies": copies, "layer_bytes": wl.layer_weight_bytes(),
                                           "by_m": res}
-    # batched decode and short prefill: the Qwen3-8B mixed layer at 16, 32
-    # and 64 tokens (GEMV over 8-token chunks), 128 and 256 (the tile kernel,
+    # batched decode and prefill: the Qwen3-8B mixed layer at 16, 32 and 64
+    # tokens (GEMV over 8-token chunks), 128, 256 and 512 (the tile kernel,
     # split over K where a projection's tiles leave SMs idle)
     wl = synth.WORKLOADS["qwen3-8b-mixed-layer"]
     lw = synth.gen_layer_weights(wl, 0)
@@ -892,7 +892,7 @@ def secondary_workloads(device, world):
     base = [torch.from_numpy(w.reshape(-1)).to(device) for w in lw]
     reps = [base] + [[w.clone() for w in base] for _ in range(copies - 1)]
     res = {}
-    for M in (16, 32, 64, 128, 256):
+    for M in (16, 32, 64, 128, 256, 512):
         ins = [torch.from_numpy(x).to(device) for x in synth.gen_layer_inputs(wl, M, 0)]
         ys = [torch.empty((M, p.N), dtype=torch.float32, device=device) for p in wl.projs]
         descs = [[(p.qtype, p.N, p.K, reps[c][t], ys[t], p.input) for t, p in enumerate(wl.projs)]
@@ -906,6 +906,9 @@ def secondary_workloads(device, world):
         sec = max_over_ranks(time_region(step, 3, 2, world, device), world, device) / (3 * copies)
         res[str(M)] = {"us_per_layer": round(1e6 * sec, 2), "GBps": round(wl.layer_weight_bytes() / sec / 1e9, 1),
                        "tokens_per_s": round(M / sec, 1)}
+        if M > 64:
+            flops = sum(2.0 * M * p.N * p.K for p in wl.projs)
+            res[str(M)]["TOPS_int"] = round(flops / sec / 1e12, 1)
     out["qwen3-8b-mixed-layer-batched"] = {"rotated_copies": copies, "layer_bytes": wl.layer_weight_bytes(),
                                            "by_m": res,
                                            "path": "GEMV over 8-token chunks up to 64 tokens, tile above (K-split "
