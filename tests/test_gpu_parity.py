@@ -261,9 +261,11 @@ def test_more_than_eight_tokens(xq, qtype, M):
 # Q6_K rows whose byte length is not a multiple of 16 (row windows start at
 # varying offsets; for (37, 256) and (130, 1536) the last window is cut at
 # the end of the weight buffer, and N not a multiple of 2^gs keeps the copy
-# per row; (128, 2304), (48, 1024) and (64, 1536) take the grouped tensor-map
-# view with 8, 2 and 4 rows per map row).
-TILE_SHAPES = [(37, 256, 70), (130, 1536, 200), (300, 4096, 129), (128, 2304, 65), (48, 1024, 128), (64, 1536, 96)]
+# per row; (128, 2304), (48, 1024), (64, 1536), (64, 256) and (136, 8960)
+# take the grouped tensor-map view with 8, 2, 4, 8 and 8 rows per map row,
+# (64, 256) with its last windows running past the end of the buffer).
+TILE_SHAPES = [(37, 256, 70), (130, 1536, 200), (300, 4096, 129), (128, 2304, 65), (48, 1024, 128), (64, 1536, 96),
+               (64, 256, 80), (136, 8960, 100)]
 
 
 @pytest.mark.parametrize("qtype", [synth.Q4_K, synth.Q6_K])
