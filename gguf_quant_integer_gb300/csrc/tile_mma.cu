@@ -258,10 +258,11 @@ __device__ __forceinline__ void store_row(uint8_t* op, int r, const uint32_t (&v
     *reinterpret_cast<uint4*>(p + q * 128) = make_uint4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
 }
 
-// GV: the Q6_K grouped tensor-map view, a kernel of its own so that the
-// plain Q6_K kernel carries none of its code (measured 7% slower on the
-// 12288-wide down projection when the two shared one kernel).
-template <int TYPE, bool SUMS, bool GV>
+// GV: the Q6_K grouped tensor-map view; SPLIT: a launch with K ranges
+// (splits > 1). Each is a kernel of its own so that the plain kernel carries
+// none of their code: compiled into it, the two cost the 512-token Qwen3-8B
+// FFN tiles 7% (grouped view, down) and 5% (K ranges, up and down).
+template <int TYPE, bool SUMS, bool GV, bool SPLIT>
 __global__ void __launch_bounds__(Roles<TYPE>::kThreads, 1) tile_mma_kernel(const __grid_constant__ TileArgs A) {
   using R = Roles<TYPE>;
   using F = Fmt<TYPE>;
@@ -286,9 +287,9 @@ __global__ void __launch_bounds__(Roles<TYPE>::kThreads, 1) tile_mma_kernel(cons
   // CTA = (weight tile, K range, token tile), token tile fastest so that the
   // CTAs of one weight tile run side by side
   const int tt = blockIdx.x % A.ttiles, wks = blockIdx.x / A.ttiles;
-  const int ks = wks % A.splits, wt = wks / A.splits;
-  const int kb0 = A.nsb * ks / A.splits;           // first super-block of this CTA
-  const int nb = A.nsb * (ks + 1) / A.splits - kb0;  // super-blocks of this CTA
+  const int ks = SPLIT ? wks % A.splits : 0, wt = SPLIT ? wks / A.splits : wks;
+  const int kb0 = SPLIT ? A.nsb * ks / A.splits : 0;                 // first super-block of this CTA
+  const int nb = SPLIT ? A.nsb * (ks + 1) / A.splits - kb0 : A.nsb;  // super-blocks of this CTA
   const int nitems = nb * kItems;
 #define BAR(i) (bar0 + 8u * static_cast<uint32_t>(i))
 
@@ -821,7 +822,7 @@ __global__ void __launch_bounds__(Roles<TYPE>::kThreads, 1) tile_mma_kernel(cons
               if (m < A.M) {
                 const int nc = n0 + 16 * c;
                 // y, or this K range's partial sums (same [M][N] layout)
-                float* yr = (A.splits > 1 ? A.partial + static_cast<size_t>(ks) * A.M * A.N : A.y) +
+                float* yr = (SPLIT ? A.partial + static_cast<size_t>(ks) * A.M * A.N : A.y) +
                             static_cast<size_t>(m) * A.N;
                 if (!XQ_IN(static_cast<size_t>(m) * A.N + (nc < A.N ? nc : 0), static_cast<size_t>(A.M) * A.N,
                            kChkTileY)) {
@@ -852,7 +853,7 @@ __global__ void __launch_bounds__(Roles<TYPE>::kThreads, 1) tile_mma_kernel(cons
         }
       }
     }
-    if (A.splits > 1) {
+    if constexpr (SPLIT) {
       // K-split: once every epilogue thread has stored its partial sums
       // (named barrier 1, the epilogue warps only), one thread counts the CTA
       // in with an acquire-release increment (its release publishes the
@@ -909,7 +910,7 @@ __global__ void __launch_bounds__(Roles<TYPE>::kThreads, 1) tile_mma_kernel(cons
   if (!A.wait_prev) cudaGridDependencySynchronize();
 }
 
-template <int TYPE, bool SUMS, bool GV = false>
+template <int TYPE, bool SUMS, bool GV, bool SPLIT>
 cudaError_t launch_tile(const TileArgs& A, int grid, cudaStream_t s, bool pdl) {
   // The register split inside the kernel is sized for a launch allocation
   // of exactly kRegsLaunch registers a thread; anything else is refused
@@ -917,15 +918,16 @@ cudaError_t launch_tile(const TileArgs& A, int grid, cudaStream_t s, bool pdl) {
   static int regs_ok = -1;
   if (regs_ok < 0) {
     cudaFuncAttributes fa;
-    regs_ok = (cudaFuncGetAttributes(&fa, tile_mma_kernel<TYPE, SUMS, GV>) == cudaSuccess && fa.numRegs == kRegsLaunch)
+    regs_ok = (cudaFuncGetAttributes(&fa, tile_mma_kernel<TYPE, SUMS, GV, SPLIT>) == cudaSuccess &&
+               fa.numRegs == kRegsLaunch)
                   ? 1
                   : 0;
   }
   if (!regs_ok) return cudaErrorInvalidConfiguration;
   static bool smem_set = false;
   if (!smem_set) {
-    const cudaError_t e = cudaFuncSetAttribute(tile_mma_kernel<TYPE, SUMS, GV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               smem_bytes<TYPE>());
+    const cudaError_t e = cudaFuncSetAttribute(tile_mma_kernel<TYPE, SUMS, GV, SPLIT>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes<TYPE>());
     if (e != cudaSuccess) return e;
     smem_set = true;
   }
@@ -939,7 +941,7 @@ cudaError_t launch_tile(const TileArgs& A, int grid, cudaStream_t s, bool pdl) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, tile_mma_kernel<TYPE, SUMS, GV>, A);
+  return cudaLaunchKernelEx(&cfg, tile_mma_kernel<TYPE, SUMS, GV, SPLIT>, A);
 }
 
 }  // namespace
@@ -952,6 +954,15 @@ cudaError_t take_tile_error(unsigned int* code) {
   if (e == cudaSuccess) e = cudaMemcpyToSymbol(g_tile_error, &z, sizeof(z));
   *code = v;
   return e;
+}
+
+// The instantiation for a launch: K ranges (never with the sums hook, which
+// the caller refuses), else with or without the hook.
+template <int TYPE, bool GV = false>
+cudaError_t launch_tile_for(const TileArgs& A, int grid, cudaStream_t s, bool pdl) {
+  if (A.splits > 1) return launch_tile<TYPE, false, GV, true>(A, grid, s, pdl);
+  return A.sums ? launch_tile<TYPE, true, GV, false>(A, grid, s, pdl)
+                : launch_tile<TYPE, false, GV, false>(A, grid, s, pdl);
 }
 
 cudaError_t launch_tile_mma(int type, const uint8_t* W, const uint8_t* xq, int M, int N, int K, float* y,
@@ -989,19 +1000,19 @@ cudaError_t launch_tile_mma(int type, const uint8_t* W, const uint8_t* xq, int M
     if (!encode_tma_2d(&A.map, CU_TENSOR_MAP_DATA_TYPE_UINT64, W, A.row_bytes / 8, static_cast<unsigned long long>(N),
                        A.row_bytes, kQ4kBytes / 8, kRows))
       return cudaErrorInvalidValue;
-    return sums ? launch_tile<12, true>(A, grid, s, pdl) : launch_tile<12, false>(A, grid, s, pdl);
+    return launch_tile_for<12>(A, grid, s, pdl);
   }
   if (type == 23) {
     if (!encode_tma_2d(&A.map, CU_TENSOR_MAP_DATA_TYPE_UINT8, W, A.row_bytes, static_cast<unsigned long long>(N),
                        A.row_bytes, Fmt<23>::kRawRow, kRows))
       return cudaErrorInvalidValue;
-    return sums ? launch_tile<23, true>(A, grid, s, pdl) : launch_tile<23, false>(A, grid, s, pdl);
+    return launch_tile_for<23>(A, grid, s, pdl);
   }
   if (type == 8) {
     if (!encode_tma_2d(&A.map, CU_TENSOR_MAP_DATA_TYPE_UINT64, W, A.row_bytes / 8, static_cast<unsigned long long>(N),
                        A.row_bytes, kQ80Group / 8, kRows))
       return cudaErrorInvalidValue;
-    return sums ? launch_tile<8, true>(A, grid, s, pdl) : launch_tile<8, false>(A, grid, s, pdl);
+    return launch_tile_for<8>(A, grid, s, pdl);
   }
   // Q6_K by tensor map: one box per super-block when rows are 16-byte
   // multiples (K a multiple of 2048); else 2^gs rows per map row (the fewest
@@ -1015,9 +1026,7 @@ cudaError_t launch_tile_mma(int type, const uint8_t* W, const uint8_t* xq, int M
                        vrow, kQ6Pitch, kRows >> A.q6_gs))
       return cudaErrorInvalidValue;
   }
-  if (A.q6_tma && A.q6_gs)
-    return sums ? launch_tile<14, true, true>(A, grid, s, pdl) : launch_tile<14, false, true>(A, grid, s, pdl);
-  return sums ? launch_tile<14, true>(A, grid, s, pdl) : launch_tile<14, false>(A, grid, s, pdl);
+  return A.q6_tma && A.q6_gs ? launch_tile_for<14, true>(A, grid, s, pdl) : launch_tile_for<14>(A, grid, s, pdl);
 }
 
 }  // namespace xq
