@@ -737,8 +737,14 @@ __global__ void __launch_bounds__(Roles<TYPE>::kThreads, 1) tile_mma_kernel(cons
       const int gb = kb0 + b;  // super-block in the row
       for (int it = 0; it < kItems; ++it, ++f) {
         const int d = f % kNumD, ts = f % kTokStages;
-        if (!warp_wait(BAR(B::kDFull + d), (f / kNumD) & 1, 10) ||
-            !warp_wait(BAR(B::kTokFull + ts), (f / kTokStages) & 1, 13)) {
+        // Both phases tested at once, so that their latencies overlap (the
+        // token stage's is long complete); a phase not yet complete falls
+        // back to the bounded wait. Every lane acquires both.
+        const bool d_now = mbar_try_wait(BAR(B::kDFull + d), (f / kNumD) & 1);
+        const bool t_now = mbar_try_wait(BAR(B::kTokFull + ts), (f / kTokStages) & 1);
+        bool got = d_now || wait_bar(BAR(B::kDFull + d), (f / kNumD) & 1, 10);
+        got = got && (t_now || wait_bar(BAR(B::kTokFull + ts), (f / kTokStages) & 1, 13));
+        if (!__all_sync(0xffffffffu, got)) {
           ok = false;
           break;
         }
