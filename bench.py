@@ -49,8 +49,8 @@ HEADLINE = "llama3-8b-32layer"
 # The headline metric, the same string on both arms.
 METRIC = "Q4_K/Q6_K x Q8 matmul weight GB/s (M=%d) and %% of GB300 HBM roofline"
 # workloads --profile-workload runs (one launch per call)
-PROFILE_WORKLOADS = ("prefill512-up", "prefill512-down", "qwen3-q6k-layer", "llama3-layer", "iq4xs-ffn-up",
-                     "q8_0-qwen25-layer", "qwen25-layer")
+PROFILE_WORKLOADS = ("prefill512-up", "prefill512-down", "prefill512-q8_0", "qwen3-q6k-layer", "q4km-q6k-layer",
+                     "llama3-layer", "iq4xs-ffn-up", "q8_0-qwen25-layer", "qwen25-layer")
 
 
 def parse_args(argv=None):
@@ -1024,6 +1024,14 @@ def profile_workload(args):
         buf = xq.quantize_q8(x)
         y = torch.empty((M, p.N), dtype=torch.float32, device=device)
         run = lambda: xq.matmul(p.qtype, W, buf, M, p.N, p.K, y=y)
+    elif name == "prefill512-q8_0":
+        # the Qwen3-8B ffn_up shape (12288 x 4096) as Q8_0 on the tile kernel, as the bench's secondary line
+        N, K = 12288, 4096
+        M = args.m if args.m > 64 else 512
+        W = torch.from_numpy(synth.gen_q8_0(23, N, K).reshape(-1)).to(device)
+        buf = xq.quantize_q8(torch.from_numpy(synth.gen_x(24, M, K)).to(device))
+        y = torch.empty((M, N), dtype=torch.float32, device=device)
+        run = lambda: xq.matmul(synth.Q8_0, W, buf, M, N, K, y=y)
     elif name == "iq4xs-ffn-up":
         # IQ4_XS 17408 x 5120 (47.3 MB), synthetic codebook, M from --m
         N, K, M = 17408, 5120, args.m
@@ -1033,9 +1041,12 @@ def profile_workload(args):
         y = torch.empty((M, N), dtype=torch.float32, device=device)
         run = lambda: xq.matmul_iq4xs_q8(W, cb, buf, M, N, K, y=y)
     else:
-        wl = synth.WORKLOADS[{"qwen3-q6k-layer": "qwen3-8b-mixed-layer", "qwen25-layer": "qwen2.5-1.5b-layer",
+        wl = synth.WORKLOADS[{"qwen3-q6k-layer": "qwen3-8b-mixed-layer", "q4km-q6k-layer": "qwen2.5-1.5b-q4km-layer",
+                              "qwen25-layer": "qwen2.5-1.5b-layer",
                               "q8_0-qwen25-layer": "qwen2.5-1.5b-q8_0-layer"}.get(name, "llama3-8b-32layer")]
-        keep = [t for t, p in enumerate(wl.projs) if name != "qwen3-q6k-layer" or p.qtype == synth.Q6_K]
+        # the *-q6k-layer workloads keep only the layer's Q6_K projections
+        q6_only = name.endswith("q6k-layer")
+        keep = [t for t, p in enumerate(wl.projs) if not q6_only or p.qtype == synth.Q6_K]
         M = args.m
         weights = synth.gen_layer_weights(wl, 0)
         inputs = synth.gen_layer_inputs(wl, M, 0)
