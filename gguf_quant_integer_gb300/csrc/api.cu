@@ -426,7 +426,7 @@ xq_status layer_matmuls(const xq_proj* proj, int n_proj, const uint8_t* const* q
         if (g != first) type_order[k++] = g;
     } else {
       long long tasks[kTypes] = {0, 0, 0, 0};
-      for (int p = 0; p < n_proj; ++p)
+      for (int p = 0; p < n_proj && p < 64; ++p)
         if (in_group(proj[p], M))
           tasks[type_index(proj[p].type)] += static_cast<long long>(xq::gemv_row_blocks(proj[p].N)) * sc.nch[p];
       for (int g = 0; g < kTypes; ++g)
