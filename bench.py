@@ -50,7 +50,7 @@ HEADLINE = "llama3-8b-32layer"
 METRIC = "Q4_K/Q6_K x Q8 matmul weight GB/s (M=%d) and %% of GB300 HBM roofline"
 # workloads --profile-workload runs (one launch per call)
 PROFILE_WORKLOADS = ("prefill512-up", "prefill512-down", "prefill512-q8_0", "qwen3-q6k-layer", "q4km-q6k-layer",
-                     "llama3-layer", "iq4xs-ffn-up", "q8_0-qwen25-layer", "qwen25-layer")
+                     "qwen3-layer", "llama3-layer", "iq4xs-ffn-up", "q8_0-qwen25-layer", "qwen25-layer")
 
 
 def parse_args(argv=None):
@@ -1042,6 +1042,7 @@ def profile_workload(args):
         run = lambda: xq.matmul_iq4xs_q8(W, cb, buf, M, N, K, y=y)
     else:
         wl = synth.WORKLOADS[{"qwen3-q6k-layer": "qwen3-8b-mixed-layer", "q4km-q6k-layer": "qwen2.5-1.5b-q4km-layer",
+                              "qwen3-layer": "qwen3-8b-mixed-layer",
                               "qwen25-layer": "qwen2.5-1.5b-layer",
                               "q8_0-qwen25-layer": "qwen2.5-1.5b-q8_0-layer"}.get(name, "llama3-8b-32layer")]
         # the *-q6k-layer workloads keep only the layer's Q6_K projections
